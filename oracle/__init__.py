@@ -1,0 +1,207 @@
+"""fp64 CPU oracle for the selective scan, the chunked SSD and the decode step.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  It shares no code
+with the CUDA library: the arithmetic lives in ``oracle.c`` (plain C, double
+precision, sequential within every row), compiled here with the host's gcc;
+this module only converts numpy arrays to contiguous float64 and calls it.
+
+Citations for every function are in ``oracle.c``.  Parity of the
+functions exported here is pinned by ``tests/test_oracle.py`` against
+closed forms, brute-force unrolling, invariants and textbook special cases.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+# A test may point the oracle at another build of oracle.c (the mutation test
+# plants mistakes in a copy of the source to show that the pins catch them).
+_LIB_OVERRIDE = os.environ.get("SSM_ORACLE_LIB")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``liboracle.so`` (gcc, -O2, OpenMP)."""
+    stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+    if force or stale:
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+               "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            if _LIB_OVERRIDE:
+                lib = ctypes.CDLL(_LIB_OVERRIDE)
+            else:
+                build()
+                lib = ctypes.CDLL(_LIB)
+            dp = ctypes.POINTER(ctypes.c_double)
+            i = ctypes.c_int
+            lib.oracle_scan.argtypes = [dp] * 8 + [i] + [dp] * 3 + [i] * 5
+            lib.oracle_scan_pieces.argtypes = ([dp] * 8 + [i] + [dp] * 3 + [i] * 5
+                                               + [ctypes.POINTER(ctypes.c_int), i])
+            lib.oracle_ssd_recurrence.argtypes = [dp] * 8 + [i] * 6
+            lib.oracle_ssd_chunked.argtypes = [dp] * 8 + [i] * 7
+            lib.oracle_decode_step.argtypes = [dp] * 9 + [i] * 5
+            lib.oracle_combine.argtypes = [ctypes.c_double] * 4 + [dp, dp]
+            lib.oracle_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(a):
+    """Contiguous float64 copy (or view) of an array-like; None stays None."""
+    if a is None:
+        return None
+    if hasattr(a, "detach"):  # torch tensor: exact upcast on the CPU
+        a = a.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return ctypes.POINTER(ctypes.c_double)()
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def combine(a1, b1, a2, b2):
+    """(a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2): first map, then second."""
+    lib = _load()
+    ao, bo = ctypes.c_double(), ctypes.c_double()
+    lib.oracle_combine(float(a1), float(b1), float(a2), float(b2),
+                       ctypes.byref(ao), ctypes.byref(bo))
+    return ao.value, bo.value
+
+
+def _scan_args(u, delta, A, B, C, D, z, delta_bias, h0):
+    u, delta, A, B, C = (_f64(t) for t in (u, delta, A, B, C))
+    D, z, delta_bias, h0 = (_f64(t) for t in (D, z, delta_bias, h0))
+    batch, dim, seqlen = u.shape
+    dstate = A.shape[1]
+    ngroups = B.shape[1]
+    assert delta.shape == u.shape and A.shape == (dim, dstate)
+    assert B.shape == (batch, ngroups, dstate, seqlen) and C.shape == B.shape
+    assert dim % ngroups == 0
+    return (u, delta, A, B, C, D, z, delta_bias, h0), (batch, dim, seqlen, dstate, ngroups)
+
+
+def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=False,
+         h0=None):
+    """Selective scan.  u, delta, z: (B, D, L); A: (D, N); B, C: (B, G, N, L).
+
+    Returns (y (B, D, L), final_state (B, D, N)) in float64.
+    """
+    arrs, dims = _scan_args(u, delta, A, B, C, D, z, delta_bias, h0)
+    batch, dim, seqlen, dstate, _ = dims
+    y = np.empty((batch, dim, seqlen), np.float64)
+    hs = np.empty((batch, dim, dstate), np.float64)
+    _load().oracle_scan(*[_ptr(a) for a in arrs[:8]], int(bool(delta_softplus)),
+                        _ptr(arrs[8]), _ptr(y), _ptr(hs), *dims)
+    return y, hs
+
+
+def scan_pieces(u, delta, A, B, C, cuts, D=None, z=None, delta_bias=None,
+                delta_softplus=False, h0=None):
+    """The scan evaluated piecewise: cut at ``cuts``, combined with the o operator."""
+    arrs, dims = _scan_args(u, delta, A, B, C, D, z, delta_bias, h0)
+    batch, dim, seqlen, dstate, _ = dims
+    cuts = np.ascontiguousarray(np.asarray(cuts, dtype=np.int32))
+    assert np.all(np.diff(cuts) > 0) and (cuts.size == 0 or (cuts[0] > 0 and cuts[-1] < seqlen))
+    y = np.empty((batch, dim, seqlen), np.float64)
+    hs = np.empty((batch, dim, dstate), np.float64)
+    _load().oracle_scan_pieces(*[_ptr(a) for a in arrs[:8]], int(bool(delta_softplus)),
+                               _ptr(arrs[8]), _ptr(y), _ptr(hs), *dims,
+                               cuts.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
+                               int(cuts.size))
+    return y, hs
+
+
+def _ssd_args(x, dt, A_head, B, C, h0):
+    x, dt, A_head, B, C, h0 = (_f64(t) for t in (x, dt, A_head, B, C, h0))
+    batch, seqlen, nheads, headdim = x.shape
+    ngroups, dstate = B.shape[2], B.shape[3]
+    assert dt.shape == (batch, seqlen, nheads) and A_head.shape == (nheads,)
+    assert B.shape == (batch, seqlen, ngroups, dstate) and C.shape == B.shape
+    assert nheads % ngroups == 0
+    return (x, dt, A_head, B, C, h0), (batch, seqlen, nheads, headdim, dstate, ngroups)
+
+
+def ssd_recurrence(x, dt, A_head, B, C, h0=None):
+    """SSD as the step-by-step recurrence.  x: (B, L, H, P); dt: (B, L, H);
+    A_head: (H,); B, C: (B, L, G, N).  Returns (y (B, L, H, P), state (B, H, P, N))."""
+    arrs, dims = _ssd_args(x, dt, A_head, B, C, h0)
+    batch, seqlen, nheads, headdim, dstate, _ = dims
+    y = np.empty((batch, seqlen, nheads, headdim), np.float64)
+    hs = np.empty((batch, nheads, headdim, dstate), np.float64)
+    _load().oracle_ssd_recurrence(*[_ptr(a) for a in arrs], _ptr(y), _ptr(hs), *dims)
+    return y, hs
+
+
+def ssd_chunked(x, dt, A_head, B, C, chunk, h0=None):
+    """SSD by the chunked algorithm (fp64 loops), for pinning against the recurrence."""
+    arrs, dims = _ssd_args(x, dt, A_head, B, C, h0)
+    batch, seqlen, nheads, headdim, dstate, _ = dims
+    y = np.empty((batch, seqlen, nheads, headdim), np.float64)
+    hs = np.empty((batch, nheads, headdim, dstate), np.float64)
+    _load().oracle_ssd_chunked(*[_ptr(a) for a in arrs], _ptr(y), _ptr(hs), *dims, int(chunk))
+    return y, hs
+
+
+def decode_step(state, x, dt, A, B, C, D=None, z=None):
+    """One decode step.  state: (B, H, P, N) (not modified; a new array is
+    returned); x, z: (B, H, P); dt: (B, H); A, D: (H,); B, C: (B, G, N).
+    Returns (y (B, H, P), new_state (B, H, P, N))."""
+    st = _f64(state).copy()
+    x, dt, A, B, C, D, z = (_f64(t) for t in (x, dt, A, B, C, D, z))
+    batch, nheads, headdim, dstate = st.shape
+    ngroups = B.shape[1]
+    assert x.shape == (batch, nheads, headdim) and dt.shape == (batch, nheads)
+    assert B.shape == (batch, ngroups, dstate) and C.shape == B.shape
+    y = np.empty((batch, nheads, headdim), np.float64)
+    _load().oracle_decode_step(_ptr(st), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
+                               _ptr(D), _ptr(z), _ptr(y),
+                               batch, nheads, headdim, dstate, ngroups)
+    return y, st
+
+
+def scan_rows(u, delta, A, B, C, rows, D=None, z=None, delta_bias=None,
+              delta_softplus=False):
+    """Oracle scan of a subset of (batch, channel) rows of a large problem.
+
+    ``rows`` is a list of (b, d) pairs.  Only those rows' inputs are gathered,
+    so a sample of a multi-GB workload can be checked in seconds.  Returns
+    (y (len(rows), L), final_state (len(rows), N)).
+    """
+    out_y, out_h = [], []
+    ngroups = B.shape[1]
+    dim = u.shape[1]
+    dpg = dim // ngroups
+    for (b, d) in rows:
+        g = d // dpg
+        sl = slice(d, d + 1)
+        y, h = scan(u[b:b + 1, sl], delta[b:b + 1, sl], A[sl], B[b:b + 1, g:g + 1],
+                    C[b:b + 1, g:g + 1],
+                    None if D is None else D[sl], None if z is None else z[b:b + 1, sl],
+                    None if delta_bias is None else delta_bias[sl], delta_softplus)
+        out_y.append(y[0, 0])
+        out_h.append(h[0, 0])
+    return np.stack(out_y), np.stack(out_h)

@@ -1,0 +1,419 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle for the selective state-space
+ * scan, its scalar-A-per-head chunked SSD form and its single-token decode
+ * step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file: only the tests, the smoke check and the benchmark's CPU
+ * baseline leg use it.  It shares no code, header or constant with the CUDA
+ * library; the two meet only through seeded inputs.
+ *
+ * Every quantity is computed in double precision, in the order the pages
+ * state it, one time step after another.  Loops over independent rows
+ * (batch x channel, batch x head x headdim) are spread over OpenMP threads;
+ * nothing inside a row is reordered.
+ *
+ * Sources (page title, section):
+ *  [P1] "We brought Mamba to Trainium -- and mapped where custom kernels
+ *       actually help", section "Mamba: bringing an unsupported model to the
+ *       chip, and writing its missing kernel": the recurrence
+ *       h_t = A_t h_{t-1} + B_t x_t and the read-out y_t = sum_n C_t h_t.
+ *  [P1] same page, section "We built the parallel scan -- and it taught us
+ *       something sharper": the recurrence is associative, so it may be
+ *       evaluated as a combination of pieces (used by oracle_scan_pieces).
+ *  [P2] "Mamba-3 NKI Kernels for AWS Neuron", section "How it works",
+ *       Phase 0: dt = softplus(dt + dt_bias), alpha = exp(dt * A);
+ *       Phase 5: D skip connection, then the silu gate;
+ *       decode (Eq. 9): h_t = alpha h_{t-1} + beta prev_Bx + gamma B_t (x) x_t,
+ *       y_t = C_t^T h_t.  With lambda = 1 the coefficients are gamma = dt and
+ *       beta = (dt - gamma) alpha = 0, which is the update used here.
+ *  [P2] same page, section "Kernel details", mamba3_siso_ssd_kernel: the
+ *       chunked form (chunk 64, Mamba-2 SSD structure) is mathematically
+ *       equivalent to the step-by-step recurrence (oracle_ssd_chunked).
+ *
+ * Readings taken where the pages are silent (each is listed with its reason
+ * in the design notes):
+ *  - B is discretised by Euler (b = dt * B * x), A by zero-order hold
+ *    (a = exp(dt * A)).
+ *  - The bias is added before softplus; with softplus off it is still added.
+ *  - The gate multiplies after the D skip: y = (sum_n C h + D x) * silu(z),
+ *    silu(z) = z / (1 + exp(-z)).
+ *  - The prefill state starts at zero unless an initial state is given.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* softplus(x) = log(1 + e^x), written so that no intermediate overflows:
+ * for x > 0, log(1 + e^x) = x + log(1 + e^-x). */
+static double softplus_d(double x)
+{
+    if (x > 0.0) return x + log1p(exp(-x));
+    return log1p(exp(x));
+}
+
+/* silu(z) = z * sigmoid(z) = z / (1 + e^-z). */
+static double silu_d(double z)
+{
+    return z / (1.0 + exp(-z));
+}
+
+/* The associative combine of two affine maps h -> a h + b applied in
+ * sequence, first (a1, b1) then (a2, b2):
+ *     (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2).
+ * [P1] section "We built the parallel scan": associativity is what lets the
+ * sequence be split into pieces. */
+void oracle_combine(double a1, double b1, double a2, double b2,
+                    double* a_out, double* b_out)
+{
+    *a_out = a1 * a2;
+    *b_out = a2 * b1 + b2;
+}
+
+/*
+ * Selective scan (Mamba-1 form), one channel at a time.
+ *
+ *   u, delta, z, y : (batch, dim, seqlen), seqlen contiguous
+ *   A              : (dim, dstate)
+ *   Bm, Cm         : (batch, ngroups, dstate, seqlen); channel d uses group
+ *                    d / (dim / ngroups)
+ *   Dskip, delta_bias : (dim,)   (either may be NULL)
+ *   z              : may be NULL (no gate)
+ *   h0             : (batch, dim, dstate) initial state, or NULL for zero
+ *   final_state    : (batch, dim, dstate), may be NULL
+ *
+ * Per step t, for every state n:
+ *   dl = delta + bias;  dl = softplus(dl) if delta_softplus
+ *   h_n = exp(dl * A[d,n]) * h_n + dl * B[n,t] * u_t
+ *   y_t = sum_n C[n,t] * h_n + D[d] * u_t;   y_t *= silu(z_t) if z given
+ */
+void oracle_scan(const double* u, const double* delta, const double* A,
+                 const double* Bm, const double* Cm, const double* Dskip,
+                 const double* z, const double* delta_bias, int delta_softplus,
+                 const double* h0, double* y, double* final_state,
+                 int batch, int dim, int seqlen, int dstate, int ngroups)
+{
+    const int dim_per_group = dim / ngroups;
+    const long long rows = (long long)batch * dim;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (long long row = 0; row < rows; ++row) {
+        const int b = (int)(row / dim);
+        const int d = (int)(row % dim);
+        const int g = d / dim_per_group;
+        double* h = (double*)malloc(sizeof(double) * (size_t)dstate);
+        for (int n = 0; n < dstate; ++n)
+            h[n] = h0 ? h0[row * dstate + n] : 0.0;
+        const size_t io = (size_t)row * (size_t)seqlen;
+        const size_t bc = ((size_t)b * ngroups + g) * (size_t)dstate * (size_t)seqlen;
+        for (int t = 0; t < seqlen; ++t) {
+            double dl = delta[io + t] + (delta_bias ? delta_bias[d] : 0.0);
+            if (delta_softplus) dl = softplus_d(dl);
+            const double x = u[io + t];
+            double acc = 0.0;
+            for (int n = 0; n < dstate; ++n) {
+                const double a = exp(dl * A[(size_t)d * dstate + n]);
+                const double bn = Bm[bc + (size_t)n * seqlen + t];
+                const double cn = Cm[bc + (size_t)n * seqlen + t];
+                h[n] = a * h[n] + dl * bn * x;
+                acc += cn * h[n];
+            }
+            double out = acc + (Dskip ? Dskip[d] * x : 0.0);
+            if (z) out *= silu_d(z[io + t]);
+            y[io + t] = out;
+        }
+        if (final_state)
+            for (int n = 0; n < dstate; ++n) final_state[row * dstate + n] = h[n];
+        free(h);
+    }
+}
+
+/*
+ * The same scan evaluated piecewise, to pin the split-and-combine algorithm
+ * against the sequential definition.  The sequence is cut at the
+ * npieces - 1 increasing positions in `cuts` (0 < cut < seqlen).  Each piece
+ * is first scanned from a zero state, giving its aggregate map
+ * (prod a, h_end); the carried-in state of piece k is the exclusive
+ * o-combination of the aggregates of pieces 0..k-1 applied to h0; each piece
+ * is then scanned again from its carried-in state to produce y.
+ * Arguments otherwise as oracle_scan.
+ */
+void oracle_scan_pieces(const double* u, const double* delta, const double* A,
+                        const double* Bm, const double* Cm, const double* Dskip,
+                        const double* z, const double* delta_bias, int delta_softplus,
+                        const double* h0, double* y, double* final_state,
+                        int batch, int dim, int seqlen, int dstate, int ngroups,
+                        const int* cuts, int ncuts)
+{
+    const int dim_per_group = dim / ngroups;
+    const long long rows = (long long)batch * dim;
+    const int npieces = ncuts + 1;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (long long row = 0; row < rows; ++row) {
+        const int b = (int)(row / dim);
+        const int d = (int)(row % dim);
+        const int g = d / dim_per_group;
+        const size_t io = (size_t)row * (size_t)seqlen;
+        const size_t bc = ((size_t)b * ngroups + g) * (size_t)dstate * (size_t)seqlen;
+        double* agg_a = (double*)malloc(sizeof(double) * (size_t)npieces * dstate);
+        double* agg_b = (double*)malloc(sizeof(double) * (size_t)npieces * dstate);
+        double* carry = (double*)malloc(sizeof(double) * (size_t)dstate);
+        /* pass 1: aggregate of every piece, from a zero state */
+        for (int k = 0; k < npieces; ++k) {
+            const int t0 = k == 0 ? 0 : cuts[k - 1];
+            const int t1 = k == npieces - 1 ? seqlen : cuts[k];
+            for (int n = 0; n < dstate; ++n) {
+                double pa = 1.0, hb = 0.0;
+                for (int t = t0; t < t1; ++t) {
+                    double dl = delta[io + t] + (delta_bias ? delta_bias[d] : 0.0);
+                    if (delta_softplus) dl = softplus_d(dl);
+                    const double a = exp(dl * A[(size_t)d * dstate + n]);
+                    const double bt = dl * Bm[bc + (size_t)n * seqlen + t] * u[io + t];
+                    oracle_combine(pa, hb, a, bt, &pa, &hb);
+                }
+                agg_a[k * dstate + n] = pa;
+                agg_b[k * dstate + n] = hb;
+            }
+        }
+        /* pass 2: carried-in state of every piece, then the piece's outputs */
+        for (int n = 0; n < dstate; ++n) carry[n] = h0 ? h0[row * dstate + n] : 0.0;
+        for (int k = 0; k < npieces; ++k) {
+            const int t0 = k == 0 ? 0 : cuts[k - 1];
+            const int t1 = k == npieces - 1 ? seqlen : cuts[k];
+            double* h = (double*)malloc(sizeof(double) * (size_t)dstate);
+            memcpy(h, carry, sizeof(double) * (size_t)dstate);
+            for (int t = t0; t < t1; ++t) {
+                double dl = delta[io + t] + (delta_bias ? delta_bias[d] : 0.0);
+                if (delta_softplus) dl = softplus_d(dl);
+                const double x = u[io + t];
+                double acc = 0.0;
+                for (int n = 0; n < dstate; ++n) {
+                    const double a = exp(dl * A[(size_t)d * dstate + n]);
+                    h[n] = a * h[n] + dl * Bm[bc + (size_t)n * seqlen + t] * x;
+                    acc += Cm[bc + (size_t)n * seqlen + t] * h[n];
+                }
+                double out = acc + (Dskip ? Dskip[d] * x : 0.0);
+                if (z) out *= silu_d(z[io + t]);
+                y[io + t] = out;
+            }
+            free(h);
+            /* carry into the next piece: (1, carry) o aggregate(k) */
+            for (int n = 0; n < dstate; ++n) {
+                double na, nb;
+                oracle_combine(1.0, carry[n], agg_a[k * dstate + n], agg_b[k * dstate + n],
+                               &na, &nb);
+                carry[n] = nb;
+            }
+        }
+        if (final_state)
+            for (int n = 0; n < dstate; ++n) final_state[row * dstate + n] = carry[n];
+        free(agg_a);
+        free(agg_b);
+        free(carry);
+    }
+}
+
+/*
+ * Scalar-A-per-head SSD, evaluated as the plain recurrence.
+ *
+ *   x, y        : (batch, seqlen, nheads, headdim)
+ *   dt          : (batch, seqlen, nheads)   (already discretised: > 0)
+ *   A_head      : (nheads,)
+ *   Bm, Cm      : (batch, seqlen, ngroups, dstate); head h uses group
+ *                 h / (nheads / ngroups)
+ *   h0          : (batch, nheads, headdim, dstate) or NULL for zero
+ *   final_state : (batch, nheads, headdim, dstate), may be NULL
+ *
+ * Per step t:  S[p,n] = exp(dt_t A_h) S[p,n] + dt_t B_t[n] x_t[p],
+ *              y_t[p] = sum_n C_t[n] S[p,n].
+ */
+void oracle_ssd_recurrence(const double* x, const double* dt, const double* A_head,
+                           const double* Bm, const double* Cm, const double* h0,
+                           double* y, double* final_state,
+                           int batch, int seqlen, int nheads, int headdim, int dstate,
+                           int ngroups)
+{
+    const int heads_per_group = nheads / ngroups;
+    const long long rows = (long long)batch * nheads * headdim;
+#pragma omp parallel for schedule(dynamic, 8)
+    for (long long row = 0; row < rows; ++row) {
+        const int p = (int)(row % headdim);
+        const int h = (int)((row / headdim) % nheads);
+        const int b = (int)(row / ((long long)headdim * nheads));
+        const int g = h / heads_per_group;
+        double* S = (double*)malloc(sizeof(double) * (size_t)dstate);
+        for (int n = 0; n < dstate; ++n) S[n] = h0 ? h0[row * dstate + n] : 0.0;
+        for (int t = 0; t < seqlen; ++t) {
+            const size_t bt = (size_t)b * seqlen + t;
+            const double dtv = dt[bt * nheads + h];
+            const double a = exp(dtv * A_head[h]);
+            const double xv = x[(bt * nheads + h) * headdim + p];
+            const double* Bt = Bm + (bt * ngroups + g) * dstate;
+            const double* Ct = Cm + (bt * ngroups + g) * dstate;
+            double acc = 0.0;
+            for (int n = 0; n < dstate; ++n) {
+                S[n] = a * S[n] + dtv * Bt[n] * xv;
+                acc += Ct[n] * S[n];
+            }
+            y[(bt * nheads + h) * headdim + p] = acc;
+        }
+        if (final_state)
+            for (int n = 0; n < dstate; ++n) final_state[row * dstate + n] = S[n];
+        free(S);
+    }
+}
+
+/*
+ * The same SSD evaluated by the chunked algorithm, in fp64, as plain loops.
+ * [P2] "Kernel details", mamba3_siso_ssd_kernel: the chunked (Mamba-2 SSD)
+ * structure, stated there to be mathematically equivalent to the recurrence.
+ * For each chunk c of `chunk` steps (the last one may be shorter):
+ *   cs_i      = sum_{j <= i} dt_j A_h                 (within the chunk)
+ *   G[i,j]    = sum_n C_i[n] B_j[n]
+ *   M[i,j]    = G[i,j] exp(cs_i - cs_j)   for j <= i, else 0
+ *   Y_diag    = M (dt o x)
+ *   Y_off[i]  = exp(cs_i) sum_n C_i[n] S_prev[:, n]
+ *   S_chunk   = sum_j exp(cs_last - cs_j) dt_j x_j (x) B_j
+ *   S_prev    = exp(cs_last) S_prev + S_chunk
+ * Arguments as oracle_ssd_recurrence.
+ */
+void oracle_ssd_chunked(const double* x, const double* dt, const double* A_head,
+                        const double* Bm, const double* Cm, const double* h0,
+                        double* y, double* final_state,
+                        int batch, int seqlen, int nheads, int headdim, int dstate,
+                        int ngroups, int chunk)
+{
+    const int heads_per_group = nheads / ngroups;
+    const long long units = (long long)batch * nheads;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long long unit = 0; unit < units; ++unit) {
+        const int h = (int)(unit % nheads);
+        const int b = (int)(unit / nheads);
+        const int g = h / heads_per_group;
+        const double Ah = A_head[h];
+        double* S = (double*)calloc((size_t)headdim * dstate, sizeof(double));
+        double* cs = (double*)malloc(sizeof(double) * (size_t)chunk);
+        double* M = (double*)malloc(sizeof(double) * (size_t)chunk * chunk);
+        double* Sc = (double*)malloc(sizeof(double) * (size_t)headdim * dstate);
+        if (h0)
+            for (int p = 0; p < headdim; ++p)
+                for (int n = 0; n < dstate; ++n)
+                    S[(size_t)p * dstate + n] =
+                        h0[(((size_t)b * nheads + h) * headdim + p) * dstate + n];
+        for (int t0 = 0; t0 < seqlen; t0 += chunk) {
+            const int q = seqlen - t0 < chunk ? seqlen - t0 : chunk;
+#define DT(i) dt[((size_t)b * seqlen + t0 + (i)) * nheads + h]
+#define XV(i, p) x[(((size_t)b * seqlen + t0 + (i)) * nheads + h) * headdim + (p)]
+#define BV(i, n) Bm[(((size_t)b * seqlen + t0 + (i)) * ngroups + g) * dstate + (n)]
+#define CV(i, n) Cm[(((size_t)b * seqlen + t0 + (i)) * ngroups + g) * dstate + (n)]
+            /* cumulative log-decay inside the chunk */
+            double run = 0.0;
+            for (int i = 0; i < q; ++i) {
+                run += DT(i) * Ah;
+                cs[i] = run;
+            }
+            /* M = (C B^T) masked by the causal decay exp(cs_i - cs_j) */
+            for (int i = 0; i < q; ++i)
+                for (int j = 0; j < q; ++j) {
+                    double m = 0.0;
+                    if (j <= i) {
+                        double gij = 0.0;
+                        for (int n = 0; n < dstate; ++n) gij += CV(i, n) * BV(j, n);
+                        m = gij * exp(cs[i] - cs[j]);
+                    }
+                    M[(size_t)i * chunk + j] = m;
+                }
+            /* outputs: diagonal block plus the contribution of the carried state */
+            for (int i = 0; i < q; ++i)
+                for (int p = 0; p < headdim; ++p) {
+                    double yd = 0.0;
+                    for (int j = 0; j <= i; ++j) yd += M[(size_t)i * chunk + j] * DT(j) * XV(j, p);
+                    double yo = 0.0;
+                    for (int n = 0; n < dstate; ++n) yo += CV(i, n) * S[(size_t)p * dstate + n];
+                    yo *= exp(cs[i]);
+                    y[(((size_t)b * seqlen + t0 + i) * nheads + h) * headdim + p] = yd + yo;
+                }
+            /* state produced inside the chunk, then the inter-chunk recurrence */
+            for (int p = 0; p < headdim; ++p)
+                for (int n = 0; n < dstate; ++n) {
+                    double s = 0.0;
+                    for (int j = 0; j < q; ++j)
+                        s += exp(cs[q - 1] - cs[j]) * DT(j) * XV(j, p) * BV(j, n);
+                    Sc[(size_t)p * dstate + n] = s;
+                }
+            const double decay = exp(cs[q - 1]);
+            for (size_t k = 0; k < (size_t)headdim * dstate; ++k) S[k] = decay * S[k] + Sc[k];
+#undef DT
+#undef XV
+#undef BV
+#undef CV
+        }
+        if (final_state)
+            for (int p = 0; p < headdim; ++p)
+                for (int n = 0; n < dstate; ++n)
+                    final_state[(((size_t)b * nheads + h) * headdim + p) * dstate + n] =
+                        S[(size_t)p * dstate + n];
+        free(S);
+        free(cs);
+        free(M);
+        free(Sc);
+    }
+}
+
+/*
+ * One decode step, updating `state` in place.
+ * [P2] "How it works", decode via step(), Eq. 9 with lambda = 1.
+ *
+ *   state : (batch, nheads, headdim, dstate), read and overwritten
+ *   x, z, y : (batch, nheads, headdim); z may be NULL
+ *   dt    : (batch, nheads);  A, D : (nheads,); D may be NULL
+ *   Bm, Cm : (batch, ngroups, dstate)
+ *
+ *   alpha = exp(dt A_h);  s[n] = alpha s[n] + dt x B[n];
+ *   y = sum_n C[n] s[n] + D_h x;  y *= silu(z) if z given.
+ */
+void oracle_decode_step(double* state, const double* x, const double* dt,
+                        const double* A, const double* Bm, const double* Cm,
+                        const double* Dskip, const double* z, double* y,
+                        int batch, int nheads, int headdim, int dstate, int ngroups)
+{
+    const int heads_per_group = nheads / ngroups;
+    const long long rows = (long long)batch * nheads * headdim;
+#pragma omp parallel for schedule(static)
+    for (long long row = 0; row < rows; ++row) {
+        const int h = (int)((row / headdim) % nheads);
+        const int b = (int)(row / ((long long)headdim * nheads));
+        const int g = h / heads_per_group;
+        const double dtv = dt[(size_t)b * nheads + h];
+        const double alpha = exp(dtv * A[h]);
+        const double xv = x[row];
+        const double* Bt = Bm + ((size_t)b * ngroups + g) * dstate;
+        const double* Ct = Cm + ((size_t)b * ngroups + g) * dstate;
+        double* s = state + (size_t)row * dstate;
+        double acc = 0.0;
+        for (int n = 0; n < dstate; ++n) {
+            s[n] = alpha * s[n] + dtv * xv * Bt[n];
+            acc += Ct[n] * s[n];
+        }
+        double out = acc + (Dskip ? Dskip[h] * xv : 0.0);
+        if (z) out *= silu_d(z[row]);
+        y[row] = out;
+    }
+}
+
+/* Number of OpenMP threads the oracle's parallel loops use. */
+int oracle_num_threads(void)
+{
+    int n = 1;
+#pragma omp parallel
+    {
+#pragma omp single
+        {
+#ifdef _OPENMP
+            extern int omp_get_num_threads(void);
+            n = omp_get_num_threads();
+#endif
+        }
+    }
+    return n;
+}

@@ -1,0 +1,139 @@
+"""Seeded synthetic inputs shaped like the pages' workloads.
+
+This module holds no arithmetic of the method itself: it only draws random
+numbers and shapes them into the distributions the workloads name.  Both the
+CUDA path and the fp64 oracle consume exactly the tensors returned here
+(bf16 values are upcast exactly by the oracle).
+
+Recipes (fixed draw order, one ``torch.Generator`` per call):
+
+* selective scan (``scan_inputs``): u, z ~ N(0, 1); raw delta = 0.5 N(0, 1);
+  per-channel dt0 = exp(U[ln 1e-3, ln 1e-1]) and delta_bias = inv_softplus(dt0)
+  = log(expm1(dt0)), so the kernel's softplus(delta + bias) has the stated
+  distribution; A[d, n] = -(n + 1); B, C ~ N(0, 1) of shape (B, G, N, L)
+  shared by the channels of a group; D = 1.
+* chunked SSD (``ssd_inputs``): x, B, C ~ N(0, 1); dt = softplus(N(0, 1) - 4);
+  A_head = -U[1, 16].
+* decode (``decode_inputs``): state ~ N(0, 0.1) (standard deviation 0.1);
+  per step x, B, C ~ N(0, 1), dt = softplus(N(0, 1) - 4); A_head = -U[1, 16];
+  D = 1, no gate unless asked for.
+
+Tensors are created on the CPU by default so that the same seed gives the
+same values on any machine; pass ``device="cuda"`` to draw large workloads
+directly on the GPU with a CUDA generator (used by the benchmark, whose
+inputs need not match any stored value).
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def torch_dtype(name: str) -> torch.dtype:
+    return _DTYPES[name]
+
+
+def _gen(seed: int, device: str) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+def _randn(shape, g, device):
+    return torch.randn(*shape, generator=g, device=device, dtype=torch.float32)
+
+
+def _rand(shape, g, device):
+    return torch.rand(*shape, generator=g, device=device, dtype=torch.float32)
+
+
+def scan_inputs(batch: int, dim: int, seqlen: int, dstate: int = 16, ngroups: int = 1,
+                dtype: str = "bf16", seed: int = 1002, gate: bool = True,
+                dskip: str = "ones", device: str = "cpu") -> dict:
+    """Inputs of the selective scan in the layouts the C ABI takes.
+
+    u, delta, z: (batch, dim, seqlen); A: (dim, dstate) fp32;
+    B, C: (batch, ngroups, dstate, seqlen); D, delta_bias: (dim,) fp32.
+    ``dskip`` is "ones" (the workloads' D = 1), "randn" or "none".
+    """
+    g = _gen(seed, device)
+    td = _DTYPES[dtype]
+    u = _randn((batch, dim, seqlen), g, device)
+    delta = 0.5 * _randn((batch, dim, seqlen), g, device)
+    z = _randn((batch, dim, seqlen), g, device)
+    Bm = _randn((batch, ngroups, dstate, seqlen), g, device)
+    Cm = _randn((batch, ngroups, dstate, seqlen), g, device)
+    lo, hi = math.log(1e-3), math.log(1e-1)
+    dt0 = torch.exp(lo + (hi - lo) * _rand((dim,), g, device))
+    delta_bias = torch.log(torch.expm1(dt0))
+    A = -torch.arange(1, dstate + 1, dtype=torch.float32, device=device).repeat(dim, 1)
+    if dskip == "ones":
+        D = torch.ones(dim, dtype=torch.float32, device=device)
+    elif dskip == "randn":
+        D = _randn((dim,), g, device)
+    else:
+        D = None
+    return {
+        "u": u.to(td).contiguous(),
+        "delta": delta.to(td).contiguous(),
+        "A": A.contiguous(),
+        "B": Bm.to(td).contiguous(),
+        "C": Cm.to(td).contiguous(),
+        "D": D,
+        "z": z.to(td).contiguous() if gate else None,
+        "delta_bias": delta_bias.contiguous(),
+        "delta_softplus": True,
+    }
+
+
+def ssd_inputs(batch: int, seqlen: int, nheads: int, headdim: int, dstate: int,
+               ngroups: int = 1, dtype: str = "bf16", seed: int = 1004,
+               device: str = "cpu") -> dict:
+    """Inputs of the chunked SSD: x (B, L, H, P); dt (B, L, H) fp32;
+    A_head (H,) fp32; B, C (B, L, G, N)."""
+    g = _gen(seed, device)
+    td = _DTYPES[dtype]
+    x = _randn((batch, seqlen, nheads, headdim), g, device)
+    Bm = _randn((batch, seqlen, ngroups, dstate), g, device)
+    Cm = _randn((batch, seqlen, ngroups, dstate), g, device)
+    dt = torch.nn.functional.softplus(_randn((batch, seqlen, nheads), g, device) - 4.0)
+    A_head = -(1.0 + 15.0 * _rand((nheads,), g, device))
+    return {
+        "x": x.to(td).contiguous(),
+        "dt": dt.contiguous(),
+        "A_head": A_head.contiguous(),
+        "B": Bm.to(td).contiguous(),
+        "C": Cm.to(td).contiguous(),
+    }
+
+
+def decode_inputs(batch: int, nheads: int, headdim: int, dstate: int, ngroups: int = 1,
+                  steps: int = 1, dtype: str = "f32", seed: int = 1005,
+                  gate: bool = False, dskip: str = "ones", device: str = "cpu") -> dict:
+    """Inputs of ``steps`` chained decode steps.
+
+    state (B, H, P, N) fp32; per step t: x[t], z[t] (B, H, P); dt[t] (B, H) fp32;
+    B[t], C[t] (B, G, N); A_head, D (H,) fp32.
+    """
+    g = _gen(seed, device)
+    td = _DTYPES[dtype]
+    state = 0.1 * _randn((batch, nheads, headdim, dstate), g, device)
+    A_head = -(1.0 + 15.0 * _rand((nheads,), g, device))
+    if dskip == "ones":
+        D = torch.ones(nheads, dtype=torch.float32, device=device)
+    elif dskip == "randn":
+        D = _randn((nheads,), g, device)
+    else:
+        D = None
+    xs, dts, Bs, Cs, zs = [], [], [], [], []
+    for _ in range(steps):
+        xs.append(_randn((batch, nheads, headdim), g, device).to(td))
+        Bs.append(_randn((batch, ngroups, dstate), g, device).to(td))
+        Cs.append(_randn((batch, ngroups, dstate), g, device).to(td))
+        dts.append(torch.nn.functional.softplus(_randn((batch, nheads), g, device) - 4.0))
+        zs.append(_randn((batch, nheads, headdim), g, device).to(td) if gate else None)
+    return {"state": state.contiguous(), "A": A_head.contiguous(), "D": D,
+            "x": xs, "dt": dts, "B": Bs, "C": Cs, "z": zs}

@@ -1,0 +1,410 @@
+"""Pins for the fp64 oracle: nothing here calls the CUDA library.
+
+The oracle is checked against things other than itself: closed forms,
+brute-force unrolling written as explicit sums (not as the recurrence),
+linearity, exact associativity of the combine on dyadic rationals,
+textbook special cases (numpy.cumsum, scipy's expit, numpy's logaddexp),
+the chunked SSD against the recurrence, the scan against the SSD through a
+layout change, chained decode steps against the recurrence, and the
+Mamba-3 three-term update (decode, Eq. 9 of "Mamba-3 NKI Kernels for AWS
+Neuron", section "How it works") reduced at lambda = 1.
+"""
+import itertools
+
+import numpy as np
+import pytest
+from scipy.special import expit
+
+import oracle
+
+RTOL = 1e-12
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _softplus_np(x):
+    return np.logaddexp(0.0, x)
+
+
+def _silu_np(z):
+    return z * expit(z)
+
+
+# ---------------------------------------------------------------- closed forms
+
+@pytest.mark.parametrize("ngroups", [1, 2])
+def test_scan_geometric_closed_form(ngroups):
+    """Constant dt, A, B, C and u: h_t = dt*B*u*(1 - r^(t+1)) / (1 - r), r = e^(dt*a)."""
+    batch, dim, seqlen, dstate = 2, 4, 40, 5
+    dt, beta, c, xval = 0.07, 1.3, -0.6, 0.8
+    a = -np.linspace(0.2, 3.0, dim * dstate).reshape(dim, dstate)
+    u = np.full((batch, dim, seqlen), xval)
+    delta = np.full_like(u, dt)
+    B = np.full((batch, ngroups, dstate, seqlen), beta)
+    C = np.full_like(B, c)
+    y, hs = oracle.scan(u, delta, a, B, C)
+    t = np.arange(seqlen)
+    r = np.exp(dt * a)                                    # (dim, dstate)
+    h = dt * beta * xval * (1 - r[..., None] ** (t + 1)) / (1 - r[..., None])  # (dim, N, L)
+    y_ref = c * h.sum(axis=1)
+    np.testing.assert_allclose(y, np.broadcast_to(y_ref, y.shape), rtol=RTOL)
+    np.testing.assert_allclose(hs, np.broadcast_to(h[..., -1], hs.shape), rtol=RTOL)
+
+
+def test_ssd_geometric_closed_form():
+    batch, seqlen, nheads, headdim, dstate = 1, 33, 3, 2, 4
+    dtv, beta, c, xval = 0.05, 0.9, 1.1, -1.5
+    A_head = np.array([-1.0, -4.0, -9.5])
+    x = np.full((batch, seqlen, nheads, headdim), xval)
+    dt = np.full((batch, seqlen, nheads), dtv)
+    B = np.full((batch, seqlen, 1, dstate), beta)
+    C = np.full_like(B, c)
+    t = np.arange(seqlen)
+    r = np.exp(dtv * A_head)
+    S = dtv * beta * xval * (1 - r[None, :] ** (t[:, None] + 1)) / (1 - r[None, :])  # (L, H)
+    y_ref = dstate * c * S
+    for fn in (lambda: oracle.ssd_recurrence(x, dt, A_head, B, C),
+               lambda: oracle.ssd_chunked(x, dt, A_head, B, C, 8)):
+        y, hs = fn()
+        np.testing.assert_allclose(y[0], np.broadcast_to(y_ref[:, :, None], y[0].shape), rtol=RTOL)
+        np.testing.assert_allclose(hs[0], np.broadcast_to(S[-1][:, None, None], hs[0].shape),
+                                   rtol=RTOL)
+
+
+# ------------------------------------------------------------ brute force
+
+def _scan_bruteforce(u, delta, A, B, C, D, z, bias, softplus, h0):
+    """y_t = gate_t * (sum_n C_t,n sum_{s<=t} exp(A_n sum_{k=s+1..t} dl_k) dl_s B_s,n u_s
+    + exp(A_n sum_{k<=t} dl_k) h0_n) + D u_t), with explicit sums (O(L^2))."""
+    batch, dim, seqlen = u.shape
+    dstate = A.shape[1]
+    ngroups = B.shape[1]
+    dpg = dim // ngroups
+    y = np.zeros_like(u)
+    hs = np.zeros((batch, dim, dstate))
+    for b in range(batch):
+        for d in range(dim):
+            g = d // dpg
+            dl = delta[b, d] + (bias[d] if bias is not None else 0.0)
+            if softplus:
+                dl = _softplus_np(dl)
+            cum = np.concatenate([[0.0], np.cumsum(dl)])  # cum[t+1] = sum_{k<=t}
+            for t in range(seqlen):
+                acc = 0.0
+                for n in range(dstate):
+                    hn = 0.0
+                    for s in range(t + 1):
+                        hn += np.exp(A[d, n] * (cum[t + 1] - cum[s + 1])) * dl[s] * B[b, g, n, s] * u[b, d, s]
+                    if h0 is not None:
+                        hn += np.exp(A[d, n] * cum[t + 1]) * h0[b, d, n]
+                    acc += C[b, g, n, t] * hn
+                    if t == seqlen - 1:
+                        hs[b, d, n] = hn
+                out = acc + (D[d] * u[b, d, t] if D is not None else 0.0)
+                if z is not None:
+                    out *= _silu_np(z[b, d, t])
+                y[b, d, t] = out
+    return y, hs
+
+
+@pytest.mark.parametrize("softplus,use_z,use_D,use_h0,ngroups",
+                         [(True, True, True, False, 1), (False, False, False, False, 2),
+                          (True, False, True, True, 2), (False, True, False, True, 1)])
+def test_scan_bruteforce(softplus, use_z, use_D, use_h0, ngroups):
+    rng = _rng(7)
+    batch, dim, seqlen, dstate = 2, 4, 17, 3
+    u = rng.standard_normal((batch, dim, seqlen))
+    delta = 0.5 * rng.standard_normal((batch, dim, seqlen)) + (0.0 if softplus else 0.6)
+    A = -rng.uniform(0.1, 2.0, (dim, dstate))
+    B = rng.standard_normal((batch, ngroups, dstate, seqlen))
+    C = rng.standard_normal((batch, ngroups, dstate, seqlen))
+    D = rng.standard_normal(dim) if use_D else None
+    z = rng.standard_normal((batch, dim, seqlen)) if use_z else None
+    bias = rng.standard_normal(dim) * 0.3
+    h0 = rng.standard_normal((batch, dim, dstate)) if use_h0 else None
+    y, hs = oracle.scan(u, delta, A, B, C, D, z, bias, softplus, h0)
+    y_ref, hs_ref = _scan_bruteforce(u, delta, A, B, C, D, z, bias, softplus, h0)
+    np.testing.assert_allclose(y, y_ref, rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(hs, hs_ref, rtol=1e-11, atol=1e-13)
+
+
+def test_ssd_bruteforce():
+    """SSD: y_t[p] = sum_n C_t,n sum_{s<=t} exp(A_h sum_{k=s+1..t} dt_k) dt_s B_s,n x_s[p]."""
+    rng = _rng(11)
+    batch, seqlen, nheads, headdim, dstate, ngroups = 2, 9, 4, 3, 5, 2
+    x = rng.standard_normal((batch, seqlen, nheads, headdim))
+    dt = rng.uniform(0.01, 0.5, (batch, seqlen, nheads))
+    A_head = -rng.uniform(0.5, 4.0, nheads)
+    B = rng.standard_normal((batch, seqlen, ngroups, dstate))
+    C = rng.standard_normal((batch, seqlen, ngroups, dstate))
+    y_ref = np.zeros_like(x)
+    hs_ref = np.zeros((batch, nheads, headdim, dstate))
+    hpg = nheads // ngroups
+    for b, h in itertools.product(range(batch), range(nheads)):
+        g = h // hpg
+        cum = np.concatenate([[0.0], np.cumsum(dt[b, :, h])])
+        for t in range(seqlen):
+            w = np.exp(A_head[h] * (cum[t + 1] - cum[1:t + 2])) * dt[b, :t + 1, h]  # (t+1,)
+            S = np.einsum("s,sn,sp->pn", w, B[b, :t + 1, g], x[b, :t + 1, h])
+            y_ref[b, t, h] = S @ C[b, t, g]
+            if t == seqlen - 1:
+                hs_ref[b, h] = S
+    y, hs = oracle.ssd_recurrence(x, dt, A_head, B, C)
+    np.testing.assert_allclose(y, y_ref, rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(hs, hs_ref, rtol=1e-11, atol=1e-13)
+
+
+# ------------------------------------------------------------- invariants
+
+def test_scan_linear_in_u():
+    rng = _rng(3)
+    batch, dim, seqlen, dstate = 1, 3, 50, 4
+    u1 = rng.standard_normal((batch, dim, seqlen))
+    u2 = rng.standard_normal((batch, dim, seqlen))
+    delta = 0.5 * rng.standard_normal((batch, dim, seqlen))
+    A = -rng.uniform(0.5, 3, (dim, dstate))
+    B = rng.standard_normal((batch, 1, dstate, seqlen))
+    C = rng.standard_normal((batch, 1, dstate, seqlen))
+    D = rng.standard_normal(dim)
+    z = rng.standard_normal((batch, dim, seqlen))
+    bias = rng.standard_normal(dim)
+    al, be = 1.7, -0.4
+    f = lambda uu: oracle.scan(uu, delta, A, B, C, D, z, bias, True)
+    y12, h12 = f(al * u1 + be * u2)
+    y1, h1 = f(u1)
+    y2, h2 = f(u2)
+    np.testing.assert_allclose(y12, al * y1 + be * y2, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(h12, al * h1 + be * h2, rtol=1e-11, atol=1e-12)
+
+
+def _dyadic(rng, size):
+    return rng.integers(-64, 65, size) / 64.0
+
+
+def test_combine_is_composition_and_associative():
+    """(a1,b1) o (a2,b2) is 'apply map 1, then map 2', and o is associative
+    (exact in fp64 on dyadic rationals with few bits)."""
+    rng = _rng(5)
+    for _ in range(200):
+        a1, b1, a2, b2, a3, b3, h = _dyadic(rng, 7)
+        a12, b12 = oracle.combine(a1, b1, a2, b2)
+        assert a12 * h + b12 == a2 * (a1 * h + b1) + b2
+        left = oracle.combine(a12, b12, a3, b3)
+        a23, b23 = oracle.combine(a2, b2, a3, b3)
+        right = oracle.combine(a1, b1, a23, b23)
+        assert left == right
+    # identity element (1, 0) on both sides
+    assert oracle.combine(1.0, 0.0, 0.375, -2.5) == (0.375, -2.5)
+    assert oracle.combine(0.375, -2.5, 1.0, 0.0) == (0.375, -2.5)
+
+
+def _small_scan_problem(seed, seqlen=13, dim=3, dstate=4, ngroups=1, batch=2):
+    rng = _rng(seed)
+    return dict(
+        u=rng.standard_normal((batch, dim, seqlen)),
+        delta=0.5 * rng.standard_normal((batch, dim, seqlen)),
+        A=-rng.uniform(0.2, 3, (dim, dstate)),
+        B=rng.standard_normal((batch, ngroups, dstate, seqlen)),
+        C=rng.standard_normal((batch, ngroups, dstate, seqlen)),
+        D=rng.standard_normal(dim),
+        z=rng.standard_normal((batch, dim, seqlen)),
+        delta_bias=rng.standard_normal(dim),
+        delta_softplus=True,
+        h0=rng.standard_normal((batch, dim, dstate)),
+    )
+
+
+def test_scan_pieces_every_split_point():
+    p = _small_scan_problem(9)
+    y, hs = oracle.scan(**p)
+    L = p["u"].shape[-1]
+    for cut in range(1, L):
+        yp, hp = oracle.scan_pieces(cuts=[cut], **p)
+        np.testing.assert_allclose(yp, y, rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(hp, hs, rtol=1e-13, atol=1e-14)
+    rng = _rng(10)
+    for _ in range(10):
+        k = int(rng.integers(2, L - 1))
+        cuts = np.sort(rng.choice(np.arange(1, L), size=k, replace=False))
+        yp, hp = oracle.scan_pieces(cuts=cuts, **p)
+        np.testing.assert_allclose(yp, y, rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(hp, hs, rtol=1e-13, atol=1e-14)
+
+
+def test_scan_resume_from_final_state():
+    """Scanning [0, k) and then [k, L) from the first part's final state equals one scan."""
+    p = _small_scan_problem(12, seqlen=20)
+    y, hs = oracle.scan(**p)
+    k = 8
+    first = {key: (v[..., :k] if key in ("u", "delta", "z", "B", "C") else v) for key, v in p.items()}
+    second = {key: (v[..., k:] if key in ("u", "delta", "z", "B", "C") else v) for key, v in p.items()}
+    y1, h1 = oracle.scan(**first)
+    second["h0"] = h1
+    y2, h2 = oracle.scan(**second)
+    np.testing.assert_allclose(np.concatenate([y1, y2], axis=-1), y, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(h2, hs, rtol=1e-13, atol=1e-14)
+
+
+# ------------------------------------------------------- special cases
+
+def test_scan_reduces_to_cumsum():
+    """A = 0, N = 1, B = C = 1, no softplus, gate or skip: y = cumsum(dt * u)."""
+    rng = _rng(2)
+    batch, dim, seqlen = 2, 3, 64
+    u = rng.standard_normal((batch, dim, seqlen))
+    delta = rng.uniform(0, 1, (batch, dim, seqlen))
+    A = np.zeros((dim, 1))
+    B = np.ones((batch, 1, 1, seqlen))
+    y, hs = oracle.scan(u, delta, A, B, B)
+    np.testing.assert_allclose(y, np.cumsum(delta * u, axis=-1), rtol=1e-13)
+    np.testing.assert_allclose(hs[..., 0], np.sum(delta * u, axis=-1), rtol=1e-13)
+
+
+def test_scan_zero_delta_is_skip_times_gate():
+    rng = _rng(4)
+    batch, dim, seqlen, dstate = 1, 4, 10, 3
+    u = rng.standard_normal((batch, dim, seqlen))
+    z = 3 * rng.standard_normal((batch, dim, seqlen))
+    D = rng.standard_normal(dim)
+    A = -rng.uniform(0.5, 2, (dim, dstate))
+    B = rng.standard_normal((batch, 1, dstate, seqlen))
+    y, hs = oracle.scan(u, np.zeros_like(u), A, B, B, D, z)
+    np.testing.assert_allclose(y, D[None, :, None] * u * z * expit(z), rtol=1e-14)
+    assert np.all(hs == 0.0)
+
+
+def test_scan_single_step_and_softplus_bias_order():
+    """L = 1: y = dl * u * sum_n B_n C_n + D u, with dl = softplus(delta + bias)."""
+    rng = _rng(6)
+    batch, dim, dstate = 2, 5, 4
+    u = rng.standard_normal((batch, dim, 1))
+    delta = rng.standard_normal((batch, dim, 1))
+    bias = rng.standard_normal(dim)
+    A = -rng.uniform(0.5, 2, (dim, dstate))
+    B = rng.standard_normal((batch, 1, dstate, 1))
+    C = rng.standard_normal((batch, 1, dstate, 1))
+    D = rng.standard_normal(dim)
+    bc = np.sum(B[:, 0, :, 0] * C[:, 0, :, 0], axis=-1)  # (batch,)
+    for softplus in (True, False):
+        dl = delta[..., 0] + bias[None, :]
+        if softplus:
+            dl = _softplus_np(dl)
+        y, _ = oracle.scan(u, delta, A, B, C, D, None, bias, softplus)
+        ref = dl * u[..., 0] * bc[:, None] + D[None, :] * u[..., 0]
+        np.testing.assert_allclose(y[..., 0], ref, rtol=1e-13)
+
+
+def test_softplus_large_arguments():
+    """softplus stays finite and exact far out: softplus(800) = 800, softplus(-800) ~ e^-800 = 0."""
+    u = np.ones((1, 2, 1))
+    delta = np.array([[[800.0], [-800.0]]])
+    A = np.zeros((2, 1))
+    B = np.ones((1, 1, 1, 1))
+    y, _ = oracle.scan(u, delta, A, B, B, delta_softplus=True)
+    assert y[0, 0, 0] == 800.0
+    assert y[0, 1, 0] == 0.0
+
+
+# ------------------------------------------------------ cross-path pins
+
+@pytest.mark.parametrize("chunk", [1, 2, 12, 24, 7])
+def test_ssd_chunked_equals_recurrence(chunk):
+    rng = _rng(13)
+    batch, seqlen, nheads, headdim, dstate, ngroups = 2, 24, 4, 3, 6, 2
+    x = rng.standard_normal((batch, seqlen, nheads, headdim))
+    dt = _softplus_np(rng.standard_normal((batch, seqlen, nheads)) - 1.0)
+    A_head = -rng.uniform(1, 16, nheads)
+    B = rng.standard_normal((batch, seqlen, ngroups, dstate))
+    C = rng.standard_normal((batch, seqlen, ngroups, dstate))
+    h0 = rng.standard_normal((batch, nheads, headdim, dstate))
+    y, hs = oracle.ssd_recurrence(x, dt, A_head, B, C, h0)
+    yc, hc = oracle.ssd_chunked(x, dt, A_head, B, C, chunk, h0)
+    np.testing.assert_allclose(yc, y, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(hc, hs, rtol=1e-12, atol=1e-13)
+
+
+def test_scan_with_head_constant_A_equals_ssd():
+    """Scan channels d = h*P + p with A[d, n] = A_h equal the SSD of (B, L, H, P)."""
+    rng = _rng(17)
+    batch, seqlen, nheads, headdim, dstate, ngroups = 2, 15, 4, 3, 5, 2
+    x = rng.standard_normal((batch, seqlen, nheads, headdim))
+    dt = rng.uniform(0.01, 0.3, (batch, seqlen, nheads))
+    A_head = -rng.uniform(1, 8, nheads)
+    B = rng.standard_normal((batch, seqlen, ngroups, dstate))
+    C = rng.standard_normal((batch, seqlen, ngroups, dstate))
+    y_ssd, hs_ssd = oracle.ssd_recurrence(x, dt, A_head, B, C)
+    dim = nheads * headdim
+    u = x.reshape(batch, seqlen, dim).transpose(0, 2, 1)
+    delta = np.repeat(dt, headdim, axis=2).transpose(0, 2, 1)
+    A = np.repeat(A_head, headdim)[:, None] * np.ones((1, dstate))
+    Bs = B.transpose(0, 2, 3, 1)
+    Cs = C.transpose(0, 2, 3, 1)
+    y_scan, hs_scan = oracle.scan(u, delta, A, Bs, Cs)
+    np.testing.assert_allclose(y_scan, y_ssd.reshape(batch, seqlen, dim).transpose(0, 2, 1),
+                               rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(hs_scan, hs_ssd.reshape(batch, dim, dstate), rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("with_gate", [False, True])
+def test_decode_chain_equals_recurrence(with_gate):
+    rng = _rng(19)
+    batch, T, nheads, headdim, dstate, ngroups = 2, 12, 4, 3, 5, 2
+    x = rng.standard_normal((batch, T, nheads, headdim))
+    dt = rng.uniform(0.01, 0.4, (batch, T, nheads))
+    A_head = -rng.uniform(1, 8, nheads)
+    B = rng.standard_normal((batch, T, ngroups, dstate))
+    C = rng.standard_normal((batch, T, ngroups, dstate))
+    D = rng.standard_normal(nheads) if with_gate else None
+    z = rng.standard_normal((batch, T, nheads, headdim)) if with_gate else None
+    h0 = rng.standard_normal((batch, nheads, headdim, dstate))
+    y_ref, hs_ref = oracle.ssd_recurrence(x, dt, A_head, B, C, h0)
+    state = h0.copy()
+    for t in range(T):
+        y, state = oracle.decode_step(state, x[:, t], dt[:, t], A_head, B[:, t], C[:, t], D,
+                                      None if z is None else z[:, t])
+        ref = y_ref[:, t]
+        if with_gate:
+            ref = (ref + D[None, :, None] * x[:, t]) * _silu_np(z[:, t])
+        np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(state, hs_ref, rtol=1e-12, atol=1e-13)
+
+
+def test_mamba3_three_term_update_reduces_at_lambda_one():
+    """Eq. 9: h_t = alpha h_{t-1} + beta prev_Bx + gamma (B_t x_t), with
+    alpha = exp(dt A), gamma = lambda dt, beta = (dt - gamma) alpha.  At
+    lambda = 1, beta = 0 and gamma = dt: the decode step is this update."""
+    rng = _rng(23)
+    batch, T, nheads, headdim, dstate = 1, 10, 2, 3, 4
+    x = rng.standard_normal((batch, T, nheads, headdim))
+    dt = rng.uniform(0.01, 0.4, (batch, T, nheads))
+    A_head = -rng.uniform(1, 8, nheads)
+    B = rng.standard_normal((batch, T, 1, dstate))
+    C = rng.standard_normal((batch, T, 1, dstate))
+
+    def mamba3(lam):
+        h = np.zeros((batch, nheads, headdim, dstate))
+        prev_bx = np.zeros_like(h)
+        ys = []
+        for t in range(T):
+            alpha = np.exp(dt[:, t] * A_head)[..., None, None]
+            gamma = lam * dt[:, t][..., None, None]
+            beta = (dt[:, t][..., None, None] - gamma) * alpha
+            bx = np.einsum("bp,bn->bpn", x[:, t, 0], B[:, t, 0])[:, None] if nheads == 1 else \
+                np.einsum("bhp,bn->bhpn", x[:, t], B[:, t, 0])
+            h = alpha * h + beta * prev_bx + gamma * bx
+            prev_bx = bx
+            ys.append(np.einsum("bhpn,bn->bhp", h, C[:, t, 0]))
+        return np.stack(ys, axis=1), h
+
+    state = np.zeros((batch, nheads, headdim, dstate))
+    ys = []
+    for t in range(T):
+        y, state = oracle.decode_step(state, x[:, t], dt[:, t], A_head, B[:, t], C[:, t])
+        ys.append(y)
+    y_m3, h_m3 = mamba3(1.0)
+    np.testing.assert_allclose(np.stack(ys, axis=1), y_m3, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(state, h_m3, rtol=1e-12, atol=1e-13)
+    y_half, _ = mamba3(0.5)
+    assert np.max(np.abs(y_half - y_m3)) > 1e-3  # lambda matters away from 1

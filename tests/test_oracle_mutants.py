@@ -1,0 +1,71 @@
+"""The oracle's pins are strong enough to catch plausible mistakes.
+
+Each case copies ``oracle/oracle.c``, plants one mistake of the kind a
+careless implementation makes (a dropped term, a wrong sign, a transposed
+index, two steps in the wrong order), builds the copy, and runs the pin
+suite ``tests/test_oracle.py`` against it: the suite must fail.  The real
+oracle is never modified.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.c")
+
+MUTANTS = {
+    "scan_drops_dt_in_input_term": (
+        "h[n] = a * h[n] + dl * bn * x;", "h[n] = a * h[n] + bn * x;"),
+    "scan_wrong_sign_in_decay": (
+        "const double a = exp(dl * A[(size_t)d * dstate + n]);\n                const double bn",
+        "const double a = exp(-dl * A[(size_t)d * dstate + n]);\n                const double bn"),
+    "scan_transposed_B_index": (
+        "const double bn = Bm[bc + (size_t)n * seqlen + t];",
+        "const double bn = Bm[bc + (size_t)t * dstate + n];"),
+    "scan_reads_state_before_update": (
+        "h[n] = a * h[n] + dl * bn * x;\n                acc += cn * h[n];",
+        "acc += cn * h[n];\n                h[n] = a * h[n] + dl * bn * x;"),
+    "scan_gate_before_skip": (
+        "double out = acc + (Dskip ? Dskip[d] * x : 0.0);\n            if (z) out *= silu_d(z[io + t]);\n            y[io + t] = out;\n        }\n        if (final_state)\n            for (int n = 0; n < dstate; ++n) final_state[row * dstate + n] = h[n];",
+        "double out = acc;\n            if (z) out *= silu_d(z[io + t]);\n            out += (Dskip ? Dskip[d] * x : 0.0);\n            y[io + t] = out;\n        }\n        if (final_state)\n            for (int n = 0; n < dstate; ++n) final_state[row * dstate + n] = h[n];"),
+    "scan_bias_after_softplus": (
+        "double dl = delta[io + t] + (delta_bias ? delta_bias[d] : 0.0);\n            if (delta_softplus) dl = softplus_d(dl);\n            const double x = u[io + t];\n            double acc = 0.0;\n            for (int n = 0; n < dstate; ++n) {\n                const double a",
+        "double dl = delta[io + t];\n            if (delta_softplus) dl = softplus_d(dl);\n            dl += (delta_bias ? delta_bias[d] : 0.0);\n            const double x = u[io + t];\n            double acc = 0.0;\n            for (int n = 0; n < dstate; ++n) {\n                const double a"),
+    "scan_wrong_group_index": (
+        "const int g = d / dim_per_group;\n        double* h = (double*)malloc",
+        "const int g = d % ngroups;\n        double* h = (double*)malloc"),
+    "silu_wrong_sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
+    "softplus_negative_branch": ("return log1p(exp(x));", "return log(exp(x));"),
+    "combine_swapped": ("*b_out = a2 * b1 + b2;", "*b_out = a1 * b2 + b1;"),
+    "ssd_drops_dt": ("S[n] = a * S[n] + dtv * Bt[n] * xv;", "S[n] = a * S[n] + Bt[n] * xv;"),
+    "ssd_decay_uses_wrong_head": ("const double a = exp(dtv * A_head[h]);",
+                                  "const double a = exp(dtv * A_head[0]);"),
+    "ssd_chunked_mask_drops_diagonal": ("if (j <= i) {", "if (j < i) {"),
+    "ssd_chunked_drops_offdiag_decay": ("yo *= exp(cs[i]);", "yo *= 1.0;"),
+    "ssd_chunked_state_decay_reversed": (
+        "s += exp(cs[q - 1] - cs[j]) * DT(j)", "s += exp(cs[j] - cs[q - 1]) * DT(j)"),
+    "decode_missing_skip": ("double out = acc + (Dskip ? Dskip[h] * xv : 0.0);",
+                            "double out = acc;"),
+    "decode_alpha_without_dt": ("const double alpha = exp(dtv * A[h]);",
+                                "const double alpha = exp(A[h]);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mutant_c = tmp_path / "oracle_mutant.c"
+    mutant_c.write_text(src.replace(old, new))
+    lib = tmp_path / "liboracle_mutant.so"
+    subprocess.run(["gcc", "-O1", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-o", str(lib),
+                    str(mutant_c), "-lm"], check=True)
+    env = dict(os.environ, SSM_ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle.py")],
+                       env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"pins did not catch mutant {name}:\n{r.stdout[-2000:]}"
+    assert "failed" in r.stdout, r.stdout[-2000:]
