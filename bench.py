@@ -1,0 +1,365 @@
+"""Benchmark of the selective-scan hot path on GB300.
+
+Workload (one "step"): one ssm_scan_fwd over the bf16 selective-scan
+workload batch 8, L 2048, 1536 channels, N 16 (z gate and softplus on,
+final_state returned, y in fp32), inputs resident in HBM.  Metric: scan
+elements per second, B*L*D*N / time, whole job.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun each rank runs its own copy of the workload on its GPU
+(independent problems, no collective on the data path: weak scaling); the
+timed region is bracketed by barriers and the slowest rank's time is used.
+
+--impl reference times the fp64 CPU oracle (the only reference this method
+has) on a bounded sample of the same workload, on the host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+BATCH, DIM, SEQLEN, DSTATE, NGROUPS = 8, 1536, 2048, 16, 1
+METRIC = "scan elements/s (B*L*D*N per s)"
+UNIT = "elements/s"
+WORKLOAD = ("selective scan, bf16 inputs / fp32 state / fp32 y, batch 8, L 2048, "
+            "D 1536, N 16, z gate + softplus(delta + bias), final_state")
+
+# Roofline of the scan kernel: multi-function-unit (MUFU) bound.  Per
+# element (b, l, d, n) one exp2; per (b, l, d) two MUFU ops for softplus
+# (ex2, rcp) and two for the silu gate (ex2, rcp).  Peak = 152 SMs x 16 MUFU
+# results per clock x 2070 MHz (maximum SM clock).
+SMS, MUFU_PER_CLK, SM_MAX_MHZ = 152, 16, 2070.0
+MUFU_PEAK_GOPS = SMS * MUFU_PER_CLK * SM_MAX_MHZ * 1e6 / 1e9
+# DRAM bytes per launch of the scan kernel from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum) of this exact kernel build and
+# workload; None until captured.
+SCAN_TRAFFIC_BYTES = None
+
+
+def algorithmic_counts():
+    bld = BATCH * SEQLEN * DIM
+    elements = bld * DSTATE
+    mufu = elements + 4 * bld
+    # bytes: u, delta, z (bf16) in; y (fp32) out; B, C (bf16) in; A, D, bias;
+    # final_state out
+    hbm = bld * (3 * 2 + 4) + 2 * BATCH * NGROUPS * DSTATE * SEQLEN * 2 \
+        + DIM * DSTATE * 4 + 2 * DIM * 4 + BATCH * DIM * DSTATE * 4
+    return elements, mufu, hbm
+
+
+# ------------------------------------------------------------------ ranks
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, value: float, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms", str(self.period)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+        time.sleep(0.3)  # let the first sample arrive
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        rows = [l for (t, l) in self.lines if t0 - 0.05 <= t <= t1 + 0.15] or \
+               [l for (_, l) in self.lines[-3:]]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ ours
+
+def make_inputs(rank):
+    from state_space_model_selective_gb300 import inputs
+    return inputs.scan_inputs(BATCH, DIM, SEQLEN, DSTATE, NGROUPS, "bf16", seed=1002 + rank,
+                              gate=True, dskip="ones", device="cpu")
+
+
+def cpu_baseline(inp, max_seconds=20.0):
+    """Time the fp64 oracle (as it stands) on a bounded sample of the workload:
+    the first `nb` batch rows of the same inputs, nb grown until the run
+    takes at least ~2 s, capped so the total stays within max_seconds."""
+    import oracle
+    nb, elapsed, el = 1, 0.0, 0
+    dims = None
+    while True:
+        sl = slice(0, nb)
+        args = (inp["u"][sl], inp["delta"][sl], inp["A"], inp["B"][sl], inp["C"][sl],
+                inp["D"], inp["z"][sl], inp["delta_bias"], True)
+        t0 = time.perf_counter()
+        oracle.scan(*args)
+        elapsed = time.perf_counter() - t0
+        el = nb * SEQLEN * DIM * DSTATE
+        dims = nb
+        if elapsed >= 2.0 or nb >= BATCH or elapsed * 2 * 2 > max_seconds:
+            break
+        nb = min(BATCH, nb * 2)
+    return {"value": el / elapsed, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"batch rows 0..{dims - 1} of the workload ({dims}x{DIM}x{SEQLEN}x{DSTATE} "
+                      f"= {el} elements), fp64, one run, {elapsed:.2f} s"}
+
+
+def run_ours(args):
+    import torch
+    from state_space_model_selective_gb300 import binding
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+
+    host = make_inputs(rank)
+    # pinned host copies (the e2e leg copies them in every step)
+    pinned = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    y = torch.empty((BATCH, DIM, SEQLEN), dtype=torch.float32, device=dev)
+    fs = torch.empty((BATCH, DIM, DSTATE), dtype=torch.float32, device=dev)
+    ws = torch.empty(binding.ssm_scan_workspace_bytes(BATCH, DIM, SEQLEN, DSTATE, NGROUPS),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        binding.ssm_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                             d["delta_bias"], True, out_dtype=torch.float32, y=y,
+                             final_state=fs, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert binding.ssm_last_device_status(ws) == 0
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    barrier(dist)
+    sampler.stop()
+    ms_local = ev0.elapsed_time(ev1)
+    ms = max_over_ranks(dist, ms_local, dev)
+    clocks = sampler.summary(t_wall0, t_wall1)
+    assert binding.ssm_last_device_status(ws) == 0
+
+    elements, mufu, hbm = algorithmic_counts()
+    total_elements = sum_over_ranks(dist, float(elements * args.steps), dev)
+    value = total_elements / (ms / 1e3)
+    per_launch_s = ms_local / 1e3 / args.steps
+    achieved = mufu / per_launch_s / 1e9
+
+    # ---- e2e: same call with host buffers; H2D of the step's inputs and D2H
+    # of its outputs inside the timed region
+    e2e_steps = max(3, min(args.steps, 20))
+    names = ["u", "delta", "z", "B", "C", "A", "D", "delta_bias"]
+    h2d = sum(pinned[k].numel() * pinned[k].element_size() for k in names)
+    y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    fs_host = torch.empty(fs.shape, dtype=fs.dtype, pin_memory=True)
+    d2h = y_host.numel() * 4 + fs_host.numel() * 4
+
+    def e2e_step():
+        for k in names:
+            d[k].copy_(pinned[k], non_blocking=True)
+        step()
+        y_host.copy_(y, non_blocking=True)
+        fs_host.copy_(fs, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1), dev)
+    e2e_total = sum_over_ranks(dist, float(elements * e2e_steps), dev)
+
+    out = None
+    if rank == 0:
+        cpu = cpu_baseline(host) if world == 1 else None  # rank 0 at N=1 only
+        out = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": BATCH, "seqlen": SEQLEN, "dim": DIM,
+                       "dstate": DSTATE, "ngroups": NGROUPS, "in_dtype": "bf16",
+                       "state_dtype": "f32", "out_dtype": "f32",
+                       "l2": "inputs 152 MB > 129 MB L2 (no flush)",
+                       "parallelism": f"independent workload per GPU x{world}"},
+            "e2e": {"value": e2e_total / (e2e_ms / 1e3), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps,
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": MUFU_PEAK_GOPS,
+                         "unit": "Gop/s (MUFU)", "frac": achieved / MUFU_PEAK_GOPS,
+                         "traffic": SCAN_TRAFFIC_BYTES,
+                         "algorithmic_mufu_ops_per_launch": mufu,
+                         "algorithmic_hbm_bytes_per_launch": hbm,
+                         "hbm_gbs_at_this_time": hbm / per_launch_s / 1e9},
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return out
+
+
+# ------------------------------------------------------------------ reference
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    from state_space_model_selective_gb300 import inputs
+    inp = inputs.scan_inputs(BATCH, DIM, SEQLEN, DSTATE, NGROUPS, "bf16", seed=1002, gate=True,
+                             dskip="ones", device="cpu")
+    import oracle
+    # each step: the oracle over one batch row of the workload (bounded sample)
+    sl = slice(0, 1)
+    a = (inp["u"][sl], inp["delta"][sl], inp["A"], inp["B"][sl], inp["C"][sl], inp["D"],
+         inp["z"][sl], inp["delta_bias"], True)
+    oracle.scan(*a)  # one untimed warm-up run (the oracle has no state to warm)
+    steps = max(1, min(args.steps, 5))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.scan(*a)
+    el = time.perf_counter() - t0
+    elements = steps * SEQLEN * DIM * DSTATE
+    value = elements / el
+    sample = (f"{steps} step(s), each the fp64 oracle over batch row 0 of the workload "
+              f"(1x{DIM}x{SEQLEN}x{DSTATE} elements)")
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+           "n_gpus": world, "steps": steps, "warmup": args.warmup,
+           "ms_per_step": el / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": WORKLOAD, "batch": BATCH, "seqlen": SEQLEN, "dim": DIM,
+                      "dstate": DSTATE},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                            "kind": "oracle", "sample": sample}}
+    print(json.dumps(out), flush=True)
+    return out
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

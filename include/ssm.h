@@ -1,0 +1,169 @@
+/*
+ * ssm.h -- C ABI of the GB300 (sm_103a) selective state-space scan library.
+ *
+ * Three operations, each a hand-written CUDA kernel on one GPU:
+ *
+ *   ssm_scan_fwd     selective scan, per-channel per-state A (Mamba-1 form)
+ *   ssd_chunked_fwd  scalar-A-per-head chunked SSD (Mamba-2 form), tensor cores
+ *   ssm_decode_step  single-token state update, in place
+ *
+ * Conventions shared by every entry point
+ *  - Pointers are DEVICE pointers unless stated otherwise, to dense row-major
+ *    (C-contiguous) arrays in the layouts given per function.  The caller owns
+ *    every buffer, including the scan's workspace; the library allocates
+ *    nothing and keeps no state between calls.
+ *  - Every base pointer must be 16-byte aligned (any cudaMalloc or PyTorch
+ *    allocation is), else SSM_ERR_ALIGN.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Work is only enqueued on it; no entry point synchronises
+ *    except ssm_last_device_status.
+ *  - Arguments are checked on the host before anything is enqueued; on any
+ *    error nothing is launched and the error code is returned.  A launch
+ *    failure returns SSM_ERR_CUDA.  Device-side waits are bounded: if one
+ *    runs out, the kernel records SSM_ERR_TIMEOUT in the workspace (read it
+ *    with ssm_last_device_status) and finishes without hanging; its outputs
+ *    are then undefined.  No entry point aborts, prints or traps.
+ *  - Outputs must not overlap inputs (SSM_ERR_ALIAS).  Inputs are never
+ *    written, except `state` of ssm_decode_step, which is updated in place.
+ *  - All state and accumulation is fp32.  `in_dtype` is the type of the
+ *    activations (u/delta/z/B/C, or x/B/C); `out_dtype` the type of y.
+ *    A, D, delta_bias, dt and every state array are always fp32.
+ *
+ * Page citations are by page title and section.
+ */
+#ifndef SSM_GB300_H
+#define SSM_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_NULL = 1,        /* a required pointer is NULL */
+    SSM_ERR_SHAPE = 2,       /* a size is negative or inconsistent */
+    SSM_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+    SSM_ERR_DTYPE = 4,       /* unknown dtype code */
+    SSM_ERR_UNSUPPORTED = 5, /* valid, but not a size this library implements */
+    SSM_ERR_WORKSPACE = 6,   /* workspace NULL or smaller than required */
+    SSM_ERR_TIMEOUT = 7,     /* a bounded device-side wait ran out */
+    SSM_ERR_CUDA = 8,        /* a CUDA runtime call or a launch failed */
+    SSM_ERR_ALIAS = 9        /* an output overlaps an input */
+} ssm_status_t;
+
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype_t;
+
+/* Version of this ABI (incremented on any incompatible change). */
+int ssm_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* ssm_status_string(ssm_status_t status);
+
+/*
+ * Bytes of device workspace ssm_scan_fwd needs for this problem (a pure
+ * function of its arguments; 0 never returned for a valid problem).
+ * Returns 0 if the arguments are invalid.
+ */
+size_t ssm_scan_workspace_bytes(int batch, int dim, int seqlen, int dstate, int ngroups);
+
+/*
+ * Selective scan.
+ *   "We brought Mamba to Trainium -- and mapped where custom kernels actually
+ *   help", section "Mamba: bringing an unsupported model to the chip, and
+ *   writing its missing kernel": h_t = A_t h_{t-1} + B_t x_t, y_t = sum_n C_t h_t.
+ *   "Mamba-3 NKI Kernels for AWS Neuron", section "How it works": Phase 0,
+ *   dt = softplus(dt + dt_bias) and alpha = exp(dt A); Phase 5, D skip then
+ *   silu gate.
+ *
+ * For every batch b, channel d (group g = d / (dim / ngroups)), step t and
+ * state n, in fp32:
+ *   dl      = delta[b,d,t] + delta_bias[d];  dl = softplus(dl) if delta_softplus
+ *   h[n]    = exp(dl * A[d,n]) * h[n] + dl * B[b,g,n,t] * u[b,d,t]
+ *   y[b,d,t] = (sum_n C[b,g,n,t] h[n] + D[d] u[b,d,t]) * silu(z[b,d,t])
+ * starting from h = initial_state[b,d,:] (or 0); final_state[b,d,:] = h
+ * after the last step.
+ *
+ * Layouts (in_dtype for u, delta, z, B, C; out_dtype for y):
+ *   u, delta, z, y    (batch, dim, seqlen)          seqlen contiguous
+ *   A                 (dim, dstate)        fp32
+ *   B, C              (batch, ngroups, dstate, seqlen)
+ *   D, delta_bias     (dim,)               fp32, each may be NULL (0)
+ *   z                 may be NULL (no gate)
+ *   initial_state     (batch, dim, dstate) fp32, may be NULL (zero state)
+ *   final_state       (batch, dim, dstate) fp32, may be NULL (not written)
+ *   workspace         device memory of at least
+ *                     ssm_scan_workspace_bytes(...) bytes; its contents on
+ *                     entry do not matter; it must not be used by another
+ *                     call that may run concurrently.
+ * Supported: dstate == 16; dim % ngroups == 0; any batch, dim, seqlen >= 0.
+ * seqlen == 0 writes final_state = initial_state (or 0).
+ */
+ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const float* A,
+                          const void* B, const void* C, const float* D, const void* z,
+                          const float* delta_bias, int delta_softplus,
+                          const float* initial_state, void* y, float* final_state,
+                          int batch, int dim, int seqlen, int dstate, int ngroups,
+                          ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Chunked SSD, scalar A per head.
+ *   "Mamba-3 NKI Kernels for AWS Neuron", section "Kernel details",
+ *   mamba3_siso_ssd_kernel (the Mamba-2 SSD structure, chunk 64, stated to be
+ *   mathematically equivalent to the recurrence), and section
+ *   "Configuration constraints" (seqlen must be divisible by chunk_size).
+ *
+ * Computes, exactly up to rounding, the recurrence
+ *   S[p,n] = exp(dt[b,t,h] A_head[h]) S[p,n] + dt[b,t,h] B[b,t,g,n] x[b,t,h,p]
+ *   y[b,t,h,p] = sum_n C[b,t,g,n] S[p,n]
+ * from S = 0 (g = h / (nheads / ngroups)); final_state[b,h,p,n] = S after
+ * the last step.  dt is taken as given (already discretised).
+ *
+ * Layouts: x, y (batch, seqlen, nheads, headdim); dt (batch, seqlen, nheads)
+ * fp32; A_head (nheads,) fp32; B, C (batch, seqlen, ngroups, dstate);
+ * final_state (batch, nheads, headdim, dstate) fp32, may be NULL.
+ * Supported: chunk == 64, headdim == 64, dstate == 128, in_dtype == SSM_BF16,
+ * seqlen % chunk == 0 (else SSM_ERR_SHAPE), nheads % ngroups == 0.
+ */
+ssm_status_t ssd_chunked_fwd(const void* x, const float* dt, const float* A_head,
+                             const void* B, const void* C, int chunk,
+                             void* y, float* final_state,
+                             int batch, int seqlen, int nheads, int headdim, int dstate,
+                             int ngroups, ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                             void* stream);
+
+/*
+ * One decode step, in place.
+ *   "Mamba-3 NKI Kernels for AWS Neuron", section "How it works", decode via
+ *   step(), Eq. 9 with lambda = 1 (beta = 0, gamma = dt), and Phase 5 (D skip,
+ *   silu gate); section "Kernel details", mamba3_siso_decode_state_kernel.
+ *
+ *   alpha = exp(dt[b,h] A[h])
+ *   state[b,h,p,n] = alpha state[b,h,p,n] + dt[b,h] x[b,h,p] B[b,g,n]
+ *   y[b,h,p] = (sum_n C[b,g,n] state[b,h,p,n] + D[h] x[b,h,p]) * silu(z[b,h,p])
+ *
+ * Layouts: state (batch, nheads, headdim, dstate) fp32, read and written;
+ * x, z, y (batch, nheads, headdim) in dtype; dt (batch, nheads) fp32;
+ * A, D (nheads,) fp32 (D may be NULL); B, C (batch, ngroups, dstate) in
+ * dtype; z may be NULL.  Supported: dstate % 32 == 0 and dstate <= 256.
+ */
+ssm_status_t ssm_decode_step(float* state, const void* x, const float* dt,
+                             const float* A, const void* B, const void* C,
+                             const float* D, const void* z, void* y,
+                             int batch, int nheads, int headdim, int dstate, int ngroups,
+                             ssm_dtype_t dtype, void* stream);
+
+/*
+ * Waits for `stream` to drain, then returns the device-side status the last
+ * ssm_scan_fwd that used `workspace` recorded (SSM_OK or SSM_ERR_TIMEOUT),
+ * or SSM_ERR_CUDA if the stream itself reports an error.
+ */
+ssm_status_t ssm_last_device_status(const void* workspace, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_GB300_H */

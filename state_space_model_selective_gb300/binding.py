@@ -1,0 +1,211 @@
+"""Thin Python binding of ``libssm.so`` (ctypes; argument marshalling only).
+
+Every function here has the name of the C entry point it calls.  Tensors
+are torch CUDA tensors; this module only checks that they are contiguous
+CUDA tensors of the expected dtype, allocates outputs when the caller does
+not pass them (PyTorch is the memory allocator), and passes raw pointers
+and the current CUDA stream.  All arithmetic happens in the library's
+kernels.  There is no fallback: if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libssm.so")
+
+SSM_F32, SSM_BF16 = 0, 1
+_DT = {torch.float32: SSM_F32, torch.bfloat16: SSM_BF16}
+_TORCH_DT = {SSM_F32: torch.float32, SSM_BF16: torch.bfloat16}
+
+STATUS_NAMES = {0: "SSM_OK", 1: "SSM_ERR_NULL", 2: "SSM_ERR_SHAPE", 3: "SSM_ERR_ALIGN",
+                4: "SSM_ERR_DTYPE", 5: "SSM_ERR_UNSUPPORTED", 6: "SSM_ERR_WORKSPACE",
+                7: "SSM_ERR_TIMEOUT", 8: "SSM_ERR_CUDA", 9: "SSM_ERR_ALIAS"}
+
+# every symbol include/ssm.h declares
+EXPORTS = ["ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_bytes", "ssm_scan_fwd",
+           "ssd_chunked_fwd", "ssm_decode_step", "ssm_last_device_status"]
+
+
+class SSMError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} "
+                         f"({status_string(status)})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.ssm_abi_version.restype = i
+        L.ssm_status_string.restype = ctypes.c_char_p
+        L.ssm_status_string.argtypes = [i]
+        L.ssm_scan_workspace_bytes.restype = sz
+        L.ssm_scan_workspace_bytes.argtypes = [i] * 5
+        L.ssm_scan_fwd.restype = i
+        L.ssm_scan_fwd.argtypes = [vp] * 8 + [i] + [vp] * 3 + [i] * 7 + [vp, sz, vp]
+        L.ssd_chunked_fwd.restype = i
+        L.ssd_chunked_fwd.argtypes = [vp] * 5 + [i] + [vp] * 2 + [i] * 8 + [vp]
+        L.ssm_decode_step.restype = i
+        L.ssm_decode_step.argtypes = [vp] * 9 + [i] * 6 + [vp]
+        L.ssm_last_device_status.restype = i
+        L.ssm_last_device_status.argtypes = [vp, vp]
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().ssm_status_string(int(status)).decode()
+
+
+def ssm_abi_version() -> int:
+    return int(lib().ssm_abi_version())
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise SSMError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _req(t, name, dtype=None, ndim=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+    return t
+
+
+def _opt(t, name, dtype=None, ndim=None):
+    return None if t is None else _req(t, name, dtype, ndim)
+
+
+def ssm_scan_workspace_bytes(batch, dim, seqlen, dstate=16, ngroups=1) -> int:
+    return int(lib().ssm_scan_workspace_bytes(batch, dim, seqlen, dstate, ngroups))
+
+
+def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=False,
+                 initial_state=None, out_dtype=None, y=None, final_state=None,
+                 workspace=None, return_final_state=True, stream=None):
+    """Selective scan.  u, delta, z: (batch, dim, seqlen); A: (dim, dstate) fp32;
+    B, C: (batch, ngroups, dstate, seqlen); D, delta_bias: (dim,) fp32;
+    initial_state: (batch, dim, dstate) fp32.  Returns (y, final_state)."""
+    _req(u, "u", ndim=3)
+    in_dt = u.dtype
+    if in_dt not in _DT:
+        raise TypeError("u must be float32 or bfloat16")
+    batch, dim, seqlen = u.shape
+    _req(delta, "delta", in_dt)
+    _req(A, "A", torch.float32, 2)
+    dstate = A.shape[1]
+    _req(B, "B", in_dt, 4)
+    _req(C, "C", in_dt, 4)
+    ngroups = B.shape[1]
+    _opt(D, "D", torch.float32)
+    _opt(z, "z", in_dt)
+    _opt(delta_bias, "delta_bias", torch.float32)
+    _opt(initial_state, "initial_state", torch.float32)
+    out_dt = in_dt if out_dtype is None else out_dtype
+    if y is None:
+        y = torch.empty((batch, dim, seqlen), dtype=out_dt, device=u.device)
+    _req(y, "y", out_dt)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((batch, dim, dstate), dtype=torch.float32, device=u.device)
+    _opt(final_state, "final_state", torch.float32)
+    need = ssm_scan_workspace_bytes(batch, dim, seqlen, dstate, ngroups)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=u.device)
+    _req(workspace, "workspace", torch.uint8)
+    st = lib().ssm_scan_fwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                            _ptr(delta_bias), int(bool(delta_softplus)), _ptr(initial_state),
+                            _ptr(y), _ptr(final_state), batch, dim, seqlen, dstate, ngroups,
+                            _DT[in_dt], _DT[out_dt], _ptr(workspace), workspace.numel(),
+                            _stream(stream))
+    _check(st, "ssm_scan_fwd")
+    return y, final_state
+
+
+def ssd_chunked_fwd(x, dt, A_head, B, C, chunk=64, out_dtype=None, y=None, final_state=None,
+                    return_final_state=True, stream=None):
+    """Chunked SSD.  x: (batch, seqlen, nheads, headdim); dt: (batch, seqlen, nheads) fp32;
+    A_head: (nheads,) fp32; B, C: (batch, seqlen, ngroups, dstate).  Returns (y, final_state)."""
+    _req(x, "x", ndim=4)
+    in_dt = x.dtype
+    if in_dt not in _DT:
+        raise TypeError("x must be float32 or bfloat16")
+    batch, seqlen, nheads, headdim = x.shape
+    _req(dt, "dt", torch.float32, 3)
+    _req(A_head, "A_head", torch.float32, 1)
+    _req(B, "B", in_dt, 4)
+    _req(C, "C", in_dt, 4)
+    ngroups, dstate = B.shape[2], B.shape[3]
+    out_dt = in_dt if out_dtype is None else out_dtype
+    if y is None:
+        y = torch.empty_like(x, dtype=out_dt)
+    _req(y, "y", out_dt)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((batch, nheads, headdim, dstate), dtype=torch.float32,
+                                  device=x.device)
+    _opt(final_state, "final_state", torch.float32)
+    st = lib().ssd_chunked_fwd(_ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C), int(chunk),
+                               _ptr(y), _ptr(final_state), batch, seqlen, nheads, headdim, dstate,
+                               ngroups, _DT[in_dt], _DT[out_dt], _stream(stream))
+    _check(st, "ssd_chunked_fwd")
+    return y, final_state
+
+
+def ssm_decode_step(state, x, dt, A, B, C, D=None, z=None, y=None, stream=None):
+    """One decode step; ``state`` (batch, nheads, headdim, dstate) fp32 is updated in place.
+    x, z: (batch, nheads, headdim); dt: (batch, nheads) fp32; A, D: (nheads,) fp32;
+    B, C: (batch, ngroups, dstate).  Returns y (batch, nheads, headdim)."""
+    _req(state, "state", torch.float32, 4)
+    batch, nheads, headdim, dstate = state.shape
+    _req(x, "x", ndim=3)
+    dt_ = x.dtype
+    if dt_ not in _DT:
+        raise TypeError("x must be float32 or bfloat16")
+    _req(dt, "dt", torch.float32, 2)
+    _req(A, "A", torch.float32, 1)
+    _req(B, "B", dt_, 3)
+    _req(C, "C", dt_, 3)
+    ngroups = B.shape[1]
+    _opt(D, "D", torch.float32)
+    _opt(z, "z", dt_)
+    if y is None:
+        y = torch.empty_like(x)
+    _req(y, "y", dt_)
+    st = lib().ssm_decode_step(_ptr(state), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
+                               _ptr(D), _ptr(z), _ptr(y), batch, nheads, headdim, dstate,
+                               ngroups, _DT[dt_], _stream(stream))
+    _check(st, "ssm_decode_step")
+    return y
+
+
+def ssm_last_device_status(workspace, stream=None) -> int:
+    """Device-side status recorded in a scan workspace (waits for the stream)."""
+    return int(lib().ssm_last_device_status(_ptr(workspace), _stream(stream)))

@@ -1,0 +1,683 @@
+// scan.cu -- selective scan forward (ssm_scan_fwd) for GB300 / sm_103a.
+//
+// What it computes: "We brought Mamba to Trainium -- and mapped where custom
+// kernels actually help", section "Mamba: bringing an unsupported model to the
+// chip, and writing its missing kernel" (h_t = A_t h_{t-1} + B_t x_t,
+// y_t = sum_n C_t h_t, state kept on chip for the whole sequence), with the
+// discretisation and epilogue of "Mamba-3 NKI Kernels for AWS Neuron",
+// section "How it works" (Phase 0: dt = softplus(dt + dt_bias),
+// alpha = exp(dt A); Phase 5: D skip, then silu gate).
+//
+// How (work-efficient: every (b, l, d, n) element costs one exp and four
+// fp32 operations, nothing is recomputed):
+//  * A CTA owns one (batch, group, block of CH channels) and one L-chunk.
+//    Four lanes share a channel; each holds 4 of the 16 states in registers
+//    and walks the chunk's time steps in order.
+//  * A producer warp streams 64-step tiles of u, delta, z, B and C into a
+//    ring of shared-memory stages with 2-D TMA (128-byte swizzle), tracked
+//    by mbarriers.  The compute warps first "prep" each tile once per
+//    (channel, step) -- dl = softplus(delta + bias) and dl*u -- and convert
+//    B/C to fp32 [t][n], then run the recurrence from shared memory.
+//  * y partial sums over the 4 lanes' states are reduce-scattered with warp
+//    shuffles; each lane then finishes 2 of every 8 steps (D skip, silu gate)
+//    and stores them.
+//  * Consecutive L-chunks of one channel block are chained across CTAs: CTA
+//    order is a ticket taken at start (chunk-major), and a CTA reads its
+//    carried-in state from the predecessor chunk's published inclusive state
+//    (bounded wait, acquire/release flags).  A predecessor always holds an
+//    earlier ticket, so it is running or finished: the wait always ends.
+//    The associativity of the recurrence ("We built the parallel scan"
+//    section of the first page) is what makes the chunk split exact.
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace {
+
+using namespace ssm;
+
+constexpr int kN = 16;          // dstate
+constexpr int kSPT = 4;         // states per thread
+constexpr int kNG = kN / kSPT;  // threads per channel
+constexpr int kTL = 64;         // time steps per tile
+constexpr int kMaxChunks = 32;  // upper bound on L-chunks per channel block
+constexpr int kPrepStride = kTL * 8 + 16;  // bytes per channel row of the prep tile
+
+struct alignas(16) WsHeader {
+    uint32_t ticket;
+    uint32_t status;
+    uint32_t pad[62];
+};
+static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
+
+struct ScanArgs {
+    const void* u;
+    const void* delta;
+    const void* z;
+    const float* A;
+    const float* Dskip;
+    const float* bias;
+    const float* h0;
+    void* y;
+    float* final_state;
+    uint32_t* ticket;
+    uint32_t* status;
+    uint32_t* flags;  // [nchunks - 1][nblocks]
+    float* carry;     // [nchunks - 1][batch * dim][kN]
+    const void* Bm;
+    const void* Cm;
+    int batch, dim, seqlen, ngroups;
+    int dpg;          // channels per group
+    int bpg;          // channel blocks per group
+    int nblocks;      // batch * ngroups * bpg
+    int nchunks;
+    int chunk_tiles;  // tiles per chunk
+    int softplus;
+};
+
+// Byte offset of (row r, step t) in a tile of ROWS rows x kTL steps laid out
+// as the 128-byte-swizzled TMA boxes: boxes of 128 bytes per row along time,
+// the 16-byte chunk index XORed with (row mod 8).
+template <typename T, int ROWS>
+__device__ __forceinline__ int tile_off(int r, int t) {
+    constexpr int E = sizeof(T);
+    constexpr int TPB = 128 / E;
+    const int box = t / TPB;
+    const int byte = (t % TPB) * E;
+    return box * (ROWS * 128) + r * 128 + ((((byte >> 4) ^ (r & 7)) << 4) | (byte & 15));
+}
+
+// 8 consecutive steps t0..t0+7 (t0 % 8 == 0) of row r, as fp32.
+template <typename T, int ROWS>
+__device__ __forceinline__ void load8(const uint8_t* tile, int r, int t0, float* v) {
+    if constexpr (sizeof(T) == 2) {
+        const uint4 w = *reinterpret_cast<const uint4*>(tile + tile_off<T, ROWS>(r, t0));
+        v[0] = bf16lo(w.x); v[1] = bf16hi(w.x); v[2] = bf16lo(w.y); v[3] = bf16hi(w.y);
+        v[4] = bf16lo(w.z); v[5] = bf16hi(w.z); v[6] = bf16lo(w.w); v[7] = bf16hi(w.w);
+    } else {
+        const float4 a = *reinterpret_cast<const float4*>(tile + tile_off<T, ROWS>(r, t0));
+        const float4 b = *reinterpret_cast<const float4*>(tile + tile_off<T, ROWS>(r, t0 + 4));
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+}
+
+// 2 consecutive steps t, t+1 (t even) of row r, as fp32.
+template <typename T, int ROWS>
+__device__ __forceinline__ void load2(const uint8_t* tile, int r, int t, float* v) {
+    if constexpr (sizeof(T) == 2) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(tile + tile_off<T, ROWS>(r, t));
+        v[0] = bf16lo(w); v[1] = bf16hi(w);
+    } else {
+        const float2 a = *reinterpret_cast<const float2*>(tile + tile_off<T, ROWS>(r, t));
+        v[0] = a.x; v[1] = a.y;
+    }
+}
+
+// Fallback staging when the rows are not 16-byte aligned for TMA: plain
+// loads with bounds checks into the same swizzled layout.
+template <typename T, int ROWS>
+__device__ __forceinline__ void stage_plain(uint8_t* tile, const T* src, long long row0,
+                                            long long rows_total, int L, int t0, int tid,
+                                            int nthreads) {
+    for (int i = tid; i < ROWS * kTL; i += nthreads) {
+        const int r = i / kTL, t = i % kTL;
+        const long long row = row0 + r;
+        const int tg = t0 + t;
+        T v = from_f32<T>(0.0f);
+        if (row < rows_total && tg < L) v = src[row * (long long)L + tg];
+        *reinterpret_cast<T*>(tile + tile_off<T, ROWS>(r, t)) = v;
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void store_y2(T* p, float a, float b, bool ok0, bool ok1, bool vec) {
+    if (vec && ok1) {
+        if constexpr (sizeof(T) == 4) {
+            *reinterpret_cast<float2*>(p) = make_float2(a, b);
+        } else {
+            __nv_bfloat162 v;
+            v.x = __float2bfloat16_rn(a);
+            v.y = __float2bfloat16_rn(b);
+            *reinterpret_cast<__nv_bfloat162*>(p) = v;
+        }
+    } else {
+        if (ok0) p[0] = from_f32<T>(a);
+        if (ok1) p[1] = from_f32<T>(b);
+    }
+}
+
+template <typename Tin>
+struct Geom {
+    static constexpr int E = sizeof(Tin);
+    static constexpr int TPB = 128 / E;       // steps per 128-byte box row
+    static constexpr int NBOX = kTL / TPB;    // boxes per tile along time
+    static constexpr int kStages = E == 2 ? 3 : 2;
+};
+
+template <typename Tin, int CH, bool TMA>
+struct Smem {
+    static constexpr int E = sizeof(Tin);
+    static constexpr int IN_TILE = CH * kTL * E;
+    static constexpr int BC_TILE = kN * kTL * E;
+    static constexpr int STAGE = 3 * IN_TILE + 2 * BC_TILE;
+    static constexpr int NSTAGE = TMA ? Geom<Tin>::kStages : 1;
+    static constexpr int PREP = CH * kPrepStride;
+    static constexpr int BCF = 2 * kTL * kN * 4;
+    static constexpr int BARS = 2 * NSTAGE * 8 + 16;
+    static constexpr int BYTES = NSTAGE * STAGE + PREP + BCF + BARS;
+    static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024
+};
+
+template <typename Tin, typename Tout, int CH, bool TMA>
+__global__ void __launch_bounds__(CH * kNG + 32)
+    scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u,
+                    const __grid_constant__ CUtensorMap tm_d,
+                    const __grid_constant__ CUtensorMap tm_z,
+                    const __grid_constant__ CUtensorMap tm_B,
+                    const __grid_constant__ CUtensorMap tm_C, const ScanArgs a) {
+    using S = Smem<Tin, CH, TMA>;
+    using G = Geom<Tin>;
+    constexpr int NCOMP = CH * kNG;
+    constexpr int NSTAGE = S::NSTAGE;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    uint8_t* stages = smem;
+    uint8_t* prep = stages + NSTAGE * S::STAGE;
+    float* bcf = reinterpret_cast<float*>(prep + S::PREP);  // [2][kTL][kN]
+    uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(bcf) + S::BCF);
+    uint64_t* empty = full + NSTAGE;
+    int* s_ticket = reinterpret_cast<int*>(empty + NSTAGE);
+
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        *s_ticket = static_cast<int>(atomicAdd(a.ticket, 1u));
+        if constexpr (TMA) {
+            for (int s = 0; s < NSTAGE; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], NCOMP / 32);
+            }
+            fence_mbar_init();
+        }
+    }
+    __syncthreads();
+
+    const int ticket = *s_ticket;
+    const int chunk = ticket / a.nblocks;
+    const int blk = ticket % a.nblocks;
+    const int cb = blk % a.bpg;
+    const int bg = blk / a.bpg;  // b * ngroups + g
+    const int g = bg % a.ngroups;
+    const int b = bg / a.ngroups;
+    const int d0 = g * a.dpg + cb * CH;
+    const long long row0 = static_cast<long long>(b) * a.dim + d0;
+    const long long bcrow0 = static_cast<long long>(bg) * kN;
+    const int t_begin = chunk * a.chunk_tiles * kTL;
+    const int t_end = min(a.seqlen, t_begin + a.chunk_tiles * kTL);
+    const int ntiles = (t_end - t_begin + kTL - 1) / kTL;
+    const bool has_z = a.z != nullptr;
+
+    // ------------------------------------------------------------ producer
+    if (tid >= NCOMP) {
+        if constexpr (TMA) {
+            if (tid == NCOMP) {
+                prefetch_tensormap(&tm_u);
+                prefetch_tensormap(&tm_d);
+                if (has_z) prefetch_tensormap(&tm_z);
+                prefetch_tensormap(&tm_B);
+                prefetch_tensormap(&tm_C);
+                const uint32_t bytes = (has_z ? 3 : 2) * S::IN_TILE + 2 * S::BC_TILE;
+                int issued = 0;
+                for (int k = 0; k < ntiles; ++k) {
+                    const int s = k % NSTAGE;
+                    if (k >= NSTAGE && !mbar_wait(&empty[s], ((k / NSTAGE) & 1) ^ 1, a.status))
+                        break;
+                    mbar_arrive_expect_tx(&full[s], bytes);
+                    uint8_t* st = stages + s * S::STAGE;
+                    const int t0 = t_begin + k * kTL;
+#pragma unroll
+                    for (int bx = 0; bx < G::NBOX; ++bx) {
+                        const int tc = t0 + bx * G::TPB;
+                        tma_load_2d(st + bx * CH * 128, &tm_u, &full[s], tc, (int)row0);
+                        tma_load_2d(st + S::IN_TILE + bx * CH * 128, &tm_d, &full[s], tc,
+                                    (int)row0);
+                        if (has_z)
+                            tma_load_2d(st + 2 * S::IN_TILE + bx * CH * 128, &tm_z, &full[s], tc,
+                                        (int)row0);
+                        tma_load_2d(st + 3 * S::IN_TILE + bx * kN * 128, &tm_B, &full[s], tc,
+                                    (int)bcrow0);
+                        tma_load_2d(st + 3 * S::IN_TILE + S::BC_TILE + bx * kN * 128, &tm_C,
+                                    &full[s], tc, (int)bcrow0);
+                    }
+                    issued = k + 1;
+                }
+                // Never leave the CTA with copies still landing in its shared
+                // memory: wait (bounded) for the last stages issued.
+                for (int k = max(0, issued - NSTAGE); k < issued; ++k)
+                    mbar_wait(&full[k % NSTAGE], (k / NSTAGE) & 1, a.status);
+            }
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------- compute
+    const int warp = tid >> 5, lane = tid & 31;
+    const int cl = warp * 8 + (lane >> 2);  // channel within the block
+    const int ng = lane & 3;                // which 4 of the 16 states
+    const int n0 = ng * kSPT;
+    const int d = d0 + cl;
+    const bool valid = (cb * CH + cl) < a.dpg;
+    const long long drow = static_cast<long long>(b) * a.dim + d;
+
+    float A2[kSPT], h[kSPT];
+#pragma unroll
+    for (int k = 0; k < kSPT; ++k) {
+        A2[k] = valid ? a.A[static_cast<long long>(d) * kN + n0 + k] * kLog2e : 0.0f;
+        h[k] = 0.0f;
+    }
+    const float Dd = (a.Dskip && valid) ? a.Dskip[d] : 0.0f;
+
+    // prep mapping: one channel, 16 consecutive steps per thread
+    const int pc = tid % CH;
+    const int pq = tid / CH;
+    const bool pvalid = (cb * CH + pc) < a.dpg;
+    const float pbias = (a.bias && pvalid) ? a.bias[d0 + pc] : 0.0f;
+
+    const float* prow = reinterpret_cast<const float*>(prep + cl * kPrepStride);
+    const float* Bt = bcf;
+    const float* Ct = bcf + kTL * kN;
+    Tout* yrow = reinterpret_cast<Tout*>(a.y) + drow * a.seqlen;
+    // vector stores need the row start aligned to 2 elements; TMA implies it
+    const bool vec_store = TMA;
+
+    bool ok = true;
+    for (int k = 0; k < ntiles; ++k) {
+        const int s = k % NSTAGE;
+        uint8_t* st = stages + s * S::STAGE;
+        const int t0 = t_begin + k * kTL;
+
+        if constexpr (TMA) {
+            const bool got = mbar_wait(&full[s], (k / NSTAGE) & 1, a.status);
+            if (!named_bar_and(1, NCOMP, got)) { ok = false; break; }
+        } else {
+            stage_plain<Tin, CH>(st, reinterpret_cast<const Tin*>(a.u), row0,
+                                 (long long)a.batch * a.dim, a.seqlen, t0, tid, NCOMP);
+            stage_plain<Tin, CH>(st + S::IN_TILE, reinterpret_cast<const Tin*>(a.delta), row0,
+                                 (long long)a.batch * a.dim, a.seqlen, t0, tid, NCOMP);
+            if (has_z)
+                stage_plain<Tin, CH>(st + 2 * S::IN_TILE, reinterpret_cast<const Tin*>(a.z),
+                                     row0, (long long)a.batch * a.dim, a.seqlen, t0, tid, NCOMP);
+            stage_plain<Tin, kN>(st + 3 * S::IN_TILE, reinterpret_cast<const Tin*>(a.Bm),
+                                 bcrow0, (long long)a.batch * a.ngroups * kN, a.seqlen, t0, tid,
+                                 NCOMP);
+            stage_plain<Tin, kN>(st + 3 * S::IN_TILE + S::BC_TILE,
+                                 reinterpret_cast<const Tin*>(a.Cm), bcrow0,
+                                 (long long)a.batch * a.ngroups * kN, a.seqlen, t0, tid, NCOMP);
+            named_bar_sync(1, NCOMP);
+        }
+
+        // ---- prep: dl = softplus(delta + bias) (or delta + bias) and dl * u,
+        // once per (channel, step); steps past the chunk end get dl = 0, an
+        // exact identity step (exp(0) = 1, input term 0).
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int tl = pq * 16 + hh * 8;
+            float uv[8], dv[8];
+            load8<Tin, CH>(st, pc, tl, uv);
+            load8<Tin, CH>(st + S::IN_TILE, pc, tl, dv);
+            float o[16];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float x = dv[j] + pbias;
+                float dl = a.softplus ? softplus_f(x) : x;
+                if (t0 + tl + j >= t_end) dl = 0.0f;
+                o[2 * j] = dl;
+                o[2 * j + 1] = dl * uv[j];
+            }
+            float4* dst = reinterpret_cast<float4*>(prep + pc * kPrepStride + tl * 8);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        }
+        // ---- B, C: swizzled [n][t] in the input type -> fp32 [t][n]
+        for (int i = tid; i < 2 * kN * (kTL / 8); i += NCOMP) {
+            const int arr = i / (kN * kTL / 8);
+            const int rem = i % (kN * kTL / 8);
+            const int n = rem % kN, j = rem / kN;
+            float v[8];
+            load8<Tin, kN>(st + 3 * S::IN_TILE + arr * S::BC_TILE, n, j * 8, v);
+            float* dst = bcf + arr * kTL * kN;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) dst[(j * 8 + q) * kN + n] = v[q];
+        }
+        named_bar_sync(1, NCOMP);
+
+        // ---- carried-in state, once per CTA, after the first prep
+        if (k == 0) {
+            if (chunk == 0) {
+                if (a.h0 && valid) {
+                    const float4 v =
+                        *reinterpret_cast<const float4*>(a.h0 + drow * kN + n0);
+                    h[0] = v.x; h[1] = v.y; h[2] = v.z; h[3] = v.w;
+                }
+            } else {
+                const uint32_t* flag = a.flags + (size_t)(chunk - 1) * a.nblocks + blk;
+                if (tid == 0) {
+                    bool seen = false;
+                    uint32_t ns = 32;
+                    for (uint32_t it = 0; it < kFlagSpinLimit; ++it) {
+                        if (ld_acquire_gpu(flag)) { seen = true; break; }
+                        __nanosleep(ns);
+                        ns = ns < 256 ? ns * 2 : 256;
+                    }
+                    if (!seen) record_status(a.status, SSM_ERR_TIMEOUT);
+                }
+                named_bar_sync(1, NCOMP);
+                (void)ld_acquire_gpu(flag);  // order this thread's reads after the flag
+                if (valid) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(
+                        a.carry + ((size_t)(chunk - 1) * a.batch * a.dim + drow) * kN + n0));
+                    h[0] = v.x; h[1] = v.y; h[2] = v.z; h[3] = v.w;
+                }
+            }
+        }
+
+        // ---- the recurrence over the tile, 8 steps per group
+        const uint8_t* tz = st + 2 * S::IN_TILE;
+#pragma unroll 1
+        for (int j = 0; j < kTL / 8; ++j) {
+            float yp[8];
+#pragma unroll
+            for (int q = 0; q < 8; q += 2) {
+                const float4 pp = *reinterpret_cast<const float4*>(prow + (j * 8 + q) * 2);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int t = j * 8 + q + r;
+                    const float dl = r ? pp.z : pp.x;
+                    const float du = r ? pp.w : pp.y;
+                    const float4 bv = *reinterpret_cast<const float4*>(Bt + t * kN + n0);
+                    const float4 cv = *reinterpret_cast<const float4*>(Ct + t * kN + n0);
+                    h[0] = fmaf(ex2_approx(dl * A2[0]), h[0], du * bv.x);
+                    h[1] = fmaf(ex2_approx(dl * A2[1]), h[1], du * bv.y);
+                    h[2] = fmaf(ex2_approx(dl * A2[2]), h[2], du * bv.z);
+                    h[3] = fmaf(ex2_approx(dl * A2[3]), h[3], du * bv.w);
+                    float acc = cv.x * h[0];
+                    acc = fmaf(cv.y, h[1], acc);
+                    acc = fmaf(cv.z, h[2], acc);
+                    acc = fmaf(cv.w, h[3], acc);
+                    yp[q + r] = acc;
+                }
+            }
+            // reduce-scatter the 8 partial sums over the 4 lanes of the channel:
+            // afterwards lane ng holds the full sums of steps 2ng and 2ng+1.
+            const bool hi2 = ng & 2, hi1 = ng & 1;
+            float k4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float send = hi2 ? yp[i] : yp[i + 4];
+                const float keep = hi2 ? yp[i + 4] : yp[i];
+                k4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+            }
+            float f[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float send = hi1 ? k4[i] : k4[i + 2];
+                const float keep = hi1 ? k4[i + 2] : k4[i];
+                f[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+            }
+            const int tl = j * 8 + 2 * ng;
+            const int tg = t0 + tl;
+            float uu[2];
+            load2<Tin, CH>(st, cl, tl, uu);
+            float o0 = fmaf(Dd, uu[0], f[0]);
+            float o1 = fmaf(Dd, uu[1], f[1]);
+            if (has_z) {
+                float zz[2];
+                load2<Tin, CH>(tz, cl, tl, zz);
+                o0 *= silu_f(zz[0]);
+                o1 *= silu_f(zz[1]);
+            }
+            if (valid && tg < t_end) store_y2<Tout>(yrow + tg, o0, o1, true, tg + 1 < t_end, vec_store);
+        }
+
+        if constexpr (TMA) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        named_bar_sync(1, NCOMP);  // prep / bcf are rewritten by the next tile
+    }
+
+    // ---- outgoing state: final_state for the last chunk, else the carry
+    if (valid && ok) {
+        const float4 v = make_float4(h[0], h[1], h[2], h[3]);
+        if (chunk == a.nchunks - 1) {
+            if (a.final_state)
+                *reinterpret_cast<float4*>(a.final_state + drow * kN + n0) = v;
+        } else {
+            __stcg(reinterpret_cast<float4*>(
+                       a.carry + ((size_t)chunk * a.batch * a.dim + drow) * kN + n0),
+                   v);
+        }
+    }
+    if (chunk < a.nchunks - 1) {
+        __threadfence();
+        named_bar_sync(1, NCOMP);
+        if (tid == 0) st_release_gpu(a.flags + (size_t)chunk * a.nblocks + blk, 1u);
+    }
+}
+
+// ------------------------------------------------------------------ host
+
+struct Plan {
+    int CH;
+    int bpg, nblocks, nchunks, chunk_tiles;
+    bool tma;
+};
+
+struct DevInfo {
+    int sms = 0;
+};
+
+DevInfo dev_info() {
+    static std::mutex m;
+    static int cached_dev = -1;
+    static DevInfo info;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(m);
+    if (dev != cached_dev) {
+        cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (info.sms <= 0) info.sms = 1;
+        cached_dev = dev;
+    }
+    return info;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Workspace is sized for the largest plan any device could pick, so that
+// ssm_scan_workspace_bytes is a pure function of the problem.
+size_t workspace_bound(long long batch, long long dim, int seqlen, int ngroups) {
+    const long long dpg = dim / ngroups;
+    const long long max_blocks = batch * ngroups * ((dpg + 15) / 16);
+    const long long tiles = (seqlen + kTL - 1) / kTL;
+    const long long max_chunks = std::min<long long>(kMaxChunks, std::max<long long>(1, tiles));
+    size_t bytes = sizeof(WsHeader);
+    bytes += round256(sizeof(uint32_t) * (size_t)(max_chunks - 1) * (size_t)max_blocks);
+    bytes += (size_t)(max_chunks - 1) * (size_t)batch * (size_t)dim * kN * sizeof(float);
+    return round256(bytes);
+}
+
+template <typename Tin, typename Tout, int CH, bool TMA>
+int occupancy_blocks() {
+    using S = Smem<Tin, CH, TMA>;
+    static int cached = -1;
+    if (cached < 0) {
+        auto kern = scan_fwd_kernel<Tin, Tout, CH, TMA>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
+        int nb = 0;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, CH * kNG + 32, S::ALLOC);
+        cached = std::max(nb, 1);
+    }
+    return cached;
+}
+
+template <typename Tin, typename Tout, int CH, bool TMA>
+ssm_status_t launch(const ScanArgs& base, const Plan& p, const CUtensorMap* maps,
+                    cudaStream_t stream) {
+    using S = Smem<Tin, CH, TMA>;
+    auto kern = scan_fwd_kernel<Tin, Tout, CH, TMA>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC) !=
+        cudaSuccess)
+        return SSM_ERR_CUDA;
+    ScanArgs a = base;
+    a.bpg = p.bpg;
+    a.nblocks = p.nblocks;
+    a.nchunks = p.nchunks;
+    a.chunk_tiles = p.chunk_tiles;
+    const unsigned grid = (unsigned)p.nblocks * (unsigned)p.nchunks;
+    kern<<<grid, CH * kNG + 32, S::ALLOC, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
+                                                     a);
+    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+template <typename Tin, typename Tout, int CH, bool TMA>
+void plan_for(const ScanArgs& a, Plan& p) {
+    p.CH = CH;
+    p.tma = TMA;
+    p.bpg = (a.dpg + CH - 1) / CH;
+    p.nblocks = a.batch * a.ngroups * p.bpg;
+    const int tiles = (a.seqlen + kTL - 1) / kTL;
+    const long long slots = (long long)occupancy_blocks<Tin, Tout, CH, TMA>() * dev_info().sms;
+    int nchunks = 1;
+    if (p.nblocks >= slots) {
+        // Enough independent channel blocks to fill the GPU: cut L into
+        // chained chunks so that about 8 waves of CTAs balance the SMs.
+        const long long want = (8 * slots + p.nblocks - 1) / p.nblocks;
+        nchunks = (int)std::min<long long>(std::min<long long>(want, kMaxChunks), tiles);
+        nchunks = std::max(nchunks, 1);
+    }
+    p.chunk_tiles = (tiles + nchunks - 1) / nchunks;
+    p.nchunks = (tiles + p.chunk_tiles - 1) / p.chunk_tiles;
+}
+
+template <typename Tin, typename Tout>
+ssm_status_t dispatch(ScanArgs& a, ssm_dtype_t in_dtype, bool tma, cudaStream_t stream,
+                      void* workspace) {
+    Plan p{};
+    if (tma) plan_for<Tin, Tout, 32, true>(a, p);
+    else plan_for<Tin, Tout, 32, false>(a, p);
+
+    // workspace: header | flags | carry
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+    a.ticket = &hdr->ticket;
+    a.status = &hdr->status;
+    a.flags = reinterpret_cast<uint32_t*>(ws + sizeof(WsHeader));
+    const size_t flag_bytes = round256(sizeof(uint32_t) * (size_t)(p.nchunks - 1) * p.nblocks);
+    a.carry = reinterpret_cast<float*>(ws + sizeof(WsHeader) + flag_bytes);
+    if (cudaMemsetAsync(ws, 0, sizeof(WsHeader) + flag_bytes, stream) != cudaSuccess)
+        return SSM_ERR_CUDA;
+
+    CUtensorMap maps[5];
+    memset(maps, 0, sizeof(maps));
+    if (tma) {
+        const uint64_t rows = (uint64_t)a.batch * a.dim;
+        const uint64_t bcrows = (uint64_t)a.batch * a.ngroups * kN;
+        const uint32_t tpb = Geom<Tin>::TPB;
+        bool okm = ssm_host::make_tmap_2d(&maps[0], a.u, in_dtype, rows, a.seqlen, 32, tpb) &&
+                   ssm_host::make_tmap_2d(&maps[1], a.delta, in_dtype, rows, a.seqlen, 32, tpb) &&
+                   ssm_host::make_tmap_2d(&maps[3], a.Bm, in_dtype, bcrows, a.seqlen, kN, tpb) &&
+                   ssm_host::make_tmap_2d(&maps[4], a.Cm, in_dtype, bcrows, a.seqlen, kN, tpb);
+        if (okm && a.z)
+            okm = ssm_host::make_tmap_2d(&maps[2], a.z, in_dtype, rows, a.seqlen, 32, tpb);
+        if (!okm) return SSM_ERR_CUDA;
+        return launch<Tin, Tout, 32, true>(a, p, maps, stream);
+    }
+    return launch<Tin, Tout, 32, false>(a, p, maps, stream);
+}
+
+}  // namespace
+
+extern "C" size_t ssm_scan_workspace_bytes(int batch, int dim, int seqlen, int dstate,
+                                           int ngroups) {
+    if (batch < 0 || dim < 0 || seqlen < 0 || dstate != kN || ngroups < 1 || dim % ngroups)
+        return 0;
+    return workspace_bound(batch, dim, seqlen, ngroups);
+}
+
+extern "C" ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const float* A,
+                                     const void* B, const void* C, const float* D, const void* z,
+                                     const float* delta_bias, int delta_softplus,
+                                     const float* initial_state, void* y, float* final_state,
+                                     int batch, int dim, int seqlen, int dstate, int ngroups,
+                                     ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+    using namespace ssm_host;
+    if (batch < 0 || dim < 0 || seqlen < 0 || ngroups < 1 || dstate < 1) return SSM_ERR_SHAPE;
+    if (dim % ngroups != 0) return SSM_ERR_SHAPE;
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return SSM_ERR_DTYPE;
+    if (dstate != kN) return SSM_ERR_UNSUPPORTED;
+    const size_t rows = (size_t)batch * dim;
+    if (rows == 0) return SSM_OK;
+    // TMA coordinates and CTA counts are 32-bit
+    if (rows > (size_t)INT32_MAX || (size_t)batch * ngroups * kN > (size_t)INT32_MAX)
+        return SSM_ERR_UNSUPPORTED;
+    if (seqlen > 0 && (!u || !delta || !B || !C || !y || !A)) return SSM_ERR_NULL;
+    if (seqlen > 0 && !workspace) return SSM_ERR_WORKSPACE;
+    const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, initial_state, y, final_state,
+                          workspace};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return SSM_ERR_ALIGN;
+
+    const size_t es = dtype_size(in_dtype), eo = dtype_size(out_dtype);
+    const size_t act = rows * (size_t)seqlen * es;
+    const size_t bc = (size_t)batch * ngroups * kN * (size_t)seqlen * es;
+    struct R { const void* p; size_t n; } ins[] = {
+        {u, act}, {delta, act}, {z, z ? act : 0}, {B, bc}, {C, bc}, {A, (size_t)dim * kN * 4},
+        {D, D ? (size_t)dim * 4 : 0}, {delta_bias, delta_bias ? (size_t)dim * 4 : 0},
+        {initial_state, initial_state ? rows * kN * 4 : 0}};
+    const size_t ybytes = rows * (size_t)seqlen * eo;
+    const size_t fbytes = final_state ? rows * kN * 4 : 0;
+    for (const R& r : ins) {
+        if (overlaps(y, ybytes, r.p, r.n)) return SSM_ERR_ALIAS;
+        if (overlaps(final_state, fbytes, r.p, r.n)) return SSM_ERR_ALIAS;
+    }
+    if (overlaps(y, ybytes, final_state, fbytes)) return SSM_ERR_ALIAS;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (seqlen == 0) {
+        if (final_state) {
+            cudaError_t e = initial_state
+                                ? cudaMemcpyAsync(final_state, initial_state, rows * kN * 4,
+                                                  cudaMemcpyDeviceToDevice, s)
+                                : cudaMemsetAsync(final_state, 0, rows * kN * 4, s);
+            if (e != cudaSuccess) return SSM_ERR_CUDA;
+        }
+        return SSM_OK;
+    }
+    const size_t need = workspace_bound(batch, dim, seqlen, ngroups);
+    if (workspace_bytes < need) return SSM_ERR_WORKSPACE;
+    if (overlaps(workspace, need, y, ybytes) || overlaps(workspace, need, final_state, fbytes))
+        return SSM_ERR_ALIAS;
+    for (const R& r : ins)
+        if (overlaps(workspace, need, r.p, r.n)) return SSM_ERR_ALIAS;
+
+    ScanArgs a{};
+    a.u = u; a.delta = delta; a.z = z; a.A = A; a.Dskip = D; a.bias = delta_bias;
+    a.h0 = initial_state; a.y = y; a.final_state = final_state; a.Bm = B; a.Cm = C;
+    a.batch = batch; a.dim = dim; a.seqlen = seqlen; a.ngroups = ngroups;
+    a.dpg = dim / ngroups; a.softplus = delta_softplus ? 1 : 0;
+
+    // TMA needs 16-byte row strides (base alignment is already checked).
+    const bool tma = ((size_t)seqlen * es) % 16 == 0;
+    if (in_dtype == SSM_BF16) {
+        return out_dtype == SSM_BF16
+                   ? dispatch<__nv_bfloat16, __nv_bfloat16>(a, in_dtype, tma, s, workspace)
+                   : dispatch<__nv_bfloat16, float>(a, in_dtype, tma, s, workspace);
+    }
+    return out_dtype == SSM_BF16 ? dispatch<float, __nv_bfloat16>(a, in_dtype, tma, s, workspace)
+                                 : dispatch<float, float>(a, in_dtype, tma, s, workspace);
+}

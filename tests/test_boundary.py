@@ -1,0 +1,155 @@
+"""The C ABI loads without a GPU, exports every symbol the header declares,
+and rejects bad arguments on the host before anything is launched.
+
+No call here reaches the GPU: every call carries an argument error that the
+host-side checks catch first, and the pointers are fake addresses that are
+never dereferenced.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from state_space_model_selective_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssm.h")
+
+OK, NULL, SHAPE, ALIGN, DTYPE, UNSUP, WS, TIMEOUT, CUDA, ALIAS = range(10)
+
+
+@pytest.fixture(scope="module")
+def L():
+    return binding.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)
+    return sorted({n for n in names if n.startswith(("ssm_", "ssd_"))})
+
+
+def test_header_symbols_exported(L):
+    declared = _declared_functions()
+    assert set(declared) == set(binding.EXPORTS), declared
+    for name in declared:
+        assert hasattr(L, name), f"libssm.so does not export {name}"
+
+
+def test_version_and_status_strings(L):
+    assert binding.ssm_abi_version() == 1
+    for code in range(10):
+        s = binding.status_string(code)
+        assert isinstance(s, str) and s
+    assert binding.status_string(123) == "unknown status"
+
+
+def test_workspace_bytes_pure_function():
+    f = binding.ssm_scan_workspace_bytes
+    assert f(8, 1536, 2048) == f(8, 1536, 2048) > 0
+    assert f(1, 1536, 128) >= 256
+    assert f(1, 10, 5, dstate=8) == 0            # unsupported dstate
+    assert f(1, 10, 5, ngroups=3) == 0           # dim % ngroups != 0
+    assert f(-1, 10, 5) == 0
+    # grows with the problem
+    assert f(4, 5120, 16384) > f(8, 1536, 2048)
+
+
+# fake, 16-byte aligned device addresses, far apart (never dereferenced)
+def P(i):
+    return ctypes.c_void_p(0x10000000 * (i + 1))
+
+
+def scan_call(L, **kw):
+    args = dict(u=P(0), delta=P(1), A=P(2), B=P(3), C=P(4), D=None, z=None, bias=None,
+                softplus=1, h0=None, y=P(5), fs=P(6), batch=2, dim=32, seqlen=64, dstate=16,
+                ngroups=1, in_dt=1, out_dt=0, ws=P(7), wsb=1 << 30, stream=None)
+    args.update(kw)
+    return L.ssm_scan_fwd(args["u"], args["delta"], args["A"], args["B"], args["C"], args["D"],
+                          args["z"], args["bias"], args["softplus"], args["h0"], args["y"],
+                          args["fs"], args["batch"], args["dim"], args["seqlen"], args["dstate"],
+                          args["ngroups"], args["in_dt"], args["out_dt"], args["ws"], args["wsb"],
+                          args["stream"])
+
+
+def test_scan_argument_errors(L):
+    assert scan_call(L, u=None) == NULL
+    assert scan_call(L, y=None) == NULL
+    assert scan_call(L, A=None) == NULL
+    assert scan_call(L, batch=-1) == SHAPE
+    assert scan_call(L, seqlen=-5) == SHAPE
+    assert scan_call(L, ngroups=3) == SHAPE          # 32 % 3 != 0
+    assert scan_call(L, ngroups=0) == SHAPE
+    assert scan_call(L, dstate=8) == UNSUP
+    assert scan_call(L, dstate=0) == SHAPE
+    assert scan_call(L, in_dt=7) == DTYPE
+    assert scan_call(L, out_dt=-1) == DTYPE
+    assert scan_call(L, u=ctypes.c_void_p(0x10000008)) == ALIGN
+    assert scan_call(L, fs=ctypes.c_void_p(0x70000004)) == ALIGN
+    assert scan_call(L, ws=None) == WS
+    assert scan_call(L, wsb=16) == WS
+    assert scan_call(L, y=P(0)) == ALIAS             # y on top of u
+    assert scan_call(L, fs=P(2)) == ALIAS            # final_state on top of A
+    assert scan_call(L, ws=P(1)) == ALIAS            # workspace on top of delta
+    # empty problems are valid and launch nothing
+    assert scan_call(L, batch=0, u=None, y=None) == OK
+    assert scan_call(L, dim=0, u=None, y=None) == OK
+
+
+def ssd_call(L, **kw):
+    args = dict(x=P(0), dt=P(1), A=P(2), B=P(3), C=P(4), chunk=64, y=P(5), fs=P(6), batch=2,
+                seqlen=128, nheads=4, headdim=64, dstate=128, ngroups=1, in_dt=1, out_dt=0,
+                stream=None)
+    args.update(kw)
+    return L.ssd_chunked_fwd(args["x"], args["dt"], args["A"], args["B"], args["C"],
+                             args["chunk"], args["y"], args["fs"], args["batch"], args["seqlen"],
+                             args["nheads"], args["headdim"], args["dstate"], args["ngroups"],
+                             args["in_dt"], args["out_dt"], args["stream"])
+
+
+def test_ssd_argument_errors(L):
+    assert ssd_call(L, seqlen=100) == SHAPE           # seqlen % chunk != 0
+    assert ssd_call(L, nheads=6, ngroups=4) == SHAPE
+    assert ssd_call(L, chunk=0) == SHAPE
+    assert ssd_call(L, batch=-1) == SHAPE
+    assert ssd_call(L, in_dt=9) == DTYPE
+    assert ssd_call(L, chunk=32) == UNSUP
+    assert ssd_call(L, headdim=32) == UNSUP
+    assert ssd_call(L, dstate=64) == UNSUP
+    assert ssd_call(L, in_dt=0) == UNSUP
+    assert ssd_call(L, x=None) == NULL
+    assert ssd_call(L, y=P(3)) == ALIAS
+    assert ssd_call(L, x=ctypes.c_void_p(0x10000002)) == ALIGN
+    assert ssd_call(L, batch=0, x=None, y=None) == OK
+
+
+def decode_call(L, **kw):
+    args = dict(state=P(0), x=P(1), dt=P(2), A=P(3), B=P(4), C=P(5), D=None, z=None, y=P(6),
+                batch=4, nheads=8, headdim=64, dstate=128, ngroups=1, dtype=0, stream=None)
+    args.update(kw)
+    return L.ssm_decode_step(args["state"], args["x"], args["dt"], args["A"], args["B"],
+                             args["C"], args["D"], args["z"], args["y"], args["batch"],
+                             args["nheads"], args["headdim"], args["dstate"], args["ngroups"],
+                             args["dtype"], args["stream"])
+
+
+def test_decode_argument_errors(L):
+    assert decode_call(L, state=None) == NULL
+    assert decode_call(L, y=None) == NULL
+    assert decode_call(L, nheads=6, ngroups=4) == SHAPE
+    assert decode_call(L, dstate=48) == UNSUP
+    assert decode_call(L, dtype=3) == DTYPE
+    assert decode_call(L, x=ctypes.c_void_p(0x20000004)) == ALIGN
+    assert decode_call(L, y=P(1)) == ALIAS
+    assert decode_call(L, state=P(4)) == ALIAS
+    assert decode_call(L, batch=0, state=None) == OK
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    u = torch.zeros(1, 4, 8)
+    with pytest.raises(TypeError):
+        binding.ssm_scan_fwd(u, u, torch.zeros(4, 16), torch.zeros(1, 1, 16, 8),
+                             torch.zeros(1, 1, 16, 8))

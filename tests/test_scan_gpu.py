@@ -1,0 +1,165 @@
+"""Parity of the CUDA selective scan (through the C ABI) with the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from state_space_model_selective_gb300 import binding, inputs
+from tests.helpers import TOL_BF16, TOL_F32, assert_close, to64
+
+pytestmark = pytest.mark.gpu
+
+
+def _to_dev(d):
+    return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+
+def _run(inp, out_dtype=torch.float32, initial_state=None, poison=True):
+    x = _to_dev(inp)
+    batch, dim, seqlen = x["u"].shape
+    y = torch.empty((batch, dim, seqlen), dtype=out_dtype, device="cuda")
+    fs = torch.empty((batch, dim, 16), dtype=torch.float32, device="cuda")
+    if poison:  # catch elements the kernel never writes
+        y.fill_(float("nan"))
+        fs.fill_(float("nan"))
+    need = binding.ssm_scan_workspace_bytes(batch, dim, seqlen, 16, x["B"].shape[1])
+    ws = torch.full((need,), 0xAB, dtype=torch.uint8, device="cuda")
+    binding.ssm_scan_fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"],
+                         x["delta_bias"], x["delta_softplus"],
+                         None if initial_state is None else initial_state.cuda(),
+                         out_dtype=out_dtype, y=y, final_state=fs, workspace=ws)
+    torch.cuda.synchronize()
+    assert binding.ssm_last_device_status(ws) == 0
+    return y, fs
+
+
+def _oracle(inp, initial_state=None):
+    return oracle.scan(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                       inp["delta_bias"], inp["delta_softplus"], initial_state)
+
+
+CASES = [
+    # batch, dim, seqlen, ngroups, dtype, gate, dskip, softplus
+    (1, 32, 64, 1, "f32", True, "ones", True),       # one tile, one block
+    (2, 64, 200, 1, "f32", True, "randn", True),     # ragged tail (200 % 64), TMA rows
+    (2, 48, 333, 1, "f32", False, "none", False),    # odd L: plain-load path; partial block
+    (3, 96, 256, 2, "bf16", True, "ones", True),     # groups
+    (2, 40, 130, 4, "bf16", True, "randn", True),    # 10 channels per group: partial blocks
+    (1, 32, 1000, 1, "bf16", False, "ones", True),   # bf16 rows 16B-aligned, ragged tail
+    (2, 32, 77, 1, "bf16", True, "ones", False),     # odd L with bf16: plain-load path
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"B{c[0]}D{c[1]}L{c[2]}G{c[3]}{c[4]}" for c in CASES])
+def test_scan_matches_oracle(case):
+    batch, dim, seqlen, ngroups, dt, gate, dskip, softplus = case
+    inp = inputs.scan_inputs(batch, dim, seqlen, 16, ngroups, dt, seed=100 + seqlen, gate=gate,
+                             dskip=dskip)
+    inp["delta_softplus"] = softplus
+    if not softplus:  # keep dt positive and moderate without softplus
+        inp["delta"] = (inp["delta"].float().abs() * 0.1).to(inp["delta"].dtype)
+    y, fs = _run(inp)
+    y_ref, fs_ref = _oracle(inp)
+    tol = TOL_F32 if dt == "f32" else TOL_BF16
+    assert_close(y, y_ref, tol, "y")
+    assert_close(fs, fs_ref, tol, "final_state")
+
+
+def test_scan_initial_state_and_resume():
+    """Scanning [0, k) then [k, L) from the first part's final state equals one scan."""
+    inp = inputs.scan_inputs(2, 64, 384, 16, 1, "f32", seed=5)
+    h0 = torch.randn(2, 64, 16, generator=torch.Generator().manual_seed(1)) * 0.5
+    y, fs = _run(inp, initial_state=h0)
+    y_ref, fs_ref = _oracle(inp, h0)
+    assert_close(y, y_ref, TOL_F32, "y with initial state")
+    assert_close(fs, fs_ref, TOL_F32, "final_state with initial state")
+    k = 192
+    first = {kk: (v[..., :k].contiguous() if kk in ("u", "delta", "z", "B", "C") else v)
+             for kk, v in inp.items()}
+    second = {kk: (v[..., k:].contiguous() if kk in ("u", "delta", "z", "B", "C") else v)
+              for kk, v in inp.items()}
+    y1, f1 = _run(first, initial_state=h0)
+    y2, f2 = _run(second, initial_state=f1.cpu())
+    assert_close(torch.cat([y1, y2], -1), y_ref, TOL_F32, "resumed y")
+    assert_close(f2, fs_ref, TOL_F32, "resumed final_state")
+
+
+def test_scan_bf16_output_is_rounded_fp32_output():
+    inp = inputs.scan_inputs(2, 64, 256, 16, 1, "bf16", seed=9)
+    y32, f32 = _run(inp, torch.float32)
+    y16, f16 = _run(inp, torch.bfloat16)
+    assert torch.equal(y16, y32.to(torch.bfloat16))
+    assert torch.equal(f16, f32)
+
+
+def test_scan_deterministic():
+    inp = inputs.scan_inputs(2, 64, 300, 16, 1, "bf16", seed=11)
+    a = _run(inp)
+    b = _run(inp)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_scan_empty_and_zero_length():
+    u = torch.zeros(2, 32, 0, device="cuda")
+    A = -torch.ones(32, 16, device="cuda")
+    B = torch.zeros(2, 1, 16, 0, device="cuda")
+    h0 = torch.randn(2, 32, 16, device="cuda")
+    y, fs = binding.ssm_scan_fwd(u, u, A, B, B, initial_state=h0)
+    torch.cuda.synchronize()
+    assert y.shape == (2, 32, 0) and torch.equal(fs, h0)
+    y, fs = binding.ssm_scan_fwd(u, u, A, B, B)
+    assert torch.count_nonzero(fs).item() == 0
+    u0 = torch.zeros(0, 32, 10, device="cuda")
+    B0 = torch.zeros(0, 1, 16, 10, device="cuda")
+    y, fs = binding.ssm_scan_fwd(u0, u0, A, B0, B0)
+    assert y.shape == (0, 32, 10)
+
+
+def test_scan_chained_chunks_many_blocks():
+    """Enough channel blocks that L is cut into chained chunks across CTAs."""
+    inp = inputs.scan_inputs(4, 4096, 512, 16, 1, "bf16", seed=21)
+    y, fs = _run(inp)
+    rows = [(0, 0), (1, 1234), (2, 4095), (3, 2048), (3, 7), (0, 4000)]
+    y_ref, fs_ref = oracle.scan_rows(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], rows,
+                                     inp["D"], inp["z"], inp["delta_bias"], True)
+    ys = torch.stack([y[b, d] for b, d in rows])
+    fss = torch.stack([fs[b, d] for b, d in rows])
+    assert_close(ys, y_ref, TOL_BF16, "y rows")
+    assert_close(fss, fs_ref, TOL_BF16, "final_state rows")
+
+
+# ------------------------------------------------------------------ workloads
+
+def test_workload_scan_fp32_L128_D1536():
+    """Selective scan fp32, batch 1, L 128, 1536 channels, N 16: every output."""
+    inp = inputs.scan_inputs(1, 1536, 128, 16, 1, "f32", seed=1001)
+    y, fs = _run(inp)
+    y_ref, fs_ref = _oracle(inp)
+    assert_close(y, y_ref, TOL_F32, "y")
+    assert_close(fs, fs_ref, TOL_F32, "final_state")
+
+
+def _sampled_rows(batch, dim, n, seed):
+    rng = np.random.default_rng(seed)
+    rows = {(0, 0), (batch - 1, dim - 1)}
+    while len(rows) < n:
+        rows.add((int(rng.integers(batch)), int(rng.integers(dim))))
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("shape,seed", [((8, 1536, 2048), 1002), ((4, 5120, 16384), 1003)],
+                         ids=["B8_D1536_L2048", "B4_D5120_L16384"])
+def test_workload_scan_bf16_sampled(shape, seed):
+    """Full-size bf16 workloads, launched as the benchmark launches them;
+    sampled (batch, channel) rows checked against the oracle."""
+    batch, dim, seqlen = shape
+    inp = inputs.scan_inputs(batch, dim, seqlen, 16, 1, "bf16", seed=seed)
+    y, fs = _run(inp, poison=False)
+    rows = _sampled_rows(batch, dim, 24, seed)
+    y_ref, fs_ref = oracle.scan_rows(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], rows,
+                                     inp["D"], inp["z"], inp["delta_bias"], True)
+    ys = torch.stack([y[b, d] for b, d in rows])
+    fss = torch.stack([fs[b, d] for b, d in rows])
+    assert_close(ys, y_ref, TOL_BF16, "y rows")
+    assert_close(fss, fs_ref, TOL_BF16, "final_state rows")
+    assert torch.isfinite(y).all() and torch.isfinite(fs).all()
