@@ -56,8 +56,9 @@ def test_scan_matches_oracle(case):
     inp = inputs.scan_inputs(batch, dim, seqlen, 16, ngroups, dt, seed=100 + seqlen, gate=gate,
                              dskip=dskip)
     inp["delta_softplus"] = softplus
-    if not softplus:  # keep dt positive and moderate without softplus
+    if not softplus:  # without softplus, delta + bias must stay positive (a decaying state)
         inp["delta"] = (inp["delta"].float().abs() * 0.1).to(inp["delta"].dtype)
+        inp["delta_bias"] = torch.full_like(inp["delta_bias"], 0.01)
     y, fs = _run(inp)
     y_ref, fs_ref = _oracle(inp)
     tol = TOL_F32 if dt == "f32" else TOL_BF16
