@@ -1,0 +1,64 @@
+"""Measure the per-clock throughput of the units the selective scan uses:
+MUFU ex2, fp32 FMA and packed fp32x2 FMA, on the current GPU.
+
+Prints one JSON line with results per second and per SM per clock (the SM
+clock is sampled with nvidia-smi during each probe).  These rates, times the
+SM count and the maximum SM clock, are the scan's arithmetic roofline.
+"""
+from __future__ import annotations
+
+import ctypes
+import json
+import os
+import subprocess
+
+import torch
+
+_LIB = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libssm_peaks.so")
+
+
+def _sm_clock_mhz():
+    try:
+        r = subprocess.run(["nvidia-smi", "--query-gpu=clocks.sm", "--format=csv,noheader,nounits",
+                            f"--id={torch.cuda.current_device()}"],
+                           capture_output=True, text=True, timeout=10)
+        return float(r.stdout.strip().splitlines()[0])
+    except Exception:
+        return None
+
+
+def measure(iters: int = 20000, reps: int = 3) -> dict:
+    lib = ctypes.CDLL(_LIB)
+    lib.ssm_peak_probe.restype = ctypes.c_double
+    lib.ssm_peak_probe.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p, ctypes.c_void_p]
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    sms = props.multi_processor_count
+    blocks, threads = sms * 8, 256
+    out = torch.empty(blocks * threads, device="cuda")
+    stream = torch.cuda.current_stream()
+    res = {"sms": sms, "gpu": props.name}
+    for kind, name in ((0, "mufu_ex2"), (1, "ffma"), (2, "ffma2_lanes")):
+        best = None
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            n = lib.ssm_peak_probe(kind, blocks, threads, iters, ctypes.c_void_p(out.data_ptr()),
+                                   ctypes.c_void_p(stream.cuda_stream))
+            e1.record(stream)
+            torch.cuda.synchronize()
+            mhz = _sm_clock_mhz()
+            ms = e0.elapsed_time(e1)
+            if n <= 0:
+                raise RuntimeError("probe launch failed")
+            rate = n / (ms / 1e3)
+            if best is None or rate > best[0]:
+                best = (rate, mhz)
+        rate, mhz = best
+        res[name] = {"per_s": rate, "sm_mhz": mhz,
+                     "per_sm_per_clk": rate / sms / (mhz * 1e6) if mhz else None}
+    return res
+
+
+if __name__ == "__main__":
+    torch.cuda.init()
+    print(json.dumps(measure()))
