@@ -156,6 +156,42 @@ ssm_status_t ssm_decode_step(float* state, const void* x, const float* dt,
                              ssm_dtype_t dtype, void* stream);
 
 /*
+ * Selective scan for callers that cannot allocate device memory.
+ *
+ * No counterpart on the pages: this is an interface addition of this
+ * library.  Some callers of this code cannot call cudaMalloc (or any
+ * allocator) when they run the scan: an inference-engine plug-in whose device
+ * memory is budgeted once at start-up, a real-time loop that may not take
+ * cudaMalloc's implicit device synchronisation or its unbounded latency, or a
+ * thin C wrapper that has no handle on the framework's caching allocator.
+ * For them this entry point computes exactly what ssm_scan_fwd computes, with
+ * the same arguments except that there is no workspace: its scratch lives in
+ * a fixed 4 MiB array inside the library's device image, which every GPU that
+ * loads the library holds until the process exits.  It allocates nothing.
+ *
+ *  - Limit: problems whose scratch (a 256-byte header, plus, when the scan
+ *    is split into chained L-chunks on this GPU, one flag per chunk and
+ *    channel block and 64 bytes of carried state per channel and chunk)
+ *    exceeds 4 MiB are rejected with SSM_ERR_WORKSPACE before anything is
+ *    enqueued; ssm_scan_fwd with a caller-supplied workspace handles them.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls on a device share the one array, which keeps the contents the
+ *    last call left; each call clears what must start at zero on its stream.
+ *    Calls whose executions overlap on the GPU (different streams, or
+ *    different host threads without ordering) race on the array and give
+ *    undefined results: serialise them.
+ *  - ssm_last_device_status does not apply (there is no workspace to read).
+ */
+ssm_status_t ssm_scan_fwd_noalloc(const void* u, const void* delta, const float* A,
+                                  const void* B, const void* C, const float* D, const void* z,
+                                  const float* delta_bias, int delta_softplus,
+                                  const float* initial_state, void* y, float* final_state,
+                                  int batch, int dim, int seqlen, int dstate, int ngroups,
+                                  ssm_dtype_t in_dtype, ssm_dtype_t out_dtype, void* stream);
+
+/*
  * Waits for `stream` to drain, then returns the device-side status the last
  * ssm_scan_fwd that used `workspace` recorded (SSM_OK or SSM_ERR_TIMEOUT),
  * or SSM_ERR_CUDA if the stream itself reports an error.

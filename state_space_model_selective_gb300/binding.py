@@ -27,7 +27,8 @@ STATUS_NAMES = {0: "SSM_OK", 1: "SSM_ERR_NULL", 2: "SSM_ERR_SHAPE", 3: "SSM_ERR_
 
 # every symbol include/ssm.h declares
 EXPORTS = ["ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_bytes", "ssm_scan_fwd",
-           "ssd_chunked_fwd", "ssm_decode_step", "ssm_last_device_status"]
+           "ssd_chunked_fwd", "ssm_decode_step", "ssm_last_device_status",
+           "ssm_scan_fwd_noalloc"]
 
 
 class SSMError(RuntimeError):
@@ -60,6 +61,8 @@ def lib() -> ctypes.CDLL:
         L.ssd_chunked_fwd.argtypes = [vp] * 5 + [i] + [vp] * 2 + [i] * 8 + [vp]
         L.ssm_decode_step.restype = i
         L.ssm_decode_step.argtypes = [vp] * 9 + [i] * 6 + [vp]
+        L.ssm_scan_fwd_noalloc.restype = i
+        L.ssm_scan_fwd_noalloc.argtypes = [vp] * 8 + [i] + [vp] * 3 + [i] * 7 + [vp]
         L.ssm_last_device_status.restype = i
         L.ssm_last_device_status.argtypes = [vp, vp]
         _lib = L
@@ -147,6 +150,38 @@ def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softp
                             _DT[in_dt], _DT[out_dt], _ptr(workspace), workspace.numel(),
                             _stream(stream))
     _check(st, "ssm_scan_fwd")
+    return y, final_state
+
+
+def ssm_scan_fwd_noalloc(u, delta, A, B, C, y, final_state=None, D=None, z=None,
+                         delta_bias=None, delta_softplus=False, initial_state=None, stream=None):
+    """The selective scan without a workspace, for callers that cannot
+    allocate: its scratch is a fixed array inside the library.  The caller
+    passes every input and output (y, and final_state or None); nothing is
+    allocated here or in the library.  Same layouts as ssm_scan_fwd."""
+    _req(u, "u", ndim=3)
+    in_dt = u.dtype
+    if in_dt not in _DT:
+        raise TypeError("u must be float32 or bfloat16")
+    batch, dim, seqlen = u.shape
+    _req(delta, "delta", in_dt)
+    _req(A, "A", torch.float32, 2)
+    _req(B, "B", in_dt, 4)
+    _req(C, "C", in_dt, 4)
+    _opt(D, "D", torch.float32)
+    _opt(z, "z", in_dt)
+    _opt(delta_bias, "delta_bias", torch.float32)
+    _opt(initial_state, "initial_state", torch.float32)
+    _req(y, "y")
+    if y.dtype not in _DT:
+        raise TypeError("y must be float32 or bfloat16")
+    _opt(final_state, "final_state", torch.float32)
+    st = lib().ssm_scan_fwd_noalloc(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                    _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)),
+                                    _ptr(initial_state), _ptr(y), _ptr(final_state), batch, dim,
+                                    seqlen, A.shape[1], B.shape[1], _DT[in_dt], _DT[y.dtype],
+                                    _stream(stream))
+    _check(st, "ssm_scan_fwd_noalloc")
     return y, final_state
 
 

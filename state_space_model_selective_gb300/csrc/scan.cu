@@ -681,3 +681,124 @@ extern "C" ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const flo
     return out_dtype == SSM_BF16 ? dispatch<float, __nv_bfloat16>(a, in_dtype, tma, s, workspace)
                                  : dispatch<float, float>(a, in_dtype, tma, s, workspace);
 }
+
+// ------------------------------------------------ allocation-free variant
+//
+// ssm_scan_fwd_noalloc: the same scan kernel, with its look-back scratch
+// (ticket, status word, per-chunk flags and carried states) taken from a
+// fixed array in the library's device image instead of a caller-supplied
+// workspace.  Every GPU that loads the library holds this array until the
+// process exits.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the symbol names a host-side shadow, not device memory, so the address is
+// looked up once per device with that device current, then cached.
+void* noalloc_scratch_address() {
+    static std::mutex m;
+    static void* addr[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+    std::lock_guard<std::mutex> lk(m);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
+// Scratch bytes the plan for this problem uses: header | flags | carry,
+// exactly as dispatch() lays it out.
+template <typename Tin, typename Tout>
+size_t planned_scratch_bytes(const ScanArgs& a, bool tma) {
+    Plan p{};
+    if (tma) plan_for<Tin, Tout, 32, true>(a, p);
+    else plan_for<Tin, Tout, 32, false>(a, p);
+    return sizeof(WsHeader) + round256(sizeof(uint32_t) * (size_t)(p.nchunks - 1) * p.nblocks) +
+           (size_t)(p.nchunks - 1) * (size_t)a.batch * a.dim * kN * sizeof(float);
+}
+
+}  // namespace
+
+extern "C" ssm_status_t ssm_scan_fwd_noalloc(const void* u, const void* delta, const float* A,
+                                             const void* B, const void* C, const float* D,
+                                             const void* z, const float* delta_bias,
+                                             int delta_softplus, const float* initial_state,
+                                             void* y, float* final_state, int batch, int dim,
+                                             int seqlen, int dstate, int ngroups,
+                                             ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                                             void* stream) {
+    using namespace ssm_host;
+    if (batch < 0 || dim < 0 || seqlen < 0 || ngroups < 1 || dstate < 1) return SSM_ERR_SHAPE;
+    if (dim % ngroups != 0) return SSM_ERR_SHAPE;
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return SSM_ERR_DTYPE;
+    if (dstate != kN) return SSM_ERR_UNSUPPORTED;
+    const size_t rows = (size_t)batch * dim;
+    if (rows == 0) return SSM_OK;
+    if (rows > (size_t)INT32_MAX || (size_t)batch * ngroups * kN > (size_t)INT32_MAX)
+        return SSM_ERR_UNSUPPORTED;
+    if (seqlen > 0 && (!u || !delta || !B || !C || !y || !A)) return SSM_ERR_NULL;
+    const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, initial_state, y, final_state};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return SSM_ERR_ALIGN;
+    const size_t es = dtype_size(in_dtype), eo = dtype_size(out_dtype);
+    const size_t act = rows * (size_t)seqlen * es;
+    const size_t bc = (size_t)batch * ngroups * kN * (size_t)seqlen * es;
+    struct R { const void* p; size_t n; } ins[] = {
+        {u, act}, {delta, act}, {z, z ? act : 0}, {B, bc}, {C, bc}, {A, (size_t)dim * kN * 4},
+        {D, D ? (size_t)dim * 4 : 0}, {delta_bias, delta_bias ? (size_t)dim * 4 : 0},
+        {initial_state, initial_state ? rows * kN * 4 : 0}};
+    const size_t ybytes = rows * (size_t)seqlen * eo;
+    const size_t fbytes = final_state ? rows * kN * 4 : 0;
+    for (const R& r : ins) {
+        if (overlaps(y, ybytes, r.p, r.n)) return SSM_ERR_ALIAS;
+        if (overlaps(final_state, fbytes, r.p, r.n)) return SSM_ERR_ALIAS;
+    }
+    if (overlaps(y, ybytes, final_state, fbytes)) return SSM_ERR_ALIAS;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (seqlen == 0) {
+        if (final_state) {
+            cudaError_t e = initial_state
+                                ? cudaMemcpyAsync(final_state, initial_state, rows * kN * 4,
+                                                  cudaMemcpyDeviceToDevice, s)
+                                : cudaMemsetAsync(final_state, 0, rows * kN * 4, s);
+            if (e != cudaSuccess) return SSM_ERR_CUDA;
+        }
+        return SSM_OK;
+    }
+    void* scratch = noalloc_scratch_address();
+    if (!scratch) return SSM_ERR_CUDA;
+
+    ScanArgs a{};
+    a.u = u; a.delta = delta; a.z = z; a.A = A; a.Dskip = D; a.bias = delta_bias;
+    a.h0 = initial_state; a.y = y; a.final_state = final_state; a.Bm = B; a.Cm = C;
+    a.batch = batch; a.dim = dim; a.seqlen = seqlen; a.ngroups = ngroups;
+    a.dpg = dim / ngroups; a.softplus = delta_softplus ? 1 : 0;
+    const bool tma = ((size_t)seqlen * es) % 16 == 0;
+
+    size_t need;
+    if (in_dtype == SSM_BF16)
+        need = out_dtype == SSM_BF16 ? planned_scratch_bytes<__nv_bfloat16, __nv_bfloat16>(a, tma)
+                                     : planned_scratch_bytes<__nv_bfloat16, float>(a, tma);
+    else
+        need = out_dtype == SSM_BF16 ? planned_scratch_bytes<float, __nv_bfloat16>(a, tma)
+                                     : planned_scratch_bytes<float, float>(a, tma);
+    if (need > kNoAllocScratchBytes) return SSM_ERR_WORKSPACE;
+
+    // dispatch() clears the header and flags on the stream before the launch;
+    // the carried states need no clearing (each is written before it is read).
+    if (in_dtype == SSM_BF16) {
+        return out_dtype == SSM_BF16
+                   ? dispatch<__nv_bfloat16, __nv_bfloat16>(a, in_dtype, tma, s, scratch)
+                   : dispatch<__nv_bfloat16, float>(a, in_dtype, tma, s, scratch);
+    }
+    return out_dtype == SSM_BF16 ? dispatch<float, __nv_bfloat16>(a, in_dtype, tma, s, scratch)
+                                 : dispatch<float, float>(a, in_dtype, tma, s, scratch);
+}
