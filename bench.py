@@ -36,9 +36,12 @@ WORKLOAD = ("selective scan, bf16 inputs / fp32 state / fp32 y, batch 8, L 2048,
 
 # Roofline of the scan kernel: multi-function-unit (MUFU) bound.  Per
 # element (b, l, d, n) one exp2; per (b, l, d) two MUFU ops for softplus
-# (ex2, rcp) and two for the silu gate (ex2, rcp).  Peak = 152 SMs x 16 MUFU
-# results per clock x 2070 MHz (maximum SM clock).
-SMS, MUFU_PER_CLK, SM_MAX_MHZ = 152, 16, 2070.0
+# (ex2, rcp) and two for the silu gate (ex2, rcp).  Peak = 152 SMs x 32 MUFU
+# results per clock (the ex2 rate measured on GB300 by
+# state_space_model_selective_gb300.peaks: 31.4 per SM per clock) x 2070 MHz
+# (maximum SM clock).
+SMS, MUFU_PER_CLK, SM_MAX_MHZ = 152, 32, 2070.0
+HBM_PEAK_GBS = 6778.0  # measured copy bandwidth of the GB300s
 MUFU_PEAK_GOPS = SMS * MUFU_PER_CLK * SM_MAX_MHZ * 1e6 / 1e9
 # DRAM bytes per launch of the scan kernel from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum) of this exact kernel build and
@@ -278,6 +281,8 @@ def run_ours(args):
     e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1), dev)
     e2e_total = sum_over_ranks(dist, float(elements * e2e_steps), dev)
 
+    paths = measure_other_paths(dev) if rank == 0 else None
+
     out = None
     if rank == 0:
         cpu = cpu_baseline(host) if world == 1 else None  # rank 0 at N=1 only
@@ -302,11 +307,80 @@ def run_ours(args):
                          "hbm_gbs_at_this_time": hbm / per_launch_s / 1e9},
             "clocks": clocks,
             "cpu_baseline": cpu,
+            "other_paths": paths,
         }
         print(json.dumps(out), flush=True)
     if dist is not None:
         dist.destroy_process_group()
     return out
+
+
+def measure_other_paths(dev, reps=20):
+    """Device time of the chunked SSD (batch 32, L 256, 32 heads, headdim 64,
+    d_state 128, bf16 in, fp32 y) and of one decode step (batch 256, 32 heads,
+    headdim 64, d_state 128, fp32), against the HBM roofline of their
+    algorithmic bytes."""
+    import torch
+    from state_space_model_selective_gb300 import binding, inputs
+    res = {}
+    inp = inputs.ssd_inputs(32, 256, 32, 64, 128, 1, "bf16", seed=1004, device="cuda")
+    y = torch.empty(inp["x"].shape, device=dev)
+    fs = torch.empty(32, 32, 64, 128, device=dev)
+
+    def ssd():
+        binding.ssd_chunked_fwd(inp["x"], inp["dt"], inp["A_head"], inp["B"], inp["C"], 64,
+                                out_dtype=torch.float32, y=y, final_state=fs)
+    ms = _time(ssd, reps)
+    nbytes = inp["x"].numel() * 2 + y.numel() * 4 + 2 * inp["B"].numel() * 2 + \
+        inp["dt"].numel() * 4 + fs.numel() * 4
+    el = 32 * 256 * 32 * 64 * 128
+    res["ssd_chunked_fwd"] = {
+        "workload": "chunked SSD bf16 in / fp32 y, batch 32, L 256, 32 heads, headdim 64, "
+                    "d_state 128, chunk 64", "ms": ms, "elements_per_s": el / (ms / 1e3),
+        "roofline": {"bound": "hbm", "achieved": nbytes / (ms / 1e3) / 1e9,
+                     "peak": HBM_PEAK_GBS, "unit": "GB/s",
+                     "frac": nbytes / (ms / 1e3) / 1e9 / HBM_PEAK_GBS,
+                     "algorithmic_bytes": nbytes}}
+    del inp, y, fs
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1005)
+    B_, H, P, N = 256, 32, 64, 128
+    state = 0.1 * torch.randn(B_, H, P, N, device=dev, generator=g)
+    x = torch.randn(B_, H, P, device=dev, generator=g)
+    Bm = torch.randn(B_, 1, N, device=dev, generator=g)
+    Cm = torch.randn(B_, 1, N, device=dev, generator=g)
+    dt = torch.nn.functional.softplus(torch.randn(B_, H, device=dev, generator=g) - 4)
+    A = -(1 + 15 * torch.rand(H, device=dev, generator=g))
+    D = torch.ones(H, device=dev)
+    yd = torch.empty_like(x)
+
+    def dec():
+        binding.ssm_decode_step(state, x, dt, A, Bm, Cm, D, y=yd)
+    ms = _time(dec, reps)
+    nbytes = 2 * state.numel() * 4 + 2 * x.numel() * 4 + 2 * Bm.numel() * 4 + dt.numel() * 4
+    res["ssm_decode_step"] = {
+        "workload": "decode step fp32, batch 256, 32 heads, headdim 64, d_state 128",
+        "ms": ms, "elements_per_s": state.numel() / (ms / 1e3),
+        "roofline": {"bound": "hbm", "achieved": nbytes / (ms / 1e3) / 1e9,
+                     "peak": HBM_PEAK_GBS, "unit": "GB/s",
+                     "frac": nbytes / (ms / 1e3) / 1e9 / HBM_PEAK_GBS,
+                     "algorithmic_bytes": nbytes}}
+    return res
+
+
+def _time(fn, reps):
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(reps):
+        fn()
+    e1.record(s)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
 
 
 # ------------------------------------------------------------------ reference

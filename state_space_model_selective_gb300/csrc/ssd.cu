@@ -425,7 +425,15 @@ extern "C" ssm_status_t ssd_chunked_fwd(const void* x, const float* dt, const fl
     const size_t rows = (size_t)batch * seqlen;
     if (batch == 0 || nheads == 0) return SSM_OK;
     if ((size_t)batch * nheads > (size_t)INT32_MAX) return SSM_ERR_UNSUPPORTED;
-    if (!x || !dt || !A_head || !B || !C || (rows > 0 && !y)) return SSM_ERR_NULL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (seqlen == 0) {  // empty sequence: the state stays zero
+        const size_t fb0 = (size_t)batch * nheads * headdim * dstate * 4;
+        if (final_state && !aligned16(final_state)) return SSM_ERR_ALIGN;
+        if (final_state && cudaMemsetAsync(final_state, 0, fb0, s) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        return SSM_OK;
+    }
+    if (!x || !dt || !A_head || !B || !C || !y) return SSM_ERR_NULL;
     const void* ptrs[] = {x, dt, A_head, B, C, y, final_state};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return SSM_ERR_ALIGN;
@@ -439,12 +447,6 @@ extern "C" ssm_status_t ssd_chunked_fwd(const void* x, const float* dt, const fl
         if (overlaps(y, yb, r.p, r.n) || overlaps(final_state, fb, r.p, r.n)) return SSM_ERR_ALIAS;
     if (overlaps(y, yb, final_state, fb)) return SSM_ERR_ALIAS;
 
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (seqlen == 0) {
-        if (final_state && cudaMemsetAsync(final_state, 0, fb, s) != cudaSuccess)
-            return SSM_ERR_CUDA;
-        return SSM_OK;
-    }
     CUtensorMap mc, mb;
     if (!make_bc_map(&mc, C, batch, seqlen, ngroups) || !make_bc_map(&mb, B, batch, seqlen, ngroups))
         return SSM_ERR_CUDA;
