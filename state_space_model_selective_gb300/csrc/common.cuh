@@ -54,22 +54,20 @@ constexpr float kLog2e = 1.4426950408889634f;
 // softplus(x) = log(1 + e^x) = max(x, 0) + log1p(e^-|x|), accurate to a few
 // ulp in fp32 including far into the negative tail (where 1 + e^x would round
 // away e^x).  log1p(t) for t = e^-|x| in (0, 1] is evaluated as
-// 2 atanh(s), s = t / (2 + t) in (0, 1/3], by the odd series
-// 2 s (1 + s^2/3 + s^4/5 + ...), truncated after the s^14/15 term (the next
-// one is below 2e-9 relative since s^2 <= 1/9).  2 MUFU ops + ~13 FP32 ops.
+// 2 atanh(s) = 2 s f(s^2), s = t / (2 + t) in (0, 1/3], with f(w) =
+// atanh(sqrt(w)) / sqrt(w) replaced by a degree-4 polynomial fitted for
+// minimum relative error on [0, 1/9] (csrc/fit_softplus_poly.py: 4e-9, about
+// 1 ulp once evaluated in fp32).  2 MUFU ops + ~11 FP32 ops.
 __device__ __forceinline__ float softplus_f(float x) {
     const float t = ex2_approx(-fabsf(x) * kLog2e);
     const float s = t * rcp_approx(2.0f + t);
     const float w = s * s;
-    float p = 1.0f / 15.0f;
-    p = fmaf(p, w, 1.0f / 13.0f);
-    p = fmaf(p, w, 1.0f / 11.0f);
-    p = fmaf(p, w, 1.0f / 9.0f);
-    p = fmaf(p, w, 1.0f / 7.0f);
-    p = fmaf(p, w, 1.0f / 5.0f);
-    p = fmaf(p, w, 1.0f / 3.0f);
+    float p = 0.1408916562795639f;
+    p = fmaf(p, w, 0.13980305194854736f);
+    p = fmaf(p, w, 0.20012454688549042f);
+    p = fmaf(p, w, 0.3333315849304199f);
     p = fmaf(p, w, 1.0f);
-    return fmaxf(x, 0.0f) + 2.0f * s * p;
+    return fmaf(s + s, p, fmaxf(x, 0.0f));
 }
 
 // silu(z) = z / (1 + e^-z); -> -0 for z -> -inf, z for z -> +inf.
@@ -151,6 +149,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Order this thread's generic-proxy shared-memory accesses before later
+// async-proxy accesses (TMA writes, tcgen05.mma operand reads) that follow
+// the next synchronisation.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ------------------------------------------------------------ barriers

@@ -9,9 +9,9 @@
 // The step is one streaming read-modify-write of the fp32 state
 // (batch, nheads, headdim, dstate), so it is bound by HBM bandwidth: each
 // (b, h, p) row of dstate floats is owned by dstate/16 lanes holding 16
-// consecutive states each (four 16-byte loads in flight per lane, evict-first
-// cache hints), the C^T h contraction is an intra-warp shuffle reduction, and
-// the row's first lane writes y.
+// consecutive states each (16-byte loads with evict-first cache hints, two
+// rows' loads in flight per lane), the C^T h contraction is an intra-warp
+// shuffle reduction, and the row's first lane writes y.
 #include "common.cuh"
 
 namespace {
@@ -38,59 +38,83 @@ __device__ __forceinline__ void load16(const T* p, float* v) {
     }
 }
 
+// One CTA per (batch, head): alpha = exp(dt A) and each thread's slice of B
+// and C are loaded once and reused for every headdim row the thread updates.
+// A row of dstate floats is split over LPR = dstate / 16 lanes (16 states,
+// four 16-byte loads each); the CTA's 256 threads cover 256 / LPR rows at a
+// time, and each thread handles up to RPT rows with all their loads issued
+// before any arithmetic.
 template <typename T, int LPR>
 __global__ void __launch_bounds__(256)
     decode_kernel(float* __restrict__ state, const T* __restrict__ x,
                   const float* __restrict__ dt, const float* __restrict__ A,
                   const T* __restrict__ Bm, const T* __restrict__ Cm,
                   const float* __restrict__ Dskip, const T* __restrict__ z, T* __restrict__ y,
-                  long long rows, int nheads, int headdim, int ngroups) {
+                  int nheads, int headdim, int ngroups) {
     constexpr int kDstate = LPR * 16;
-    const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const long long row_raw = gtid / LPR;  // (b, h, p) row
-    const int part = (int)(gtid % LPR);
-    // Lanes past the last row stay for the shuffle reduction (full-warp
-    // mask) but touch no memory.
-    const bool active = row_raw < rows;
-    const long long row = active ? row_raw : rows - 1;
-    const int h = (int)((row / headdim) % nheads);
-    const long long b = row / ((long long)headdim * nheads);
+    constexpr int kRowsPerPass = 256 / LPR;
+    constexpr int RPT = 2;
+    const int h = blockIdx.x % nheads;
+    const long long b = blockIdx.x / nheads;
     const int g = h / (nheads / ngroups);
+    const int part = threadIdx.x % LPR;
+    const int r0 = threadIdx.x / LPR;
 
     const float dtv = dt[b * nheads + h];
     const float alpha = expf(dtv * A[h]);
-    const float xv = to_f32(x[row]);
-    const float dbx = dtv * xv;
-
-    float4* sp = reinterpret_cast<float4*>(state + row * kDstate + part * 16);
-    float s[16];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float4 v = __ldcs(sp + i);
-        s[4 * i] = v.x; s[4 * i + 1] = v.y; s[4 * i + 2] = v.z; s[4 * i + 3] = v.w;
-    }
+    const float Dh = Dskip ? Dskip[h] : 0.0f;
     float bv[16], cv[16];
     const long long bc = (b * ngroups + g) * kDstate + part * 16;
     load16<T>(Bm + bc, bv);
     load16<T>(Cm + bc, cv);
+    const long long row_base = (b * nheads + h) * (long long)headdim;
 
-    float acc = 0.0f;
+    for (int p0 = 0; p0 < headdim; p0 += kRowsPerPass * RPT) {
+        float s[RPT][16];
+        float xv[RPT], zv[RPT];
+        bool act[RPT];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        s[i] = fmaf(alpha, s[i], dbx * bv[i]);
-        acc = fmaf(cv[i], s[i], acc);
-    }
-    if (active) {
+        for (int r = 0; r < RPT; ++r) {
+            const int p = p0 + r * kRowsPerPass + r0;
+            act[r] = p < headdim;
+            const long long row = row_base + (act[r] ? p : 0);
+            const float4* sp = reinterpret_cast<const float4*>(state + row * kDstate + part * 16);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            __stcs(sp + i, make_float4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]));
-    }
+            for (int i = 0; i < 4; ++i) {
+                const float4 v = act[r] ? __ldcs(sp + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                s[r][4 * i] = v.x; s[r][4 * i + 1] = v.y; s[r][4 * i + 2] = v.z; s[r][4 * i + 3] = v.w;
+            }
+            xv[r] = act[r] ? to_f32(x[row]) : 0.0f;
+            zv[r] = (act[r] && z) ? to_f32(z[row]) : 0.0f;
+        }
 #pragma unroll
-    for (int o = LPR / 2; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (active && part == 0) {
-        float out = acc + (Dskip ? Dskip[h] * xv : 0.0f);
-        if (z) out *= silu_f(to_f32(z[row]));
-        y[row] = from_f32<T>(out);
+        for (int r = 0; r < RPT; ++r) {
+            const int p = p0 + r * kRowsPerPass + r0;
+            const long long row = row_base + (act[r] ? p : 0);
+            const float dbx = dtv * xv[r];
+            float acc = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                s[r][i] = fmaf(alpha, s[r][i], dbx * bv[i]);
+                acc = fmaf(cv[i], s[r][i], acc);
+            }
+            if (act[r]) {
+                float4* sp = reinterpret_cast<float4*>(state + row * kDstate + part * 16);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    __stcs(sp + i, make_float4(s[r][4 * i], s[r][4 * i + 1], s[r][4 * i + 2],
+                                               s[r][4 * i + 3]));
+            }
+            // whole rows share a warp (LPR divides 32), so the row's lanes
+            // reduce among themselves; every lane takes part in the shuffles
+#pragma unroll
+            for (int o = LPR / 2; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (act[r] && part == 0) {
+                float out = acc + Dh * xv[r];
+                if (z) out *= silu_f(zv[r]);
+                y[row] = from_f32<T>(out);
+            }
+        }
     }
 }
 
@@ -98,11 +122,10 @@ template <typename T, int LPR>
 ssm_status_t launch(float* state, const void* x, const float* dt, const float* A, const void* B,
                     const void* C, const float* D, const void* z, void* y, long long rows,
                     int nheads, int headdim, int ngroups, cudaStream_t s) {
-    const long long threads = rows * LPR;
-    const unsigned grid = (unsigned)((threads + 255) / 256);
-    decode_kernel<T, LPR><<<grid, 256, 0, s>>>(
+    const long long grid = rows / headdim;  // batch * nheads
+    decode_kernel<T, LPR><<<(unsigned)grid, 256, 0, s>>>(
         state, static_cast<const T*>(x), dt, A, static_cast<const T*>(B),
-        static_cast<const T*>(C), D, static_cast<const T*>(z), static_cast<T*>(y), rows, nheads,
+        static_cast<const T*>(C), D, static_cast<const T*>(z), static_cast<T*>(y), nheads,
         headdim, ngroups);
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }

@@ -63,7 +63,107 @@ __global__ void probe_ffma2(float* out, int iters, float a, float b) {
     out[blockIdx.x * blockDim.x + threadIdx.x] = s;
 }
 
+// Latency probes: one warp runs a chain of dependent operations (16 per loop
+// iteration, unrolled); thread 0 writes the elapsed SM clocks per operation.
+template <int KIND>
+__global__ void latency_probe(float* out, int iters) {
+    __shared__ float sm[256];
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) sm[i] = 0.0f;
+    __syncthreads();
+    float x = 0.001f * (threadIdx.x + 1);
+    const float2 av = make_float2(0.999f, 0.999f), bv = make_float2(0.001f, 0.001f);
+    const uint64_t ar = *reinterpret_cast<const uint64_t*>(&av);
+    const uint64_t br = *reinterpret_cast<const uint64_t*>(&bv);
+    const float2 xv = make_float2(x, x);
+    uint64_t v = *reinterpret_cast<const uint64_t*>(&xv);
+    unsigned addr = (unsigned)__cvta_generic_to_shared(sm) + 4 * (threadIdx.x & 7);
+    __syncwarp();
+    const long long t0 = clock64();
+    for (int i = 0; i < iters; ++i) {
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            if constexpr (KIND == 0) asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(x) : "f"(-x));
+            if constexpr (KIND == 1) asm volatile("rcp.approx.ftz.f32 %0, %1;" : "=f"(x) : "f"(x));
+            if constexpr (KIND == 2)
+                asm volatile("fma.rn.f32 %0, %0, %1, %2;" : "+f"(x) : "f"(0.999f), "f"(0.001f));
+            if constexpr (KIND == 3)
+                asm volatile("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(v) : "l"(ar), "l"(br));
+            if constexpr (KIND == 4) {  // the loaded value (0) is added to the next address
+                unsigned w;
+                asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(addr));
+                addr += w;
+            }
+        }
+    }
+    const long long t1 = clock64();
+    if (threadIdx.x == 0) out[0] = (float)(t1 - t0) / (16.0f * iters);
+    if (threadIdx.x == 1) out[1] = x + (float)(v & 1) + (float)(addr & 1);
+}
+
+// The selective scan's per-step arithmetic for NS states of one channel, from
+// registers only: exponent products, NS ex2, state update and read-out, in
+// scalar fp32.  y is accumulated so the work is not dead.  Timed by the host.
+template <int NS>
+__global__ void scan_mix_probe(float* out, int steps) {
+    float h[NS], A[NS], Bv[NS], Cv[NS];
+#pragma unroll
+    for (int k = 0; k < NS; ++k) {
+        h[k] = 0.0f;
+        A[k] = -1.4427f * (k + 1);
+        Bv[k] = 0.01f * (k + threadIdx.x % 7);
+        Cv[k] = 0.02f * (k - 3);
+    }
+    float ysum = 0.0f;
+    float dl = 0.01f + 1e-5f * threadIdx.x, du = 0.003f;
+    for (int t = 0; t < steps; ++t) {
+        dl = fmaf(dl, 0.9999f, 1e-6f);  // a fresh step value
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            float e;
+            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(dl * A[k]));
+            h[k] = fmaf(e, h[k], du * Bv[k]);
+            acc[k & 3] = fmaf(Cv[k], h[k], acc[k & 3]);
+        }
+        ysum += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    }
+    out[blockIdx.x * blockDim.x + threadIdx.x] = ysum + h[0] + h[NS - 1];
+}
+
 }  // namespace
+
+// Per-step arithmetic of the scan with `ns` (4, 8 or 16) states per thread;
+// returns the number of steps x threads executed, or -1.
+extern "C" double ssm_scan_mix_probe(int ns, int blocks, int threads, int steps, float* out,
+                                     void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (ns) {
+        case 4: scan_mix_probe<4><<<blocks, threads, 0, s>>>(out, steps); break;
+        case 8: scan_mix_probe<8><<<blocks, threads, 0, s>>>(out, steps); break;
+        case 16: scan_mix_probe<16><<<blocks, threads, 0, s>>>(out, steps); break;
+        default: return -1.0;
+    }
+    if (cudaGetLastError() != cudaSuccess) return -1.0;
+    return (double)blocks * threads * steps;
+}
+
+// Cycles per dependent operation for kind 0 ex2, 1 rcp, 2 fp32 FMA,
+// 3 fp32x2 FMA, 4 shared-memory load; one warp, `iters` operations.
+extern "C" float ssm_latency_probe(int kind, int iters, float* out, void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (kind) {
+        case 0: latency_probe<0><<<1, 32, 0, s>>>(out, iters); break;
+        case 1: latency_probe<1><<<1, 32, 0, s>>>(out, iters); break;
+        case 2: latency_probe<2><<<1, 32, 0, s>>>(out, iters); break;
+        case 3: latency_probe<3><<<1, 32, 0, s>>>(out, iters); break;
+        case 4: latency_probe<4><<<1, 32, 0, s>>>(out, iters); break;
+        default: return -1.0f;
+    }
+    float h[2] = {0, 0};
+    if (cudaMemcpyAsync(h, out, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return -1.0f;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return -1.0f;
+    return h[0];
+}
 
 // kind 0: ex2 (one MUFU op per lane per instruction)
 // kind 1: fp32 FMA; kind 2: packed fp32x2 FMA (two FMAs per lane per instruction)

@@ -44,7 +44,7 @@ constexpr int kThreads = 128;
 // shared-memory regions (offsets from a 1024-aligned base)
 constexpr uint32_t kRC = 0;            // C tile [128 t][128 n]  -> later M' hi
 constexpr uint32_t kRB = 32768;        // B tile [128 j][128 n]  -> later M' lo
-constexpr uint32_t kRBT = 65536;       // B^T [128 n][128 j]     -> later S staging (fp32)
+constexpr uint32_t kRBT = 65536;       // x tile [128 j][64 p] -> B^T [128 n][128 j] -> S staging
 constexpr uint32_t kRX = 98304;        // X^T [64 p][128 j]
 constexpr uint32_t kRXP = 114688;      // X'^T hi [64][128] | lo [64][128]
 constexpr uint32_t kRS = 147456;       // S hi [64 p][128 n] | lo [64][128]
@@ -83,7 +83,7 @@ __device__ __forceinline__ uint64_t kdesc(uint32_t tile_saddr, int kk) {
 template <typename Tout>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_B,
-                   const SsdArgs a) {
+                   const __grid_constant__ CUtensorMap tm_x, const SsdArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t sbase = smem_u32(smem);
@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
         prefetch_tensormap(&tm_C);
         prefetch_tensormap(&tm_B);
+        prefetch_tensormap(&tm_x);
     }
     // S_prev = 0: zero both halves of the S operand tile
     for (int i = tid; i < 32768 / 16; i += kThreads)
@@ -133,11 +134,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nv = min(kQ, a.seqlen - t0);
 
         if (tid == 0) {
-            mbar_arrive_expect_tx(bar_tma, 4 * 16384);
+            mbar_arrive_expect_tx(bar_tma, 5 * 16384);
             tma_load_4d(smem + kRC, &tm_C, bar_tma, 0, g, t0, b);
             tma_load_4d(smem + kRC + 16384, &tm_C, bar_tma, 64, g, t0, b);
             tma_load_4d(smem + kRB, &tm_B, bar_tma, 0, g, t0, b);
             tma_load_4d(smem + kRB + 16384, &tm_B, bar_tma, 64, g, t0, b);
+            tma_load_3d(smem + kRBT, &tm_x, bar_tma, h * kP, t0, b);
         }
 
         // ---- cumulative log-decay of the block (padding steps: dt = 0)
@@ -161,39 +163,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float a_blk = ex2_approx(cs_last * kLog2e);
         __syncthreads();
 
-        // ---- X^T (exact) and X'^T = (w o X)^T split hi/lo, [64 p][128 j]
-        for (int item = tid; item < kP * (kQ / 8); item += kThreads) {
-            const int p = item % kP, jg = item / kP;
-            float xv[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int j = jg * 8 + q;
-                xv[q] = j < nv ? __bfloat162float(
-                                     a.x[((xrow0 + t0 + j) * a.nheads + h) * kP + p])
-                               : 0.0f;
-            }
-            uint4 wx, wh, wl;
-            float hi[8], lo[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) split_bf16(s_w[jg * 8 + q] * xv[q], hi[q], lo[q]);
-            wx = make_uint4(pack_bf16(xv[0], xv[1]), pack_bf16(xv[2], xv[3]),
-                            pack_bf16(xv[4], xv[5]), pack_bf16(xv[6], xv[7]));
-            wh = make_uint4(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]),
-                            pack_bf16(hi[4], hi[5]), pack_bf16(hi[6], hi[7]));
-            wl = make_uint4(pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]),
-                            pack_bf16(lo[4], lo[5]), pack_bf16(lo[6], lo[7]));
-            const uint32_t off = kmaj_off<kP>(p, jg * 8);
-            *reinterpret_cast<uint4*>(smem + kRX + off) = wx;
-            *reinterpret_cast<uint4*>(smem + kRXP + off) = wh;
-            *reinterpret_cast<uint4*>(smem + kRXP + 16384 + off) = wl;
-        }
-
         // ---- C, B tiles landed?  Then B^T [128 n][128 j] (exact)
         {
             const bool got = mbar_wait(bar_tma, tma_phase, nullptr);
             tma_phase ^= 1;
             if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
         }
+        // ---- X^T (exact) and X'^T = (w o X)^T split hi/lo, [64 p][128 j],
+        // from the x tile [128 j][64 p] that TMA put in the B^T region
+        for (int item = tid; item < kP * (kQ / 8); item += kThreads) {
+            const int p = item % kP, jg = item / kP;
+            float xv[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                xv[q] = bf16lo(*reinterpret_cast<const uint16_t*>(
+                    smem + kRBT + kmaj_off<kQ>(jg * 8 + q, p)));
+            float hi[8], lo[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) split_bf16(s_w[jg * 8 + q] * xv[q], hi[q], lo[q]);
+            const uint4 wx = make_uint4(pack_bf16(xv[0], xv[1]), pack_bf16(xv[2], xv[3]),
+                                        pack_bf16(xv[4], xv[5]), pack_bf16(xv[6], xv[7]));
+            const uint4 wh = make_uint4(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]),
+                                        pack_bf16(hi[4], hi[5]), pack_bf16(hi[6], hi[7]));
+            const uint4 wl = make_uint4(pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]),
+                                        pack_bf16(lo[4], lo[5]), pack_bf16(lo[6], lo[7]));
+            const uint32_t off = kmaj_off<kP>(p, jg * 8);
+            *reinterpret_cast<uint4*>(smem + kRX + off) = wx;
+            *reinterpret_cast<uint4*>(smem + kRXP + off) = wh;
+            *reinterpret_cast<uint4*>(smem + kRXP + 16384 + off) = wl;
+        }
+        __syncthreads();  // the x tile is read; B^T overwrites it
         for (int item = tid; item < kNs * (kQ / 8); item += kThreads) {
             const int n = item % kNs, jg = item / kNs;
             uint16_t e[8];
@@ -362,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        fence_proxy_async_smem();  // generic reads/writes before the next block's TMA
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
@@ -394,15 +394,30 @@ bool make_bc_map(CUtensorMap* map, const void* base, int batch, int seqlen, int 
            CUDA_SUCCESS;
 }
 
+bool make_x_map(CUtensorMap* map, const void* base, int batch, int seqlen, int nheads) {
+    ssm_host::EncodeTiledFn fn = ssm_host::encode_tiled_fn();
+    if (!fn) return false;
+    // (batch, seqlen, nheads, headdim) as 3-D {nheads * headdim, seqlen, batch}
+    const cuuint64_t dims[3] = {(cuuint64_t)nheads * kP, (cuuint64_t)seqlen, (cuuint64_t)batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)nheads * kP * 2,
+                                   (cuuint64_t)seqlen * nheads * kP * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)kP, (cuuint32_t)kQ, 1};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+              box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 template <typename Tout>
-ssm_status_t launch(const CUtensorMap& mc, const CUtensorMap& mb, const SsdArgs& a,
-                    cudaStream_t s) {
+ssm_status_t launch(const CUtensorMap& mc, const CUtensorMap& mb, const CUtensorMap& mx,
+                    const SsdArgs& a, cudaStream_t s) {
     auto kern = ssd_fwd_kernel<Tout>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
         cudaSuccess)
         return SSM_ERR_CUDA;
     const unsigned grid = (unsigned)(a.batch * a.nheads);
-    kern<<<grid, kThreads, kSmemAlloc, s>>>(mc, mb, a);
+    kern<<<grid, kThreads, kSmemAlloc, s>>>(mc, mb, mx, a);
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
@@ -447,8 +462,9 @@ extern "C" ssm_status_t ssd_chunked_fwd(const void* x, const float* dt, const fl
         if (overlaps(y, yb, r.p, r.n) || overlaps(final_state, fb, r.p, r.n)) return SSM_ERR_ALIAS;
     if (overlaps(y, yb, final_state, fb)) return SSM_ERR_ALIAS;
 
-    CUtensorMap mc, mb;
-    if (!make_bc_map(&mc, C, batch, seqlen, ngroups) || !make_bc_map(&mb, B, batch, seqlen, ngroups))
+    CUtensorMap mc, mb, mx;
+    if (!make_bc_map(&mc, C, batch, seqlen, ngroups) || !make_bc_map(&mb, B, batch, seqlen, ngroups) ||
+        !make_x_map(&mx, x, batch, seqlen, nheads))
         return SSM_ERR_CUDA;
     SsdArgs a{};
     a.x = static_cast<const __nv_bfloat16*>(x);
@@ -460,5 +476,6 @@ extern "C" ssm_status_t ssd_chunked_fwd(const void* x, const float* dt, const fl
     a.seqlen = seqlen;
     a.nheads = nheads;
     a.ngroups = ngroups;
-    return out_dtype == SSM_BF16 ? launch<__nv_bfloat16>(mc, mb, a, s) : launch<float>(mc, mb, a, s);
+    return out_dtype == SSM_BF16 ? launch<__nv_bfloat16>(mc, mb, mx, a, s)
+                                 : launch<float>(mc, mb, mx, a, s);
 }

@@ -56,6 +56,47 @@ def measure(iters: int = 20000, reps: int = 3) -> dict:
         rate, mhz = best
         res[name] = {"per_s": rate, "sm_mhz": mhz,
                      "per_sm_per_clk": rate / sms / (mhz * 1e6) if mhz else None}
+    # the same probes with one warp per SM sub-partition (4 per SM)
+    for kind, name in ((0, "mufu_ex2_1warp_per_smsp"), (2, "ffma2_lanes_1warp_per_smsp")):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        n = lib.ssm_peak_probe(kind, sms * 4, 32, iters, ctypes.c_void_p(out.data_ptr()),
+                               ctypes.c_void_p(stream.cuda_stream))
+        e1.record(stream)
+        torch.cuda.synchronize()
+        mhz = _sm_clock_mhz()
+        rate = n / (e0.elapsed_time(e1) / 1e3)
+        res[name] = {"per_s": rate, "sm_mhz": mhz,
+                     "per_sm_per_clk": rate / sms / (mhz * 1e6) if mhz else None}
+    # the scan's per-step arithmetic (ns states per thread, scalar fp32):
+    # SM-sub-partition cycles per element with 1..4 warps per sub-partition
+    lib.ssm_scan_mix_probe.restype = ctypes.c_double
+    lib.ssm_scan_mix_probe.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p, ctypes.c_void_p]
+    mix = {}
+    for ns in (4, 8, 16):
+        for wps in (1, 2, 3, 4):
+            steps = 4000
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            lib.ssm_scan_mix_probe(ns, sms * 4 * wps, 32, 100, ctypes.c_void_p(out.data_ptr()),
+                                   ctypes.c_void_p(stream.cuda_stream))
+            e0.record(stream)
+            lib.ssm_scan_mix_probe(ns, sms * 4 * wps, 32, steps,
+                                   ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(stream.cuda_stream))
+            e1.record(stream)
+            torch.cuda.synchronize()
+            mhz = _sm_clock_mhz() or 2070.0
+            cyc = e0.elapsed_time(e1) / 1e3 * mhz * 1e6 / steps
+            mix[f"ns{ns}_{wps}warp_per_smsp"] = cyc / (wps * 32 * ns)  # cycles per element
+    res["scan_step_mix"] = mix
+    lib.ssm_latency_probe.restype = ctypes.c_float
+    lib.ssm_latency_probe.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    lat = {}
+    for kind, name in ((0, "ex2"), (1, "rcp"), (2, "ffma"), (3, "ffma2"), (4, "lds")):
+        lib.ssm_latency_probe(kind, 64, ctypes.c_void_p(out.data_ptr()),
+                              ctypes.c_void_p(stream.cuda_stream))
+        lat[name] = lib.ssm_latency_probe(kind, 2000, ctypes.c_void_p(out.data_ptr()),
+                                          ctypes.c_void_p(stream.cuda_stream))
+    res["latency_cycles"] = lat
     return res
 
 
