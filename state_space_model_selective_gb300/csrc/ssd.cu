@@ -39,7 +39,9 @@ using namespace ssm;
 constexpr int kQ = 128;   // steps per block (MMA M)
 constexpr int kP = 64;    // headdim
 constexpr int kNs = 128;  // dstate
-constexpr int kThreads = 128;
+constexpr int kGroups = 4;                // warpgroups; each per-row phase splits the columns
+constexpr int kThreads = 128 * kGroups;
+constexpr int kPart = kP / kGroups;       // columns of a 64-wide row per warpgroup
 
 // shared-memory regions (offsets from a 1024-aligned base)
 constexpr uint32_t kRC = 0;            // C tile [128 t][128 n]  -> later M' hi
@@ -96,6 +98,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_mma + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3;   // TMEM lane quarter this warp may access
+    const int part = warp >> 2;     // which part of a row's columns this warp takes
+    const int row = quarter * 32 + lane;  // the TMEM lane (row i, or state n) of this thread
     const int h = blockIdx.x % a.nheads;
     const int b = blockIdx.x / a.nheads;
     const int g = h / (a.nheads / a.ngroups);
@@ -118,16 +123,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lane base
+    const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's lane base
 
-    float S[kP];  // S_prev[n = tid][p]
+    float S[kPart];  // S_prev[n = row][part * kPart + p]
 #pragma unroll
-    for (int p = 0; p < kP; ++p) S[p] = 0.0f;
+    for (int p = 0; p < kPart; ++p) S[p] = 0.0f;
 
     const int nblocks = (a.seqlen + kQ - 1) / kQ;
     const long long xrow0 = (long long)b * a.seqlen;
     bool ok = true;
     uint32_t tma_phase = 0;
+    // dt of this block's step tid, loaded one block ahead
+    float dt_next = (tid < kQ && tid < a.seqlen) ? a.dt[(xrow0 + tid) * a.nheads + h] : 0.0f;
 
     for (int blk = 0; blk < nblocks && ok; ++blk) {
         const int t0 = blk * kQ;
@@ -142,24 +149,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(smem + kRBT, &tm_x, bar_tma, h * kP, t0, b);
         }
 
-        // ---- cumulative log-decay of the block (padding steps: dt = 0)
-        const float dti = tid < nv ? a.dt[(xrow0 + t0 + tid) * a.nheads + h] : 0.0f;
+        // ---- cumulative log-decay of the block (padding steps: dt = 0); the
+        // first warpgroup holds one step per thread
+        const float dti = dt_next;
+        dt_next = (tid < kQ && t0 + kQ + tid < a.seqlen)
+                      ? a.dt[(xrow0 + t0 + kQ + tid) * a.nheads + h]
+                      : 0.0f;  // padding steps of a partial last block: dt = 0
         float v = dti * Ah;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const float u = __shfl_up_sync(0xffffffffu, v, o);
             if (lane >= o) v += u;
         }
-        if (lane == 31) s_wsum[warp] = v;
+        if (lane == 31 && warp < 4) s_wsum[warp] = v;
         __syncthreads();
-        for (int w = 0; w < warp; ++w) v += s_wsum[w];
-        s_cs[tid] = v;
-        s_dt[tid] = dti;
+        if (tid < kQ) {
+            for (int w = 0; w < warp; ++w) v += s_wsum[w];
+            s_cs[tid] = v;
+            s_dt[tid] = dti;
+        }
         __syncthreads();
         const float cs_last = s_cs[kQ - 1];
-        const float cs_i = v;
-        s_w[tid] = ex2_approx((cs_last - cs_i) * kLog2e) * dti;
-        const float e_i = ex2_approx(cs_i * kLog2e);
+        if (tid < kQ) s_w[tid] = ex2_approx((cs_last - v) * kLog2e) * dti;
+        const float e_i = ex2_approx(s_cs[row] * kLog2e);
         const float a_blk = ex2_approx(cs_last * kLog2e);
         __syncthreads();
 
@@ -240,11 +252,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
 
-        // ---- M' row i = tid from G (TMEM cols 0..127) -> hi into RC, lo into RB
+        // ---- M' row i = row from G (TMEM cols 0..127) -> hi into RC, lo into RB;
+        // warpgroup `part` takes columns 32 part .. 32 part + 31.  Chunks wholly
+        // above the causal diagonal (all j > i for the warp's rows) are zero.
         {
-            const float csi = s_cs[tid];
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            const float csi = s_cs[row];
+            const int c = part;
+            if (c > quarter) {
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    const uint32_t off = kmaj_off<kQ>(row, c * 32 + q8 * 8);
+                    *reinterpret_cast<uint4*>(smem + kRC + off) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4*>(smem + kRB + off) = make_uint4(0, 0, 0, 0);
+                }
+            } else {
                 float gv[32];
                 tmem_ld32(t_lane + c * 32, gv);
                 tmem_wait_ld();
@@ -255,10 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int q = 0; q < 8; ++q) {
                         const int j = c * 32 + q8 * 8 + q;
                         float m = 0.0f;
-                        if (j <= tid) m = gv[q8 * 8 + q] * ex2_approx((csi - s_cs[j]) * kLog2e) * s_dt[j];
+                        if (j <= row) m = gv[q8 * 8 + q] * ex2_approx((csi - s_cs[j]) * kLog2e) * s_dt[j];
                         split_bf16(m, hi[q], lo[q]);
                     }
-                    const uint32_t off = kmaj_off<kQ>(tid, c * 32 + q8 * 8);
+                    const uint32_t off = kmaj_off<kQ>(row, c * 32 + q8 * 8);
                     *reinterpret_cast<uint4*>(smem + kRC + off) =
                         make_uint4(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]),
                                    pack_bf16(hi[4], hi[5]), pack_bf16(hi[6], hi[7]));
@@ -268,21 +289,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        // ---- state: S_prev[n = tid][:] = exp(cs_last) S_prev + S_chunk^T[n][:];
+        // ---- state: S_prev[n = row][part * kPart + :] = exp(cs_last) S_prev + S_chunk^T;
         // staged as fp32 rows (16-byte chunks XOR-swizzled by n mod 8) in RBT
         {
-            float sc[32];
+            float sc[kPart];
+            tmem_ld16(t_lane + 192 + part * kPart, sc);
+            tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                tmem_ld32(t_lane + 192 + c * 32, sc);
-                tmem_wait_ld();
+            for (int q = 0; q < kPart; ++q) S[q] = fmaf(a_blk, S[q], sc[q]);
+            float* st = reinterpret_cast<float*>(smem + kRBT) + row * kP;
 #pragma unroll
-                for (int q = 0; q < 32; ++q) S[c * 32 + q] = fmaf(a_blk, S[c * 32 + q], sc[q]);
-            }
-            float* st = reinterpret_cast<float*>(smem + kRBT) + tid * kP;
-#pragma unroll
-            for (int c4 = 0; c4 < kP / 4; ++c4)
-                reinterpret_cast<float4*>(st)[c4 ^ (tid & 7)] =
+            for (int c4 = 0; c4 < kPart / 4; ++c4)
+                reinterpret_cast<float4*>(st)[(part * (kPart / 4) + c4) ^ (row & 7)] =
                     make_float4(S[4 * c4], S[4 * c4 + 1], S[4 * c4 + 2], S[4 * c4 + 3]);
         }
         fence_proxy_async_smem();
@@ -329,27 +347,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
 
-        // ---- y[i = tid] = Y_diag + exp(cs_i) Y_off
+        // ---- y[i = row][part * kPart + :] = Y_diag + exp(cs_i) Y_off
         {
-            float yd[32], yo[32];
-            Tout* yrow = reinterpret_cast<Tout*>(a.y) + ((xrow0 + t0 + tid) * a.nheads + h) * kP;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                tmem_ld32(t_lane + c * 32, yd);
-                tmem_ld32(t_lane + 128 + c * 32, yo);
+            float yd[kPart], yo[kPart];
+            Tout* yrow = reinterpret_cast<Tout*>(a.y) + ((xrow0 + t0 + row) * a.nheads + h) * kP;
+            {
+                const int c = part;
+                tmem_ld16(t_lane + c * kPart, yd);
+                tmem_ld16(t_lane + 128 + c * kPart, yo);
                 tmem_wait_ld();
-                if (tid < nv) {
+                if (row < nv) {
                     if constexpr (sizeof(Tout) == 4) {
 #pragma unroll
-                        for (int q = 0; q < 32; q += 4)
-                            *reinterpret_cast<float4*>(reinterpret_cast<float*>(yrow) + c * 32 + q) =
+                        for (int q = 0; q < kPart; q += 4)
+                            *reinterpret_cast<float4*>(reinterpret_cast<float*>(yrow) + c * kPart + q) =
                                 make_float4(fmaf(e_i, yo[q], yd[q]), fmaf(e_i, yo[q + 1], yd[q + 1]),
                                             fmaf(e_i, yo[q + 2], yd[q + 2]),
                                             fmaf(e_i, yo[q + 3], yd[q + 3]));
                     } else {
 #pragma unroll
-                        for (int q = 0; q < 32; q += 8)
-                            *reinterpret_cast<uint4*>(yrow + c * 32 + q) = make_uint4(
+                        for (int q = 0; q < kPart; q += 8)
+                            *reinterpret_cast<uint4*>(yrow + c * kPart + q) = make_uint4(
                                 pack_bf16(fmaf(e_i, yo[q], yd[q]), fmaf(e_i, yo[q + 1], yd[q + 1])),
                                 pack_bf16(fmaf(e_i, yo[q + 2], yd[q + 2]),
                                           fmaf(e_i, yo[q + 3], yd[q + 3])),
@@ -367,11 +385,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
     }
 
-    // ---- final state [b][h][p][n = tid]
+    // ---- final state [b][h][p = part * kPart + :][n = row]
     if (ok && a.final_state) {
-        float* fs = a.final_state + ((long long)(b * a.nheads + h) * kP) * kNs + tid;
+        float* fs = a.final_state + ((long long)(b * a.nheads + h) * kP + part * kPart) * kNs + row;
 #pragma unroll
-        for (int p = 0; p < kP; ++p) fs[p * kNs] = S[p];
+        for (int p = 0; p < kPart; ++p) fs[p * kNs] = S[p];
     }
     tc_fence_before();
     __syncthreads();
