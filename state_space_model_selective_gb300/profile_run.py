@@ -1,0 +1,58 @@
+"""Run one workload a few times on the GPU (the target of ncu captures).
+
+    python -m state_space_model_selective_gb300.profile_run scan   [--reps 5]
+    python -m state_space_model_selective_gb300.profile_run ssd    [--reps 5]
+    python -m state_space_model_selective_gb300.profile_run decode [--reps 5]
+
+scan:   selective scan, bf16 in / fp32 y, batch 8, L 2048, D 1536, N 16
+ssd:    chunked SSD, bf16 in / fp32 y, batch 32, L 256, 32 heads, headdim 64, N 128
+decode: decode step, fp32, batch 256, 32 heads, headdim 64, N 128
+Inputs are drawn on the GPU (seeded); the process exits non-zero on any error.
+"""
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+from . import binding, inputs
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("workload", choices=["scan", "ssd", "decode"])
+    p.add_argument("--reps", type=int, default=5)
+    a = p.parse_args(argv)
+    dev = torch.device("cuda")
+    if a.workload == "scan":
+        B, D, L = 8, 1536, 2048
+        inp = inputs.scan_inputs(B, D, L, 16, 1, "bf16", seed=1002, device="cuda")
+        y = torch.empty(B, D, L, device=dev)
+        fs = torch.empty(B, D, 16, device=dev)
+        ws = torch.empty(binding.ssm_scan_workspace_bytes(B, D, L), dtype=torch.uint8, device=dev)
+        for _ in range(a.reps):
+            binding.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                 inp["z"], inp["delta_bias"], True, out_dtype=torch.float32,
+                                 y=y, final_state=fs, workspace=ws)
+        torch.cuda.synchronize()
+        assert binding.ssm_last_device_status(ws) == 0
+    elif a.workload == "ssd":
+        inp = inputs.ssd_inputs(32, 256, 32, 64, 128, 1, "bf16", seed=1004, device="cuda")
+        y = torch.empty(inp["x"].shape, device=dev)
+        fs = torch.empty(32, 32, 64, 128, device=dev)
+        for _ in range(a.reps):
+            binding.ssd_chunked_fwd(inp["x"], inp["dt"], inp["A_head"], inp["B"], inp["C"], 64,
+                                    out_dtype=torch.float32, y=y, final_state=fs)
+        torch.cuda.synchronize()
+    else:
+        inp = inputs.decode_inputs(256, 32, 64, 128, 1, 1, "f32", seed=1005, device="cuda")
+        state = inp["state"]
+        for _ in range(a.reps):
+            binding.ssm_decode_step(state, inp["x"][0], inp["dt"][0], inp["A"], inp["B"][0],
+                                    inp["C"][0], inp["D"])
+        torch.cuda.synchronize()
+    print(f"{a.workload}: {a.reps} runs ok")
+
+
+if __name__ == "__main__":
+    main()
