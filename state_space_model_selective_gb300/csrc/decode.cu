@@ -38,14 +38,14 @@ __device__ __forceinline__ void load16(const T* p, float* v) {
     }
 }
 
-// One CTA per (batch, head): alpha = exp(dt A) and each thread's slice of B
-// and C are loaded once and reused for every headdim row the thread updates.
+// One CTA per (batch, head): alpha = exp(dt A) and the head's B and C vectors
+// (in shared memory, fp32) are loaded once and reused for every headdim row.
 // A row of dstate floats is split over LPR = dstate / 16 lanes (16 states,
 // four 16-byte loads each); the CTA's 256 threads cover 256 / LPR rows at a
 // time, and each thread handles up to RPT rows with all their loads issued
 // before any arithmetic.
 template <typename T, int LPR>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 3)
     decode_kernel(float* __restrict__ state, const T* __restrict__ x,
                   const float* __restrict__ dt, const float* __restrict__ A,
                   const T* __restrict__ Bm, const T* __restrict__ Cm,
@@ -60,14 +60,12 @@ __global__ void __launch_bounds__(256)
     const int part = threadIdx.x % LPR;
     const int r0 = threadIdx.x / LPR;
 
-    const float dtv = dt[b * nheads + h];
-    const float alpha = expf(dtv * A[h]);
-    const float Dh = Dskip ? Dskip[h] : 0.0f;
-    float bv[16], cv[16];
-    const long long bc = (b * ngroups + g) * kDstate + part * 16;
-    load16<T>(Bm + bc, bv);
-    load16<T>(Cm + bc, cv);
+    __shared__ __align__(16) float sB[kDstate], sC[kDstate];
     const long long row_base = (b * nheads + h) * (long long)headdim;
+    const long long bc0 = (b * ngroups + g) * kDstate;
+    const float4* sB4 = reinterpret_cast<const float4*>(sB + part * 16);
+    const float4* sC4 = reinterpret_cast<const float4*>(sC + part * 16);
+    float dtv = 0.0f, alpha = 0.0f, Dh = 0.0f;
 
     for (int p0 = 0; p0 < headdim; p0 += kRowsPerPass * RPT) {
         float s[RPT][16];
@@ -87,6 +85,17 @@ __global__ void __launch_bounds__(256)
             xv[r] = act[r] ? to_f32(x[row]) : 0.0f;
             zv[r] = (act[r] && z) ? to_f32(z[row]) : 0.0f;
         }
+        if (p0 == 0) {
+            // B, C, alpha: after the first rows' loads are in flight
+            for (int i = threadIdx.x; i < kDstate; i += 256) {
+                sB[i] = to_f32(Bm[bc0 + i]);
+                sC[i] = to_f32(Cm[bc0 + i]);
+            }
+            dtv = dt[b * nheads + h];
+            alpha = expf(dtv * A[h]);
+            Dh = Dskip ? Dskip[h] : 0.0f;
+            __syncthreads();
+        }
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
             const int p = p0 + r * kRowsPerPass + r0;
@@ -94,9 +103,14 @@ __global__ void __launch_bounds__(256)
             const float dbx = dtv * xv[r];
             float acc = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                s[r][i] = fmaf(alpha, s[r][i], dbx * bv[i]);
-                acc = fmaf(cv[i], s[r][i], acc);
+            for (int i4 = 0; i4 < 4; ++i4) {
+                const float4 bq = sB4[i4], cq = sC4[i4];
+                const float bb[4] = {bq.x, bq.y, bq.z, bq.w}, cc[4] = {cq.x, cq.y, cq.z, cq.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    s[r][4 * i4 + k] = fmaf(alpha, s[r][4 * i4 + k], dbx * bb[k]);
+                    acc = fmaf(cc[k], s[r][4 * i4 + k], acc);
+                }
             }
             if (act[r]) {
                 float4* sp = reinterpret_cast<float4*>(state + row * kDstate + part * 16);
