@@ -130,7 +130,139 @@ __global__ void scan_mix_probe(float* out, int steps) {
     out[blockIdx.x * blockDim.x + threadIdx.x] = ysum + h[0] + h[NS - 1];
 }
 
+// Shared-memory load throughput by access pattern: each thread issues
+// `iters` x 8 loads (volatile, so none is merged or hoisted).  WIDTH = 4, 8 or
+// 16 bytes; PATTERN 0: every lane of the warp reads the same address; 1: 4
+// distinct addresses (lane % 4); 2: 4 distinct addresses (lane / 8, one per
+// quarter-warp); 3: 32 distinct consecutive addresses.
+template <int WIDTH, int PATTERN>
+__global__ void lds_probe(float* out, int iters) {
+    __shared__ __align__(16) float sm[4096];
+    for (int i = threadIdx.x; i < 4096; i += blockDim.x) sm[i] = 0.001f * i;
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    int slot = 0;
+    if (PATTERN == 1) slot = lane & 3;
+    if (PATTERN == 2) slot = lane >> 3;
+    if (PATTERN == 3) slot = lane;
+    const unsigned base = (unsigned)__cvta_generic_to_shared(sm) + slot * WIDTH;
+    float acc = 0.0f;
+    for (int i = 0; i < iters; ++i) {
+        // 8 loads 128 bytes apart in one of 8 1-KB rows (all below 9 KB)
+        const unsigned row = base + ((unsigned)i & 7u) * 1024u;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const unsigned q = row + u * 128u;
+            float v0, v1, v2, v3;
+            if constexpr (WIDTH == 4) {
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v0) : "r"(q));
+            } else if constexpr (WIDTH == 8) {
+                asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v0), "=f"(v1) : "r"(q));
+            } else {
+                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                             : "=f"(v0), "=f"(v1), "=f"(v2), "=f"(v3)
+                             : "r"(q));
+            }
+            acc += v0;  // one add per load keeps the issue cost per load low
+        }
+    }
+    out[blockIdx.x * blockDim.x + threadIdx.x] = acc;
+}
+
+// The scan's full per-element arithmetic (dl*A, ex2, du*B, state FMA,
+// read-out FMA) for NS states of one channel, from registers, with dl and
+// du changing every step.  PACKED = 1 does the four fp32 operations on pairs
+// of states with the fp32x2 instructions (mul/fma .f32x2).
+template <int NS, int PACKED>
+__global__ void scan_mix2_probe(float* out, int steps) {
+    float h[NS], A[NS], Bv[NS], Cv[NS];
+#pragma unroll
+    for (int k = 0; k < NS; ++k) {
+        h[k] = 0.0f;
+        A[k] = -1.4427f * (k + 1);
+        Bv[k] = 0.01f * (k + threadIdx.x % 7);
+        Cv[k] = 0.02f * (k - 3);
+    }
+    float ysum = 0.0f;
+    float dl = 0.01f + 1e-5f * threadIdx.x, du = 0.003f;
+    for (int t = 0; t < steps; ++t) {
+        dl = fmaf(dl, 0.9999f, 1e-6f);
+        du = fmaf(du, 0.9999f, 1e-6f);
+        if constexpr (PACKED) {
+            uint64_t acc2 = 0;
+            const float2 dd = make_float2(dl, dl), uu = make_float2(du, du);
+            const uint64_t dl2 = *reinterpret_cast<const uint64_t*>(&dd);
+            const uint64_t du2 = *reinterpret_cast<const uint64_t*>(&uu);
+#pragma unroll
+            for (int k = 0; k < NS; k += 2) {
+                const float2 ap = make_float2(A[k], A[k + 1]);
+                const float2 bp = make_float2(Bv[k], Bv[k + 1]);
+                const float2 cp = make_float2(Cv[k], Cv[k + 1]);
+                float2 hp = make_float2(h[k], h[k + 1]);
+                uint64_t arg, bx, hh = *reinterpret_cast<uint64_t*>(&hp);
+                asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(arg) : "l"(dl2),
+                    "l"(*reinterpret_cast<const uint64_t*>(&ap)));
+                asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(bx) : "l"(du2),
+                    "l"(*reinterpret_cast<const uint64_t*>(&bp)));
+                float2 av = *reinterpret_cast<float2*>(&arg);
+                float e0, e1;
+                asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(av.x));
+                asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(av.y));
+                const float2 ep = make_float2(e0, e1);
+                asm("fma.rn.f32x2 %0, %1, %0, %2;" : "+l"(hh)
+                    : "l"(*reinterpret_cast<const uint64_t*>(&ep)), "l"(bx));
+                asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2)
+                    : "l"(*reinterpret_cast<const uint64_t*>(&cp)), "l"(hh));
+                hp = *reinterpret_cast<float2*>(&hh);
+                h[k] = hp.x;
+                h[k + 1] = hp.y;
+            }
+            const float2 a = *reinterpret_cast<float2*>(&acc2);
+            ysum += a.x + a.y;
+        } else {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < NS; ++k) {
+                float e;
+                asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(dl * A[k]));
+                h[k] = fmaf(e, h[k], du * Bv[k]);
+                acc[k & 3] = fmaf(Cv[k], h[k], acc[k & 3]);
+            }
+            ysum += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        }
+    }
+    out[blockIdx.x * blockDim.x + threadIdx.x] = ysum + h[0] + h[NS - 1];
+}
+
 }  // namespace
+
+// Shared-memory load probe (see lds_probe); returns warp-level loads issued.
+extern "C" double ssm_lds_probe(int width, int pattern, int blocks, int threads, int iters,
+                                float* out, void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+#define LDS_CASE(W, P) \
+    if (width == W && pattern == P) lds_probe<W, P><<<blocks, threads, 0, s>>>(out, iters);
+    LDS_CASE(4, 0) LDS_CASE(4, 1) LDS_CASE(4, 2) LDS_CASE(4, 3)
+    LDS_CASE(8, 0) LDS_CASE(8, 1) LDS_CASE(8, 2) LDS_CASE(8, 3)
+    LDS_CASE(16, 0) LDS_CASE(16, 1) LDS_CASE(16, 2) LDS_CASE(16, 3)
+#undef LDS_CASE
+    if (cudaGetLastError() != cudaSuccess) return -1.0;
+    return (double)blocks * (threads / 32) * iters * 8;
+}
+
+// Full per-element scan arithmetic (scan_mix2_probe), scalar or packed;
+// returns the number of steps x threads executed, or -1.
+extern "C" double ssm_scan_mix2_probe(int ns, int packed, int blocks, int threads, int steps,
+                                      float* out, void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+#define MIX2_CASE(N, P) \
+    if (ns == N && packed == P) scan_mix2_probe<N, P><<<blocks, threads, 0, s>>>(out, steps);
+    MIX2_CASE(4, 0) MIX2_CASE(4, 1) MIX2_CASE(8, 0) MIX2_CASE(8, 1) MIX2_CASE(16, 0)
+    MIX2_CASE(16, 1)
+#undef MIX2_CASE
+    if (cudaGetLastError() != cudaSuccess) return -1.0;
+    return (double)blocks * threads * steps;
+}
 
 // Per-step arithmetic of the scan with `ns` (4, 8 or 16) states per thread;
 // returns the number of steps x threads executed, or -1.

@@ -39,21 +39,22 @@ using namespace ssm;
 constexpr int kQ = 128;   // steps per block (MMA M)
 constexpr int kP = 64;    // headdim
 constexpr int kNs = 128;  // dstate
-constexpr int kGroups = 4;                // warpgroups; each per-row phase splits the columns
-constexpr int kThreads = 128 * kGroups;
-constexpr int kPart = kP / kGroups;       // columns of a 64-wide row per warpgroup
+constexpr int kThreads = 256;  // two warpgroups; each per-row phase splits a row's columns
+constexpr int kHalf = 32;      // columns of a 64-wide row per warpgroup
 
-// shared-memory regions (offsets from a 1024-aligned base)
-constexpr uint32_t kRC = 0;            // C tile [128 t][128 n]  -> later M' hi
-constexpr uint32_t kRB = 32768;        // B tile [128 j][128 n]  -> later M' lo
-constexpr uint32_t kRBT = 65536;       // x tile [128 j][64 p] -> B^T [128 n][128 j] -> S staging
-constexpr uint32_t kRX = 98304;        // X^T [64 p][128 j]
-constexpr uint32_t kRXP = 114688;      // X'^T hi [64][128] | lo [64][128]
-constexpr uint32_t kRS = 147456;       // S hi [64 p][128 n] | lo [64][128]
-constexpr uint32_t kMisc = 180224;     // cs, dt, w arrays, warp sums, barriers
-constexpr uint32_t kSmemBytes = kMisc + 3 * kQ * 4 + 64 + 64;
-constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
-constexpr uint32_t kTmemCols = 256;    // G / Y_diag: 0..127, Y_off: 128..191, S^T: 192..255
+// Shared memory (offsets from the 1024-aligned dynamic base).  The total stays
+// under half of an SM's shared memory so that two CTAs share an SM.
+constexpr uint32_t kRC = 0;        // C tile [128 i][128 n], K-major -> X' hi | X' lo [128 j][64 p]
+constexpr uint32_t kRB = 32768;    // B tile [128 j][128 n]: G's B (K-major), S_chunk's A (MN-major)
+constexpr uint32_t kRX = 65536;    // x tile [128 j][64 p]: Y_diag's B (MN-major)
+constexpr uint32_t kRS = 81920;    // S_prev hi | lo [128 n][64 p]: Y_off's B (MN-major)
+constexpr uint32_t kMisc = 114688; // q2[128], warp sums [2][4], 3 mbarriers, TMEM address
+constexpr uint32_t kSmemBytes = kMisc + kQ * 4 + 32 + 24 + 8;
+// TMEM columns
+constexpr uint32_t kTmG = 0;    // G = C B^T (fp32), overwritten in place by M' hi/lo (bf16 pairs)
+constexpr uint32_t kTmY = 128;  // exp(cs_i) Y_off, then + Y_diag
+constexpr uint32_t kTmS = 192;  // S_chunk^T [n][p]
+constexpr uint32_t kTmemCols = 256;
 
 struct SsdArgs {
     const __nv_bfloat16* x;
@@ -82,314 +83,324 @@ __device__ __forceinline__ uint64_t kdesc(uint32_t tile_saddr, int kk) {
     return smem_desc_k128(tile_saddr + (uint32_t)((kk >> 2) * (R * 128) + (kk & 3) * 32));
 }
 
+// MN-major operand descriptor for k-step kk of a tile of 128-byte rows (one
+// row per k); 64-wide MN blocks `lbo` bytes apart.
+__device__ __forceinline__ uint64_t mdesc(uint32_t tile_saddr, int kk, uint32_t lbo) {
+    return smem_desc_mn128(tile_saddr + (uint32_t)kk * 2048u, lbo);
+}
+
+// TMEM column of M' (hi part) for k-step kk: row i's columns j in
+// [64 part + 32 half, +32) are held as 16 packed hi columns followed by 16 lo
+// columns, in place of the 32 fp32 G columns they were computed from.
+__device__ __forceinline__ uint32_t mcol_hi(int kk) {
+    return (uint32_t)(64 * (kk >> 2) + 32 * ((kk >> 1) & 1) + 8 * (kk & 1));
+}
+
 template <typename Tout>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_B,
                    const __grid_constant__ CUtensorMap tm_x, const SsdArgs a) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
-    float* s_cs = reinterpret_cast<float*>(smem + kMisc);
-    float* s_dt = s_cs + kQ;
-    float* s_w = s_dt + kQ;
-    float* s_wsum = s_w + kQ;  // [4] warp totals
-    uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + kMisc + 3 * kQ * 4 + 32);
-    uint64_t* bar_mma = bar_tma + 1;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_mma + 1);
+    float* s_q2 = reinterpret_cast<float*>(smem + kMisc);
+    float* s_wsum = s_q2 + kQ;  // [2][4] per-warpgroup warp totals
+    uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + kMisc + kQ * 4 + 32);
+    uint64_t* bar_mma1 = bar_tma + 1;
+    uint64_t* bar_mma2 = bar_tma + 2;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_tma + 3);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3;   // TMEM lane quarter this warp may access
-    const int part = warp >> 2;     // which part of a row's columns this warp takes
-    const int row = quarter * 32 + lane;  // the TMEM lane (row i, or state n) of this thread
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int part = warp >> 2;    // which half of a row's columns this warpgroup takes
+    const int row = quarter * 32 + lane;  // TMEM lane: row i of G / Y, state n of S
     const int h = blockIdx.x % a.nheads;
     const int b = blockIdx.x / a.nheads;
     const int g = h / (a.nheads / a.ngroups);
     const float Ah = a.A[h];
+    const long long xrow0 = (long long)b * a.seqlen;
+
+    if (sbase & 1023u) {
+        // The swizzled tiles need a 1024-byte-aligned base and there is no
+        // room to realign: make the failure visible instead of computing.
+        const float nanv = __int_as_float(0x7fc00000);
+        for (int t = tid; t < a.seqlen; t += kThreads) {
+            Tout* yr = reinterpret_cast<Tout*>(a.y) + ((xrow0 + t) * a.nheads + h) * kP;
+            for (int p = 0; p < kP; ++p) yr[p] = from_f32<Tout>(nanv);
+        }
+        return;
+    }
 
     if (warp == 0) tmem_alloc(s_tmem, kTmemCols);
     if (tid == 0) {
         mbar_init(bar_tma, 1);
-        mbar_init(bar_mma, 1);
+        mbar_init(bar_mma1, 1);
+        mbar_init(bar_mma2, 1);
         fence_mbar_init();
         prefetch_tensormap(&tm_C);
         prefetch_tensormap(&tm_B);
         prefetch_tensormap(&tm_x);
     }
-    // S_prev = 0: zero both halves of the S operand tile
-    for (int i = tid; i < 32768 / 16; i += kThreads)
-        reinterpret_cast<uint4*>(smem + kRS)[i] = make_uint4(0, 0, 0, 0);
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's lane base
 
-    float S[kPart];  // S_prev[n = row][part * kPart + p]
+    float S[kHalf];  // S_prev[n = row][32 part + q]
 #pragma unroll
-    for (int p = 0; p < kPart; ++p) S[p] = 0.0f;
+    for (int q = 0; q < kHalf; ++q) S[q] = 0.0f;
 
     const int nblocks = (a.seqlen + kQ - 1) / kQ;
-    const long long xrow0 = (long long)b * a.seqlen;
+    constexpr uint32_t kTmaBytes = 2 * 32768 + 16384;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(bar_tma, kTmaBytes);
+        tma_load_4d(smem + kRC, &tm_C, bar_tma, 0, g, 0, b);
+        tma_load_4d(smem + kRC + 16384, &tm_C, bar_tma, 64, g, 0, b);
+        tma_load_4d(smem + kRB, &tm_B, bar_tma, 0, g, 0, b);
+        tma_load_4d(smem + kRB + 16384, &tm_B, bar_tma, 64, g, 0, b);
+        tma_load_3d(smem + kRX, &tm_x, bar_tma, h * kP, 0, b);
+    }
+    // dt of step `row` of the block, loaded one block ahead
+    float dt_next = row < a.seqlen ? a.dt[(xrow0 + row) * a.nheads + h] : 0.0f;
     bool ok = true;
+    bool tma_pending = true;  // (thread 0) a block's loads were issued and not yet seen complete
     uint32_t tma_phase = 0;
-    // dt of this block's step tid, loaded one block ahead
-    float dt_next = (tid < kQ && tid < a.seqlen) ? a.dt[(xrow0 + tid) * a.nheads + h] : 0.0f;
 
-    for (int blk = 0; blk < nblocks && ok; ++blk) {
+    for (int blk = 0; blk < nblocks; ++blk) {
         const int t0 = blk * kQ;
         const int nv = min(kQ, a.seqlen - t0);
+        const uint32_t ph = (uint32_t)(blk & 1);
 
-        if (tid == 0) {
-            mbar_arrive_expect_tx(bar_tma, 5 * 16384);
-            tma_load_4d(smem + kRC, &tm_C, bar_tma, 0, g, t0, b);
-            tma_load_4d(smem + kRC + 16384, &tm_C, bar_tma, 64, g, t0, b);
-            tma_load_4d(smem + kRB, &tm_B, bar_tma, 0, g, t0, b);
-            tma_load_4d(smem + kRB + 16384, &tm_B, bar_tma, 64, g, t0, b);
-            tma_load_3d(smem + kRBT, &tm_x, bar_tma, h * kP, t0, b);
-        }
-
-        // ---- cumulative log-decay of the block (padding steps: dt = 0); the
-        // first warpgroup holds one step per thread
+        // ---- cumulative log-decay cs_i = sum_{j<=i} dt_j A (padding: dt = 0),
+        // computed by both warpgroups for their own rows
         const float dti = dt_next;
-        dt_next = (tid < kQ && t0 + kQ + tid < a.seqlen)
-                      ? a.dt[(xrow0 + t0 + kQ + tid) * a.nheads + h]
-                      : 0.0f;  // padding steps of a partial last block: dt = 0
+        dt_next = (t0 + kQ + row < a.seqlen) ? a.dt[(xrow0 + t0 + kQ + row) * a.nheads + h] : 0.0f;
         float v = dti * Ah;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const float u = __shfl_up_sync(0xffffffffu, v, o);
             if (lane >= o) v += u;
         }
-        if (lane == 31 && warp < 4) s_wsum[warp] = v;
+        if (lane == 31) s_wsum[part * 4 + quarter] = v;
         __syncthreads();
-        if (tid < kQ) {
-            for (int w = 0; w < warp; ++w) v += s_wsum[w];
-            s_cs[tid] = v;
-            s_dt[tid] = dti;
+        float cs_last = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float ws = s_wsum[part * 4 + w];
+            if (w < quarter) v += ws;
+            cs_last += ws;
         }
-        __syncthreads();
-        const float cs_last = s_cs[kQ - 1];
-        if (tid < kQ) s_w[tid] = ex2_approx((cs_last - v) * kLog2e) * dti;
-        const float e_i = ex2_approx(s_cs[row] * kLog2e);
-        const float a_blk = ex2_approx(cs_last * kLog2e);
-        __syncthreads();
+        const float cs2_i = v * kLog2e;           // log2-scaled cs_i
+        const float cs2_last = cs_last * kLog2e;
+        // q2_j = log2(dt_j) - cs_j log2(e): exp(cs_i - cs_j) dt_j = 2^(cs2_i + q2_j)
+        if (part == 0) {
+            float lg;
+            asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(dti));
+            s_q2[row] = lg - cs2_i;
+        }
+        const float e_i = ex2_approx(cs2_i);
+        const float a_blk = ex2_approx(cs2_last);
 
-        // ---- C, B tiles landed?  Then B^T [128 n][128 j] (exact)
-        {
-            const bool got = mbar_wait(bar_tma, tma_phase, nullptr);
-            tma_phase ^= 1;
-            if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
-        }
-        // ---- X^T (exact) and X'^T = (w o X)^T split hi/lo, [64 p][128 j],
-        // from the x tile [128 j][64 p] that TMA put in the B^T region
-        for (int item = tid; item < kP * (kQ / 8); item += kThreads) {
-            const int p = item % kP, jg = item / kP;
-            float xv[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                xv[q] = bf16lo(*reinterpret_cast<const uint16_t*>(
-                    smem + kRBT + kmaj_off<kQ>(jg * 8 + q, p)));
-            float hi[8], lo[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) split_bf16(s_w[jg * 8 + q] * xv[q], hi[q], lo[q]);
-            const uint4 wx = make_uint4(pack_bf16(xv[0], xv[1]), pack_bf16(xv[2], xv[3]),
-                                        pack_bf16(xv[4], xv[5]), pack_bf16(xv[6], xv[7]));
-            const uint4 wh = make_uint4(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]),
-                                        pack_bf16(hi[4], hi[5]), pack_bf16(hi[6], hi[7]));
-            const uint4 wl = make_uint4(pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]),
-                                        pack_bf16(lo[4], lo[5]), pack_bf16(lo[6], lo[7]));
-            const uint32_t off = kmaj_off<kP>(p, jg * 8);
-            *reinterpret_cast<uint4*>(smem + kRX + off) = wx;
-            *reinterpret_cast<uint4*>(smem + kRXP + off) = wh;
-            *reinterpret_cast<uint4*>(smem + kRXP + 16384 + off) = wl;
-        }
-        __syncthreads();  // the x tile is read; B^T overwrites it
-        for (int item = tid; item < kNs * (kQ / 8); item += kThreads) {
-            const int n = item % kNs, jg = item / kNs;
-            uint16_t e[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                e[q] = *reinterpret_cast<const uint16_t*>(smem + kRB + kmaj_off<kQ>(jg * 8 + q, n));
-            const uint4 w4 = make_uint4(e[0] | ((uint32_t)e[1] << 16), e[2] | ((uint32_t)e[3] << 16),
-                                        e[4] | ((uint32_t)e[5] << 16), e[6] | ((uint32_t)e[7] << 16));
-            *reinterpret_cast<uint4*>(smem + kRBT + kmaj_off<kNs>(n, jg * 8)) = w4;
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-
-        // ---- MMA batch 1: G = C B^T, Y_off = C S^T (hi + lo), S_chunk^T = B^T X'^T^T (hi + lo)
+        // ---- MMA batch 1: G = C B^T; Y_off = C S_prev^T (hi + lo; none on block 0)
+        const bool got_tma = mbar_wait(bar_tma, ph, nullptr);
         if (tid == 0) {
-            constexpr uint32_t id128 = idesc_bf16_f32(128, 128);
-            constexpr uint32_t id64 = idesc_bf16_f32(128, 64);
+            if (got_tma) tma_pending = false;
+            tc_fence_after();
+            if (got_tma) {
+                constexpr uint32_t id128 = idesc_bf16_f32(128, 128);
+                constexpr uint32_t id64n = idesc_bf16_f32(128, 64) | kIdescBMN;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tmem + 0, kdesc<kQ>(sbase + kRC, kk), kdesc<kQ>(sbase + kRB, kk), id128,
-                         kk > 0);
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tmem + kTmG, kdesc<kQ>(sbase + kRC, kk), kdesc<kQ>(sbase + kRB, kk),
+                             id128, kk > 0);
+                if (blk > 0) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tmem + 128, kdesc<kQ>(sbase + kRC, kk), kdesc<kP>(sbase + kRS, kk), id64,
-                         kk > 0);
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16(tmem + kTmY, kdesc<kQ>(sbase + kRC, kk),
+                                 mdesc(sbase + kRS, kk, 16384), id64n, kk > 0);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tmem + 128, kdesc<kQ>(sbase + kRC, kk),
-                         kdesc<kP>(sbase + kRS + 16384, kk), id64, 1);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tmem + 192, kdesc<kNs>(sbase + kRBT, kk), kdesc<kP>(sbase + kRXP, kk),
-                         id64, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tmem + 192, kdesc<kNs>(sbase + kRBT, kk),
-                         kdesc<kP>(sbase + kRXP + 16384, kk), id64, 1);
-            mma_commit(bar_mma);
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16(tmem + kTmY, kdesc<kQ>(sbase + kRC, kk),
+                                 mdesc(sbase + kRS + 16384, kk, 16384), id64n, 1);
+                }
+                mma_commit(bar_mma1);
+            }
         }
         {
-            const bool got = mbar_wait(bar_mma, 0, nullptr);
+            const bool got = mbar_wait(bar_mma1, ph, nullptr);
             if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
         }
         tc_fence_after();
 
-        // ---- M' row i = row from G (TMEM cols 0..127) -> hi into RC, lo into RB;
-        // warpgroup `part` takes columns 32 part .. 32 part + 31.  Chunks wholly
-        // above the causal diagonal (all j > i for the warp's rows) are zero.
-        {
-            const float csi = s_cs[row];
-            const int c = part;
-            if (c > quarter) {
+        // ---- X' = w o X (w_j = exp(cs_last - cs_j) dt_j), hi and lo, into the
+        // C region in the x tile's own MN-major layout
 #pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {
-                    const uint32_t off = kmaj_off<kQ>(row, c * 32 + q8 * 8);
-                    *reinterpret_cast<uint4*>(smem + kRC + off) = make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4*>(smem + kRB + off) = make_uint4(0, 0, 0, 0);
-                }
+        for (int r = 0; r < 4; ++r) {
+            const int item = tid + kThreads * r;
+            const int j = item >> 3, c = item & 7;
+            const uint32_t off = (uint32_t)(j * 128 + ((c ^ (j & 7)) << 4));
+            const uint4 xv = *reinterpret_cast<const uint4*>(smem + kRX + off);
+            const float w = ex2_approx(cs2_last + s_q2[j]);
+            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+            uint32_t hp[4], lp[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float h0, l0, h1, l1;
+                split_bf16(bf16lo(xw[e]) * w, h0, l0);
+                split_bf16(bf16hi(xw[e]) * w, h1, l1);
+                hp[e] = pack_bf16(h0, h1);
+                lp[e] = pack_bf16(l0, l1);
+            }
+            *reinterpret_cast<uint4*>(smem + kRC + off) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+            *reinterpret_cast<uint4*>(smem + kRC + 16384 + off) =
+                make_uint4(lp[0], lp[1], lp[2], lp[3]);
+        }
+
+        // ---- M'[i][j] = G[i][j] exp(cs_i - cs_j) dt_j for j <= i, else 0,
+        // split hi/lo and written back over G in TMEM (row i = this lane)
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int c0 = 64 * part + 32 * half;
+            uint32_t hp[16], lp[16];
+            if (2 * part + half > quarter) {  // every j of the chunk is above the diagonal
+#pragma unroll
+                for (int q = 0; q < 16; ++q) hp[q] = lp[q] = 0u;
             } else {
                 float gv[32];
-                tmem_ld32(t_lane + c * 32, gv);
+                tmem_ld32(t_lane + kTmG + c0, gv);
                 tmem_wait_ld();
 #pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {
-                    float hi[8], lo[8];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const int j = c * 32 + q8 * 8 + q;
-                        float m = 0.0f;
-                        if (j <= row) m = gv[q8 * 8 + q] * ex2_approx((csi - s_cs[j]) * kLog2e) * s_dt[j];
-                        split_bf16(m, hi[q], lo[q]);
-                    }
-                    const uint32_t off = kmaj_off<kQ>(row, c * 32 + q8 * 8);
-                    *reinterpret_cast<uint4*>(smem + kRC + off) =
-                        make_uint4(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]),
-                                   pack_bf16(hi[4], hi[5]), pack_bf16(hi[6], hi[7]));
-                    *reinterpret_cast<uint4*>(smem + kRB + off) =
-                        make_uint4(pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]),
-                                   pack_bf16(lo[4], lo[5]), pack_bf16(lo[6], lo[7]));
+                for (int q = 0; q < 32; q += 2) {
+                    const int j = c0 + q;
+                    const float m0 = j <= row ? gv[q] * ex2_approx(cs2_i + s_q2[j]) : 0.0f;
+                    const float m1 = j + 1 <= row ? gv[q + 1] * ex2_approx(cs2_i + s_q2[j + 1]) : 0.0f;
+                    float h0, l0, h1, l1;
+                    split_bf16(m0, h0, l0);
+                    split_bf16(m1, h1, l1);
+                    hp[q >> 1] = pack_bf16(h0, h1);
+                    lp[q >> 1] = pack_bf16(l0, l1);
                 }
             }
+            tmem_st16(t_lane + kTmG + c0, hp);
+            tmem_st16(t_lane + kTmG + c0 + 16, lp);
         }
-        // ---- state: S_prev[n = row][part * kPart + :] = exp(cs_last) S_prev + S_chunk^T;
-        // staged as fp32 rows (16-byte chunks XOR-swizzled by n mod 8) in RBT
-        {
-            float sc[kPart];
-            tmem_ld16(t_lane + 192 + part * kPart, sc);
+
+        // ---- scale Y_off rows by exp(cs_i) in place; Y_diag accumulates onto it
+        if (blk > 0) {
+            float yo[kHalf];
+            tmem_ld32(t_lane + kTmY + kHalf * part, yo);
             tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < kPart; ++q) S[q] = fmaf(a_blk, S[q], sc[q]);
-            float* st = reinterpret_cast<float*>(smem + kRBT) + row * kP;
-#pragma unroll
-            for (int c4 = 0; c4 < kPart / 4; ++c4)
-                reinterpret_cast<float4*>(st)[(part * (kPart / 4) + c4) ^ (row & 7)] =
-                    make_float4(S[4 * c4], S[4 * c4 + 1], S[4 * c4 + 2], S[4 * c4 + 3]);
+            for (int q = 0; q < kHalf; ++q) yo[q] *= e_i;
+            tmem_st32f(t_lane + kTmY + kHalf * part, yo);
         }
+        tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        tc_fence_after();
 
-        // ---- MMA batch 2: Y_diag = M' X (hi + lo) into TMEM cols 0..63
+        // ---- MMA batch 2: S_chunk^T = B^T X' (hi + lo); Y += M' X (hi + lo)
         if (tid == 0) {
-            constexpr uint32_t id64 = idesc_bf16_f32(128, 64);
+            tc_fence_after();
+            constexpr uint32_t idS = idesc_bf16_f32(128, 64) | kIdescAMN | kIdescBMN;
+            constexpr uint32_t idY = idesc_bf16_f32(128, 64) | kIdescBMN;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tmem + 0, kdesc<kQ>(sbase + kRC, kk), kdesc<kP>(sbase + kRX, kk), id64,
-                         kk > 0);
+                mma_bf16(tmem + kTmS, mdesc(sbase + kRB, kk, 16384), mdesc(sbase + kRC, kk, 16384),
+                         idS, kk > 0);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tmem + 0, kdesc<kQ>(sbase + kRB, kk), kdesc<kP>(sbase + kRX, kk), id64, 1);
-            mma_commit(bar_mma);
-        }
-
-        // ---- S operand for the next block: [64 p][128 n] hi/lo from the staging
-        for (int item = tid; item < kP * (kNs / 8); item += kThreads) {
-            const int p = item % kP, ng = item / kP;
-            float hi[8], lo[8];
+                mma_bf16(tmem + kTmS, mdesc(sbase + kRB, kk, 16384),
+                         mdesc(sbase + kRC + 16384, kk, 16384), idS, 1);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int n = ng * 8 + q;
-                const float* st = reinterpret_cast<const float*>(smem + kRBT) + n * kP;
-                const float sv = st[(((p >> 2) ^ (n & 7)) << 2) | (p & 3)];
-                split_bf16(sv, hi[q], lo[q]);
-            }
-            const uint32_t off = kmaj_off<kP>(p, ng * 8);
-            *reinterpret_cast<uint4*>(smem + kRS + off) =
-                make_uint4(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]),
-                           pack_bf16(hi[4], hi[5]), pack_bf16(hi[6], hi[7]));
-            *reinterpret_cast<uint4*>(smem + kRS + 16384 + off) =
-                make_uint4(pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]),
-                           pack_bf16(lo[4], lo[5]), pack_bf16(lo[6], lo[7]));
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16_ta(tmem + kTmY, tmem + kTmG + mcol_hi(kk), mdesc(sbase + kRX, kk, 16384),
+                            idY, (blk > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16_ta(tmem + kTmY, tmem + kTmG + mcol_hi(kk) + 16,
+                            mdesc(sbase + kRX, kk, 16384), idY, 1);
+            mma_commit(bar_mma2);
         }
-
         {
-            const bool got = mbar_wait(bar_mma, 1, nullptr);
+            const bool got = mbar_wait(bar_mma2, ph, nullptr);
             if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
         }
         tc_fence_after();
 
-        // ---- y[i = row][part * kPart + :] = Y_diag + exp(cs_i) Y_off
+        // ---- the C, B, x regions are free: start the next block's loads
+        if (tid == 0 && blk + 1 < nblocks) {
+            const int tn = t0 + kQ;
+            mbar_arrive_expect_tx(bar_tma, kTmaBytes);
+            tma_load_4d(smem + kRC, &tm_C, bar_tma, 0, g, tn, b);
+            tma_load_4d(smem + kRC + 16384, &tm_C, bar_tma, 64, g, tn, b);
+            tma_load_4d(smem + kRB, &tm_B, bar_tma, 0, g, tn, b);
+            tma_load_4d(smem + kRB + 16384, &tm_B, bar_tma, 64, g, tn, b);
+            tma_load_3d(smem + kRX, &tm_x, bar_tma, h * kP, tn, b);
+            tma_pending = true;
+            tma_phase = (uint32_t)((blk + 1) & 1);
+        }
+
+        // ---- state: S_prev[n = row][32 part + :] = exp(cs_last) S_prev + S_chunk^T,
+        // and its hi/lo operand for the next block (row n, p contiguous)
         {
-            float yd[kPart], yo[kPart];
-            Tout* yrow = reinterpret_cast<Tout*>(a.y) + ((xrow0 + t0 + row) * a.nheads + h) * kP;
-            {
-                const int c = part;
-                tmem_ld16(t_lane + c * kPart, yd);
-                tmem_ld16(t_lane + 128 + c * kPart, yo);
-                tmem_wait_ld();
-                if (row < nv) {
-                    if constexpr (sizeof(Tout) == 4) {
+            float sc[kHalf];
+            tmem_ld32(t_lane + kTmS + kHalf * part, sc);
+            tmem_wait_ld();
 #pragma unroll
-                        for (int q = 0; q < kPart; q += 4)
-                            *reinterpret_cast<float4*>(reinterpret_cast<float*>(yrow) + c * kPart + q) =
-                                make_float4(fmaf(e_i, yo[q], yd[q]), fmaf(e_i, yo[q + 1], yd[q + 1]),
-                                            fmaf(e_i, yo[q + 2], yd[q + 2]),
-                                            fmaf(e_i, yo[q + 3], yd[q + 3]));
-                    } else {
+            for (int q = 0; q < kHalf; ++q) S[q] = fmaf(a_blk, S[q], sc[q]);
 #pragma unroll
-                        for (int q = 0; q < kPart; q += 8)
-                            *reinterpret_cast<uint4*>(yrow + c * kPart + q) = make_uint4(
-                                pack_bf16(fmaf(e_i, yo[q], yd[q]), fmaf(e_i, yo[q + 1], yd[q + 1])),
-                                pack_bf16(fmaf(e_i, yo[q + 2], yd[q + 2]),
-                                          fmaf(e_i, yo[q + 3], yd[q + 3])),
-                                pack_bf16(fmaf(e_i, yo[q + 4], yd[q + 4]),
-                                          fmaf(e_i, yo[q + 5], yd[q + 5])),
-                                pack_bf16(fmaf(e_i, yo[q + 6], yd[q + 6]),
-                                          fmaf(e_i, yo[q + 7], yd[q + 7])));
-                    }
+            for (int c4 = 0; c4 < 4; ++c4) {
+                float hi[8], lo[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) split_bf16(S[8 * c4 + e], hi[e], lo[e]);
+                const uint32_t off = (uint32_t)(row * 128 + (((part * 4 + c4) ^ (row & 7)) << 4));
+                *reinterpret_cast<uint4*>(smem + kRS + off) =
+                    make_uint4(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]),
+                               pack_bf16(hi[4], hi[5]), pack_bf16(hi[6], hi[7]));
+                *reinterpret_cast<uint4*>(smem + kRS + 16384 + off) =
+                    make_uint4(pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]),
+                               pack_bf16(lo[4], lo[5]), pack_bf16(lo[6], lo[7]));
+            }
+        }
+
+        // ---- y[i = row][32 part + :] = Y
+        {
+            float yv[kHalf];
+            tmem_ld32(t_lane + kTmY + kHalf * part, yv);
+            tmem_wait_ld();
+            if (row < nv) {
+                Tout* yrow = reinterpret_cast<Tout*>(a.y) + ((xrow0 + t0 + row) * a.nheads + h) * kP +
+                             kHalf * part;
+                if constexpr (sizeof(Tout) == 4) {
+#pragma unroll
+                    for (int q = 0; q < kHalf; q += 4)
+                        *reinterpret_cast<float4*>(reinterpret_cast<float*>(yrow) + q) =
+                            make_float4(yv[q], yv[q + 1], yv[q + 2], yv[q + 3]);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < kHalf; q += 8)
+                        *reinterpret_cast<uint4*>(yrow + q) =
+                            make_uint4(pack_bf16(yv[q], yv[q + 1]), pack_bf16(yv[q + 2], yv[q + 3]),
+                                       pack_bf16(yv[q + 4], yv[q + 5]), pack_bf16(yv[q + 6], yv[q + 7]));
                 }
             }
         }
-        fence_proxy_async_smem();  // generic reads/writes before the next block's TMA
+        fence_proxy_async_smem();  // S operand writes before the next block's MMAs
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
     }
 
-    // ---- final state [b][h][p = part * kPart + :][n = row]
+    // ---- final state [b][h][p = 32 part + :][n = row]
     if (ok && a.final_state) {
-        float* fs = a.final_state + ((long long)(b * a.nheads + h) * kP + part * kPart) * kNs + row;
+        float* fs = a.final_state + ((long long)(b * a.nheads + h) * kP + kHalf * part) * kNs + row;
 #pragma unroll
-        for (int p = 0; p < kPart; ++p) fs[p * kNs] = S[p];
+        for (int q = 0; q < kHalf; ++q) fs[q * kNs] = S[q];
+    }
+    if (tid == 0 && tma_pending) {
+        // never leave with a load still landing in shared memory (bounded)
+        (void)mbar_wait(bar_tma, tma_phase, nullptr);
     }
     tc_fence_before();
     __syncthreads();
@@ -431,11 +442,11 @@ template <typename Tout>
 ssm_status_t launch(const CUtensorMap& mc, const CUtensorMap& mb, const CUtensorMap& mx,
                     const SsdArgs& a, cudaStream_t s) {
     auto kern = ssd_fwd_kernel<Tout>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
         cudaSuccess)
         return SSM_ERR_CUDA;
     const unsigned grid = (unsigned)(a.batch * a.nheads);
-    kern<<<grid, kThreads, kSmemAlloc, s>>>(mc, mb, mx, a);
+    kern<<<grid, kThreads, kSmemBytes, s>>>(mc, mb, mx, a);
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 

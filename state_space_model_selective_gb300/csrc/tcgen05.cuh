@@ -74,6 +74,30 @@ __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Store 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
+// Store 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float* v) {
+    uint32_t r[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
+    tmem_st16(taddr, r);
+    tmem_st16(taddr + 16, r + 16);
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // ------------------------------------------------------ descriptors
 
 // Shared-memory matrix descriptor of a K-major operand tile stored in the
@@ -93,12 +117,45 @@ __device__ __forceinline__ uint64_t smem_desc_k128(uint32_t saddr) {
     return d;
 }
 
+// Shared-memory matrix descriptor of an MN-major operand tile in the
+// 128-byte-swizzle layout: each row holds 64 consecutive bf16 of M (or N) for
+// one k, rows 128 bytes apart, groups of 8 rows (k) 1024 bytes apart (stride
+// byte offset); further 64-wide M (N) blocks `lbo` bytes apart (leading byte
+// offset).  Tile base 1024-byte aligned; advancing K by 16 moves the start by
+// 2048 bytes.
+__device__ __forceinline__ uint64_t smem_desc_mn128(uint32_t saddr, uint32_t lbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)2u << 61;
+    return d;
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A
 // and B (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
            ((uint32_t)(M >> 4) << 24);
+}
+
+// Transpose flags of the instruction descriptor: bit 15 = A is MN-major,
+// bit 16 = B is MN-major.
+constexpr uint32_t kIdescAMN = 1u << 15;
+constexpr uint32_t kIdescBMN = 1u << 16;
+
+// D[tmem] (+)= A[tmem] * B[smem]^T with A read from tensor memory (row m in
+// lane m, two bf16 of K per 32-bit column, lower k in the low half).
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, one 128 x N x 16 MMA, issued by one thread.

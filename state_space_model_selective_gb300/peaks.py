@@ -88,6 +88,50 @@ def measure(iters: int = 20000, reps: int = 3) -> dict:
             cyc = e0.elapsed_time(e1) / 1e3 * mhz * 1e6 / steps
             mix[f"ns{ns}_{wps}warp_per_smsp"] = cyc / (wps * 32 * ns)  # cycles per element
     res["scan_step_mix"] = mix
+    # full per-element arithmetic, scalar vs packed fp32x2 (cycles per element
+    # per sub-partition; 4 MUFU cycles per 32 elements = 0.125)
+    lib.ssm_scan_mix2_probe.restype = ctypes.c_double
+    lib.ssm_scan_mix2_probe.argtypes = [ctypes.c_int] * 5 + [ctypes.c_void_p, ctypes.c_void_p]
+    mix2 = {}
+    for packed in (0, 1):
+        for ns in (4, 8, 16):
+            for wps in (1, 2, 4):
+                steps = 4000
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                lib.ssm_scan_mix2_probe(ns, packed, sms * 4 * wps, 32, 100,
+                                        ctypes.c_void_p(out.data_ptr()),
+                                        ctypes.c_void_p(stream.cuda_stream))
+                e0.record(stream)
+                lib.ssm_scan_mix2_probe(ns, packed, sms * 4 * wps, 32, steps,
+                                        ctypes.c_void_p(out.data_ptr()),
+                                        ctypes.c_void_p(stream.cuda_stream))
+                e1.record(stream)
+                torch.cuda.synchronize()
+                mhz = _sm_clock_mhz() or 2070.0
+                cyc = e0.elapsed_time(e1) / 1e3 * mhz * 1e6 / steps
+                mix2[f"{'x2' if packed else 'f32'}_ns{ns}_{wps}warp_per_smsp"] = cyc / (wps * 32 * ns)
+    res["scan_full_mix"] = mix2
+    # shared-memory load cost by width and address pattern: SM clocks per
+    # warp-wide load instruction (1 = one 128-byte wavefront per clock)
+    lib.ssm_lds_probe.restype = ctypes.c_double
+    lib.ssm_lds_probe.argtypes = [ctypes.c_int] * 5 + [ctypes.c_void_p, ctypes.c_void_p]
+    lds = {}
+    names = {0: "same_addr", 1: "4addr_lane_mod4", 2: "4addr_per_quarter", 3: "32addr"}
+    for width in (4, 8, 16):
+        for pattern in (0, 1, 2, 3):
+            its = 4000
+            lib.ssm_lds_probe(width, pattern, sms * 4, 512, 50, ctypes.c_void_p(out.data_ptr()),
+                              ctypes.c_void_p(stream.cuda_stream))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            n = lib.ssm_lds_probe(width, pattern, sms * 4, 512, its,
+                                  ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(stream.cuda_stream))
+            e1.record(stream)
+            torch.cuda.synchronize()
+            mhz = _sm_clock_mhz() or 2070.0
+            clocks = e0.elapsed_time(e1) / 1e3 * mhz * 1e6
+            lds[f"lds{width * 8}_{names[pattern]}"] = clocks * sms / n
+    res["lds_clocks_per_warp_load"] = lds
     lib.ssm_latency_probe.restype = ctypes.c_float
     lib.ssm_latency_probe.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
     lat = {}
