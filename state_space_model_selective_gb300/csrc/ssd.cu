@@ -52,8 +52,8 @@ constexpr uint32_t kMisc = 114688; // q2[128], warp sums [2][4], 3 mbarriers, TM
 constexpr uint32_t kSmemBytes = kMisc + kQ * 4 + 32 + 24 + 8;
 // TMEM columns
 constexpr uint32_t kTmG = 0;    // G = C B^T (fp32), overwritten in place by M' hi/lo (bf16 pairs)
-constexpr uint32_t kTmY = 128;  // exp(cs_i) Y_off, then + Y_diag
-constexpr uint32_t kTmS = 192;  // S_chunk^T [n][p]
+constexpr uint32_t kTmY = 128;  // C S_hi^T | C S_lo^T (128 columns), then exp(cs_i) Y_off + Y_diag (64)
+constexpr uint32_t kTmS = 192;  // S_chunk^T [n][p], once the C S_lo^T half has been read
 constexpr uint32_t kTmemCols = 256;
 
 struct SsdArgs {
@@ -65,16 +65,38 @@ struct SsdArgs {
     int batch, seqlen, nheads, ngroups;
 };
 
+// Two fp32 values rounded to nearest-even bf16 and packed (a in the low half),
+// one conversion instruction.
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
-    const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(b));
-    return lo | (hi << 16);
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// v = hi + lo with hi = bf16(v), lo = bf16(v - hi); returns (hi, lo) as floats
-__device__ __forceinline__ void split_bf16(float v, float& hi, float& lo) {
-    hi = __bfloat162float(__float2bfloat16_rn(v));
-    lo = v - hi;
+// (a, b) = hi + lo with hi = bf16(v), lo = bf16(v - hi) (about 16 significant
+// bits in all), returned as the packed hi pair and the packed lo pair.
+__device__ __forceinline__ void split2_bf16(float a, float b, uint32_t& hp, uint32_t& lp) {
+    hp = pack_bf16(a, b);
+    lp = pack_bf16(a - bf16lo(hp), b - bf16hi(hp));
+}
+
+// One 32-column chunk of M' for row i: m_j = G[i][j] 2^(cs2_i + q2_j), with
+// j > i zeroed when MASK (the diagonal chunk; jmax = i - first column).
+template <bool MASK>
+__device__ __forceinline__ void mprime_chunk(const float* gv, const float* q2c, float cs2_i, int jmax,
+                                             uint32_t* hp, uint32_t* lp) {
+#pragma unroll
+    for (int q = 0; q < 32; q += 4) {
+        const float4 qq = *reinterpret_cast<const float4*>(q2c + q);
+        const float qv[4] = {qq.x, qq.y, qq.z, qq.w};
+        float m[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            m[k] = gv[q + k] * ex2_approx(cs2_i + qv[k]);
+            if (MASK && q + k > jmax) m[k] = 0.0f;
+        }
+        split2_bf16(m[0], m[1], hp[q >> 1], lp[q >> 1]);
+        split2_bf16(m[2], m[3], hp[(q >> 1) + 1], lp[(q >> 1) + 1]);
+    }
 }
 
 // K-major operand descriptor for k-step kk (16 bf16) of a tile with R rows.
@@ -99,7 +121,8 @@ __device__ __forceinline__ uint32_t mcol_hi(int kk) {
 template <typename Tout>
 __global__ void __launch_bounds__(kThreads, 2)
     ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_B,
-                   const __grid_constant__ CUtensorMap tm_x, const SsdArgs a) {
+                   const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
+                   const SsdArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
     float* s_q2 = reinterpret_cast<float*>(smem + kMisc);
@@ -139,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         prefetch_tensormap(&tm_C);
         prefetch_tensormap(&tm_B);
         prefetch_tensormap(&tm_x);
+        prefetch_tensormap(&tm_y);
     }
     tc_fence_before();
     __syncthreads();
@@ -208,20 +232,16 @@ __global__ void __launch_bounds__(kThreads, 2)
             tc_fence_after();
             if (got_tma) {
                 constexpr uint32_t id128 = idesc_bf16_f32(128, 128);
-                constexpr uint32_t id64n = idesc_bf16_f32(128, 64) | kIdescBMN;
+                constexpr uint32_t id128n = idesc_bf16_f32(128, 128) | kIdescBMN;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_bf16(tmem + kTmG, kdesc<kQ>(sbase + kRC, kk), kdesc<kQ>(sbase + kRB, kk),
                              id128, kk > 0);
-                if (blk > 0) {
+                if (blk > 0) {  // N = 128: S_hi in columns 0..63, S_lo in 64..127
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         mma_bf16(tmem + kTmY, kdesc<kQ>(sbase + kRC, kk),
-                                 mdesc(sbase + kRS, kk, 16384), id64n, kk > 0);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_bf16(tmem + kTmY, kdesc<kQ>(sbase + kRC, kk),
-                                 mdesc(sbase + kRS + 16384, kk, 16384), id64n, 1);
+                                 mdesc(sbase + kRS, kk, 16384), id128n, kk > 0);
                 }
                 mma_commit(bar_mma1);
             }
@@ -244,54 +264,46 @@ __global__ void __launch_bounds__(kThreads, 2)
             const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
             uint32_t hp[4], lp[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float h0, l0, h1, l1;
-                split_bf16(bf16lo(xw[e]) * w, h0, l0);
-                split_bf16(bf16hi(xw[e]) * w, h1, l1);
-                hp[e] = pack_bf16(h0, h1);
-                lp[e] = pack_bf16(l0, l1);
-            }
+            for (int e = 0; e < 4; ++e) split2_bf16(bf16lo(xw[e]) * w, bf16hi(xw[e]) * w, hp[e], lp[e]);
             *reinterpret_cast<uint4*>(smem + kRC + off) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
             *reinterpret_cast<uint4*>(smem + kRC + 16384 + off) =
                 make_uint4(lp[0], lp[1], lp[2], lp[3]);
         }
 
         // ---- M'[i][j] = G[i][j] exp(cs_i - cs_j) dt_j for j <= i, else 0,
-        // split hi/lo and written back over G in TMEM (row i = this lane)
+        // split hi/lo and written back over G in TMEM (row i = this lane).
+        // 32-column chunk k of this warpgroup is wholly above the diagonal for
+        // k > quarter, on it for k == quarter, below it otherwise.
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-            const int c0 = 64 * part + 32 * half;
+            const int ck = 2 * part + half;
+            const int c0 = 32 * ck;
             uint32_t hp[16], lp[16];
-            if (2 * part + half > quarter) {  // every j of the chunk is above the diagonal
+            if (ck > quarter) {
 #pragma unroll
                 for (int q = 0; q < 16; ++q) hp[q] = lp[q] = 0u;
             } else {
                 float gv[32];
                 tmem_ld32(t_lane + kTmG + c0, gv);
                 tmem_wait_ld();
-#pragma unroll
-                for (int q = 0; q < 32; q += 2) {
-                    const int j = c0 + q;
-                    const float m0 = j <= row ? gv[q] * ex2_approx(cs2_i + s_q2[j]) : 0.0f;
-                    const float m1 = j + 1 <= row ? gv[q + 1] * ex2_approx(cs2_i + s_q2[j + 1]) : 0.0f;
-                    float h0, l0, h1, l1;
-                    split_bf16(m0, h0, l0);
-                    split_bf16(m1, h1, l1);
-                    hp[q >> 1] = pack_bf16(h0, h1);
-                    lp[q >> 1] = pack_bf16(l0, l1);
-                }
+                if (ck == quarter)
+                    mprime_chunk<true>(gv, s_q2 + c0, cs2_i, lane, hp, lp);
+                else
+                    mprime_chunk<false>(gv, s_q2 + c0, cs2_i, 31, hp, lp);
             }
             tmem_st16(t_lane + kTmG + c0, hp);
             tmem_st16(t_lane + kTmG + c0 + 16, lp);
         }
 
-        // ---- scale Y_off rows by exp(cs_i) in place; Y_diag accumulates onto it
+        // ---- Y_off = (C S_hi^T + C S_lo^T) scaled by exp(cs_i), into the first 64
+        // of its 128 columns; Y_diag accumulates onto it
         if (blk > 0) {
-            float yo[kHalf];
+            float yo[kHalf], yl[kHalf];
             tmem_ld32(t_lane + kTmY + kHalf * part, yo);
+            tmem_ld32(t_lane + kTmY + kP + kHalf * part, yl);
             tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < kHalf; ++q) yo[q] *= e_i;
+            for (int q = 0; q < kHalf; ++q) yo[q] = (yo[q] + yl[q]) * e_i;
             tmem_st32f(t_lane + kTmY + kHalf * part, yo);
         }
         tmem_wait_st();
@@ -341,50 +353,58 @@ __global__ void __launch_bounds__(kThreads, 2)
             tma_phase = (uint32_t)((blk + 1) & 1);
         }
 
-        // ---- state: S_prev[n = row][32 part + :] = exp(cs_last) S_prev + S_chunk^T,
-        // and its hi/lo operand for the next block (row n, p contiguous)
-        {
-            float sc[kHalf];
-            tmem_ld32(t_lane + kTmS + kHalf * part, sc);
-            tmem_wait_ld();
-#pragma unroll
-            for (int q = 0; q < kHalf; ++q) S[q] = fmaf(a_blk, S[q], sc[q]);
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-                float hi[8], lo[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) split_bf16(S[8 * c4 + e], hi[e], lo[e]);
-                const uint32_t off = (uint32_t)(row * 128 + (((part * 4 + c4) ^ (row & 7)) << 4));
-                *reinterpret_cast<uint4*>(smem + kRS + off) =
-                    make_uint4(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]),
-                               pack_bf16(hi[4], hi[5]), pack_bf16(hi[6], hi[7]));
-                *reinterpret_cast<uint4*>(smem + kRS + 16384 + off) =
-                    make_uint4(pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]),
-                               pack_bf16(lo[4], lo[5]), pack_bf16(lo[6], lo[7]));
-            }
-        }
-
-        // ---- y[i = row][32 part + :] = Y
+        // ---- rows of Y and of S_chunk^T out of tensor memory
+        float sc[kHalf];
         {
             float yv[kHalf];
             tmem_ld32(t_lane + kTmY + kHalf * part, yv);
+            tmem_ld32(t_lane + kTmS + kHalf * part, sc);
             tmem_wait_ld();
-            if (row < nv) {
-                Tout* yrow = reinterpret_cast<Tout*>(a.y) + ((xrow0 + t0 + row) * a.nheads + h) * kP +
-                             kHalf * part;
-                if constexpr (sizeof(Tout) == 4) {
+            // y tile staged in the S region in the tensor-store layout (128-byte
+            // rows, 16-byte chunks XOR-swizzled by row mod 8): fp32 as two
+            // [128 t][32 p] boxes, bf16 as one [128 t][64 p] box
+            if constexpr (sizeof(Tout) == 4) {
+                uint8_t* box = smem + kRS + part * 16384 + row * 128;
 #pragma unroll
-                    for (int q = 0; q < kHalf; q += 4)
-                        *reinterpret_cast<float4*>(reinterpret_cast<float*>(yrow) + q) =
-                            make_float4(yv[q], yv[q + 1], yv[q + 2], yv[q + 3]);
-                } else {
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<float4*>(box + ((c ^ (row & 7)) << 4)) =
+                        make_float4(yv[4 * c], yv[4 * c + 1], yv[4 * c + 2], yv[4 * c + 3]);
+            } else {
 #pragma unroll
-                    for (int q = 0; q < kHalf; q += 8)
-                        *reinterpret_cast<uint4*>(yrow + q) =
-                            make_uint4(pack_bf16(yv[q], yv[q + 1]), pack_bf16(yv[q + 2], yv[q + 3]),
-                                       pack_bf16(yv[q + 4], yv[q + 5]), pack_bf16(yv[q + 6], yv[q + 7]));
-                }
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4*>(smem + kRS + row * 128 +
+                                              (((part * 4 + c) ^ (row & 7)) << 4)) =
+                        make_uint4(pack_bf16(yv[8 * c], yv[8 * c + 1]),
+                                   pack_bf16(yv[8 * c + 2], yv[8 * c + 3]),
+                                   pack_bf16(yv[8 * c + 4], yv[8 * c + 5]),
+                                   pack_bf16(yv[8 * c + 6], yv[8 * c + 7]));
             }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, kThreads);
+        if (tid == 0) {
+            // rows past the sequence end are clipped by the tensor store
+            tma_store_3d(&tm_y, smem + kRS, h * kP, t0, b);
+            if constexpr (sizeof(Tout) == 4) tma_store_3d(&tm_y, smem + kRS + 16384, h * kP + 32, t0, b);
+            bulk_commit();
+            bulk_wait_read_all();
+        }
+
+        // ---- state: S_prev[n = row][32 part + :] = exp(cs_last) S_prev + S_chunk^T,
+        // then (once the store has read the y tile) its hi/lo operand for the
+        // next block (row n, p contiguous)
+#pragma unroll
+        for (int q = 0; q < kHalf; ++q) S[q] = fmaf(a_blk, S[q], sc[q]);
+        named_bar_sync(1, kThreads);
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+            uint32_t hp[4], lp[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                split2_bf16(S[8 * c4 + 2 * e], S[8 * c4 + 2 * e + 1], hp[e], lp[e]);
+            const uint32_t off = (uint32_t)(row * 128 + (((part * 4 + c4) ^ (row & 7)) << 4));
+            *reinterpret_cast<uint4*>(smem + kRS + off) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+            *reinterpret_cast<uint4*>(smem + kRS + 16384 + off) = make_uint4(lp[0], lp[1], lp[2], lp[3]);
         }
         fence_proxy_async_smem();  // S operand writes before the next block's MMAs
         tc_fence_before();
@@ -398,9 +418,11 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int q = 0; q < kHalf; ++q) fs[q * kNs] = S[q];
     }
-    if (tid == 0 && tma_pending) {
-        // never leave with a load still landing in shared memory (bounded)
-        (void)mbar_wait(bar_tma, tma_phase, nullptr);
+    if (tid == 0) {
+        // never leave with a load still landing in shared memory (bounded), nor
+        // with a tensor store still in flight
+        if (tma_pending) (void)mbar_wait(bar_tma, tma_phase, nullptr);
+        bulk_wait_all();
     }
     tc_fence_before();
     __syncthreads();
@@ -438,15 +460,32 @@ bool make_x_map(CUtensorMap* map, const void* base, int batch, int seqlen, int n
            CUDA_SUCCESS;
 }
 
+// y (batch, seqlen, nheads, headdim) as 3-D {nheads * headdim, seqlen, batch};
+// boxes of 128 bytes x 128 steps (32 fp32 or 64 bf16 of a head's row).
+bool make_y_map(CUtensorMap* map, void* base, int batch, int seqlen, int nheads, bool f32) {
+    ssm_host::EncodeTiledFn fn = ssm_host::encode_tiled_fn();
+    if (!fn) return false;
+    const cuuint64_t es = f32 ? 4 : 2;
+    const cuuint64_t dims[3] = {(cuuint64_t)nheads * kP, (cuuint64_t)seqlen, (cuuint64_t)batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)nheads * kP * es,
+                                   (cuuint64_t)seqlen * nheads * kP * es};
+    const cuuint32_t box[3] = {(cuuint32_t)(128 / es), (cuuint32_t)kQ, 1};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    return fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base,
+              dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename Tout>
 ssm_status_t launch(const CUtensorMap& mc, const CUtensorMap& mb, const CUtensorMap& mx,
-                    const SsdArgs& a, cudaStream_t s) {
+                    const CUtensorMap& my, const SsdArgs& a, cudaStream_t s) {
     auto kern = ssd_fwd_kernel<Tout>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
         cudaSuccess)
         return SSM_ERR_CUDA;
     const unsigned grid = (unsigned)(a.batch * a.nheads);
-    kern<<<grid, kThreads, kSmemBytes, s>>>(mc, mb, mx, a);
+    kern<<<grid, kThreads, kSmemBytes, s>>>(mc, mb, mx, my, a);
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
@@ -491,9 +530,10 @@ extern "C" ssm_status_t ssd_chunked_fwd(const void* x, const float* dt, const fl
         if (overlaps(y, yb, r.p, r.n) || overlaps(final_state, fb, r.p, r.n)) return SSM_ERR_ALIAS;
     if (overlaps(y, yb, final_state, fb)) return SSM_ERR_ALIAS;
 
-    CUtensorMap mc, mb, mx;
+    CUtensorMap mc, mb, mx, my;
     if (!make_bc_map(&mc, C, batch, seqlen, ngroups) || !make_bc_map(&mb, B, batch, seqlen, ngroups) ||
-        !make_x_map(&mx, x, batch, seqlen, nheads))
+        !make_x_map(&mx, x, batch, seqlen, nheads) ||
+        !make_y_map(&my, y, batch, seqlen, nheads, out_dtype == SSM_F32))
         return SSM_ERR_CUDA;
     SsdArgs a{};
     a.x = static_cast<const __nv_bfloat16*>(x);
@@ -505,6 +545,6 @@ extern "C" ssm_status_t ssd_chunked_fwd(const void* x, const float* dt, const fl
     a.seqlen = seqlen;
     a.nheads = nheads;
     a.ngroups = ngroups;
-    return out_dtype == SSM_BF16 ? launch<__nv_bfloat16>(mc, mb, mx, a, s)
-                                 : launch<float>(mc, mb, mx, a, s);
+    return out_dtype == SSM_BF16 ? launch<__nv_bfloat16>(mc, mb, mx, my, a, s)
+                                 : launch<float>(mc, mb, mx, my, a, s);
 }
