@@ -48,8 +48,8 @@ constexpr uint32_t kRC = 0;        // C tile [128 i][128 n], K-major -> X' hi | 
 constexpr uint32_t kRB = 32768;    // B tile [128 j][128 n]: G's B (K-major), S_chunk's A (MN-major)
 constexpr uint32_t kRX = 65536;    // x tile [128 j][64 p]: Y_diag's B (MN-major)
 constexpr uint32_t kRS = 81920;    // S_prev hi | lo [128 n][64 p]: Y_off's B (MN-major)
-constexpr uint32_t kMisc = 114688; // q2[128], warp sums [2][4], 3 mbarriers, TMEM address
-constexpr uint32_t kSmemBytes = kMisc + kQ * 4 + 32 + 24 + 8;
+constexpr uint32_t kMisc = 114688; // q2[128], warp sums [2][4], 6 mbarriers, TMEM address
+constexpr uint32_t kSmemBytes = kMisc + kQ * 4 + 32 + 48 + 8;
 // TMEM columns
 constexpr uint32_t kTmG = 0;    // G = C B^T (fp32), overwritten in place by M' hi/lo (bf16 pairs)
 constexpr uint32_t kTmY = 128;  // C S_hi^T | C S_lo^T (128 columns), then exp(cs_i) Y_off + Y_diag (64)
@@ -121,48 +121,59 @@ __device__ __forceinline__ uint32_t mcol_hi(int kk) {
 template <typename Tout>
 __global__ void __launch_bounds__(kThreads, 2)
     ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_B,
-                   const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
-                   const SsdArgs a) {
+                   const __grid_constant__ CUtensorMap tm_x, const SsdArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
     float* s_q2 = reinterpret_cast<float*>(smem + kMisc);
     float* s_wsum = s_q2 + kQ;  // [2][4] per-warpgroup warp totals
-    uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + kMisc + kQ * 4 + 32);
-    uint64_t* bar_mma1 = bar_tma + 1;
-    uint64_t* bar_mma2 = bar_tma + 2;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_tma + 3);
+    uint64_t* bar_cb = reinterpret_cast<uint64_t*>(smem + kMisc + kQ * 4 + 32);  // C, B tiles in
+    uint64_t* bar_x = bar_cb + 1;      // x tile in
+    uint64_t* bar_g = bar_cb + 2;      // G = C B^T done
+    uint64_t* bar_yoff = bar_cb + 3;   // Y_off done (committed every step, empty on block 0)
+    uint64_t* bar_s = bar_cb + 4;      // S_chunk done: the B and X' (C) regions are free
+    uint64_t* bar_mma2 = bar_cb + 5;   // Y_diag done: the x region is free
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_cb + 6);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int part = warp >> 2;    // which half of a row's columns this warpgroup takes
     const int row = quarter * 32 + lane;  // TMEM lane: row i of G / Y, state n of S
-    const int h = blockIdx.x % a.nheads;
-    const int b = blockIdx.x / a.nheads;
-    const int g = h / (a.nheads / a.ngroups);
-    const float Ah = a.A[h];
-    const long long xrow0 = (long long)b * a.seqlen;
+    // Work items are (batch, head) pairs blockIdx.x, blockIdx.x + gridDim.x, ...;
+    // each is nblocks steps of kQ time steps, run in order.
+    const int nblocks = (a.seqlen + kQ - 1) / kQ;
+    const int nitems = a.batch * a.nheads;
+    const int my_items = ((int)blockIdx.x < nitems) ? (nitems - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int nsteps = my_items * nblocks;
+    const int hpg = a.nheads / a.ngroups;
 
     if (sbase & 1023u) {
         // The swizzled tiles need a 1024-byte-aligned base and there is no
         // room to realign: make the failure visible instead of computing.
         const float nanv = __int_as_float(0x7fc00000);
-        for (int t = tid; t < a.seqlen; t += kThreads) {
-            Tout* yr = reinterpret_cast<Tout*>(a.y) + ((xrow0 + t) * a.nheads + h) * kP;
-            for (int p = 0; p < kP; ++p) yr[p] = from_f32<Tout>(nanv);
+        for (int it = 0; it < my_items; ++it) {
+            const int item = (int)blockIdx.x + it * (int)gridDim.x;
+            const int hh = item % a.nheads, bb = item / a.nheads;
+            for (int t = tid; t < a.seqlen; t += kThreads) {
+                Tout* yr = reinterpret_cast<Tout*>(a.y) +
+                           (((long long)bb * a.seqlen + t) * a.nheads + hh) * kP;
+                for (int p = 0; p < kP; ++p) yr[p] = from_f32<Tout>(nanv);
+            }
         }
         return;
     }
 
     if (warp == 0) tmem_alloc(s_tmem, kTmemCols);
     if (tid == 0) {
-        mbar_init(bar_tma, 1);
-        mbar_init(bar_mma1, 1);
+        mbar_init(bar_cb, 1);
+        mbar_init(bar_x, 1);
+        mbar_init(bar_g, 1);
+        mbar_init(bar_yoff, 1);
+        mbar_init(bar_s, 1);
         mbar_init(bar_mma2, 1);
         fence_mbar_init();
         prefetch_tensormap(&tm_C);
         prefetch_tensormap(&tm_B);
         prefetch_tensormap(&tm_x);
-        prefetch_tensormap(&tm_y);
     }
     tc_fence_before();
     __syncthreads();
@@ -170,35 +181,80 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t tmem = *s_tmem;
     const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's lane base
 
-    float S[kHalf];  // S_prev[n = row][32 part + q]
+    float S[kHalf];  // S_prev[n = row][32 part + q] of the current item
 #pragma unroll
     for (int q = 0; q < kHalf; ++q) S[q] = 0.0f;
 
-    const int nblocks = (a.seqlen + kQ - 1) / kQ;
-    constexpr uint32_t kTmaBytes = 2 * 32768 + 16384;
-    if (tid == 0) {
-        mbar_arrive_expect_tx(bar_tma, kTmaBytes);
-        tma_load_4d(smem + kRC, &tm_C, bar_tma, 0, g, 0, b);
-        tma_load_4d(smem + kRC + 16384, &tm_C, bar_tma, 64, g, 0, b);
-        tma_load_4d(smem + kRB, &tm_B, bar_tma, 0, g, 0, b);
-        tma_load_4d(smem + kRB + 16384, &tm_B, bar_tma, 64, g, 0, b);
-        tma_load_3d(smem + kRX, &tm_x, bar_tma, h * kP, 0, b);
-    }
-    // dt of step `row` of the block, loaded one block ahead
-    float dt_next = row < a.seqlen ? a.dt[(xrow0 + row) * a.nheads + h] : 0.0f;
+    // Loads are issued by thread kLoader: C and B of step st as soon as the
+    // previous step's S_chunk MMAs are done, x once its Y_diag MMAs are.  At
+    // most one load per barrier is ever outstanding.
+    constexpr int kLoader = 32;
+    int cb_issued = 0, x_issued = 0;  // (loader) loads issued so far
+    auto step_coords = [&](int st, int& hn, int& bn, int& gn, int& tn) {
+        const int item = (int)blockIdx.x + (st / nblocks) * (int)gridDim.x;
+        hn = item % a.nheads;
+        bn = item / a.nheads;
+        gn = hn / hpg;
+        tn = (st % nblocks) * kQ;
+    };
+    auto load_cb = [&](int st) {
+        int hn, bn, gn, tn;
+        step_coords(st, hn, bn, gn, tn);
+        mbar_arrive_expect_tx(bar_cb, 2 * 32768);
+        tma_load_4d(smem + kRC, &tm_C, bar_cb, 0, gn, tn, bn);
+        tma_load_4d(smem + kRC + 16384, &tm_C, bar_cb, 64, gn, tn, bn);
+        tma_load_4d(smem + kRB, &tm_B, bar_cb, 0, gn, tn, bn);
+        tma_load_4d(smem + kRB + 16384, &tm_B, bar_cb, 64, gn, tn, bn);
+        ++cb_issued;
+    };
+    auto load_x = [&](int st) {
+        int hn, bn, gn, tn;
+        step_coords(st, hn, bn, gn, tn);
+        mbar_arrive_expect_tx(bar_x, 16384);
+        tma_load_3d(smem + kRX, &tm_x, bar_x, hn * kP, tn, bn);
+        ++x_issued;
+    };
+    // dt of step st for this thread's row (0 past the sequence end), and A_h
+    auto load_dt = [&](int st, float& dtv, float& av) {
+        const int item = (int)blockIdx.x + (st / nblocks) * (int)gridDim.x;
+        const int hn = item % a.nheads, bn = item / a.nheads;
+        const int t = (st % nblocks) * kQ + row;
+        dtv = t < a.seqlen ? a.dt[((long long)bn * a.seqlen + t) * a.nheads + hn] : 0.0f;
+        av = a.A[hn];
+    };
     bool ok = true;
-    bool tma_pending = true;  // (thread 0) a block's loads were issued and not yet seen complete
-    uint32_t tma_phase = 0;
+    if (tid == kLoader && nsteps > 0) {
+        load_cb(0);
+        load_x(0);
+    }
+    float dt_next = 0.0f, A_next = 0.0f;  // loaded one step ahead
+    if (nsteps > 0) load_dt(0, dt_next, A_next);
 
-    for (int blk = 0; blk < nblocks; ++blk) {
+    for (int st = 0; st < nsteps; ++st) {
+        const int item = (int)blockIdx.x + (st / nblocks) * (int)gridDim.x;
+        const int blk = st % nblocks;
+        const int h = item % a.nheads, b = item / a.nheads;
         const int t0 = blk * kQ;
-        const int nv = min(kQ, a.seqlen - t0);
-        const uint32_t ph = (uint32_t)(blk & 1);
+        const uint32_t ph = (uint32_t)(st & 1);
+
+        // ---- G = C B^T as soon as the C and B tiles are in (thread 0)
+        if (tid == 0) {
+            const bool got = mbar_wait(bar_cb, ph, nullptr);
+            tc_fence_after();
+            if (got) {
+                constexpr uint32_t id128 = idesc_bf16_f32(128, 128);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tmem + kTmG, kdesc<kQ>(sbase + kRC, kk), kdesc<kQ>(sbase + kRB, kk),
+                             id128, kk > 0);
+                mma_commit(bar_g);
+            }
+        }
 
         // ---- cumulative log-decay cs_i = sum_{j<=i} dt_j A (padding: dt = 0),
         // computed by both warpgroups for their own rows
-        const float dti = dt_next;
-        dt_next = (t0 + kQ + row < a.seqlen) ? a.dt[(xrow0 + t0 + kQ + row) * a.nheads + h] : 0.0f;
+        const float dti = dt_next, Ah = A_next;
+        if (st + 1 < nsteps) load_dt(st + 1, dt_next, A_next);
         float v = dti * Ah;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -206,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (lane >= o) v += u;
         }
         if (lane == 31) s_wsum[part * 4 + quarter] = v;
-        __syncthreads();
+        __syncthreads();  // also: the previous step's y tile has been read out
         float cs_last = 0.0f;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
@@ -225,55 +281,45 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float e_i = ex2_approx(cs2_i);
         const float a_blk = ex2_approx(cs2_last);
 
-        // ---- MMA batch 1: G = C B^T; Y_off = C S_prev^T (hi + lo; none on block 0)
-        const bool got_tma = mbar_wait(bar_tma, ph, nullptr);
+        // ---- S_prev as the hi/lo operand of Y_off (row n, p contiguous)
+        if (blk > 0) {
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint32_t hp[4], lp[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    split2_bf16(S[8 * c4 + 2 * e], S[8 * c4 + 2 * e + 1], hp[e], lp[e]);
+                const uint32_t off = (uint32_t)(row * 128 + (((part * 4 + c4) ^ (row & 7)) << 4));
+                *reinterpret_cast<uint4*>(smem + kRS + off) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+                *reinterpret_cast<uint4*>(smem + kRS + 16384 + off) =
+                    make_uint4(lp[0], lp[1], lp[2], lp[3]);
+            }
+            fence_proxy_async_smem();
+        }
+        __syncthreads();  // S operand and q2 visible
+
+        // ---- Y_off = C S_prev^T: N = 128, S_hi in columns 0..63, S_lo in 64..127
         if (tid == 0) {
-            if (got_tma) tma_pending = false;
             tc_fence_after();
-            if (got_tma) {
-                constexpr uint32_t id128 = idesc_bf16_f32(128, 128);
+            if (blk > 0) {
                 constexpr uint32_t id128n = idesc_bf16_f32(128, 128) | kIdescBMN;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tmem + kTmG, kdesc<kQ>(sbase + kRC, kk), kdesc<kQ>(sbase + kRB, kk),
-                             id128, kk > 0);
-                if (blk > 0) {  // N = 128: S_hi in columns 0..63, S_lo in 64..127
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_bf16(tmem + kTmY, kdesc<kQ>(sbase + kRC, kk),
-                                 mdesc(sbase + kRS, kk, 16384), id128n, kk > 0);
-                }
-                mma_commit(bar_mma1);
+                    mma_bf16(tmem + kTmY, kdesc<kQ>(sbase + kRC, kk), mdesc(sbase + kRS, kk, 16384),
+                             id128n, kk > 0);
             }
-        }
-        {
-            const bool got = mbar_wait(bar_mma1, ph, nullptr);
-            if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
-        }
-        tc_fence_after();
-
-        // ---- X' = w o X (w_j = exp(cs_last - cs_j) dt_j), hi and lo, into the
-        // C region in the x tile's own MN-major layout
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int item = tid + kThreads * r;
-            const int j = item >> 3, c = item & 7;
-            const uint32_t off = (uint32_t)(j * 128 + ((c ^ (j & 7)) << 4));
-            const uint4 xv = *reinterpret_cast<const uint4*>(smem + kRX + off);
-            const float w = ex2_approx(cs2_last + s_q2[j]);
-            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-            uint32_t hp[4], lp[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) split2_bf16(bf16lo(xw[e]) * w, bf16hi(xw[e]) * w, hp[e], lp[e]);
-            *reinterpret_cast<uint4*>(smem + kRC + off) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
-            *reinterpret_cast<uint4*>(smem + kRC + 16384 + off) =
-                make_uint4(lp[0], lp[1], lp[2], lp[3]);
+            mma_commit(bar_yoff);
         }
 
         // ---- M'[i][j] = G[i][j] exp(cs_i - cs_j) dt_j for j <= i, else 0,
         // split hi/lo and written back over G in TMEM (row i = this lane).
         // 32-column chunk k of this warpgroup is wholly above the diagonal for
         // k > quarter, on it for k == quarter, below it otherwise.
+        {
+            const bool got = mbar_wait(bar_g, ph, nullptr);
+            if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
+        }
+        tc_fence_after();
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             const int ck = 2 * part + half;
@@ -295,8 +341,29 @@ __global__ void __launch_bounds__(kThreads, 2)
             tmem_st16(t_lane + kTmG + c0 + 16, lp);
         }
 
-        // ---- Y_off = (C S_hi^T + C S_lo^T) scaled by exp(cs_i), into the first 64
-        // of its 128 columns; Y_diag accumulates onto it
+        // ---- Y_off done (the C region is free):  X' = w o X (w_j = exp(cs_last -
+        // cs_j) dt_j), hi and lo, into the C region in the x tile's own MN-major
+        // layout; Y_off summed over its hi/lo halves and scaled by exp(cs_i)
+        {
+            const bool got = mbar_wait(bar_yoff, ph, nullptr) && mbar_wait(bar_x, ph, nullptr);
+            if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int it = tid + kThreads * r;
+            const int j = it >> 3, c = it & 7;
+            const uint32_t off = (uint32_t)(j * 128 + ((c ^ (j & 7)) << 4));
+            const uint4 xv = *reinterpret_cast<const uint4*>(smem + kRX + off);
+            const float w = ex2_approx(cs2_last + s_q2[j]);
+            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+            uint32_t hp[4], lp[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) split2_bf16(bf16lo(xw[e]) * w, bf16hi(xw[e]) * w, hp[e], lp[e]);
+            *reinterpret_cast<uint4*>(smem + kRC + off) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+            *reinterpret_cast<uint4*>(smem + kRC + 16384 + off) =
+                make_uint4(lp[0], lp[1], lp[2], lp[3]);
+        }
         if (blk > 0) {
             float yo[kHalf], yl[kHalf];
             tmem_ld32(t_lane + kTmY + kHalf * part, yo);
@@ -311,58 +378,50 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc_fence_before();
         __syncthreads();
 
-        // ---- MMA batch 2: S_chunk^T = B^T X' (hi + lo); Y += M' X (hi + lo)
+        // ---- MMA batch 2: S_chunk^T = B^T X' (hi + lo), committed on its own;
+        // then Y += M' X (hi + lo)
         if (tid == 0) {
             tc_fence_after();
             constexpr uint32_t idS = idesc_bf16_f32(128, 64) | kIdescAMN | kIdescBMN;
             constexpr uint32_t idY = idesc_bf16_f32(128, 64) | kIdescBMN;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
+            for (int kk = 0; kk < 8; ++kk) {
                 mma_bf16(tmem + kTmS, mdesc(sbase + kRB, kk, 16384), mdesc(sbase + kRC, kk, 16384),
                          idS, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
                 mma_bf16(tmem + kTmS, mdesc(sbase + kRB, kk, 16384),
                          mdesc(sbase + kRC + 16384, kk, 16384), idS, 1);
+            }
+            mma_commit(bar_s);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
+            for (int kk = 0; kk < 8; ++kk) {
                 mma_bf16_ta(tmem + kTmY, tmem + kTmG + mcol_hi(kk), mdesc(sbase + kRX, kk, 16384),
                             idY, (blk > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
                 mma_bf16_ta(tmem + kTmY, tmem + kTmG + mcol_hi(kk) + 16,
                             mdesc(sbase + kRX, kk, 16384), idY, 1);
+            }
             mma_commit(bar_mma2);
         }
-        {
-            const bool got = mbar_wait(bar_mma2, ph, nullptr);
-            if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
+        // ---- next step's loads (the next block, or the next item's first):
+        // C and B once S_chunk has read the B and X' regions, x after Y_diag
+        bool got2 = true;
+        if (tid == kLoader && st + 1 < nsteps) {
+            got2 = mbar_wait(bar_s, ph, nullptr);
+            if (got2) load_cb(st + 1);
         }
+        got2 = mbar_wait(bar_mma2, ph, nullptr) && got2;
+        if (!named_bar_and(1, kThreads, got2)) { ok = false; break; }
         tc_fence_after();
+        if (tid == kLoader && st + 1 < nsteps) load_x(st + 1);
 
-        // ---- the C, B, x regions are free: start the next block's loads
-        if (tid == 0 && blk + 1 < nblocks) {
-            const int tn = t0 + kQ;
-            mbar_arrive_expect_tx(bar_tma, kTmaBytes);
-            tma_load_4d(smem + kRC, &tm_C, bar_tma, 0, g, tn, b);
-            tma_load_4d(smem + kRC + 16384, &tm_C, bar_tma, 64, g, tn, b);
-            tma_load_4d(smem + kRB, &tm_B, bar_tma, 0, g, tn, b);
-            tma_load_4d(smem + kRB + 16384, &tm_B, bar_tma, 64, g, tn, b);
-            tma_load_3d(smem + kRX, &tm_x, bar_tma, h * kP, tn, b);
-            tma_pending = true;
-            tma_phase = (uint32_t)((blk + 1) & 1);
-        }
-
-        // ---- rows of Y and of S_chunk^T out of tensor memory
+        // ---- rows of Y and of S_chunk^T out of tensor memory; the y tile is
+        // staged in the S region (128-byte rows, 16-byte chunks XOR-swizzled by
+        // row mod 8): fp32 as two [128 t][32 p] halves, bf16 as one [128 t][64 p]
         float sc[kHalf];
         {
             float yv[kHalf];
             tmem_ld32(t_lane + kTmY + kHalf * part, yv);
             tmem_ld32(t_lane + kTmS + kHalf * part, sc);
             tmem_wait_ld();
-            // y tile staged in the S region in the tensor-store layout (128-byte
-            // rows, 16-byte chunks XOR-swizzled by row mod 8): fp32 as two
-            // [128 t][32 p] boxes, bf16 as one [128 t][64 p] box
             if constexpr (sizeof(Tout) == 4) {
                 uint8_t* box = smem + kRS + part * 16384 + row * 128;
 #pragma unroll
@@ -380,49 +439,61 @@ __global__ void __launch_bounds__(kThreads, 2)
                                    pack_bf16(yv[8 * c + 6], yv[8 * c + 7]));
             }
         }
-        fence_proxy_async_smem();
-        named_bar_sync(1, kThreads);
-        if (tid == 0) {
-            // rows past the sequence end are clipped by the tensor store
-            tma_store_3d(&tm_y, smem + kRS, h * kP, t0, b);
-            if constexpr (sizeof(Tout) == 4) tma_store_3d(&tm_y, smem + kRS + 16384, h * kP + 32, t0, b);
-            bulk_commit();
-            bulk_wait_read_all();
+        tc_fence_before();  // every TMEM read of the step precedes the next step's MMAs
+        __syncthreads();
+        if (tid == 0) tc_fence_after();
+
+        // ---- y rows out of the staged tile: each warp writes whole rows of
+        // the head (coalesced); rows past the sequence end are skipped
+        {
+            const long long yrow0 = ((long long)b * a.seqlen + t0) * a.nheads + h;
+            if constexpr (sizeof(Tout) == 4) {
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int idx = tid + kThreads * r;
+                    const int t = idx >> 4, c16 = idx & 15;
+                    const float4 v = *reinterpret_cast<const float4*>(
+                        smem + kRS + (c16 >> 3) * 16384 + t * 128 + (((c16 & 7) ^ (t & 7)) << 4));
+                    if (t0 + t < a.seqlen)
+                        *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.y) +
+                                                   (yrow0 + (long long)t * a.nheads) * kP + 4 * c16) = v;
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int idx = tid + kThreads * r;
+                    const int t = idx >> 3, c = idx & 7;
+                    const uint4 v = *reinterpret_cast<const uint4*>(smem + kRS + t * 128 +
+                                                                    ((c ^ (t & 7)) << 4));
+                    if (t0 + t < a.seqlen)
+                        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.y) +
+                                                  (yrow0 + (long long)t * a.nheads) * kP + 8 * c) = v;
+                }
+            }
         }
 
-        // ---- state: S_prev[n = row][32 part + :] = exp(cs_last) S_prev + S_chunk^T,
-        // then (once the store has read the y tile) its hi/lo operand for the
-        // next block (row n, p contiguous)
+        // ---- state: S_prev[n = row][32 part + :] = exp(cs_last) S_prev + S_chunk^T;
+        // at the item's last block, its final state [b][h][p = 32 part + :][n = row]
 #pragma unroll
         for (int q = 0; q < kHalf; ++q) S[q] = fmaf(a_blk, S[q], sc[q]);
-        named_bar_sync(1, kThreads);
+        if (blk == nblocks - 1) {
+            if (a.final_state) {
+                float* fs =
+                    a.final_state + ((long long)(b * a.nheads + h) * kP + kHalf * part) * kNs + row;
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-            uint32_t hp[4], lp[4];
+                for (int q = 0; q < kHalf; ++q) fs[q * kNs] = S[q];
+            }
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                split2_bf16(S[8 * c4 + 2 * e], S[8 * c4 + 2 * e + 1], hp[e], lp[e]);
-            const uint32_t off = (uint32_t)(row * 128 + (((part * 4 + c4) ^ (row & 7)) << 4));
-            *reinterpret_cast<uint4*>(smem + kRS + off) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
-            *reinterpret_cast<uint4*>(smem + kRS + 16384 + off) = make_uint4(lp[0], lp[1], lp[2], lp[3]);
+            for (int q = 0; q < kHalf; ++q) S[q] = 0.0f;
         }
-        fence_proxy_async_smem();  // S operand writes before the next block's MMAs
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
     }
+    (void)ok;
 
-    // ---- final state [b][h][p = 32 part + :][n = row]
-    if (ok && a.final_state) {
-        float* fs = a.final_state + ((long long)(b * a.nheads + h) * kP + kHalf * part) * kNs + row;
-#pragma unroll
-        for (int q = 0; q < kHalf; ++q) fs[q * kNs] = S[q];
-    }
-    if (tid == 0) {
-        // never leave with a load still landing in shared memory (bounded), nor
-        // with a tensor store still in flight
-        if (tma_pending) (void)mbar_wait(bar_tma, tma_phase, nullptr);
-        bulk_wait_all();
+    if (tid == kLoader) {
+        // never leave with a load still landing in shared memory: wait (bounded)
+        // for the phase of the last load issued on each barrier
+        if (cb_issued > 0) (void)mbar_wait(bar_cb, (uint32_t)((cb_issued - 1) & 1), nullptr);
+        if (x_issued > 0) (void)mbar_wait(bar_x, (uint32_t)((x_issued - 1) & 1), nullptr);
     }
     tc_fence_before();
     __syncthreads();
@@ -460,32 +531,31 @@ bool make_x_map(CUtensorMap* map, const void* base, int batch, int seqlen, int n
            CUDA_SUCCESS;
 }
 
-// y (batch, seqlen, nheads, headdim) as 3-D {nheads * headdim, seqlen, batch};
-// boxes of 128 bytes x 128 steps (32 fp32 or 64 bf16 of a head's row).
-bool make_y_map(CUtensorMap* map, void* base, int batch, int seqlen, int nheads, bool f32) {
-    ssm_host::EncodeTiledFn fn = ssm_host::encode_tiled_fn();
-    if (!fn) return false;
-    const cuuint64_t es = f32 ? 4 : 2;
-    const cuuint64_t dims[3] = {(cuuint64_t)nheads * kP, (cuuint64_t)seqlen, (cuuint64_t)batch};
-    const cuuint64_t strides[2] = {(cuuint64_t)nheads * kP * es,
-                                   (cuuint64_t)seqlen * nheads * kP * es};
-    const cuuint32_t box[3] = {(cuuint32_t)(128 / es), (cuuint32_t)kQ, 1};
-    const cuuint32_t estride[3] = {1, 1, 1};
-    return fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base,
-              dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <typename Tout>
 ssm_status_t launch(const CUtensorMap& mc, const CUtensorMap& mb, const CUtensorMap& mx,
-                    const CUtensorMap& my, const SsdArgs& a, cudaStream_t s) {
+                    const SsdArgs& a, cudaStream_t s) {
     auto kern = ssd_fwd_kernel<Tout>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
         cudaSuccess)
         return SSM_ERR_CUDA;
-    const unsigned grid = (unsigned)(a.batch * a.nheads);
-    kern<<<grid, kThreads, kSmemBytes, s>>>(mc, mb, mx, my, a);
+    // persistent: two CTAs per SM (shared memory and tensor memory are sized
+    // for two), each looping over (batch, head) items
+    static std::mutex m;
+    static int cached_dev = -1, sms = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lk(m);
+        if (dev != cached_dev) {
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                sms <= 0)
+                return SSM_ERR_CUDA;
+            cached_dev = dev;
+        }
+    }
+    const long long items = (long long)a.batch * a.nheads;
+    const unsigned grid = (unsigned)std::min<long long>(items, 2LL * sms);
+    kern<<<grid, kThreads, kSmemBytes, s>>>(mc, mb, mx, a);
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
@@ -530,10 +600,9 @@ extern "C" ssm_status_t ssd_chunked_fwd(const void* x, const float* dt, const fl
         if (overlaps(y, yb, r.p, r.n) || overlaps(final_state, fb, r.p, r.n)) return SSM_ERR_ALIAS;
     if (overlaps(y, yb, final_state, fb)) return SSM_ERR_ALIAS;
 
-    CUtensorMap mc, mb, mx, my;
+    CUtensorMap mc, mb, mx;
     if (!make_bc_map(&mc, C, batch, seqlen, ngroups) || !make_bc_map(&mb, B, batch, seqlen, ngroups) ||
-        !make_x_map(&mx, x, batch, seqlen, nheads) ||
-        !make_y_map(&my, y, batch, seqlen, nheads, out_dtype == SSM_F32))
+        !make_x_map(&mx, x, batch, seqlen, nheads))
         return SSM_ERR_CUDA;
     SsdArgs a{};
     a.x = static_cast<const __nv_bfloat16*>(x);
@@ -545,6 +614,6 @@ extern "C" ssm_status_t ssd_chunked_fwd(const void* x, const float* dt, const fl
     a.seqlen = seqlen;
     a.nheads = nheads;
     a.ngroups = ngroups;
-    return out_dtype == SSM_BF16 ? launch<__nv_bfloat16>(mc, mb, mx, my, a, s)
-                                 : launch<float>(mc, mb, mx, my, a, s);
+    return out_dtype == SSM_BF16 ? launch<__nv_bfloat16>(mc, mb, mx, a, s)
+                                 : launch<float>(mc, mb, mx, a, s);
 }
