@@ -7,11 +7,19 @@
 // gate).
 //
 // The step is one streaming read-modify-write of the fp32 state
-// (batch, nheads, headdim, dstate), so it is bound by HBM bandwidth: each
-// (b, h, p) row of dstate floats is owned by dstate/16 lanes holding 16
-// consecutive states each (16-byte loads with evict-first cache hints, two
-// rows' loads in flight per lane), the C^T h contraction is an intra-warp
-// shuffle reduction, and the row's first lane writes y.
+// (batch, nheads, headdim, dstate), so it is bound by HBM bandwidth.
+//  * dstate 128 (decode_bulk_kernel): the state streams through shared
+//    memory in tiles of up to 64 rows (32 KB, contiguous per (b, h)) by bulk
+//    asynchronous copies -- one load and one store per tile, issued by a
+//    producer warp, two tiles in flight per CTA, persistent CTAs -- and four
+//    compute warps update each tile in place (lane = 4 consecutive states).
+//  * other dstate (decode_kernel): each (b, h, p) row of dstate floats is
+//    owned by dstate/16 lanes holding 16 consecutive states each (16-byte
+//    loads with evict-first cache hints, two rows' loads in flight per lane).
+// In both, the C^T h contraction is an intra-warp shuffle reduction.
+#include <algorithm>
+#include <mutex>
+
 #include "common.cuh"
 
 namespace {
@@ -144,6 +152,216 @@ ssm_status_t launch(float* state, const void* x, const float* dt, const float* A
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
+// ------------------------------------------------------- dstate 128, bulk copies
+
+constexpr int kBulkRows = 64;                    // rows per tile
+constexpr int kBulkN = 128;                      // dstate
+constexpr int kTileBytes = kBulkRows * kBulkN * 4;
+constexpr int kBulkCompute = 128;                // 4 compute warps
+constexpr int kBulkThreads = kBulkCompute + 32;  // + 1 producer warp
+constexpr int kBulkSmem = 2 * kTileBytes + 64;
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(dst)),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Tiles are (b, h, chunk of up to 64 rows); CTA k takes tiles k, k + grid, ...
+// Stage s of the two shared-memory stages holds the CTA's tiles s, s + 2, ...:
+// full[s] completes when a tile has landed, empty[s] when the compute warps
+// have updated it in place (then the producer stores it and reuses the stage).
+template <typename T>
+__global__ void __launch_bounds__(kBulkThreads)
+    decode_bulk_kernel(float* __restrict__ state, const T* __restrict__ x,
+                       const float* __restrict__ dt, const float* __restrict__ A,
+                       const T* __restrict__ Bm, const T* __restrict__ Cm,
+                       const float* __restrict__ Dskip, const T* __restrict__ z,
+                       T* __restrict__ y, int batch, int nheads, int headdim, int ngroups) {
+    extern __shared__ __align__(128) uint8_t dsm[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(dsm + 2 * kTileBytes);
+    uint64_t* empty = full + 2;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nchunks = (headdim + kBulkRows - 1) / kBulkRows;
+    const long long ntiles = (long long)batch * nheads * nchunks;
+    const long long my = ntiles > blockIdx.x ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+    if (tid == 0) {
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kBulkCompute / 32);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // tile i of this CTA: (b, h) pair bh, first row p0, rows nr
+    auto tile = [&](long long i, long long& bh, int& p0, int& nr) {
+        const long long t = blockIdx.x + i * gridDim.x;
+        bh = t / nchunks;
+        p0 = (int)(t % nchunks) * kBulkRows;
+        nr = min(kBulkRows, headdim - p0);
+    };
+
+    if (warp == kBulkCompute / 32) {  // ------------------------------ producer
+        if (lane == 0) {
+            for (long long i = 0; i < 2 && i < my; ++i) {
+                long long bh; int p0, nr;
+                tile(i, bh, p0, nr);
+                mbar_arrive_expect_tx(&full[i], (uint32_t)nr * kBulkN * 4);
+                bulk_load(dsm + i * kTileBytes, state + (bh * headdim + p0) * kBulkN,
+                          (uint32_t)nr * kBulkN * 4, &full[i]);
+            }
+            for (long long i = 0; i < my; ++i) {
+                const int s = (int)(i & 1);
+                if (!mbar_wait(&empty[s], (uint32_t)((i >> 1) & 1), nullptr)) break;
+                long long bh; int p0, nr;
+                tile(i, bh, p0, nr);
+                bulk_store(state + (bh * headdim + p0) * kBulkN, dsm + s * kTileBytes,
+                           (uint32_t)nr * kBulkN * 4);
+                bulk_commit_group();
+                if (i + 2 < my) {
+                    bulk_wait_read_all();  // the stage has been read out
+                    tile(i + 2, bh, p0, nr);
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)nr * kBulkN * 4);
+                    bulk_load(dsm + s * kTileBytes, state + (bh * headdim + p0) * kBulkN,
+                              (uint32_t)nr * kBulkN * 4, &full[s]);
+                }
+            }
+            bulk_wait_all();
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------- compute
+    for (long long i = 0; i < my; ++i) {
+        const int s = (int)(i & 1);
+        long long bh; int p0, nr;
+        tile(i, bh, p0, nr);
+        const int h = (int)(bh % nheads);
+        const long long b = bh / nheads;
+        const int g = h / (nheads / ngroups);
+        // per-tile inputs, loaded before waiting for the state
+        const long long bc = (b * ngroups + g) * kBulkN + 4 * lane;
+        float bv[4], cv[4];
+        if constexpr (sizeof(T) == 2) {
+            const uint2 wb = __ldg(reinterpret_cast<const uint2*>(Bm + bc));
+            const uint2 wc = __ldg(reinterpret_cast<const uint2*>(Cm + bc));
+            bv[0] = bf16lo(wb.x); bv[1] = bf16hi(wb.x); bv[2] = bf16lo(wb.y); bv[3] = bf16hi(wb.y);
+            cv[0] = bf16lo(wc.x); cv[1] = bf16hi(wc.x); cv[2] = bf16lo(wc.y); cv[3] = bf16hi(wc.y);
+        } else {
+            const float4 fb = __ldg(reinterpret_cast<const float4*>(Bm + bc));
+            const float4 fc = __ldg(reinterpret_cast<const float4*>(Cm + bc));
+            bv[0] = fb.x; bv[1] = fb.y; bv[2] = fb.z; bv[3] = fb.w;
+            cv[0] = fc.x; cv[1] = fc.y; cv[2] = fc.z; cv[3] = fc.w;
+        }
+        const float dtv = dt[bh];
+        const float alpha = expf(dtv * A[h]);
+        const long long row0 = bh * headdim + p0;  // (b, h, p0) row index
+        float dbx[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const int p = warp + 4 * r;
+            dbx[r] = p < nr ? dtv * to_f32(x[row0 + p]) : 0.0f;
+        }
+        if (!mbar_wait(&full[s], (uint32_t)((i >> 1) & 1), nullptr)) break;
+
+        // rows warp, warp + 4, ...: state (in place) and the C^T h partial sums
+        float* st = reinterpret_cast<float*>(dsm + s * kTileBytes);
+        float acc[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const int p = warp + 4 * r;
+            acc[r] = 0.0f;
+            if (p < nr) {
+                float4* q = reinterpret_cast<float4*>(st + p * kBulkN) + lane;
+                const float4 v = *q;
+                const float n0 = fmaf(alpha, v.x, dbx[r] * bv[0]);
+                const float n1 = fmaf(alpha, v.y, dbx[r] * bv[1]);
+                const float n2 = fmaf(alpha, v.z, dbx[r] * bv[2]);
+                const float n3 = fmaf(alpha, v.w, dbx[r] * bv[3]);
+                *q = make_float4(n0, n1, n2, n3);
+                acc[r] = fmaf(cv[3], n3, fmaf(cv[2], n2, fmaf(cv[1], n1, cv[0] * n0)));
+            }
+        }
+        fence_proxy_async_smem();  // the updated tile is read by the bulk store
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+
+        // reduce-scatter the 16 rows' sums over the warp: afterwards lanes
+        // 2k and 2k + 1 hold the total of warp-local row k
+#pragma unroll
+        for (int m = 16, n = 8; m >= 2; m >>= 1, n >>= 1) {
+            const bool hi = lane & m;
+#pragma unroll
+            for (int k = 0; k < n; ++k) {
+                const float send = hi ? acc[k] : acc[k + n];
+                const float keep = hi ? acc[k + n] : acc[k];
+                acc[k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+            }
+        }
+        acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 1);
+        const int p = warp + 4 * (lane >> 1);
+        if ((lane & 1) == 0 && p < nr) {
+            const long long row = row0 + p;
+            const float xv = to_f32(x[row]);
+            float out = acc[0] + (Dskip ? Dskip[h] : 0.0f) * xv;
+            if (z) out *= silu_f(to_f32(z[row]));
+            y[row] = from_f32<T>(out);
+        }
+    }
+}
+
+template <typename T>
+ssm_status_t launch_bulk(float* state, const void* x, const float* dt, const float* A,
+                         const void* B, const void* C, const float* D, const void* z, void* y,
+                         int batch, int nheads, int headdim, int ngroups, cudaStream_t s) {
+    static std::mutex m;
+    static int cached_dev = -1, sms = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lk(m);
+        if (dev != cached_dev) {
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                sms <= 0)
+                return SSM_ERR_CUDA;
+            if (cudaFuncSetAttribute(decode_bulk_kernel<T>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kBulkSmem) != cudaSuccess)
+                return SSM_ERR_CUDA;
+            cached_dev = dev;
+        }
+    }
+    const long long tiles =
+        (long long)batch * nheads * ((headdim + kBulkRows - 1) / kBulkRows);
+    const unsigned grid = (unsigned)std::min<long long>(tiles, 3LL * sms);
+    decode_bulk_kernel<T><<<grid, kBulkThreads, kBulkSmem, s>>>(
+        state, static_cast<const T*>(x), dt, A, static_cast<const T*>(B),
+        static_cast<const T*>(C), D, static_cast<const T*>(z), static_cast<T*>(y), batch, nheads,
+        headdim, ngroups);
+    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 template <typename T>
 ssm_status_t by_dstate(int dstate, float* state, const void* x, const float* dt, const float* A,
                        const void* B, const void* C, const float* D, const void* z, void* y,
@@ -152,7 +370,9 @@ ssm_status_t by_dstate(int dstate, float* state, const void* x, const float* dt,
         case 16: return launch<T, 1>(state, x, dt, A, B, C, D, z, y, rows, nheads, headdim, ngroups, s);
         case 32: return launch<T, 2>(state, x, dt, A, B, C, D, z, y, rows, nheads, headdim, ngroups, s);
         case 64: return launch<T, 4>(state, x, dt, A, B, C, D, z, y, rows, nheads, headdim, ngroups, s);
-        case 128: return launch<T, 8>(state, x, dt, A, B, C, D, z, y, rows, nheads, headdim, ngroups, s);
+        case 128:
+            return launch_bulk<T>(state, x, dt, A, B, C, D, z, y, (int)(rows / headdim / nheads),
+                                  nheads, headdim, ngroups, s);
         case 256: return launch<T, 16>(state, x, dt, A, B, C, D, z, y, rows, nheads, headdim, ngroups, s);
     }
     return SSM_ERR_UNSUPPORTED;

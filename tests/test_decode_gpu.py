@@ -13,7 +13,11 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("batch,nheads,headdim,dstate,ngroups,dtype,gate",
                          [(2, 4, 64, 128, 1, "f32", True), (3, 6, 16, 64, 2, "f32", False),
                           (1, 2, 8, 16, 1, "f32", True), (2, 4, 32, 256, 4, "bf16", True),
-                          (5, 3, 7, 32, 1, "bf16", False)])
+                          (5, 3, 7, 32, 1, "bf16", False),
+                          # dstate 128 runs the bulk-copy kernel: tiles of up to 64 rows
+                          (3, 2, 100, 128, 1, "bf16", True),   # a 64-row and a 36-row tile
+                          (2, 3, 8, 128, 3, "f32", False),     # one short tile per head
+                          (1, 1, 192, 128, 1, "f32", True)])   # three full tiles, one head
 def test_decode_chain_matches_oracle(batch, nheads, headdim, dstate, ngroups, dtype, gate):
     steps = 6
     inp = inputs.decode_inputs(batch, nheads, headdim, dstate, ngroups, steps, dtype, seed=31,
