@@ -164,14 +164,14 @@ struct Smem {
     static constexpr int STAGE = 3 * IN_TILE + 2 * BC_TILE;
     static constexpr int NSTAGE = TMA ? Geom<Tin>::kStages : 1;
     static constexpr int PREP = CH * kPrepStride;
-    static constexpr int BCF = 2 * kTL * kN * 4;
+    static constexpr int BCF = (E == 2 ? 1 : 2) * kTL * kN * 4;
     static constexpr int BARS = 2 * NSTAGE * 8 + 16;
     static constexpr int BYTES = NSTAGE * STAGE + PREP + BCF + BARS;
     static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024
 };
 
 template <typename Tin, typename Tout, int CH, bool TMA>
-__global__ void __launch_bounds__(CH * kNG + 32)
+__global__ void __launch_bounds__(CH * kNG + 32, 3)
     scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u,
                     const __grid_constant__ CUtensorMap tm_d,
                     const __grid_constant__ CUtensorMap tm_z,
@@ -186,7 +186,9 @@ __global__ void __launch_bounds__(CH * kNG + 32)
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t* stages = smem;
     uint8_t* prep = stages + NSTAGE * S::STAGE;
-    float* bcf = reinterpret_cast<float*>(prep + S::PREP);  // [2][kTL][kN]
+    float* bcf = reinterpret_cast<float*>(prep + S::PREP);  // [2][kTL][kN] fp32 B, C
+    uint8_t* bcf_raw = prep + S::PREP;  // bf16 inputs: [kTL][4] 16-byte B/C chunks
+    constexpr bool kPackedBC = sizeof(Tin) == 2;
     uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(bcf) + S::BCF);
     uint64_t* empty = full + NSTAGE;
     int* s_ticket = reinterpret_cast<int*>(empty + NSTAGE);
@@ -341,16 +343,35 @@ __global__ void __launch_bounds__(CH * kNG + 32)
             for (int j = 0; j < 4; ++j)
                 dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
         }
-        // ---- B, C: swizzled [n][t] in the input type -> fp32 [t][n]
-        for (int i = tid; i < 2 * kN * (kTL / 8); i += NCOMP) {
-            const int arr = i / (kN * kTL / 8);
-            const int rem = i % (kN * kTL / 8);
-            const int n = rem % kN, j = rem / kN;
-            float v[8];
-            load8<Tin, kN>(st + 3 * S::IN_TILE + arr * S::BC_TILE, n, j * 8, v);
-            float* dst = bcf + arr * kTL * kN;
+        if constexpr (kPackedBC) {
+            // ---- B, C (bf16, exact): swizzled [n][t] -> per step t, four
+            // 16-byte chunks, chunk g = B[4g..4g+3][t], C[4g..4g+3][t]
+            const uint8_t* tb = st + 3 * S::IN_TILE;
+            const uint8_t* tc = tb + S::BC_TILE;
+            for (int i = tid; i < 4 * kTL; i += NCOMP) {
+                const int t = i % kTL, g4 = i / kTL;
+                uint32_t hb[4], hc[4];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) dst[(j * 8 + q) * kN + n] = v[q];
+                for (int k = 0; k < 4; ++k) {
+                    hb[k] = *reinterpret_cast<const uint16_t*>(tb + tile_off<Tin, kN>(4 * g4 + k, t));
+                    hc[k] = *reinterpret_cast<const uint16_t*>(tc + tile_off<Tin, kN>(4 * g4 + k, t));
+                }
+                *reinterpret_cast<uint4*>(bcf_raw + (t * 4 + g4) * 16) =
+                    make_uint4(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16), hc[0] | (hc[1] << 16),
+                               hc[2] | (hc[3] << 16));
+            }
+        } else {
+            // ---- B, C: swizzled [n][t] in the input type -> fp32 [t][n]
+            for (int i = tid; i < 2 * kN * (kTL / 8); i += NCOMP) {
+                const int arr = i / (kN * kTL / 8);
+                const int rem = i % (kN * kTL / 8);
+                const int n = rem % kN, j = rem / kN;
+                float v[8];
+                load8<Tin, kN>(st + 3 * S::IN_TILE + arr * S::BC_TILE, n, j * 8, v);
+                float* dst = bcf + arr * kTL * kN;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) dst[(j * 8 + q) * kN + n] = v[q];
+            }
         }
         named_bar_sync(1, NCOMP);
 
@@ -397,8 +418,15 @@ __global__ void __launch_bounds__(CH * kNG + 32)
                     const int t = j * 8 + q + r;
                     const float dl = r ? pp.z : pp.x;
                     const float du = r ? pp.w : pp.y;
-                    const float4 bv = *reinterpret_cast<const float4*>(Bt + t * kN + n0);
-                    const float4 cv = *reinterpret_cast<const float4*>(Ct + t * kN + n0);
+                    float4 bv, cv;
+                    if constexpr (kPackedBC) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(bcf_raw + (t * 4 + ng) * 16);
+                        bv = make_float4(bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y));
+                        cv = make_float4(bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w));
+                    } else {
+                        bv = *reinterpret_cast<const float4*>(Bt + t * kN + n0);
+                        cv = *reinterpret_cast<const float4*>(Ct + t * kN + n0);
+                    }
                     h[0] = fmaf(ex2_approx(dl * A2[0]), h[0], du * bv.x);
                     h[1] = fmaf(ex2_approx(dl * A2[1]), h[1], du * bv.y);
                     h[2] = fmaf(ex2_approx(dl * A2[2]), h[2], du * bv.z);
