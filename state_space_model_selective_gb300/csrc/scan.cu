@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
 
         // ---- the recurrence over the tile, 8 steps per group
         const uint8_t* tz = st + 2 * S::IN_TILE;
-#pragma unroll 1
+#pragma unroll 2
         for (int j = 0; j < kTL / 8; ++j) {
             float yp[8];
 #pragma unroll
