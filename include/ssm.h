@@ -118,18 +118,24 @@ ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const float* A,
  * Computes, exactly up to rounding, the recurrence
  *   S[p,n] = exp(dt[b,t,h] A_head[h]) S[p,n] + dt[b,t,h] B[b,t,g,n] x[b,t,h,p]
  *   y[b,t,h,p] = sum_n C[b,t,g,n] S[p,n]
- * from S = 0 (g = h / (nheads / ngroups)); final_state[b,h,p,n] = S after
- * the last step.  dt is taken as given (already discretised).
+ * from S = initial_state[b,h] (0 when initial_state is NULL; g = h /
+ * (nheads / ngroups)); final_state[b,h,p,n] = S after the last step.  dt is
+ * taken as given (already discretised).  With initial_state the call resumes
+ * a sequence: the SSD over L1 + L2 steps equals the SSD over L1 steps followed
+ * by the SSD over L2 steps from its final state.
  *
  * Layouts: x, y (batch, seqlen, nheads, headdim); dt (batch, seqlen, nheads)
  * fp32; A_head (nheads,) fp32; B, C (batch, seqlen, ngroups, dstate);
- * final_state (batch, nheads, headdim, dstate) fp32, may be NULL.
+ * initial_state, final_state (batch, nheads, headdim, dstate) fp32, each may
+ * be NULL; initial_state may be the same buffer as final_state (updated in
+ * place), any other overlap returns SSM_ERR_ALIAS.
  * Supported: chunk == 64, headdim == 64, dstate == 128, in_dtype == SSM_BF16,
  * seqlen % chunk == 0 (else SSM_ERR_SHAPE), nheads % ngroups == 0.
+ * seqlen == 0 writes final_state = initial_state (or 0).
  */
 ssm_status_t ssd_chunked_fwd(const void* x, const float* dt, const float* A_head,
                              const void* B, const void* C, int chunk,
-                             void* y, float* final_state,
+                             const float* initial_state, void* y, float* final_state,
                              int batch, int seqlen, int nheads, int headdim, int dstate,
                              int ngroups, ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
                              void* stream);

@@ -58,7 +58,7 @@ def lib() -> ctypes.CDLL:
         L.ssm_scan_fwd.restype = i
         L.ssm_scan_fwd.argtypes = [vp] * 8 + [i] + [vp] * 3 + [i] * 7 + [vp, sz, vp]
         L.ssd_chunked_fwd.restype = i
-        L.ssd_chunked_fwd.argtypes = [vp] * 5 + [i] + [vp] * 2 + [i] * 8 + [vp]
+        L.ssd_chunked_fwd.argtypes = [vp] * 5 + [i] + [vp] * 3 + [i] * 8 + [vp]
         L.ssm_decode_step.restype = i
         L.ssm_decode_step.argtypes = [vp] * 9 + [i] * 6 + [vp]
         L.ssm_scan_fwd_noalloc.restype = i
@@ -186,9 +186,11 @@ def ssm_scan_fwd_noalloc(u, delta, A, B, C, y, final_state=None, D=None, z=None,
 
 
 def ssd_chunked_fwd(x, dt, A_head, B, C, chunk=64, out_dtype=None, y=None, final_state=None,
-                    return_final_state=True, stream=None):
+                    return_final_state=True, stream=None, initial_state=None):
     """Chunked SSD.  x: (batch, seqlen, nheads, headdim); dt: (batch, seqlen, nheads) fp32;
-    A_head: (nheads,) fp32; B, C: (batch, seqlen, ngroups, dstate).  Returns (y, final_state)."""
+    A_head: (nheads,) fp32; B, C: (batch, seqlen, ngroups, dstate); initial_state (optional,
+    may be ``final_state`` itself): (batch, nheads, headdim, dstate) fp32.
+    Returns (y, final_state)."""
     _req(x, "x", ndim=4)
     in_dt = x.dtype
     if in_dt not in _DT:
@@ -207,8 +209,12 @@ def ssd_chunked_fwd(x, dt, A_head, B, C, chunk=64, out_dtype=None, y=None, final
         final_state = torch.empty((batch, nheads, headdim, dstate), dtype=torch.float32,
                                   device=x.device)
     _opt(final_state, "final_state", torch.float32)
+    _opt(initial_state, "initial_state", torch.float32)
+    if initial_state is not None and tuple(initial_state.shape) != (batch, nheads, headdim, dstate):
+        raise ValueError("initial_state must be (batch, nheads, headdim, dstate)")
     st = lib().ssd_chunked_fwd(_ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C), int(chunk),
-                               _ptr(y), _ptr(final_state), batch, seqlen, nheads, headdim, dstate,
+                               _ptr(initial_state), _ptr(y), _ptr(final_state), batch, seqlen,
+                               nheads, headdim, dstate,
                                ngroups, _DT[in_dt], _DT[out_dt], _stream(stream))
     _check(st, "ssd_chunked_fwd")
     return y, final_state

@@ -60,6 +60,7 @@ struct SsdArgs {
     const __nv_bfloat16* x;
     const float* dt;
     const float* A;
+    const float* h0;  // initial state (batch, nheads, headdim, dstate) or NULL
     void* y;
     float* final_state;
     int batch, seqlen, nheads, ngroups;
@@ -184,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     float S[kHalf];  // S_prev[n = row][32 part + q] of the current item
 #pragma unroll
     for (int q = 0; q < kHalf; ++q) S[q] = 0.0f;
+    const bool has_h0 = a.h0 != nullptr;
 
     // Loads are issued by thread kLoader: C and B of step st as soon as the
     // previous step's S_chunk MMAs are done, x once its Y_diag MMAs are.  At
@@ -236,6 +238,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int h = item % a.nheads, b = item / a.nheads;
         const int t0 = blk * kQ;
         const uint32_t ph = (uint32_t)(st & 1);
+        // a state enters this block: carried from the previous block, or given
+        const bool carry = blk > 0 || has_h0;
+        if (blk == 0 && has_h0) {
+            const float* ip = a.h0 + ((long long)(b * a.nheads + h) * kP + kHalf * part) * kNs + row;
+#pragma unroll
+            for (int q = 0; q < kHalf; ++q) S[q] = ip[q * kNs];
+        }
 
         // ---- G = C B^T as soon as the C and B tiles are in (thread 0)
         if (tid == 0) {
@@ -282,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float a_blk = ex2_approx(cs2_last);
 
         // ---- S_prev as the hi/lo operand of Y_off (row n, p contiguous)
-        if (blk > 0) {
+        if (carry) {
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
                 uint32_t hp[4], lp[4];
@@ -299,9 +308,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         __syncthreads();  // S operand and q2 visible
 
         // ---- Y_off = C S_prev^T: N = 128, S_hi in columns 0..63, S_lo in 64..127
+        // (none when no state enters the block)
         if (tid == 0) {
             tc_fence_after();
-            if (blk > 0) {
+            if (carry) {
                 constexpr uint32_t id128n = idesc_bf16_f32(128, 128) | kIdescBMN;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
@@ -364,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             *reinterpret_cast<uint4*>(smem + kRC + 16384 + off) =
                 make_uint4(lp[0], lp[1], lp[2], lp[3]);
         }
-        if (blk > 0) {
+        if (carry) {
             float yo[kHalf], yl[kHalf];
             tmem_ld32(t_lane + kTmY + kHalf * part, yo);
             tmem_ld32(t_lane + kTmY + kP + kHalf * part, yl);
@@ -395,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 mma_bf16_ta(tmem + kTmY, tmem + kTmG + mcol_hi(kk), mdesc(sbase + kRX, kk, 16384),
-                            idY, (blk > 0 || kk > 0) ? 1u : 0u);
+                            idY, (carry || kk > 0) ? 1u : 0u);
                 mma_bf16_ta(tmem + kTmY, tmem + kTmG + mcol_hi(kk) + 16,
                             mdesc(sbase + kRX, kk, 16384), idY, 1);
             }
@@ -562,7 +572,8 @@ ssm_status_t launch(const CUtensorMap& mc, const CUtensorMap& mb, const CUtensor
 }  // namespace
 
 extern "C" ssm_status_t ssd_chunked_fwd(const void* x, const float* dt, const float* A_head,
-                                        const void* B, const void* C, int chunk, void* y,
+                                        const void* B, const void* C, int chunk,
+                                        const float* initial_state, void* y,
                                         float* final_state, int batch, int seqlen, int nheads,
                                         int headdim, int dstate, int ngroups,
                                         ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
@@ -579,26 +590,38 @@ extern "C" ssm_status_t ssd_chunked_fwd(const void* x, const float* dt, const fl
     if (batch == 0 || nheads == 0) return SSM_OK;
     if ((size_t)batch * nheads > (size_t)INT32_MAX) return SSM_ERR_UNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (seqlen == 0) {  // empty sequence: the state stays zero
-        const size_t fb0 = (size_t)batch * nheads * headdim * dstate * 4;
+    const size_t sb = (size_t)batch * nheads * headdim * dstate * 4;  // one state tensor
+    if (seqlen == 0) {  // empty sequence: the state passes through unchanged
         if (final_state && !aligned16(final_state)) return SSM_ERR_ALIGN;
-        if (final_state && cudaMemsetAsync(final_state, 0, fb0, s) != cudaSuccess)
-            return SSM_ERR_CUDA;
+        if (initial_state && !aligned16(initial_state)) return SSM_ERR_ALIGN;
+        if (final_state && initial_state != final_state) {
+            if (initial_state && overlaps(final_state, sb, initial_state, sb)) return SSM_ERR_ALIAS;
+            const cudaError_t e =
+                initial_state ? cudaMemcpyAsync(final_state, initial_state, sb,
+                                                cudaMemcpyDeviceToDevice, s)
+                              : cudaMemsetAsync(final_state, 0, sb, s);
+            if (e != cudaSuccess) return SSM_ERR_CUDA;
+        }
         return SSM_OK;
     }
     if (!x || !dt || !A_head || !B || !C || !y) return SSM_ERR_NULL;
-    const void* ptrs[] = {x, dt, A_head, B, C, y, final_state};
+    const void* ptrs[] = {x, dt, A_head, B, C, y, final_state, initial_state};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return SSM_ERR_ALIGN;
     const size_t xb = rows * nheads * headdim * 2;
     const size_t yb = rows * nheads * headdim * dtype_size(out_dtype);
     const size_t bcb = rows * ngroups * dstate * 2;
-    const size_t fb = final_state ? (size_t)batch * nheads * headdim * dstate * 4 : 0;
+    const size_t fb = final_state ? sb : 0;
+    // initial_state may be final_state itself (each (batch, head) state is read
+    // before it is written, by the same threads), but no other overlap
+    const size_t ib = (initial_state && initial_state != final_state) ? sb : 0;
     struct R { const void* p; size_t n; } ins[] = {
-        {x, xb}, {dt, rows * nheads * 4}, {A_head, (size_t)nheads * 4}, {B, bcb}, {C, bcb}};
+        {x, xb}, {dt, rows * nheads * 4}, {A_head, (size_t)nheads * 4}, {B, bcb}, {C, bcb},
+        {initial_state, ib}};
     for (const R& r : ins)
         if (overlaps(y, yb, r.p, r.n) || overlaps(final_state, fb, r.p, r.n)) return SSM_ERR_ALIAS;
     if (overlaps(y, yb, final_state, fb)) return SSM_ERR_ALIAS;
+    if (initial_state && overlaps(y, yb, initial_state, sb)) return SSM_ERR_ALIAS;
 
     CUtensorMap mc, mb, mx;
     if (!make_bc_map(&mc, C, batch, seqlen, ngroups) || !make_bc_map(&mb, B, batch, seqlen, ngroups) ||
@@ -608,6 +631,7 @@ extern "C" ssm_status_t ssd_chunked_fwd(const void* x, const float* dt, const fl
     a.x = static_cast<const __nv_bfloat16*>(x);
     a.dt = dt;
     a.A = A_head;
+    a.h0 = initial_state;
     a.y = y;
     a.final_state = final_state;
     a.batch = batch;

@@ -39,7 +39,7 @@ def test_header_symbols_exported(L):
 
 
 def test_version_and_status_strings(L):
-    assert binding.ssm_abi_version() == 1
+    assert binding.ssm_abi_version() == 2
     for code in range(10):
         s = binding.status_string(code)
         assert isinstance(s, str) and s
@@ -99,12 +99,13 @@ def test_scan_argument_errors(L):
 
 
 def ssd_call(L, **kw):
-    args = dict(x=P(0), dt=P(1), A=P(2), B=P(3), C=P(4), chunk=64, y=P(5), fs=P(6), batch=2,
+    args = dict(x=P(0), dt=P(1), A=P(2), B=P(3), C=P(4), chunk=64, h0=None, y=P(5), fs=P(6), batch=2,
                 seqlen=128, nheads=4, headdim=64, dstate=128, ngroups=1, in_dt=1, out_dt=0,
                 stream=None)
     args.update(kw)
     return L.ssd_chunked_fwd(args["x"], args["dt"], args["A"], args["B"], args["C"],
-                             args["chunk"], args["y"], args["fs"], args["batch"], args["seqlen"],
+                             args["chunk"], args["h0"], args["y"], args["fs"], args["batch"],
+                             args["seqlen"],
                              args["nheads"], args["headdim"], args["dstate"], args["ngroups"],
                              args["in_dt"], args["out_dt"], args["stream"])
 
@@ -123,6 +124,10 @@ def test_ssd_argument_errors(L):
     assert ssd_call(L, y=P(3)) == ALIAS
     assert ssd_call(L, x=ctypes.c_void_p(0x10000002)) == ALIGN
     assert ssd_call(L, batch=0, x=None, y=None) == OK
+    # the initial state may be the final state itself, nothing else that is written
+    assert ssd_call(L, h0=P(5)) == ALIAS               # initial state on top of y
+    assert ssd_call(L, h0=ctypes.c_void_p(0x70000000 + 4096)) == ALIAS  # inside final_state
+    assert ssd_call(L, h0=ctypes.c_void_p(0x10000008)) == ALIGN
 
 
 def decode_call(L, **kw):

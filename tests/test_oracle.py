@@ -325,8 +325,11 @@ def test_ssd_chunked_equals_recurrence(chunk):
     np.testing.assert_allclose(hc, hs, rtol=1e-12, atol=1e-13)
 
 
-def test_scan_with_head_constant_A_equals_ssd():
-    """Scan channels d = h*P + p with A[d, n] = A_h equal the SSD of (B, L, H, P)."""
+@pytest.mark.parametrize("use_h0", [False, True])
+def test_scan_with_head_constant_A_equals_ssd(use_h0):
+    """Scan channels d = h*P + p with A[d, n] = A_h equal the SSD of (B, L, H, P),
+    from zero or from a given initial state (the scan's initial-state path is
+    pinned by brute force above)."""
     rng = _rng(17)
     batch, seqlen, nheads, headdim, dstate, ngroups = 2, 15, 4, 3, 5, 2
     x = rng.standard_normal((batch, seqlen, nheads, headdim))
@@ -334,14 +337,16 @@ def test_scan_with_head_constant_A_equals_ssd():
     A_head = -rng.uniform(1, 8, nheads)
     B = rng.standard_normal((batch, seqlen, ngroups, dstate))
     C = rng.standard_normal((batch, seqlen, ngroups, dstate))
-    y_ssd, hs_ssd = oracle.ssd_recurrence(x, dt, A_head, B, C)
+    h0 = rng.standard_normal((batch, nheads, headdim, dstate)) if use_h0 else None
+    y_ssd, hs_ssd = oracle.ssd_recurrence(x, dt, A_head, B, C, h0)
     dim = nheads * headdim
     u = x.reshape(batch, seqlen, dim).transpose(0, 2, 1)
     delta = np.repeat(dt, headdim, axis=2).transpose(0, 2, 1)
     A = np.repeat(A_head, headdim)[:, None] * np.ones((1, dstate))
     Bs = B.transpose(0, 2, 3, 1)
     Cs = C.transpose(0, 2, 3, 1)
-    y_scan, hs_scan = oracle.scan(u, delta, A, Bs, Cs)
+    h0s = None if h0 is None else h0.reshape(batch, dim, dstate)
+    y_scan, hs_scan = oracle.scan(u, delta, A, Bs, Cs, h0=h0s)
     np.testing.assert_allclose(y_scan, y_ssd.reshape(batch, seqlen, dim).transpose(0, 2, 1),
                                rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(hs_scan, hs_ssd.reshape(batch, dim, dstate), rtol=1e-12, atol=1e-13)

@@ -11,7 +11,7 @@ from tests.helpers import TOL_BF16, assert_close
 pytestmark = pytest.mark.gpu
 
 
-def _run(inp, out_dtype=torch.float32, poison=True):
+def _run(inp, out_dtype=torch.float32, poison=True, h0=None):
     d = {k: v.cuda() for k, v in inp.items()}
     x = d["x"]
     batch, seqlen, nheads, headdim = x.shape
@@ -21,9 +21,15 @@ def _run(inp, out_dtype=torch.float32, poison=True):
         y.fill_(float("nan"))
         fs.fill_(float("nan"))
     binding.ssd_chunked_fwd(d["x"], d["dt"], d["A_head"], d["B"], d["C"], 64, out_dtype=out_dtype,
-                            y=y, final_state=fs)
+                            y=y, final_state=fs,
+                            initial_state=None if h0 is None else h0.cuda())
     torch.cuda.synchronize()
     return y, fs
+
+
+def _slice_steps(inp, t0, t1):
+    return {k: (v[:, t0:t1].contiguous() if k in ("x", "dt", "B", "C") else v)
+            for k, v in inp.items()}
 
 
 CASES = [  # batch, seqlen, nheads, ngroups
@@ -101,3 +107,61 @@ def test_workload_ssd_B32_L256_H32():
                                               inp["B"][sl], inp["C"][sl])
         assert_close(y[sl], y_ref, TOL_BF16, f"y batch {b}")
         assert_close(fs[sl], fs_ref, TOL_BF16, f"final_state batch {b}")
+
+
+@pytest.mark.parametrize("seqlen", [64, 192, 256])
+def test_ssd_initial_state_matches_recurrence(seqlen):
+    """Prefill resumed from a given state: the recurrence starts at h0."""
+    batch, nheads = 2, 4
+    inp = inputs.ssd_inputs(batch, seqlen, nheads, 64, 128, 2, "bf16", seed=70 + seqlen)
+    h0 = torch.randn(batch, nheads, 64, 128, generator=torch.Generator().manual_seed(5))
+    y, fs = _run(inp, h0=h0)
+    y_ref, fs_ref = oracle.ssd_recurrence(inp["x"], inp["dt"], inp["A_head"], inp["B"], inp["C"],
+                                          h0.double().numpy())
+    assert_close(y, y_ref, TOL_BF16, "y")
+    assert_close(fs, fs_ref, TOL_BF16, "final_state")
+
+
+@pytest.mark.parametrize("split", [128, 64])
+def test_ssd_resume_equals_whole_sequence(split):
+    """The SSD over 384 steps equals the SSD over the first `split` steps
+    followed by the SSD over the rest from its final state; with the split on a
+    128-step block boundary the two runs do the same arithmetic (bit-equal)."""
+    batch, nheads, L = 2, 4, 384
+    inp = inputs.ssd_inputs(batch, L, nheads, 64, 128, 1, "bf16", seed=81)
+    y_all, fs_all = _run(inp)
+    y1, fs1 = _run(_slice_steps(inp, 0, split))
+    y2, fs2 = _run(_slice_steps(inp, split, L), h0=fs1.cpu())
+    y_cat = torch.cat([y1, y2], dim=1)
+    if split % 128 == 0:
+        assert torch.equal(y_cat, y_all) and torch.equal(fs2, fs_all)
+    else:
+        assert_close(y_cat, y_all.double().cpu().numpy(), 1e-5, "y")
+        assert_close(fs2, fs_all.double().cpu().numpy(), 1e-5, "final_state")
+
+
+def test_ssd_initial_state_in_place():
+    """initial_state may be final_state itself: the state is updated in place."""
+    batch, nheads = 2, 4
+    inp = inputs.ssd_inputs(batch, 256, nheads, 64, 128, 1, "bf16", seed=90)
+    d = {k: v.cuda() for k, v in inp.items()}
+    h0 = torch.randn(batch, nheads, 64, 128, generator=torch.Generator().manual_seed(6)).cuda()
+    ref_y, ref_fs = _run(inp, h0=h0.cpu())
+    state = h0.clone()
+    y = torch.empty(d["x"].shape, device="cuda")
+    binding.ssd_chunked_fwd(d["x"], d["dt"], d["A_head"], d["B"], d["C"], 64, out_dtype=torch.float32,
+                            y=y, final_state=state, initial_state=state)
+    torch.cuda.synchronize()
+    assert torch.equal(y, ref_y) and torch.equal(state, ref_fs)
+
+
+def test_ssd_zero_length_passes_state_through():
+    x = torch.zeros(2, 0, 4, 64, dtype=torch.bfloat16, device="cuda")
+    dt = torch.zeros(2, 0, 4, device="cuda")
+    A = -torch.ones(4, device="cuda")
+    B = torch.zeros(2, 0, 1, 128, dtype=torch.bfloat16, device="cuda")
+    h0 = torch.randn(2, 4, 64, 128, device="cuda")
+    fs = torch.full((2, 4, 64, 128), 7.0, device="cuda")
+    binding.ssd_chunked_fwd(x, dt, A, B, B, 64, final_state=fs, initial_state=h0)
+    torch.cuda.synchronize()
+    assert torch.equal(fs, h0)
