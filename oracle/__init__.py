@@ -58,6 +58,9 @@ def _load():
             lib.oracle_ssd_recurrence.argtypes = [dp] * 8 + [i] * 6
             lib.oracle_ssd_chunked.argtypes = [dp] * 8 + [i] * 7
             lib.oracle_decode_step.argtypes = [dp] * 9 + [i] * 5
+            lib.oracle_mamba3_recurrence.argtypes = [dp] * 11 + [i] * 6
+            lib.oracle_mamba3_chunked.argtypes = [dp] * 11 + [i] * 7
+            lib.oracle_mamba3_decode_step.argtypes = [dp] * 12 + [i] * 5
             lib.oracle_combine.argtypes = [ctypes.c_double] * 4 + [dp, dp]
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -164,6 +167,66 @@ def ssd_chunked(x, dt, A_head, B, C, chunk, h0=None):
     hs = np.empty((batch, nheads, headdim, dstate), np.float64)
     _load().oracle_ssd_chunked(*[_ptr(a) for a in arrs], _ptr(y), _ptr(hs), *dims, int(chunk))
     return y, hs
+
+
+def _mamba3_args(x, dt, lam, A_head, B, C, h0, prev_B, prev_x):
+    (x, dt, lam, A_head, B, C, h0, prev_B, prev_x) = (
+        _f64(t) for t in (x, dt, lam, A_head, B, C, h0, prev_B, prev_x))
+    batch, seqlen, nheads, headdim = x.shape
+    ngroups, dstate = B.shape[2], B.shape[3]
+    assert dt.shape == (batch, seqlen, nheads) and lam.shape == dt.shape
+    assert A_head.shape == (nheads,) and C.shape == B.shape
+    assert B.shape == (batch, seqlen, ngroups, dstate) and nheads % ngroups == 0
+    assert (prev_B is None) == (prev_x is None)
+    if prev_B is not None:
+        assert prev_B.shape == (batch, ngroups, dstate)
+        assert prev_x.shape == (batch, nheads, headdim)
+    return ((x, dt, lam, A_head, B, C, h0, prev_B, prev_x),
+            (batch, seqlen, nheads, headdim, dstate, ngroups))
+
+
+def mamba3_recurrence(x, dt, lam, A_head, B, C, h0=None, prev_B=None, prev_x=None):
+    """Mamba-3 SISO by the step-by-step recurrence (Eq. 9).  x: (B, L, H, P);
+    dt, lam: (B, L, H) (dt after softplus, lam after sigmoid); A_head: (H,);
+    B, C: (B, L, G, N); h0: (B, H, P, N); prev_B: (B, G, N) and prev_x: (B, H, P),
+    the token before the first.  Returns (y (B, L, H, P), state (B, H, P, N))."""
+    arrs, dims = _mamba3_args(x, dt, lam, A_head, B, C, h0, prev_B, prev_x)
+    batch, seqlen, nheads, headdim, dstate, _ = dims
+    y = np.empty((batch, seqlen, nheads, headdim), np.float64)
+    hs = np.empty((batch, nheads, headdim, dstate), np.float64)
+    _load().oracle_mamba3_recurrence(*[_ptr(a) for a in arrs], _ptr(y), _ptr(hs), *dims)
+    return y, hs
+
+
+def mamba3_chunked(x, dt, lam, A_head, B, C, chunk, h0=None, prev_B=None, prev_x=None):
+    """Mamba-3 SISO by the chunked single-SSD form with the diagonal correction
+    (fp64 loops), for pinning against the recurrence."""
+    arrs, dims = _mamba3_args(x, dt, lam, A_head, B, C, h0, prev_B, prev_x)
+    batch, seqlen, nheads, headdim, dstate, _ = dims
+    y = np.empty((batch, seqlen, nheads, headdim), np.float64)
+    hs = np.empty((batch, nheads, headdim, dstate), np.float64)
+    _load().oracle_mamba3_chunked(*[_ptr(a) for a in arrs], _ptr(y), _ptr(hs), *dims,
+                                  int(chunk))
+    return y, hs
+
+
+def mamba3_decode_step(state, prev_B, prev_x, x, dt, lam, A, B, C, D=None, z=None):
+    """One Mamba-3 SISO decode step.  state: (B, H, P, N) (not modified; a new
+    array is returned); prev_B, B, C: (B, G, N); prev_x, x, z: (B, H, P);
+    dt, lam: (B, H); A, D: (H,).  Returns (y (B, H, P), new_state)."""
+    st = _f64(state).copy()
+    prev_B, prev_x, x, dt, lam, A, B, C, D, z = (
+        _f64(t) for t in (prev_B, prev_x, x, dt, lam, A, B, C, D, z))
+    batch, nheads, headdim, dstate = st.shape
+    ngroups = B.shape[1]
+    assert x.shape == (batch, nheads, headdim) and prev_x.shape == x.shape
+    assert dt.shape == (batch, nheads) and lam.shape == dt.shape
+    assert B.shape == (batch, ngroups, dstate) and C.shape == B.shape and prev_B.shape == B.shape
+    y = np.empty((batch, nheads, headdim), np.float64)
+    _load().oracle_mamba3_decode_step(_ptr(st), _ptr(prev_B), _ptr(prev_x), _ptr(x), _ptr(dt),
+                                      _ptr(lam), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                      _ptr(y), batch, nheads, headdim, dstate, ngroups)
+    return y, st
 
 
 def decode_step(state, x, dt, A, B, C, D=None, z=None):

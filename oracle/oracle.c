@@ -30,6 +30,12 @@
  *  [P2] same page, section "Kernel details", mamba3_siso_ssd_kernel: the
  *       chunked form (chunk 64, Mamba-2 SSD structure) is mathematically
  *       equivalent to the step-by-step recurrence (oracle_ssd_chunked).
+ *  [P2] same page, "How it works", Phase 0 with a general lambda:
+ *       gamma = lambda dt, beta = (dt - gamma) alpha, and Eq. 9 with its
+ *       beta prev_Bx term (oracle_mamba3_*); "Kernel details",
+ *       mamba3_siso_ssd_kernel: the single-SSD form with
+ *       scale = gamma + dt_{t+1} (1 - lambda_{t+1}) and a diagonal
+ *       correction (oracle_mamba3_chunked).
  *
  * Readings taken where the pages are silent (each is listed with its reason
  * in the design notes):
@@ -402,6 +408,217 @@ void oracle_decode_step(double* state, const double* x, const double* dt,
 }
 
 /* Number of OpenMP threads the oracle's parallel loops use. */
+/*
+ * Mamba-3 SISO recurrence, one step after another.
+ * [P2] "How it works", Phase 0 (alpha = exp(dt A), gamma = lambda dt,
+ * beta = (dt - gamma) alpha) and decode via step(), Eq. 9:
+ *   h_t = alpha_t h_{t-1} + beta_t (B_{t-1} (x) x_{t-1}) + gamma_t (B_t (x) x_t),
+ *   y_t = C_t^T h_t.
+ * dt and lambda are taken as given (dt after softplus, lambda after sigmoid).
+ * The term before the first step uses h0 (NULL: 0) and the previous token's
+ * B and x, prev_B (batch, ngroups, dstate) and prev_x (batch, nheads,
+ * headdim) (NULL: no previous token).
+ *
+ *   x, y : (batch, seqlen, nheads, headdim);  dt, lam : (batch, seqlen, nheads)
+ *   A_head : (nheads,);  Bm, Cm : (batch, seqlen, ngroups, dstate)
+ *   h0, final_state : (batch, nheads, headdim, dstate); either may be NULL
+ */
+void oracle_mamba3_recurrence(const double* x, const double* dt, const double* lam,
+                              const double* A_head, const double* Bm, const double* Cm,
+                              const double* h0, const double* prev_B, const double* prev_x,
+                              double* y, double* final_state, int batch, int seqlen, int nheads,
+                              int headdim, int dstate, int ngroups)
+{
+    const int heads_per_group = nheads / ngroups;
+    const long long rows = (long long)batch * nheads * headdim;
+#pragma omp parallel for schedule(dynamic, 8)
+    for (long long row = 0; row < rows; ++row) {
+        const int p = (int)(row % headdim);
+        const int h = (int)((row / headdim) % nheads);
+        const int b = (int)(row / ((long long)headdim * nheads));
+        const int g = h / heads_per_group;
+        double* S = (double*)malloc(sizeof(double) * (size_t)dstate);
+        double* Bprev = (double*)malloc(sizeof(double) * (size_t)dstate);
+        for (int n = 0; n < dstate; ++n) {
+            S[n] = h0 ? h0[row * dstate + n] : 0.0;
+            Bprev[n] = prev_B ? prev_B[((size_t)b * ngroups + g) * dstate + n] : 0.0;
+        }
+        double xprev = prev_x ? prev_x[row] : 0.0;
+        for (int t = 0; t < seqlen; ++t) {
+            const size_t bt = (size_t)b * seqlen + t;
+            const double dtv = dt[bt * nheads + h];
+            const double alpha = exp(dtv * A_head[h]);
+            const double gamma = lam[bt * nheads + h] * dtv;
+            const double beta = (dtv - gamma) * alpha;
+            const double xv = x[(bt * nheads + h) * headdim + p];
+            const double* Bt = Bm + (bt * ngroups + g) * dstate;
+            const double* Ct = Cm + (bt * ngroups + g) * dstate;
+            double acc = 0.0;
+            for (int n = 0; n < dstate; ++n) {
+                S[n] = alpha * S[n] + beta * Bprev[n] * xprev + gamma * Bt[n] * xv;
+                acc += Ct[n] * S[n];
+            }
+            y[(bt * nheads + h) * headdim + p] = acc;
+            for (int n = 0; n < dstate; ++n) Bprev[n] = Bt[n];
+            xprev = xv;
+        }
+        if (final_state)
+            for (int n = 0; n < dstate; ++n) final_state[row * dstate + n] = S[n];
+        free(S);
+        free(Bprev);
+    }
+}
+
+/*
+ * Mamba-3 SISO, chunked single-SSD form.
+ * [P2] "Kernel details", mamba3_siso_ssd_kernel: the Mamba-2 chunked SSD
+ * (as oracle_ssd_chunked) with x weighted by
+ *   scale_s = gamma_s + dt_{s+1} (1 - lambda_{s+1})   (0 past the last step)
+ * instead of dt_s, and a diagonal correction: on the diagonal (s = t) the
+ * weight is gamma_t alone, since the beta_{t+1} part of step s reaches the
+ * state only at step t + 1.  The carried state is therefore the true state
+ * plus the not-yet-applied dt_{t+1} (1 - lambda_{t+1}) (B_t (x) x_t) of the
+ * chunk's last step, which is exactly what the next chunk's decay turns into
+ * its beta term.  Before the first step that pending term comes from the
+ * previous token: S = h0 + dt_0 (1 - lambda_0) (prev_B (x) prev_x).
+ * Arguments as oracle_mamba3_recurrence, plus the chunk length.
+ */
+void oracle_mamba3_chunked(const double* x, const double* dt, const double* lam,
+                           const double* A_head, const double* Bm, const double* Cm,
+                           const double* h0, const double* prev_B, const double* prev_x,
+                           double* y, double* final_state, int batch, int seqlen, int nheads,
+                           int headdim, int dstate, int ngroups, int chunk)
+{
+    const int heads_per_group = nheads / ngroups;
+    const long long units = (long long)batch * nheads;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long long unit = 0; unit < units; ++unit) {
+        const int h = (int)(unit % nheads);
+        const int b = (int)(unit / nheads);
+        const int g = h / heads_per_group;
+        const double Ah = A_head[h];
+        double* S = (double*)calloc((size_t)headdim * dstate, sizeof(double));
+        double* cs = (double*)malloc(sizeof(double) * (size_t)chunk);
+        double* w = (double*)malloc(sizeof(double) * (size_t)chunk);
+        double* wd = (double*)malloc(sizeof(double) * (size_t)chunk);
+        double* M = (double*)malloc(sizeof(double) * (size_t)chunk * chunk);
+        double* Sc = (double*)malloc(sizeof(double) * (size_t)headdim * dstate);
+#define DTA(t) dt[((size_t)b * seqlen + (t)) * nheads + h]
+#define LMA(t) lam[((size_t)b * seqlen + (t)) * nheads + h]
+        for (int p = 0; p < headdim; ++p)
+            for (int n = 0; n < dstate; ++n) {
+                double s0 = h0 ? h0[(((size_t)b * nheads + h) * headdim + p) * dstate + n] : 0.0;
+                if (prev_B && prev_x && seqlen > 0)
+                    s0 += DTA(0) * (1.0 - LMA(0)) *
+                          prev_B[((size_t)b * ngroups + g) * dstate + n] *
+                          prev_x[((size_t)b * nheads + h) * headdim + p];
+                S[(size_t)p * dstate + n] = s0;
+            }
+        for (int t0 = 0; t0 < seqlen; t0 += chunk) {
+            const int q = seqlen - t0 < chunk ? seqlen - t0 : chunk;
+#define XV(i, p) x[(((size_t)b * seqlen + t0 + (i)) * nheads + h) * headdim + (p)]
+#define BV(i, n) Bm[(((size_t)b * seqlen + t0 + (i)) * ngroups + g) * dstate + (n)]
+#define CV(i, n) Cm[(((size_t)b * seqlen + t0 + (i)) * ngroups + g) * dstate + (n)]
+            double run = 0.0;
+            for (int i = 0; i < q; ++i) {
+                const int t = t0 + i;
+                run += DTA(t) * Ah;
+                cs[i] = run;
+                wd[i] = LMA(t) * DTA(t);  /* gamma_t: the diagonal weight */
+                w[i] = wd[i] + (t + 1 < seqlen ? DTA(t + 1) * (1.0 - LMA(t + 1)) : 0.0);
+            }
+            for (int i = 0; i < q; ++i)
+                for (int j = 0; j < q; ++j) {
+                    double m = 0.0;
+                    if (i >= j) {
+                        double gij = 0.0;
+                        for (int n = 0; n < dstate; ++n) gij += CV(i, n) * BV(j, n);
+                        m = gij * exp(cs[i] - cs[j]) * (j < i ? w[j] : wd[j]);
+                    }
+                    M[(size_t)i * chunk + j] = m;
+                }
+            for (int i = 0; i < q; ++i)
+                for (int p = 0; p < headdim; ++p) {
+                    double yd = 0.0;
+                    for (int j = 0; j <= i; ++j) yd += M[(size_t)i * chunk + j] * XV(j, p);
+                    double yo = 0.0;
+                    for (int n = 0; n < dstate; ++n) yo += CV(i, n) * S[(size_t)p * dstate + n];
+                    yo = exp(cs[i]) * yo;
+                    y[(((size_t)b * seqlen + t0 + i) * nheads + h) * headdim + p] = yd + yo;
+                }
+            for (int p = 0; p < headdim; ++p)
+                for (int n = 0; n < dstate; ++n) {
+                    double s = 0.0;
+                    for (int j = 0; j < q; ++j)
+                        s += exp(cs[q - 1] - cs[j]) * w[j] * XV(j, p) * BV(j, n);
+                    Sc[(size_t)p * dstate + n] = s;
+                }
+            const double decay = exp(cs[q - 1]);
+            for (size_t k = 0; k < (size_t)headdim * dstate; ++k) S[k] = decay * S[k] + Sc[k];
+#undef XV
+#undef BV
+#undef CV
+        }
+#undef DTA
+#undef LMA
+        if (final_state)
+            for (int p = 0; p < headdim; ++p)
+                for (int n = 0; n < dstate; ++n)
+                    final_state[(((size_t)b * nheads + h) * headdim + p) * dstate + n] =
+                        S[(size_t)p * dstate + n];
+        free(S);
+        free(cs);
+        free(w);
+        free(wd);
+        free(M);
+        free(Sc);
+    }
+}
+
+/*
+ * One Mamba-3 SISO decode step, updating `state` in place.
+ * [P2] "How it works", decode via step(), Eq. 9, and Phase 5 (D skip, silu).
+ *
+ *   alpha = exp(dt A_h), gamma = lambda dt, beta = (dt - gamma) alpha;
+ *   s = alpha s + beta prev_B (x) prev_x + gamma B (x) x;
+ *   y = sum_n C s + D_h x;  y *= silu(z) if z given.
+ * prev_B (batch, ngroups, dstate) and prev_x (batch, nheads, headdim) are the
+ * previous token's B and x; dt, lam (batch, nheads); other arguments as
+ * oracle_decode_step.
+ */
+void oracle_mamba3_decode_step(double* state, const double* prev_B, const double* prev_x,
+                               const double* x, const double* dt, const double* lam,
+                               const double* A, const double* Bm, const double* Cm,
+                               const double* Dskip, const double* z, double* y, int batch,
+                               int nheads, int headdim, int dstate, int ngroups)
+{
+    const int heads_per_group = nheads / ngroups;
+    const long long rows = (long long)batch * nheads * headdim;
+#pragma omp parallel for schedule(static)
+    for (long long row = 0; row < rows; ++row) {
+        const int h = (int)((row / headdim) % nheads);
+        const int b = (int)(row / ((long long)headdim * nheads));
+        const int g = h / heads_per_group;
+        const double dtv = dt[(size_t)b * nheads + h];
+        const double alpha = exp(A[h] * dtv);
+        const double gamma = lam[(size_t)b * nheads + h] * dtv;
+        const double beta = alpha * (dtv - gamma);
+        const double xv = x[row], xp = prev_x[row];
+        const double* Bt = Bm + ((size_t)b * ngroups + g) * dstate;
+        const double* Bp = prev_B + ((size_t)b * ngroups + g) * dstate;
+        const double* Ct = Cm + ((size_t)b * ngroups + g) * dstate;
+        double* s = state + row * dstate;
+        double acc = 0.0;
+        for (int n = 0; n < dstate; ++n) {
+            s[n] = alpha * s[n] + beta * Bp[n] * xp + gamma * Bt[n] * xv;
+            acc += Ct[n] * s[n];
+        }
+        double out = acc + (Dskip ? xv * Dskip[h] : 0.0);
+        if (z) out *= silu_d(z[row]);
+        y[row] = out;
+    }
+}
+
 int oracle_num_threads(void)
 {
     int n = 1;

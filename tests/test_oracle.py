@@ -413,3 +413,128 @@ def test_mamba3_three_term_update_reduces_at_lambda_one():
     np.testing.assert_allclose(state, h_m3, rtol=1e-12, atol=1e-13)
     y_half, _ = mamba3(0.5)
     assert np.max(np.abs(y_half - y_m3)) > 1e-3  # lambda matters away from 1
+
+
+# ------------------------------------------------------ Mamba-3 SISO pins
+
+def _mamba3_case(seed, batch=2, seqlen=13, nheads=4, headdim=3, dstate=5, ngroups=2,
+                 lam_value=None):
+    rng = _rng(seed)
+    x = rng.standard_normal((batch, seqlen, nheads, headdim))
+    dt = rng.uniform(0.02, 0.5, (batch, seqlen, nheads))
+    if lam_value is None:
+        lam = 1.0 / (1.0 + np.exp(-rng.standard_normal((batch, seqlen, nheads))))
+    else:
+        lam = np.full((batch, seqlen, nheads), float(lam_value))
+    A_head = -rng.uniform(1, 8, nheads)
+    B = rng.standard_normal((batch, seqlen, ngroups, dstate))
+    C = rng.standard_normal((batch, seqlen, ngroups, dstate))
+    h0 = rng.standard_normal((batch, nheads, headdim, dstate))
+    prev_B = rng.standard_normal((batch, ngroups, dstate))
+    prev_x = rng.standard_normal((batch, nheads, headdim))
+    return dict(x=x, dt=dt, lam=lam, A_head=A_head, B=B, C=C, h0=h0, prev_B=prev_B,
+                prev_x=prev_x)
+
+
+def _mamba3_bruteforce(x, dt, lam, A_head, B, C, h0, prev_B, prev_x):
+    """Eq. 9 unrolled with explicit products (O(L^2)):
+    h_t = (prod_{k<=t} alpha_k) h0
+          + sum_{s<=t} (prod_{s<k<=t} alpha_k) (gamma_s u_s + beta_s u_{s-1}),
+    u_s = B_s (x) x_s, u_{-1} = prev_B (x) prev_x; y_t = C_t . h_t."""
+    batch, seqlen, nheads, headdim = x.shape
+    ngroups, dstate = B.shape[2], B.shape[3]
+    hpg = nheads // ngroups
+    y = np.zeros_like(x)
+    hs = np.zeros((batch, nheads, headdim, dstate))
+    for b in range(batch):
+        for h in range(nheads):
+            g = h // hpg
+            alpha = np.exp(dt[b, :, h] * A_head[h])
+            gamma = lam[b, :, h] * dt[b, :, h]
+            beta = (dt[b, :, h] - gamma) * alpha
+            u = [np.outer(x[b, s, h], B[b, s, g]) for s in range(seqlen)]
+            u_prev = np.outer(prev_x[b, h], prev_B[b, g])
+            for t in range(seqlen):
+                ht = np.prod(alpha[:t + 1]) * h0[b, h]
+                for s in range(t + 1):
+                    carry = np.prod(alpha[s + 1:t + 1])
+                    before = u[s - 1] if s > 0 else u_prev
+                    ht = ht + carry * (gamma[s] * u[s] + beta[s] * before)
+                y[b, t, h] = ht @ C[b, t, g]
+                if t == seqlen - 1:
+                    hs[b, h] = ht
+    return y, hs
+
+
+def test_mamba3_recurrence_bruteforce():
+    c = _mamba3_case(101)
+    y, hs = oracle.mamba3_recurrence(**c)
+    y_ref, hs_ref = _mamba3_bruteforce(**c)
+    np.testing.assert_allclose(y, y_ref, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(hs, hs_ref, rtol=1e-11, atol=1e-12)
+
+
+def test_mamba3_lambda_one_is_mamba2():
+    """lambda = 1: gamma = dt, beta = 0, the previous token drops out and Eq. 9
+    is the Mamba-2 update of ssd_recurrence."""
+    c = _mamba3_case(103, lam_value=1.0)
+    y, hs = oracle.mamba3_recurrence(**c)
+    y2, hs2 = oracle.ssd_recurrence(c["x"], c["dt"], c["A_head"], c["B"], c["C"], c["h0"])
+    np.testing.assert_allclose(y, y2, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(hs, hs2, rtol=1e-12, atol=1e-13)
+
+
+def test_mamba3_lambda_zero_is_shifted_mamba2():
+    """lambda = 0: gamma = 0, beta = dt alpha, so h_t = alpha_t h_{t-1} +
+    dt_t (alpha_t u_{t-1}): the Mamba-2 recurrence on the inputs shifted one
+    step later (x'_t = alpha_t x_{t-1}, B'_t = B_{t-1}, the first from the
+    previous token)."""
+    c = _mamba3_case(107, lam_value=0.0)
+    y, hs = oracle.mamba3_recurrence(**c)
+    alpha = np.exp(c["dt"] * c["A_head"][None, None, :])
+    xs = np.concatenate([c["prev_x"][:, None], c["x"][:, :-1]], axis=1) * alpha[..., None]
+    Bs = np.concatenate([c["prev_B"][:, None], c["B"][:, :-1]], axis=1)
+    y2, hs2 = oracle.ssd_recurrence(xs, c["dt"], c["A_head"], Bs, c["C"], c["h0"])
+    np.testing.assert_allclose(y, y2, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(hs, hs2, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("chunk", [1, 2, 5, 13, 64])
+@pytest.mark.parametrize("with_prev", [False, True])
+def test_mamba3_chunked_single_ssd_equals_recurrence(chunk, with_prev):
+    c = _mamba3_case(109)
+    if not with_prev:
+        c["prev_B"] = c["prev_x"] = None
+        c["h0"] = None
+    y, hs = oracle.mamba3_recurrence(**c)
+    yc, hc = oracle.mamba3_chunked(chunk=chunk, **c)
+    np.testing.assert_allclose(yc, y, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(hc, hs, rtol=1e-11, atol=1e-12)
+
+
+def test_mamba3_decode_chain_equals_recurrence():
+    c = _mamba3_case(113, seqlen=9)
+    y_ref, hs_ref = oracle.mamba3_recurrence(**c)
+    state, pB, px = c["h0"].copy(), c["prev_B"], c["prev_x"]
+    for t in range(c["x"].shape[1]):
+        y, state = oracle.mamba3_decode_step(state, pB, px, c["x"][:, t], c["dt"][:, t],
+                                             c["lam"][:, t], c["A_head"], c["B"][:, t],
+                                             c["C"][:, t])
+        np.testing.assert_allclose(y, y_ref[:, t], rtol=1e-12, atol=1e-13)
+        pB, px = c["B"][:, t], c["x"][:, t]
+    np.testing.assert_allclose(state, hs_ref, rtol=1e-12, atol=1e-13)
+
+
+def test_mamba3_decode_skip_and_gate():
+    """D skip then silu gate on top of the state read-out, as in the Mamba-2 decode."""
+    c = _mamba3_case(127, seqlen=1)
+    rng = _rng(128)
+    D = rng.standard_normal(c["A_head"].shape)
+    z = rng.standard_normal(c["prev_x"].shape)
+    args = (c["h0"], c["prev_B"], c["prev_x"], c["x"][:, 0], c["dt"][:, 0], c["lam"][:, 0],
+            c["A_head"], c["B"][:, 0], c["C"][:, 0])
+    y0, s0 = oracle.mamba3_decode_step(*args)
+    y1, s1 = oracle.mamba3_decode_step(*args, D=D, z=z)
+    np.testing.assert_array_equal(s0, s1)
+    np.testing.assert_allclose(y1, (y0 + D[None, :, None] * c["x"][:, 0]) * _silu_np(z),
+                               rtol=1e-13, atol=1e-14)

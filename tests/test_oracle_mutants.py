@@ -50,6 +50,17 @@ MUTANTS = {
                             "double out = acc;"),
     "decode_alpha_without_dt": ("const double alpha = exp(dtv * A[h]);",
                                 "const double alpha = exp(A[h]);"),
+    "mamba3_beta_without_alpha": ("const double beta = (dtv - gamma) * alpha;",
+                                  "const double beta = (dtv - gamma);"),
+    "mamba3_previous_x_not_advanced": ("            xprev = xv;\n", "\n"),
+    "mamba3_chunked_diagonal_not_corrected": ("(j < i ? w[j] : wd[j])", "w[j]"),
+    "mamba3_chunked_scale_uses_this_lambda": ("DTA(t + 1) * (1.0 - LMA(t + 1))",
+                                              "DTA(t + 1) * (1.0 - LMA(t))"),
+    "mamba3_chunked_drops_previous_token": ("s0 += DTA(0) * (1.0 - LMA(0)) *",
+                                            "s0 += 0.0 * DTA(0) * (1.0 - LMA(0)) *"),
+    "mamba3_decode_terms_swapped": (
+        "s[n] = alpha * s[n] + beta * Bp[n] * xp + gamma * Bt[n] * xv;",
+        "s[n] = alpha * s[n] + beta * Bt[n] * xv + gamma * Bp[n] * xp;"),
 }
 
 
