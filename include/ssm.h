@@ -6,6 +6,8 @@
  *   ssm_scan_fwd     selective scan, per-channel per-state A (Mamba-1 form)
  *   ssd_chunked_fwd  scalar-A-per-head chunked SSD (Mamba-2 form), tensor cores
  *   ssm_decode_step  single-token state update, in place
+ *   ssd_mamba3_fwd, ssm_decode_step_mamba3  the same two for Mamba-3 SISO
+ *                    (trapezoidal three-term recurrence)
  *
  * Conventions shared by every entry point
  *  - Pointers are DEVICE pointers unless stated otherwise, to dense row-major
@@ -141,6 +143,38 @@ ssm_status_t ssd_chunked_fwd(const void* x, const float* dt, const float* A_head
                              void* stream);
 
 /*
+ * Mamba-3 SISO chunked prefill (trapezoidal discretisation), scalar A per head.
+ *   "Mamba-3 NKI Kernels for AWS Neuron", section "How it works" (Phase 0:
+ *   alpha = exp(dt A), gamma = lambda dt, beta = (dt - gamma) alpha; Eq. 9)
+ *   and section "Kernel details", mamba3_siso_ssd_kernel (single-SSD form
+ *   with scale = gamma + dt_{t+1} (1 - lambda_{t+1}) and a diagonal
+ *   correction, chunk 64).
+ *
+ * Computes, exactly up to rounding, the recurrence (u_t = B[b,t,g] (x) x[b,t,h])
+ *   S = alpha_t S + beta_t u_{t-1} + gamma_t u_t,   y[b,t,h,p] = sum_n C[b,t,g,n] S[p,n]
+ * from S = initial_state[b,h] (0 when NULL), where u_{-1} = prev_B[b,g] (x)
+ * prev_x[b,h] is the token before the first (both NULL: none).  dt and lam
+ * are taken as given (dt after softplus, lambda after sigmoid); rotary
+ * position terms on B and C are applied by the caller (B, C are the rotated
+ * tensors; per-head rotations use ngroups == nheads).  final_state is S after
+ * the last step; with prev_B = B[:, L-1], prev_x = x[:, L-1] a later call
+ * (or ssm_decode_step_mamba3) continues the sequence.
+ *
+ * Layouts as ssd_chunked_fwd; lam (batch, seqlen, nheads) fp32; prev_B
+ * (batch, ngroups, dstate) and prev_x (batch, nheads, headdim) in in_dtype.
+ * Supported: as ssd_chunked_fwd.  prev_B and prev_x must be both NULL or both
+ * given (else SSM_ERR_NULL); lam must be given.  The pages give no
+ * counterpart to the resumption inputs: they follow from Eq. 9.
+ */
+ssm_status_t ssd_mamba3_fwd(const void* x, const float* dt, const float* lam,
+                            const float* A_head, const void* B, const void* C, int chunk,
+                            const float* initial_state, const void* prev_B, const void* prev_x,
+                            void* y, float* final_state,
+                            int batch, int seqlen, int nheads, int headdim, int dstate,
+                            int ngroups, ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                            void* stream);
+
+/*
  * One decode step, in place.
  *   "Mamba-3 NKI Kernels for AWS Neuron", section "How it works", decode via
  *   step(), Eq. 9 with lambda = 1 (beta = 0, gamma = dt), and Phase 5 (D skip,
@@ -160,6 +194,28 @@ ssm_status_t ssm_decode_step(float* state, const void* x, const float* dt,
                              const float* D, const void* z, void* y,
                              int batch, int nheads, int headdim, int dstate, int ngroups,
                              ssm_dtype_t dtype, void* stream);
+
+/*
+ * One Mamba-3 SISO decode step, in place.
+ *   "Mamba-3 NKI Kernels for AWS Neuron", section "How it works", decode via
+ *   step(), Eq. 9 (h_t = alpha h_{t-1} + beta prev_Bx + gamma B_t (x) x_t,
+ *   y_t = C_t^T h_t) and Phase 5; section "Kernel details",
+ *   mamba3_siso_decode_state_kernel.
+ *
+ *   alpha = exp(dt A), gamma = lam dt, beta = (dt - gamma) alpha
+ *   state = alpha state + beta prev_B (x) prev_x + gamma B (x) x
+ *   y = (sum_n C state + D x) * silu(z)
+ *
+ * Arguments as ssm_decode_step, plus lam (batch, nheads) fp32 (lambda after
+ * sigmoid) and the previous token's prev_B (batch, ngroups, dstate) and
+ * prev_x (batch, nheads, headdim) in dtype (all required; pass the last
+ * prefill token's B and x after ssd_mamba3_fwd, then each step's own).
+ */
+ssm_status_t ssm_decode_step_mamba3(float* state, const void* prev_B, const void* prev_x,
+                                    const void* x, const float* dt, const float* lam,
+                                    const float* A, const void* B, const void* C, const float* D,
+                                    const void* z, void* y, int batch, int nheads, int headdim,
+                                    int dstate, int ngroups, ssm_dtype_t dtype, void* stream);
 
 /*
  * Selective scan for callers that cannot allocate device memory.

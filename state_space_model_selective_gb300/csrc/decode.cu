@@ -52,13 +52,23 @@ __device__ __forceinline__ void load16(const T* p, float* v) {
 // four 16-byte loads each); the CTA's 256 threads cover 256 / LPR rows at a
 // time, and each thread handles up to RPT rows with all their loads issued
 // before any arithmetic.
-template <typename T, int LPR>
+// Mamba-3 SISO inputs of a decode step (M3 kernels only): lambda (batch,
+// nheads) fp32 and the previous token's B (batch, ngroups, dstate) and x
+// (batch, nheads, headdim).
+template <typename T>
+struct M3In {
+    const float* lam;
+    const T* prev_B;
+    const T* prev_x;
+};
+
+template <typename T, int LPR, bool M3>
 __global__ void __launch_bounds__(256, 3)
     decode_kernel(float* __restrict__ state, const T* __restrict__ x,
                   const float* __restrict__ dt, const float* __restrict__ A,
                   const T* __restrict__ Bm, const T* __restrict__ Cm,
                   const float* __restrict__ Dskip, const T* __restrict__ z, T* __restrict__ y,
-                  int nheads, int headdim, int ngroups) {
+                  int nheads, int headdim, int ngroups, M3In<T> m3) {
     constexpr int kDstate = LPR * 16;
     constexpr int kRowsPerPass = 256 / LPR;
     constexpr int RPT = 2;
@@ -68,16 +78,19 @@ __global__ void __launch_bounds__(256, 3)
     const int part = threadIdx.x % LPR;
     const int r0 = threadIdx.x / LPR;
 
-    __shared__ __align__(16) float sB[kDstate], sC[kDstate];
+    __shared__ __align__(16) float sB[kDstate], sC[kDstate], sBp[M3 ? kDstate : 4];
     const long long row_base = (b * nheads + h) * (long long)headdim;
     const long long bc0 = (b * ngroups + g) * kDstate;
     const float4* sB4 = reinterpret_cast<const float4*>(sB + part * 16);
     const float4* sC4 = reinterpret_cast<const float4*>(sC + part * 16);
-    float dtv = 0.0f, alpha = 0.0f, Dh = 0.0f;
+    const float4* sBp4 = reinterpret_cast<const float4*>(sBp + (M3 ? part * 16 : 0));
+    // input weight of B (x) x (Mamba-2: dt; Mamba-3: gamma) and of the
+    // previous token's term (Mamba-3: beta)
+    float wx = 0.0f, wp = 0.0f, alpha = 0.0f, Dh = 0.0f;
 
     for (int p0 = 0; p0 < headdim; p0 += kRowsPerPass * RPT) {
         float s[RPT][16];
-        float xv[RPT], zv[RPT];
+        float xv[RPT], zv[RPT], xpv[RPT];
         bool act[RPT];
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
@@ -92,15 +105,22 @@ __global__ void __launch_bounds__(256, 3)
             }
             xv[r] = act[r] ? to_f32(x[row]) : 0.0f;
             zv[r] = (act[r] && z) ? to_f32(z[row]) : 0.0f;
+            xpv[r] = (M3 && act[r]) ? to_f32(m3.prev_x[row]) : 0.0f;
         }
         if (p0 == 0) {
             // B, C, alpha: after the first rows' loads are in flight
             for (int i = threadIdx.x; i < kDstate; i += 256) {
                 sB[i] = to_f32(Bm[bc0 + i]);
                 sC[i] = to_f32(Cm[bc0 + i]);
+                if constexpr (M3) sBp[i] = to_f32(m3.prev_B[bc0 + i]);
             }
-            dtv = dt[b * nheads + h];
+            const float dtv = dt[b * nheads + h];
             alpha = expf(dtv * A[h]);
+            wx = dtv;
+            if constexpr (M3) {
+                wx = m3.lam[b * nheads + h] * dtv;  // gamma
+                wp = (dtv - wx) * alpha;            // beta
+            }
             Dh = Dskip ? Dskip[h] : 0.0f;
             __syncthreads();
         }
@@ -108,15 +128,21 @@ __global__ void __launch_bounds__(256, 3)
         for (int r = 0; r < RPT; ++r) {
             const int p = p0 + r * kRowsPerPass + r0;
             const long long row = row_base + (act[r] ? p : 0);
-            const float dbx = dtv * xv[r];
+            const float dbx = wx * xv[r], pbx = wp * xpv[r];
             float acc = 0.0f;
 #pragma unroll
             for (int i4 = 0; i4 < 4; ++i4) {
                 const float4 bq = sB4[i4], cq = sC4[i4];
                 const float bb[4] = {bq.x, bq.y, bq.z, bq.w}, cc[4] = {cq.x, cq.y, cq.z, cq.w};
+                float pp[4] = {0.f, 0.f, 0.f, 0.f};
+                if constexpr (M3) {
+                    const float4 pq = sBp4[i4];
+                    pp[0] = pq.x; pp[1] = pq.y; pp[2] = pq.z; pp[3] = pq.w;
+                }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    s[r][4 * i4 + k] = fmaf(alpha, s[r][4 * i4 + k], dbx * bb[k]);
+                    const float in = M3 ? fmaf(dbx, bb[k], pbx * pp[k]) : dbx * bb[k];
+                    s[r][4 * i4 + k] = fmaf(alpha, s[r][4 * i4 + k], in);
                     acc = fmaf(cc[k], s[r][4 * i4 + k], acc);
                 }
             }
@@ -140,16 +166,28 @@ __global__ void __launch_bounds__(256, 3)
     }
 }
 
-template <typename T, int LPR>
+template <typename T, int LPR, bool M3>
 ssm_status_t launch(float* state, const void* x, const float* dt, const float* A, const void* B,
                     const void* C, const float* D, const void* z, void* y, long long rows,
-                    int nheads, int headdim, int ngroups, cudaStream_t s) {
+                    int nheads, int headdim, int ngroups, M3In<T> m3, cudaStream_t s) {
     const long long grid = rows / headdim;  // batch * nheads
-    decode_kernel<T, LPR><<<(unsigned)grid, 256, 0, s>>>(
+    decode_kernel<T, LPR, M3><<<(unsigned)grid, 256, 0, s>>>(
         state, static_cast<const T*>(x), dt, A, static_cast<const T*>(B),
         static_cast<const T*>(C), D, static_cast<const T*>(z), static_cast<T*>(y), nheads,
-        headdim, ngroups);
+        headdim, ngroups, m3);
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+// 4 consecutive values as fp32 (8-byte bf16 or 16-byte fp32 load)
+template <typename T>
+__device__ __forceinline__ void load4(const T* p, float* v) {
+    if constexpr (sizeof(T) == 2) {
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(p));
+        v[0] = bf16lo(w.x); v[1] = bf16hi(w.x); v[2] = bf16lo(w.y); v[3] = bf16hi(w.y);
+    } else {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(p));
+        v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+    }
 }
 
 // ------------------------------------------------------- dstate 128, bulk copies
@@ -190,13 +228,14 @@ __device__ __forceinline__ void bulk_wait_all() {
 // Stage s of the two shared-memory stages holds the CTA's tiles s, s + 2, ...:
 // full[s] completes when a tile has landed, empty[s] when the compute warps
 // have updated it in place (then the producer stores it and reuses the stage).
-template <typename T>
+template <typename T, bool M3>
 __global__ void __launch_bounds__(kBulkThreads)
     decode_bulk_kernel(float* __restrict__ state, const T* __restrict__ x,
                        const float* __restrict__ dt, const float* __restrict__ A,
                        const T* __restrict__ Bm, const T* __restrict__ Cm,
                        const float* __restrict__ Dskip, const T* __restrict__ z,
-                       T* __restrict__ y, int batch, int nheads, int headdim, int ngroups) {
+                       T* __restrict__ y, int batch, int nheads, int headdim, int ngroups,
+                       M3In<T> m3) {
     extern __shared__ __align__(128) uint8_t dsm[];
     uint64_t* full = reinterpret_cast<uint64_t*>(dsm + 2 * kTileBytes);
     uint64_t* empty = full + 2;
@@ -262,26 +301,26 @@ __global__ void __launch_bounds__(kBulkThreads)
         const int g = h / (nheads / ngroups);
         // per-tile inputs, loaded before waiting for the state
         const long long bc = (b * ngroups + g) * kBulkN + 4 * lane;
-        float bv[4], cv[4];
-        if constexpr (sizeof(T) == 2) {
-            const uint2 wb = __ldg(reinterpret_cast<const uint2*>(Bm + bc));
-            const uint2 wc = __ldg(reinterpret_cast<const uint2*>(Cm + bc));
-            bv[0] = bf16lo(wb.x); bv[1] = bf16hi(wb.x); bv[2] = bf16lo(wb.y); bv[3] = bf16hi(wb.y);
-            cv[0] = bf16lo(wc.x); cv[1] = bf16hi(wc.x); cv[2] = bf16lo(wc.y); cv[3] = bf16hi(wc.y);
-        } else {
-            const float4 fb = __ldg(reinterpret_cast<const float4*>(Bm + bc));
-            const float4 fc = __ldg(reinterpret_cast<const float4*>(Cm + bc));
-            bv[0] = fb.x; bv[1] = fb.y; bv[2] = fb.z; bv[3] = fb.w;
-            cv[0] = fc.x; cv[1] = fc.y; cv[2] = fc.z; cv[3] = fc.w;
-        }
+        float bv[4], cv[4], bp[4] = {0.f, 0.f, 0.f, 0.f};
+        load4<T>(Bm + bc, bv);
+        load4<T>(Cm + bc, cv);
+        if constexpr (M3) load4<T>(m3.prev_B + bc, bp);
         const float dtv = dt[bh];
         const float alpha = expf(dtv * A[h]);
+        // input weights: Mamba-2 dt; Mamba-3 gamma = lambda dt and, for the
+        // previous token, beta = (dt - gamma) alpha
+        float wx = dtv, wp = 0.0f;
+        if constexpr (M3) {
+            wx = m3.lam[bh] * dtv;
+            wp = (dtv - wx) * alpha;
+        }
         const long long row0 = bh * headdim + p0;  // (b, h, p0) row index
-        float dbx[16];
+        float dbx[16], pbx[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
             const int p = warp + 4 * r;
-            dbx[r] = p < nr ? dtv * to_f32(x[row0 + p]) : 0.0f;
+            dbx[r] = p < nr ? wx * to_f32(x[row0 + p]) : 0.0f;
+            pbx[r] = (M3 && p < nr) ? wp * to_f32(m3.prev_x[row0 + p]) : 0.0f;
         }
         if (!mbar_wait(&full[s], (uint32_t)((i >> 1) & 1), nullptr)) break;
 
@@ -295,10 +334,14 @@ __global__ void __launch_bounds__(kBulkThreads)
             if (p < nr) {
                 float4* q = reinterpret_cast<float4*>(st + p * kBulkN) + lane;
                 const float4 v = *q;
-                const float n0 = fmaf(alpha, v.x, dbx[r] * bv[0]);
-                const float n1 = fmaf(alpha, v.y, dbx[r] * bv[1]);
-                const float n2 = fmaf(alpha, v.z, dbx[r] * bv[2]);
-                const float n3 = fmaf(alpha, v.w, dbx[r] * bv[3]);
+                float in[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    in[k] = M3 ? fmaf(dbx[r], bv[k], pbx[r] * bp[k]) : dbx[r] * bv[k];
+                const float n0 = fmaf(alpha, v.x, in[0]);
+                const float n1 = fmaf(alpha, v.y, in[1]);
+                const float n2 = fmaf(alpha, v.z, in[2]);
+                const float n3 = fmaf(alpha, v.w, in[3]);
                 *q = make_float4(n0, n1, n2, n3);
                 acc[r] = fmaf(cv[3], n3, fmaf(cv[2], n2, fmaf(cv[1], n1, cv[0] * n0)));
             }
@@ -331,10 +374,11 @@ __global__ void __launch_bounds__(kBulkThreads)
     }
 }
 
-template <typename T>
+template <typename T, bool M3>
 ssm_status_t launch_bulk(float* state, const void* x, const float* dt, const float* A,
                          const void* B, const void* C, const float* D, const void* z, void* y,
-                         int batch, int nheads, int headdim, int ngroups, cudaStream_t s) {
+                         int batch, int nheads, int headdim, int ngroups, M3In<T> m3,
+                         cudaStream_t s) {
     static std::mutex m;
     static int cached_dev = -1, sms = 0;
     int dev = 0;
@@ -345,7 +389,7 @@ ssm_status_t launch_bulk(float* state, const void* x, const float* dt, const flo
             if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
                 sms <= 0)
                 return SSM_ERR_CUDA;
-            if (cudaFuncSetAttribute(decode_bulk_kernel<T>,
+            if (cudaFuncSetAttribute(decode_bulk_kernel<T, M3>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kBulkSmem) != cudaSuccess)
                 return SSM_ERR_CUDA;
@@ -355,36 +399,46 @@ ssm_status_t launch_bulk(float* state, const void* x, const float* dt, const flo
     const long long tiles =
         (long long)batch * nheads * ((headdim + kBulkRows - 1) / kBulkRows);
     const unsigned grid = (unsigned)std::min<long long>(tiles, 3LL * sms);
-    decode_bulk_kernel<T><<<grid, kBulkThreads, kBulkSmem, s>>>(
+    decode_bulk_kernel<T, M3><<<grid, kBulkThreads, kBulkSmem, s>>>(
         state, static_cast<const T*>(x), dt, A, static_cast<const T*>(B),
         static_cast<const T*>(C), D, static_cast<const T*>(z), static_cast<T*>(y), batch, nheads,
-        headdim, ngroups);
+        headdim, ngroups, m3);
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
-template <typename T>
+template <typename T, bool M3>
 ssm_status_t by_dstate(int dstate, float* state, const void* x, const float* dt, const float* A,
                        const void* B, const void* C, const float* D, const void* z, void* y,
-                       long long rows, int nheads, int headdim, int ngroups, cudaStream_t s) {
+                       long long rows, int nheads, int headdim, int ngroups, M3In<T> m3,
+                       cudaStream_t s) {
     switch (dstate) {
-        case 16: return launch<T, 1>(state, x, dt, A, B, C, D, z, y, rows, nheads, headdim, ngroups, s);
-        case 32: return launch<T, 2>(state, x, dt, A, B, C, D, z, y, rows, nheads, headdim, ngroups, s);
-        case 64: return launch<T, 4>(state, x, dt, A, B, C, D, z, y, rows, nheads, headdim, ngroups, s);
+        case 16:
+            return launch<T, 1, M3>(state, x, dt, A, B, C, D, z, y, rows, nheads, headdim, ngroups,
+                                    m3, s);
+        case 32:
+            return launch<T, 2, M3>(state, x, dt, A, B, C, D, z, y, rows, nheads, headdim, ngroups,
+                                    m3, s);
+        case 64:
+            return launch<T, 4, M3>(state, x, dt, A, B, C, D, z, y, rows, nheads, headdim, ngroups,
+                                    m3, s);
         case 128:
-            return launch_bulk<T>(state, x, dt, A, B, C, D, z, y, (int)(rows / headdim / nheads),
-                                  nheads, headdim, ngroups, s);
-        case 256: return launch<T, 16>(state, x, dt, A, B, C, D, z, y, rows, nheads, headdim, ngroups, s);
+            return launch_bulk<T, M3>(state, x, dt, A, B, C, D, z, y,
+                                      (int)(rows / headdim / nheads), nheads, headdim, ngroups, m3,
+                                      s);
+        case 256:
+            return launch<T, 16, M3>(state, x, dt, A, B, C, D, z, y, rows, nheads, headdim,
+                                     ngroups, m3, s);
     }
     return SSM_ERR_UNSUPPORTED;
 }
 
-}  // namespace
-
-extern "C" ssm_status_t ssm_decode_step(float* state, const void* x, const float* dt,
-                                        const float* A, const void* B, const void* C,
-                                        const float* D, const void* z, void* y, int batch,
-                                        int nheads, int headdim, int dstate, int ngroups,
-                                        ssm_dtype_t dtype, void* stream) {
+// Validation and dispatch shared by the Mamba-2 (m3 = false) and Mamba-3 SISO
+// (m3 = true) decode entry points.
+ssm_status_t decode_entry(float* state, const void* x, const float* dt, const float* lam,
+                          const float* A, const void* B, const void* C, const float* D,
+                          const void* z, const void* prev_B, const void* prev_x, void* y,
+                          int batch, int nheads, int headdim, int dstate, int ngroups,
+                          ssm_dtype_t dtype, bool m3, void* stream) {
     using namespace ssm_host;
     if (batch < 0 || nheads < 0 || headdim < 0 || dstate < 1 || ngroups < 1)
         return SSM_ERR_SHAPE;
@@ -395,7 +449,8 @@ extern "C" ssm_status_t ssm_decode_step(float* state, const void* x, const float
     const long long rows = (long long)batch * nheads * headdim;
     if (rows == 0) return SSM_OK;
     if (!state || !x || !dt || !A || !B || !C || !y) return SSM_ERR_NULL;
-    const void* ptrs[] = {state, x, dt, A, B, C, D, z, y};
+    if (m3 && (!lam || !prev_B || !prev_x)) return SSM_ERR_NULL;
+    const void* ptrs[] = {state, x, dt, A, B, C, D, z, y, lam, prev_B, prev_x};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return SSM_ERR_ALIGN;
     const size_t es = dtype_size(dtype);
@@ -403,16 +458,48 @@ extern "C" ssm_status_t ssm_decode_step(float* state, const void* x, const float
     const size_t bcbytes = (size_t)batch * ngroups * dstate * es;
     struct R { const void* p; size_t n; } ins[] = {
         {x, rbytes}, {dt, (size_t)batch * nheads * 4}, {A, (size_t)nheads * 4},
-        {B, bcbytes}, {C, bcbytes}, {D, D ? (size_t)nheads * 4 : 0}, {z, z ? rbytes : 0}};
+        {B, bcbytes}, {C, bcbytes}, {D, D ? (size_t)nheads * 4 : 0}, {z, z ? rbytes : 0},
+        {lam, m3 ? (size_t)batch * nheads * 4 : 0}, {prev_B, m3 ? bcbytes : 0},
+        {prev_x, m3 ? rbytes : 0}};
     for (const R& r : ins) {
         if (overlaps(state, sbytes, r.p, r.n)) return SSM_ERR_ALIAS;
         if (overlaps(y, rbytes, r.p, r.n)) return SSM_ERR_ALIAS;
     }
     if (overlaps(y, rbytes, state, sbytes)) return SSM_ERR_ALIAS;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return dtype == SSM_BF16
-               ? by_dstate<__nv_bfloat16>(dstate, state, x, dt, A, B, C, D, z, y, rows, nheads,
-                                          headdim, ngroups, s)
-               : by_dstate<float>(dstate, state, x, dt, A, B, C, D, z, y, rows, nheads, headdim,
-                                  ngroups, s);
+    if (dtype == SSM_BF16) {
+        using T = __nv_bfloat16;
+        const M3In<T> m{lam, static_cast<const T*>(prev_B), static_cast<const T*>(prev_x)};
+        return m3 ? by_dstate<T, true>(dstate, state, x, dt, A, B, C, D, z, y, rows, nheads,
+                                       headdim, ngroups, m, s)
+                  : by_dstate<T, false>(dstate, state, x, dt, A, B, C, D, z, y, rows, nheads,
+                                        headdim, ngroups, m, s);
+    }
+    const M3In<float> m{lam, static_cast<const float*>(prev_B), static_cast<const float*>(prev_x)};
+    return m3 ? by_dstate<float, true>(dstate, state, x, dt, A, B, C, D, z, y, rows, nheads,
+                                       headdim, ngroups, m, s)
+              : by_dstate<float, false>(dstate, state, x, dt, A, B, C, D, z, y, rows, nheads,
+                                        headdim, ngroups, m, s);
+}
+
+}  // namespace
+
+extern "C" ssm_status_t ssm_decode_step(float* state, const void* x, const float* dt,
+                                        const float* A, const void* B, const void* C,
+                                        const float* D, const void* z, void* y, int batch,
+                                        int nheads, int headdim, int dstate, int ngroups,
+                                        ssm_dtype_t dtype, void* stream) {
+    return decode_entry(state, x, dt, nullptr, A, B, C, D, z, nullptr, nullptr, y, batch, nheads,
+                        headdim, dstate, ngroups, dtype, false, stream);
+}
+
+extern "C" ssm_status_t ssm_decode_step_mamba3(float* state, const void* prev_B,
+                                               const void* prev_x, const void* x,
+                                               const float* dt, const float* lam,
+                                               const float* A, const void* B, const void* C,
+                                               const float* D, const void* z, void* y, int batch,
+                                               int nheads, int headdim, int dstate, int ngroups,
+                                               ssm_dtype_t dtype, void* stream) {
+    return decode_entry(state, x, dt, lam, A, B, C, D, z, prev_B, prev_x, y, batch, nheads,
+                        headdim, dstate, ngroups, dtype, true, stream);
 }

@@ -110,6 +110,23 @@ def ssd_inputs(batch: int, seqlen: int, nheads: int, headdim: int, dstate: int,
     }
 
 
+def mamba3_inputs(batch: int, seqlen: int, nheads: int, headdim: int, dstate: int,
+                  ngroups: int = 1, dtype: str = "bf16", seed: int = 1006,
+                  device: str = "cpu") -> dict:
+    """Inputs of the Mamba-3 SISO prefill: those of ``ssd_inputs`` (drawn first,
+    from the same seed) plus lam (B, L, H) fp32 = sigmoid(N(0, 1)); the token
+    before the first, prev_B (B, G, N) and prev_x (B, H, P); and an initial
+    state h0 (B, H, P, N) fp32 ~ 0.1 N(0, 1)."""
+    out = ssd_inputs(batch, seqlen, nheads, headdim, dstate, ngroups, dtype, seed, device)
+    g = _gen(seed + 7919, device)
+    td = _DTYPES[dtype]
+    out["lam"] = torch.sigmoid(_randn((batch, seqlen, nheads), g, device)).contiguous()
+    out["prev_B"] = _randn((batch, ngroups, dstate), g, device).to(td).contiguous()
+    out["prev_x"] = _randn((batch, nheads, headdim), g, device).to(td).contiguous()
+    out["h0"] = (0.1 * _randn((batch, nheads, headdim, dstate), g, device)).contiguous()
+    return out
+
+
 def decode_inputs(batch: int, nheads: int, headdim: int, dstate: int, ngroups: int = 1,
                   steps: int = 1, dtype: str = "f32", seed: int = 1005,
                   gate: bool = False, dskip: str = "ones", device: str = "cpu") -> dict:

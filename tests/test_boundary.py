@@ -158,3 +158,49 @@ def test_binding_refuses_cpu_tensors():
     with pytest.raises(TypeError):
         binding.ssm_scan_fwd(u, u, torch.zeros(4, 16), torch.zeros(1, 1, 16, 8),
                              torch.zeros(1, 1, 16, 8))
+
+
+def m3_ssd_call(L, **kw):
+    args = dict(x=P(0), dt=P(1), lam=P(7), A=P(2), B=P(3), C=P(4), chunk=64, h0=None, pB=None,
+                px=None, y=P(5), fs=P(6), batch=2, seqlen=128, nheads=4, headdim=64, dstate=128,
+                ngroups=1, in_dt=1, out_dt=0, stream=None)
+    args.update(kw)
+    a = args
+    return L.ssd_mamba3_fwd(a["x"], a["dt"], a["lam"], a["A"], a["B"], a["C"], a["chunk"], a["h0"],
+                            a["pB"], a["px"], a["y"], a["fs"], a["batch"], a["seqlen"],
+                            a["nheads"], a["headdim"], a["dstate"], a["ngroups"], a["in_dt"],
+                            a["out_dt"], a["stream"])
+
+
+def test_mamba3_ssd_argument_errors(L):
+    assert m3_ssd_call(L, seqlen=100) == SHAPE
+    assert m3_ssd_call(L, lam=None) == NULL
+    assert m3_ssd_call(L, pB=P(8)) == NULL              # prev_B without prev_x
+    assert m3_ssd_call(L, px=P(8)) == NULL              # prev_x without prev_B
+    assert m3_ssd_call(L, dstate=64) == UNSUP
+    assert m3_ssd_call(L, lam=P(5)) == ALIAS            # lambda on top of y
+    assert m3_ssd_call(L, lam=ctypes.c_void_p(0x80000004)) == ALIGN
+    assert m3_ssd_call(L, batch=0, x=None, y=None) == OK
+
+
+def m3_decode_call(L, **kw):
+    args = dict(state=P(0), pB=P(1), px=P(2), x=P(3), dt=P(4), lam=P(5), A=P(6), B=P(7), C=P(8),
+                D=None, z=None, y=P(9), batch=2, nheads=4, headdim=64, dstate=128, ngroups=1,
+                dtype=0, stream=None)
+    args.update(kw)
+    a = args
+    return L.ssm_decode_step_mamba3(a["state"], a["pB"], a["px"], a["x"], a["dt"], a["lam"],
+                                    a["A"], a["B"], a["C"], a["D"], a["z"], a["y"], a["batch"],
+                                    a["nheads"], a["headdim"], a["dstate"], a["ngroups"],
+                                    a["dtype"], a["stream"])
+
+
+def test_mamba3_decode_argument_errors(L):
+    assert m3_decode_call(L, lam=None) == NULL
+    assert m3_decode_call(L, pB=None) == NULL
+    assert m3_decode_call(L, px=None) == NULL
+    assert m3_decode_call(L, dstate=48) == UNSUP
+    assert m3_decode_call(L, nheads=6, ngroups=4) == SHAPE
+    assert m3_decode_call(L, px=P(0)) == ALIAS          # previous x inside the state
+    assert m3_decode_call(L, y=P(1)) == ALIAS           # y on top of prev_B
+    assert m3_decode_call(L, batch=0) == OK
