@@ -318,8 +318,8 @@ def run_ours(args):
 def measure_other_paths(dev, reps=20):
     """Device time of the chunked SSD (batch 32, L 256, 32 heads, headdim 64,
     d_state 128, bf16 in, fp32 y) and of one decode step (batch 256, 32 heads,
-    headdim 64, d_state 128, fp32), against the HBM roofline of their
-    algorithmic bytes."""
+    headdim 64, d_state 128, fp32), Mamba-2 and Mamba-3 SISO forms, against
+    the HBM roofline of their algorithmic bytes."""
     import torch
     from state_space_model_selective_gb300 import binding, inputs
     res = {}
@@ -341,7 +341,24 @@ def measure_other_paths(dev, reps=20):
                      "peak": HBM_PEAK_GBS, "unit": "GB/s",
                      "frac": nbytes / (ms / 1e3) / 1e9 / HBM_PEAK_GBS,
                      "algorithmic_bytes": nbytes}}
-    del inp, y, fs
+    del inp
+    m3 = inputs.mamba3_inputs(32, 256, 32, 64, 128, 1, "bf16", seed=1006, device="cuda")
+
+    def ssd_m3():
+        binding.ssd_mamba3_fwd(m3["x"], m3["dt"], m3["lam"], m3["A_head"], m3["B"], m3["C"], 64,
+                               out_dtype=torch.float32, y=y, final_state=fs,
+                               prev_B=m3["prev_B"], prev_x=m3["prev_x"])
+    ms = _time(ssd_m3, reps)
+    nbytes3 = nbytes + m3["lam"].numel() * 4 + m3["prev_B"].numel() * 2 + m3["prev_x"].numel() * 2
+    res["ssd_mamba3_fwd"] = {
+        "workload": "Mamba-3 SISO chunked prefill bf16 in / fp32 y, batch 32, L 256, 32 heads, "
+                    "headdim 64, d_state 128, chunk 64", "ms": ms,
+        "elements_per_s": el / (ms / 1e3),
+        "roofline": {"bound": "hbm", "achieved": nbytes3 / (ms / 1e3) / 1e9,
+                     "peak": HBM_PEAK_GBS, "unit": "GB/s",
+                     "frac": nbytes3 / (ms / 1e3) / 1e9 / HBM_PEAK_GBS,
+                     "algorithmic_bytes": nbytes3}}
+    del m3, y, fs
     g = torch.Generator(device="cuda")
     g.manual_seed(1005)
     B_, H, P, N = 256, 32, 64, 128
@@ -365,6 +382,21 @@ def measure_other_paths(dev, reps=20):
                      "peak": HBM_PEAK_GBS, "unit": "GB/s",
                      "frac": nbytes / (ms / 1e3) / 1e9 / HBM_PEAK_GBS,
                      "algorithmic_bytes": nbytes}}
+    lam = torch.sigmoid(torch.randn(B_, H, device=dev, generator=g))
+    xp = torch.randn(B_, H, P, device=dev, generator=g)
+    Bp = torch.randn(B_, 1, N, device=dev, generator=g)
+
+    def dec_m3():
+        binding.ssm_decode_step_mamba3(state, Bp, xp, x, dt, lam, A, Bm, Cm, D, y=yd)
+    ms = _time(dec_m3, reps)
+    nbytes3 = nbytes + lam.numel() * 4 + xp.numel() * 4 + Bp.numel() * 4
+    res["ssm_decode_step_mamba3"] = {
+        "workload": "Mamba-3 SISO decode step fp32, batch 256, 32 heads, headdim 64, d_state 128",
+        "ms": ms, "elements_per_s": state.numel() / (ms / 1e3),
+        "roofline": {"bound": "hbm", "achieved": nbytes3 / (ms / 1e3) / 1e9,
+                     "peak": HBM_PEAK_GBS, "unit": "GB/s",
+                     "frac": nbytes3 / (ms / 1e3) / 1e9 / HBM_PEAK_GBS,
+                     "algorithmic_bytes": nbytes3}}
     return res
 
 
