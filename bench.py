@@ -177,8 +177,10 @@ def make_inputs(rank):
 
 def cpu_baseline(inp, max_seconds=20.0):
     """Time the fp64 oracle (as it stands) on a bounded sample of the workload:
-    the first `nb` batch rows of the same inputs, nb grown until the run
-    takes at least ~2 s, capped so the total stays within max_seconds."""
+    the first `nb` batch rows of the same inputs, nb grown until one run takes
+    at least ~2 s (capped so the total stays within max_seconds); when the
+    whole workload takes less, it is run repeatedly for ~2 s and the mean
+    taken."""
     import oracle
     nb, elapsed, el = 1, 0.0, 0
     dims = None
@@ -194,9 +196,16 @@ def cpu_baseline(inp, max_seconds=20.0):
         if elapsed >= 2.0 or nb >= BATCH or elapsed * 2 * 2 > max_seconds:
             break
         nb = min(BATCH, nb * 2)
+    runs = 1
+    if elapsed < 2.0:
+        runs = max(1, min(int(2.0 / max(elapsed, 1e-3)), int(max_seconds / max(elapsed, 1e-3))))
+        t0 = time.perf_counter()
+        for _ in range(runs):
+            oracle.scan(*args)
+        elapsed = (time.perf_counter() - t0) / runs
     return {"value": el / elapsed, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"batch rows 0..{dims - 1} of the workload ({dims}x{DIM}x{SEQLEN}x{DSTATE} "
-                      f"= {el} elements), fp64, one run, {elapsed:.2f} s"}
+                      f"= {el} elements), fp64, mean of {runs} run(s), {elapsed:.2f} s each"}
 
 
 def run_ours(args):
