@@ -61,6 +61,9 @@ def _load():
             lib.oracle_mamba3_recurrence.argtypes = [dp] * 11 + [i] * 6
             lib.oracle_mamba3_chunked.argtypes = [dp] * 11 + [i] * 7
             lib.oracle_mamba3_decode_step.argtypes = [dp] * 12 + [i] * 5
+            lib.oracle_mamba3_mimo_recurrence.argtypes = [dp] * 11 + [i] * 7
+            lib.oracle_mamba3_mimo_chunked.argtypes = [dp] * 11 + [i] * 8
+            lib.oracle_mamba3_mimo_decode_step.argtypes = [dp] * 12 + [i] * 6
             lib.oracle_combine.argtypes = [ctypes.c_double] * 4 + [dp, dp]
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -226,6 +229,68 @@ def mamba3_decode_step(state, prev_B, prev_x, x, dt, lam, A, B, C, D=None, z=Non
     _load().oracle_mamba3_decode_step(_ptr(st), _ptr(prev_B), _ptr(prev_x), _ptr(x), _ptr(dt),
                                       _ptr(lam), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
                                       _ptr(y), batch, nheads, headdim, dstate, ngroups)
+    return y, st
+
+
+def _mimo_args(x, dt, lam, A_head, B, C, h0, prev_B, prev_x):
+    (x, dt, lam, A_head, B, C, h0, prev_B, prev_x) = (
+        _f64(t) for t in (x, dt, lam, A_head, B, C, h0, prev_B, prev_x))
+    batch, seqlen, rank, nheads, headdim = x.shape
+    ngroups, dstate = B.shape[3], B.shape[4]
+    assert dt.shape == (batch, seqlen, nheads) and lam.shape == dt.shape
+    assert A_head.shape == (nheads,) and C.shape == B.shape
+    assert B.shape == (batch, seqlen, rank, ngroups, dstate) and nheads % ngroups == 0
+    assert (prev_B is None) == (prev_x is None)
+    if prev_B is not None:
+        assert prev_B.shape == (batch, rank, ngroups, dstate)
+        assert prev_x.shape == (batch, rank, nheads, headdim)
+    return ((x, dt, lam, A_head, B, C, h0, prev_B, prev_x),
+            (batch, seqlen, rank, nheads, headdim, dstate, ngroups))
+
+
+def mamba3_mimo_recurrence(x, dt, lam, A_head, B, C, h0=None, prev_B=None, prev_x=None):
+    """Mamba-3 MIMO (rank R) by the step-by-step recurrence.  x: (B, L, R, H, P);
+    dt, lam: (B, L, H); A_head: (H,); B, C: (B, L, R, G, N); h0: (B, H, P, N);
+    prev_B: (B, R, G, N) and prev_x: (B, R, H, P), the token before the first.
+    Returns (y (B, L, R, H, P), state (B, H, P, N))."""
+    arrs, dims = _mimo_args(x, dt, lam, A_head, B, C, h0, prev_B, prev_x)
+    batch, seqlen, rank, nheads, headdim, dstate, _ = dims
+    y = np.empty((batch, seqlen, rank, nheads, headdim), np.float64)
+    hs = np.empty((batch, nheads, headdim, dstate), np.float64)
+    _load().oracle_mamba3_mimo_recurrence(*[_ptr(a) for a in arrs], _ptr(y), _ptr(hs), *dims)
+    return y, hs
+
+
+def mamba3_mimo_chunked(x, dt, lam, A_head, B, C, chunk, h0=None, prev_B=None, prev_x=None):
+    """Mamba-3 MIMO by the rank-flattened chunked form with the block-diagonal
+    correction (fp64 loops; `chunk` counts steps), for pinning against the recurrence."""
+    arrs, dims = _mimo_args(x, dt, lam, A_head, B, C, h0, prev_B, prev_x)
+    batch, seqlen, rank, nheads, headdim, dstate, _ = dims
+    y = np.empty((batch, seqlen, rank, nheads, headdim), np.float64)
+    hs = np.empty((batch, nheads, headdim, dstate), np.float64)
+    _load().oracle_mamba3_mimo_chunked(*[_ptr(a) for a in arrs], _ptr(y), _ptr(hs), *dims,
+                                       int(chunk))
+    return y, hs
+
+
+def mamba3_mimo_decode_step(state, prev_B, prev_x, x, dt, lam, A, B, C, D=None, z=None):
+    """One Mamba-3 MIMO decode step.  state: (B, H, P, N) (a new array is returned);
+    prev_B, B, C: (B, R, G, N); prev_x, x, z: (B, R, H, P); dt, lam: (B, H); A, D: (H,).
+    Returns (y (B, R, H, P), new_state)."""
+    st = _f64(state).copy()
+    prev_B, prev_x, x, dt, lam, A, B, C, D, z = (
+        _f64(t) for t in (prev_B, prev_x, x, dt, lam, A, B, C, D, z))
+    batch, nheads, headdim, dstate = st.shape
+    rank, ngroups = B.shape[1], B.shape[2]
+    assert x.shape == (batch, rank, nheads, headdim) and prev_x.shape == x.shape
+    assert dt.shape == (batch, nheads) and lam.shape == dt.shape
+    assert B.shape == (batch, rank, ngroups, dstate) and C.shape == B.shape
+    assert prev_B.shape == B.shape
+    y = np.empty((batch, rank, nheads, headdim), np.float64)
+    _load().oracle_mamba3_mimo_decode_step(_ptr(st), _ptr(prev_B), _ptr(prev_x), _ptr(x),
+                                           _ptr(dt), _ptr(lam), _ptr(A), _ptr(B), _ptr(C),
+                                           _ptr(D), _ptr(z), _ptr(y), batch, rank, nheads,
+                                           headdim, dstate, ngroups)
     return y, st
 
 

@@ -36,6 +36,11 @@
  *       mamba3_siso_ssd_kernel: the single-SSD form with
  *       scale = gamma + dt_{t+1} (1 - lambda_{t+1}) and a diagonal
  *       correction (oracle_mamba3_chunked).
+ *  [P2] same page, "Kernel details", mamba3_mimo_ssd_kernel and
+ *       mamba3_mimo_decode_kernel: the rank-R (MIMO) state update,
+ *       B x = sum_r B[n,r] x[p,r] and y[p,r] = sum_n state[n,p] C[n,r], and the
+ *       rank-flattened chunked form with a block-diagonal correction
+ *       (oracle_mamba3_mimo_*).
  *
  * Readings taken where the pages are silent (each is listed with its reason
  * in the design notes):
@@ -616,6 +621,231 @@ void oracle_mamba3_decode_step(double* state, const double* prev_B, const double
         double out = acc + (Dskip ? xv * Dskip[h] : 0.0);
         if (z) out *= silu_d(z[row]);
         y[row] = out;
+    }
+}
+
+/*
+ * Mamba-3 MIMO (rank R) recurrence.
+ * [P2] "How it works" (Phase 0, Eq. 9) with the rank-R terms of "Kernel
+ * details", mamba3_mimo_decode_kernel:
+ *   BX_t[n,p] = sum_r B_t[n,r] x_t[p,r]
+ *   h_t = alpha_t h_{t-1} + beta_t BX_{t-1} + gamma_t BX_t
+ *   y_t[p,r] = sum_n h_t[n,p] C_t[n,r]
+ * Layouts (rank inside the time position):
+ *   x, y : (batch, seqlen, R, nheads, headdim);  dt, lam : (batch, seqlen, nheads)
+ *   Bm, Cm : (batch, seqlen, R, ngroups, dstate);  A_head : (nheads,)
+ *   h0, final_state : (batch, nheads, headdim, dstate); either may be NULL
+ *   prev_B : (batch, R, ngroups, dstate), prev_x : (batch, R, nheads, headdim):
+ *   the token before the first (NULL: none).
+ */
+void oracle_mamba3_mimo_recurrence(const double* x, const double* dt, const double* lam,
+                                   const double* A_head, const double* Bm, const double* Cm,
+                                   const double* h0, const double* prev_B, const double* prev_x,
+                                   double* y, double* final_state, int batch, int seqlen,
+                                   int rank, int nheads, int headdim, int dstate, int ngroups)
+{
+    const int heads_per_group = nheads / ngroups;
+    const long long rows = (long long)batch * nheads * headdim;
+#pragma omp parallel for schedule(dynamic, 8)
+    for (long long row = 0; row < rows; ++row) {
+        const int p = (int)(row % headdim);
+        const int h = (int)((row / headdim) % nheads);
+        const int b = (int)(row / ((long long)headdim * nheads));
+        const int g = h / heads_per_group;
+        double* S = (double*)malloc(sizeof(double) * (size_t)dstate);
+        double* BXp = (double*)malloc(sizeof(double) * (size_t)dstate);
+        double* BX = (double*)malloc(sizeof(double) * (size_t)dstate);
+        for (int n = 0; n < dstate; ++n) {
+            S[n] = h0 ? h0[row * dstate + n] : 0.0;
+            double bx = 0.0;
+            if (prev_B && prev_x)
+                for (int r = 0; r < rank; ++r)
+                    bx += prev_B[(((size_t)b * rank + r) * ngroups + g) * dstate + n] *
+                          prev_x[(((size_t)b * rank + r) * nheads + h) * headdim + p];
+            BXp[n] = bx;
+        }
+        for (int t = 0; t < seqlen; ++t) {
+            const size_t bt = (size_t)b * seqlen + t;
+            const double dtv = dt[bt * nheads + h];
+            const double alpha = exp(dtv * A_head[h]);
+            const double gamma = lam[bt * nheads + h] * dtv;
+            const double beta_t = (dtv - gamma) * alpha;
+            for (int n = 0; n < dstate; ++n) {
+                double bx = 0.0;
+                for (int r = 0; r < rank; ++r)
+                    bx += Bm[((bt * rank + r) * ngroups + g) * dstate + n] *
+                          x[((bt * rank + r) * nheads + h) * headdim + p];
+                BX[n] = bx;
+                S[n] = alpha * S[n] + beta_t * BXp[n] + gamma * bx;
+            }
+            for (int r = 0; r < rank; ++r) {
+                double acc = 0.0;
+                for (int n = 0; n < dstate; ++n)
+                    acc += Cm[((bt * rank + r) * ngroups + g) * dstate + n] * S[n];
+                y[((bt * rank + r) * nheads + h) * headdim + p] = acc;
+            }
+            for (int n = 0; n < dstate; ++n) BXp[n] = BX[n];
+        }
+        if (final_state)
+            for (int n = 0; n < dstate; ++n) final_state[row * dstate + n] = S[n];
+        free(S);
+        free(BXp);
+        free(BX);
+    }
+}
+
+/*
+ * Mamba-3 MIMO, rank-flattened chunked form.
+ * [P2] "Kernel details", mamba3_mimo_ssd_kernel: the (step, rank) pairs of a
+ * chunk are taken as chunk * R sub-tokens, and the chunked single-SSD form of
+ * oracle_mamba3_chunked runs over them: sub-tokens share the decay and the
+ * weights of their step (scale off the diagonal, gamma on it), and the
+ * causal mask is block-lower-triangular -- a sub-token sees every sub-token of
+ * its own step (the block-diagonal part, weight gamma) and of earlier steps.
+ * `chunk` counts steps.  Arguments as oracle_mamba3_mimo_recurrence.
+ */
+void oracle_mamba3_mimo_chunked(const double* x, const double* dt, const double* lam,
+                                const double* A_head, const double* Bm, const double* Cm,
+                                const double* h0, const double* prev_B, const double* prev_x,
+                                double* y, double* final_state, int batch, int seqlen, int rank,
+                                int nheads, int headdim, int dstate, int ngroups, int chunk)
+{
+    const int heads_per_group = nheads / ngroups;
+    const long long units = (long long)batch * nheads;
+    const int qmax = chunk * rank;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long long unit = 0; unit < units; ++unit) {
+        const int h = (int)(unit % nheads);
+        const int b = (int)(unit / nheads);
+        const int g = h / heads_per_group;
+        const double Ah = A_head[h];
+        double* S = (double*)calloc((size_t)headdim * dstate, sizeof(double));
+        double* cs = (double*)malloc(sizeof(double) * (size_t)chunk);
+        double* w = (double*)malloc(sizeof(double) * (size_t)chunk);
+        double* wd = (double*)malloc(sizeof(double) * (size_t)chunk);
+        double* M = (double*)malloc(sizeof(double) * (size_t)qmax * qmax);
+        double* Sc = (double*)malloc(sizeof(double) * (size_t)headdim * dstate);
+#define DTM(t) dt[((size_t)b * seqlen + (t)) * nheads + h]
+#define LMM(t) lam[((size_t)b * seqlen + (t)) * nheads + h]
+        for (int p = 0; p < headdim; ++p)
+            for (int n = 0; n < dstate; ++n) {
+                double s0 = h0 ? h0[(((size_t)b * nheads + h) * headdim + p) * dstate + n] : 0.0;
+                if (prev_B && prev_x && seqlen > 0)
+                    for (int r = 0; r < rank; ++r)
+                        s0 += DTM(0) * (1.0 - LMM(0)) *
+                              prev_B[(((size_t)b * rank + r) * ngroups + g) * dstate + n] *
+                              prev_x[(((size_t)b * rank + r) * nheads + h) * headdim + p];
+                S[(size_t)p * dstate + n] = s0;
+            }
+        for (int t0 = 0; t0 < seqlen; t0 += chunk) {
+            const int q = seqlen - t0 < chunk ? seqlen - t0 : chunk;
+            const int qs = q * rank;  /* sub-tokens i = (step i / R, rank i % R) */
+#define XS(i, p) x[((((size_t)b * seqlen + t0) * rank + (i)) * nheads + h) * headdim + (p)]
+#define BS(i, n) Bm[((((size_t)b * seqlen + t0) * rank + (i)) * ngroups + g) * dstate + (n)]
+#define CS(i, n) Cm[((((size_t)b * seqlen + t0) * rank + (i)) * ngroups + g) * dstate + (n)]
+            double run = 0.0;
+            for (int k = 0; k < q; ++k) {
+                const int t = t0 + k;
+                run += DTM(t) * Ah;
+                cs[k] = run;
+                wd[k] = LMM(t) * DTM(t);
+                w[k] = wd[k] + (t + 1 < seqlen ? DTM(t + 1) * (1.0 - LMM(t + 1)) : 0.0);
+            }
+            for (int i = 0; i < qs; ++i)
+                for (int j = 0; j < qs; ++j) {
+                    const int si = i / rank, sj = j / rank;
+                    double m = 0.0;
+                    if (sj <= si) {
+                        double gij = 0.0;
+                        for (int n = 0; n < dstate; ++n) gij += CS(i, n) * BS(j, n);
+                        m = gij * exp(cs[si] - cs[sj]) * (sj < si ? w[sj] : wd[sj]);
+                    }
+                    M[(size_t)i * qmax + j] = m;
+                }
+            for (int i = 0; i < qs; ++i)
+                for (int p = 0; p < headdim; ++p) {
+                    double yd = 0.0;
+                    for (int j = 0; j < qs; ++j) yd += M[(size_t)i * qmax + j] * XS(j, p);
+                    double yo = 0.0;
+                    for (int n = 0; n < dstate; ++n) yo += CS(i, n) * S[(size_t)p * dstate + n];
+                    y[((((size_t)b * seqlen + t0) * rank + i) * nheads + h) * headdim + p] =
+                        yd + exp(cs[i / rank]) * yo;
+                }
+            for (int p = 0; p < headdim; ++p)
+                for (int n = 0; n < dstate; ++n) {
+                    double s = 0.0;
+                    for (int j = 0; j < qs; ++j)
+                        s += exp(cs[q - 1] - cs[j / rank]) * w[j / rank] * XS(j, p) * BS(j, n);
+                    Sc[(size_t)p * dstate + n] = s;
+                }
+            const double decay = exp(cs[q - 1]);
+            for (size_t k = 0; k < (size_t)headdim * dstate; ++k) S[k] = decay * S[k] + Sc[k];
+#undef XS
+#undef BS
+#undef CS
+        }
+#undef DTM
+#undef LMM
+        if (final_state)
+            for (int p = 0; p < headdim; ++p)
+                for (int n = 0; n < dstate; ++n)
+                    final_state[(((size_t)b * nheads + h) * headdim + p) * dstate + n] =
+                        S[(size_t)p * dstate + n];
+        free(S);
+        free(cs);
+        free(w);
+        free(wd);
+        free(M);
+        free(Sc);
+    }
+}
+
+/*
+ * One Mamba-3 MIMO decode step, updating `state` in place.
+ * [P2] "Kernel details", mamba3_mimo_decode_kernel, with Phase 5 per rank:
+ *   s = alpha s + beta sum_r prev_B[.,r] (x) prev_x[.,r] + gamma sum_r B[.,r] (x) x[.,r]
+ *   y[p,r] = (sum_n C[n,r] s[p,n] + D_h x[p,r]) * silu(z[p,r])
+ * x, z, y, prev_x : (batch, R, nheads, headdim); B, C, prev_B :
+ * (batch, R, ngroups, dstate); dt, lam : (batch, nheads); A, D : (nheads,).
+ */
+void oracle_mamba3_mimo_decode_step(double* state, const double* prev_B, const double* prev_x,
+                                    const double* x, const double* dt, const double* lam,
+                                    const double* A, const double* Bm, const double* Cm,
+                                    const double* Dskip, const double* z, double* y, int batch,
+                                    int rank, int nheads, int headdim, int dstate, int ngroups)
+{
+    const int heads_per_group = nheads / ngroups;
+    const long long rows = (long long)batch * nheads * headdim;
+#pragma omp parallel for schedule(static)
+    for (long long row = 0; row < rows; ++row) {
+        const int p = (int)(row % headdim);
+        const int h = (int)((row / headdim) % nheads);
+        const int b = (int)(row / ((long long)headdim * nheads));
+        const int g = h / heads_per_group;
+        const double dtv = dt[(size_t)b * nheads + h];
+        const double alpha = exp(A[h] * dtv);
+        const double gamma = lam[(size_t)b * nheads + h] * dtv;
+        const double beta = alpha * (dtv - gamma);
+        double* s = state + row * dstate;
+        for (int n = 0; n < dstate; ++n) {
+            double bx = 0.0, bxp = 0.0;
+            for (int r = 0; r < rank; ++r) {
+                const size_t ib = (((size_t)b * rank + r) * ngroups + g) * dstate + n;
+                const size_t ix = (((size_t)b * rank + r) * nheads + h) * headdim + p;
+                bx += Bm[ib] * x[ix];
+                bxp += prev_B[ib] * prev_x[ix];
+            }
+            s[n] = alpha * s[n] + beta * bxp + gamma * bx;
+        }
+        for (int r = 0; r < rank; ++r) {
+            const size_t ix = (((size_t)b * rank + r) * nheads + h) * headdim + p;
+            const double* Cr = Cm + (((size_t)b * rank + r) * ngroups + g) * dstate;
+            double acc = 0.0;
+            for (int n = 0; n < dstate; ++n) acc += Cr[n] * s[n];
+            double out = acc + (Dskip ? Dskip[h] * x[ix] : 0.0);
+            if (z) out *= silu_d(z[ix]);
+            y[ix] = out;
+        }
     }
 }
 

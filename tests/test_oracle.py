@@ -538,3 +538,99 @@ def test_mamba3_decode_skip_and_gate():
     np.testing.assert_array_equal(s0, s1)
     np.testing.assert_allclose(y1, (y0 + D[None, :, None] * c["x"][:, 0]) * _silu_np(z),
                                rtol=1e-13, atol=1e-14)
+
+
+# ------------------------------------------------------ Mamba-3 MIMO pins
+
+def _mimo_case(seed, batch=2, seqlen=7, rank=3, nheads=4, headdim=3, dstate=5, ngroups=2):
+    rng = _rng(seed)
+    return dict(
+        x=rng.standard_normal((batch, seqlen, rank, nheads, headdim)),
+        dt=rng.uniform(0.02, 0.5, (batch, seqlen, nheads)),
+        lam=1.0 / (1.0 + np.exp(-rng.standard_normal((batch, seqlen, nheads)))),
+        A_head=-rng.uniform(1, 8, nheads),
+        B=rng.standard_normal((batch, seqlen, rank, ngroups, dstate)),
+        C=rng.standard_normal((batch, seqlen, rank, ngroups, dstate)),
+        h0=rng.standard_normal((batch, nheads, headdim, dstate)),
+        prev_B=rng.standard_normal((batch, rank, ngroups, dstate)),
+        prev_x=rng.standard_normal((batch, rank, nheads, headdim)))
+
+
+def test_mimo_is_a_sum_of_siso_paths():
+    """The state update is linear in the inputs, so output rank r of MIMO equals
+    the sum over input ranks r' of the SISO recurrence driven by (B[.,r'], x[.,r'])
+    and read out by C[.,r] (the initial state carried by one of them)."""
+    c = _mimo_case(131)
+    y, hs = oracle.mamba3_mimo_recurrence(**c)
+    rank = c["x"].shape[2]
+    for r in range(rank):
+        y_sum = 0.0
+        hs_sum = 0.0
+        for rp in range(rank):
+            ys, hss = oracle.mamba3_recurrence(
+                c["x"][:, :, rp], c["dt"], c["lam"], c["A_head"], c["B"][:, :, rp],
+                c["C"][:, :, r], c["h0"] if rp == 0 else None,
+                c["prev_B"][:, rp], c["prev_x"][:, rp])
+            y_sum = y_sum + ys
+            hs_sum = hs_sum + hss
+        np.testing.assert_allclose(y[:, :, r], y_sum, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(hs, hs_sum, rtol=1e-11, atol=1e-12)
+
+
+def test_mimo_rank_one_is_siso():
+    c = _mimo_case(137, rank=1)
+    y, hs = oracle.mamba3_mimo_recurrence(**c)
+    ys, hss = oracle.mamba3_recurrence(c["x"][:, :, 0], c["dt"], c["lam"], c["A_head"],
+                                       c["B"][:, :, 0], c["C"][:, :, 0], c["h0"],
+                                       c["prev_B"][:, 0], c["prev_x"][:, 0])
+    np.testing.assert_allclose(y[:, :, 0], ys, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(hs, hss, rtol=1e-13, atol=1e-14)
+
+
+def test_mimo_bruteforce():
+    """Explicit rank sums and products, O(L^2), written independently."""
+    c = _mimo_case(139, batch=1, nheads=2, ngroups=1)
+    y, hs = oracle.mamba3_mimo_recurrence(**c)
+    x, dt, lam, A = c["x"], c["dt"], c["lam"], c["A_head"]
+    B, C = c["B"], c["C"]
+    _, L, R, H, P = x.shape
+    for h in range(H):
+        alpha = np.exp(dt[0, :, h] * A[h])
+        gamma = lam[0, :, h] * dt[0, :, h]
+        beta = (dt[0, :, h] - gamma) * alpha
+        U = [sum(np.outer(B[0, t, r, 0], x[0, t, r, h]) for r in range(R)) for t in range(L)]
+        U_prev = sum(np.outer(c["prev_B"][0, r, 0], c["prev_x"][0, r, h]) for r in range(R))
+        for t in range(L):
+            ht = np.prod(alpha[:t + 1]) * c["h0"][0, h].T
+            for s in range(t + 1):
+                ht = ht + np.prod(alpha[s + 1:t + 1]) * (
+                    gamma[s] * U[s] + beta[s] * (U[s - 1] if s > 0 else U_prev))
+            for r in range(R):
+                np.testing.assert_allclose(y[0, t, r, h], C[0, t, r, 0] @ ht,
+                                           rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(hs[0, h], ht.T, rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("chunk", [1, 2, 3, 7, 16])
+def test_mimo_flattened_chunked_equals_recurrence(chunk):
+    c = _mimo_case(149)
+    y, hs = oracle.mamba3_mimo_recurrence(**c)
+    yc, hc = oracle.mamba3_mimo_chunked(chunk=chunk, **c)
+    np.testing.assert_allclose(yc, y, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(hc, hs, rtol=1e-11, atol=1e-12)
+
+
+def test_mimo_decode_chain_equals_recurrence():
+    c = _mimo_case(151, seqlen=5)
+    rng = _rng(152)
+    D = rng.standard_normal(c["A_head"].shape)
+    y_ref, hs_ref = oracle.mamba3_mimo_recurrence(**c)
+    state, pB, px = c["h0"].copy(), c["prev_B"], c["prev_x"]
+    for t in range(c["x"].shape[1]):
+        y, state = oracle.mamba3_mimo_decode_step(state, pB, px, c["x"][:, t], c["dt"][:, t],
+                                                  c["lam"][:, t], c["A_head"], c["B"][:, t],
+                                                  c["C"][:, t], D)
+        ref = y_ref[:, t] + D[None, None, :, None] * c["x"][:, t]
+        np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-13)
+        pB, px = c["B"][:, t], c["x"][:, t]
+    np.testing.assert_allclose(state, hs_ref, rtol=1e-12, atol=1e-13)

@@ -58,6 +58,14 @@ MUTANTS = {
                                               "DTA(t + 1) * (1.0 - LMA(t))"),
     "mamba3_chunked_drops_previous_token": ("s0 += DTA(0) * (1.0 - LMA(0)) *",
                                             "s0 += 0.0 * DTA(0) * (1.0 - LMA(0)) *"),
+    "mimo_input_drops_ranks": (
+        "                for (int r = 0; r < rank; ++r)\n                    bx += Bm[((bt * rank + r)",
+        "                for (int r = 0; r < 1; ++r)\n                    bx += Bm[((bt * rank + r)"),
+    "mimo_chunked_mask_by_subtoken": ("if (sj <= si) {", "if (j <= i) {"),
+    "mimo_chunked_block_diagonal_not_corrected": ("(sj < si ? w[sj] : wd[sj])", "w[sj]"),
+    "mimo_decode_reads_out_rank0": (
+        "const double* Cr = Cm + (((size_t)b * rank + r) * ngroups + g) * dstate;",
+        "const double* Cr = Cm + (((size_t)b * rank + 0) * ngroups + g) * dstate;"),
     "mamba3_decode_terms_swapped": (
         "s[n] = alpha * s[n] + beta * Bp[n] * xp + gamma * Bt[n] * xv;",
         "s[n] = alpha * s[n] + beta * Bt[n] * xv + gamma * Bp[n] * xp;"),
