@@ -8,6 +8,7 @@
  *   ssm_decode_step  single-token state update, in place
  *   ssd_mamba3_fwd, ssm_decode_step_mamba3  the same two for Mamba-3 SISO
  *                    (trapezoidal three-term recurrence)
+ *   ssd_mamba3_mimo_fwd, ssm_decode_step_mamba3_mimo  Mamba-3 MIMO (rank R)
  *
  * Conventions shared by every entry point
  *  - Pointers are DEVICE pointers unless stated otherwise, to dense row-major
@@ -175,6 +176,34 @@ ssm_status_t ssd_mamba3_fwd(const void* x, const float* dt, const float* lam,
                             void* stream);
 
 /*
+ * Mamba-3 MIMO (rank R) chunked prefill.
+ *   "Mamba-3 NKI Kernels for AWS Neuron", section "Kernel details",
+ *   mamba3_mimo_ssd_kernel (rank flattening: the (step, rank) pairs of a chunk
+ *   are taken as chunk * R sub-tokens, with a block-diagonal correction;
+ *   chunk 16 for R = 4) and mamba3_mimo_decode_kernel (the rank-R terms).
+ *
+ * Computes, exactly up to rounding, per (b, h) with BX_t[n,p] = sum_r
+ * B[b,t,r,g,n] x[b,t,r,h,p]:
+ *   S = alpha_t S + beta_t BX_{t-1} + gamma_t BX_t
+ *   y[b,t,r,h,p] = sum_n C[b,t,r,g,n] S[p,n]
+ * with the coefficients, initial state and previous token of ssd_mamba3_fwd.
+ *
+ * Layouts: x, y (batch, seqlen, rank, nheads, headdim); B, C (batch, seqlen,
+ * rank, ngroups, dstate); dt, lam (batch, seqlen, nheads) fp32; prev_B (batch,
+ * rank, ngroups, dstate) and prev_x (batch, rank, nheads, headdim) in
+ * in_dtype; states as ssd_chunked_fwd.  seqlen counts steps.
+ * Supported: rank 1, 2 or 4 with chunk * rank == 64; otherwise as
+ * ssd_mamba3_fwd (rank 1 is ssd_mamba3_fwd).
+ */
+ssm_status_t ssd_mamba3_mimo_fwd(const void* x, const float* dt, const float* lam,
+                                 const float* A_head, const void* B, const void* C, int chunk,
+                                 int rank, const float* initial_state, const void* prev_B,
+                                 const void* prev_x, void* y, float* final_state,
+                                 int batch, int seqlen, int nheads, int headdim, int dstate,
+                                 int ngroups, ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                                 void* stream);
+
+/*
  * One decode step, in place.
  *   "Mamba-3 NKI Kernels for AWS Neuron", section "How it works", decode via
  *   step(), Eq. 9 with lambda = 1 (beta = 0, gamma = dt), and Phase 5 (D skip,
@@ -216,6 +245,26 @@ ssm_status_t ssm_decode_step_mamba3(float* state, const void* prev_B, const void
                                     const float* A, const void* B, const void* C, const float* D,
                                     const void* z, void* y, int batch, int nheads, int headdim,
                                     int dstate, int ngroups, ssm_dtype_t dtype, void* stream);
+
+/*
+ * One Mamba-3 MIMO (rank R) decode step, in place.
+ *   "Mamba-3 NKI Kernels for AWS Neuron", section "Kernel details",
+ *   mamba3_mimo_decode_kernel (BX = sum_r B[n,r] x[p,r]; y[p,r] = sum_n
+ *   state[n,p] C[n,r]), with the Eq. 9 coefficients and Phase 5 per rank.
+ *
+ *   state = alpha state + beta sum_r prev_B[r] (x) prev_x[r] + gamma sum_r B[r] (x) x[r]
+ *   y[b,r,h,p] = (sum_n C[b,r,g,n] state[b,h,p,n] + D[h] x[b,r,h,p]) * silu(z[b,r,h,p])
+ *
+ * Layouts: x, z, y, prev_x (batch, rank, nheads, headdim); B, C, prev_B
+ * (batch, rank, ngroups, dstate); others as ssm_decode_step_mamba3.
+ * Supported: rank 1 (as ssm_decode_step_mamba3), 2 or 4 with dstate == 128.
+ */
+ssm_status_t ssm_decode_step_mamba3_mimo(float* state, const void* prev_B, const void* prev_x,
+                                         const void* x, const float* dt, const float* lam,
+                                         const float* A, const void* B, const void* C,
+                                         const float* D, const void* z, void* y, int batch,
+                                         int rank, int nheads, int headdim, int dstate,
+                                         int ngroups, ssm_dtype_t dtype, void* stream);
 
 /*
  * Selective scan for callers that cannot allocate device memory.

@@ -27,8 +27,9 @@ STATUS_NAMES = {0: "SSM_OK", 1: "SSM_ERR_NULL", 2: "SSM_ERR_SHAPE", 3: "SSM_ERR_
 
 # every symbol include/ssm.h declares
 EXPORTS = ["ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_bytes", "ssm_scan_fwd",
-           "ssd_chunked_fwd", "ssd_mamba3_fwd", "ssm_decode_step", "ssm_decode_step_mamba3",
-           "ssm_last_device_status", "ssm_scan_fwd_noalloc"]
+           "ssd_chunked_fwd", "ssd_mamba3_fwd", "ssd_mamba3_mimo_fwd", "ssm_decode_step",
+           "ssm_decode_step_mamba3", "ssm_decode_step_mamba3_mimo", "ssm_last_device_status",
+           "ssm_scan_fwd_noalloc"]
 
 
 class SSMError(RuntimeError):
@@ -65,6 +66,10 @@ def lib() -> ctypes.CDLL:
         L.ssd_mamba3_fwd.argtypes = [vp] * 6 + [i] + [vp] * 5 + [i] * 8 + [vp]
         L.ssm_decode_step_mamba3.restype = i
         L.ssm_decode_step_mamba3.argtypes = [vp] * 12 + [i] * 6 + [vp]
+        L.ssd_mamba3_mimo_fwd.restype = i
+        L.ssd_mamba3_mimo_fwd.argtypes = [vp] * 6 + [i] * 2 + [vp] * 5 + [i] * 8 + [vp]
+        L.ssm_decode_step_mamba3_mimo.restype = i
+        L.ssm_decode_step_mamba3_mimo.argtypes = [vp] * 12 + [i] * 7 + [vp]
         L.ssm_scan_fwd_noalloc.restype = i
         L.ssm_scan_fwd_noalloc.argtypes = [vp] * 8 + [i] + [vp] * 3 + [i] * 7 + [vp]
         L.ssm_last_device_status.restype = i
@@ -323,4 +328,76 @@ def ssm_decode_step_mamba3(state, prev_B, prev_x, x, dt, lam, A, B, C, D=None, z
                                       _ptr(z), _ptr(y), batch, nheads, headdim, dstate, ngroups,
                                       _DT[dt_], _stream(stream))
     _check(st, "ssm_decode_step_mamba3")
+    return y
+
+
+def ssd_mamba3_mimo_fwd(x, dt, lam, A_head, B, C, chunk=16, out_dtype=None, y=None,
+                        final_state=None, return_final_state=True, initial_state=None,
+                        prev_B=None, prev_x=None, stream=None):
+    """Mamba-3 MIMO (rank R) chunked prefill.  x: (batch, seqlen, R, nheads, headdim);
+    B, C: (batch, seqlen, R, ngroups, dstate); dt, lam: (batch, seqlen, nheads) fp32;
+    prev_B: (batch, R, ngroups, dstate), prev_x: (batch, R, nheads, headdim) (both or
+    neither).  Returns (y (batch, seqlen, R, nheads, headdim), final_state)."""
+    _req(x, "x", ndim=5)
+    in_dt = x.dtype
+    if in_dt not in _DT:
+        raise TypeError("x must be float32 or bfloat16")
+    batch, seqlen, rank, nheads, headdim = x.shape
+    _req(dt, "dt", torch.float32, 3)
+    _req(lam, "lam", torch.float32, 3)
+    _req(A_head, "A_head", torch.float32, 1)
+    _req(B, "B", in_dt, 5)
+    _req(C, "C", in_dt, 5)
+    ngroups, dstate = B.shape[3], B.shape[4]
+    out_dt = in_dt if out_dtype is None else out_dtype
+    if y is None:
+        y = torch.empty_like(x, dtype=out_dt)
+    _req(y, "y", out_dt)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((batch, nheads, headdim, dstate), dtype=torch.float32,
+                                  device=x.device)
+    _opt(final_state, "final_state", torch.float32)
+    _opt(initial_state, "initial_state", torch.float32)
+    _opt(prev_B, "prev_B", in_dt)
+    _opt(prev_x, "prev_x", in_dt)
+    st = lib().ssd_mamba3_mimo_fwd(_ptr(x), _ptr(dt), _ptr(lam), _ptr(A_head), _ptr(B), _ptr(C),
+                                   int(chunk), int(rank), _ptr(initial_state), _ptr(prev_B),
+                                   _ptr(prev_x), _ptr(y), _ptr(final_state), batch, seqlen,
+                                   nheads, headdim, dstate, ngroups, _DT[in_dt], _DT[out_dt],
+                                   _stream(stream))
+    _check(st, "ssd_mamba3_mimo_fwd")
+    return y, final_state
+
+
+def ssm_decode_step_mamba3_mimo(state, prev_B, prev_x, x, dt, lam, A, B, C, D=None, z=None,
+                                y=None, stream=None):
+    """One Mamba-3 MIMO (rank R) decode step; ``state`` (batch, nheads, headdim, dstate)
+    fp32 is updated in place.  x, z, prev_x: (batch, R, nheads, headdim); B, C, prev_B:
+    (batch, R, ngroups, dstate); dt, lam: (batch, nheads) fp32; A, D: (nheads,) fp32.
+    Returns y (batch, R, nheads, headdim)."""
+    _req(state, "state", torch.float32, 4)
+    batch, nheads, headdim, dstate = state.shape
+    _req(x, "x", ndim=4)
+    dt_ = x.dtype
+    if dt_ not in _DT:
+        raise TypeError("x must be float32 or bfloat16")
+    rank = x.shape[1]
+    _req(dt, "dt", torch.float32, 2)
+    _req(lam, "lam", torch.float32, 2)
+    _req(A, "A", torch.float32, 1)
+    _req(B, "B", dt_, 4)
+    _req(C, "C", dt_, 4)
+    _req(prev_B, "prev_B", dt_, 4)
+    _req(prev_x, "prev_x", dt_, 4)
+    ngroups = B.shape[2]
+    _opt(D, "D", torch.float32)
+    _opt(z, "z", dt_)
+    if y is None:
+        y = torch.empty_like(x)
+    _req(y, "y", dt_)
+    st = lib().ssm_decode_step_mamba3_mimo(_ptr(state), _ptr(prev_B), _ptr(prev_x), _ptr(x),
+                                           _ptr(dt), _ptr(lam), _ptr(A), _ptr(B), _ptr(C),
+                                           _ptr(D), _ptr(z), _ptr(y), batch, rank, nheads,
+                                           headdim, dstate, ngroups, _DT[dt_], _stream(stream))
+    _check(st, "ssm_decode_step_mamba3_mimo")
     return y

@@ -224,6 +224,41 @@ __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Producer loop of the bulk decode kernels (one thread): load the CTA's
+// first two tiles, then for each tile i wait until the compute warps have
+// updated it (empty), store it, and reuse the stage for tile i + 2 once the
+// store has read it.  `tile(i, bh, p0, nr)` gives tile i's (b, h) pair, first
+// row and row count.
+template <typename TileFn>
+__device__ __forceinline__ void bulk_producer(float* state, uint8_t* dsm, uint64_t* full,
+                                              uint64_t* empty, long long my, int headdim,
+                                              TileFn tile) {
+    for (long long i = 0; i < 2 && i < my; ++i) {
+        long long bh; int p0, nr;
+        tile(i, bh, p0, nr);
+        mbar_arrive_expect_tx(&full[i], (uint32_t)nr * kBulkN * 4);
+        bulk_load(dsm + i * kTileBytes, state + (bh * headdim + p0) * kBulkN,
+                  (uint32_t)nr * kBulkN * 4, &full[i]);
+    }
+    for (long long i = 0; i < my; ++i) {
+        const int s = (int)(i & 1);
+        if (!mbar_wait(&empty[s], (uint32_t)((i >> 1) & 1), nullptr)) break;
+        long long bh; int p0, nr;
+        tile(i, bh, p0, nr);
+        bulk_store(state + (bh * headdim + p0) * kBulkN, dsm + s * kTileBytes,
+                   (uint32_t)nr * kBulkN * 4);
+        bulk_commit_group();
+        if (i + 2 < my) {
+            bulk_wait_read_all();  // the stage has been read out
+            tile(i + 2, bh, p0, nr);
+            mbar_arrive_expect_tx(&full[s], (uint32_t)nr * kBulkN * 4);
+            bulk_load(dsm + s * kTileBytes, state + (bh * headdim + p0) * kBulkN,
+                      (uint32_t)nr * kBulkN * 4, &full[s]);
+        }
+    }
+    bulk_wait_all();
+}
+
 // Tiles are (b, h, chunk of up to 64 rows); CTA k takes tiles k, k + grid, ...
 // Stage s of the two shared-memory stages holds the CTA's tiles s, s + 2, ...:
 // full[s] completes when a tile has landed, empty[s] when the compute warps
@@ -262,32 +297,7 @@ __global__ void __launch_bounds__(kBulkThreads)
     };
 
     if (warp == kBulkCompute / 32) {  // ------------------------------ producer
-        if (lane == 0) {
-            for (long long i = 0; i < 2 && i < my; ++i) {
-                long long bh; int p0, nr;
-                tile(i, bh, p0, nr);
-                mbar_arrive_expect_tx(&full[i], (uint32_t)nr * kBulkN * 4);
-                bulk_load(dsm + i * kTileBytes, state + (bh * headdim + p0) * kBulkN,
-                          (uint32_t)nr * kBulkN * 4, &full[i]);
-            }
-            for (long long i = 0; i < my; ++i) {
-                const int s = (int)(i & 1);
-                if (!mbar_wait(&empty[s], (uint32_t)((i >> 1) & 1), nullptr)) break;
-                long long bh; int p0, nr;
-                tile(i, bh, p0, nr);
-                bulk_store(state + (bh * headdim + p0) * kBulkN, dsm + s * kTileBytes,
-                           (uint32_t)nr * kBulkN * 4);
-                bulk_commit_group();
-                if (i + 2 < my) {
-                    bulk_wait_read_all();  // the stage has been read out
-                    tile(i + 2, bh, p0, nr);
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)nr * kBulkN * 4);
-                    bulk_load(dsm + s * kTileBytes, state + (bh * headdim + p0) * kBulkN,
-                              (uint32_t)nr * kBulkN * 4, &full[s]);
-                }
-            }
-            bulk_wait_all();
-        }
+        if (lane == 0) bulk_producer(state, dsm, full, empty, my, headdim, tile);
         return;
     }
 
@@ -374,6 +384,133 @@ __global__ void __launch_bounds__(kBulkThreads)
     }
 }
 
+// Mamba-3 MIMO decode, rank RK ("Mamba-3 NKI Kernels for AWS Neuron",
+// "Kernel details", mamba3_mimo_decode_kernel): the same tile stream as
+// decode_bulk_kernel, with the rank-R input terms
+//   state = alpha state + beta sum_r prev_B[r] (x) prev_x[r] + gamma sum_r B[r] (x) x[r]
+// and RK read-outs per row, y[r][p] = sum_n C[r][n] state[p][n] (+ D x[r][p],
+// gate), each reduce-scattered over the warp like the single one.
+// x, z, y, prev_x: (batch, RK, nheads, headdim); B, C, prev_B: (batch, RK,
+// ngroups, 128).
+template <typename T, int RK>
+__global__ void __launch_bounds__(kBulkThreads)
+    decode_bulk_mimo_kernel(float* __restrict__ state, const T* __restrict__ x,
+                            const float* __restrict__ dt, const float* __restrict__ A,
+                            const T* __restrict__ Bm, const T* __restrict__ Cm,
+                            const float* __restrict__ Dskip, const T* __restrict__ z,
+                            T* __restrict__ y, int batch, int nheads, int headdim, int ngroups,
+                            M3In<T> m3) {
+    extern __shared__ __align__(128) uint8_t dsm[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(dsm + 2 * kTileBytes);
+    uint64_t* empty = full + 2;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nchunks = (headdim + kBulkRows - 1) / kBulkRows;
+    const long long ntiles = (long long)batch * nheads * nchunks;
+    const long long my = ntiles > blockIdx.x ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+    if (tid == 0) {
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kBulkCompute / 32);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto tile = [&](long long i, long long& bh, int& p0, int& nr) {
+        const long long t = blockIdx.x + i * gridDim.x;
+        bh = t / nchunks;
+        p0 = (int)(t % nchunks) * kBulkRows;
+        nr = min(kBulkRows, headdim - p0);
+    };
+
+    if (warp == kBulkCompute / 32) {
+        if (lane == 0) bulk_producer(state, dsm, full, empty, my, headdim, tile);
+        return;
+    }
+
+    const long long rstride_x = (long long)nheads * headdim;  // between ranks of x
+    const long long rstride_b = (long long)ngroups * kBulkN;  // between ranks of B
+    for (long long i = 0; i < my; ++i) {
+        const int s = (int)(i & 1);
+        long long bh; int p0, nr;
+        tile(i, bh, p0, nr);
+        const int h = (int)(bh % nheads);
+        const long long b = bh / nheads;
+        const int g = h / (nheads / ngroups);
+        const long long bc = ((b * RK) * ngroups + g) * kBulkN + 4 * lane;
+        float bv[RK][4], bp[RK][4];
+#pragma unroll
+        for (int r = 0; r < RK; ++r) {
+            load4<T>(Bm + bc + r * rstride_b, bv[r]);
+            load4<T>(m3.prev_B + bc + r * rstride_b, bp[r]);
+        }
+        const float dtv = dt[bh];
+        const float alpha = expf(dtv * A[h]);
+        const float gam = m3.lam[bh] * dtv;
+        const float bet = (dtv - gam) * alpha;
+        const long long xrow0 = (b * RK * nheads + h) * (long long)headdim + p0;  // rank 0
+        if (!mbar_wait(&full[s], (uint32_t)((i >> 1) & 1), nullptr)) break;
+        float* st = reinterpret_cast<float*>(dsm + s * kTileBytes);
+
+        // state update of rows warp, warp + 4, ... (in place)
+#pragma unroll 4
+        for (int r16 = 0; r16 < 16; ++r16) {
+            const int p = warp + 4 * r16;
+            if (p >= nr) continue;
+            float in[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int r = 0; r < RK; ++r) {
+                const float xg = gam * to_f32(x[xrow0 + r * rstride_x + p]);
+                const float xb = bet * to_f32(m3.prev_x[xrow0 + r * rstride_x + p]);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) in[k] = fmaf(xg, bv[r][k], fmaf(xb, bp[r][k], in[k]));
+            }
+            float4* q = reinterpret_cast<float4*>(st + p * kBulkN) + lane;
+            const float4 v = *q;
+            *q = make_float4(fmaf(alpha, v.x, in[0]), fmaf(alpha, v.y, in[1]),
+                             fmaf(alpha, v.z, in[2]), fmaf(alpha, v.w, in[3]));
+        }
+        // one read-out per rank
+#pragma unroll 1
+        for (int r = 0; r < RK; ++r) {
+            float cv[4];
+            load4<T>(Cm + bc + r * rstride_b, cv);
+            float acc[16];
+#pragma unroll
+            for (int r16 = 0; r16 < 16; ++r16) {
+                const int p = warp + 4 * r16;
+                acc[r16] = 0.0f;
+                if (p < nr) {
+                    const float4 v = reinterpret_cast<const float4*>(st + p * kBulkN)[lane];
+                    acc[r16] = fmaf(cv[3], v.w, fmaf(cv[2], v.z, fmaf(cv[1], v.y, cv[0] * v.x)));
+                }
+            }
+#pragma unroll
+            for (int m = 16, n = 8; m >= 2; m >>= 1, n >>= 1) {
+                const bool hi = lane & m;
+#pragma unroll
+                for (int k = 0; k < n; ++k) {
+                    const float send = hi ? acc[k] : acc[k + n];
+                    const float keep = hi ? acc[k + n] : acc[k];
+                    acc[k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                }
+            }
+            acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 1);
+            const int p = warp + 4 * (lane >> 1);
+            if ((lane & 1) == 0 && p < nr) {
+                const long long row = xrow0 + r * rstride_x + p;
+                float out = acc[0] + (Dskip ? Dskip[h] : 0.0f) * to_f32(x[row]);
+                if (z) out *= silu_f(to_f32(z[row]));
+                y[row] = from_f32<T>(out);
+            }
+        }
+        fence_proxy_async_smem();  // the updated tile is read by the bulk store
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+}
+
 template <typename T, bool M3>
 ssm_status_t launch_bulk(float* state, const void* x, const float* dt, const float* A,
                          const void* B, const void* C, const float* D, const void* z, void* y,
@@ -400,6 +537,38 @@ ssm_status_t launch_bulk(float* state, const void* x, const float* dt, const flo
         (long long)batch * nheads * ((headdim + kBulkRows - 1) / kBulkRows);
     const unsigned grid = (unsigned)std::min<long long>(tiles, 3LL * sms);
     decode_bulk_kernel<T, M3><<<grid, kBulkThreads, kBulkSmem, s>>>(
+        state, static_cast<const T*>(x), dt, A, static_cast<const T*>(B),
+        static_cast<const T*>(C), D, static_cast<const T*>(z), static_cast<T*>(y), batch, nheads,
+        headdim, ngroups, m3);
+    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+template <typename T, int RK>
+ssm_status_t launch_bulk_mimo(float* state, const void* x, const float* dt, const float* A,
+                              const void* B, const void* C, const float* D, const void* z,
+                              void* y, int batch, int nheads, int headdim, int ngroups,
+                              M3In<T> m3, cudaStream_t s) {
+    static std::mutex m;
+    static int cached_dev = -1, sms = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lk(m);
+        if (dev != cached_dev) {
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                sms <= 0)
+                return SSM_ERR_CUDA;
+            if (cudaFuncSetAttribute(decode_bulk_mimo_kernel<T, RK>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kBulkSmem) != cudaSuccess)
+                return SSM_ERR_CUDA;
+            cached_dev = dev;
+        }
+    }
+    const long long tiles =
+        (long long)batch * nheads * ((headdim + kBulkRows - 1) / kBulkRows);
+    const unsigned grid = (unsigned)std::min<long long>(tiles, 3LL * sms);
+    decode_bulk_mimo_kernel<T, RK><<<grid, kBulkThreads, kBulkSmem, s>>>(
         state, static_cast<const T*>(x), dt, A, static_cast<const T*>(B),
         static_cast<const T*>(C), D, static_cast<const T*>(z), static_cast<T*>(y), batch, nheads,
         headdim, ngroups, m3);
@@ -502,4 +671,56 @@ extern "C" ssm_status_t ssm_decode_step_mamba3(float* state, const void* prev_B,
                                                ssm_dtype_t dtype, void* stream) {
     return decode_entry(state, x, dt, lam, A, B, C, D, z, prev_B, prev_x, y, batch, nheads,
                         headdim, dstate, ngroups, dtype, true, stream);
+}
+
+extern "C" ssm_status_t ssm_decode_step_mamba3_mimo(float* state, const void* prev_B,
+                                                    const void* prev_x, const void* x,
+                                                    const float* dt, const float* lam,
+                                                    const float* A, const void* B, const void* C,
+                                                    const float* D, const void* z, void* y,
+                                                    int batch, int rank, int nheads, int headdim,
+                                                    int dstate, int ngroups, ssm_dtype_t dtype,
+                                                    void* stream) {
+    using namespace ssm_host;
+    if (rank < 1 || batch < 0 || nheads < 0 || headdim < 0 || dstate < 1 || ngroups < 1)
+        return SSM_ERR_SHAPE;
+    if (rank == 1)  // the (batch, 1, ...) layouts are the single-input ones
+        return ssm_decode_step_mamba3(state, prev_B, prev_x, x, dt, lam, A, B, C, D, z, y, batch,
+                                      nheads, headdim, dstate, ngroups, dtype, stream);
+    if (nheads % ngroups != 0) return SSM_ERR_SHAPE;
+    if (!dtype_ok(dtype)) return SSM_ERR_DTYPE;
+    if ((rank != 2 && rank != 4) || dstate != kBulkN) return SSM_ERR_UNSUPPORTED;
+    const long long rows = (long long)batch * nheads * headdim;
+    if (rows == 0) return SSM_OK;
+    if (!state || !x || !dt || !A || !B || !C || !y || !lam || !prev_B || !prev_x)
+        return SSM_ERR_NULL;
+    const void* ptrs[] = {state, x, dt, A, B, C, D, z, y, lam, prev_B, prev_x};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return SSM_ERR_ALIGN;
+    const size_t es = dtype_size(dtype);
+    const size_t sbytes = (size_t)rows * dstate * 4, rbytes = (size_t)rows * rank * es;
+    const size_t bcbytes = (size_t)batch * rank * ngroups * dstate * es;
+    struct R { const void* p; size_t n; } ins[] = {
+        {x, rbytes}, {dt, (size_t)batch * nheads * 4}, {A, (size_t)nheads * 4},
+        {B, bcbytes}, {C, bcbytes}, {D, D ? (size_t)nheads * 4 : 0}, {z, z ? rbytes : 0},
+        {lam, (size_t)batch * nheads * 4}, {prev_B, bcbytes}, {prev_x, rbytes}};
+    for (const R& r : ins) {
+        if (overlaps(state, sbytes, r.p, r.n)) return SSM_ERR_ALIAS;
+        if (overlaps(y, rbytes, r.p, r.n)) return SSM_ERR_ALIAS;
+    }
+    if (overlaps(y, rbytes, state, sbytes)) return SSM_ERR_ALIAS;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == SSM_BF16) {
+        using T = __nv_bfloat16;
+        const M3In<T> m{lam, static_cast<const T*>(prev_B), static_cast<const T*>(prev_x)};
+        return rank == 2 ? launch_bulk_mimo<T, 2>(state, x, dt, A, B, C, D, z, y, batch, nheads,
+                                                  headdim, ngroups, m, s)
+                         : launch_bulk_mimo<T, 4>(state, x, dt, A, B, C, D, z, y, batch, nheads,
+                                                  headdim, ngroups, m, s);
+    }
+    const M3In<float> m{lam, static_cast<const float*>(prev_B), static_cast<const float*>(prev_x)};
+    return rank == 2 ? launch_bulk_mimo<float, 2>(state, x, dt, A, B, C, D, z, y, batch, nheads,
+                                                  headdim, ngroups, m, s)
+                     : launch_bulk_mimo<float, 4>(state, x, dt, A, B, C, D, z, y, batch, nheads,
+                                                  headdim, ngroups, m, s);
 }

@@ -86,11 +86,13 @@ __device__ __forceinline__ void split2_bf16(float a, float b, uint32_t& hp, uint
 }
 
 // One 32-column chunk of M' for row i: m_j = G[i][j] 2^(cs2_i + q2_j), with
-// j > i zeroed when MASK (the diagonal chunk; jmax = i - first column).  With
-// DIAG (Mamba-3) the diagonal entry is G[i][i] diag_w instead.
+// columns past jmax zeroed when MASK (the chunk holding row i's own step; jmax
+// = its last column relative to the chunk).  With DIAG (Mamba-3) the entries
+// of row i's own step, columns jd0 .. jmax, are G[i][j] diag_w instead (one
+// entry for SISO, the step's R sub-tokens for MIMO).
 template <bool MASK, bool DIAG>
 __device__ __forceinline__ void mprime_chunk(const float* gv, const float* q2c, float cs2_i, int jmax,
-                                             float diag_w, uint32_t* hp, uint32_t* lp) {
+                                             int jd0, float diag_w, uint32_t* hp, uint32_t* lp) {
 #pragma unroll
     for (int q = 0; q < 32; q += 4) {
         const float4 qq = *reinterpret_cast<const float4*>(q2c + q);
@@ -99,7 +101,7 @@ __device__ __forceinline__ void mprime_chunk(const float* gv, const float* q2c, 
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             m[k] = gv[q + k] * ex2_approx(cs2_i + qv[k]);
-            if (MASK && DIAG && q + k == jmax) m[k] = gv[q + k] * diag_w;
+            if (MASK && DIAG && q + k >= jd0) m[k] = gv[q + k] * diag_w;
             if (MASK && q + k > jmax) m[k] = 0.0f;
         }
         split2_bf16(m[0], m[1], hp[q >> 1], lp[q >> 1]);
@@ -132,7 +134,12 @@ __device__ __forceinline__ uint32_t mcol_hi(int kk) {
 // scale_j = gamma_j + dt_{j+1} (1 - lambda_{j+1}) (gamma = lambda dt; 0 past
 // the last step), the diagonal of M' takes gamma_i, and the previous token's
 // B (x) x enters the state as dt_0 (1 - lambda_0) prev_B (x) prev_x.
-template <typename Tout, bool M3>
+// RK > 1 (Mamba-3 MIMO, "Kernel details", mamba3_mimo_ssd_kernel): the rank
+// is flattened into the sequence -- x, y, B, C hold RK sub-tokens per step,
+// row u of a block is sub-token u % RK of step u / RK -- and sub-tokens share
+// their step's decay and weights; a sub-token sees every sub-token of its own
+// step (the block-diagonal part, weight gamma) and of earlier steps.
+template <typename Tout, bool M3, int RK>
 __global__ void __launch_bounds__(kThreads, 2)
     ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_B,
                    const __grid_constant__ CUtensorMap tm_x, const SsdArgs a) {
@@ -154,7 +161,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int row = quarter * 32 + lane;  // TMEM lane: row i of G / Y, state n of S
     // Work items are (batch, head) pairs blockIdx.x, blockIdx.x + gridDim.x, ...;
     // each is nblocks steps of kQ time steps, run in order.
-    const int nblocks = (a.seqlen + kQ - 1) / kQ;
+    const int nsub = a.seqlen * RK;  // sub-tokens (rows) per sequence
+    const int nblocks = (nsub + kQ - 1) / kQ;
     const int nitems = a.batch * a.nheads;
     const int my_items = ((int)blockIdx.x < nitems) ? (nitems - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int nsteps = my_items * nblocks;
@@ -167,9 +175,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int it = 0; it < my_items; ++it) {
             const int item = (int)blockIdx.x + it * (int)gridDim.x;
             const int hh = item % a.nheads, bb = item / a.nheads;
-            for (int t = tid; t < a.seqlen; t += kThreads) {
+            for (int t = tid; t < nsub; t += kThreads) {
                 Tout* yr = reinterpret_cast<Tout*>(a.y) +
-                           (((long long)bb * a.seqlen + t) * a.nheads + hh) * kP;
+                           (((long long)bb * nsub + t) * a.nheads + hh) * kP;
                 for (int p = 0; p < kP; ++p) yr[p] = from_f32<Tout>(nanv);
             }
         }
@@ -235,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     auto load_step = [&](int st, StepIn& v) {
         const int item = (int)blockIdx.x + (st / nblocks) * (int)gridDim.x;
         const int hn = item % a.nheads, bn = item / a.nheads;
-        const int t = (st % nblocks) * kQ + row;
+        const int t = ((st % nblocks) * kQ + row) / RK;  // the row's step
         const long long i0 = ((long long)bn * a.seqlen + t) * a.nheads + hn;
         v.dt = t < a.seqlen ? a.dt[i0] : 0.0f;
         v.A = a.A[hn];
@@ -272,17 +280,21 @@ __global__ void __launch_bounds__(kThreads, 2)
             const long long i0 = (long long)b * a.seqlen * a.nheads + h;
             const float pw = a.seqlen > 0 ? a.dt[i0] * (1.0f - a.lam[i0]) : 0.0f;
             const int g = h / hpg;
-            const float pb = pw * __bfloat162float(a.prev_B[((long long)b * a.ngroups + g) * kNs + row]);
-            const uint4* px = reinterpret_cast<const uint4*>(
-                a.prev_x + ((long long)b * a.nheads + h) * kP + kHalf * part);
+#pragma unroll 1
+            for (int r = 0; r < RK; ++r) {  // sum over the previous token's ranks
+                const float pb =
+                    pw * __bfloat162float(a.prev_B[(((long long)b * RK + r) * a.ngroups + g) * kNs + row]);
+                const uint4* px = reinterpret_cast<const uint4*>(
+                    a.prev_x + (((long long)b * RK + r) * a.nheads + h) * kP + kHalf * part);
 #pragma unroll
-            for (int c = 0; c < kHalf / 8; ++c) {
-                const uint4 w = px[c];
-                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                for (int c = 0; c < kHalf / 8; ++c) {
+                    const uint4 w = px[c];
+                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    S[8 * c + 2 * e] = fmaf(pb, bf16lo(ww[e]), S[8 * c + 2 * e]);
-                    S[8 * c + 2 * e + 1] = fmaf(pb, bf16hi(ww[e]), S[8 * c + 2 * e + 1]);
+                    for (int e = 0; e < 4; ++e) {
+                        S[8 * c + 2 * e] = fmaf(pb, bf16lo(ww[e]), S[8 * c + 2 * e]);
+                        S[8 * c + 2 * e + 1] = fmaf(pb, bf16hi(ww[e]), S[8 * c + 2 * e + 1]);
+                    }
                 }
             }
         }
@@ -313,7 +325,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             gamma_i = in.lam * dti;
             w_i = gamma_i + in.dt1 * (1.0f - in.lam1);
         }
-        float v = dti * in.A;
+        // the step's log-decay enters the running sum once, at its first sub-token
+        float v = (RK == 1 || row % RK == 0) ? dti * in.A : 0.0f;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const float u = __shfl_up_sync(0xffffffffu, v, o);
@@ -392,9 +405,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 tmem_ld32(t_lane + kTmG + c0, gv);
                 tmem_wait_ld();
                 if (ck == quarter)
-                    mprime_chunk<true, M3>(gv, s_q2 + c0, cs2_i, lane, gamma_i, hp, lp);
+                    mprime_chunk<true, M3>(gv, s_q2 + c0, cs2_i, RK * (lane / RK) + RK - 1,
+                                           RK * (lane / RK), gamma_i, hp, lp);
                 else
-                    mprime_chunk<false, M3>(gv, s_q2 + c0, cs2_i, 31, gamma_i, hp, lp);
+                    mprime_chunk<false, M3>(gv, s_q2 + c0, cs2_i, 31, 0, gamma_i, hp, lp);
             }
             tmem_st16(t_lane + kTmG + c0, hp);
             tmem_st16(t_lane + kTmG + c0 + 16, lp);
@@ -505,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // ---- y rows out of the staged tile: each warp writes whole rows of
         // the head (coalesced); rows past the sequence end are skipped
         {
-            const long long yrow0 = ((long long)b * a.seqlen + t0) * a.nheads + h;
+            const long long yrow0 = ((long long)b * nsub + t0) * a.nheads + h;
             if constexpr (sizeof(Tout) == 4) {
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
@@ -513,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     const int t = idx >> 4, c16 = idx & 15;
                     const float4 v = *reinterpret_cast<const float4*>(
                         smem + kRS + (c16 >> 3) * 16384 + t * 128 + (((c16 & 7) ^ (t & 7)) << 4));
-                    if (t0 + t < a.seqlen)
+                    if (t0 + t < nsub)
                         *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.y) +
                                                    (yrow0 + (long long)t * a.nheads) * kP + 4 * c16) = v;
                 }
@@ -524,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     const int t = idx >> 3, c = idx & 7;
                     const uint4 v = *reinterpret_cast<const uint4*>(smem + kRS + t * 128 +
                                                                     ((c ^ (t & 7)) << 4));
-                    if (t0 + t < a.seqlen)
+                    if (t0 + t < nsub)
                         *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.y) +
                                                   (yrow0 + (long long)t * a.nheads) * kP + 8 * c) = v;
                 }
@@ -590,10 +604,10 @@ bool make_x_map(CUtensorMap* map, const void* base, int batch, int seqlen, int n
            CUDA_SUCCESS;
 }
 
-template <typename Tout, bool M3>
+template <typename Tout, bool M3, int RK>
 ssm_status_t launch(const CUtensorMap& mc, const CUtensorMap& mb, const CUtensorMap& mx,
                     const SsdArgs& a, cudaStream_t s) {
-    auto kern = ssd_fwd_kernel<Tout, M3>;
+    auto kern = ssd_fwd_kernel<Tout, M3, RK>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
         cudaSuccess)
         return SSM_ERR_CUDA;
@@ -618,22 +632,29 @@ ssm_status_t launch(const CUtensorMap& mc, const CUtensorMap& mb, const CUtensor
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
-// Validation and launch shared by the Mamba-2 (m3 = false) and Mamba-3 SISO
-// (m3 = true) entry points.
+// Validation and launch shared by the Mamba-2 (m3 = false), Mamba-3 SISO
+// (m3, rank 1) and Mamba-3 MIMO (m3, rank > 1) entry points.  seqlen counts
+// steps; x, y, B, C hold `rank` sub-tokens per step.
 ssm_status_t ssd_entry(const void* x, const float* dt, const float* lam, const float* A_head,
-                       const void* B, const void* C, int chunk, const float* initial_state,
-                       const void* prev_B, const void* prev_x, void* y, float* final_state,
-                       int batch, int seqlen, int nheads, int headdim, int dstate, int ngroups,
-                       ssm_dtype_t in_dtype, ssm_dtype_t out_dtype, bool m3, void* stream) {
+                       const void* B, const void* C, int chunk, int rank,
+                       const float* initial_state, const void* prev_B, const void* prev_x,
+                       void* y, float* final_state, int batch, int seqlen, int nheads,
+                       int headdim, int dstate, int ngroups, ssm_dtype_t in_dtype,
+                       ssm_dtype_t out_dtype, bool m3, void* stream) {
     using namespace ssm_host;
     if (batch < 0 || seqlen < 0 || nheads < 0 || headdim < 1 || dstate < 1 || ngroups < 1 ||
-        chunk < 1)
+        chunk < 1 || rank < 1)
         return SSM_ERR_SHAPE;
     if (nheads % ngroups != 0 || seqlen % chunk != 0) return SSM_ERR_SHAPE;
     if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return SSM_ERR_DTYPE;
-    if (chunk != 64 || headdim != kP || dstate != kNs || in_dtype != SSM_BF16)
+    // ranks 1, 2, 4 with chunk * rank = 64 sub-tokens (the pages: chunk 64 for
+    // SISO, 16 for MIMO rank 4)
+    if ((rank != 1 && rank != 2 && rank != 4) || chunk * rank != 64 || headdim != kP ||
+        dstate != kNs || in_dtype != SSM_BF16)
         return SSM_ERR_UNSUPPORTED;
-    const size_t rows = (size_t)batch * seqlen;
+    if ((long long)seqlen * rank > (long long)INT32_MAX) return SSM_ERR_UNSUPPORTED;
+    const size_t rows = (size_t)batch * seqlen * rank;   // sub-token rows
+    const size_t steps = (size_t)batch * seqlen;
     if (batch == 0 || nheads == 0) return SSM_OK;
     if ((size_t)batch * nheads > (size_t)INT32_MAX) return SSM_ERR_UNSUPPORTED;
     if (m3 && ((prev_B == nullptr) != (prev_x == nullptr))) return SSM_ERR_NULL;
@@ -665,18 +686,19 @@ ssm_status_t ssd_entry(const void* x, const float* dt, const float* lam, const f
     // before it is written, by the same threads), but no other overlap
     const size_t ib = (initial_state && initial_state != final_state) ? sb : 0;
     struct R { const void* p; size_t n; } ins[] = {
-        {x, xb}, {dt, rows * nheads * 4}, {A_head, (size_t)nheads * 4}, {B, bcb}, {C, bcb},
-        {initial_state, ib}, {lam, m3 ? rows * nheads * 4 : 0},
-        {prev_B, m3 && prev_B ? (size_t)batch * ngroups * dstate * 2 : 0},
-        {prev_x, m3 && prev_x ? (size_t)batch * nheads * headdim * 2 : 0}};
+        {x, xb}, {dt, steps * nheads * 4}, {A_head, (size_t)nheads * 4}, {B, bcb}, {C, bcb},
+        {initial_state, ib}, {lam, m3 ? steps * nheads * 4 : 0},
+        {prev_B, m3 && prev_B ? (size_t)batch * rank * ngroups * dstate * 2 : 0},
+        {prev_x, m3 && prev_x ? (size_t)batch * rank * nheads * headdim * 2 : 0}};
     for (const R& r : ins)
         if (overlaps(y, yb, r.p, r.n) || overlaps(final_state, fb, r.p, r.n)) return SSM_ERR_ALIAS;
     if (overlaps(y, yb, final_state, fb)) return SSM_ERR_ALIAS;
     if (initial_state && overlaps(y, yb, initial_state, sb)) return SSM_ERR_ALIAS;
 
     CUtensorMap mc, mb, mx;
-    if (!make_bc_map(&mc, C, batch, seqlen, ngroups) || !make_bc_map(&mb, B, batch, seqlen, ngroups) ||
-        !make_x_map(&mx, x, batch, seqlen, nheads))
+    const int nsub = seqlen * rank;
+    if (!make_bc_map(&mc, C, batch, nsub, ngroups) || !make_bc_map(&mb, B, batch, nsub, ngroups) ||
+        !make_x_map(&mx, x, batch, nsub, nheads))
         return SSM_ERR_CUDA;
     SsdArgs a{};
     a.x = static_cast<const __nv_bfloat16*>(x);
@@ -692,11 +714,17 @@ ssm_status_t ssd_entry(const void* x, const float* dt, const float* lam, const f
     a.seqlen = seqlen;
     a.nheads = nheads;
     a.ngroups = ngroups;
-    if (m3)
-        return out_dtype == SSM_BF16 ? launch<__nv_bfloat16, true>(mc, mb, mx, a, s)
-                                     : launch<float, true>(mc, mb, mx, a, s);
-    return out_dtype == SSM_BF16 ? launch<__nv_bfloat16, false>(mc, mb, mx, a, s)
-                                 : launch<float, false>(mc, mb, mx, a, s);
+    const bool bf = out_dtype == SSM_BF16;
+    if (!m3) return bf ? launch<__nv_bfloat16, false, 1>(mc, mb, mx, a, s)
+                       : launch<float, false, 1>(mc, mb, mx, a, s);
+    switch (rank) {
+        case 1: return bf ? launch<__nv_bfloat16, true, 1>(mc, mb, mx, a, s)
+                          : launch<float, true, 1>(mc, mb, mx, a, s);
+        case 2: return bf ? launch<__nv_bfloat16, true, 2>(mc, mb, mx, a, s)
+                          : launch<float, true, 2>(mc, mb, mx, a, s);
+        default: return bf ? launch<__nv_bfloat16, true, 4>(mc, mb, mx, a, s)
+                           : launch<float, true, 4>(mc, mb, mx, a, s);
+    }
 }
 
 }  // namespace
@@ -708,7 +736,7 @@ extern "C" ssm_status_t ssd_chunked_fwd(const void* x, const float* dt, const fl
                                         int headdim, int dstate, int ngroups,
                                         ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
                                         void* stream) {
-    return ssd_entry(x, dt, nullptr, A_head, B, C, chunk, initial_state, nullptr, nullptr, y,
+    return ssd_entry(x, dt, nullptr, A_head, B, C, chunk, 1, initial_state, nullptr, nullptr, y,
                      final_state, batch, seqlen, nheads, headdim, dstate, ngroups, in_dtype,
                      out_dtype, false, stream);
 }
@@ -720,7 +748,20 @@ extern "C" ssm_status_t ssd_mamba3_fwd(const void* x, const float* dt, const flo
                                        int batch, int seqlen, int nheads, int headdim,
                                        int dstate, int ngroups, ssm_dtype_t in_dtype,
                                        ssm_dtype_t out_dtype, void* stream) {
-    return ssd_entry(x, dt, lam, A_head, B, C, chunk, initial_state, prev_B, prev_x, y,
+    return ssd_entry(x, dt, lam, A_head, B, C, chunk, 1, initial_state, prev_B, prev_x, y,
+                     final_state, batch, seqlen, nheads, headdim, dstate, ngroups, in_dtype,
+                     out_dtype, true, stream);
+}
+
+extern "C" ssm_status_t ssd_mamba3_mimo_fwd(const void* x, const float* dt, const float* lam,
+                                            const float* A_head, const void* B, const void* C,
+                                            int chunk, int rank, const float* initial_state,
+                                            const void* prev_B, const void* prev_x, void* y,
+                                            float* final_state, int batch, int seqlen,
+                                            int nheads, int headdim, int dstate, int ngroups,
+                                            ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                                            void* stream) {
+    return ssd_entry(x, dt, lam, A_head, B, C, chunk, rank, initial_state, prev_B, prev_x, y,
                      final_state, batch, seqlen, nheads, headdim, dstate, ngroups, in_dtype,
                      out_dtype, true, stream);
 }

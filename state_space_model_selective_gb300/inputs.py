@@ -127,6 +127,31 @@ def mamba3_inputs(batch: int, seqlen: int, nheads: int, headdim: int, dstate: in
     return out
 
 
+def mamba3_mimo_inputs(batch: int, seqlen: int, rank: int, nheads: int, headdim: int,
+                       dstate: int, ngroups: int = 1, dtype: str = "bf16", seed: int = 1007,
+                       device: str = "cpu") -> dict:
+    """Inputs of the Mamba-3 MIMO prefill, rank inside the time position:
+    x (B, L, R, H, P), B, C (B, L, R, G, N) ~ N(0, 1) in dtype; dt (B, L, H) =
+    softplus(N(0, 1) - 4); lam (B, L, H) = sigmoid(N(0, 1)); A_head (H,) =
+    -U[1, 16]; the token before the first, prev_B (B, R, G, N) and prev_x
+    (B, R, H, P); an initial state h0 (B, H, P, N) ~ 0.1 N(0, 1)."""
+    g = _gen(seed, device)
+    td = _DTYPES[dtype]
+    x = _randn((batch, seqlen, rank, nheads, headdim), g, device)
+    Bm = _randn((batch, seqlen, rank, ngroups, dstate), g, device)
+    Cm = _randn((batch, seqlen, rank, ngroups, dstate), g, device)
+    dt = torch.nn.functional.softplus(_randn((batch, seqlen, nheads), g, device) - 4.0)
+    lam = torch.sigmoid(_randn((batch, seqlen, nheads), g, device))
+    A_head = -(1.0 + 15.0 * _rand((nheads,), g, device))
+    prev_B = _randn((batch, rank, ngroups, dstate), g, device)
+    prev_x = _randn((batch, rank, nheads, headdim), g, device)
+    h0 = 0.1 * _randn((batch, nheads, headdim, dstate), g, device)
+    return {"x": x.to(td).contiguous(), "dt": dt.contiguous(), "lam": lam.contiguous(),
+            "A_head": A_head.contiguous(), "B": Bm.to(td).contiguous(),
+            "C": Cm.to(td).contiguous(), "prev_B": prev_B.to(td).contiguous(),
+            "prev_x": prev_x.to(td).contiguous(), "h0": h0.contiguous()}
+
+
 def decode_inputs(batch: int, nheads: int, headdim: int, dstate: int, ngroups: int = 1,
                   steps: int = 1, dtype: str = "f32", seed: int = 1005,
                   gate: bool = False, dskip: str = "ones", device: str = "cpu") -> dict:

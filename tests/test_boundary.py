@@ -204,3 +204,40 @@ def test_mamba3_decode_argument_errors(L):
     assert m3_decode_call(L, px=P(0)) == ALIAS          # previous x inside the state
     assert m3_decode_call(L, y=P(1)) == ALIAS           # y on top of prev_B
     assert m3_decode_call(L, batch=0) == OK
+
+
+def test_mimo_argument_errors(L):
+    def ssd(**kw):
+        a = dict(x=P(0), dt=P(1), lam=P(7), A=P(2), B=P(3), C=P(4), chunk=16, rank=4, h0=None,
+                 pB=None, px=None, y=P(5), fs=P(6), batch=2, seqlen=32, nheads=4, headdim=64,
+                 dstate=128, ngroups=1, in_dt=1, out_dt=0, stream=None)
+        a.update(kw)
+        return L.ssd_mamba3_mimo_fwd(a["x"], a["dt"], a["lam"], a["A"], a["B"], a["C"],
+                                     a["chunk"], a["rank"], a["h0"], a["pB"], a["px"], a["y"],
+                                     a["fs"], a["batch"], a["seqlen"], a["nheads"], a["headdim"],
+                                     a["dstate"], a["ngroups"], a["in_dt"], a["out_dt"],
+                                     a["stream"])
+    assert ssd(rank=3, chunk=16) == UNSUP              # rank 3 unsupported
+    assert ssd(chunk=64, seqlen=64) == UNSUP           # chunk * rank must be 64
+    assert ssd(seqlen=40) == SHAPE                     # seqlen % chunk
+    assert ssd(rank=0) == SHAPE
+    assert ssd(lam=None) == NULL
+    assert ssd(pB=P(8)) == NULL
+    assert ssd(batch=0, x=None, y=None) == OK
+
+    def dec(**kw):
+        a = dict(state=P(0), pB=P(1), px=P(2), x=P(3), dt=P(4), lam=P(5), A=P(6), B=P(7),
+                 C=P(8), D=None, z=None, y=P(9), batch=2, rank=4, nheads=4, headdim=64,
+                 dstate=128, ngroups=1, dtype=0, stream=None)
+        a.update(kw)
+        return L.ssm_decode_step_mamba3_mimo(a["state"], a["pB"], a["px"], a["x"], a["dt"],
+                                             a["lam"], a["A"], a["B"], a["C"], a["D"], a["z"],
+                                             a["y"], a["batch"], a["rank"], a["nheads"],
+                                             a["headdim"], a["dstate"], a["ngroups"], a["dtype"],
+                                             a["stream"])
+    assert dec(dstate=64) == UNSUP                     # MIMO decode runs dstate 128 only
+    assert dec(rank=3) == UNSUP
+    assert dec(rank=0) == SHAPE
+    assert dec(lam=None) == NULL
+    assert dec(y=P(1)) == ALIAS
+    assert dec(batch=0) == OK
