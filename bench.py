@@ -368,6 +368,26 @@ def measure_other_paths(dev, reps=20):
                      "frac": nbytes3 / (ms / 1e3) / 1e9 / HBM_PEAK_GBS,
                      "algorithmic_bytes": nbytes3}}
     del m3, y, fs
+    mi = inputs.mamba3_mimo_inputs(32, 256, 4, 32, 64, 128, 1, "bf16", seed=1007, device="cuda")
+    ym = torch.empty(mi["x"].shape, device=dev)
+    fsm = torch.empty(32, 32, 64, 128, device=dev)
+
+    def ssd_mimo():
+        binding.ssd_mamba3_mimo_fwd(mi["x"], mi["dt"], mi["lam"], mi["A_head"], mi["B"], mi["C"],
+                                    16, out_dtype=torch.float32, y=ym, final_state=fsm,
+                                    prev_B=mi["prev_B"], prev_x=mi["prev_x"])
+    ms = _time(ssd_mimo, reps)
+    nbm = (mi["x"].numel() * 2 + ym.numel() * 4 + 2 * mi["B"].numel() * 2 +
+           2 * mi["dt"].numel() * 4 + fsm.numel() * 4 + mi["prev_B"].numel() * 2 +
+           mi["prev_x"].numel() * 2)
+    res["ssd_mamba3_mimo_fwd"] = {
+        "workload": "Mamba-3 MIMO rank 4 chunked prefill bf16 in / fp32 y, batch 32, L 256, "
+                    "32 heads, headdim 64, d_state 128, chunk 16", "ms": ms,
+        "elements_per_s": el * 4 / (ms / 1e3),
+        "roofline": {"bound": "hbm", "achieved": nbm / (ms / 1e3) / 1e9,
+                     "peak": HBM_PEAK_GBS, "unit": "GB/s",
+                     "frac": nbm / (ms / 1e3) / 1e9 / HBM_PEAK_GBS, "algorithmic_bytes": nbm}}
+    del mi, ym, fsm
     g = torch.Generator(device="cuda")
     g.manual_seed(1005)
     B_, H, P, N = 256, 32, 64, 128
@@ -399,6 +419,25 @@ def measure_other_paths(dev, reps=20):
         binding.ssm_decode_step_mamba3(state, Bp, xp, x, dt, lam, A, Bm, Cm, D, y=yd)
     ms = _time(dec_m3, reps)
     nbytes3 = nbytes + lam.numel() * 4 + xp.numel() * 4 + Bp.numel() * 4
+    xr = torch.randn(B_, 4, H, P, device=dev, generator=g)
+    xpr = torch.randn(B_, 4, H, P, device=dev, generator=g)
+    Br = torch.randn(B_, 4, 1, N, device=dev, generator=g)
+    Cr = torch.randn(B_, 4, 1, N, device=dev, generator=g)
+    Bpr = torch.randn(B_, 4, 1, N, device=dev, generator=g)
+    yr = torch.empty_like(xr)
+
+    def dec_mimo():
+        binding.ssm_decode_step_mamba3_mimo(state, Bpr, xpr, xr, dt, lam, A, Br, Cr, D, y=yr)
+    ms_m = _time(dec_mimo, reps)
+    nbytes_m = (2 * state.numel() * 4 + (xr.numel() + xpr.numel() + yr.numel()) * 4 +
+                (Br.numel() + Cr.numel() + Bpr.numel()) * 4 + 2 * dt.numel() * 4)
+    res["ssm_decode_step_mamba3_mimo"] = {
+        "workload": "Mamba-3 MIMO rank 4 decode step fp32, batch 256, 32 heads, headdim 64, "
+                    "d_state 128", "ms": ms_m, "elements_per_s": state.numel() / (ms_m / 1e3),
+        "roofline": {"bound": "hbm", "achieved": nbytes_m / (ms_m / 1e3) / 1e9,
+                     "peak": HBM_PEAK_GBS, "unit": "GB/s",
+                     "frac": nbytes_m / (ms_m / 1e3) / 1e9 / HBM_PEAK_GBS,
+                     "algorithmic_bytes": nbytes_m}}
     res["ssm_decode_step_mamba3"] = {
         "workload": "Mamba-3 SISO decode step fp32, batch 256, 32 heads, headdim 64, d_state 128",
         "ms": ms, "elements_per_s": state.numel() / (ms / 1e3),
