@@ -403,6 +403,9 @@ __global__ void __launch_bounds__(kBulkThreads)
     extern __shared__ __align__(128) uint8_t dsm[];
     uint64_t* full = reinterpret_cast<uint64_t*>(dsm + 2 * kTileBytes);
     uint64_t* empty = full + 2;
+    // the tile's weighted inputs, gamma x[r][p] and beta prev_x[r][p], fp32
+    float* sx = reinterpret_cast<float*>(dsm + 2 * kTileBytes + 64);
+    float* sxp = sx + RK * kBulkRows;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nchunks = (headdim + kBulkRows - 1) / kBulkRows;
     const long long ntiles = (long long)batch * nheads * nchunks;
@@ -450,7 +453,18 @@ __global__ void __launch_bounds__(kBulkThreads)
         const float gam = m3.lam[bh] * dtv;
         const float bet = (dtv - gam) * alpha;
         const long long xrow0 = (b * RK * nheads + h) * (long long)headdim + p0;  // rank 0
-        if (!mbar_wait(&full[s], (uint32_t)((i >> 1) & 1), nullptr)) break;
+        // stage gamma x and beta prev_x of the tile's rows (the previous tile's
+        // reads are finished: named barrier at the end of each tile)
+        for (int k = tid; k < RK * kBulkRows; k += kBulkCompute) {
+            const int r = k / kBulkRows, p = k % kBulkRows;
+            const bool v = p < nr;
+            sx[k] = v ? gam * to_f32(x[xrow0 + r * rstride_x + p]) : 0.0f;
+            sxp[k] = v ? bet * to_f32(m3.prev_x[xrow0 + r * rstride_x + p]) : 0.0f;
+        }
+        // every compute warp takes the same branch: a timed-out wait ends all of
+        // them here, before the barrier at the end of the tile
+        const bool got = mbar_wait(&full[s], (uint32_t)((i >> 1) & 1), nullptr);
+        if (!named_bar_and(1, kBulkCompute, got)) break;
         float* st = reinterpret_cast<float*>(dsm + s * kTileBytes);
 
         // state update of rows warp, warp + 4, ... (in place)
@@ -461,8 +475,7 @@ __global__ void __launch_bounds__(kBulkThreads)
             float in[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int r = 0; r < RK; ++r) {
-                const float xg = gam * to_f32(x[xrow0 + r * rstride_x + p]);
-                const float xb = bet * to_f32(m3.prev_x[xrow0 + r * rstride_x + p]);
+                const float xg = sx[r * kBulkRows + p], xb = sxp[r * kBulkRows + p];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) in[k] = fmaf(xg, bv[r][k], fmaf(xb, bp[r][k], in[k]));
             }
@@ -508,6 +521,7 @@ __global__ void __launch_bounds__(kBulkThreads)
         fence_proxy_async_smem();  // the updated tile is read by the bulk store
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
+        named_bar_sync(1, kBulkCompute);  // sx, sxp are rewritten for the next tile
     }
 }
 
@@ -560,7 +574,7 @@ ssm_status_t launch_bulk_mimo(float* state, const void* x, const float* dt, cons
                 return SSM_ERR_CUDA;
             if (cudaFuncSetAttribute(decode_bulk_mimo_kernel<T, RK>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kBulkSmem) != cudaSuccess)
+                                     kBulkSmem + 2 * RK * kBulkRows * 4) != cudaSuccess)
                 return SSM_ERR_CUDA;
             cached_dev = dev;
         }
@@ -568,7 +582,7 @@ ssm_status_t launch_bulk_mimo(float* state, const void* x, const float* dt, cons
     const long long tiles =
         (long long)batch * nheads * ((headdim + kBulkRows - 1) / kBulkRows);
     const unsigned grid = (unsigned)std::min<long long>(tiles, 3LL * sms);
-    decode_bulk_mimo_kernel<T, RK><<<grid, kBulkThreads, kBulkSmem, s>>>(
+    decode_bulk_mimo_kernel<T, RK><<<grid, kBulkThreads, kBulkSmem + 2 * RK * kBulkRows * 4, s>>>(
         state, static_cast<const T*>(x), dt, A, static_cast<const T*>(B),
         static_cast<const T*>(C), D, static_cast<const T*>(z), static_cast<T*>(y), batch, nheads,
         headdim, ngroups, m3);
