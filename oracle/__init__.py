@@ -64,6 +64,7 @@ def _load():
             lib.oracle_mamba3_mimo_recurrence.argtypes = [dp] * 11 + [i] * 7
             lib.oracle_mamba3_mimo_chunked.argtypes = [dp] * 11 + [i] * 8
             lib.oracle_mamba3_mimo_decode_step.argtypes = [dp] * 12 + [i] * 6
+            lib.oracle_scan_bwd.argtypes = [dp] * 8 + [i] + [dp] * 12 + [i] * 5
             lib.oracle_combine.argtypes = [ctypes.c_double] * 4 + [dp, dp]
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -123,6 +124,33 @@ def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=Fals
     _load().oracle_scan(*[_ptr(a) for a in arrs[:8]], int(bool(delta_softplus)),
                         _ptr(arrs[8]), _ptr(y), _ptr(hs), *dims)
     return y, hs
+
+
+def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softplus=False,
+             h0=None, dfinal=None):
+    """Gradient of ``scan`` for the loss sum(dy * y) + sum(dfinal * final_state).
+
+    Returns a dict of float64 arrays: du, ddelta, dz (B, D, L); dA (D, N);
+    dB, dC (B, G, N, L); dD, dbias (D,); dh0 (B, D, N).  dz, dD, dbias are None
+    when z, D, delta_bias are."""
+    arrs, dims = _scan_args(u, delta, A, B, C, D, z, delta_bias, h0)
+    batch, dim, seqlen, dstate, ngroups = dims
+    dy, dfinal = _f64(dy), _f64(dfinal)
+    assert dy.shape == (batch, dim, seqlen)
+    assert dfinal is None or dfinal.shape == (batch, dim, dstate)
+    g = {"du": np.empty((batch, dim, seqlen)), "ddelta": np.empty((batch, dim, seqlen)),
+         "dA": np.empty((dim, dstate)), "dB": np.empty((batch, ngroups, dstate, seqlen)),
+         "dC": np.empty((batch, ngroups, dstate, seqlen)),
+         "dD": np.empty(dim) if arrs[5] is not None else None,
+         "dz": np.empty((batch, dim, seqlen)) if arrs[6] is not None else None,
+         "dbias": np.empty(dim) if arrs[7] is not None else None,
+         "dh0": np.empty((batch, dim, dstate))}
+    _load().oracle_scan_bwd(*[_ptr(a) for a in arrs[:8]], int(bool(delta_softplus)),
+                            _ptr(arrs[8]), _ptr(dy), _ptr(dfinal), _ptr(g["du"]),
+                            _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
+                            _ptr(g["dD"]), _ptr(g["dz"]), _ptr(g["dbias"]), _ptr(g["dh0"]),
+                            *dims)
+    return g
 
 
 def scan_pieces(u, delta, A, B, C, cuts, D=None, z=None, delta_bias=None,

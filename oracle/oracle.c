@@ -41,6 +41,10 @@
  *       B x = sum_r B[n,r] x[p,r] and y[p,r] = sum_n state[n,p] C[n,r], and the
  *       rank-flattened chunked form with a block-diagonal correction
  *       (oracle_mamba3_mimo_*).
+ *  oracle_scan_bwd: the gradient of the scan above by reverse-mode
+ *       differentiation of the same recurrence (the pages mention backward
+ *       parity but print no formula; the derivative is pinned by finite
+ *       differences of oracle_scan).
  *
  * Readings taken where the pages are silent (each is listed with its reason
  * in the design notes):
@@ -847,6 +851,106 @@ void oracle_mamba3_mimo_decode_step(double* state, const double* prev_B, const d
             y[ix] = out;
         }
     }
+}
+
+/*
+ * Gradient of oracle_scan for the loss  sum_t dy . y + sum dfinal . final_state
+ * (dfinal may be NULL), by differentiating the recurrence in reverse:
+ *   lambda_t = dL/dh_t = dy0_t C_t + a_{t+1} lambda_{t+1},   dy0_t = dy_t silu(z_t)
+ *   dC_t += dy0_t h_t;  dB_t += lambda_t dl_t u_t;  du_t = dy0_t D + sum_n lambda_t dl_t B_t
+ *   d dl_t = sum_n lambda_t (h_{t-1} A a_t + B_t u_t);  dA += lambda_t h_{t-1} a_t dl_t
+ *   ddelta_t = d dl_t * sigmoid(delta_t + bias) (softplus) or d dl_t;  dbias += ddelta_t
+ *   dz_t = dy_t y0_t silu'(z_t);  dD += dy0_t u_t;  dh0 = a_0 lambda_0.
+ * Serial over rows (dB, dC, dA, dD, dbias are sums over several rows), for
+ * small problems.  Arguments as oracle_scan plus dy (batch, dim, seqlen) and
+ * dfinal (batch, dim, dstate) in, and out: du, ddelta, dz (batch, dim,
+ * seqlen), dA (dim, dstate), dB, dC (batch, ngroups, dstate, seqlen), dD,
+ * dbias (dim), dh0 (batch, dim, dstate).  dz, dD, dbias, dh0 may be NULL
+ * (their inputs absent or the gradient not wanted).
+ */
+void oracle_scan_bwd(const double* u, const double* delta, const double* A,
+                     const double* Bm, const double* Cm, const double* Dskip,
+                     const double* z, const double* delta_bias, int delta_softplus,
+                     const double* h0, const double* dy, const double* dfinal,
+                     double* du, double* ddelta, double* dA, double* dB, double* dC,
+                     double* dD, double* dz, double* dbias, double* dh0,
+                     int batch, int dim, int seqlen, int dstate, int ngroups)
+{
+    const int dim_per_group = dim / ngroups;
+    memset(dA, 0, sizeof(double) * (size_t)dim * dstate);
+    memset(dB, 0, sizeof(double) * (size_t)batch * ngroups * dstate * seqlen);
+    memset(dC, 0, sizeof(double) * (size_t)batch * ngroups * dstate * seqlen);
+    if (dD) memset(dD, 0, sizeof(double) * (size_t)dim);
+    if (dbias) memset(dbias, 0, sizeof(double) * (size_t)dim);
+    double* H = (double*)malloc(sizeof(double) * (size_t)(seqlen + 1) * dstate);  /* h_{t-1} at t */
+    double* Aa = (double*)malloc(sizeof(double) * (size_t)seqlen * dstate);        /* a_t */
+    double* dl = (double*)malloc(sizeof(double) * (size_t)seqlen);
+    double* pre = (double*)malloc(sizeof(double) * (size_t)seqlen);  /* delta + bias */
+    double* y0 = (double*)malloc(sizeof(double) * (size_t)seqlen);
+    double* lam = (double*)malloc(sizeof(double) * (size_t)dstate);
+    for (long long row = 0; row < (long long)batch * dim; ++row) {
+        const int b = (int)(row / dim);
+        const int d = (int)(row % dim);
+        const int g = d / dim_per_group;
+        const size_t io = (size_t)row * (size_t)seqlen;
+        const size_t bc = ((size_t)b * ngroups + g) * (size_t)dstate * (size_t)seqlen;
+        const double Dd = Dskip ? Dskip[d] : 0.0;
+        /* forward, keeping every state */
+        for (int n = 0; n < dstate; ++n) H[n] = h0 ? h0[row * dstate + n] : 0.0;
+        for (int t = 0; t < seqlen; ++t) {
+            pre[t] = delta[io + t] + (delta_bias ? delta_bias[d] : 0.0);
+            dl[t] = delta_softplus ? softplus_d(pre[t]) : pre[t];
+            double acc = 0.0;
+            for (int n = 0; n < dstate; ++n) {
+                const double a = exp(dl[t] * A[(size_t)d * dstate + n]);
+                Aa[(size_t)t * dstate + n] = a;
+                const double hn = a * H[(size_t)t * dstate + n] +
+                                  dl[t] * Bm[bc + (size_t)n * seqlen + t] * u[io + t];
+                H[(size_t)(t + 1) * dstate + n] = hn;
+                acc += Cm[bc + (size_t)n * seqlen + t] * hn;
+            }
+            y0[t] = acc + Dd * u[io + t];
+        }
+        /* reverse */
+        for (int n = 0; n < dstate; ++n) lam[n] = dfinal ? dfinal[row * dstate + n] : 0.0;
+        for (int t = seqlen - 1; t >= 0; --t) {
+            const double ut = u[io + t];
+            double dy0 = dy[io + t];
+            if (z) {
+                const double zt = z[io + t];
+                const double sg = 1.0 / (1.0 + exp(-zt));
+                if (dz) dz[io + t] = dy0 * y0[t] * sg * (1.0 + zt * (1.0 - sg));
+                dy0 *= zt * sg;
+            }
+            double dut = dy0 * Dd;
+            if (dD) dD[d] += dy0 * ut;
+            double ddl = 0.0;
+            for (int n = 0; n < dstate; ++n) {
+                const size_t ib = bc + (size_t)n * seqlen + t;
+                const double a = Aa[(size_t)t * dstate + n];
+                const double hprev = H[(size_t)t * dstate + n];
+                lam[n] += dy0 * Cm[ib];
+                dC[ib] += dy0 * H[(size_t)(t + 1) * dstate + n];
+                dB[ib] += lam[n] * dl[t] * ut;
+                dA[(size_t)d * dstate + n] += lam[n] * hprev * a * dl[t];
+                ddl += lam[n] * (hprev * a * A[(size_t)d * dstate + n] + Bm[ib] * ut);
+                dut += lam[n] * dl[t] * Bm[ib];
+                lam[n] *= a;
+            }
+            du[io + t] = dut;
+            const double dd = delta_softplus ? ddl / (1.0 + exp(-pre[t])) : ddl;
+            ddelta[io + t] = dd;
+            if (dbias) dbias[d] += dd;
+        }
+        if (dh0)
+            for (int n = 0; n < dstate; ++n) dh0[row * dstate + n] = lam[n];
+    }
+    free(H);
+    free(Aa);
+    free(dl);
+    free(pre);
+    free(y0);
+    free(lam);
 }
 
 int oracle_num_threads(void)

@@ -634,3 +634,71 @@ def test_mimo_decode_chain_equals_recurrence():
         np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-13)
         pB, px = c["B"][:, t], c["x"][:, t]
     np.testing.assert_allclose(state, hs_ref, rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------------ scan backward pins
+
+_BWD_INPUTS = ("u", "delta", "A", "B", "C", "D", "z", "delta_bias", "h0")
+
+
+def _bwd_case(seed, softplus, use_z, use_D, use_bias, use_h0, ngroups=1):
+    rng = _rng(seed)
+    batch, dim, seqlen, dstate = 2, 4, 6, 3
+    c = dict(u=rng.standard_normal((batch, dim, seqlen)),
+             delta=0.5 * rng.standard_normal((batch, dim, seqlen)) + (0.0 if softplus else 0.6),
+             A=-rng.uniform(0.5, 2.0, (dim, dstate)),
+             B=rng.standard_normal((batch, ngroups, dstate, seqlen)),
+             C=rng.standard_normal((batch, ngroups, dstate, seqlen)),
+             D=rng.standard_normal(dim) if use_D else None,
+             z=rng.standard_normal((batch, dim, seqlen)) if use_z else None,
+             delta_bias=0.3 * rng.standard_normal(dim) if use_bias else None,
+             h0=rng.standard_normal((batch, dim, dstate)) if use_h0 else None)
+    dy = rng.standard_normal((batch, dim, seqlen))
+    dfinal = rng.standard_normal((batch, dim, dstate))
+    return c, dy, dfinal
+
+
+def _loss(c, dy, dfinal, softplus):
+    y, hs = oracle.scan(c["u"], c["delta"], c["A"], c["B"], c["C"], c["D"], c["z"],
+                        c["delta_bias"], softplus, c["h0"])
+    return float(np.sum(dy * y) + np.sum(dfinal * hs))
+
+
+@pytest.mark.parametrize("softplus,use_z,use_D,use_bias,use_h0,ngroups",
+                         [(True, True, True, True, True, 1), (False, False, False, False, False, 2),
+                          (True, False, True, False, True, 4), (False, True, False, True, False, 1)])
+def test_scan_bwd_equals_finite_differences(softplus, use_z, use_D, use_bias, use_h0, ngroups):
+    """Every gradient entry against a central difference of the forward oracle's
+    loss sum(dy y) + sum(dfinal final_state), step 1e-6 (fp64)."""
+    c, dy, dfinal = _bwd_case(211, softplus, use_z, use_D, use_bias, use_h0, ngroups)
+    g = oracle.scan_bwd(c["u"], c["delta"], c["A"], c["B"], c["C"], dy, c["D"], c["z"],
+                        c["delta_bias"], softplus, c["h0"], dfinal)
+    names = {"u": "du", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
+             "z": "dz", "delta_bias": "dbias", "h0": "dh0"}
+    eps = 1e-6
+    for k in _BWD_INPUTS:
+        if c[k] is None:
+            continue
+        grad = g[names[k]]
+        fd = np.zeros_like(c[k])
+        for idx in np.ndindex(c[k].shape):
+            cp = {kk: (None if vv is None else vv.copy()) for kk, vv in c.items()}
+            cp[k][idx] += eps
+            lp = _loss(cp, dy, dfinal, softplus)
+            cp[k][idx] -= 2 * eps
+            lm = _loss(cp, dy, dfinal, softplus)
+            fd[idx] = (lp - lm) / (2 * eps)
+        np.testing.assert_allclose(grad, fd, rtol=1e-6, atol=1e-7, err_msg=k)
+
+
+def test_scan_bwd_is_linear_in_dy():
+    """The gradient is linear in the output cotangent: g(dy1 + 2 dy2) = g(dy1) + 2 g(dy2)."""
+    c, dy, _ = _bwd_case(223, True, True, True, True, True)
+    dy2 = _rng(224).standard_normal(dy.shape)
+    args = (c["u"], c["delta"], c["A"], c["B"], c["C"])
+    kw = dict(D=c["D"], z=c["z"], delta_bias=c["delta_bias"], delta_softplus=True, h0=c["h0"])
+    g1 = oracle.scan_bwd(*args, dy, **kw)
+    g2 = oracle.scan_bwd(*args, dy2, **kw)
+    g3 = oracle.scan_bwd(*args, dy + 2 * dy2, **kw)
+    for k in ("du", "dB", "dC", "dD", "dh0"):
+        np.testing.assert_allclose(g3[k], g1[k] + 2 * g2[k], rtol=1e-11, atol=1e-12, err_msg=k)

@@ -66,6 +66,12 @@ MUTANTS = {
     "mimo_decode_reads_out_rank0": (
         "const double* Cr = Cm + (((size_t)b * rank + r) * ngroups + g) * dstate;",
         "const double* Cr = Cm + (((size_t)b * rank + 0) * ngroups + g) * dstate;"),
+    "bwd_adjoint_not_decayed": ("                lam[n] *= a;\n", "                lam[n] *= 1.0;\n"),
+    "bwd_dA_drops_dt": ("dA[(size_t)d * dstate + n] += lam[n] * hprev * a * dl[t];",
+                        "dA[(size_t)d * dstate + n] += lam[n] * hprev * a;"),
+    "bwd_softplus_derivative_sign": ("ddl / (1.0 + exp(-pre[t]))", "ddl / (1.0 + exp(pre[t]))"),
+    "bwd_dC_uses_previous_state": ("dC[ib] += dy0 * H[(size_t)(t + 1) * dstate + n];",
+                                   "dC[ib] += dy0 * H[(size_t)t * dstate + n];"),
     "mamba3_decode_terms_swapped": (
         "s[n] = alpha * s[n] + beta * Bp[n] * xp + gamma * Bt[n] * xv;",
         "s[n] = alpha * s[n] + beta * Bt[n] * xv + gamma * Bp[n] * xp;"),
