@@ -9,6 +9,7 @@
  *   ssd_mamba3_fwd, ssm_decode_step_mamba3  the same two for Mamba-3 SISO
  *                    (trapezoidal three-term recurrence)
  *   ssd_mamba3_mimo_fwd, ssm_decode_step_mamba3_mimo  Mamba-3 MIMO (rank R)
+ *   ssm_scan_bwd     gradient of ssm_scan_fwd (reverse mode, every input)
  *
  * Conventions shared by every entry point
  *  - Pointers are DEVICE pointers unless stated otherwise, to dense row-major
@@ -301,6 +302,67 @@ ssm_status_t ssm_scan_fwd_noalloc(const void* u, const void* delta, const float*
                                   const float* initial_state, void* y, float* final_state,
                                   int batch, int dim, int seqlen, int dstate, int ngroups,
                                   ssm_dtype_t in_dtype, ssm_dtype_t out_dtype, void* stream);
+
+/*
+ * Bytes of device workspace ssm_scan_bwd needs for this problem (a pure
+ * function of its arguments).  Returns 0 if the arguments are invalid.
+ * About (ceil(seqlen / 16) * batch * dim * 64 + ceil(dim / ngroups / 32) *
+ * batch * ngroups * seqlen * 128) bytes plus ssm_scan_workspace_bytes.
+ */
+size_t ssm_scan_bwd_workspace_bytes(int batch, int dim, int seqlen, int dstate, int ngroups);
+
+/*
+ * Gradient of the selective scan.
+ *   The forward operation is ssm_scan_fwd's ("We brought Mamba to Trainium --
+ *   and mapped where custom kernels actually help", section "Mamba: bringing
+ *   an unsupported model to the chip, and writing its missing kernel", with
+ *   the discretisation, D skip and gate of "Mamba-3 NKI Kernels for AWS
+ *   Neuron", section "How it works").  The second page reports gradient
+ *   parity of its mixer (section "Correctness", backward parity through
+ *   autograd) but prints no backward formula; this is the exact reverse-mode
+ *   derivative of the recurrence.
+ *
+ * For the scalar loss  sum(dy * y) + sum(dfinal_state * final_state), with y
+ * and final_state what ssm_scan_fwd returns for the same inputs, writes the
+ * loss's derivative with respect to every input:
+ *   du, ddelta            (batch, dim, seqlen)            fp32
+ *   dA                    (dim, dstate)                   fp32
+ *   dB, dC                (batch, ngroups, dstate, seqlen) fp32
+ *   dD, ddelta_bias       (dim,)                          fp32, may be NULL
+ *   dz                    (batch, dim, seqlen)            fp32
+ *   dinitial_state        (batch, dim, dstate)            fp32, may be NULL
+ * ddelta is the derivative with respect to the raw delta (through the
+ * softplus when delta_softplus is set).  dD and ddelta_bias are written
+ * whenever they are non-NULL, also when D or delta_bias is NULL (then they are
+ * the derivative at D = 0 or delta_bias = 0).  dz is required when z is given
+ * (SSM_ERR_NULL otherwise) and ignored when z is NULL.  dinitial_state is the
+ * derivative with respect to the initial state (zero when initial_state is
+ * NULL).
+ *
+ * Inputs: u, delta, A, B, C, D, z, delta_bias, delta_softplus, initial_state
+ * exactly as for ssm_scan_fwd; dy (batch, dim, seqlen) in in_dtype;
+ * dfinal_state (batch, dim, dstate) fp32 or NULL (zero).
+ * workspace: at least ssm_scan_bwd_workspace_bytes(...) bytes, contents on
+ * entry irrelevant, not shared with a concurrent call.  ssm_last_device_status
+ * reads it afterwards like ssm_scan_fwd's (the call runs the forward
+ * recurrence once more to store the state every 16 steps, then sweeps
+ * backwards; both run on `stream`).
+ * Every output must be disjoint from every input, from the other outputs and
+ * from the workspace (SSM_ERR_ALIAS).  The sums over channels (dB, dC) and
+ * over the batch (dA, dD, ddelta_bias) are added in a fixed order: the result
+ * is the same on every run.
+ * Supported: dstate == 16; dim % ngroups == 0; any batch, dim, seqlen >= 0.
+ * With no steps (seqlen == 0 or batch == 0) dA, dD, ddelta_bias are zeroed and
+ * dinitial_state = dfinal_state (or 0); the workspace is not touched then.
+ */
+ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B,
+                          const void* C, const float* D, const void* z, const float* delta_bias,
+                          int delta_softplus, const float* initial_state, const void* dy,
+                          const float* dfinal_state, float* du, float* ddelta, float* dA,
+                          float* dB, float* dC, float* dD, float* dz, float* ddelta_bias,
+                          float* dinitial_state, int batch, int dim, int seqlen, int dstate,
+                          int ngroups, ssm_dtype_t in_dtype, void* workspace,
+                          size_t workspace_bytes, void* stream);
 
 /*
  * Waits for `stream` to drain, then returns the device-side status the last

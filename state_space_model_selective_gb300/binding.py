@@ -29,7 +29,7 @@ STATUS_NAMES = {0: "SSM_OK", 1: "SSM_ERR_NULL", 2: "SSM_ERR_SHAPE", 3: "SSM_ERR_
 EXPORTS = ["ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_bytes", "ssm_scan_fwd",
            "ssd_chunked_fwd", "ssd_mamba3_fwd", "ssd_mamba3_mimo_fwd", "ssm_decode_step",
            "ssm_decode_step_mamba3", "ssm_decode_step_mamba3_mimo", "ssm_last_device_status",
-           "ssm_scan_fwd_noalloc"]
+           "ssm_scan_fwd_noalloc", "ssm_scan_bwd_workspace_bytes", "ssm_scan_bwd"]
 
 
 class SSMError(RuntimeError):
@@ -72,6 +72,10 @@ def lib() -> ctypes.CDLL:
         L.ssm_decode_step_mamba3_mimo.argtypes = [vp] * 12 + [i] * 7 + [vp]
         L.ssm_scan_fwd_noalloc.restype = i
         L.ssm_scan_fwd_noalloc.argtypes = [vp] * 8 + [i] + [vp] * 3 + [i] * 7 + [vp]
+        L.ssm_scan_bwd_workspace_bytes.restype = sz
+        L.ssm_scan_bwd_workspace_bytes.argtypes = [i] * 5
+        L.ssm_scan_bwd.restype = i
+        L.ssm_scan_bwd.argtypes = [vp] * 8 + [i] + [vp] * 12 + [i] * 6 + [vp, sz, vp]
         L.ssm_last_device_status.restype = i
         L.ssm_last_device_status.argtypes = [vp, vp]
         _lib = L
@@ -160,6 +164,75 @@ def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softp
                             _stream(stream))
     _check(st, "ssm_scan_fwd")
     return y, final_state
+
+
+def ssm_scan_bwd_workspace_bytes(batch, dim, seqlen, dstate=16, ngroups=1) -> int:
+    return int(lib().ssm_scan_bwd_workspace_bytes(batch, dim, seqlen, dstate, ngroups))
+
+
+def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softplus=False,
+                 initial_state=None, dfinal_state=None, workspace=None, want_dD=None,
+                 want_ddelta_bias=None, want_dinitial_state=True, out=None, stream=None):
+    """Gradient of ``ssm_scan_fwd`` for the loss sum(dy * y) + sum(dfinal_state *
+    final_state).  Inputs as for ``ssm_scan_fwd``; dy (batch, dim, seqlen) in u's
+    dtype; dfinal_state (batch, dim, dstate) fp32 or None.  Returns a dict of fp32
+    tensors: du, ddelta, dz (batch, dim, seqlen); dA (dim, dstate); dB, dC
+    (batch, ngroups, dstate, seqlen); dD, ddelta_bias (dim,); dinitial_state
+    (batch, dim, dstate).  dz is None without z; dD / ddelta_bias are computed
+    when D / delta_bias is given, or when want_dD / want_ddelta_bias is true.
+    ``out`` may map any of these names to a preallocated fp32 tensor to write."""
+    _req(u, "u", ndim=3)
+    in_dt = u.dtype
+    if in_dt not in _DT:
+        raise TypeError("u must be float32 or bfloat16")
+    batch, dim, seqlen = u.shape
+    _req(delta, "delta", in_dt)
+    _req(A, "A", torch.float32, 2)
+    dstate = A.shape[1]
+    _req(B, "B", in_dt, 4)
+    _req(C, "C", in_dt, 4)
+    ngroups = B.shape[1]
+    _req(dy, "dy", in_dt, 3)
+    _opt(D, "D", torch.float32)
+    _opt(z, "z", in_dt)
+    _opt(delta_bias, "delta_bias", torch.float32)
+    _opt(initial_state, "initial_state", torch.float32)
+    _opt(dfinal_state, "dfinal_state", torch.float32)
+    dev, f32 = u.device, torch.float32
+    g = {"du": torch.empty((batch, dim, seqlen), dtype=f32, device=dev),
+         "ddelta": torch.empty((batch, dim, seqlen), dtype=f32, device=dev),
+         "dA": torch.empty((dim, dstate), dtype=f32, device=dev),
+         "dB": torch.empty(tuple(B.shape), dtype=f32, device=dev),
+         "dC": torch.empty(tuple(C.shape), dtype=f32, device=dev),
+         "dD": None, "dz": None, "ddelta_bias": None, "dinitial_state": None}
+    if D is not None or want_dD:
+        g["dD"] = torch.empty(dim, dtype=f32, device=dev)
+    if delta_bias is not None or want_ddelta_bias:
+        g["ddelta_bias"] = torch.empty(dim, dtype=f32, device=dev)
+    if z is not None:
+        g["dz"] = torch.empty((batch, dim, seqlen), dtype=f32, device=dev)
+    if want_dinitial_state:
+        g["dinitial_state"] = torch.empty((batch, dim, dstate), dtype=f32, device=dev)
+    for k, t in (out or {}).items():
+        if k not in g or g[k] is None:
+            raise ValueError(f"out[{k!r}] is not an output of this call")
+        _req(t, f"out[{k!r}]", f32)
+        if t.shape != g[k].shape:
+            raise ValueError(f"out[{k!r}] must have shape {tuple(g[k].shape)}")
+        g[k] = t
+    need = ssm_scan_bwd_workspace_bytes(batch, dim, seqlen, dstate, ngroups)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _req(workspace, "workspace", torch.uint8)
+    st = lib().ssm_scan_bwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                            _ptr(delta_bias), int(bool(delta_softplus)), _ptr(initial_state),
+                            _ptr(dy), _ptr(dfinal_state), _ptr(g["du"]), _ptr(g["ddelta"]),
+                            _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]),
+                            _ptr(g["dz"]), _ptr(g["ddelta_bias"]), _ptr(g["dinitial_state"]),
+                            batch, dim, seqlen, dstate, ngroups, _DT[in_dt], _ptr(workspace),
+                            workspace.numel(), _stream(stream))
+    _check(st, "ssm_scan_bwd")
+    return g
 
 
 def ssm_scan_fwd_noalloc(u, delta, A, B, C, y, final_state=None, D=None, z=None,

@@ -67,6 +67,9 @@ struct ScanArgs {
     float* carry;     // [nchunks - 1][batch * dim][kN]
     const void* Bm;
     const void* Cm;
+    // optional: the state entering every 16-step segment, [seg][batch * dim][kN]
+    // (the backward pass recomputes from these); y may then be NULL
+    float* ckpt;
     int batch, dim, seqlen, ngroups;
     int dpg;          // channels per group
     int bpg;          // channel blocks per group
@@ -409,6 +412,12 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
         const uint8_t* tz = st + 2 * S::IN_TILE;
 #pragma unroll 2
         for (int j = 0; j < kTL / 8; ++j) {
+            if (a.ckpt && (j & 1) == 0 && valid && t0 + j * 8 < a.seqlen) {
+                const long long seg = (t0 + j * 8) / 16;
+                __stcg(reinterpret_cast<float4*>(
+                           a.ckpt + (seg * a.batch * a.dim + drow) * kN + n0),
+                       make_float4(h[0], h[1], h[2], h[3]));
+            }
             float yp[8];
 #pragma unroll
             for (int q = 0; q < 8; q += 2) {
@@ -467,7 +476,8 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
                 o0 *= silu_f(zz[0]);
                 o1 *= silu_f(zz[1]);
             }
-            if (valid && tg < t_end) store_y2<Tout>(yrow + tg, o0, o1, true, tg + 1 < t_end, vec_store);
+            if (a.y && valid && tg < t_end)
+                store_y2<Tout>(yrow + tg, o0, o1, true, tg + 1 < t_end, vec_store);
         }
 
         if constexpr (TMA) {
@@ -628,6 +638,35 @@ ssm_status_t dispatch(ScanArgs& a, ssm_dtype_t in_dtype, bool tma, cudaStream_t 
 }
 
 }  // namespace
+
+namespace ssm_internal {
+
+size_t scan_forward_workspace_bytes(int batch, int dim, int seqlen, int ngroups) {
+    return workspace_bound(batch, dim, seqlen, ngroups);
+}
+
+// The forward recurrence writing only the state entering every 16-step
+// segment (ckpt [ceil(seqlen/16)][batch * dim][16]); no y, no final state.
+// Arguments are validated by the caller; workspace holds
+// scan_forward_workspace_bytes.
+ssm_status_t scan_forward_checkpoints(const void* u, const void* delta, const float* A,
+                                      const void* B, const void* C, const float* delta_bias,
+                                      int delta_softplus, const float* h0, float* ckpt,
+                                      int batch, int dim, int seqlen, int ngroups,
+                                      ssm_dtype_t in_dtype, void* workspace,
+                                      cudaStream_t stream) {
+    ScanArgs a{};
+    a.u = u; a.delta = delta; a.z = nullptr; a.A = A; a.Dskip = nullptr; a.bias = delta_bias;
+    a.h0 = h0; a.y = nullptr; a.final_state = nullptr; a.Bm = B; a.Cm = C; a.ckpt = ckpt;
+    a.batch = batch; a.dim = dim; a.seqlen = seqlen; a.ngroups = ngroups;
+    a.dpg = dim / ngroups; a.softplus = delta_softplus ? 1 : 0;
+    const size_t es = in_dtype == SSM_BF16 ? 2 : 4;
+    const bool tma = ((size_t)seqlen * es) % 16 == 0;
+    if (in_dtype == SSM_BF16) return dispatch<__nv_bfloat16, float>(a, in_dtype, tma, stream, workspace);
+    return dispatch<float, float>(a, in_dtype, tma, stream, workspace);
+}
+
+}  // namespace ssm_internal
 
 extern "C" size_t ssm_scan_workspace_bytes(int batch, int dim, int seqlen, int dstate,
                                            int ngroups) {

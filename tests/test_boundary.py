@@ -241,3 +241,50 @@ def test_mimo_argument_errors(L):
     assert dec(lam=None) == NULL
     assert dec(y=P(1)) == ALIAS
     assert dec(batch=0) == OK
+
+
+def bwd_call(L, **kw):
+    args = dict(u=P(0), delta=P(1), A=P(2), B=P(3), C=P(4), D=None, z=None, bias=None,
+                softplus=1, h0=None, dy=P(5), dfs=None, du=P(6), ddelta=P(7), dA=P(8), dB=P(9),
+                dC=P(10), dD=None, dz=None, dbias=None, dh0=None, batch=2, dim=32, seqlen=64,
+                dstate=16, ngroups=1, in_dt=1, ws=P(11), wsb=1 << 30, stream=None)
+    args.update(kw)
+    a = args
+    return L.ssm_scan_bwd(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["bias"],
+                          a["softplus"], a["h0"], a["dy"], a["dfs"], a["du"], a["ddelta"],
+                          a["dA"], a["dB"], a["dC"], a["dD"], a["dz"], a["dbias"], a["dh0"],
+                          a["batch"], a["dim"], a["seqlen"], a["dstate"], a["ngroups"],
+                          a["in_dt"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_scan_bwd_argument_errors(L):
+    assert bwd_call(L, u=None) == NULL
+    assert bwd_call(L, dy=None) == NULL
+    assert bwd_call(L, du=None) == NULL
+    assert bwd_call(L, dB=None) == NULL
+    assert bwd_call(L, dA=None) == NULL
+    assert bwd_call(L, z=P(12), dz=None) == NULL      # dz required with a gate
+    assert bwd_call(L, batch=-1) == SHAPE
+    assert bwd_call(L, ngroups=3) == SHAPE
+    assert bwd_call(L, dstate=8) == UNSUP
+    assert bwd_call(L, in_dt=5) == DTYPE
+    assert bwd_call(L, dA=ctypes.c_void_p(0x90000004)) == ALIGN
+    assert bwd_call(L, ws=None) == WS
+    assert bwd_call(L, wsb=64) == WS
+    assert bwd_call(L, du=P(0)) == ALIAS              # du on top of u
+    assert bwd_call(L, dC=P(9)) == ALIAS              # two outputs on one buffer
+    assert bwd_call(L, dD=P(13), dbias=P(13)) == ALIAS
+    assert bwd_call(L, ws=P(5)) == ALIAS              # workspace on top of dy
+    assert bwd_call(L, ws=P(8)) == ALIAS              # workspace on top of dA
+    # no channels: nothing to write, nothing launched
+    assert bwd_call(L, dim=0, u=None, dA=None, du=None) == OK
+
+
+def test_scan_bwd_workspace_bytes():
+    f, fw = binding.ssm_scan_bwd_workspace_bytes, binding.ssm_scan_workspace_bytes
+    assert f(8, 1536, 2048) == f(8, 1536, 2048) > fw(8, 1536, 2048)
+    # checkpoints every 16 steps (64 bytes a channel) and the channel blocks' dB, dC partials
+    assert f(8, 1536, 2048) >= fw(8, 1536, 2048) + 128 * 8 * 1536 * 64 + 48 * 8 * 2048 * 128
+    assert f(1, 10, 5, dstate=8) == 0
+    assert f(1, 10, 5, ngroups=3) == 0
+    assert f(-1, 10, 5) == 0
