@@ -16,16 +16,18 @@
 //  1. the forward kernel re-runs and writes only the state entering every
 //     16-step segment (checkpoints);
 //  2. scan_bwd_kernel: a CTA owns one (batch, group, 32-channel block) and
-//     walks its 64-step tiles in reverse, with the forward kernel's lane map
-//     (4 lanes per channel, 4 states each).  Per tile it stages the per-step
-//     terms (dl, dl*u, dy0, u; softplus', dy silu') in shared memory once per
-//     (channel, step); per 16-step segment it recomputes the states from the
-//     checkpoint into registers, then runs the adjoint recurrence backwards.
-//     Sums over states (du, ddelta, the gate's y0) are reduce-scattered over
-//     the channel's 4 lanes; sums over channels (dB, dC) are reduce-scattered
-//     over a warp's 8 channels, then the 4 warps' sums are added in warp
-//     order into a per-tile shared buffer, which is written out as this
-//     channel block's partial;
+//     walks its 32-step tiles in reverse, with the forward kernel's lane map
+//     (4 lanes per channel, 4 states each).  While a tile is computed, the
+//     raw inputs of the tile before it (u, delta, dy, z, B, C and the two
+//     checkpoints) stream into shared memory with 16-byte cp.async copies.
+//     Per tile the per-step terms (dl, dl*u, dy0, u; softplus', dy silu')
+//     are formed once per (channel, step); per 16-step segment the states
+//     are recomputed from the checkpoint into registers, then the adjoint
+//     recurrence runs backwards.  Sums over states (du, ddelta, the gate's
+//     y0) are reduce-scattered over the channel's 4 lanes; sums over
+//     channels (dB, dC) are reduce-scattered over a warp's 8 channels, then
+//     the 4 warps' sums are added in warp order into a per-tile shared
+//     buffer, which is written out as this channel block's partial;
 //  3. scan_bwd_reduce_kernel adds the partials: dB, dC over channel blocks,
 //     dA, dD, dbias over the batch (a fixed order, so results are
 //     deterministic).
@@ -41,8 +43,9 @@ using namespace ssm;
 constexpr int kN = 16;        // dstate
 constexpr int kCH = 32;       // channels per CTA
 constexpr int kThreads = 128; // 4 lanes x 32 channels
-constexpr int kTL = 64;       // steps per tile
-constexpr int kSeg = 16;      // steps per recomputed segment
+constexpr int kTL = 32;       // steps per tile
+constexpr int kSeg = 16;      // steps per recomputed segment (one checkpoint)
+constexpr int kSegPerTile = kTL / kSeg;
 constexpr int kRecA = kTL * 16 + 16;  // bytes per channel row of recA (float4 per step, padded)
 constexpr int kRecB = kTL * 8 + 16;   // bytes per channel row of recB (float2 per step, padded)
 
@@ -69,70 +72,188 @@ struct BwdArgs {
     int batch, dim, seqlen, ngroups, dpg, bpg, softplus;
 };
 
-// smem layout (bytes from the base)
-constexpr int kOffRecA = 0;
-constexpr int kOffRecB = kOffRecA + kCH * kRecA;
-constexpr int kOffBC = kOffRecB + kCH * kRecB;    // fp32 B [t][16] then C [t][16]
-constexpr int kOffSum = kOffBC + 2 * kTL * kN * 4; // fp32 partial dB [t][16], dC [t][16]
-constexpr int kOffSeg = kOffSum + 2 * kTL * kN * 4; // per warp: dB, dC of one segment
-constexpr int kSmem = kOffSeg + 4 * 2 * kSeg * kN * 4;
-
+// Shared memory (bytes from the base).  The raw tile holds one tile's inputs
+// as they are in global memory: 4 activation arrays x 32 channel rows, B and
+// C x 16 state rows (each row kTL elements, padded by 16 bytes), then the
+// tile's two checkpoints [seg][channel][16] fp32.
 template <typename T>
-__device__ __forceinline__ float ld(const void* p, long long i) {
-    return to_f32(static_cast<const T*>(p)[i]);
-}
+struct Lay {
+    static constexpr int ES = sizeof(T);
+    static constexpr int ROW = kTL * ES + 16;
+    static constexpr int CHUNKS = kTL * ES / 16;  // 16-byte chunks per row
+    static constexpr int ACT = 4 * kCH * ROW;     // u, delta, dy, z
+    static constexpr int BCR = 2 * kN * ROW;      // B, C
+    static constexpr int CK = kSegPerTile * kCH * kN * 4;
+    static constexpr int RAW = ACT + BCR + CK;
+    static constexpr int OFF_RAW = 0;
+    static constexpr int OFF_RECA = OFF_RAW + RAW;
+    static constexpr int OFF_RECB = OFF_RECA + kCH * kRecA;
+    static constexpr int OFF_BC = OFF_RECB + kCH * kRecB;    // fp32 B [t][16] then C [t][16]
+    static constexpr int OFF_SUM = OFF_BC + 2 * kTL * kN * 4;  // fp32 dB [t][16], dC [t][16]
+    static constexpr int OFF_SEG = OFF_SUM + 2 * kTL * kN * 4; // per warp: one segment's dB, dC
+    static constexpr int OFF_CK = OFF_SEG + 4 * 2 * kSeg * kN * 4;  // the checkpoints, copied
+    static constexpr int SMEM = OFF_CK + CK;
+    static_assert(OFF_RECA % 16 == 0 && OFF_BC % 16 == 0 && ROW % 16 == 0, "16-byte alignment");
+};
 
 __device__ __forceinline__ float sigmoid_f(float x) {
     return rcp_approx(1.0f + ex2_approx(-x * kLog2e));
 }
 
-// Per-step terms of one tile, once per (channel, step): thread -> channel
-// tid % 32, steps 16 (tid / 32) .. + 15.  Steps past the sequence end get
-// dl = 0 and dy = 0: an identity step that contributes nothing.
-template <typename T>
-__device__ __forceinline__ void stage_tile(const BwdArgs& a, uint8_t* smem, long long row0,
-                                           int d0, int t0, int tn, int tid) {
-    const int pc = tid % kCH, pq = tid / kCH;
-    const bool pvalid = (d0 - (d0 / a.dpg) * a.dpg) + pc < a.dpg;
-    const long long io = (row0 + pc) * (long long)a.seqlen + t0;
-    const float bias = (a.bias && pvalid) ? a.bias[d0 + pc] : 0.0f;
-    float4* ra = reinterpret_cast<float4*>(smem + kOffRecA + pc * kRecA);
-    float2* rb = reinterpret_cast<float2*>(smem + kOffRecB + pc * kRecB);
-#pragma unroll 4
-    for (int q = 0; q < kSeg; ++q) {
-        const int t = pq * kSeg + q;
-        float dl = 0.f, u = 0.f, dy0 = 0.f, spd = 0.f, dygd = 0.f;
-        if (pvalid && t < tn) {
-            u = ld<T>(a.u, io + t);
-            const float x = ld<T>(a.delta, io + t) + bias;
-            dl = a.softplus ? softplus_f(x) : x;
-            spd = a.softplus ? sigmoid_f(x) : 1.0f;
-            const float dyv = ld<T>(a.dy, io + t);
-            if (a.z) {
-                const float zv = ld<T>(a.z, io + t);
-                const float sg = sigmoid_f(zv);
-                dy0 = dyv * zv * sg;
-                dygd = dyv * sg * fmaf(zv, 1.0f - sg, 1.0f);
+// 16-byte asynchronous global -> shared copy; src_bytes < 16 zero-fills the
+// rest (0: nothing is read).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)),
+                 "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+// Starts (VEC: cp.async) or performs (plain loads) the copy of tile `tile`'s
+// raw inputs into the raw area.  VEC requires rows of 16-byte multiples
+// (seqlen * sizeof(T) % 16 == 0); then a 16-byte chunk is either wholly
+// inside the sequence or wholly past it (zero-filled).  Channels past the
+// group's end read nothing and hold zeros.
+template <typename T, bool VEC>
+__device__ __forceinline__ void fetch_tile(const BwdArgs& a, uint8_t* smem, int tile,
+                                           long long row0, int cvalid, long long bcrow0,
+                                           int tid) {
+    using Y = Lay<T>;
+    uint8_t* raw = smem + Y::OFF_RAW;
+    const int t0 = tile * kTL;
+    const long long L = a.seqlen;
+    auto act = [&](int arr) -> const void* {
+        return arr == 0 ? a.u : arr == 1 ? a.delta : arr == 2 ? a.dy : a.z;
+    };
+    if constexpr (VEC) {
+        // activations and B, C: (4 * 32 + 2 * 16) rows x CHUNKS chunks
+        constexpr int NCH = (4 * kCH + 2 * kN) * Y::CHUNKS;
+        for (int i = tid; i < NCH; i += kThreads) {
+            const int r = i / Y::CHUNKS, c = i % Y::CHUNKS;
+            const int tc = t0 + c * (16 / Y::ES);  // first step of the chunk
+            const char* src;
+            bool ok;
+            if (r < 4 * kCH) {
+                const int arr = r / kCH, ch = r % kCH;
+                ok = ch < cvalid && tc < a.seqlen && act(arr) != nullptr;
+                src = static_cast<const char*>(ok ? act(arr) : a.u) +
+                      (ok ? ((row0 + ch) * L + tc) * Y::ES : 0);
             } else {
-                dy0 = dyv;
+                const int arr = (r - 4 * kCH) / kN, n = (r - 4 * kCH) % kN;
+                ok = tc < a.seqlen;
+                src = static_cast<const char*>(arr ? a.Cm : a.Bm) +
+                      (ok ? ((bcrow0 + n) * L + tc) * Y::ES : 0);
             }
+            cp_async16(raw + r * Y::ROW + c * 16, src, ok ? 16u : 0u);
         }
-        ra[t] = make_float4(dl, dl * u, dy0, u);
-        rb[t] = make_float2(spd, dygd);
+    } else {
+        for (int i = tid; i < (4 * kCH + 2 * kN) * kTL; i += kThreads) {
+            const int r = i / kTL, t = i % kTL;
+            const int tg = t0 + t;
+            T v = from_f32<T>(0.0f);
+            if (r < 4 * kCH) {
+                const int arr = r / kCH, ch = r % kCH;
+                if (ch < cvalid && tg < a.seqlen && act(arr) != nullptr)
+                    v = static_cast<const T*>(act(arr))[(row0 + ch) * L + tg];
+            } else {
+                const int arr = (r - 4 * kCH) / kN, n = (r - 4 * kCH) % kN;
+                if (tg < a.seqlen)
+                    v = static_cast<const T*>(arr ? a.Cm : a.Bm)[(bcrow0 + n) * L + tg];
+            }
+            reinterpret_cast<T*>(raw + r * Y::ROW)[t] = v;
+        }
+    }
+    // checkpoints of the tile's segments: [seg][channel][16] fp32, 4 chunks each
+    {
+        const long long BD = (long long)a.batch * a.dim;
+        const int nseg_total = (a.seqlen + kSeg - 1) / kSeg;
+        float* ck = reinterpret_cast<float*>(raw + Y::ACT + Y::BCR);
+        for (int i = tid; i < kSegPerTile * kCH * 4; i += kThreads) {
+            const int s = i / (kCH * 4), ch = (i / 4) % kCH, c = i % 4;
+            const long long seg = (long long)tile * kSegPerTile + s;
+            const bool ok = seg < nseg_total && ch < cvalid;
+            const float* src = a.ckpt + (ok ? (seg * BD + row0 + ch) * kN + c * 4 : 0);
+            cp_async16(ck + (s * kCH + ch) * kN + c * 4, src, ok ? 16u : 0u);
+        }
+    }
+    cp_async_commit();
+}
+
+// 8 consecutive elements of a raw row as fp32.
+template <typename T>
+__device__ __forceinline__ void load8(const uint8_t* p, float* v) {
+    if constexpr (sizeof(T) == 2) {
+        const uint4 w = *reinterpret_cast<const uint4*>(p);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = bf16lo(ws[i]);
+            v[2 * i + 1] = bf16hi(ws[i]);
+        }
+    } else {
+        const float4 a = *reinterpret_cast<const float4*>(p);
+        const float4 b = *reinterpret_cast<const float4*>(p + 16);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
     }
 }
 
-// B and C rows (b, g, n, t0 .. t0 + 63) as fp32 [t][n]; zero past the end.
+// Per-step terms of one tile from the raw area, once per (channel, step):
+// thread -> channel tid % 32, steps 8 (tid / 32) .. + 7.  Steps past the
+// sequence end (tn = the tile's steps) and channels past the group get
+// dl = 0 and dy = 0 (zero-filled): an identity step that contributes
+// nothing.  Also converts B, C to fp32 [t][n].
 template <typename T>
-__device__ __forceinline__ void stage_bc(const BwdArgs& a, uint8_t* smem, long long bcrow0,
-                                         int t0, int tn, int tid) {
-    float* bcf = reinterpret_cast<float*>(smem + kOffBC);
-    for (int i = tid; i < 2 * kN * kTL; i += kThreads) {
-        const int arr = i / (kN * kTL), rem = i % (kN * kTL);
-        const int n = rem / kTL, t = rem % kTL;
-        const void* src = arr ? a.Cm : a.Bm;
-        const float v = t < tn ? ld<T>(src, (bcrow0 + n) * a.seqlen + t0 + t) : 0.0f;
-        bcf[arr * kTL * kN + t * kN + n] = v;
+__device__ __forceinline__ void prep_tile(const BwdArgs& a, uint8_t* smem, float bias_p,
+                                          bool pvalid, int tn, bool has_z, int tid) {
+    using Y = Lay<T>;
+    const uint8_t* raw = smem + Y::OFF_RAW;
+    {
+        const int pc = tid % kCH, pq = tid / kCH;
+        float u[8], dl_[8], dy[8], zz[8];
+        const int off = pq * 8 * Y::ES;
+        load8<T>(raw + (0 * kCH + pc) * Y::ROW + off, u);
+        load8<T>(raw + (1 * kCH + pc) * Y::ROW + off, dl_);
+        load8<T>(raw + (2 * kCH + pc) * Y::ROW + off, dy);
+        if (has_z) load8<T>(raw + (3 * kCH + pc) * Y::ROW + off, zz);
+        float4* ra = reinterpret_cast<float4*>(smem + Y::OFF_RECA + pc * kRecA) + pq * 8;
+        float2* rb = reinterpret_cast<float2*>(smem + Y::OFF_RECB + pc * kRecB) + pq * 8;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float x = dl_[j] + bias_p;
+            const float dl = a.softplus ? softplus_f(x) : x;
+            const float spd = a.softplus ? sigmoid_f(x) : 1.0f;
+            float dy0 = dy[j], dygd = 0.0f;
+            if (has_z) {
+                const float sg = sigmoid_f(zz[j]);
+                dy0 = dy[j] * zz[j] * sg;
+                dygd = dy[j] * sg * fmaf(zz[j], 1.0f - sg, 1.0f);
+            }
+            // a step past the end must be the identity whatever the bias
+            const bool live = pvalid && pq * 8 + j < tn;
+            ra[j] = make_float4(live ? dl : 0.0f, live ? dl * u[j] : 0.0f, dy0, u[j]);
+            rb[j] = make_float2(spd, dygd);
+        }
+    }
+    {
+        const int arr = tid / 64, n = (tid / 4) % kN, q = tid % 4;
+        float v[8];
+        load8<T>(raw + (4 * kCH + arr * kN + n) * Y::ROW + q * 8 * Y::ES, v);
+        float* bcf = reinterpret_cast<float*>(smem + Y::OFF_BC) + arr * kTL * kN;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) bcf[(q * 8 + j) * kN + n] = v[j];
+    }
+    // the checkpoints leave the raw area, which the next tile's copies reuse
+    {
+        const float4* src = reinterpret_cast<const float4*>(raw + Y::ACT + Y::BCR);
+        float4* dst = reinterpret_cast<float4*>(smem + Y::OFF_CK);
+#pragma unroll
+        for (int i = tid; i < Y::CK / 16; i += kThreads) dst[i] = src[i];
     }
 }
 
@@ -159,21 +280,23 @@ __device__ __forceinline__ float reduce_scatter8_channels(const float* v, int la
     return keep + __shfl_xor_sync(0xffffffffu, send, 4);
 }
 
-template <typename T>
+template <typename T, bool VEC, bool Z>
 __global__ void __launch_bounds__(kThreads, 3) scan_bwd_kernel(const BwdArgs a) {
+    using Y = Lay<T>;
     extern __shared__ __align__(16) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cb = blockIdx.x % a.bpg, bg = blockIdx.x / a.bpg;
     const int g = bg % a.ngroups, b = bg / a.ngroups;
     const int d0 = g * a.dpg + cb * kCH;
+    const int cvalid = min(kCH, a.dpg - cb * kCH);  // channels of this block in the group
     const long long row0 = (long long)b * a.dim + d0;
     const long long bcrow0 = (long long)bg * kN;
     const int cl = warp * 8 + (lane >> 2), ng = lane & 3, n0 = ng * 4;
     const int d = d0 + cl;
-    const bool valid = cb * kCH + cl < a.dpg;
+    const bool valid = cl < cvalid;
     const long long drow = row0 + cl;
-    const long long BD = (long long)a.batch * a.dim;
     const long long L = a.seqlen;
+    const float bias_p = (a.bias && tid % kCH < cvalid) ? a.bias[d0 + tid % kCH] : 0.0f;
 
     float A2[4], An[4], lam[4], dA[4];
 #pragma unroll
@@ -185,31 +308,29 @@ __global__ void __launch_bounds__(kThreads, 3) scan_bwd_kernel(const BwdArgs a) 
     }
     const float Dd = (a.Dskip && valid) ? a.Dskip[d] : 0.0f;
     float accD = 0.0f, accBias = 0.0f;
-    const float4* recA = reinterpret_cast<const float4*>(smem + kOffRecA + cl * kRecA);
-    const float2* recB = reinterpret_cast<const float2*>(smem + kOffRecB + cl * kRecB);
-    const float* Bt = reinterpret_cast<const float*>(smem + kOffBC);
+    const float4* recA = reinterpret_cast<const float4*>(smem + Y::OFF_RECA + cl * kRecA);
+    const float2* recB = reinterpret_cast<const float2*>(smem + Y::OFF_RECB + cl * kRecB);
+    const float* Bt = reinterpret_cast<const float*>(smem + Y::OFF_BC);
     const float* Ct = Bt + kTL * kN;
-    float* sum = reinterpret_cast<float*>(smem + kOffSum);  // [2][kTL][kN]
-    float* segw = reinterpret_cast<float*>(smem + kOffSeg);  // [warp][2][kSeg][kN]
+    float* sum = reinterpret_cast<float*>(smem + Y::OFF_SUM);  // [2][kTL][kN]
+    float* segw = reinterpret_cast<float*>(smem + Y::OFF_SEG);  // [warp][2][kSeg][kN]
+    const float* ckp = reinterpret_cast<const float*>(smem + Y::OFF_CK);  // [seg][ch][16]
     const int ntiles = (a.seqlen + kTL - 1) / kTL;
-    const bool has_z = a.z != nullptr;
 
+    fetch_tile<T, VEC>(a, smem, ntiles - 1, row0, cvalid, bcrow0, tid);
     for (int tile = ntiles - 1; tile >= 0; --tile) {
         const int t0 = tile * kTL, tn = min(kTL, a.seqlen - t0);
-        stage_tile<T>(a, smem, row0, d0, t0, tn, tid);
-        stage_bc<T>(a, smem, bcrow0, t0, tn, tid);
-        __syncthreads();
+        cp_async_wait_all();
+        __syncthreads();  // every thread's copies of this tile have landed
+        prep_tile<T>(a, smem, bias_p, tid % kCH < cvalid, tn, Z, tid);
+        __syncthreads();  // per-step terms ready; the raw area is free
+        if (tile > 0) fetch_tile<T, VEC>(a, smem, tile - 1, row0, cvalid, bcrow0, tid);
         const int nseg = (tn + kSeg - 1) / kSeg;
 #pragma unroll 1
         for (int s = nseg - 1; s >= 0; --s) {
             const int ts0 = s * kSeg;
-            const long long seg = (t0 + ts0) / kSeg;
-            float hs[4] = {0.f, 0.f, 0.f, 0.f};
-            if (valid) {
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(
-                    a.ckpt + (seg * BD + drow) * kN + n0));
-                hs[0] = v.x; hs[1] = v.y; hs[2] = v.z; hs[3] = v.w;
-            }
+            const float4 hv = *reinterpret_cast<const float4*>(ckp + (s * kCH + cl) * kN + n0);
+            const float hs[4] = {hv.x, hv.y, hv.z, hv.w};
             // ---- recompute the segment's states from its checkpoint
             float H[kSeg][4], ys[kSeg];
             {
@@ -219,20 +340,22 @@ __global__ void __launch_bounds__(kThreads, 3) scan_bwd_kernel(const BwdArgs a) 
                     const int t = ts0 + i;
                     const float4 ra = recA[t];
                     const float4 bq = *reinterpret_cast<const float4*>(Bt + t * kN + n0);
-                    const float4 cq = *reinterpret_cast<const float4*>(Ct + t * kN + n0);
                     h[0] = fmaf(ex2_approx(ra.x * A2[0]), h[0], ra.y * bq.x);
                     h[1] = fmaf(ex2_approx(ra.x * A2[1]), h[1], ra.y * bq.y);
                     h[2] = fmaf(ex2_approx(ra.x * A2[2]), h[2], ra.y * bq.z);
                     h[3] = fmaf(ex2_approx(ra.x * A2[3]), h[3], ra.y * bq.w);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) H[i][k] = h[k];
-                    ys[i] = fmaf(cq.w, h[3], fmaf(cq.z, h[2], fmaf(cq.y, h[1], cq.x * h[0])));
+                    if constexpr (Z) {
+                        const float4 cq = *reinterpret_cast<const float4*>(Ct + t * kN + n0);
+                        ys[i] = fmaf(cq.w, h[3], fmaf(cq.z, h[2], fmaf(cq.y, h[1], cq.x * h[0])));
+                    }
                 }
             }
             // ---- the gate's derivative needs y0 = sum_n C h + D u: reduce-scatter
             // the 16 steps' partial sums over the channel's 4 lanes (lane ng ends
             // with steps 4 ng .. 4 ng + 3)
-            if (has_z) {
+            if constexpr (Z) {
                 const bool b1 = lane & 2, b0 = lane & 1;
                 float w8[8], w4[4];
 #pragma unroll
@@ -272,8 +395,8 @@ __global__ void __launch_bounds__(kThreads, 3) scan_bwd_kernel(const BwdArgs a) 
                     const float av = ex2_approx(ra.x * A2[k]);
                     const float hp = i > 0 ? H[i - 1][k] : hs[k];
                     lam[k] = fmaf(ra.z, cc[k], lam[k]);
-                    v[4 + k] = ra.z * H[i][k];       // dC
-                    v[k] = lam[k] * ra.y;            // dB
+                    v[4 + k] = ra.z * H[i][k];  // dC
+                    v[k] = lam[k] * ra.y;       // dB
                     const float t1 = lam[k] * hp * av;
                     dA[k] = fmaf(t1, ra.x, dA[k]);
                     const float lb = lam[k] * bb[k];
@@ -345,7 +468,6 @@ __global__ void __launch_bounds__(kThreads, 3) scan_bwd_kernel(const BwdArgs a) 
                         sum[(rest >> 4) * kTL * kN + tn_i * kN + (rest & 15)];
             }
         }
-        __syncthreads();
     }
 
     // ---- per-channel sums: dA (this batch row), dD, dbias, and dh0
@@ -403,6 +525,23 @@ __global__ void scan_bwd_reduce_kernel(const float* __restrict__ pBC, const floa
             out[dd] = s;
         }
     }
+}
+
+template <typename T, bool VEC, bool Z>
+ssm_status_t launch_bwd_one(const BwdArgs& a, unsigned grid, cudaStream_t s) {
+    auto kern = scan_bwd_kernel<T, VEC, Z>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<T>::SMEM) !=
+        cudaSuccess)
+        return SSM_ERR_CUDA;
+    kern<<<grid, kThreads, Lay<T>::SMEM, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+template <typename T>
+ssm_status_t launch_bwd(const BwdArgs& a, bool vec, bool z, unsigned grid, cudaStream_t s) {
+    if (vec) return z ? launch_bwd_one<T, true, true>(a, grid, s)
+                      : launch_bwd_one<T, true, false>(a, grid, s);
+    return z ? launch_bwd_one<T, false, true>(a, grid, s) : launch_bwd_one<T, false, false>(a, grid, s);
 }
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -531,14 +670,13 @@ extern "C" ssm_status_t ssm_scan_bwd(
     if (rc != SSM_OK) return rc;
 
     // 2. the adjoint sweep, one CTA per (batch, group, channel block)
-    auto kern = in_dtype == SSM_BF16 ? scan_bwd_kernel<__nv_bfloat16> : scan_bwd_kernel<float>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
-        cudaSuccess)
-        return SSM_ERR_CUDA;
     const long long grid = (long long)batch * ngroups * a.bpg;
     if (grid > INT32_MAX) return SSM_ERR_UNSUPPORTED;
-    kern<<<(unsigned)grid, kThreads, kSmem, s>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
+    // 16-byte copies need rows of whole 16-byte chunks (bases are checked above)
+    const bool vec = ((size_t)seqlen * es) % 16 == 0;
+    rc = in_dtype == SSM_BF16 ? launch_bwd<__nv_bfloat16>(a, vec, z != nullptr, (unsigned)grid, s)
+                              : launch_bwd<float>(a, vec, z != nullptr, (unsigned)grid, s);
+    if (rc != SSM_OK) return rc;
 
     // 3. sums of the partials
     int dev = 0, sms = 1;
