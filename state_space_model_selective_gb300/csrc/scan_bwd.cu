@@ -48,6 +48,8 @@ constexpr int kSeg = 16;      // steps per recomputed segment (one checkpoint)
 constexpr int kSegPerTile = kTL / kSeg;
 constexpr int kRecA = kTL * 16 + 16;  // bytes per channel row of recA (float4 per step, padded)
 constexpr int kRecB = kTL * 8 + 16;   // bytes per channel row of recB (float2 per step, padded)
+constexpr int kSumT = kN + 1;          // floats per step row of the tile's dB, dC sums (padded)
+constexpr int kSegT = kSeg * kN + 16;  // floats per (warp, dB or dC) block of a segment (padded)
 
 struct BwdArgs {
     const void* u;
@@ -89,9 +91,9 @@ struct Lay {
     static constexpr int OFF_RECA = OFF_RAW + RAW;
     static constexpr int OFF_RECB = OFF_RECA + kCH * kRecA;
     static constexpr int OFF_BC = OFF_RECB + kCH * kRecB;    // fp32 B [t][16] then C [t][16]
-    static constexpr int OFF_SUM = OFF_BC + 2 * kTL * kN * 4;  // fp32 dB [t][16], dC [t][16]
-    static constexpr int OFF_SEG = OFF_SUM + 2 * kTL * kN * 4; // per warp: one segment's dB, dC
-    static constexpr int OFF_CK = OFF_SEG + 4 * 2 * kSeg * kN * 4;  // the checkpoints, copied
+    static constexpr int OFF_SUM = OFF_BC + 2 * kTL * kN * 4;     // fp32 dB, dC [type][t][kSumT]
+    static constexpr int OFF_SEG = OFF_SUM + 2 * kTL * kSumT * 4; // per warp: a segment's dB, dC
+    static constexpr int OFF_CK = OFF_SEG + 4 * 2 * kSegT * 4;     // the checkpoints, copied
     static constexpr int SMEM = OFF_CK + CK;
     static_assert(OFF_RECA % 16 == 0 && OFF_BC % 16 == 0 && ROW % 16 == 0, "16-byte alignment");
 };
@@ -241,12 +243,15 @@ __device__ __forceinline__ void prep_tile(const BwdArgs& a, uint8_t* smem, float
         }
     }
     {
-        const int arr = tid / 64, n = (tid / 4) % kN, q = tid % 4;
+        // a warp holds 16 states x one even and one odd q; odd q store their
+        // steps pairwise swapped, so the two halves hit different banks
+        const int arr = tid / 64, n = tid % kN, q = (tid / kN) % 4;
         float v[8];
         load8<T>(raw + (4 * kCH + arr * kN + n) * Y::ROW + q * 8 * Y::ES, v);
         float* bcf = reinterpret_cast<float*>(smem + Y::OFF_BC) + arr * kTL * kN;
+        const bool odd = q & 1;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) bcf[(q * 8 + j) * kN + n] = v[j];
+        for (int j = 0; j < 8; ++j) bcf[(q * 8 + (j ^ (int)odd)) * kN + n] = odd ? v[j ^ 1] : v[j];
     }
     // the checkpoints leave the raw area, which the next tile's copies reuse
     {
@@ -312,8 +317,8 @@ __global__ void __launch_bounds__(kThreads, 3) scan_bwd_kernel(const BwdArgs a) 
     const float2* recB = reinterpret_cast<const float2*>(smem + Y::OFF_RECB + cl * kRecB);
     const float* Bt = reinterpret_cast<const float*>(smem + Y::OFF_BC);
     const float* Ct = Bt + kTL * kN;
-    float* sum = reinterpret_cast<float*>(smem + Y::OFF_SUM);  // [2][kTL][kN]
-    float* segw = reinterpret_cast<float*>(smem + Y::OFF_SEG);  // [warp][2][kSeg][kN]
+    float* sum = reinterpret_cast<float*>(smem + Y::OFF_SUM);  // [2][kTL][kSumT]
+    float* segw = reinterpret_cast<float*>(smem + Y::OFF_SEG);  // [warp][2][kSegT]
     const float* ckp = reinterpret_cast<const float*>(smem + Y::OFF_CK);  // [seg][ch][16]
     const int ntiles = (a.seqlen + kTL - 1) / kTL;
 
@@ -410,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 3) scan_bwd_kernel(const BwdArgs a) 
                 {
                     const float r = reduce_scatter8_channels(v, lane);
                     const int type = (lane >> 4) & 1, kk = (lane >> 2) & 3;
-                    segw[((warp * 2 + type) * kSeg + i) * kN + n0 + kk] = r;
+                    segw[(warp * 2 + type) * kSegT + i * kN + n0 + kk] = r;
                 }
                 if ((i & 3) == 0) {
                     // (du, d dl) of steps i .. i + 3 over the channel's 4 lanes:
@@ -450,10 +455,10 @@ __global__ void __launch_bounds__(kThreads, 3) scan_bwd_kernel(const BwdArgs a) 
             __syncthreads();
             for (int e = tid; e < 2 * kSeg * kN; e += kThreads) {
                 const int type = e / (kSeg * kN), rem = e % (kSeg * kN);  // rem = i * 16 + n
-                float acc = segw[(0 * 2 + type) * kSeg * kN + rem];
+                float acc = segw[(0 * 2 + type) * kSegT + rem];
 #pragma unroll
-                for (int w = 1; w < 4; ++w) acc += segw[(w * 2 + type) * kSeg * kN + rem];
-                sum[type * kTL * kN + ts0 * kN + rem] = acc;
+                for (int w = 1; w < 4; ++w) acc += segw[(w * 2 + type) * kSegT + rem];
+                sum[(type * kTL + ts0 + rem / kN) * kSumT + rem % kN] = acc;
             }
             __syncthreads();
         }
@@ -465,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 3) scan_bwd_kernel(const BwdArgs a) 
                 const int tn_i = i % kTL, rest = i / kTL;  // rest = type * 16 + n
                 if (tn_i < tn)
                     a.pBC[base + rest * L + t0 + tn_i] =
-                        sum[(rest >> 4) * kTL * kN + tn_i * kN + (rest & 15)];
+                        sum[((rest >> 4) * kTL + tn_i) * kSumT + (rest & 15)];
             }
         }
     }
