@@ -43,6 +43,15 @@ WORKLOAD = ("selective scan, bf16 inputs / fp32 state / fp32 y, batch 8, L 2048,
 SMS, MUFU_PER_CLK, SM_MAX_MHZ = 152, 32, 2070.0
 HBM_PEAK_GBS = 6778.0  # measured copy bandwidth of the GB300s
 MUFU_PEAK_GOPS = SMS * MUFU_PER_CLK * SM_MAX_MHZ * 1e6 / 1e9
+# FP32 pipe: 128 lane-operations per SM per clock (FFMA rate measured by
+# state_space_model_selective_gb300.peaks: 123 per SM per clock).
+FP32_PER_CLK = 128
+FP32_PEAK_GOPS = SMS * FP32_PER_CLK * SM_MAX_MHZ * 1e6 / 1e9
+# The scan gradient's arithmetic per element (b, l, d, n), counted on the FP32
+# pipe with no recomputation: the state h_t (dl*u*B, one FMA), the adjoint
+# (lambda += dy0 C, lambda *= a, and dl*A for a), dC (dy0 h), dB (lambda dl u),
+# dA (lambda h_{t-1} a, times dl), d dl (two FMAs), du (one FMA): 12 ops.
+SCAN_BWD_FP32_PER_ELEMENT = 12
 # DRAM bytes per launch of the scan kernel from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum = 152.2 MB + 64.7 MB) of this
 # kernel build on this workload; set to None whenever the kernel changes.
@@ -351,6 +360,7 @@ def measure_other_paths(dev, reps=20):
                      "frac": nbytes / (ms / 1e3) / 1e9 / HBM_PEAK_GBS,
                      "algorithmic_bytes": nbytes}}
     del inp
+    res["ssm_scan_bwd"] = _measure_scan_bwd(dev, reps)
     m3 = inputs.mamba3_inputs(32, 256, 32, 64, 128, 1, "bf16", seed=1006, device="cuda")
 
     def ssd_m3():
@@ -446,6 +456,42 @@ def measure_other_paths(dev, reps=20):
                      "frac": nbytes3 / (ms / 1e3) / 1e9 / HBM_PEAK_GBS,
                      "algorithmic_bytes": nbytes3}}
     return res
+
+
+def _measure_scan_bwd(dev, reps):
+    """The scan gradient (ssm_scan_bwd: checkpointing forward, reverse sweep,
+    reductions) on the benchmark workload (bf16, batch 8, L 2048, 1536
+    channels, d_state 16, D, gate, bias, softplus), against the FP32 pipe."""
+    import torch
+    from state_space_model_selective_gb300 import binding, inputs
+    inp = inputs.scan_inputs(BATCH, DIM, SEQLEN, DSTATE, 1, "bf16", seed=1002, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1008)
+    dy = torch.randn(BATCH, DIM, SEQLEN, device=dev, generator=g).to(torch.bfloat16)
+    f = dict(dtype=torch.float32, device=dev)
+    act = (BATCH, DIM, SEQLEN)
+    out = {"du": torch.empty(act, **f), "ddelta": torch.empty(act, **f),
+           "dz": torch.empty(act, **f), "dA": torch.empty(DIM, DSTATE, **f),
+           "dB": torch.empty(BATCH, 1, DSTATE, SEQLEN, **f),
+           "dC": torch.empty(BATCH, 1, DSTATE, SEQLEN, **f), "dD": torch.empty(DIM, **f),
+           "ddelta_bias": torch.empty(DIM, **f),
+           "dinitial_state": torch.empty(BATCH, DIM, DSTATE, **f)}
+    ws = torch.empty(binding.ssm_scan_bwd_workspace_bytes(BATCH, DIM, SEQLEN, DSTATE, 1),
+                     dtype=torch.uint8, device=dev)
+
+    def bwd():
+        binding.ssm_scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], dy, inp["D"],
+                             inp["z"], inp["delta_bias"], True, workspace=ws, out=out)
+    ms = _time(bwd, reps)
+    el = BATCH * SEQLEN * DIM * DSTATE
+    ops = SCAN_BWD_FP32_PER_ELEMENT * el
+    achieved = ops / (ms / 1e3) / 1e9
+    return {"workload": "selective-scan gradient bf16 in / fp32 gradients, batch 8, L 2048, "
+                        "1536 channels, d_state 16, D, gate, bias, softplus",
+            "ms": ms, "elements_per_s": el / (ms / 1e3),
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_GOPS,
+                         "unit": "Gop/s (FP32 pipe)", "frac": achieved / FP32_PEAK_GOPS,
+                         "algorithmic_fp32_ops": ops}}
 
 
 def _time(fn, reps):

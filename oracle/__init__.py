@@ -65,6 +65,7 @@ def _load():
             lib.oracle_mamba3_mimo_chunked.argtypes = [dp] * 11 + [i] * 8
             lib.oracle_mamba3_mimo_decode_step.argtypes = [dp] * 12 + [i] * 6
             lib.oracle_scan_bwd.argtypes = [dp] * 8 + [i] + [dp] * 12 + [i] * 5
+            lib.oracle_ssd_bwd.argtypes = [dp] * 14 + [i] * 6
             lib.oracle_combine.argtypes = [ctypes.c_double] * 4 + [dp, dp]
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -188,6 +189,26 @@ def ssd_recurrence(x, dt, A_head, B, C, h0=None):
     hs = np.empty((batch, nheads, headdim, dstate), np.float64)
     _load().oracle_ssd_recurrence(*[_ptr(a) for a in arrs], _ptr(y), _ptr(hs), *dims)
     return y, hs
+
+
+def ssd_bwd(x, dt, A_head, B, C, dy, h0=None, dfinal=None):
+    """Gradient of ``ssd_recurrence`` for the loss sum(dy * y) + sum(dfinal * final_state).
+
+    Returns a dict of float64 arrays: dx (B, L, H, P), ddt (B, L, H), dA (H,),
+    dB, dC (B, L, G, N), dh0 (B, H, P, N)."""
+    arrs, dims = _ssd_args(x, dt, A_head, B, C, h0)
+    batch, seqlen, nheads, headdim, dstate, ngroups = dims
+    dy, dfinal = _f64(dy), _f64(dfinal)
+    assert dy.shape == (batch, seqlen, nheads, headdim)
+    assert dfinal is None or dfinal.shape == (batch, nheads, headdim, dstate)
+    g = {"dx": np.empty((batch, seqlen, nheads, headdim)), "ddt": np.empty((batch, seqlen, nheads)),
+         "dA": np.empty(nheads), "dB": np.empty((batch, seqlen, ngroups, dstate)),
+         "dC": np.empty((batch, seqlen, ngroups, dstate)),
+         "dh0": np.empty((batch, nheads, headdim, dstate))}
+    _load().oracle_ssd_bwd(*[_ptr(a) for a in arrs], _ptr(dy), _ptr(dfinal), _ptr(g["dx"]),
+                           _ptr(g["ddt"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
+                           _ptr(g["dh0"]), *dims)
+    return g
 
 
 def ssd_chunked(x, dt, A_head, B, C, chunk, h0=None):

@@ -953,6 +953,84 @@ void oracle_scan_bwd(const double* u, const double* delta, const double* A,
     free(lam);
 }
 
+/*
+ * Gradient of oracle_ssd_recurrence for the loss  sum dy . y + sum dfinal .
+ * final_state (dfinal may be NULL), by differentiating the recurrence in
+ * reverse, with Lambda_t = dL/dS_t (a headdim x dstate matrix per head):
+ *   Lambda_t = dy_t (outer) C_t + a_{t+1} Lambda_{t+1}
+ *   dC_t[n] += sum_p dy_t[p] S_t[p,n];   dB_t[n] += dt_t sum_p Lambda_t[p,n] x_t[p]
+ *   dx_t[p]  = dt_t sum_n Lambda_t[p,n] B_t[n]
+ *   ddt_t   += sum_{p,n} Lambda_t[p,n] (A_h a_t S_{t-1}[p,n] + B_t[n] x_t[p])
+ *   dA_h    += sum_{t,p,n} Lambda_t[p,n] dt_t a_t S_{t-1}[p,n];   dh0 = a_0 Lambda_0
+ * Serial over rows (dB, dC, ddt, dA are sums over several rows), for small
+ * problems.  Arguments as oracle_ssd_recurrence plus dy (like x) and dfinal
+ * (like h0) in; out: dx (like x), ddt (like dt), dA (nheads), dB, dC (like
+ * Bm) and dh0 (like h0, may be NULL).
+ */
+void oracle_ssd_bwd(const double* x, const double* dt, const double* A_head,
+                    const double* Bm, const double* Cm, const double* h0,
+                    const double* dy, const double* dfinal,
+                    double* dx, double* ddt, double* dA, double* dB, double* dC, double* dh0,
+                    int batch, int seqlen, int nheads, int headdim, int dstate, int ngroups)
+{
+    const int heads_per_group = nheads / ngroups;
+    const size_t nbc = (size_t)batch * seqlen * ngroups * dstate;
+    memset(ddt, 0, sizeof(double) * (size_t)batch * seqlen * nheads);
+    memset(dA, 0, sizeof(double) * (size_t)nheads);
+    memset(dB, 0, sizeof(double) * nbc);
+    memset(dC, 0, sizeof(double) * nbc);
+    /* Sx[t * dstate + n] is the state entering step t; Sx[(t + 1) * dstate + n] after it */
+    double* Sx = (double*)malloc(sizeof(double) * (size_t)(seqlen + 1) * dstate);
+    double* adj = (double*)malloc(sizeof(double) * (size_t)dstate);
+    const long long rows = (long long)batch * nheads * headdim;
+    for (long long row = 0; row < rows; ++row) {
+        const int p = (int)(row % headdim);
+        const int h = (int)((row / headdim) % nheads);
+        const int b = (int)(row / ((long long)headdim * nheads));
+        const int g = h / heads_per_group;
+        for (int n = 0; n < dstate; ++n) Sx[n] = h0 ? h0[row * dstate + n] : 0.0;
+        for (int t = 0; t < seqlen; ++t) {
+            const size_t bt = (size_t)b * seqlen + t;
+            const double step_dt = dt[bt * nheads + h];
+            const double decay = exp(A_head[h] * step_dt);
+            const double xin = x[(bt * nheads + h) * headdim + p];
+            const double* Bt = Bm + (bt * ngroups + g) * dstate;
+            for (int n = 0; n < dstate; ++n)
+                Sx[(size_t)(t + 1) * dstate + n] =
+                    decay * Sx[(size_t)t * dstate + n] + step_dt * xin * Bt[n];
+        }
+        for (int n = 0; n < dstate; ++n) adj[n] = dfinal ? dfinal[row * dstate + n] : 0.0;
+        for (int t = seqlen - 1; t >= 0; --t) {
+            const size_t bt = (size_t)b * seqlen + t;
+            const size_t ix = (bt * nheads + h) * headdim + p;
+            const double step_dt = dt[bt * nheads + h];
+            const double decay = exp(A_head[h] * step_dt);
+            const double xin = x[ix], dyv = dy[ix];
+            const double* Bt = Bm + (bt * ngroups + g) * dstate;
+            const double* Ct = Cm + (bt * ngroups + g) * dstate;
+            double* dBt = dB + (bt * ngroups + g) * dstate;
+            double* dCt = dC + (bt * ngroups + g) * dstate;
+            double sum_b = 0.0, sum_dt = 0.0;
+            for (int n = 0; n < dstate; ++n) {
+                const double s_prev = Sx[(size_t)t * dstate + n];
+                adj[n] += dyv * Ct[n];
+                dCt[n] += dyv * Sx[(size_t)(t + 1) * dstate + n];
+                dBt[n] += adj[n] * step_dt * xin;
+                sum_b += adj[n] * Bt[n];
+                sum_dt += adj[n] * (A_head[h] * decay * s_prev + Bt[n] * xin);
+                dA[h] += adj[n] * step_dt * decay * s_prev;
+                adj[n] *= decay;
+            }
+            dx[ix] = step_dt * sum_b;
+            ddt[bt * nheads + h] += sum_dt;
+        }
+        if (dh0)
+            for (int n = 0; n < dstate; ++n) dh0[row * dstate + n] = adj[n];
+    }
+    free(Sx);
+    free(adj);
+}
+
 int oracle_num_threads(void)
 {
     int n = 1;

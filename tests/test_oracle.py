@@ -702,3 +702,90 @@ def test_scan_bwd_is_linear_in_dy():
     g3 = oracle.scan_bwd(*args, dy + 2 * dy2, **kw)
     for k in ("du", "dB", "dC", "dD", "dh0"):
         np.testing.assert_allclose(g3[k], g1[k] + 2 * g2[k], rtol=1e-11, atol=1e-12, err_msg=k)
+
+
+# ------------------------------------------------------- SSD backward pins
+
+def _ssd_bwd_case(seed, ngroups, use_h0):
+    rng = _rng(seed)
+    batch, seqlen, nheads, headdim, dstate = 2, 5, 4, 3, 4
+    c = dict(x=rng.standard_normal((batch, seqlen, nheads, headdim)),
+             dt=rng.uniform(0.05, 0.6, (batch, seqlen, nheads)),
+             A_head=-rng.uniform(0.5, 2.0, nheads),
+             B=rng.standard_normal((batch, seqlen, ngroups, dstate)),
+             C=rng.standard_normal((batch, seqlen, ngroups, dstate)),
+             h0=rng.standard_normal((batch, nheads, headdim, dstate)) if use_h0 else None)
+    dy = rng.standard_normal((batch, seqlen, nheads, headdim))
+    dfinal = rng.standard_normal((batch, nheads, headdim, dstate))
+    return c, dy, dfinal
+
+
+def _ssd_loss(c, dy, dfinal):
+    y, hs = oracle.ssd_recurrence(c["x"], c["dt"], c["A_head"], c["B"], c["C"], c["h0"])
+    return float(np.sum(dy * y) + np.sum(dfinal * hs))
+
+
+@pytest.mark.parametrize("ngroups,use_h0", [(1, True), (2, False), (4, True)])
+def test_ssd_bwd_equals_finite_differences(ngroups, use_h0):
+    """Every entry of the SSD gradient against a central difference of the
+    forward recurrence oracle's loss sum(dy y) + sum(dfinal final_state)."""
+    c, dy, dfinal = _ssd_bwd_case(301 + ngroups, ngroups, use_h0)
+    g = oracle.ssd_bwd(c["x"], c["dt"], c["A_head"], c["B"], c["C"], dy, c["h0"], dfinal)
+    names = {"x": "dx", "dt": "ddt", "A_head": "dA", "B": "dB", "C": "dC", "h0": "dh0"}
+    eps = 1e-6
+    for k, gk in names.items():
+        if c[k] is None:
+            continue
+        fd = np.zeros_like(c[k])
+        for idx in np.ndindex(c[k].shape):
+            cp = {kk: (None if vv is None else vv.copy()) for kk, vv in c.items()}
+            cp[k][idx] += eps
+            lp = _ssd_loss(cp, dy, dfinal)
+            cp[k][idx] -= 2 * eps
+            lm = _ssd_loss(cp, dy, dfinal)
+            fd[idx] = (lp - lm) / (2 * eps)
+        np.testing.assert_allclose(g[gk], fd, rtol=1e-6, atol=1e-7, err_msg=k)
+
+
+def test_ssd_bwd_is_the_scan_gradient_with_head_constant_A():
+    """The SSD is the selective scan with channels (h, p), A constant over a
+    head's channels and states, delta = dt without softplus or bias.  Its
+    gradient is then the scan gradient with the layouts exchanged, dt's
+    gradient summed over p and A's over (p, n): checked against the scan
+    gradient oracle (itself pinned by finite differences)."""
+    c, dy, dfinal = _ssd_bwd_case(331, 2, True)
+    x, dt, Ah, B, C, h0 = c["x"], c["dt"], c["A_head"], c["B"], c["C"], c["h0"]
+    batch, seqlen, nheads, headdim = x.shape
+    dstate = B.shape[3]
+    u = x.transpose(0, 2, 3, 1).reshape(batch, nheads * headdim, seqlen)
+    delta = np.repeat(dt.transpose(0, 2, 1), headdim, axis=1)
+    A = np.repeat(Ah, headdim)[:, None] * np.ones((1, dstate))
+    Bs, Cs = B.transpose(0, 2, 3, 1), C.transpose(0, 2, 3, 1)
+    dys = dy.transpose(0, 2, 3, 1).reshape(batch, nheads * headdim, seqlen)
+    gs = oracle.scan_bwd(u, delta, A, Bs, Cs, dys, None, None, None, False,
+                         h0.reshape(batch, nheads * headdim, dstate),
+                         dfinal.reshape(batch, nheads * headdim, dstate))
+    g = oracle.ssd_bwd(x, dt, Ah, B, C, dy, h0, dfinal)
+    tol = dict(rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(
+        g["dx"], gs["du"].reshape(batch, nheads, headdim, seqlen).transpose(0, 3, 1, 2), **tol)
+    np.testing.assert_allclose(
+        g["ddt"], gs["ddelta"].reshape(batch, nheads, headdim, seqlen).sum(2).transpose(0, 2, 1),
+        **tol)
+    np.testing.assert_allclose(g["dA"], gs["dA"].reshape(nheads, headdim, dstate).sum((1, 2)),
+                               **tol)
+    np.testing.assert_allclose(g["dB"], gs["dB"].transpose(0, 3, 1, 2), **tol)
+    np.testing.assert_allclose(g["dC"], gs["dC"].transpose(0, 3, 1, 2), **tol)
+    np.testing.assert_allclose(g["dh0"], gs["dh0"].reshape(batch, nheads, headdim, dstate), **tol)
+
+
+def test_ssd_bwd_is_linear_in_the_cotangents():
+    c, dy, dfinal = _ssd_bwd_case(341, 1, True)
+    r = _rng(342)
+    dy2, df2 = r.standard_normal(dy.shape), r.standard_normal(dfinal.shape)
+    args = (c["x"], c["dt"], c["A_head"], c["B"], c["C"])
+    g1 = oracle.ssd_bwd(*args, dy, c["h0"], dfinal)
+    g2 = oracle.ssd_bwd(*args, dy2, c["h0"], df2)
+    g3 = oracle.ssd_bwd(*args, dy + 2 * dy2, c["h0"], dfinal + 2 * df2)
+    for k in g1:
+        np.testing.assert_allclose(g3[k], g1[k] + 2 * g2[k], rtol=1e-11, atol=1e-12, err_msg=k)

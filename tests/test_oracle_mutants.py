@@ -72,6 +72,13 @@ MUTANTS = {
     "bwd_softplus_derivative_sign": ("ddl / (1.0 + exp(-pre[t]))", "ddl / (1.0 + exp(pre[t]))"),
     "bwd_dC_uses_previous_state": ("dC[ib] += dy0 * H[(size_t)(t + 1) * dstate + n];",
                                    "dC[ib] += dy0 * H[(size_t)t * dstate + n];"),
+    "ssd_bwd_adjoint_not_decayed": ("adj[n] *= decay;", "adj[n] *= 1.0;"),
+    "ssd_bwd_dx_drops_dt": ("dx[ix] = step_dt * sum_b;", "dx[ix] = sum_b;"),
+    "ssd_bwd_ddt_drops_input_term": (
+        "sum_dt += adj[n] * (A_head[h] * decay * s_prev + Bt[n] * xin);",
+        "sum_dt += adj[n] * (A_head[h] * decay * s_prev);"),
+    "ssd_bwd_dA_undecayed_state": ("dA[h] += adj[n] * step_dt * decay * s_prev;",
+                                   "dA[h] += adj[n] * step_dt * s_prev;"),
     "mamba3_decode_terms_swapped": (
         "s[n] = alpha * s[n] + beta * Bp[n] * xp + gamma * Bt[n] * xv;",
         "s[n] = alpha * s[n] + beta * Bt[n] * xv + gamma * Bp[n] * xp;"),
