@@ -10,6 +10,7 @@
  *                    (trapezoidal three-term recurrence)
  *   ssd_mamba3_mimo_fwd, ssm_decode_step_mamba3_mimo  Mamba-3 MIMO (rank R)
  *   ssm_scan_bwd     gradient of ssm_scan_fwd (reverse mode, every input)
+ *   ssd_chunked_bwd  gradient of ssd_chunked_fwd, tensor cores
  *
  * Conventions shared by every entry point
  *  - Pointers are DEVICE pointers unless stated otherwise, to dense row-major
@@ -363,6 +364,53 @@ ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float* A, cons
                           float* dinitial_state, int batch, int dim, int seqlen, int dstate,
                           int ngroups, ssm_dtype_t in_dtype, void* workspace,
                           size_t workspace_bytes, void* stream);
+
+/*
+ * Bytes of device workspace ssd_chunked_bwd needs (a pure function of its
+ * arguments; 0 if they are invalid or unsupported).  About batch * nheads *
+ * (ceil(seqlen / 128) + 1) * 32 KiB of block states plus 2 * nheads * batch *
+ * seqlen * 512 bytes of per-head dB, dC partials.
+ */
+size_t ssd_chunked_bwd_workspace_bytes(int batch, int seqlen, int nheads, int headdim,
+                                       int dstate, int ngroups);
+
+/*
+ * Gradient of the chunked SSD.
+ *   The forward operation is ssd_chunked_fwd's ("Mamba-3 NKI Kernels for AWS
+ *   Neuron", section "Kernel details": the Mamba-2 SSD structure, equal to the
+ *   step recurrence S = exp(dt A_h) S + dt B x^T, y = C S).  The same page
+ *   reports gradient parity through autograd (section "Correctness") but
+ *   prints no backward formula; this is the exact reverse-mode derivative.
+ *
+ * For the loss sum(dy * y) + sum(dfinal_state * final_state), with y and
+ * final_state what ssd_chunked_fwd returns for the same inputs, writes:
+ *   dx              (batch, seqlen, nheads, headdim)  fp32
+ *   ddt             (batch, seqlen, nheads)           fp32 (dt as given: no softplus)
+ *   dA_head         (nheads,)                         fp32
+ *   dB, dC          (batch, seqlen, ngroups, dstate)  fp32 (summed over the group's heads)
+ *   dinitial_state  (batch, nheads, headdim, dstate)  fp32, may be NULL (not written)
+ * Inputs as for ssd_chunked_fwd (x, B, C bf16; dt, A_head, initial_state fp32)
+ * plus dy (batch, seqlen, nheads, headdim) in in_dtype and dfinal_state
+ * (batch, nheads, headdim, dstate) fp32 or NULL (zero).
+ * workspace: at least ssd_chunked_bwd_workspace_bytes(...) bytes, contents on
+ * entry irrelevant; ssm_last_device_status reads it afterwards.  The call runs
+ * the forward kernel once more to store the state entering every 128-step
+ * block, then one CTA per (batch, head) walks the blocks in reverse; all on
+ * `stream`.  Sums over heads and over the batch are added in a fixed order:
+ * the same bits on every run.
+ * Every output must be disjoint from every input, from the other outputs and
+ * from the workspace (SSM_ERR_ALIAS).
+ * Supported: chunk 64, headdim 64, dstate 128, bf16 in_dtype, seqlen % chunk
+ * == 0, nheads % ngroups == 0.  With no step (seqlen == 0 or batch == 0)
+ * dA_head is zeroed and dinitial_state = dfinal_state (or 0).
+ */
+ssm_status_t ssd_chunked_bwd(const void* x, const float* dt, const float* A_head, const void* B,
+                             const void* C, int chunk, const float* initial_state, const void* dy,
+                             const float* dfinal_state, float* dx, float* ddt, float* dA_head,
+                             float* dB, float* dC, float* dinitial_state, int batch, int seqlen,
+                             int nheads, int headdim, int dstate, int ngroups,
+                             ssm_dtype_t in_dtype, void* workspace, size_t workspace_bytes,
+                             void* stream);
 
 /*
  * Waits for `stream` to drain, then returns the device-side status the last

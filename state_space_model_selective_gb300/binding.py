@@ -29,7 +29,8 @@ STATUS_NAMES = {0: "SSM_OK", 1: "SSM_ERR_NULL", 2: "SSM_ERR_SHAPE", 3: "SSM_ERR_
 EXPORTS = ["ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_bytes", "ssm_scan_fwd",
            "ssd_chunked_fwd", "ssd_mamba3_fwd", "ssd_mamba3_mimo_fwd", "ssm_decode_step",
            "ssm_decode_step_mamba3", "ssm_decode_step_mamba3_mimo", "ssm_last_device_status",
-           "ssm_scan_fwd_noalloc", "ssm_scan_bwd_workspace_bytes", "ssm_scan_bwd"]
+           "ssm_scan_fwd_noalloc", "ssm_scan_bwd_workspace_bytes", "ssm_scan_bwd",
+           "ssd_chunked_bwd_workspace_bytes", "ssd_chunked_bwd"]
 
 
 class SSMError(RuntimeError):
@@ -76,6 +77,10 @@ def lib() -> ctypes.CDLL:
         L.ssm_scan_bwd_workspace_bytes.argtypes = [i] * 5
         L.ssm_scan_bwd.restype = i
         L.ssm_scan_bwd.argtypes = [vp] * 8 + [i] + [vp] * 12 + [i] * 6 + [vp, sz, vp]
+        L.ssd_chunked_bwd_workspace_bytes.restype = sz
+        L.ssd_chunked_bwd_workspace_bytes.argtypes = [i] * 6
+        L.ssd_chunked_bwd.restype = i
+        L.ssd_chunked_bwd.argtypes = [vp] * 5 + [i] + [vp] * 9 + [i] * 7 + [vp, sz, vp]
         L.ssm_last_device_status.restype = i
         L.ssm_last_device_status.argtypes = [vp, vp]
         _lib = L
@@ -265,6 +270,59 @@ def ssm_scan_fwd_noalloc(u, delta, A, B, C, y, final_state=None, D=None, z=None,
                                     _stream(stream))
     _check(st, "ssm_scan_fwd_noalloc")
     return y, final_state
+
+
+def ssd_chunked_bwd_workspace_bytes(batch, seqlen, nheads, headdim=64, dstate=128,
+                                    ngroups=1) -> int:
+    return int(lib().ssd_chunked_bwd_workspace_bytes(batch, seqlen, nheads, headdim, dstate,
+                                                     ngroups))
+
+
+def ssd_chunked_bwd(x, dt, A_head, B, C, dy, chunk=64, initial_state=None, dfinal_state=None,
+                    workspace=None, want_dinitial_state=True, out=None, stream=None):
+    """Gradient of ``ssd_chunked_fwd`` for the loss sum(dy * y) + sum(dfinal_state *
+    final_state).  Inputs as for ``ssd_chunked_fwd``; dy like x (bf16); dfinal_state
+    (batch, nheads, headdim, dstate) fp32 or None.  Returns a dict of fp32 tensors:
+    dx (like x), ddt (like dt), dA_head (nheads,), dB, dC (like B) and dinitial_state
+    (batch, nheads, headdim, dstate, or None).  ``out`` may map any of these names to
+    a preallocated fp32 tensor to write."""
+    _req(x, "x", torch.bfloat16, 4)
+    batch, seqlen, nheads, headdim = x.shape
+    _req(dt, "dt", torch.float32, 3)
+    _req(A_head, "A_head", torch.float32, 1)
+    _req(B, "B", torch.bfloat16, 4)
+    _req(C, "C", torch.bfloat16, 4)
+    _req(dy, "dy", torch.bfloat16, 4)
+    ngroups, dstate = B.shape[2], B.shape[3]
+    _opt(initial_state, "initial_state", torch.float32)
+    _opt(dfinal_state, "dfinal_state", torch.float32)
+    dev, f32 = x.device, torch.float32
+    g = {"dx": torch.empty(tuple(x.shape), dtype=f32, device=dev),
+         "ddt": torch.empty(tuple(dt.shape), dtype=f32, device=dev),
+         "dA_head": torch.empty(nheads, dtype=f32, device=dev),
+         "dB": torch.empty(tuple(B.shape), dtype=f32, device=dev),
+         "dC": torch.empty(tuple(C.shape), dtype=f32, device=dev),
+         "dinitial_state": (torch.empty((batch, nheads, headdim, dstate), dtype=f32, device=dev)
+                            if want_dinitial_state else None)}
+    for k, t in (out or {}).items():
+        if k not in g or g[k] is None:
+            raise ValueError(f"out[{k!r}] is not an output of this call")
+        _req(t, f"out[{k!r}]", f32)
+        if t.shape != g[k].shape:
+            raise ValueError(f"out[{k!r}] must have shape {tuple(g[k].shape)}")
+        g[k] = t
+    need = ssd_chunked_bwd_workspace_bytes(batch, seqlen, nheads, headdim, dstate, ngroups)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _req(workspace, "workspace", torch.uint8)
+    st = lib().ssd_chunked_bwd(_ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C), int(chunk),
+                               _ptr(initial_state), _ptr(dy), _ptr(dfinal_state), _ptr(g["dx"]),
+                               _ptr(g["ddt"]), _ptr(g["dA_head"]), _ptr(g["dB"]), _ptr(g["dC"]),
+                               _ptr(g["dinitial_state"]), batch, seqlen, nheads, headdim, dstate,
+                               ngroups, _DT[torch.bfloat16], _ptr(workspace), workspace.numel(),
+                               _stream(stream))
+    _check(st, "ssd_chunked_bwd")
+    return g
 
 
 def ssd_chunked_fwd(x, dt, A_head, B, C, chunk=64, out_dtype=None, y=None, final_state=None,

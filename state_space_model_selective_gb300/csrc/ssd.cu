@@ -29,16 +29,15 @@
 #include <algorithm>
 #include <mutex>
 
-#include "common.cuh"
-#include "tcgen05.cuh"
+#include "ssd_common.cuh"
+#include "ssd_internal.h"
 
 namespace {
 
 using namespace ssm;
-
-constexpr int kQ = 128;   // steps per block (MMA M)
-constexpr int kP = 64;    // headdim
-constexpr int kNs = 128;  // dstate
+using namespace ssd_detail;
+using ssd_host::make_bc_map;
+using ssd_host::make_x_map;
 constexpr int kThreads = 256;  // two warpgroups; each per-row phase splits a row's columns
 constexpr int kHalf = 32;      // columns of a 64-wide row per warpgroup
 
@@ -68,22 +67,11 @@ struct SsdArgs {
     const __nv_bfloat16* prev_x;
     void* y;
     float* final_state;
+    // optional: the state entering every block and the final state,
+    // [batch * nheads][nblocks + 1][headdim][dstate] (the backward pass reads it)
+    float* bstates;
     int batch, seqlen, nheads, ngroups;
 };
-
-// Two fp32 values rounded to nearest-even bf16 and packed (a in the low half),
-// one conversion instruction.
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<const uint32_t*>(&v);
-}
-
-// (a, b) = hi + lo with hi = bf16(v), lo = bf16(v - hi) (about 16 significant
-// bits in all), returned as the packed hi pair and the packed lo pair.
-__device__ __forceinline__ void split2_bf16(float a, float b, uint32_t& hp, uint32_t& lp) {
-    hp = pack_bf16(a, b);
-    lp = pack_bf16(a - bf16lo(hp), b - bf16hi(hp));
-}
 
 // One 32-column chunk of M' for row i: m_j = G[i][j] 2^(cs2_i + q2_j), with
 // columns past jmax zeroed when MASK (the chunk holding row i's own step; jmax
@@ -109,25 +97,6 @@ __device__ __forceinline__ void mprime_chunk(const float* gv, const float* q2c, 
     }
 }
 
-// K-major operand descriptor for k-step kk (16 bf16) of a tile with R rows.
-template <int R>
-__device__ __forceinline__ uint64_t kdesc(uint32_t tile_saddr, int kk) {
-    return smem_desc_k128(tile_saddr + (uint32_t)((kk >> 2) * (R * 128) + (kk & 3) * 32));
-}
-
-// MN-major operand descriptor for k-step kk of a tile of 128-byte rows (one
-// row per k); 64-wide MN blocks `lbo` bytes apart.
-__device__ __forceinline__ uint64_t mdesc(uint32_t tile_saddr, int kk, uint32_t lbo) {
-    return smem_desc_mn128(tile_saddr + (uint32_t)kk * 2048u, lbo);
-}
-
-// TMEM column of M' (hi part) for k-step kk: row i's columns j in
-// [64 part + 32 half, +32) are held as 16 packed hi columns followed by 16 lo
-// columns, in place of the 32 fp32 G columns they were computed from.
-__device__ __forceinline__ uint32_t mcol_hi(int kk) {
-    return (uint32_t)(64 * (kk >> 2) + 32 * ((kk >> 1) & 1) + 8 * (kk & 1));
-}
-
 // M3 = false: Mamba-2 (the input weight of step j is dt_j).  M3 = true:
 // Mamba-3 SISO single-SSD form, "Mamba-3 NKI Kernels for AWS Neuron",
 // "Kernel details", mamba3_siso_ssd_kernel: the weight is
@@ -139,7 +108,9 @@ __device__ __forceinline__ uint32_t mcol_hi(int kk) {
 // row u of a block is sub-token u % RK of step u / RK -- and sub-tokens share
 // their step's decay and weights; a sub-token sees every sub-token of its own
 // step (the block-diagonal part, weight gamma) and of earlier steps.
-template <typename Tout, bool M3, int RK>
+// BS: write the state entering every block and the final state to a.bstates
+// instead of y (the backward pass's checkpoints).
+template <typename Tout, bool M3, int RK, bool BS = false>
 __global__ void __launch_bounds__(kThreads, 2)
     ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_B,
                    const __grid_constant__ CUtensorMap tm_x, const SsdArgs a) {
@@ -175,6 +146,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int it = 0; it < my_items; ++it) {
             const int item = (int)blockIdx.x + it * (int)gridDim.x;
             const int hh = item % a.nheads, bb = item / a.nheads;
+            if constexpr (BS) {
+                float* bs = a.bstates + (long long)item * (nblocks + 1) * kP * kNs;
+                for (int e = tid; e < (nblocks + 1) * kP * kNs; e += kThreads) bs[e] = nanv;
+                continue;
+            }
             for (int t = tid; t < nsub; t += kThreads) {
                 Tout* yr = reinterpret_cast<Tout*>(a.y) +
                            (((long long)bb * nsub + t) * a.nheads + hh) * kP;
@@ -297,6 +273,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                     }
                 }
             }
+        }
+
+        if constexpr (BS) {
+            float* bs = a.bstates +
+                        (((long long)item * (nblocks + 1) + blk) * kP + kHalf * part) * kNs + row;
+#pragma unroll
+            for (int q = 0; q < kHalf; ++q) bs[q * kNs] = S[q];
         }
 
         // ---- G = C B^T as soon as the C and B tiles are in (thread 0)
@@ -518,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
         // ---- y rows out of the staged tile: each warp writes whole rows of
         // the head (coalesced); rows past the sequence end are skipped
-        {
+        if constexpr (!BS) {
             const long long yrow0 = ((long long)b * nsub + t0) * a.nheads + h;
             if constexpr (sizeof(Tout) == 4) {
 #pragma unroll
@@ -550,6 +533,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int q = 0; q < kHalf; ++q) S[q] = fmaf(a_blk, S[q], sc[q]);
         if (blk == nblocks - 1) {
+            if constexpr (BS) {
+                float* bs = a.bstates + (((long long)item * (nblocks + 1) + nblocks) * kP +
+                                         kHalf * part) * kNs + row;
+#pragma unroll
+                for (int q = 0; q < kHalf; ++q) bs[q * kNs] = S[q];
+            }
             if (a.final_state) {
                 float* fs =
                     a.final_state + ((long long)(b * a.nheads + h) * kP + kHalf * part) * kNs + row;
@@ -573,41 +562,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-bool make_bc_map(CUtensorMap* map, const void* base, int batch, int seqlen, int ngroups) {
-    ssm_host::EncodeTiledFn fn = ssm_host::encode_tiled_fn();
-    if (!fn) return false;
-    // (batch, seqlen, ngroups, dstate) as 4-D {dstate, ngroups, seqlen, batch}
-    const cuuint64_t dims[4] = {(cuuint64_t)kNs, (cuuint64_t)ngroups, (cuuint64_t)seqlen,
-                                (cuuint64_t)batch};
-    const cuuint64_t strides[3] = {(cuuint64_t)kNs * 2, (cuuint64_t)ngroups * kNs * 2,
-                                   (cuuint64_t)seqlen * ngroups * kNs * 2};
-    const cuuint32_t box[4] = {64, 1, (cuuint32_t)kQ, 1};
-    const cuuint32_t estride[4] = {1, 1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
-              box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
-}
-
-bool make_x_map(CUtensorMap* map, const void* base, int batch, int seqlen, int nheads) {
-    ssm_host::EncodeTiledFn fn = ssm_host::encode_tiled_fn();
-    if (!fn) return false;
-    // (batch, seqlen, nheads, headdim) as 3-D {nheads * headdim, seqlen, batch}
-    const cuuint64_t dims[3] = {(cuuint64_t)nheads * kP, (cuuint64_t)seqlen, (cuuint64_t)batch};
-    const cuuint64_t strides[2] = {(cuuint64_t)nheads * kP * 2,
-                                   (cuuint64_t)seqlen * nheads * kP * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)kP, (cuuint32_t)kQ, 1};
-    const cuuint32_t estride[3] = {1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-              box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
-}
-
-template <typename Tout, bool M3, int RK>
+template <typename Tout, bool M3, int RK, bool BS = false>
 ssm_status_t launch(const CUtensorMap& mc, const CUtensorMap& mb, const CUtensorMap& mx,
                     const SsdArgs& a, cudaStream_t s) {
-    auto kern = ssd_fwd_kernel<Tout, M3, RK>;
+    auto kern = ssd_fwd_kernel<Tout, M3, RK, BS>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
         cudaSuccess)
         return SSM_ERR_CUDA;
@@ -728,6 +686,33 @@ ssm_status_t ssd_entry(const void* x, const float* dt, const float* lam, const f
 }
 
 }  // namespace
+
+namespace ssd_internal {
+
+ssm_status_t ssd_forward_block_states(const void* x, const float* dt, const float* A_head,
+                                      const void* B, const void* C, const float* initial_state,
+                                      float* bstates, int batch, int seqlen, int nheads,
+                                      int ngroups, cudaStream_t stream) {
+    CUtensorMap mc, mb, mx;
+    if (!make_bc_map(&mc, C, batch, seqlen, ngroups) || !make_bc_map(&mb, B, batch, seqlen, ngroups) ||
+        !make_x_map(&mx, x, batch, seqlen, nheads))
+        return SSM_ERR_CUDA;
+    SsdArgs a{};
+    a.x = static_cast<const __nv_bfloat16*>(x);
+    a.dt = dt;
+    a.A = A_head;
+    a.h0 = initial_state;
+    a.y = nullptr;
+    a.final_state = nullptr;
+    a.bstates = bstates;
+    a.batch = batch;
+    a.seqlen = seqlen;
+    a.nheads = nheads;
+    a.ngroups = ngroups;
+    return launch<float, false, 1, true>(mc, mb, mx, a, stream);
+}
+
+}  // namespace ssd_internal
 
 extern "C" ssm_status_t ssd_chunked_fwd(const void* x, const float* dt, const float* A_head,
                                         const void* B, const void* C, int chunk,

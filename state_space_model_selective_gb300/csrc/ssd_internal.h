@@ -1,0 +1,20 @@
+// ssd_internal.h -- entry points shared between the library's translation
+// units for the chunked SSD (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "ssm.h"
+
+namespace ssd_internal {
+
+// The chunked SSD forward writing only the state entering every 128-step
+// block and the final state: bstates [batch * nheads][ceil(seqlen / 128) + 1]
+// [64][128] fp32 (headdim 64, dstate 128, bf16 x, B, C).  No y.  Arguments are
+// validated by the caller.
+ssm_status_t ssd_forward_block_states(const void* x, const float* dt, const float* A_head,
+                                      const void* B, const void* C, const float* initial_state,
+                                      float* bstates, int batch, int seqlen, int nheads,
+                                      int ngroups, cudaStream_t stream);
+
+}  // namespace ssd_internal

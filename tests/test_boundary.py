@@ -288,3 +288,48 @@ def test_scan_bwd_workspace_bytes():
     assert f(1, 10, 5, dstate=8) == 0
     assert f(1, 10, 5, ngroups=3) == 0
     assert f(-1, 10, 5) == 0
+
+
+def ssd_bwd_call(L, **kw):
+    args = dict(x=P(0), dt=P(1), A=P(2), B=P(3), C=P(4), chunk=64, h0=None, dy=P(5), dfs=None,
+                dx=P(6), ddt=P(7), dA=P(8), dB=P(9), dC=P(10), dh0=None, batch=2, seqlen=128,
+                nheads=4, headdim=64, dstate=128, ngroups=1, in_dt=1, ws=P(11), wsb=1 << 30,
+                stream=None)
+    args.update(kw)
+    a = args
+    return L.ssd_chunked_bwd(a["x"], a["dt"], a["A"], a["B"], a["C"], a["chunk"], a["h0"], a["dy"],
+                             a["dfs"], a["dx"], a["ddt"], a["dA"], a["dB"], a["dC"], a["dh0"],
+                             a["batch"], a["seqlen"], a["nheads"], a["headdim"], a["dstate"],
+                             a["ngroups"], a["in_dt"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_ssd_bwd_argument_errors(L):
+    assert ssd_bwd_call(L, x=None) == NULL
+    assert ssd_bwd_call(L, dy=None) == NULL
+    assert ssd_bwd_call(L, dC=None) == NULL
+    assert ssd_bwd_call(L, dA=None) == NULL
+    assert ssd_bwd_call(L, seqlen=100) == SHAPE       # not a multiple of the chunk
+    assert ssd_bwd_call(L, ngroups=3) == SHAPE
+    assert ssd_bwd_call(L, batch=-1) == SHAPE
+    assert ssd_bwd_call(L, chunk=32, seqlen=128) == UNSUP
+    assert ssd_bwd_call(L, headdim=32) == UNSUP
+    assert ssd_bwd_call(L, dstate=64) == UNSUP
+    assert ssd_bwd_call(L, in_dt=0) == UNSUP          # fp32 activations: not implemented
+    assert ssd_bwd_call(L, in_dt=9) == DTYPE
+    assert ssd_bwd_call(L, dx=ctypes.c_void_p(0x70000008)) == ALIGN
+    assert ssd_bwd_call(L, ws=None) == WS
+    assert ssd_bwd_call(L, wsb=1024) == WS
+    assert ssd_bwd_call(L, dx=P(0)) == ALIAS           # dx on top of x
+    assert ssd_bwd_call(L, dC=P(9)) == ALIAS           # dB and dC on one buffer
+    assert ssd_bwd_call(L, ws=P(8)) == ALIAS           # workspace on top of dA
+    # no heads: nothing to write
+    assert ssd_bwd_call(L, nheads=0, dA=None, x=None) == OK
+
+
+def test_ssd_bwd_workspace_bytes():
+    f = binding.ssd_chunked_bwd_workspace_bytes
+    # block states (3 per (batch, head) for 256 steps) and the per-head dB, dC partials
+    assert f(32, 256, 32) >= 32 * 32 * 3 * 64 * 128 * 4 + 2 * 32 * 32 * 256 * 128 * 4
+    assert f(32, 256, 32) == f(32, 256, 32)
+    assert f(1, 64, 2, headdim=32) == 0
+    assert f(1, 64, 3, ngroups=2) == 0
