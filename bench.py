@@ -42,6 +42,7 @@ WORKLOAD = ("selective scan, bf16 inputs / fp32 state / fp32 y, batch 8, L 2048,
 # (maximum SM clock).
 SMS, MUFU_PER_CLK, SM_MAX_MHZ = 152, 32, 2070.0
 HBM_PEAK_GBS = 6778.0  # measured copy bandwidth of the GB300s
+BF16_PEAK_TFLOPS = 1908.5  # measured cuBLAS bf16 GEMM burst rate of the GB300s
 MUFU_PEAK_GOPS = SMS * MUFU_PER_CLK * SM_MAX_MHZ * 1e6 / 1e9
 # FP32 pipe: 128 lane-operations per SM per clock (FFMA rate measured by
 # state_space_model_selective_gb300.peaks: 123 per SM per clock).
@@ -361,6 +362,7 @@ def measure_other_paths(dev, reps=20):
                      "algorithmic_bytes": nbytes}}
     del inp
     res["ssm_scan_bwd"] = _measure_scan_bwd(dev, reps)
+    res["ssd_chunked_bwd"] = _measure_ssd_bwd(dev, reps)
     m3 = inputs.mamba3_inputs(32, 256, 32, 64, 128, 1, "bf16", seed=1006, device="cuda")
 
     def ssd_m3():
@@ -492,6 +494,43 @@ def _measure_scan_bwd(dev, reps):
             "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_GOPS,
                          "unit": "Gop/s (FP32 pipe)", "frac": achieved / FP32_PEAK_GOPS,
                          "algorithmic_fp32_ops": ops}}
+
+
+def _measure_ssd_bwd(dev, reps):
+    """The chunked SSD's gradient (ssd_chunked_bwd: block-state forward, reverse
+    block walk on the tensor cores, head and batch sums) on the SSD workload
+    (bf16, batch 32, L 256, 32 heads, headdim 64, d_state 128), against the bf16
+    tensor peak.  Algorithmic FLOPs per 128-step block and head: the nine
+    distinct products of the chunked gradient at full precision, 2 (3 Q^2 N +
+    2 Q^2 P + 4 Q P N); the kernel's hi/lo splits and its second (transposed)
+    Q x Q product are not counted."""
+    import torch
+    from state_space_model_selective_gb300 import binding, inputs
+    Bn, L, H, P, N = 32, 256, 32, 64, 128
+    inp = inputs.ssd_inputs(Bn, L, H, P, N, 1, "bf16", seed=1004, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1009)
+    dy = torch.randn(Bn, L, H, P, device=dev, generator=g).to(torch.bfloat16)
+    f = dict(dtype=torch.float32, device=dev)
+    out = {"dx": torch.empty(Bn, L, H, P, **f), "ddt": torch.empty(Bn, L, H, **f),
+           "dA_head": torch.empty(H, **f), "dB": torch.empty(Bn, L, 1, N, **f),
+           "dC": torch.empty(Bn, L, 1, N, **f), "dinitial_state": torch.empty(Bn, H, P, N, **f)}
+    ws = torch.empty(binding.ssd_chunked_bwd_workspace_bytes(Bn, L, H, P, N, 1),
+                     dtype=torch.uint8, device=dev)
+
+    def bwd():
+        binding.ssd_chunked_bwd(inp["x"], inp["dt"], inp["A_head"], inp["B"], inp["C"], dy, 64,
+                                workspace=ws, out=out)
+    ms = _time(bwd, reps)
+    Q = 128
+    flops = 2 * (3 * Q * Q * N + 2 * Q * Q * P + 4 * Q * P * N) * Bn * H * (L // Q)
+    achieved = flops / (ms / 1e3) / 1e12
+    return {"workload": "chunked-SSD gradient bf16 in / fp32 gradients, batch 32, L 256, 32 "
+                        "heads, headdim 64, d_state 128, chunk 64",
+            "ms": ms, "elements_per_s": Bn * L * H * P * N / (ms / 1e3),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": BF16_PEAK_TFLOPS,
+                         "unit": "TFLOP/s", "frac": achieved / BF16_PEAK_TFLOPS,
+                         "algorithmic_flops": flops}}
 
 
 def _time(fn, reps):

@@ -67,8 +67,9 @@ struct ScanArgs {
     float* carry;     // [nchunks - 1][batch * dim][kN]
     const void* Bm;
     const void* Cm;
-    // optional: the state entering every 16-step segment, [seg][batch * dim][kN]
-    // (the backward pass recomputes from these); y may then be NULL
+    // checkpoint mode (kernel flag CK): the state entering every 16-step
+    // segment, [seg][batch * dim][kN], instead of y (the backward pass
+    // recomputes from these)
     float* ckpt;
     int batch, dim, seqlen, ngroups;
     int dpg;          // channels per group
@@ -173,7 +174,7 @@ struct Smem {
     static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024
 };
 
-template <typename Tin, typename Tout, int CH, bool TMA>
+template <typename Tin, typename Tout, int CH, bool TMA, bool CK = false>
 __global__ void __launch_bounds__(CH * kNG + 32, 3)
     scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u,
                     const __grid_constant__ CUtensorMap tm_d,
@@ -412,7 +413,7 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
         const uint8_t* tz = st + 2 * S::IN_TILE;
 #pragma unroll 2
         for (int j = 0; j < kTL / 8; ++j) {
-            if (a.ckpt && (j & 1) == 0 && valid && t0 + j * 8 < a.seqlen) {
+            if (CK && (j & 1) == 0 && valid && t0 + j * 8 < a.seqlen) {
                 const long long seg = (t0 + j * 8) / 16;
                 __stcg(reinterpret_cast<float4*>(
                            a.ckpt + (seg * a.batch * a.dim + drow) * kN + n0),
@@ -476,7 +477,7 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
                 o0 *= silu_f(zz[0]);
                 o1 *= silu_f(zz[1]);
             }
-            if (a.y && valid && tg < t_end)
+            if (!CK && valid && tg < t_end)
                 store_y2<Tout>(yrow + tg, o0, o1, true, tg + 1 < t_end, vec_store);
         }
 
@@ -548,12 +549,12 @@ size_t workspace_bound(long long batch, long long dim, int seqlen, int ngroups) 
     return round256(bytes);
 }
 
-template <typename Tin, typename Tout, int CH, bool TMA>
+template <typename Tin, typename Tout, int CH, bool TMA, bool CK = false>
 int occupancy_blocks() {
     using S = Smem<Tin, CH, TMA>;
     static int cached = -1;
     if (cached < 0) {
-        auto kern = scan_fwd_kernel<Tin, Tout, CH, TMA>;
+        auto kern = scan_fwd_kernel<Tin, Tout, CH, TMA, CK>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
         int nb = 0;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, CH * kNG + 32, S::ALLOC);
@@ -562,11 +563,11 @@ int occupancy_blocks() {
     return cached;
 }
 
-template <typename Tin, typename Tout, int CH, bool TMA>
+template <typename Tin, typename Tout, int CH, bool TMA, bool CK = false>
 ssm_status_t launch(const ScanArgs& base, const Plan& p, const CUtensorMap* maps,
                     cudaStream_t stream) {
     using S = Smem<Tin, CH, TMA>;
-    auto kern = scan_fwd_kernel<Tin, Tout, CH, TMA>;
+    auto kern = scan_fwd_kernel<Tin, Tout, CH, TMA, CK>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC) !=
         cudaSuccess)
         return SSM_ERR_CUDA;
@@ -581,14 +582,14 @@ ssm_status_t launch(const ScanArgs& base, const Plan& p, const CUtensorMap* maps
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
-template <typename Tin, typename Tout, int CH, bool TMA>
+template <typename Tin, typename Tout, int CH, bool TMA, bool CK = false>
 void plan_for(const ScanArgs& a, Plan& p) {
     p.CH = CH;
     p.tma = TMA;
     p.bpg = (a.dpg + CH - 1) / CH;
     p.nblocks = a.batch * a.ngroups * p.bpg;
     const int tiles = (a.seqlen + kTL - 1) / kTL;
-    const long long slots = (long long)occupancy_blocks<Tin, Tout, CH, TMA>() * dev_info().sms;
+    const long long slots = (long long)occupancy_blocks<Tin, Tout, CH, TMA, CK>() * dev_info().sms;
     int nchunks = 1;
     if (p.nblocks >= slots) {
         // Enough independent channel blocks to fill the GPU: cut L into
@@ -601,12 +602,12 @@ void plan_for(const ScanArgs& a, Plan& p) {
     p.nchunks = (tiles + p.chunk_tiles - 1) / p.chunk_tiles;
 }
 
-template <typename Tin, typename Tout>
+template <typename Tin, typename Tout, bool CK = false>
 ssm_status_t dispatch(ScanArgs& a, ssm_dtype_t in_dtype, bool tma, cudaStream_t stream,
                       void* workspace) {
     Plan p{};
-    if (tma) plan_for<Tin, Tout, 32, true>(a, p);
-    else plan_for<Tin, Tout, 32, false>(a, p);
+    if (tma) plan_for<Tin, Tout, 32, true, CK>(a, p);
+    else plan_for<Tin, Tout, 32, false, CK>(a, p);
 
     // workspace: header | flags | carry
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -632,9 +633,9 @@ ssm_status_t dispatch(ScanArgs& a, ssm_dtype_t in_dtype, bool tma, cudaStream_t 
         if (okm && a.z)
             okm = ssm_host::make_tmap_2d(&maps[2], a.z, in_dtype, rows, a.seqlen, 32, tpb);
         if (!okm) return SSM_ERR_CUDA;
-        return launch<Tin, Tout, 32, true>(a, p, maps, stream);
+        return launch<Tin, Tout, 32, true, CK>(a, p, maps, stream);
     }
-    return launch<Tin, Tout, 32, false>(a, p, maps, stream);
+    return launch<Tin, Tout, 32, false, CK>(a, p, maps, stream);
 }
 
 }  // namespace
@@ -662,8 +663,9 @@ ssm_status_t scan_forward_checkpoints(const void* u, const void* delta, const fl
     a.dpg = dim / ngroups; a.softplus = delta_softplus ? 1 : 0;
     const size_t es = in_dtype == SSM_BF16 ? 2 : 4;
     const bool tma = ((size_t)seqlen * es) % 16 == 0;
-    if (in_dtype == SSM_BF16) return dispatch<__nv_bfloat16, float>(a, in_dtype, tma, stream, workspace);
-    return dispatch<float, float>(a, in_dtype, tma, stream, workspace);
+    if (in_dtype == SSM_BF16)
+        return dispatch<__nv_bfloat16, float, true>(a, in_dtype, tma, stream, workspace);
+    return dispatch<float, float, true>(a, in_dtype, tma, stream, workspace);
 }
 
 }  // namespace ssm_internal

@@ -51,7 +51,7 @@ constexpr uint32_t kSS = 98304;     // S_in hi | lo [128 n][64 p]
 constexpr uint32_t kSDS = 131072;   // dS_out hi | lo [128 n][64 p]
 constexpr uint32_t kSE = 163840;    // (e^cs o dY) hi | lo [128 i][64 p]
 constexpr uint32_t kMisc = 196608;  // cs2[128], q2[128], sums, mbarriers, TMEM address
-constexpr uint32_t kMiscBytes = 128 * 4 * 2 + 4 * 4 * 4 + 8 * 8 + 16;
+constexpr uint32_t kMiscBytes = 128 * 4 * 2 + 4 * 4 * 4 + 9 * 8 + 16;
 constexpr uint32_t kSmemAlloc = kMisc + kMiscBytes + 1024;  // + realignment slack
 
 // TMEM columns (one CTA per SM: all 512)
@@ -173,6 +173,14 @@ __device__ __forceinline__ float dot_row128_tmem(const uint8_t* tile, int row, u
     return acc;
 }
 
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_bwd_kernel(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_B,
                    const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
@@ -186,10 +194,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* s_rsum = s_wsum + 4;                             // [4] warp totals (d cs suffix scan)
     float* s_dot = s_rsum + 4;                              // [4] <dS_out, S_out> per warp
     float* s_da = s_dot + 4;                                // [4] dA per warp
-    uint64_t* bar_ld = reinterpret_cast<uint64_t*>(s_da + 4);
-    uint64_t* bar_mma = bar_ld + 1;  // [6] one per MMA group
-    uint64_t* bar_fin = bar_ld + 7;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_ld + 8);
+    uint64_t* bar_ld = reinterpret_cast<uint64_t*>(s_da + 4);  // C, B, S_in, S_out in
+    uint64_t* bar_ld2 = bar_ld + 1;                            // x, dy in
+    uint64_t* bar_mma = bar_ld + 2;  // [6] one per MMA group
+    uint64_t* bar_fin = bar_ld + 8;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_ld + 9);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int row = tid;  // TMEM lane and block row
@@ -199,10 +208,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int L = a.seqlen;
     const int nblocks = (L + kQ - 1) / kQ;
     const float Ah = a.A[h];
+    const float* bs_item = a.bstates + (long long)item * (nblocks + 1) * kP * kNs;
+
+    // Loads of block blk (thread 0): C, B and the states entering and leaving it
+    // (fp32 [p][n], into the regions their split forms replace), then x and dy.
+    auto load_cbs = [&](int blk) {
+        mbar_arrive_expect_tx(bar_ld, 4 * 32768);
+        tma_load_4d(smem + kSC, &tm_C, bar_ld, 0, g, blk * kQ, b);
+        tma_load_4d(smem + kSC + 16384, &tm_C, bar_ld, 64, g, blk * kQ, b);
+        tma_load_4d(smem + kSB, &tm_B, bar_ld, 0, g, blk * kQ, b);
+        tma_load_4d(smem + kSB + 16384, &tm_B, bar_ld, 64, g, blk * kQ, b);
+        bulk_load(smem + kSE, bs_item + (long long)blk * kP * kNs, 32768, bar_ld);
+        bulk_load(smem + kSDS, bs_item + (long long)(blk + 1) * kP * kNs, 32768, bar_ld);
+    };
+    auto load_xdy = [&](int blk) {
+        mbar_arrive_expect_tx(bar_ld2, 2 * 16384);
+        tma_load_3d(smem + kSX, &tm_x, bar_ld2, h * kP, blk * kQ, b);
+        tma_load_3d(smem + kSDY, &tm_dy, bar_ld2, h * kP, blk * kQ, b);
+    };
 
     if (warp == 0) tmem_alloc(s_tmem, kTmemCols);
     if (tid == 0) {
         mbar_init(bar_ld, 1);
+        mbar_init(bar_ld2, 1);
         for (int k = 0; k < 6; ++k) mbar_init(bar_mma + k, 1);
         mbar_init(bar_fin, 1);
         fence_mbar_init();
@@ -210,12 +238,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tm_B);
         prefetch_tensormap(&tm_x);
         prefetch_tensormap(&tm_dy);
+        if (nblocks > 0) {
+            load_cbs(nblocks - 1);
+            load_xdy(nblocks - 1);
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+    bool ld_pending = nblocks > 0, ld2_pending = nblocks > 0;
+    uint32_t ld_par = 0, ld2_par = 0;  // phase parity of the pending loads
 
     // the adjoint state dS_out[p][n = row], carried from block to block
     float dS[kP];
@@ -223,25 +257,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int p = 0; p < kP; ++p)
         dS[p] = a.dfinal ? a.dfinal[((long long)item * kP + p) * kNs + row] : 0.0f;
     float dA_acc = 0.0f;
-    bool ok = true, ld_pending = false;
+    bool ok = true;
     uint32_t ph = 0;
+    auto dt_of = [&](int blk) {
+        const int t = blk * kQ + row;
+        return t < L ? a.dt[((long long)b * L + t) * a.nheads + h] : 0.0f;
+    };
+    float dt_next = nblocks > 0 ? dt_of(nblocks - 1) : 0.0f;
 
     for (int blk = nblocks - 1; blk >= 0; --blk, ph ^= 1u) {
         const int t0 = blk * kQ;
-        if (tid == 0) {
-            mbar_arrive_expect_tx(bar_ld, 2 * 32768 + 2 * 16384);
-            tma_load_4d(smem + kSC, &tm_C, bar_ld, 0, g, t0, b);
-            tma_load_4d(smem + kSC + 16384, &tm_C, bar_ld, 64, g, t0, b);
-            tma_load_4d(smem + kSB, &tm_B, bar_ld, 0, g, t0, b);
-            tma_load_4d(smem + kSB + 16384, &tm_B, bar_ld, 64, g, t0, b);
-            tma_load_3d(smem + kSX, &tm_x, bar_ld, h * kP, t0, b);
-            tma_load_3d(smem + kSDY, &tm_dy, bar_ld, h * kP, t0, b);
-        }
-        ld_pending = true;
-
-        // ---- per-row decay terms: cs (inclusive, in the block), e^cs, e^(cs_last - cs)
         const int t = t0 + row;
-        const float dtr = t < L ? a.dt[((long long)b * L + t) * a.nheads + h] : 0.0f;
+        const float dtr = dt_next;
+        if (blk > 0) dt_next = dt_of(blk - 1);
+
+        // ---- cumulative log-decay within the block (warp part)
         float v = dtr * Ah;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -249,11 +279,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane >= o) v += u;
         }
         if (lane == 31) s_wsum[warp] = v;
-        // ---- S_in (block state) and dS_out as split operands [n = row][p];
-        // <dS_out, S_out> for the log-decay gradient of the block's last row
+        // ---- S_in as the split operand [n = row][p]; <dS_out, S_out> for the
+        // log-decay gradient of the block's last row
         {
-            const float* sin = a.bstates + ((long long)item * (nblocks + 1) + blk) * kP * kNs + row;
-            const float* sout = sin + kP * kNs;
+            const bool got = mbar_wait(bar_ld, ph, a.status);
+            if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
+            ld_pending = false;
+        }
+        {
+            const float* sin = reinterpret_cast<const float*>(smem + kSE) + row;
+            const float* sout = reinterpret_cast<const float*>(smem + kSDS) + row;
             float sv[kP];
             float dot = 0.0f;
 #pragma unroll
@@ -262,14 +297,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dot = fmaf(dS[p], sout[p * kNs], dot);
             }
             store_split_row(smem + kSS, row, sv);
-            store_split_row(smem + kSDS, row, dS);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
             if (lane == 0) s_dot[warp] = dot;
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
+        __syncthreads();  // S_out read out of its region; warp sums visible
+        store_split_row(smem + kSDS, row, dS);  // dS_out over S_out
         float cs_last = 0.0f;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
@@ -288,12 +321,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float u_r = dtr * eL_r;
         const float e_last = ex2_approx(cs2_last);
         const float sdot = s_dot[0] + s_dot[1] + s_dot[2] + s_dot[3];
+        fence_proxy_async_smem();
+        tc_fence_before();
 
         // ---- group 1: G^T = B C^T, T = dY X^T, T^T = X dY^T, P = dY S_in
         {
-            const bool got = mbar_wait(bar_ld, ph, a.status);
+            const bool got = mbar_wait(bar_ld2, ph, a.status);
             if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
-            ld_pending = false;
+            ld2_pending = false;
         }
         if (tid == 0) {
             tc_fence_after();
@@ -319,7 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                          kdesc<kQ>(sbase + kSS + 16384, kk), id128, 1);
             mma_commit(bar_mma + 0);
         }
-        // e^cs o dY as the split MN-major operand of dS_in^T (rows i, p contiguous)
+        // e^cs o dY as the split MN-major operand of dS_in^T (rows i, p contiguous),
+        // over the S_in region (read above)
         {
             float dyv[kP];
             load_tile_row64(smem + kSDY, row, dyv);
@@ -477,6 +513,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
         }
         tc_fence_after();
+        // C, B, S_in's and S_out's regions are free (group 5 was their last
+        // reader): the previous block's loads start now
+        if (tid == 0 && blk > 0) load_cbs(blk - 1);
+        if (blk > 0) {
+            ld_pending = true;
+            ld_par = ph ^ 1u;
+        }
         // B dS_out^T row j scaled by e^(cs_last - cs_j); the adjoint entering
         // the block: dS_in[p][n = row] = e^cs_last dS_out + (C^T (e^cs o dY))[n][p]
 #pragma unroll
@@ -552,6 +595,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t < L) a.ddt[((long long)b * L + t) * a.nheads + h] = fmaf(Ah, dcs, dw);
         dA_acc = fmaf(dtr, dcs, dA_acc);
         __syncthreads();  // s_rsum, s_wsum, s_dot are rewritten by the next block
+        if (tid == 0 && blk > 0) load_xdy(blk - 1);  // x was read above, dy by group 6
+        if (blk > 0) {
+            ld2_pending = true;
+            ld2_par = ph ^ 1u;
+        }
     }
 
     if (ok) {
@@ -568,7 +616,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // a wait ran out: let every issued MMA and load finish before leaving
         mma_commit(bar_fin);
         (void)mbar_wait(bar_fin, 0, nullptr);
-        if (ld_pending) (void)mbar_wait(bar_ld, ph, nullptr);
+        if (ld_pending) (void)mbar_wait(bar_ld, ld_par, nullptr);
+        if (ld2_pending) (void)mbar_wait(bar_ld2, ld2_par, nullptr);
     }
     tc_fence_before();
     __syncthreads();

@@ -3,10 +3,14 @@
     python -m state_space_model_selective_gb300.profile_run scan   [--reps 5]
     python -m state_space_model_selective_gb300.profile_run ssd    [--reps 5]
     python -m state_space_model_selective_gb300.profile_run decode [--reps 5]
+    python -m state_space_model_selective_gb300.profile_run scan_bwd [--reps 5]
+    python -m state_space_model_selective_gb300.profile_run ssd_bwd [--reps 5]
 
-scan:   selective scan, bf16 in / fp32 y, batch 8, L 2048, D 1536, N 16
-ssd:    chunked SSD, bf16 in / fp32 y, batch 32, L 256, 32 heads, headdim 64, N 128
-decode: decode step, fp32, batch 256, 32 heads, headdim 64, N 128
+scan:     selective scan, bf16 in / fp32 y, batch 8, L 2048, D 1536, N 16
+ssd:      chunked SSD, bf16 in / fp32 y, batch 32, L 256, 32 heads, headdim 64, N 128
+decode:   decode step, fp32, batch 256, 32 heads, headdim 64, N 128
+scan_bwd: the scan's gradient on the scan workload (D, gate, bias, softplus)
+ssd_bwd:  the chunked SSD's gradient on the SSD workload
 Inputs are drawn on the GPU (seeded); the process exits non-zero on any error.
 """
 from __future__ import annotations
@@ -20,7 +24,7 @@ from . import binding, inputs
 
 def main(argv=None):
     p = argparse.ArgumentParser()
-    p.add_argument("workload", choices=["scan", "ssd", "decode"])
+    p.add_argument("workload", choices=["scan", "ssd", "decode", "scan_bwd", "ssd_bwd"])
     p.add_argument("--reps", type=int, default=5)
     a = p.parse_args(argv)
     dev = torch.device("cuda")
@@ -44,6 +48,31 @@ def main(argv=None):
             binding.ssd_chunked_fwd(inp["x"], inp["dt"], inp["A_head"], inp["B"], inp["C"], 64,
                                     out_dtype=torch.float32, y=y, final_state=fs)
         torch.cuda.synchronize()
+    elif a.workload == "scan_bwd":
+        B, D, L = 8, 1536, 2048
+        inp = inputs.scan_inputs(B, D, L, 16, 1, "bf16", seed=1002, device="cuda")
+        g = torch.Generator(device=dev)
+        g.manual_seed(1008)
+        dy = torch.randn(B, D, L, device=dev, generator=g).to(torch.bfloat16)
+        ws = torch.empty(binding.ssm_scan_bwd_workspace_bytes(B, D, L), dtype=torch.uint8,
+                         device=dev)
+        for _ in range(a.reps):
+            binding.ssm_scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], dy,
+                                 inp["D"], inp["z"], inp["delta_bias"], True, workspace=ws)
+        torch.cuda.synchronize()
+        assert binding.ssm_last_device_status(ws) == 0
+    elif a.workload == "ssd_bwd":
+        inp = inputs.ssd_inputs(32, 256, 32, 64, 128, 1, "bf16", seed=1004, device="cuda")
+        g = torch.Generator(device=dev)
+        g.manual_seed(1009)
+        dy = torch.randn(32, 256, 32, 64, device=dev, generator=g).to(torch.bfloat16)
+        ws = torch.empty(binding.ssd_chunked_bwd_workspace_bytes(32, 256, 32), dtype=torch.uint8,
+                         device=dev)
+        for _ in range(a.reps):
+            binding.ssd_chunked_bwd(inp["x"], inp["dt"], inp["A_head"], inp["B"], inp["C"], dy,
+                                    64, workspace=ws)
+        torch.cuda.synchronize()
+        assert binding.ssm_last_device_status(ws) == 0
     else:
         inp = inputs.decode_inputs(256, 32, 64, 128, 1, 1, "f32", seed=1005, device="cuda")
         state = inp["state"]

@@ -1,22 +1,29 @@
 """Parity of the tensor-core SSD gradient (ssd_chunked_bwd, through the C ABI)
 with the fp64 oracle's reverse-mode derivative of the step recurrence.
 
-Tolerance: the forward SSD's bound (2e-3 normwise).  The kernel's products take
-bf16 operands: x, B, C and dy exactly, the fp32 intermediates (states, adjoint
-states, masked decayed Q x Q products) as bf16 hi + lo pairs (about 16
-significant bits), with fp32 accumulation.
+Tolerance.  The kernel's products take bf16 operands: x, B, C and dy exactly,
+the fp32 intermediates (states, adjoint states, masked decayed Q x Q products)
+as bf16 hi + lo pairs (about 16 significant bits, relative error <= 2^-17 per
+operand), with fp32 accumulation over K <= 128; the per-element gradients then
+carry a normwise error of order 1e-5 (measured 3-5e-6): TOL_SSD_GRAD = 1e-4.
+dA_head sums d cs over the batch and the sequence, where the C . dC and B . dB
+terms largely cancel, so its error relative to its own size is larger
+(measured up to 4.4e-5): TOL_SSD_DA = 5e-4.
 """
 import pytest
 import torch
 
 import oracle
 from state_space_model_selective_gb300 import binding, inputs
-from tests.helpers import TOL_BF16, assert_close
+from tests.helpers import assert_close
 
 pytestmark = pytest.mark.gpu
 
-KEYS = [("dx", "dx"), ("ddt", "ddt"), ("dA_head", "dA"), ("dB", "dB"), ("dC", "dC"),
-        ("dinitial_state", "dh0")]
+TOL_SSD_GRAD = 1e-4
+TOL_SSD_DA = 5e-4
+KEYS = [("dx", "dx", TOL_SSD_GRAD), ("ddt", "ddt", TOL_SSD_GRAD), ("dA_head", "dA", TOL_SSD_DA),
+        ("dB", "dB", TOL_SSD_GRAD), ("dC", "dC", TOL_SSD_GRAD),
+        ("dinitial_state", "dh0", TOL_SSD_GRAD)]
 
 
 def _cotangents(batch, seqlen, nheads, seed, with_dfinal):
@@ -74,8 +81,8 @@ def test_ssd_bwd_matches_oracle(case):
           if state else None)
     g = _gpu(inp, dy, h0, dfinal)
     ref = _ref(inp, dy, h0, dfinal)
-    for key, rkey in KEYS:
-        assert_close(g[key], ref[rkey], TOL_BF16, key)
+    for key, rkey, tol in KEYS:
+        assert_close(g[key], ref[rkey], tol, key)
 
 
 def test_ssd_bwd_deterministic():
@@ -135,6 +142,6 @@ def test_ssd_bwd_full_size_properties():
         assert torch.count_nonzero(g[key][:, T:]).item() == 0, key
     head = {k: (v[:, :T].contiguous() if k in ("x", "dt", "B", "C") else v) for k, v in inp.items()}
     ref = _ref(head, dy[:, :T].contiguous())
-    for key, rkey in KEYS:
+    for key, rkey, tol in KEYS:
         got = g[key][:, :T] if key in ("dx", "ddt", "dB", "dC") else g[key]
-        assert_close(got, ref[rkey], TOL_BF16, key)
+        assert_close(got, ref[rkey], tol, key)
