@@ -20,8 +20,9 @@
 // (the C . dC - B . dB form of the log-decay gradient: every term of y_i and
 // of S_out depends on cs only through factors e^(cs_i - cs_j)).
 //
-// GB300 mapping.  One CTA of 128 threads per (batch, head), thread r owning
-// TMEM lane r (block row r); C, B, x and dy arrive by TMA in the 128-byte-
+// GB300 mapping.  One CTA of 256 threads per (batch, head): two warpgroups,
+// thread (r, part) owning TMEM lane r (block row r) and half of each row's
+// columns (part 0 the first half); C, B, x and dy arrive by TMA in the 128-byte-
 // swizzled layout the MMAs read; S_in, dS_out and e^cs o dY are split into
 // bf16 hi + lo pairs and written by the threads.  Eleven products per block,
 // all M = 128 tcgen05 MMAs with fp32 accumulators in the CTA's 512 TMEM
@@ -40,7 +41,7 @@ namespace {
 using namespace ssm;
 using namespace ssd_detail;
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;  // two warpgroups, each taking half of every row
 
 // Shared memory (offsets from the 1024-aligned base)
 constexpr uint32_t kSC = 0;         // C tile [128 i][128 n] (two 64-n boxes, 16 KB apart)
@@ -51,7 +52,7 @@ constexpr uint32_t kSS = 98304;     // S_in hi | lo [128 n][64 p]
 constexpr uint32_t kSDS = 131072;   // dS_out hi | lo [128 n][64 p]
 constexpr uint32_t kSE = 163840;    // (e^cs o dY) hi | lo [128 i][64 p]
 constexpr uint32_t kMisc = 196608;  // cs2[128], q2[128], sums, mbarriers, TMEM address
-constexpr uint32_t kMiscBytes = 128 * 4 * 2 + 4 * 4 * 4 + 9 * 8 + 16;
+constexpr uint32_t kMiscBytes = (2 * 128 + 32 + 3 * 128) * 4 + 9 * 8 + 16;
 constexpr uint32_t kSmemAlloc = kMisc + kMiscBytes + 1024;  // + realignment slack
 
 // TMEM columns (one CTA per SM: all 512)
@@ -98,14 +99,14 @@ __device__ __forceinline__ void masked_chunk(const float* gv, const float* col2,
     }
 }
 
-// Row r of a TMEM Q x Q product turned into its masked, decayed bf16 hi/lo
-// operand in place: column k kept for k in [kmin, kmax] with factor
-// 2^(base + col2[k]).
-__device__ __forceinline__ void mask_row(uint32_t taddr, const float* col2, float base, int kmin,
-                                         int kmax) {
+// This warpgroup's half (columns 64 part .. + 63) of row r of a TMEM Q x Q
+// product, turned into its masked, decayed bf16 hi/lo operand in place: column
+// k kept for k in [kmin, kmax] with factor 2^(base + col2[k]).
+__device__ __forceinline__ void mask_row_half(uint32_t taddr, const float* col2, float base,
+                                              int kmin, int kmax, int part) {
 #pragma unroll 1
-    for (int ck = 0; ck < 4; ++ck) {
-        const int c0 = 32 * ck;
+    for (int hh = 0; hh < 2; ++hh) {
+        const int c0 = 64 * part + 32 * hh;
         uint32_t hp[16], lp[16];
         if (c0 + 31 < kmin || c0 > kmax) {
 #pragma unroll
@@ -121,25 +122,29 @@ __device__ __forceinline__ void mask_row(uint32_t taddr, const float* col2, floa
     }
 }
 
-// 64 fp32 values of one [n][p] (or [i][p]) row written as bf16 hi and lo rows
-// of a 128-byte-swizzled tile pair (lo 16 KB after hi).
-__device__ __forceinline__ void store_split_row(uint8_t* tile, int row, const float* v) {
+// 32 fp32 values (this warpgroup's p range 32 part .. + 31) of one [n][p] or
+// [i][p] row, written as bf16 hi and lo into a 128-byte-swizzled tile pair
+// (lo 16 KB after hi).
+__device__ __forceinline__ void store_split_half(uint8_t* tile, int row, int part, const float* v) {
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < 4; ++c) {
         uint32_t hp[4], lp[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) split2_bf16(v[8 * c + 2 * e], v[8 * c + 2 * e + 1], hp[e], lp[e]);
-        const uint32_t off = (uint32_t)(row * 128 + ((c ^ (row & 7)) << 4));
+        const int cc = 4 * part + c;
+        const uint32_t off = (uint32_t)(row * 128 + ((cc ^ (row & 7)) << 4));
         *reinterpret_cast<uint4*>(tile + off) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
         *reinterpret_cast<uint4*>(tile + 16384 + off) = make_uint4(lp[0], lp[1], lp[2], lp[3]);
     }
 }
 
-// Row r (64 bf16) of a TMA tile [128][64] in the 128-byte swizzle, as fp32.
-__device__ __forceinline__ void load_tile_row64(const uint8_t* tile, int row, float* v) {
+// The 32 bf16 of row r, columns 32 part .. + 31, of a TMA tile [128][64] in the
+// 128-byte swizzle, as fp32.
+__device__ __forceinline__ void load_tile_half(const uint8_t* tile, int row, int part, float* v) {
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const uint4 w = *reinterpret_cast<const uint4*>(tile + row * 128 + ((c ^ (row & 7)) << 4));
+    for (int c = 0; c < 4; ++c) {
+        const int cc = 4 * part + c;
+        const uint4 w = *reinterpret_cast<const uint4*>(tile + row * 128 + ((cc ^ (row & 7)) << 4));
         const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -149,19 +154,22 @@ __device__ __forceinline__ void load_tile_row64(const uint8_t* tile, int row, fl
     }
 }
 
-// Dot product of row r (128 bf16, two 64-wide boxes 16 KB apart) of a TMA
-// tile with 128 fp32 values read from TMEM in 32-column pieces.
-__device__ __forceinline__ float dot_row128_tmem(const uint8_t* tile, int row, uint32_t taddr) {
+// This warpgroup's half of a dot product: row r of a TMA tile [128][128] (two
+// 64-wide boxes 16 KB apart; box `part` holds columns 64 part .. + 63) against
+// the same 64 fp32 columns of TMEM row r, 32 at a time; optionally the 64
+// values are also stored to dst (global, 16-byte aligned).
+__device__ __forceinline__ float dot_half_tmem(const uint8_t* tile, int row, int part,
+                                               uint32_t taddr, float* dst) {
+    const uint8_t* box = tile + part * 16384 + row * 128;
     float acc = 0.0f;
 #pragma unroll 1
-    for (int ck = 0; ck < 4; ++ck) {
+    for (int hh = 0; hh < 2; ++hh) {
         float v[32];
-        tmem_ld32(taddr + 32 * ck, v);
+        tmem_ld32(taddr + 64 * part + 32 * hh, v);
         tmem_wait_ld();
-        const uint8_t* box = tile + (ck >> 1) * 16384 + row * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            const int cc = (ck & 1) * 4 + c;
+            const int cc = 4 * hh + c;
             const uint4 w = *reinterpret_cast<const uint4*>(box + ((cc ^ (row & 7)) << 4));
             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -169,8 +177,27 @@ __device__ __forceinline__ float dot_row128_tmem(const uint8_t* tile, int row, u
                 acc = fmaf(bf16lo(ww[e]), v[8 * c + 2 * e],
                            fmaf(bf16hi(ww[e]), v[8 * c + 2 * e + 1], acc));
         }
+        if (dst) {
+#pragma unroll
+            for (int q = 0; q < 32; q += 4)
+                *reinterpret_cast<float4*>(dst + 64 * part + 32 * hh + q) =
+                    make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+        }
     }
     return acc;
+}
+
+// This warpgroup's 64 columns of TMEM row r scaled by f in place, 32 at a time.
+__device__ __forceinline__ void scale_half(uint32_t taddr, int part, float f) {
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+        float v[32];
+        tmem_ld32(taddr + 64 * part + 32 * hh, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] *= f;
+        tmem_st32f(taddr + 64 * part + 32 * hh, v);
+    }
 }
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -190,18 +217,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sbase = smem_u32(smem);
     float* s_cs2 = reinterpret_cast<float*>(smem + kMisc);  // log2-scaled cs of each row
     float* s_q2 = s_cs2 + kQ;                               // log2(dt_j) - cs2_j
-    float* s_wsum = s_q2 + kQ;                              // [4] warp totals (cs scan)
-    float* s_rsum = s_wsum + 4;                             // [4] warp totals (d cs suffix scan)
-    float* s_dot = s_rsum + 4;                              // [4] <dS_out, S_out> per warp
-    float* s_da = s_dot + 4;                                // [4] dA per warp
-    uint64_t* bar_ld = reinterpret_cast<uint64_t*>(s_da + 4);  // C, B, S_in, S_out in
-    uint64_t* bar_ld2 = bar_ld + 1;                            // x, dy in
+    float* s_wsum = s_q2 + kQ;                              // [2][4] warp totals (cs scan)
+    float* s_rsum = s_wsum + 8;                             // [4] warp totals (d cs suffix scan)
+    float* s_dot = s_rsum + 8;                              // [8] <dS_out, S_out> per warp
+    float* s_da = s_dot + 8;                                // [4] dA per warp
+    float* s_pd = s_da + 8;                                 // [3][128] the second half's dots
+    uint64_t* bar_ld = reinterpret_cast<uint64_t*>(s_pd + 3 * kQ);  // C, B, S_in, S_out in
+    uint64_t* bar_ld2 = bar_ld + 1;                                  // x, dy in
     uint64_t* bar_mma = bar_ld + 2;  // [6] one per MMA group
     uint64_t* bar_fin = bar_ld + 8;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_ld + 9);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int row = tid;  // TMEM lane and block row
+    const int quarter = warp & 3;          // TMEM lane quarter this warp may access
+    const int part = warp >> 2;            // which half of each row's columns it takes
+    const int row = quarter * 32 + lane;   // TMEM lane and block row
     const int item = blockIdx.x;
     const int h = item % a.nheads, b = item / a.nheads;
     const int g = h / (a.nheads / a.ngroups);
@@ -247,15 +277,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
     bool ld_pending = nblocks > 0, ld2_pending = nblocks > 0;
     uint32_t ld_par = 0, ld2_par = 0;  // phase parity of the pending loads
 
-    // the adjoint state dS_out[p][n = row], carried from block to block
-    float dS[kP];
+    // the adjoint state dS_out[p = 32 part + q][n = row], carried from block to block
+    float dS[32];
 #pragma unroll
-    for (int p = 0; p < kP; ++p)
-        dS[p] = a.dfinal ? a.dfinal[((long long)item * kP + p) * kNs + row] : 0.0f;
+    for (int q = 0; q < 32; ++q)
+        dS[q] = a.dfinal ? a.dfinal[((long long)item * kP + 32 * part + q) * kNs + row] : 0.0f;
     float dA_acc = 0.0f;
     bool ok = true;
     uint32_t ph = 0;
@@ -278,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float u = __shfl_up_sync(0xffffffffu, v, o);
             if (lane >= o) v += u;
         }
-        if (lane == 31) s_wsum[warp] = v;
+        if (lane == 31) s_wsum[part * 4 + quarter] = v;
         // ---- S_in as the split operand [n = row][p]; <dS_out, S_out> for the
         // log-decay gradient of the block's last row
         {
@@ -287,40 +317,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             ld_pending = false;
         }
         {
-            const float* sin = reinterpret_cast<const float*>(smem + kSE) + row;
-            const float* sout = reinterpret_cast<const float*>(smem + kSDS) + row;
-            float sv[kP];
+            const float* sin = reinterpret_cast<const float*>(smem + kSE) + 32 * part * kNs + row;
+            const float* sout = reinterpret_cast<const float*>(smem + kSDS) + 32 * part * kNs + row;
+            float sv[32];
             float dot = 0.0f;
 #pragma unroll
-            for (int p = 0; p < kP; ++p) {
-                sv[p] = sin[p * kNs];
-                dot = fmaf(dS[p], sout[p * kNs], dot);
+            for (int q = 0; q < 32; ++q) {
+                sv[q] = sin[q * kNs];
+                dot = fmaf(dS[q], sout[q * kNs], dot);
             }
-            store_split_row(smem + kSS, row, sv);
+            store_split_half(smem + kSS, row, part, sv);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
             if (lane == 0) s_dot[warp] = dot;
         }
         __syncthreads();  // S_out read out of its region; warp sums visible
-        store_split_row(smem + kSDS, row, dS);  // dS_out over S_out
+        store_split_half(smem + kSDS, row, part, dS);  // dS_out over S_out
         float cs_last = 0.0f;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-            const float ws = s_wsum[w];
-            if (w < warp) v += ws;
+            const float ws = s_wsum[part * 4 + w];
+            if (w < quarter) v += ws;
             cs_last += ws;
         }
         const float cs2 = v * kLog2e, cs2_last = cs_last * kLog2e;
         float lg;
         asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(dtr));
         const float q2 = lg - cs2;
-        s_cs2[row] = cs2;
-        s_q2[row] = q2;
+        if (part == 0) {
+            s_cs2[row] = cs2;
+            s_q2[row] = q2;
+        }
         const float e_r = ex2_approx(cs2);
         const float eL_r = ex2_approx(cs2_last - cs2);
         const float u_r = dtr * eL_r;
         const float e_last = ex2_approx(cs2_last);
-        const float sdot = s_dot[0] + s_dot[1] + s_dot[2] + s_dot[3];
+        float sdot = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) sdot += s_dot[w];
         fence_proxy_async_smem();
         tc_fence_before();
 
@@ -354,14 +388,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                          kdesc<kQ>(sbase + kSS + 16384, kk), id128, 1);
             mma_commit(bar_mma + 0);
         }
-        // e^cs o dY as the split MN-major operand of dS_in^T (rows i, p contiguous),
-        // over the S_in region (read above)
+        // e^cs o dY as the split MN-major operand of dS_in^T (rows i, p
+        // contiguous), over the S_in region (read above)
         {
-            float dyv[kP];
-            load_tile_row64(smem + kSDY, row, dyv);
+            float dyv[32];
+            load_tile_half(smem + kSDY, row, part, dyv);
 #pragma unroll
-            for (int p = 0; p < kP; ++p) dyv[p] *= e_r;
-            store_split_row(smem + kSE, row, dyv);
+            for (int q = 0; q < 32; ++q) dyv[q] *= e_r;
+            store_split_half(smem + kSE, row, part, dyv);
         }
         {
             const bool got = mbar_wait(bar_mma + 0, ph, a.status);
@@ -369,21 +403,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         // (L o G)^T row j = row: columns i >= j, factor e^(cs_i - cs_j)
-        mask_row(t_lane + kTmGT, s_cs2, -cs2, row, kQ - 1);
+        mask_row_half(t_lane + kTmGT, s_cs2, -cs2, row, kQ - 1, part);
         // (L o T w) row i = row: columns j <= i, factor e^(cs_i - cs_j) dt_j
-        mask_row(t_lane + kTmT, s_q2, cs2, 0, row);
+        mask_row_half(t_lane + kTmT, s_q2, cs2, 0, row, part);
         // (L o T w)^T row j = row: columns i >= j, factor e^(cs_i - cs_j) dt_j
-        mask_row(t_lane + kTmTT, s_cs2, q2, row, kQ - 1);
+        mask_row_half(t_lane + kTmTT, s_cs2, q2, row, kQ - 1, part);
         // dY S_in scaled by e^cs_i
-#pragma unroll 1
-        for (int ck = 0; ck < 4; ++ck) {
-            float pv[32];
-            tmem_ld32(t_lane + kTmP + 32 * ck, pv);
-            tmem_wait_ld();
-#pragma unroll
-            for (int q = 0; q < 32; ++q) pv[q] *= e_r;
-            tmem_st32f(t_lane + kTmP + 32 * ck, pv);
-        }
+        scale_half(t_lane + kTmP, part, e_r);
         tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
@@ -420,36 +446,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                          kdesc<kQ>(sbase + kSDS + 16384, kk), id128, 1);
             mma_commit(bar_mma + 2);
         }
-        // dC row i: its log-decay term C_i . dC_i and its per-head partial
-        const float dcs_c = dot_row128_tmem(smem + kSC, row, t_lane + kTmP);
-        if (t < L) {
-            float* pc = a.pC + (((long long)h * a.batch + b) * L + t) * kNs;
-#pragma unroll 1
-            for (int ck = 0; ck < 4; ++ck) {
-                float cv[32];
-                tmem_ld32(t_lane + kTmP + 32 * ck, cv);
-                tmem_wait_ld();
-#pragma unroll
-                for (int q = 0; q < 32; q += 4)
-                    *reinterpret_cast<float4*>(pc + 32 * ck + q) =
-                        make_float4(cv[q], cv[q + 1], cv[q + 2], cv[q + 3]);
-            }
-        }
+        // dC row i: its log-decay term C_i . dC_i (this half) and its per-head partial
+        const float dcs_c = dot_half_tmem(
+            smem + kSC, row, part, t_lane + kTmP,
+            t < L ? a.pC + (((long long)h * a.batch + b) * L + t) * kNs : nullptr);
         {
             const bool got = mbar_wait(bar_mma + 2, ph, a.status);
             if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
         }
         tc_fence_after();
         // X dS_out row j scaled by dt_j e^(cs_last - cs_j)
-#pragma unroll 1
-        for (int ck = 0; ck < 4; ++ck) {
-            float qv[32];
-            tmem_ld32(t_lane + kTmT + 32 * ck, qv);
-            tmem_wait_ld();
-#pragma unroll
-            for (int q = 0; q < 32; ++q) qv[q] *= u_r;
-            tmem_st32f(t_lane + kTmT + 32 * ck, qv);
-        }
+        scale_half(t_lane + kTmT, part, u_r);
         tmem_wait_st();
         tc_fence_before();
         __syncthreads();
@@ -493,21 +500,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mma_commit(bar_mma + 4);
         }
-        // dB row j: its log-decay term B_j . dB_j and its per-head partial
-        const float dcs_b = dot_row128_tmem(smem + kSB, row, t_lane + kTmT);
-        if (t < L) {
-            float* pb = a.pB + (((long long)h * a.batch + b) * L + t) * kNs;
-#pragma unroll 1
-            for (int ck = 0; ck < 4; ++ck) {
-                float bv[32];
-                tmem_ld32(t_lane + kTmT + 32 * ck, bv);
-                tmem_wait_ld();
-#pragma unroll
-                for (int q = 0; q < 32; q += 4)
-                    *reinterpret_cast<float4*>(pb + 32 * ck + q) =
-                        make_float4(bv[q], bv[q + 1], bv[q + 2], bv[q + 3]);
-            }
-        }
+        // dB row j: its log-decay term B_j . dB_j (this half) and its per-head partial
+        const float dcs_b = dot_half_tmem(
+            smem + kSB, row, part, t_lane + kTmT,
+            t < L ? a.pB + (((long long)h * a.batch + b) * L + t) * kNs : nullptr);
         {
             const bool got = mbar_wait(bar_mma + 4, ph, a.status);
             if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
@@ -522,18 +518,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // B dS_out^T row j scaled by e^(cs_last - cs_j); the adjoint entering
         // the block: dS_in[p][n = row] = e^cs_last dS_out + (C^T (e^cs o dY))[n][p]
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        {
             float rv[32], sv[32];
-            tmem_ld32(t_lane + kTmR + 32 * half, rv);
-            tmem_ld32(t_lane + kTmDS + 32 * half, sv);
+            tmem_ld32(t_lane + kTmR + 32 * part, rv);
+            tmem_ld32(t_lane + kTmDS + 32 * part, sv);
             tmem_wait_ld();
 #pragma unroll
             for (int q = 0; q < 32; ++q) {
                 rv[q] *= eL_r;
-                dS[32 * half + q] = fmaf(e_last, dS[32 * half + q], sv[q]);
+                dS[q] = fmaf(e_last, dS[q], sv[q]);
             }
-            tmem_st32f(t_lane + kTmR + 32 * half, rv);
+            tmem_st32f(t_lane + kTmR + 32 * part, rv);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -560,41 +555,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dX_j = dt_j bracket_j; the input-weight part of ddt_j is x_j . bracket_j
         float dw = 0.0f;
         {
-            float xv[kP];
-            load_tile_row64(smem + kSX, row, xv);
-            float* dxr = a.dx + (((long long)b * L + t) * a.nheads + h) * kP;
+            float xv[32], br[32];
+            load_tile_half(smem + kSX, row, part, xv);
+            tmem_ld32(t_lane + kTmR + 32 * part, br);
+            tmem_wait_ld();
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float br[32];
-                tmem_ld32(t_lane + kTmR + 32 * half, br);
-                tmem_wait_ld();
+            for (int q = 0; q < 32; ++q) dw = fmaf(xv[q], br[q], dw);
+            if (t < L) {
+                float* dxr = a.dx + (((long long)b * L + t) * a.nheads + h) * kP + 32 * part;
 #pragma unroll
-                for (int q = 0; q < 32; ++q) dw = fmaf(xv[32 * half + q], br[q], dw);
-                if (t < L) {
-#pragma unroll
-                    for (int q = 0; q < 32; q += 4)
-                        *reinterpret_cast<float4*>(dxr + 32 * half + q) =
-                            make_float4(dtr * br[q], dtr * br[q + 1], dtr * br[q + 2], dtr * br[q + 3]);
-                }
+                for (int q = 0; q < 32; q += 4)
+                    *reinterpret_cast<float4*>(dxr + q) =
+                        make_float4(dtr * br[q], dtr * br[q + 1], dtr * br[q + 2], dtr * br[q + 3]);
             }
         }
-        // ---- log-decay gradient of each row, its suffix sums over the block,
-        // ddt and dA
-        float dcs = dcs_c - dcs_b + (row == kQ - 1 ? sdot : 0.0f);
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float u = __shfl_down_sync(0xffffffffu, dcs, o);
-            if (lane + o < 32) dcs += u;
+        // ---- log-decay gradient of each row (both halves' dots), its suffix
+        // sums over the block, ddt and dA (first warpgroup)
+        if (part == 1) {
+            s_pd[row] = dcs_c;
+            s_pd[kQ + row] = dcs_b;
+            s_pd[2 * kQ + row] = dw;
         }
-        if (lane == 0) s_rsum[warp] = dcs;
         tc_fence_before();
         __syncthreads();  // also: every read of this block's tiles and TMEM is done
+        float dcs = 0.0f, dw_all = 0.0f;
+        if (part == 0) {
+            dcs = (dcs_c + s_pd[row]) - (dcs_b + s_pd[kQ + row]) + (row == kQ - 1 ? sdot : 0.0f);
+            dw_all = dw + s_pd[2 * kQ + row];
 #pragma unroll
-        for (int w = 0; w < 4; ++w)
-            if (w > warp) dcs += s_rsum[w];
-        if (t < L) a.ddt[((long long)b * L + t) * a.nheads + h] = fmaf(Ah, dcs, dw);
-        dA_acc = fmaf(dtr, dcs, dA_acc);
-        __syncthreads();  // s_rsum, s_wsum, s_dot are rewritten by the next block
+            for (int o = 1; o < 32; o <<= 1) {
+                const float u = __shfl_down_sync(0xffffffffu, dcs, o);
+                if (lane + o < 32) dcs += u;
+            }
+            if (lane == 0) s_rsum[quarter] = dcs;
+        }
+        __syncthreads();
+        if (part == 0) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+                if (w > quarter) dcs += s_rsum[w];
+            if (t < L) a.ddt[((long long)b * L + t) * a.nheads + h] = fmaf(Ah, dcs, dw_all);
+            dA_acc = fmaf(dtr, dcs, dA_acc);
+        }
+        __syncthreads();  // s_rsum, s_wsum, s_dot, s_pd are rewritten by the next block
         if (tid == 0 && blk > 0) load_xdy(blk - 1);  // x was read above, dy by group 6
         if (blk > 0) {
             ld2_pending = true;
@@ -605,11 +608,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
         if (a.dh0) {
 #pragma unroll
-            for (int p = 0; p < kP; ++p) a.dh0[((long long)item * kP + p) * kNs + row] = dS[p];
+            for (int q = 0; q < 32; ++q)
+                a.dh0[((long long)item * kP + 32 * part + q) * kNs + row] = dS[q];
         }
+        if (part == 0) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) dA_acc += __shfl_xor_sync(0xffffffffu, dA_acc, o);
-        if (lane == 0) s_da[warp] = dA_acc;
+            for (int o = 16; o > 0; o >>= 1) dA_acc += __shfl_xor_sync(0xffffffffu, dA_acc, o);
+            if (lane == 0) s_da[quarter] = dA_acc;
+        }
         __syncthreads();
         if (tid == 0) a.pA[item] = s_da[0] + s_da[1] + s_da[2] + s_da[3];
     } else if (tid == 0) {
