@@ -41,7 +41,8 @@ namespace {
 using namespace ssm;
 using namespace ssd_detail;
 
-constexpr int kThreads = 256;  // two warpgroups, each taking half of every row
+constexpr int kWorkers = 256;              // two warpgroups: thread (row, half of the row)
+constexpr int kThreads = kWorkers + 32;   // + the issuing warp (TMA loads, MMAs)
 
 // Shared memory (offsets from the 1024-aligned base)
 constexpr uint32_t kSC = 0;         // C tile [128 i][128 n] (two 64-n boxes, 16 KB apart)
@@ -52,16 +53,16 @@ constexpr uint32_t kSS = 98304;     // S_in hi | lo [128 n][64 p]
 constexpr uint32_t kSDS = 131072;   // dS_out hi | lo [128 n][64 p]
 constexpr uint32_t kSE = 163840;    // (e^cs o dY) hi | lo [128 i][64 p]
 constexpr uint32_t kMisc = 196608;  // cs2[128], q2[128], sums, mbarriers, TMEM address
-constexpr uint32_t kMiscBytes = (2 * 128 + 32 + 3 * 128) * 4 + 9 * 8 + 16;
+constexpr int kNumBars = 18;
+constexpr uint32_t kMiscBytes = (2 * 128 + 32 + 3 * 128) * 4 + kNumBars * 8 + 16;
 constexpr uint32_t kSmemAlloc = kMisc + kMiscBytes + 1024;  // + realignment slack
 
 // TMEM columns (one CTA per SM: all 512)
-constexpr uint32_t kTmGT = 0;    // G^T = B C^T -> (L o G)^T hi/lo
-constexpr uint32_t kTmT = 128;   // T = dY X^T -> (L o T w) hi/lo; then dB
-constexpr uint32_t kTmTT = 256;  // T^T -> (L o T w)^T hi/lo; then bracket (64) | dS_in^T (64)
-constexpr uint32_t kTmR = 256;
-constexpr uint32_t kTmDS = 320;
-constexpr uint32_t kTmP = 384;   // dY S_in -> dC
+constexpr uint32_t kTmT = 0;     // T = dY X^T -> (L o T w) hi/lo; then Q -> dB
+constexpr uint32_t kTmP = 128;   // P = dY S_in -> dC
+constexpr uint32_t kTmGT = 256;  // G^T = B C^T -> (L o G)^T hi/lo; then T^T -> (L o T w)^T hi/lo
+constexpr uint32_t kTmR = 384;   // R = B dS_out^T -> bracket (64)
+constexpr uint32_t kTmDS = 448;  // dS_in^T (64)
 constexpr uint32_t kTmemCols = 512;
 
 struct BwdArgs {
@@ -72,8 +73,8 @@ struct BwdArgs {
     float* dx;             // (batch, seqlen, nheads, 64)
     float* ddt;            // (batch, seqlen, nheads)
     float* dh0;            // (batch, nheads, 64, 128) or NULL
-    float* pB;             // [nheads][batch][seqlen][128] per-head dB
-    float* pC;             // [nheads][batch][seqlen][128] per-head dC
+    float* pB;             // [nheads][batch][128][seqlen] per-head dB
+    float* pC;             // [nheads][batch][128][seqlen] per-head dC
     float* pA;             // [batch * nheads]
     uint32_t* status;
     int batch, seqlen, nheads, ngroups;
@@ -157,9 +158,10 @@ __device__ __forceinline__ void load_tile_half(const uint8_t* tile, int row, int
 // This warpgroup's half of a dot product: row r of a TMA tile [128][128] (two
 // 64-wide boxes 16 KB apart; box `part` holds columns 64 part .. + 63) against
 // the same 64 fp32 columns of TMEM row r, 32 at a time; optionally the 64
-// values are also stored to dst (global, 16-byte aligned).
+// values are also stored, column n at dst[n * stride] (the rows of a warp are
+// consecutive in dst, so each store is coalesced).
 __device__ __forceinline__ float dot_half_tmem(const uint8_t* tile, int row, int part,
-                                               uint32_t taddr, float* dst) {
+                                               uint32_t taddr, float* dst, long long stride) {
     const uint8_t* box = tile + part * 16384 + row * 128;
     float acc = 0.0f;
 #pragma unroll 1
@@ -178,10 +180,9 @@ __device__ __forceinline__ float dot_half_tmem(const uint8_t* tile, int row, int
                            fmaf(bf16hi(ww[e]), v[8 * c + 2 * e + 1], acc));
         }
         if (dst) {
+            float* d = dst + (64 * part + 32 * hh) * stride;
 #pragma unroll
-            for (int q = 0; q < 32; q += 4)
-                *reinterpret_cast<float4*>(dst + 64 * part + 32 * hh + q) =
-                    make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+            for (int q = 0; q < 32; ++q) d[q * stride] = v[q];
         }
     }
     return acc;
@@ -222,441 +223,458 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* s_dot = s_rsum + 8;                              // [8] <dS_out, S_out> per warp
     float* s_da = s_dot + 8;                                // [4] dA per warp
     float* s_pd = s_da + 8;                                 // [3][128] the second half's dots
-    uint64_t* bar_ld = reinterpret_cast<uint64_t*>(s_pd + 3 * kQ);  // C, B, S_in, S_out in
-    uint64_t* bar_ld2 = bar_ld + 1;                                  // x, dy in
-    uint64_t* bar_mma = bar_ld + 2;  // [6] one per MMA group
-    uint64_t* bar_fin = bar_ld + 8;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_ld + 9);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_pd + 3 * kQ);
+    uint64_t* bar_cb = bars + 0;   // TMA: C, B in
+    uint64_t* bar_s = bars + 1;    // bulk: S_in, S_out in
+    uint64_t* bar_xy = bars + 2;   // TMA: x, dy in
+    uint64_t* bar_fin = bars + 3;  // issuer: every MMA done (at exit)
+    uint64_t* m_tp = bars + 4;     // MMA done: T, P
+    uint64_t* m_rs = bars + 5;     // MMA done: R, dS_in^T
+    uint64_t* m_gt = bars + 6;     // MMA done: G^T
+    uint64_t* m_dc = bars + 7;     // MMA done: dC
+    uint64_t* m_br = bars + 8;     // MMA done: bracket
+    uint64_t* m_q = bars + 9;      // MMA done: Q = X dS_out
+    uint64_t* m_tt = bars + 10;    // MMA done: T^T
+    uint64_t* m_db = bars + 11;    // MMA done: dB
+    uint64_t* r_op = bars + 12;    // workers: the block's shared-memory operands written
+    uint64_t* r_dc = bars + 13;    // workers: (L o T w) and e^cs P in TMEM
+    uint64_t* r_br = bars + 14;    // workers: (L o G)^T and the scaled R in TMEM
+    uint64_t* r_db = bars + 15;    // workers: (L o T w)^T and the scaled Q in TMEM
+    uint64_t* r_x = bars + 16;     // workers: done reading the x tile
+    uint64_t* r_cb = bars + 17;    // workers: done reading the C and B tiles
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + kNumBars);
+    volatile uint32_t* s_abort = s_tmem + 1;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3;          // TMEM lane quarter this warp may access
-    const int part = warp >> 2;            // which half of each row's columns it takes
-    const int row = quarter * 32 + lane;   // TMEM lane and block row
     const int item = blockIdx.x;
     const int h = item % a.nheads, b = item / a.nheads;
     const int g = h / (a.nheads / a.ngroups);
     const int L = a.seqlen;
     const int nblocks = (L + kQ - 1) / kQ;
-    const float Ah = a.A[h];
     const float* bs_item = a.bstates + (long long)item * (nblocks + 1) * kP * kNs;
-
-    // Loads of block blk (thread 0): C, B and the states entering and leaving it
-    // (fp32 [p][n], into the regions their split forms replace), then x and dy.
-    auto load_cbs = [&](int blk) {
-        mbar_arrive_expect_tx(bar_ld, 4 * 32768);
-        tma_load_4d(smem + kSC, &tm_C, bar_ld, 0, g, blk * kQ, b);
-        tma_load_4d(smem + kSC + 16384, &tm_C, bar_ld, 64, g, blk * kQ, b);
-        tma_load_4d(smem + kSB, &tm_B, bar_ld, 0, g, blk * kQ, b);
-        tma_load_4d(smem + kSB + 16384, &tm_B, bar_ld, 64, g, blk * kQ, b);
-        bulk_load(smem + kSE, bs_item + (long long)blk * kP * kNs, 32768, bar_ld);
-        bulk_load(smem + kSDS, bs_item + (long long)(blk + 1) * kP * kNs, 32768, bar_ld);
-    };
-    auto load_xdy = [&](int blk) {
-        mbar_arrive_expect_tx(bar_ld2, 2 * 16384);
-        tma_load_3d(smem + kSX, &tm_x, bar_ld2, h * kP, blk * kQ, b);
-        tma_load_3d(smem + kSDY, &tm_dy, bar_ld2, h * kP, blk * kQ, b);
-    };
 
     if (warp == 0) tmem_alloc(s_tmem, kTmemCols);
     if (tid == 0) {
-        mbar_init(bar_ld, 1);
-        mbar_init(bar_ld2, 1);
-        for (int k = 0; k < 6; ++k) mbar_init(bar_mma + k, 1);
-        mbar_init(bar_fin, 1);
+        for (int k = 0; k < 12; ++k) mbar_init(bars + k, 1);
+        for (int k = 12; k < kNumBars; ++k) mbar_init(bars + k, kWorkers);
+        *s_abort = 0u;
         fence_mbar_init();
-        prefetch_tensormap(&tm_C);
-        prefetch_tensormap(&tm_B);
-        prefetch_tensormap(&tm_x);
-        prefetch_tensormap(&tm_dy);
-        if (nblocks > 0) {
-            load_cbs(nblocks - 1);
-            load_xdy(nblocks - 1);
-        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
-    bool ld_pending = nblocks > 0, ld2_pending = nblocks > 0;
-    uint32_t ld_par = 0, ld2_par = 0;  // phase parity of the pending loads
 
-    // the adjoint state dS_out[p = 32 part + q][n = row], carried from block to block
-    float dS[32];
-#pragma unroll
-    for (int q = 0; q < 32; ++q)
-        dS[q] = a.dfinal ? a.dfinal[((long long)item * kP + 32 * part + q) * kNs + row] : 0.0f;
-    float dA_acc = 0.0f;
-    bool ok = true;
-    uint32_t ph = 0;
-    auto dt_of = [&](int blk) {
-        const int t = blk * kQ + row;
-        return t < L ? a.dt[((long long)b * L + t) * a.nheads + h] : 0.0f;
-    };
-    float dt_next = nblocks > 0 ? dt_of(nblocks - 1) : 0.0f;
-
-    for (int blk = nblocks - 1; blk >= 0; --blk, ph ^= 1u) {
-        const int t0 = blk * kQ;
-        const int t = t0 + row;
-        const float dtr = dt_next;
-        if (blk > 0) dt_next = dt_of(blk - 1);
-
-        // ---- cumulative log-decay within the block (warp part)
-        float v = dtr * Ah;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float u = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += u;
-        }
-        if (lane == 31) s_wsum[part * 4 + quarter] = v;
-        // ---- S_in as the split operand [n = row][p]; <dS_out, S_out> for the
-        // log-decay gradient of the block's last row
-        {
-            const bool got = mbar_wait(bar_ld, ph, a.status);
-            if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
-            ld_pending = false;
-        }
-        {
-            const float* sin = reinterpret_cast<const float*>(smem + kSE) + 32 * part * kNs + row;
-            const float* sout = reinterpret_cast<const float*>(smem + kSDS) + 32 * part * kNs + row;
-            float sv[32];
-            float dot = 0.0f;
-#pragma unroll
-            for (int q = 0; q < 32; ++q) {
-                sv[q] = sin[q * kNs];
-                dot = fmaf(dS[q], sout[q * kNs], dot);
+    if (warp == kWorkers / 32) {
+        // ================= issuing warp: TMA loads and MMAs (one lane)
+        if (lane == 0) {
+            prefetch_tensormap(&tm_C);
+            prefetch_tensormap(&tm_B);
+            prefetch_tensormap(&tm_x);
+            prefetch_tensormap(&tm_dy);
+            auto load_cb = [&](int blk) {
+                mbar_arrive_expect_tx(bar_cb, 2 * 32768);
+                tma_load_4d(smem + kSC, &tm_C, bar_cb, 0, g, blk * kQ, b);
+                tma_load_4d(smem + kSC + 16384, &tm_C, bar_cb, 64, g, blk * kQ, b);
+                tma_load_4d(smem + kSB, &tm_B, bar_cb, 0, g, blk * kQ, b);
+                tma_load_4d(smem + kSB + 16384, &tm_B, bar_cb, 64, g, blk * kQ, b);
+            };
+            auto load_s = [&](int blk) {
+                mbar_arrive_expect_tx(bar_s, 2 * 32768);
+                bulk_load(smem + kSE, bs_item + (long long)blk * kP * kNs, 32768, bar_s);
+                bulk_load(smem + kSDS, bs_item + (long long)(blk + 1) * kP * kNs, 32768, bar_s);
+            };
+            auto load_xy = [&](int blk) {
+                mbar_arrive_expect_tx(bar_xy, 2 * 16384);
+                tma_load_3d(smem + kSX, &tm_x, bar_xy, h * kP, blk * kQ, b);
+                tma_load_3d(smem + kSDY, &tm_dy, bar_xy, h * kP, blk * kQ, b);
+            };
+            // pending load phases (parity), -1 when none
+            int p_cb = -1, p_s = -1, p_xy = -1;
+            if (nblocks > 0) {
+                load_cb(nblocks - 1);
+                load_s(nblocks - 1);
+                load_xy(nblocks - 1);
+                p_cb = p_s = p_xy = 0;
             }
-            store_split_half(smem + kSS, row, part, sv);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-            if (lane == 0) s_dot[warp] = dot;
-        }
-        __syncthreads();  // S_out read out of its region; warp sums visible
-        store_split_half(smem + kSDS, row, part, dS);  // dS_out over S_out
-        float cs_last = 0.0f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const float ws = s_wsum[part * 4 + w];
-            if (w < quarter) v += ws;
-            cs_last += ws;
-        }
-        const float cs2 = v * kLog2e, cs2_last = cs_last * kLog2e;
-        float lg;
-        asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(dtr));
-        const float q2 = lg - cs2;
-        if (part == 0) {
-            s_cs2[row] = cs2;
-            s_q2[row] = q2;
-        }
-        const float e_r = ex2_approx(cs2);
-        const float eL_r = ex2_approx(cs2_last - cs2);
-        const float u_r = dtr * eL_r;
-        const float e_last = ex2_approx(cs2_last);
-        float sdot = 0.0f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) sdot += s_dot[w];
-        fence_proxy_async_smem();
-        tc_fence_before();
-
-        // ---- group 1: G^T = B C^T, T = dY X^T, T^T = X dY^T, P = dY S_in
-        {
-            const bool got = mbar_wait(bar_ld2, ph, a.status);
-            if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
-            ld2_pending = false;
-        }
-        if (tid == 0) {
-            tc_fence_after();
+            uint32_t ph = 0;
             constexpr uint32_t id128 = idesc_bf16_f32(128, 128);
+            constexpr uint32_t id128b = idesc_bf16_f32(128, 128) | kIdescBMN;
+            constexpr uint32_t id64b = idesc_bf16_f32(128, 64) | kIdescBMN;
+            constexpr uint32_t id64ab = idesc_bf16_f32(128, 64) | kIdescAMN | kIdescBMN;
+            for (int blk = nblocks - 1; blk >= 0; --blk, ph ^= 1u) {
+                auto W = [&](uint64_t* bar) {
+                    if (*s_abort) return false;
+                    if (!mbar_wait(bar, ph, a.status)) {
+                        *s_abort = 1u;
+                        return false;
+                    }
+                    return true;
+                };
+                if (!W(bar_cb) || !W(bar_s) || !W(bar_xy)) break;
+                p_cb = p_s = p_xy = -1;
+                if (!W(r_op)) break;
+                tc_fence_after();
+                // T = dY X^T, P = dY S_in (hi + lo)
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tmem + kTmGT, kdesc<kQ>(sbase + kSB, kk), kdesc<kQ>(sbase + kSC, kk), id128,
-                         kk > 0);
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + kTmT, kdesc<kQ>(sbase + kSDY, kk), kdesc<kQ>(sbase + kSX, kk),
+                             id128, kk > 0);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                mma_bf16(tmem + kTmT, kdesc<kQ>(sbase + kSDY, kk), kdesc<kQ>(sbase + kSX, kk), id128,
-                         kk > 0);
-                mma_bf16(tmem + kTmTT, kdesc<kQ>(sbase + kSX, kk), kdesc<kQ>(sbase + kSDY, kk), id128,
-                         kk > 0);
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tmem + kTmP, kdesc<kQ>(sbase + kSDY, kk & 3),
+                             kdesc<kQ>(sbase + kSS + (kk >> 2) * 16384, kk & 3), id128, kk > 0);
+                mma_commit(m_tp);
+                // R = B dS_out^T (hi + lo), dS_in^T = C^T (e^cs o dY) (hi + lo)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    mma_bf16(tmem + kTmR, kdesc<kQ>(sbase + kSB, kk), mdesc(sbase + kSDS, kk, 16384),
+                             id64b, kk > 0);
+                    mma_bf16(tmem + kTmR, kdesc<kQ>(sbase + kSB, kk),
+                             mdesc(sbase + kSDS + 16384, kk, 16384), id64b, 1);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    mma_bf16(tmem + kTmDS, mdesc(sbase + kSC, kk, 16384),
+                             mdesc(sbase + kSE, kk, 16384), id64ab, kk > 0);
+                    mma_bf16(tmem + kTmDS, mdesc(sbase + kSC, kk, 16384),
+                             mdesc(sbase + kSE + 16384, kk, 16384), id64ab, 1);
+                }
+                mma_commit(m_rs);
+                // G^T = B C^T
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tmem + kTmGT, kdesc<kQ>(sbase + kSB, kk), kdesc<kQ>(sbase + kSC, kk),
+                             id128, kk > 0);
+                mma_commit(m_gt);
+                // dC = e^cs o P + (L o T w) B
+                if (!W(r_dc)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    mma_bf16_ta(tmem + kTmP, tmem + kTmT + mcol_hi(kk), mdesc(sbase + kSB, kk, 16384),
+                                id128b, 1);
+                    mma_bf16_ta(tmem + kTmP, tmem + kTmT + mcol_hi(kk) + 16,
+                                mdesc(sbase + kSB, kk, 16384), id128b, 1);
+                }
+                mma_commit(m_dc);
+                // bracket = e^(cs_last - cs) o R + (L o G)^T dY
+                if (!W(r_br)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    mma_bf16_ta(tmem + kTmR, tmem + kTmGT + mcol_hi(kk), mdesc(sbase + kSDY, kk, 16384),
+                                id64b, 1);
+                    mma_bf16_ta(tmem + kTmR, tmem + kTmGT + mcol_hi(kk) + 16,
+                                mdesc(sbase + kSDY, kk, 16384), id64b, 1);
+                }
+                mma_commit(m_br);
+                // Q = X dS_out (hi + lo) into the consumed (L o T w) columns
+                if (!W(m_dc)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tmem + kTmT, kdesc<kQ>(sbase + kSX, kk & 3),
+                             kdesc<kQ>(sbase + kSDS + (kk >> 2) * 16384, kk & 3), id128, kk > 0);
+                mma_commit(m_q);
+                // T^T = X dY^T into the consumed (L o G)^T columns
+                if (!W(m_br)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + kTmGT, kdesc<kQ>(sbase + kSX, kk), kdesc<kQ>(sbase + kSDY, kk),
+                             id128, kk > 0);
+                mma_commit(m_tt);
+                if (blk > 0) {
+                    // the states' regions are free once Q (their last reader) is done
+                    if (!W(m_q)) break;
+                    load_s(blk - 1);
+                    p_s = (int)(ph ^ 1u);
+                }
+                // dB = dt e^(cs_last - cs) o Q + (L o T w)^T C
+                if (!W(r_db)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    mma_bf16_ta(tmem + kTmT, tmem + kTmGT + mcol_hi(kk), mdesc(sbase + kSC, kk, 16384),
+                                id128b, 1);
+                    mma_bf16_ta(tmem + kTmT, tmem + kTmGT + mcol_hi(kk) + 16,
+                                mdesc(sbase + kSC, kk, 16384), id128b, 1);
+                }
+                mma_commit(m_db);
+                if (blk > 0) {
+                    // x and dy once T^T and the workers' x reads are done; C and B
+                    // once dB and the workers' dC, dB dots are
+                    if (!W(m_tt) || !W(r_x)) break;
+                    load_xy(blk - 1);
+                    p_xy = (int)(ph ^ 1u);
+                    if (!W(m_db) || !W(r_cb)) break;
+                    load_cb(blk - 1);
+                    p_cb = (int)(ph ^ 1u);
+                }
             }
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + kTmP, kdesc<kQ>(sbase + kSDY, kk), kdesc<kQ>(sbase + kSS, kk), id128,
-                         kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + kTmP, kdesc<kQ>(sbase + kSDY, kk),
-                         kdesc<kQ>(sbase + kSS + 16384, kk), id128, 1);
-            mma_commit(bar_mma + 0);
+            // never leave with an MMA or a load in flight (bounded waits)
+            mma_commit(bar_fin);
+            (void)mbar_wait(bar_fin, 0, nullptr);
+            if (p_cb >= 0) (void)mbar_wait(bar_cb, (uint32_t)p_cb, nullptr);
+            if (p_s >= 0) (void)mbar_wait(bar_s, (uint32_t)p_s, nullptr);
+            if (p_xy >= 0) (void)mbar_wait(bar_xy, (uint32_t)p_xy, nullptr);
         }
-        // e^cs o dY as the split MN-major operand of dS_in^T (rows i, p
-        // contiguous), over the S_in region (read above)
-        {
-            float dyv[32];
-            load_tile_half(smem + kSDY, row, part, dyv);
+    } else {
+        // ================= worker warpgroups: thread (row, part)
+        const int quarter = warp & 3;         // TMEM lane quarter this warp may access
+        const int part = warp >> 2;           // which half of each row's columns it takes
+        const int row = quarter * 32 + lane;  // TMEM lane and block row
+        const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+        const float Ah = a.A[h];
+        // the adjoint state dS_out[p = 32 part + q][n = row], carried from block to block
+        float dS[32];
 #pragma unroll
-            for (int q = 0; q < 32; ++q) dyv[q] *= e_r;
-            store_split_half(smem + kSE, row, part, dyv);
-        }
-        {
-            const bool got = mbar_wait(bar_mma + 0, ph, a.status);
-            if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
-        }
-        tc_fence_after();
-        // (L o G)^T row j = row: columns i >= j, factor e^(cs_i - cs_j)
-        mask_row_half(t_lane + kTmGT, s_cs2, -cs2, row, kQ - 1, part);
-        // (L o T w) row i = row: columns j <= i, factor e^(cs_i - cs_j) dt_j
-        mask_row_half(t_lane + kTmT, s_q2, cs2, 0, row, part);
-        // (L o T w)^T row j = row: columns i >= j, factor e^(cs_i - cs_j) dt_j
-        mask_row_half(t_lane + kTmTT, s_cs2, q2, row, kQ - 1, part);
-        // dY S_in scaled by e^cs_i
-        scale_half(t_lane + kTmP, part, e_r);
-        tmem_wait_st();
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
+        for (int q = 0; q < 32; ++q)
+            dS[q] = a.dfinal ? a.dfinal[((long long)item * kP + 32 * part + q) * kNs + row] : 0.0f;
+        float dA_acc = 0.0f;
+        bool ok = true;
+        uint32_t ph = 0;
+        auto dt_of = [&](int blk) {
+            const int t = blk * kQ + row;
+            return t < L ? a.dt[((long long)b * L + t) * a.nheads + h] : 0.0f;
+        };
+        float dt_next = nblocks > 0 ? dt_of(nblocks - 1) : 0.0f;
+        // per-head dB, dC partials: [h][b][n][t], t contiguous (coalesced across a warp's rows)
+        const long long pofs = ((long long)h * a.batch + b) * kNs * L;
 
-        // ---- group 2: dC = e^cs o (dY S_in) + (L o T w) B
-        if (tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t idC = idesc_bf16_f32(128, 128) | kIdescBMN;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                mma_bf16_ta(tmem + kTmP, tmem + kTmT + mcol_hi(kk), mdesc(sbase + kSB, kk, 16384),
-                            idC, 1);
-                mma_bf16_ta(tmem + kTmP, tmem + kTmT + mcol_hi(kk) + 16,
-                            mdesc(sbase + kSB, kk, 16384), idC, 1);
-            }
-            mma_commit(bar_mma + 1);
-        }
-        {
-            const bool got = mbar_wait(bar_mma + 1, ph, a.status);
-            if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
-        }
-        tc_fence_after();
-        // ---- group 3 (the (L o T w) operand is consumed): Q = X dS_out into its place
-        if (tid == 0) {
-            constexpr uint32_t id128 = idesc_bf16_f32(128, 128);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + kTmT, kdesc<kQ>(sbase + kSX, kk), kdesc<kQ>(sbase + kSDS, kk), id128,
-                         kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + kTmT, kdesc<kQ>(sbase + kSX, kk),
-                         kdesc<kQ>(sbase + kSDS + 16384, kk), id128, 1);
-            mma_commit(bar_mma + 2);
-        }
-        // dC row i: its log-decay term C_i . dC_i (this half) and its per-head partial
-        const float dcs_c = dot_half_tmem(
-            smem + kSC, row, part, t_lane + kTmP,
-            t < L ? a.pC + (((long long)h * a.batch + b) * L + t) * kNs : nullptr);
-        {
-            const bool got = mbar_wait(bar_mma + 2, ph, a.status);
-            if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
-        }
-        tc_fence_after();
-        // X dS_out row j scaled by dt_j e^(cs_last - cs_j)
-        scale_half(t_lane + kTmT, part, u_r);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncthreads();
+        for (int blk = nblocks - 1; blk >= 0; --blk, ph ^= 1u) {
+            // bounded wait on `bar`, agreed by all workers (all leave together)
+            auto Wc = [&](uint64_t* bar) {
+                bool got = !*s_abort && mbar_wait(bar, ph, a.status);
+                if (!got) *s_abort = 1u;
+                return named_bar_and(1, kWorkers, got);
+            };
+            const int t = blk * kQ + row;
+            const float dtr = dt_next;
+            if (blk > 0) dt_next = dt_of(blk - 1);
 
-        // ---- group 4: dB = dt e^(cs_last - cs) o (X dS_out) + (L o T w)^T C
-        if (tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t idB = idesc_bf16_f32(128, 128) | kIdescBMN;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                mma_bf16_ta(tmem + kTmT, tmem + kTmTT + mcol_hi(kk), mdesc(sbase + kSC, kk, 16384),
-                            idB, 1);
-                mma_bf16_ta(tmem + kTmT, tmem + kTmTT + mcol_hi(kk) + 16,
-                            mdesc(sbase + kSC, kk, 16384), idB, 1);
-            }
-            mma_commit(bar_mma + 3);
-        }
-        {
-            const bool got = mbar_wait(bar_mma + 3, ph, a.status);
-            if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
-        }
-        tc_fence_after();
-        // ---- group 5 (the (L o T w)^T operand is consumed): R = B dS_out^T and
-        // dS_in^T = C^T (e^cs o dY) into its place, N = 64 each
-        if (tid == 0) {
-            constexpr uint32_t idR = idesc_bf16_f32(128, 64) | kIdescBMN;
-            constexpr uint32_t idS = idesc_bf16_f32(128, 64) | kIdescAMN | kIdescBMN;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                mma_bf16(tmem + kTmR, kdesc<kQ>(sbase + kSB, kk), mdesc(sbase + kSDS, kk, 16384),
-                         idR, kk > 0);
-                mma_bf16(tmem + kTmR, kdesc<kQ>(sbase + kSB, kk),
-                         mdesc(sbase + kSDS + 16384, kk, 16384), idR, 1);
-            }
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                mma_bf16(tmem + kTmDS, mdesc(sbase + kSC, kk, 16384), mdesc(sbase + kSE, kk, 16384),
-                         idS, kk > 0);
-                mma_bf16(tmem + kTmDS, mdesc(sbase + kSC, kk, 16384),
-                         mdesc(sbase + kSE + 16384, kk, 16384), idS, 1);
-            }
-            mma_commit(bar_mma + 4);
-        }
-        // dB row j: its log-decay term B_j . dB_j (this half) and its per-head partial
-        const float dcs_b = dot_half_tmem(
-            smem + kSB, row, part, t_lane + kTmT,
-            t < L ? a.pB + (((long long)h * a.batch + b) * L + t) * kNs : nullptr);
-        {
-            const bool got = mbar_wait(bar_mma + 4, ph, a.status);
-            if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
-        }
-        tc_fence_after();
-        // C, B, S_in's and S_out's regions are free (group 5 was their last
-        // reader): the previous block's loads start now
-        if (tid == 0 && blk > 0) load_cbs(blk - 1);
-        if (blk > 0) {
-            ld_pending = true;
-            ld_par = ph ^ 1u;
-        }
-        // B dS_out^T row j scaled by e^(cs_last - cs_j); the adjoint entering
-        // the block: dS_in[p][n = row] = e^cs_last dS_out + (C^T (e^cs o dY))[n][p]
-        {
-            float rv[32], sv[32];
-            tmem_ld32(t_lane + kTmR + 32 * part, rv);
-            tmem_ld32(t_lane + kTmDS + 32 * part, sv);
-            tmem_wait_ld();
-#pragma unroll
-            for (int q = 0; q < 32; ++q) {
-                rv[q] *= eL_r;
-                dS[q] = fmaf(e_last, dS[q], sv[q]);
-            }
-            tmem_st32f(t_lane + kTmR + 32 * part, rv);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncthreads();
-
-        // ---- group 6: bracket = e^(cs_last - cs) o (B dS_out^T) + (L o G)^T dY
-        if (tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t idX = idesc_bf16_f32(128, 64) | kIdescBMN;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                mma_bf16_ta(tmem + kTmR, tmem + kTmGT + mcol_hi(kk), mdesc(sbase + kSDY, kk, 16384),
-                            idX, 1);
-                mma_bf16_ta(tmem + kTmR, tmem + kTmGT + mcol_hi(kk) + 16,
-                            mdesc(sbase + kSDY, kk, 16384), idX, 1);
-            }
-            mma_commit(bar_mma + 5);
-        }
-        {
-            const bool got = mbar_wait(bar_mma + 5, ph, a.status);
-            if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
-        }
-        tc_fence_after();
-        // dX_j = dt_j bracket_j; the input-weight part of ddt_j is x_j . bracket_j
-        float dw = 0.0f;
-        {
-            float xv[32], br[32];
-            load_tile_half(smem + kSX, row, part, xv);
-            tmem_ld32(t_lane + kTmR + 32 * part, br);
-            tmem_wait_ld();
-#pragma unroll
-            for (int q = 0; q < 32; ++q) dw = fmaf(xv[q], br[q], dw);
-            if (t < L) {
-                float* dxr = a.dx + (((long long)b * L + t) * a.nheads + h) * kP + 32 * part;
-#pragma unroll
-                for (int q = 0; q < 32; q += 4)
-                    *reinterpret_cast<float4*>(dxr + q) =
-                        make_float4(dtr * br[q], dtr * br[q + 1], dtr * br[q + 2], dtr * br[q + 3]);
-            }
-        }
-        // ---- log-decay gradient of each row (both halves' dots), its suffix
-        // sums over the block, ddt and dA (first warpgroup)
-        if (part == 1) {
-            s_pd[row] = dcs_c;
-            s_pd[kQ + row] = dcs_b;
-            s_pd[2 * kQ + row] = dw;
-        }
-        tc_fence_before();
-        __syncthreads();  // also: every read of this block's tiles and TMEM is done
-        float dcs = 0.0f, dw_all = 0.0f;
-        if (part == 0) {
-            dcs = (dcs_c + s_pd[row]) - (dcs_b + s_pd[kQ + row]) + (row == kQ - 1 ? sdot : 0.0f);
-            dw_all = dw + s_pd[2 * kQ + row];
+            // ---- cumulative log-decay within the block
+            float v = dtr * Ah;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const float u = __shfl_down_sync(0xffffffffu, dcs, o);
-                if (lane + o < 32) dcs += u;
+                const float u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
             }
-            if (lane == 0) s_rsum[quarter] = dcs;
-        }
-        __syncthreads();
-        if (part == 0) {
+            if (lane == 31) s_wsum[part * 4 + quarter] = v;
+            if (!Wc(bar_cb) || !Wc(bar_s) || !Wc(bar_xy)) { ok = false; break; }
+            float cs_last = 0.0f;
 #pragma unroll
-            for (int w = 0; w < 4; ++w)
-                if (w > quarter) dcs += s_rsum[w];
-            if (t < L) a.ddt[((long long)b * L + t) * a.nheads + h] = fmaf(Ah, dcs, dw_all);
-            dA_acc = fmaf(dtr, dcs, dA_acc);
-        }
-        __syncthreads();  // s_rsum, s_wsum, s_dot, s_pd are rewritten by the next block
-        if (tid == 0 && blk > 0) load_xdy(blk - 1);  // x was read above, dy by group 6
-        if (blk > 0) {
-            ld2_pending = true;
-            ld2_par = ph ^ 1u;
-        }
-    }
+            for (int w = 0; w < 4; ++w) {
+                const float ws = s_wsum[part * 4 + w];
+                if (w < quarter) v += ws;
+                cs_last += ws;
+            }
+            const float cs2 = v * kLog2e, cs2_last = cs_last * kLog2e;
+            float lg;
+            asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(dtr));
+            const float q2 = lg - cs2;
+            if (part == 0) {
+                s_cs2[row] = cs2;
+                s_q2[row] = q2;
+            }
+            const float e_r = ex2_approx(cs2);
+            const float eL_r = ex2_approx(cs2_last - cs2);
+            const float u_r = dtr * eL_r;
+            const float e_last = ex2_approx(cs2_last);
 
-    if (ok) {
-        if (a.dh0) {
+            // ---- S_in split [n = row][p]; <dS_out, S_out>; then dS_out and
+            // e^cs o dY split over the fp32 states' regions
+            {
+                const float* sin = reinterpret_cast<const float*>(smem + kSE) + 32 * part * kNs + row;
+                const float* sout = reinterpret_cast<const float*>(smem + kSDS) + 32 * part * kNs + row;
+                float sv[32];
+                float dot = 0.0f;
 #pragma unroll
-            for (int q = 0; q < 32; ++q)
-                a.dh0[((long long)item * kP + 32 * part + q) * kNs + row] = dS[q];
-        }
-        if (part == 0) {
+                for (int q = 0; q < 32; ++q) {
+                    sv[q] = sin[q * kNs];
+                    dot = fmaf(dS[q], sout[q * kNs], dot);
+                }
+                store_split_half(smem + kSS, row, part, sv);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) dA_acc += __shfl_xor_sync(0xffffffffu, dA_acc, o);
-            if (lane == 0) s_da[quarter] = dA_acc;
+                for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+                if (lane == 0) s_dot[warp] = dot;
+            }
+            named_bar_sync(1, kWorkers);  // the fp32 states are read; s_dot, s_cs2 visible
+            store_split_half(smem + kSDS, row, part, dS);
+            {
+                float dyv[32];
+                load_tile_half(smem + kSDY, row, part, dyv);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) dyv[q] *= e_r;
+                store_split_half(smem + kSE, row, part, dyv);
+            }
+            float sdot = 0.0f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) sdot += s_dot[w];
+            fence_proxy_async_smem();
+            mbar_arrive(r_op);
+
+            // ---- (L o T w) and e^cs P, for dC
+            if (!Wc(m_tp)) { ok = false; break; }
+            tc_fence_after();
+            // (L o T w) row i = row: columns j <= i, factor e^(cs_i - cs_j) dt_j
+            mask_row_half(t_lane + kTmT, s_q2, cs2, 0, row, part);
+            scale_half(t_lane + kTmP, part, e_r);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(r_dc);
+            // ---- R scaled by e^(cs_last - cs_j); the adjoint entering the block:
+            // dS_in[p][n = row] = e^cs_last dS_out + (C^T (e^cs o dY))[n][p]
+            if (!Wc(m_rs)) { ok = false; break; }
+            tc_fence_after();
+            {
+                float rv[32], sv[32];
+                tmem_ld32(t_lane + kTmR + 32 * part, rv);
+                tmem_ld32(t_lane + kTmDS + 32 * part, sv);
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    rv[q] *= eL_r;
+                    dS[q] = fmaf(e_last, dS[q], sv[q]);
+                }
+                tmem_st32f(t_lane + kTmR + 32 * part, rv);
+            }
+            // (L o G)^T row j = row: columns i >= j, factor e^(cs_i - cs_j)
+            if (!Wc(m_gt)) { ok = false; break; }
+            tc_fence_after();
+            mask_row_half(t_lane + kTmGT, s_cs2, -cs2, row, kQ - 1, part);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(r_br);
+            // ---- dC row i: its log-decay term C_i . dC_i (this half) and its partial
+            if (!Wc(m_dc)) { ok = false; break; }
+            tc_fence_after();
+            const float dcs_c =
+                dot_half_tmem(smem + kSC, row, part, t_lane + kTmP, t < L ? a.pC + pofs + t : nullptr, L);
+            // ---- dX_j = dt_j bracket_j; the input-weight part of ddt_j is x_j . bracket_j
+            if (!Wc(m_br)) { ok = false; break; }
+            tc_fence_after();
+            float dw = 0.0f;
+            {
+                float xv[32], br[32];
+                load_tile_half(smem + kSX, row, part, xv);
+                tmem_ld32(t_lane + kTmR + 32 * part, br);
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 32; ++q) dw = fmaf(xv[q], br[q], dw);
+                if (t < L) {
+                    float* dxr = a.dx + (((long long)b * L + t) * a.nheads + h) * kP + 32 * part;
+#pragma unroll
+                    for (int q = 0; q < 32; q += 4)
+                        *reinterpret_cast<float4*>(dxr + q) = make_float4(
+                            dtr * br[q], dtr * br[q + 1], dtr * br[q + 2], dtr * br[q + 3]);
+                }
+            }
+            mbar_arrive(r_x);
+            // ---- (L o T w)^T row j = row: columns i >= j, factor e^(cs_i - cs_j) dt_j
+            if (!Wc(m_tt)) { ok = false; break; }
+            tc_fence_after();
+            mask_row_half(t_lane + kTmGT, s_cs2, q2, row, kQ - 1, part);
+            // Q row j scaled by dt_j e^(cs_last - cs_j) (Q is done before T^T)
+            scale_half(t_lane + kTmT, part, u_r);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(r_db);
+            // ---- dB row j: its log-decay term B_j . dB_j (this half) and its partial
+            if (!Wc(m_db)) { ok = false; break; }
+            tc_fence_after();
+            const float dcs_b =
+                dot_half_tmem(smem + kSB, row, part, t_lane + kTmT, t < L ? a.pB + pofs + t : nullptr, L);
+            mbar_arrive(r_cb);
+
+            // ---- log-decay gradient of each row, its suffix sums over the block,
+            // ddt and dA (first warpgroup)
+            if (part == 1) {
+                s_pd[row] = dcs_c;
+                s_pd[kQ + row] = dcs_b;
+                s_pd[2 * kQ + row] = dw;
+            }
+            named_bar_sync(1, kWorkers);
+            if (part == 0) {
+                float dcs = (dcs_c + s_pd[row]) - (dcs_b + s_pd[kQ + row]) +
+                            (row == kQ - 1 ? sdot : 0.0f);
+                const float dw_all = dw + s_pd[2 * kQ + row];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float u = __shfl_down_sync(0xffffffffu, dcs, o);
+                    if (lane + o < 32) dcs += u;
+                }
+                if (lane == 0) s_rsum[quarter] = dcs;
+                named_bar_sync(2, kWorkers / 2);  // the first warpgroup only
+#pragma unroll
+                for (int w = 0; w < 4; ++w)
+                    if (w > quarter) dcs += s_rsum[w];
+                if (t < L) a.ddt[((long long)b * L + t) * a.nheads + h] = fmaf(Ah, dcs, dw_all);
+                dA_acc = fmaf(dtr, dcs, dA_acc);
+            }
+            named_bar_sync(1, kWorkers);  // s_* are rewritten by the next block
         }
-        __syncthreads();
-        if (tid == 0) a.pA[item] = s_da[0] + s_da[1] + s_da[2] + s_da[3];
-    } else if (tid == 0) {
-        // a wait ran out: let every issued MMA and load finish before leaving
-        mma_commit(bar_fin);
-        (void)mbar_wait(bar_fin, 0, nullptr);
-        if (ld_pending) (void)mbar_wait(bar_ld, ld_par, nullptr);
-        if (ld2_pending) (void)mbar_wait(bar_ld2, ld2_par, nullptr);
+        if (ok) {
+            if (a.dh0) {
+#pragma unroll
+                for (int q = 0; q < 32; ++q)
+                    a.dh0[((long long)item * kP + 32 * part + q) * kNs + row] = dS[q];
+            }
+            if (part == 0) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) dA_acc += __shfl_xor_sync(0xffffffffu, dA_acc, o);
+                if (lane == 0) s_da[quarter] = dA_acc;
+            }
+            named_bar_sync(1, kWorkers);
+            if (tid == 0) a.pA[item] = s_da[0] + s_da[1] + s_da[2] + s_da[3];
+        }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-// dB, dC = the per-head partials summed over each group's heads; dA = the
-// per-(batch, head) sums added over the batch.  Fixed order: deterministic.
-__global__ void ssd_bwd_reduce_kernel(const float* __restrict__ pB, const float* __restrict__ pC,
-                                      const float* __restrict__ pA, float* __restrict__ dB,
-                                      float* __restrict__ dC, float* __restrict__ dA, int batch,
-                                      int seqlen, int nheads, int ngroups) {
+// dB, dC = the per-head partials ([h][b][n][t]) summed over each group's heads,
+// in head order, and written as (batch, seqlen, ngroups, dstate): a 32 x 32
+// (n, t) tile per block, transposed through shared memory so that both the
+// reads (t contiguous) and the writes (n contiguous) are coalesced.
+__global__ void ssd_bwd_reduce_bc_kernel(const float* __restrict__ pB, const float* __restrict__ pC,
+                                         float* __restrict__ dB, float* __restrict__ dC, int batch,
+                                         int seqlen, int nheads, int ngroups) {
+    __shared__ float tile[32][33];
     const int hpg = nheads / ngroups;
-    const long long rows = (long long)batch * seqlen;          // (b, t)
-    const long long nbc = rows * ngroups * kNs;                // one of dB, dC
-    const long long head_stride = rows * kNs;                  // pB[h] block
-    const long long total = 2 * nbc + nheads;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        if (i < 2 * nbc) {
-            const bool isC = i >= nbc;
-            const long long e = isC ? i - nbc : i;  // ((b t) g) n
-            const long long n = e % kNs, gi = (e / kNs) % ngroups, bt = e / (kNs * ngroups);
-            const float* src = (isC ? pC : pB) + bt * kNs + n;
-            float s = 0.0f;
-            for (int hh = (int)gi * hpg; hh < ((int)gi + 1) * hpg; ++hh) s += src[hh * head_stride];
-            (isC ? dC : dB)[e] = s;
-        } else {
-            const int hh = (int)(i - 2 * nbc);
-            float s = 0.0f;
-            for (int bb = 0; bb < batch; ++bb) s += pA[(long long)bb * nheads + hh];
-            dA[hh] = s;
+    const int t0 = blockIdx.x * 32, n0 = blockIdx.y * 32;
+    const long long L = seqlen;
+    for (int z = blockIdx.z; z < 2 * batch * ngroups; z += gridDim.z) {
+        const bool isC = z & 1;
+        const int bg = z >> 1, bb = bg / ngroups, gg = bg % ngroups;
+        const float* src = isC ? pC : pB;
+        for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+            const int n = n0 + r, t = t0 + threadIdx.x;
+            float acc = 0.0f;
+            if (t < seqlen)
+                for (int hh = gg * hpg; hh < (gg + 1) * hpg; ++hh)
+                    acc += src[(((long long)hh * batch + bb) * kNs + n) * L + t];
+            tile[r][threadIdx.x] = acc;
         }
+        __syncthreads();
+        float* dst = isC ? dC : dB;
+        for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+            const int t = t0 + r, n = n0 + threadIdx.x;
+            if (t < seqlen) dst[(((long long)bb * L + t) * ngroups + gg) * kNs + n] = tile[threadIdx.x][r];
+        }
+        __syncthreads();
+    }
+}
+
+// dA = the per-(batch, head) sums added over the batch, in batch order.
+__global__ void ssd_bwd_reduce_a_kernel(const float* __restrict__ pA, float* __restrict__ dA,
+                                        int batch, int nheads) {
+    for (int hh = blockIdx.x * blockDim.x + threadIdx.x; hh < nheads; hh += gridDim.x * blockDim.x) {
+        float acc = 0.0f;
+        for (int bb = 0; bb < batch; ++bb) acc += pA[(long long)bb * nheads + hh];
+        dA[hh] = acc;
     }
 }
 
@@ -790,13 +808,14 @@ extern "C" ssm_status_t ssd_chunked_bwd(const void* x, const float* dt, const fl
     ssd_bwd_kernel<<<(unsigned)items, kThreads, kSmemAlloc, s>>>(mc, mb, mx, mdy, a);
     if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
     // 3. sums over a group's heads and over the batch
-    int dev = 0, sms = 1;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const long long total = 2LL * (long long)steps * ngroups * kNs + nheads;
-    const unsigned rgrid =
-        (unsigned)std::max<long long>(1, std::min<long long>((total + 255) / 256, 8LL * sms));
-    ssd_bwd_reduce_kernel<<<rgrid, 256, 0, s>>>(a.pB, a.pC, a.pA, dB, dC, dA_head, batch, seqlen,
-                                                nheads, ngroups);
+    {
+        const dim3 grid((unsigned)((seqlen + 31) / 32), kNs / 32,
+                        (unsigned)std::min<long long>(2LL * batch * ngroups, 65535));
+        ssd_bwd_reduce_bc_kernel<<<grid, dim3(32, 8), 0, s>>>(a.pB, a.pC, dB, dC, batch, seqlen,
+                                                             nheads, ngroups);
+        if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
+        ssd_bwd_reduce_a_kernel<<<(unsigned)((nheads + 127) / 128), 128, 0, s>>>(a.pA, dA_head,
+                                                                                batch, nheads);
+    }
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
