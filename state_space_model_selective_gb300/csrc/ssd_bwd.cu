@@ -58,11 +58,12 @@ constexpr uint32_t kMiscBytes = (2 * 128 + 32 + 3 * 128) * 4 + kNumBars * 8 + 16
 constexpr uint32_t kSmemAlloc = kMisc + kMiscBytes + 1024;  // + realignment slack
 
 // TMEM columns (one CTA per SM: all 512)
-constexpr uint32_t kTmT = 0;     // T = dY X^T -> (L o T w) hi/lo; then Q -> dB
+constexpr uint32_t kTmT = 0;     // T = dY X^T -> (L o T w) hi/lo; then T^T -> (L o T w)^T hi/lo
 constexpr uint32_t kTmP = 128;   // P = dY S_in -> dC
-constexpr uint32_t kTmGT = 256;  // G^T = B C^T -> (L o G)^T hi/lo; then T^T -> (L o T w)^T hi/lo
-constexpr uint32_t kTmR = 384;   // R = B dS_out^T -> bracket (64)
+constexpr uint32_t kTmGT = 256;  // G^T = B C^T -> (L o G)^T hi/lo
+constexpr uint32_t kTmR = 384;   // R = B dS_out^T -> bracket (64); then Q -> dB (128)
 constexpr uint32_t kTmDS = 448;  // dS_in^T (64)
+constexpr uint32_t kTmQ = 384;
 constexpr uint32_t kTmemCols = 512;
 
 struct BwdArgs {
@@ -120,6 +121,40 @@ __device__ __forceinline__ void mask_row_half(uint32_t taddr, const float* col2,
         }
         tmem_st16(taddr + c0, hp);
         tmem_st16(taddr + c0 + 16, lp);
+    }
+}
+
+// This warpgroup's half of row j of G^T and of T^T (two TMEM products with the
+// same mask and decay), each turned into its bf16 hi/lo operand in place:
+// columns i >= j kept, G^T with factor e^(cs_i - cs_j) = 2^(cs2[i] - cs2_j),
+// T^T with that factor times dt_j.  One exp2 per element serves both.
+__device__ __forceinline__ void mask_pair_half(uint32_t tg, uint32_t tt, const float* cs2,
+                                               float cs2_j, float dt_j, int j, int part) {
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+        const int c0 = 64 * part + 32 * hh;
+        uint32_t gh[16], gl[16], th[16], tl[16];
+        if (c0 + 31 < j) {
+#pragma unroll
+            for (int q = 0; q < 16; ++q) gh[q] = gl[q] = th[q] = tl[q] = 0u;
+        } else {
+            float gv[32], tv[32];
+            tmem_ld32(tg + c0, gv);
+            tmem_ld32(tt + c0, tv);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 32; q += 2) {
+                float f0 = ex2_approx(cs2[c0 + q] - cs2_j), f1 = ex2_approx(cs2[c0 + q + 1] - cs2_j);
+                if (c0 + q < j) f0 = 0.0f;
+                if (c0 + q + 1 < j) f1 = 0.0f;
+                split2_bf16(gv[q] * f0, gv[q + 1] * f1, gh[q >> 1], gl[q >> 1]);
+                split2_bf16(tv[q] * (f0 * dt_j), tv[q + 1] * (f1 * dt_j), th[q >> 1], tl[q >> 1]);
+            }
+        }
+        tmem_st16(tg + c0, gh);
+        tmem_st16(tg + c0 + 16, gl);
+        tmem_st16(tt + c0, th);
+        tmem_st16(tt + c0 + 16, tl);
     }
 }
 
@@ -358,6 +393,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 mdesc(sbase + kSB, kk, 16384), id128b, 1);
                 }
                 mma_commit(m_dc);
+                // T^T = X dY^T into the consumed (L o T w) columns
+                if (!W(m_dc)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + kTmT, kdesc<kQ>(sbase + kSX, kk), kdesc<kQ>(sbase + kSDY, kk),
+                             id128, kk > 0);
+                mma_commit(m_tt);
                 // bracket = e^(cs_last - cs) o R + (L o G)^T dY
                 if (!W(r_br)) break;
                 tc_fence_after();
@@ -369,45 +412,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 mdesc(sbase + kSDY, kk, 16384), id64b, 1);
                 }
                 mma_commit(m_br);
-                // Q = X dS_out (hi + lo) into the consumed (L o T w) columns
-                if (!W(m_dc)) break;
+                // Q = X dS_out (hi + lo) into the bracket's and dS_in's columns, once
+                // the workers have read both
+                if (!W(r_x)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tmem + kTmT, kdesc<kQ>(sbase + kSX, kk & 3),
+                    mma_bf16(tmem + kTmQ, kdesc<kQ>(sbase + kSX, kk & 3),
                              kdesc<kQ>(sbase + kSDS + (kk >> 2) * 16384, kk & 3), id128, kk > 0);
                 mma_commit(m_q);
-                // T^T = X dY^T into the consumed (L o G)^T columns
-                if (!W(m_br)) break;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + kTmGT, kdesc<kQ>(sbase + kSX, kk), kdesc<kQ>(sbase + kSDY, kk),
-                             id128, kk > 0);
-                mma_commit(m_tt);
                 if (blk > 0) {
-                    // the states' regions are free once Q (their last reader) is done
+                    // the states' regions and x, dy are free once Q, their last
+                    // reader, is done (the workers' x reads are behind r_x)
                     if (!W(m_q)) break;
                     load_s(blk - 1);
                     p_s = (int)(ph ^ 1u);
+                    load_xy(blk - 1);
+                    p_xy = (int)(ph ^ 1u);
                 }
                 // dB = dt e^(cs_last - cs) o Q + (L o T w)^T C
                 if (!W(r_db)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    mma_bf16_ta(tmem + kTmT, tmem + kTmGT + mcol_hi(kk), mdesc(sbase + kSC, kk, 16384),
+                    mma_bf16_ta(tmem + kTmQ, tmem + kTmT + mcol_hi(kk), mdesc(sbase + kSC, kk, 16384),
                                 id128b, 1);
-                    mma_bf16_ta(tmem + kTmT, tmem + kTmGT + mcol_hi(kk) + 16,
+                    mma_bf16_ta(tmem + kTmQ, tmem + kTmT + mcol_hi(kk) + 16,
                                 mdesc(sbase + kSC, kk, 16384), id128b, 1);
                 }
                 mma_commit(m_db);
                 if (blk > 0) {
-                    // x and dy once T^T and the workers' x reads are done; C and B
-                    // once dB and the workers' dC, dB dots are
-                    if (!W(m_tt) || !W(r_x)) break;
-                    load_xy(blk - 1);
-                    p_xy = (int)(ph ^ 1u);
+                    // C and B once dB and the workers' dC, dB dots are done
                     if (!W(m_db) || !W(r_cb)) break;
                     load_cb(blk - 1);
                     p_cb = (int)(ph ^ 1u);
@@ -540,18 +575,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_st32f(t_lane + kTmR + 32 * part, rv);
             }
-            // (L o G)^T row j = row: columns i >= j, factor e^(cs_i - cs_j)
-            if (!Wc(m_gt)) { ok = false; break; }
+            // ---- (L o G)^T and (L o T w)^T, row j = row: columns i >= j
+            if (!Wc(m_gt) || !Wc(m_tt)) { ok = false; break; }
             tc_fence_after();
-            mask_row_half(t_lane + kTmGT, s_cs2, -cs2, row, kQ - 1, part);
+            mask_pair_half(t_lane + kTmGT, t_lane + kTmT, s_cs2, cs2, dtr, row, part);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(r_br);
-            // ---- dC row i: its log-decay term C_i . dC_i (this half) and its partial
-            if (!Wc(m_dc)) { ok = false; break; }
-            tc_fence_after();
-            const float dcs_c =
-                dot_half_tmem(smem + kSC, row, part, t_lane + kTmP, t < L ? a.pC + pofs + t : nullptr, L);
             // ---- dX_j = dt_j bracket_j; the input-weight part of ddt_j is x_j . bracket_j
             if (!Wc(m_br)) { ok = false; break; }
             tc_fence_after();
@@ -571,21 +601,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                             dtr * br[q], dtr * br[q + 1], dtr * br[q + 2], dtr * br[q + 3]);
                 }
             }
+            tc_fence_before();
             mbar_arrive(r_x);
-            // ---- (L o T w)^T row j = row: columns i >= j, factor e^(cs_i - cs_j) dt_j
-            if (!Wc(m_tt)) { ok = false; break; }
+            // ---- Q row j scaled by dt_j e^(cs_last - cs_j)
+            if (!Wc(m_q)) { ok = false; break; }
             tc_fence_after();
-            mask_row_half(t_lane + kTmGT, s_cs2, q2, row, kQ - 1, part);
-            // Q row j scaled by dt_j e^(cs_last - cs_j) (Q is done before T^T)
-            scale_half(t_lane + kTmT, part, u_r);
+            scale_half(t_lane + kTmQ, part, u_r);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(r_db);
+            // ---- dC row i: its log-decay term C_i . dC_i (this half) and its
+            // partial (while dB runs)
+            const float dcs_c =
+                dot_half_tmem(smem + kSC, row, part, t_lane + kTmP, t < L ? a.pC + pofs + t : nullptr, L);
             // ---- dB row j: its log-decay term B_j . dB_j (this half) and its partial
             if (!Wc(m_db)) { ok = false; break; }
             tc_fence_after();
             const float dcs_b =
-                dot_half_tmem(smem + kSB, row, part, t_lane + kTmT, t < L ? a.pB + pofs + t : nullptr, L);
+                dot_half_tmem(smem + kSB, row, part, t_lane + kTmQ, t < L ? a.pB + pofs + t : nullptr, L);
             mbar_arrive(r_cb);
 
             // ---- log-decay gradient of each row, its suffix sums over the block,
