@@ -683,13 +683,20 @@ __global__ void ssd_bwd_reduce_bc_kernel(const float* __restrict__ pB, const flo
         const bool isC = z & 1;
         const int bg = z >> 1, bb = bg / ngroups, gg = bg % ngroups;
         const float* src = isC ? pC : pB;
-        for (int r = threadIdx.y; r < 32; r += blockDim.y) {
-            const int n = n0 + r, t = t0 + threadIdx.x;
-            float acc = 0.0f;
-            if (t < seqlen)
-                for (int hh = gg * hpg; hh < (gg + 1) * hpg; ++hh)
-                    acc += src[(((long long)hh * batch + bb) * kNs + n) * L + t];
-            tile[r][threadIdx.x] = acc;
+        {
+            // rows n0 + threadIdx.y + 8 k, k < 4: four independent loads per head
+            const int t = t0 + threadIdx.x;
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (t < seqlen) {
+#pragma unroll 4
+                for (int hh = gg * hpg; hh < (gg + 1) * hpg; ++hh) {
+                    const float* p0 = src + (((long long)hh * batch + bb) * kNs + n0 + threadIdx.y) * L + t;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) acc[k] += p0[8 * k * L];
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) tile[threadIdx.y + 8 * k][threadIdx.x] = acc[k];
         }
         __syncthreads();
         float* dst = isC ? dC : dB;
