@@ -467,40 +467,46 @@ __global__ void __launch_bounds__(kBulkThreads)
         if (!named_bar_and(1, kBulkCompute, got)) break;
         float* st = reinterpret_cast<float*>(dsm + s * kTileBytes);
 
-        // state update of rows warp, warp + 4, ... (in place)
-#pragma unroll 4
-        for (int r16 = 0; r16 < 16; ++r16) {
-            const int p = warp + 4 * r16;
-            if (p >= nr) continue;
-            float in[4] = {0.f, 0.f, 0.f, 0.f};
+        // state update of rows warp, warp + 4, ... (in place), four rows at a time,
+        // each row's RK read-outs taken from the updated values in registers; the
+        // 4 RK partial sums of a group are reduce-scattered over the warp
+        float cv[RK][4];
 #pragma unroll
-            for (int r = 0; r < RK; ++r) {
-                const float xg = sx[r * kBulkRows + p], xb = sxp[r * kBulkRows + p];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) in[k] = fmaf(xg, bv[r][k], fmaf(xb, bp[r][k], in[k]));
-            }
-            float4* q = reinterpret_cast<float4*>(st + p * kBulkN) + lane;
-            const float4 v = *q;
-            *q = make_float4(fmaf(alpha, v.x, in[0]), fmaf(alpha, v.y, in[1]),
-                             fmaf(alpha, v.z, in[2]), fmaf(alpha, v.w, in[3]));
-        }
-        // one read-out per rank
+        for (int r = 0; r < RK; ++r) load4<T>(Cm + bc + r * rstride_b, cv[r]);
+        constexpr int V = 4 * RK;  // values per group: (row k4, rank r) at k4 * RK + r
 #pragma unroll 1
-        for (int r = 0; r < RK; ++r) {
-            float cv[4];
-            load4<T>(Cm + bc + r * rstride_b, cv);
-            float acc[16];
+        for (int g4 = 0; g4 < 4; ++g4) {
+            float acc[V];
 #pragma unroll
-            for (int r16 = 0; r16 < 16; ++r16) {
-                const int p = warp + 4 * r16;
-                acc[r16] = 0.0f;
+            for (int k4 = 0; k4 < 4; ++k4) {
+                const int p = warp + 4 * (4 * g4 + k4);
+#pragma unroll
+                for (int r = 0; r < RK; ++r) acc[k4 * RK + r] = 0.0f;
                 if (p < nr) {
-                    const float4 v = reinterpret_cast<const float4*>(st + p * kBulkN)[lane];
-                    acc[r16] = fmaf(cv[3], v.w, fmaf(cv[2], v.z, fmaf(cv[1], v.y, cv[0] * v.x)));
+                    float in[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int r = 0; r < RK; ++r) {
+                        const float xg = sx[r * kBulkRows + p], xb = sxp[r * kBulkRows + p];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            in[k] = fmaf(xg, bv[r][k], fmaf(xb, bp[r][k], in[k]));
+                    }
+                    float4* q = reinterpret_cast<float4*>(st + p * kBulkN) + lane;
+                    const float4 v = *q;
+                    const float4 nv = make_float4(fmaf(alpha, v.x, in[0]), fmaf(alpha, v.y, in[1]),
+                                                  fmaf(alpha, v.z, in[2]), fmaf(alpha, v.w, in[3]));
+                    *q = nv;
+#pragma unroll
+                    for (int r = 0; r < RK; ++r)
+                        acc[k4 * RK + r] = fmaf(cv[r][3], nv.w, fmaf(cv[r][2], nv.z,
+                                               fmaf(cv[r][1], nv.y, cv[r][0] * nv.x)));
                 }
             }
+            // reduce-scatter over lane bits 4, 3, ...: value index = sum of the
+            // halves kept; the remaining low lane bits are summed outright
+            int idx = 0;
 #pragma unroll
-            for (int m = 16, n = 8; m >= 2; m >>= 1, n >>= 1) {
+            for (int m = 16, n = V / 2; n >= 1; m >>= 1, n >>= 1) {
                 const bool hi = lane & m;
 #pragma unroll
                 for (int k = 0; k < n; ++k) {
@@ -508,10 +514,14 @@ __global__ void __launch_bounds__(kBulkThreads)
                     const float keep = hi ? acc[k + n] : acc[k];
                     acc[k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
                 }
+                if (hi) idx += n;
             }
-            acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 1);
-            const int p = warp + 4 * (lane >> 1);
-            if ((lane & 1) == 0 && p < nr) {
+            constexpr int kLow = 32 / V;  // lanes still holding parts of one value
+#pragma unroll
+            for (int m = kLow / 2; m >= 1; m >>= 1) acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], m);
+            const int k4 = idx / RK, r = idx % RK;
+            const int p = warp + 4 * (4 * g4 + k4);
+            if ((lane & (kLow - 1)) == 0 && p < nr) {
                 const long long row = xrow0 + r * rstride_x + p;
                 float out = acc[0] + (Dskip ? Dskip[h] : 0.0f) * to_f32(x[row]);
                 if (z) out *= silu_f(to_f32(z[row]));
