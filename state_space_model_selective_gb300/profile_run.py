@@ -5,12 +5,14 @@
     python -m state_space_model_selective_gb300.profile_run decode [--reps 5]
     python -m state_space_model_selective_gb300.profile_run scan_bwd [--reps 5]
     python -m state_space_model_selective_gb300.profile_run ssd_bwd [--reps 5]
+    python -m state_space_model_selective_gb300.profile_run decode_mimo [--reps 5]
 
 scan:     selective scan, bf16 in / fp32 y, batch 8, L 2048, D 1536, N 16
 ssd:      chunked SSD, bf16 in / fp32 y, batch 32, L 256, 32 heads, headdim 64, N 128
 decode:   decode step, fp32, batch 256, 32 heads, headdim 64, N 128
 scan_bwd: the scan's gradient on the scan workload (D, gate, bias, softplus)
 ssd_bwd:  the chunked SSD's gradient on the SSD workload
+decode_mimo: Mamba-3 MIMO rank-4 decode step, fp32, batch 256, 32 heads, headdim 64, N 128
 Inputs are drawn on the GPU (seeded); the process exits non-zero on any error.
 """
 from __future__ import annotations
@@ -24,7 +26,8 @@ from . import binding, inputs
 
 def main(argv=None):
     p = argparse.ArgumentParser()
-    p.add_argument("workload", choices=["scan", "ssd", "decode", "scan_bwd", "ssd_bwd"])
+    p.add_argument("workload",
+                   choices=["scan", "ssd", "decode", "scan_bwd", "ssd_bwd", "decode_mimo"])
     p.add_argument("--reps", type=int, default=5)
     a = p.parse_args(argv)
     dev = torch.device("cuda")
@@ -73,6 +76,21 @@ def main(argv=None):
                                     64, workspace=ws)
         torch.cuda.synchronize()
         assert binding.ssm_last_device_status(ws) == 0
+    elif a.workload == "decode_mimo":
+        g = torch.Generator(device=dev)
+        g.manual_seed(1005)
+        B_, H, P, N, R = 256, 32, 64, 128, 4
+        state = 0.1 * torch.randn(B_, H, P, N, device=dev, generator=g)
+        dt = torch.nn.functional.softplus(torch.randn(B_, H, device=dev, generator=g) - 4)
+        lam = torch.sigmoid(torch.randn(B_, H, device=dev, generator=g))
+        A = -(1 + 15 * torch.rand(H, device=dev, generator=g))
+        D = torch.ones(H, device=dev)
+        xr, xpr = (torch.randn(B_, R, H, P, device=dev, generator=g) for _ in range(2))
+        Br, Cr, Bpr = (torch.randn(B_, R, 1, N, device=dev, generator=g) for _ in range(3))
+        yr = torch.empty_like(xr)
+        for _ in range(a.reps):
+            binding.ssm_decode_step_mamba3_mimo(state, Bpr, xpr, xr, dt, lam, A, Br, Cr, D, y=yr)
+        torch.cuda.synchronize()
     else:
         inp = inputs.decode_inputs(256, 32, 64, 128, 1, 1, "f32", seed=1005, device="cuda")
         state = inp["state"]

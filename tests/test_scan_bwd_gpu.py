@@ -209,3 +209,32 @@ def test_scan_bwd_full_size_properties():
     assert_close(g2["dB"][..., :T], ref2["dB"], TOL_GRAD_SUM, "dB, first 64 steps")
     assert_close(g2["dC"][..., :T], ref2["dC"], TOL_GRAD_SUM, "dC, first 64 steps")
     assert_close(g2["du"][..., :T], ref2["du"], TOL_GRAD, "du, first 64 steps")
+
+
+@pytest.mark.parametrize("name,grad", [("delta", "ddelta"), ("A", "dA"), ("B", "dB"), ("C", "dC"),
+                                       ("z", "dz"), ("delta_bias", "ddelta_bias")])
+def test_scan_bwd_directional_derivatives(name, grad):
+    """<grad, v> against a central difference of sum(dy * y) through the CUDA
+    forward, for a random direction v in one input (fp32 inputs): the two
+    kernels agree with each other in every input, not only with the oracle."""
+    inp = inputs.scan_inputs(1, 32, 160, 16, 1, "f32", seed=90, dskip="randn")
+    dy = _dy((1, 32, 160), "f32", 91)
+    g = _gpu_grad(inp, dy, poison=False)
+    v = torch.randn(inp[name].shape, generator=torch.Generator().manual_seed(92))
+    eps = 1e-2 if name in ("delta", "A", "z", "delta_bias") else 0.5
+
+    def loss(t):
+        x = {k: (_dev(u) if isinstance(u, torch.Tensor) else u) for k, u in inp.items()}
+        x[name] = t.cuda()
+        y, _ = binding.ssm_scan_fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"],
+                                    x["delta_bias"], True)
+        return float((y.double().cpu() * dy.double()).sum())
+
+    fd = (loss(inp[name] + eps * v) - loss(inp[name] - eps * v)) / (2 * eps)
+    terms = g[grad].double().cpu() * v.double()
+    an = float(terms.sum())
+    # linear inputs (B, C): exact up to rounding; the others: O(eps^2) truncation.
+    # The bound scales with sum |g v| as well as |<g, v>|: a random direction can
+    # make the dot product cancel far below its terms (the difference quotient's
+    # fp32 rounding does not cancel with it).
+    assert abs(fd - an) <= 2e-3 * abs(an) + 1e-3 * float(terms.abs().sum()), (name, fd, an)

@@ -145,3 +145,30 @@ def test_ssd_bwd_full_size_properties():
     for key, rkey, tol in KEYS:
         got = g[key][:, :T] if key in ("dx", "ddt", "dB", "dC") else g[key]
         assert_close(got, ref[rkey], tol, key)
+
+
+@pytest.mark.parametrize("name,grad", [("dt", "ddt"), ("A_head", "dA_head")])
+def test_ssd_bwd_directional_derivatives(name, grad):
+    """<grad, v> against a central difference of sum(dy y) through the CUDA
+    forward in the fp32 inputs dt and A_head (the forward is smooth in both)."""
+    inp = inputs.ssd_inputs(1, 256, 4, 64, 128, 1, "bf16", seed=93)
+    dy, _ = _cotangents(1, 256, 4, 94, False)
+    g = _gpu(inp, dy, poison=False)
+    gen = torch.Generator().manual_seed(95)
+    base = inp[name]
+    v = torch.randn(base.shape, generator=gen) * base.abs()  # relative direction
+    eps = 1e-2
+
+    def loss(t):
+        d = {k: u.cuda() for k, u in inp.items()}
+        d[name] = t.cuda()
+        y, _ = binding.ssd_chunked_fwd(d["x"], d["dt"], d["A_head"], d["B"], d["C"], 64,
+                                       out_dtype=torch.float32)
+        return float((y.double().cpu() * dy.double()).sum())
+
+    fd = (loss(base + eps * v) - loss(base - eps * v)) / (2 * eps)
+    terms = g[grad].double().cpu() * v.double()
+    an = float(terms.sum())
+    # O(eps^2) truncation; the bound also scales with sum |g v| (a random
+    # direction can make <g, v> cancel far below its terms)
+    assert abs(fd - an) <= 5e-3 * abs(an) + 1e-3 * float(terms.abs().sum()), (name, fd, an)
