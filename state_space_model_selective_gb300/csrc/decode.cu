@@ -442,11 +442,12 @@ __global__ void __launch_bounds__(kBulkThreads)
         const long long b = bh / nheads;
         const int g = h / (nheads / ngroups);
         const long long bc = ((b * RK) * ngroups + g) * kBulkN + 4 * lane;
-        float bv[RK][4], bp[RK][4];
+        float bv[RK][4], bp[RK][4], cv[RK][4];
 #pragma unroll
         for (int r = 0; r < RK; ++r) {
             load4<T>(Bm + bc + r * rstride_b, bv[r]);
             load4<T>(m3.prev_B + bc + r * rstride_b, bp[r]);
+            load4<T>(Cm + bc + r * rstride_b, cv[r]);
         }
         const float dtv = dt[bh];
         const float alpha = expf(dtv * A[h]);
@@ -470,9 +471,6 @@ __global__ void __launch_bounds__(kBulkThreads)
         // state update of rows warp, warp + 4, ... (in place), four rows at a time,
         // each row's RK read-outs taken from the updated values in registers; the
         // 4 RK partial sums of a group are reduce-scattered over the warp
-        float cv[RK][4];
-#pragma unroll
-        for (int r = 0; r < RK; ++r) load4<T>(Cm + bc + r * rstride_b, cv[r]);
         constexpr int V = 4 * RK;  // values per group: (row k4, rank r) at k4 * RK + r
 #pragma unroll 1
         for (int g4 = 0; g4 < 4; ++g4) {
