@@ -272,21 +272,25 @@ def run_ours(args):
     per_launch_s = ms_local / 1e3 / args.steps
     achieved = mufu / per_launch_s / 1e9
 
-    # ---- e2e: same call with host buffers; H2D of the step's inputs and D2H
-    # of its outputs inside the timed region
+    # ---- e2e: the scan through ssm_scan_fwd_host, the entry point for host-
+    # resident activations: every step copies u, delta, z, B, C in from pinned host
+    # memory and y and the final state out (the library pipelines the copies with
+    # the scan over segments of the sequence); A, D and delta_bias are parameters
+    # resident on the device
     e2e_steps = max(3, min(args.steps, 20))
-    names = ["u", "delta", "z", "B", "C", "A", "D", "delta_bias"]
+    names = ["u", "delta", "z", "B", "C"]
     h2d = sum(pinned[k].numel() * pinned[k].element_size() for k in names)
     y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
     fs_host = torch.empty(fs.shape, dtype=fs.dtype, pin_memory=True)
     d2h = y_host.numel() * 4 + fs_host.numel() * 4
+    ws_host = torch.empty(binding.ssm_scan_fwd_host_workspace_bytes(
+        BATCH, DIM, SEQLEN, DSTATE, NGROUPS, torch.bfloat16, torch.float32),
+        dtype=torch.uint8, device=dev)
 
     def e2e_step():
-        for k in names:
-            d[k].copy_(pinned[k], non_blocking=True)
-        step()
-        y_host.copy_(y, non_blocking=True)
-        fs_host.copy_(fs, non_blocking=True)
+        binding.ssm_scan_fwd_host(pinned["u"], pinned["delta"], d["A"], pinned["B"], pinned["C"],
+                                  y_host, fs_host, d["D"], pinned["z"], d["delta_bias"], True,
+                                  workspace=ws_host, stream=stream)
 
     e2e_step()
     torch.cuda.synchronize(dev)

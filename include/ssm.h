@@ -10,6 +10,7 @@
  *                    (trapezoidal three-term recurrence)
  *   ssd_mamba3_mimo_fwd, ssm_decode_step_mamba3_mimo  Mamba-3 MIMO (rank R)
  *   ssm_scan_bwd     gradient of ssm_scan_fwd (reverse mode, every input)
+ *   ssm_scan_fwd_host  ssm_scan_fwd on host-resident activations, copies pipelined
  *   ssd_chunked_bwd  gradient of ssd_chunked_fwd, tensor cores
  *
  * Conventions shared by every entry point
@@ -411,6 +412,48 @@ ssm_status_t ssd_chunked_bwd(const void* x, const float* dt, const float* A_head
                              int nheads, int headdim, int dstate, int ngroups,
                              ssm_dtype_t in_dtype, void* workspace, size_t workspace_bytes,
                              void* stream);
+
+/*
+ * Bytes of device workspace ssm_scan_fwd_host needs (a pure function of its
+ * arguments; 0 if they are invalid).  About two segments' worth of u, delta, z,
+ * B, C and y (a segment is ~1/8 of the sequence, a multiple of 64 steps), two
+ * states and one segment's ssm_scan_workspace_bytes.
+ */
+size_t ssm_scan_fwd_host_workspace_bytes(int batch, int dim, int seqlen, int dstate, int ngroups,
+                                         ssm_dtype_t in_dtype, ssm_dtype_t out_dtype);
+
+/*
+ * Selective scan with the activations and results in HOST memory.
+ *   Computes exactly what ssm_scan_fwd computes, same arguments and layouts,
+ *   but u, delta, z, B, C, initial_state, y and final_state are HOST pointers to
+ *   page-locked memory (cudaHostAlloc / cudaMallocHost / cudaHostRegister;
+ *   anything else returns SSM_ERR_UNSUPPORTED); A, D, delta_bias and the
+ *   workspace are DEVICE pointers.  The sequence is cut into segments that
+ *   chain through the state (the scan is associative: "We brought Mamba to
+ *   Trainium -- and mapped where custom kernels actually help", section "We
+ *   built the parallel scan -- and it taught us something sharper"); each
+ *   segment's rows are copied in with 2-D DMA copies, scanned on `stream` from
+ *   the previous segment's final state, and its y copied back, with the copies
+ *   of neighbouring segments in flight during the scan.  The result is bit-equal
+ *   to ssm_scan_fwd on device copies of the same inputs.
+ *
+ *  - Asynchronous like every entry point: work is enqueued on `stream` and on
+ *    two copy streams of the library's own (created on the first call on a
+ *    device and kept until the process exits); `stream` completes only after
+ *    every copy of the call.  The host buffers must not be modified (inputs) or
+ *    read (outputs) until then.
+ *  - workspace: at least ssm_scan_fwd_host_workspace_bytes(...) bytes, not
+ *    shared with a concurrent call; ssm_last_device_status reports the last
+ *    segment's device status.
+ *  - Calls on one device are enqueued one at a time (an internal lock).
+ */
+ssm_status_t ssm_scan_fwd_host(const void* u, const void* delta, const float* A, const void* B,
+                               const void* C, const float* D, const void* z,
+                               const float* delta_bias, int delta_softplus,
+                               const float* initial_state, void* y, float* final_state,
+                               int batch, int dim, int seqlen, int dstate, int ngroups,
+                               ssm_dtype_t in_dtype, ssm_dtype_t out_dtype, void* workspace,
+                               size_t workspace_bytes, void* stream);
 
 /*
  * Waits for `stream` to drain, then returns the device-side status the last

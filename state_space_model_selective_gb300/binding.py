@@ -30,7 +30,8 @@ EXPORTS = ["ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_bytes", "
            "ssd_chunked_fwd", "ssd_mamba3_fwd", "ssd_mamba3_mimo_fwd", "ssm_decode_step",
            "ssm_decode_step_mamba3", "ssm_decode_step_mamba3_mimo", "ssm_last_device_status",
            "ssm_scan_fwd_noalloc", "ssm_scan_bwd_workspace_bytes", "ssm_scan_bwd",
-           "ssd_chunked_bwd_workspace_bytes", "ssd_chunked_bwd"]
+           "ssd_chunked_bwd_workspace_bytes", "ssd_chunked_bwd", "ssm_scan_fwd_host_workspace_bytes",
+           "ssm_scan_fwd_host"]
 
 
 class SSMError(RuntimeError):
@@ -81,6 +82,10 @@ def lib() -> ctypes.CDLL:
         L.ssd_chunked_bwd_workspace_bytes.argtypes = [i] * 6
         L.ssd_chunked_bwd.restype = i
         L.ssd_chunked_bwd.argtypes = [vp] * 5 + [i] + [vp] * 9 + [i] * 7 + [vp, sz, vp]
+        L.ssm_scan_fwd_host_workspace_bytes.restype = sz
+        L.ssm_scan_fwd_host_workspace_bytes.argtypes = [i] * 7
+        L.ssm_scan_fwd_host.restype = i
+        L.ssm_scan_fwd_host.argtypes = [vp] * 8 + [i] + [vp] * 3 + [i] * 7 + [vp, sz, vp]
         L.ssm_last_device_status.restype = i
         L.ssm_last_device_status.argtypes = [vp, vp]
         _lib = L
@@ -238,6 +243,65 @@ def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_s
                             workspace.numel(), _stream(stream))
     _check(st, "ssm_scan_bwd")
     return g
+
+
+def ssm_scan_fwd_host_workspace_bytes(batch, dim, seqlen, dstate=16, ngroups=1,
+                                      in_dtype=torch.bfloat16, out_dtype=torch.float32) -> int:
+    return int(lib().ssm_scan_fwd_host_workspace_bytes(batch, dim, seqlen, dstate, ngroups,
+                                                       _DT[in_dtype], _DT[out_dtype]))
+
+
+def _pinned(t, name, dtype=None, ndim=None):
+    if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_pinned():
+        raise TypeError(f"{name} must be a pinned (page-locked) CPU tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+    return t
+
+
+def ssm_scan_fwd_host(u, delta, A, B, C, y, final_state=None, D=None, z=None, delta_bias=None,
+                      delta_softplus=False, initial_state=None, workspace=None, stream=None):
+    """``ssm_scan_fwd`` on pinned host tensors: u, delta, z, B, C, initial_state, y and
+    final_state are pinned CPU tensors (same layouts); A, D, delta_bias and the workspace
+    are CUDA tensors.  The copies in and out are pipelined with the scan on the library's
+    copy streams; the call returns once everything is enqueued on ``stream``."""
+    _pinned(u, "u", ndim=3)
+    in_dt = u.dtype
+    if in_dt not in _DT:
+        raise TypeError("u must be float32 or bfloat16")
+    batch, dim, seqlen = u.shape
+    _pinned(delta, "delta", in_dt)
+    _req(A, "A", torch.float32, 2)
+    dstate = A.shape[1]
+    _pinned(B, "B", in_dt, 4)
+    _pinned(C, "C", in_dt, 4)
+    ngroups = B.shape[1]
+    _opt(D, "D", torch.float32)
+    _opt(delta_bias, "delta_bias", torch.float32)
+    if z is not None:
+        _pinned(z, "z", in_dt)
+    if initial_state is not None:
+        _pinned(initial_state, "initial_state", torch.float32)
+    _pinned(y, "y")
+    if y.dtype not in _DT:
+        raise TypeError("y must be float32 or bfloat16")
+    if final_state is not None:
+        _pinned(final_state, "final_state", torch.float32)
+    need = ssm_scan_fwd_host_workspace_bytes(batch, dim, seqlen, dstate, ngroups, in_dt, y.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=A.device)
+    _req(workspace, "workspace", torch.uint8)
+    st = lib().ssm_scan_fwd_host(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                 _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)),
+                                 _ptr(initial_state), _ptr(y), _ptr(final_state), batch, dim,
+                                 seqlen, dstate, ngroups, _DT[in_dt], _DT[y.dtype],
+                                 _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "ssm_scan_fwd_host")
+    return y, final_state
 
 
 def ssm_scan_fwd_noalloc(u, delta, A, B, C, y, final_state=None, D=None, z=None,

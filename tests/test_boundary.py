@@ -333,3 +333,34 @@ def test_ssd_bwd_workspace_bytes():
     assert f(32, 256, 32) == f(32, 256, 32)
     assert f(1, 64, 2, headdim=32) == 0
     assert f(1, 64, 3, ngroups=2) == 0
+
+
+def host_call(L, **kw):
+    args = dict(u=P(0), delta=P(1), A=P(2), B=P(3), C=P(4), D=None, z=None, bias=None,
+                softplus=1, h0=None, y=P(5), fs=None, batch=2, dim=32, seqlen=64, dstate=16,
+                ngroups=1, in_dt=1, out_dt=0, ws=P(7), wsb=1 << 30, stream=None)
+    args.update(kw)
+    a = args
+    return L.ssm_scan_fwd_host(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"],
+                               a["bias"], a["softplus"], a["h0"], a["y"], a["fs"], a["batch"],
+                               a["dim"], a["seqlen"], a["dstate"], a["ngroups"], a["in_dt"],
+                               a["out_dt"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_scan_host_argument_errors(L):
+    assert host_call(L, u=None) == NULL
+    assert host_call(L, y=None) == NULL
+    assert host_call(L, A=None) == NULL
+    assert host_call(L, ws=None) == WS
+    assert host_call(L, wsb=64) == WS
+    assert host_call(L, batch=-1) == SHAPE
+    assert host_call(L, ngroups=3) == SHAPE
+    assert host_call(L, dstate=8) == UNSUP
+    assert host_call(L, in_dt=4) == DTYPE
+    assert host_call(L, A=ctypes.c_void_p(0x30000004)) == ALIGN
+    assert host_call(L, dim=0, u=None, y=None) == OK    # no rows: nothing to do
+    f = binding.ssm_scan_fwd_host_workspace_bytes
+    assert f(8, 1536, 2048) == f(8, 1536, 2048) > 0
+    # two slots of about an eighth of the sequence (u, delta, z, B, C in, y out)
+    assert f(8, 1536, 2048) >= 2 * (8 * 1536 * 256 * (3 * 2 + 4))
+    assert f(8, 1536, 2048, dstate=8) == 0
