@@ -492,9 +492,27 @@ def _measure_scan_bwd(dev, reps):
     el = BATCH * SEQLEN * DIM * DSTATE
     ops = SCAN_BWD_FP32_PER_ELEMENT * el
     achieved = ops / (ms / 1e3) / 1e9
+    # a training step's scan: the forward keeping checkpoints, then the gradient
+    # from them (no second forward recurrence)
+    y = torch.empty(BATCH, DIM, SEQLEN, **f)
+    fs = torch.empty(BATCH, DIM, DSTATE, **f)
+    ck = torch.empty(binding.ssm_scan_checkpoint_bytes(BATCH, DIM, SEQLEN) // 4, **f)
+    wsf = torch.empty(binding.ssm_scan_workspace_bytes(BATCH, DIM, SEQLEN), dtype=torch.uint8,
+                      device=dev)
+
+    def train():
+        binding.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                             inp["z"], inp["delta_bias"], True, out_dtype=torch.float32, y=y,
+                             final_state=fs, workspace=wsf, checkpoints=ck)
+        binding.ssm_scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], dy, inp["D"],
+                             inp["z"], inp["delta_bias"], True, workspace=ws, out=out,
+                             checkpoints=ck)
+    ms_train = _time(train, reps)
     return {"workload": "selective-scan gradient bf16 in / fp32 gradients, batch 8, L 2048, "
                         "1536 channels, d_state 16, D, gate, bias, softplus",
             "ms": ms, "elements_per_s": el / (ms / 1e3),
+            "train_step_ms": ms_train,
+            "train_step": "forward keeping checkpoints + gradient from them",
             "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_GOPS,
                          "unit": "Gop/s (FP32 pipe)", "frac": achieved / FP32_PEAK_GOPS,
                          "algorithmic_fp32_ops": ops}}

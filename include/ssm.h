@@ -306,6 +306,28 @@ ssm_status_t ssm_scan_fwd_noalloc(const void* u, const void* delta, const float*
                                   ssm_dtype_t in_dtype, ssm_dtype_t out_dtype, void* stream);
 
 /*
+ * Bytes of the checkpoints ssm_scan_fwd_ckpt keeps: the state entering every
+ * 16-step segment, [ceil(seqlen / 16)][batch * dim][16] fp32.  0 if invalid.
+ */
+size_t ssm_scan_checkpoint_bytes(int batch, int dim, int seqlen, int dstate);
+
+/*
+ * ssm_scan_fwd that also keeps, in `checkpoints` (device, at least
+ * ssm_scan_checkpoint_bytes(...) bytes, not overlapping anything else), the
+ * state entering every 16-step segment -- what ssm_scan_bwd needs, so that a
+ * training step does not run the forward recurrence twice.  y and final_state
+ * are exactly ssm_scan_fwd's; the same arguments and errors, plus SSM_ERR_NULL
+ * for a NULL `checkpoints` when there is work.
+ */
+ssm_status_t ssm_scan_fwd_ckpt(const void* u, const void* delta, const float* A, const void* B,
+                               const void* C, const float* D, const void* z,
+                               const float* delta_bias, int delta_softplus,
+                               const float* initial_state, void* y, float* final_state,
+                               float* checkpoints, int batch, int dim, int seqlen, int dstate,
+                               int ngroups, ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Bytes of device workspace ssm_scan_bwd needs for this problem (a pure
  * function of its arguments).  Returns 0 if the arguments are invalid.
  * About (ceil(seqlen / 16) * batch * dim * 64 + ceil(dim / ngroups / 32) *
@@ -343,7 +365,9 @@ size_t ssm_scan_bwd_workspace_bytes(int batch, int dim, int seqlen, int dstate, 
  *
  * Inputs: u, delta, A, B, C, D, z, delta_bias, delta_softplus, initial_state
  * exactly as for ssm_scan_fwd; dy (batch, dim, seqlen) in in_dtype;
- * dfinal_state (batch, dim, dstate) fp32 or NULL (zero).
+ * dfinal_state (batch, dim, dstate) fp32 or NULL (zero); checkpoints: the
+ * states ssm_scan_fwd_ckpt kept for the same inputs, or NULL (the call then
+ * re-runs the forward recurrence to make them).
  * workspace: at least ssm_scan_bwd_workspace_bytes(...) bytes, contents on
  * entry irrelevant, not shared with a concurrent call.  ssm_last_device_status
  * reads it afterwards like ssm_scan_fwd's (the call runs the forward
@@ -360,7 +384,8 @@ size_t ssm_scan_bwd_workspace_bytes(int batch, int dim, int seqlen, int dstate, 
 ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B,
                           const void* C, const float* D, const void* z, const float* delta_bias,
                           int delta_softplus, const float* initial_state, const void* dy,
-                          const float* dfinal_state, float* du, float* ddelta, float* dA,
+                          const float* dfinal_state, const float* checkpoints, float* du,
+                          float* ddelta, float* dA,
                           float* dB, float* dC, float* dD, float* dz, float* ddelta_bias,
                           float* dinitial_state, int batch, int dim, int seqlen, int dstate,
                           int ngroups, ssm_dtype_t in_dtype, void* workspace,

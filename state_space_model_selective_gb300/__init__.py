@@ -13,5 +13,6 @@ from .binding import (EXPORTS, SSMError, lib, ssd_chunked_bwd,  # noqa: F401
                       ssd_mamba3_mimo_fwd, ssm_abi_version, ssm_decode_step,
                       ssm_decode_step_mamba3, ssm_decode_step_mamba3_mimo,
                       ssm_last_device_status, ssm_scan_bwd, ssm_scan_bwd_workspace_bytes,
-                      ssm_scan_fwd, ssm_scan_fwd_host, ssm_scan_fwd_host_workspace_bytes,
+                      ssm_scan_checkpoint_bytes, ssm_scan_fwd, ssm_scan_fwd_host,
+                      ssm_scan_fwd_host_workspace_bytes,
                       ssm_scan_workspace_bytes, status_string)

@@ -31,7 +31,7 @@ EXPORTS = ["ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_bytes", "
            "ssm_decode_step_mamba3", "ssm_decode_step_mamba3_mimo", "ssm_last_device_status",
            "ssm_scan_fwd_noalloc", "ssm_scan_bwd_workspace_bytes", "ssm_scan_bwd",
            "ssd_chunked_bwd_workspace_bytes", "ssd_chunked_bwd", "ssm_scan_fwd_host_workspace_bytes",
-           "ssm_scan_fwd_host"]
+           "ssm_scan_fwd_host", "ssm_scan_checkpoint_bytes", "ssm_scan_fwd_ckpt"]
 
 
 class SSMError(RuntimeError):
@@ -77,7 +77,11 @@ def lib() -> ctypes.CDLL:
         L.ssm_scan_bwd_workspace_bytes.restype = sz
         L.ssm_scan_bwd_workspace_bytes.argtypes = [i] * 5
         L.ssm_scan_bwd.restype = i
-        L.ssm_scan_bwd.argtypes = [vp] * 8 + [i] + [vp] * 12 + [i] * 6 + [vp, sz, vp]
+        L.ssm_scan_bwd.argtypes = [vp] * 8 + [i] + [vp] * 13 + [i] * 6 + [vp, sz, vp]
+        L.ssm_scan_checkpoint_bytes.restype = sz
+        L.ssm_scan_checkpoint_bytes.argtypes = [i] * 4
+        L.ssm_scan_fwd_ckpt.restype = i
+        L.ssm_scan_fwd_ckpt.argtypes = [vp] * 8 + [i] + [vp] * 4 + [i] * 7 + [vp, sz, vp]
         L.ssd_chunked_bwd_workspace_bytes.restype = sz
         L.ssd_chunked_bwd_workspace_bytes.argtypes = [i] * 6
         L.ssd_chunked_bwd.restype = i
@@ -135,12 +139,18 @@ def ssm_scan_workspace_bytes(batch, dim, seqlen, dstate=16, ngroups=1) -> int:
     return int(lib().ssm_scan_workspace_bytes(batch, dim, seqlen, dstate, ngroups))
 
 
+def ssm_scan_checkpoint_bytes(batch, dim, seqlen, dstate=16) -> int:
+    return int(lib().ssm_scan_checkpoint_bytes(batch, dim, seqlen, dstate))
+
+
 def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=False,
                  initial_state=None, out_dtype=None, y=None, final_state=None,
-                 workspace=None, return_final_state=True, stream=None):
+                 workspace=None, return_final_state=True, stream=None, checkpoints=None):
     """Selective scan.  u, delta, z: (batch, dim, seqlen); A: (dim, dstate) fp32;
     B, C: (batch, ngroups, dstate, seqlen); D, delta_bias: (dim,) fp32;
-    initial_state: (batch, dim, dstate) fp32.  Returns (y, final_state)."""
+    initial_state: (batch, dim, dstate) fp32.  With ``checkpoints`` (a CUDA fp32
+    tensor of ssm_scan_checkpoint_bytes bytes) the states ssm_scan_bwd needs are
+    kept too (ssm_scan_fwd_ckpt).  Returns (y, final_state)."""
     _req(u, "u", ndim=3)
     in_dt = u.dtype
     if in_dt not in _DT:
@@ -167,6 +177,18 @@ def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softp
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=u.device)
     _req(workspace, "workspace", torch.uint8)
+    if checkpoints is not None:
+        _req(checkpoints, "checkpoints", torch.float32)
+        if checkpoints.numel() * 4 < ssm_scan_checkpoint_bytes(batch, dim, seqlen, dstate):
+            raise ValueError("checkpoints is smaller than ssm_scan_checkpoint_bytes(...)")
+        st = lib().ssm_scan_fwd_ckpt(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                     _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)),
+                                     _ptr(initial_state), _ptr(y), _ptr(final_state),
+                                     _ptr(checkpoints), batch, dim, seqlen, dstate, ngroups,
+                                     _DT[in_dt], _DT[out_dt], _ptr(workspace), workspace.numel(),
+                                     _stream(stream))
+        _check(st, "ssm_scan_fwd_ckpt")
+        return y, final_state
     st = lib().ssm_scan_fwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
                             _ptr(delta_bias), int(bool(delta_softplus)), _ptr(initial_state),
                             _ptr(y), _ptr(final_state), batch, dim, seqlen, dstate, ngroups,
@@ -182,7 +204,8 @@ def ssm_scan_bwd_workspace_bytes(batch, dim, seqlen, dstate=16, ngroups=1) -> in
 
 def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softplus=False,
                  initial_state=None, dfinal_state=None, workspace=None, want_dD=None,
-                 want_ddelta_bias=None, want_dinitial_state=True, out=None, stream=None):
+                 want_ddelta_bias=None, want_dinitial_state=True, out=None, stream=None,
+                 checkpoints=None):
     """Gradient of ``ssm_scan_fwd`` for the loss sum(dy * y) + sum(dfinal_state *
     final_state).  Inputs as for ``ssm_scan_fwd``; dy (batch, dim, seqlen) in u's
     dtype; dfinal_state (batch, dim, dstate) fp32 or None.  Returns a dict of fp32
@@ -190,7 +213,9 @@ def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_s
     (batch, ngroups, dstate, seqlen); dD, ddelta_bias (dim,); dinitial_state
     (batch, dim, dstate).  dz is None without z; dD / ddelta_bias are computed
     when D / delta_bias is given, or when want_dD / want_ddelta_bias is true.
-    ``out`` may map any of these names to a preallocated fp32 tensor to write."""
+    ``out`` may map any of these names to a preallocated fp32 tensor to write.
+    ``checkpoints``: what ``ssm_scan_fwd(..., checkpoints=...)`` kept for the same
+    inputs (the forward recurrence is then not run again)."""
     _req(u, "u", ndim=3)
     in_dt = u.dtype
     if in_dt not in _DT:
@@ -236,7 +261,9 @@ def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_s
     _req(workspace, "workspace", torch.uint8)
     st = lib().ssm_scan_bwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
                             _ptr(delta_bias), int(bool(delta_softplus)), _ptr(initial_state),
-                            _ptr(dy), _ptr(dfinal_state), _ptr(g["du"]), _ptr(g["ddelta"]),
+                            _ptr(dy), _ptr(dfinal_state), _ptr(_opt(checkpoints, "checkpoints",
+                                                                   torch.float32)),
+                            _ptr(g["du"]), _ptr(g["ddelta"]),
                             _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]),
                             _ptr(g["dz"]), _ptr(g["ddelta_bias"]), _ptr(g["dinitial_state"]),
                             batch, dim, seqlen, dstate, ngroups, _DT[in_dt], _ptr(workspace),

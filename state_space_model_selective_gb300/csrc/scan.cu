@@ -68,8 +68,8 @@ struct ScanArgs {
     const void* Bm;
     const void* Cm;
     // checkpoint mode (kernel flag CK): the state entering every 16-step
-    // segment, [seg][batch * dim][kN], instead of y (the backward pass
-    // recomputes from these)
+    // segment, [seg][batch * dim][kN] (the backward pass recomputes from
+    // these); y is then optional
     float* ckpt;
     int batch, dim, seqlen, ngroups;
     int dpg;          // channels per group
@@ -477,7 +477,7 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
                 o0 *= silu_f(zz[0]);
                 o1 *= silu_f(zz[1]);
             }
-            if (!CK && valid && tg < t_end)
+            if ((!CK || a.y) && valid && tg < t_end)
                 store_y2<Tout>(yrow + tg, o0, o1, true, tg + 1 < t_end, vec_store);
         }
 
@@ -677,13 +677,15 @@ extern "C" size_t ssm_scan_workspace_bytes(int batch, int dim, int seqlen, int d
     return workspace_bound(batch, dim, seqlen, ngroups);
 }
 
-extern "C" ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const float* A,
-                                     const void* B, const void* C, const float* D, const void* z,
-                                     const float* delta_bias, int delta_softplus,
-                                     const float* initial_state, void* y, float* final_state,
-                                     int batch, int dim, int seqlen, int dstate, int ngroups,
-                                     ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
-                                     void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+
+// ssm_scan_fwd, and with ckpt != NULL ssm_scan_fwd_ckpt: validation and launch.
+ssm_status_t scan_fwd_entry(const void* u, const void* delta, const float* A, const void* B,
+                            const void* C, const float* D, const void* z, const float* delta_bias,
+                            int delta_softplus, const float* initial_state, void* y,
+                            float* final_state, float* ckpt, int batch, int dim, int seqlen,
+                            int dstate, int ngroups, ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                            void* workspace, size_t workspace_bytes, void* stream) {
     using namespace ssm_host;
     if (batch < 0 || dim < 0 || seqlen < 0 || ngroups < 1 || dstate < 1) return SSM_ERR_SHAPE;
     if (dim % ngroups != 0) return SSM_ERR_SHAPE;
@@ -697,7 +699,7 @@ extern "C" ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const flo
     if (seqlen > 0 && (!u || !delta || !B || !C || !y || !A)) return SSM_ERR_NULL;
     if (seqlen > 0 && !workspace) return SSM_ERR_WORKSPACE;
     const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, initial_state, y, final_state,
-                          workspace};
+                          workspace, ckpt};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return SSM_ERR_ALIGN;
 
@@ -715,6 +717,11 @@ extern "C" ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const flo
         if (overlaps(final_state, fbytes, r.p, r.n)) return SSM_ERR_ALIAS;
     }
     if (overlaps(y, ybytes, final_state, fbytes)) return SSM_ERR_ALIAS;
+    const size_t cbytes = ckpt ? ((size_t)seqlen + 15) / 16 * rows * kN * 4 : 0;
+    for (const R& r : ins)
+        if (overlaps(ckpt, cbytes, r.p, r.n)) return SSM_ERR_ALIAS;
+    if (overlaps(ckpt, cbytes, y, ybytes) || overlaps(ckpt, cbytes, final_state, fbytes))
+        return SSM_ERR_ALIAS;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (seqlen == 0) {
@@ -729,14 +736,15 @@ extern "C" ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const flo
     }
     const size_t need = workspace_bound(batch, dim, seqlen, ngroups);
     if (workspace_bytes < need) return SSM_ERR_WORKSPACE;
-    if (overlaps(workspace, need, y, ybytes) || overlaps(workspace, need, final_state, fbytes))
+    if (overlaps(workspace, need, y, ybytes) || overlaps(workspace, need, final_state, fbytes) ||
+        overlaps(workspace, need, ckpt, cbytes))
         return SSM_ERR_ALIAS;
     for (const R& r : ins)
         if (overlaps(workspace, need, r.p, r.n)) return SSM_ERR_ALIAS;
 
     ScanArgs a{};
     a.u = u; a.delta = delta; a.z = z; a.A = A; a.Dskip = D; a.bias = delta_bias;
-    a.h0 = initial_state; a.y = y; a.final_state = final_state; a.Bm = B; a.Cm = C;
+    a.h0 = initial_state; a.y = y; a.final_state = final_state; a.Bm = B; a.Cm = C; a.ckpt = ckpt;
     a.batch = batch; a.dim = dim; a.seqlen = seqlen; a.ngroups = ngroups;
     a.dpg = dim / ngroups; a.softplus = delta_softplus ? 1 : 0;
 
@@ -744,11 +752,49 @@ extern "C" ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const flo
     const bool tma = ((size_t)seqlen * es) % 16 == 0;
     if (in_dtype == SSM_BF16) {
         return out_dtype == SSM_BF16
-                   ? dispatch<__nv_bfloat16, __nv_bfloat16>(a, in_dtype, tma, s, workspace)
-                   : dispatch<__nv_bfloat16, float>(a, in_dtype, tma, s, workspace);
+                   ? (ckpt ? dispatch<__nv_bfloat16, __nv_bfloat16, true>(a, in_dtype, tma, s, workspace)
+                           : dispatch<__nv_bfloat16, __nv_bfloat16>(a, in_dtype, tma, s, workspace))
+                   : (ckpt ? dispatch<__nv_bfloat16, float, true>(a, in_dtype, tma, s, workspace)
+                           : dispatch<__nv_bfloat16, float>(a, in_dtype, tma, s, workspace));
     }
-    return out_dtype == SSM_BF16 ? dispatch<float, __nv_bfloat16>(a, in_dtype, tma, s, workspace)
-                                 : dispatch<float, float>(a, in_dtype, tma, s, workspace);
+    if (out_dtype == SSM_BF16)
+        return ckpt ? dispatch<float, __nv_bfloat16, true>(a, in_dtype, tma, s, workspace)
+                    : dispatch<float, __nv_bfloat16>(a, in_dtype, tma, s, workspace);
+    return ckpt ? dispatch<float, float, true>(a, in_dtype, tma, s, workspace)
+                : dispatch<float, float>(a, in_dtype, tma, s, workspace);
+}
+
+}  // namespace
+
+extern "C" ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const float* A,
+                                     const void* B, const void* C, const float* D, const void* z,
+                                     const float* delta_bias, int delta_softplus,
+                                     const float* initial_state, void* y, float* final_state,
+                                     int batch, int dim, int seqlen, int dstate, int ngroups,
+                                     ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+    return scan_fwd_entry(u, delta, A, B, C, D, z, delta_bias, delta_softplus, initial_state, y,
+                          final_state, nullptr, batch, dim, seqlen, dstate, ngroups, in_dtype,
+                          out_dtype, workspace, workspace_bytes, stream);
+}
+
+extern "C" size_t ssm_scan_checkpoint_bytes(int batch, int dim, int seqlen, int dstate) {
+    if (batch < 0 || dim < 0 || seqlen < 0 || dstate != kN) return 0;
+    return ((size_t)seqlen + 15) / 16 * (size_t)batch * dim * kN * sizeof(float);
+}
+
+extern "C" ssm_status_t ssm_scan_fwd_ckpt(const void* u, const void* delta, const float* A,
+                                          const void* B, const void* C, const float* D,
+                                          const void* z, const float* delta_bias,
+                                          int delta_softplus, const float* initial_state, void* y,
+                                          float* final_state, float* checkpoints, int batch,
+                                          int dim, int seqlen, int dstate, int ngroups,
+                                          ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                                          void* workspace, size_t workspace_bytes, void* stream) {
+    if (!checkpoints && batch > 0 && dim > 0 && seqlen > 0) return SSM_ERR_NULL;
+    return scan_fwd_entry(u, delta, A, B, C, D, z, delta_bias, delta_softplus, initial_state, y,
+                          final_state, checkpoints, batch, dim, seqlen, dstate, ngroups, in_dtype,
+                          out_dtype, workspace, workspace_bytes, stream);
 }
 
 // ------------------------------------------------ allocation-free variant

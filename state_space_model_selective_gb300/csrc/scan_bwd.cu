@@ -583,7 +583,8 @@ extern "C" size_t ssm_scan_bwd_workspace_bytes(int batch, int dim, int seqlen, i
 extern "C" ssm_status_t ssm_scan_bwd(
     const void* u, const void* delta, const float* A, const void* B, const void* C,
     const float* D, const void* z, const float* delta_bias, int delta_softplus,
-    const float* initial_state, const void* dy, const float* dfinal_state, float* du,
+    const float* initial_state, const void* dy, const float* dfinal_state,
+    const float* checkpoints, float* du,
     float* ddelta, float* dA, float* dB, float* dC, float* dD, float* dz, float* ddelta_bias,
     float* dinitial_state, int batch, int dim, int seqlen, int dstate, int ngroups,
     ssm_dtype_t in_dtype, void* workspace, size_t workspace_bytes, void* stream) {
@@ -602,7 +603,8 @@ extern "C" ssm_status_t ssm_scan_bwd(
     if (rows > 0 && seqlen > 0 && z && !dz) return SSM_ERR_NULL;
     if (rows > 0 && seqlen > 0 && !workspace) return SSM_ERR_WORKSPACE;
     const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, initial_state, dy, dfinal_state,
-                          du, ddelta, dA, dB, dC, dD, dz, ddelta_bias, dinitial_state, workspace};
+                          checkpoints, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias,
+                          dinitial_state, workspace};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return SSM_ERR_ALIGN;
 
@@ -616,7 +618,8 @@ extern "C" ssm_status_t ssm_scan_bwd(
                      {A, (size_t)dim * kN * 4}, {D, D ? (size_t)dim * 4 : 0},
                      {delta_bias, delta_bias ? (size_t)dim * 4 : 0},
                      {initial_state, initial_state ? st : 0}, {dy, act},
-                     {dfinal_state, dfinal_state ? st : 0}};
+                     {dfinal_state, dfinal_state ? st : 0},
+                     {checkpoints, checkpoints ? ((size_t)seqlen + kSeg - 1) / kSeg * st : 0}};
     const R outs[] = {{du, act32}, {ddelta, act32}, {dz, z ? act32 : 0},
                       {dB, bc32}, {dC, bc32}, {dA, (size_t)dim * kN * 4},
                       {dD, dD ? (size_t)dim * 4 : 0},
@@ -657,7 +660,7 @@ extern "C" ssm_status_t ssm_scan_bwd(
     a.u = u; a.delta = delta; a.z = z; a.dy = dy; a.A = A; a.Dskip = D; a.bias = delta_bias;
     a.Bm = B; a.Cm = C;
     float* ckpt = reinterpret_cast<float*>(ws + w.fwd);
-    a.ckpt = ckpt;
+    a.ckpt = checkpoints ? checkpoints : ckpt;
     a.dfinal = dfinal_state;
     a.du = du; a.ddelta = ddelta; a.dz = z ? dz : nullptr; a.dh0 = dinitial_state;
     a.pBC = reinterpret_cast<float*>(ws + w.fwd + w.ckpt);
@@ -668,11 +671,16 @@ extern "C" ssm_status_t ssm_scan_bwd(
     a.dpg = dim / ngroups; a.bpg = (a.dpg + kCH - 1) / kCH;
     a.softplus = delta_softplus ? 1 : 0;
 
-    // 1. states entering every 16-step segment
-    ssm_status_t rc = ssm_internal::scan_forward_checkpoints(
-        u, delta, A, B, C, delta_bias, delta_softplus, initial_state, ckpt,
-        batch, dim, seqlen, ngroups, in_dtype, workspace, s);
-    if (rc != SSM_OK) return rc;
+    // 1. states entering every 16-step segment (unless the forward kept them)
+    ssm_status_t rc = SSM_OK;
+    if (!checkpoints) {
+        rc = ssm_internal::scan_forward_checkpoints(u, delta, A, B, C, delta_bias, delta_softplus,
+                                                    initial_state, ckpt, batch, dim, seqlen,
+                                                    ngroups, in_dtype, workspace, s);
+        if (rc != SSM_OK) return rc;
+    } else if (cudaMemsetAsync(ws, 0, 256, s) != cudaSuccess) {
+        return SSM_ERR_CUDA;  // a clean status word for ssm_last_device_status
+    }
 
     // 2. the adjoint sweep, one CTA per (batch, group, channel block)
     const long long grid = (long long)batch * ngroups * a.bpg;

@@ -39,7 +39,7 @@ def test_header_symbols_exported(L):
 
 
 def test_version_and_status_strings(L):
-    assert binding.ssm_abi_version() == 2
+    assert binding.ssm_abi_version() == 3
     for code in range(10):
         s = binding.status_string(code)
         assert isinstance(s, str) and s
@@ -251,7 +251,8 @@ def bwd_call(L, **kw):
     args.update(kw)
     a = args
     return L.ssm_scan_bwd(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["bias"],
-                          a["softplus"], a["h0"], a["dy"], a["dfs"], a["du"], a["ddelta"],
+                          a["softplus"], a["h0"], a["dy"], a["dfs"], a.get("ck"), a["du"],
+                          a["ddelta"],
                           a["dA"], a["dB"], a["dC"], a["dD"], a["dz"], a["dbias"], a["dh0"],
                           a["batch"], a["dim"], a["seqlen"], a["dstate"], a["ngroups"],
                           a["in_dt"], a["ws"], a["wsb"], a["stream"])
@@ -276,6 +277,8 @@ def test_scan_bwd_argument_errors(L):
     assert bwd_call(L, dD=P(13), dbias=P(13)) == ALIAS
     assert bwd_call(L, ws=P(5)) == ALIAS              # workspace on top of dy
     assert bwd_call(L, ws=P(8)) == ALIAS              # workspace on top of dA
+    assert bwd_call(L, ck=ctypes.c_void_p(0x90000008)) == ALIGN
+    assert bwd_call(L, du=P(12), ck=P(12)) == ALIAS    # checkpoints under an output
     # no channels: nothing to write, nothing launched
     assert bwd_call(L, dim=0, u=None, dA=None, du=None) == OK
 

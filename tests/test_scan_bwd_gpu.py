@@ -238,3 +238,31 @@ def test_scan_bwd_directional_derivatives(name, grad):
     # make the dot product cancel far below its terms (the difference quotient's
     # fp32 rounding does not cancel with it).
     assert abs(fd - an) <= 2e-3 * abs(an) + 1e-3 * float(terms.abs().sum()), (name, fd, an)
+
+
+@pytest.mark.parametrize("dt,out_dt", [("bf16", torch.float32), ("f32", torch.bfloat16)])
+def test_scan_checkpoints_from_the_forward(dt, out_dt):
+    """ssm_scan_fwd with checkpoints gives the plain forward's y and final state
+    bit for bit, and ssm_scan_bwd from those checkpoints gives the same bits as
+    ssm_scan_bwd recomputing them."""
+    batch, dim, seqlen = 2, 96, 530
+    inp = inputs.scan_inputs(batch, dim, seqlen, 16, 2, dt, seed=140)
+    x = {k: (_dev(v) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    h0 = torch.randn(batch, dim, 16, generator=torch.Generator().manual_seed(141)).cuda()
+    args = (x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], True, h0)
+    y0, f0 = binding.ssm_scan_fwd(*args, out_dtype=out_dt)
+    ck = torch.full((binding.ssm_scan_checkpoint_bytes(batch, dim, seqlen) // 4,), float("nan"),
+                    device="cuda")
+    y1, f1 = binding.ssm_scan_fwd(*args, out_dtype=out_dt, checkpoints=ck)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1) and torch.equal(f0, f1)
+    assert not torch.isnan(ck).any()
+    dy = _dy((batch, dim, seqlen), dt, 142).cuda()
+    kw = dict(D=x["D"], z=x["z"], delta_bias=x["delta_bias"], delta_softplus=True,
+              initial_state=h0)
+    g0 = binding.ssm_scan_bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], dy, **kw)
+    g1 = binding.ssm_scan_bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], dy, checkpoints=ck, **kw)
+    torch.cuda.synchronize()
+    for k, v in g0.items():
+        if v is not None:
+            assert torch.equal(v, g1[k]), k
