@@ -544,12 +544,26 @@ def _measure_ssd_bwd(dev, reps):
         binding.ssd_chunked_bwd(inp["x"], inp["dt"], inp["A_head"], inp["B"], inp["C"], dy, 64,
                                 workspace=ws, out=out)
     ms = _time(bwd, reps)
+    # a training step's SSD: the forward keeping block states, then the gradient
+    # from them (no second forward)
+    y = torch.empty(Bn, L, H, P, **f)
+    fs = torch.empty(Bn, H, P, N, **f)
+    bs = torch.empty(binding.ssd_chunked_checkpoint_bytes(Bn, L, H, P, N) // 4, **f)
+
+    def train():
+        binding.ssd_chunked_fwd(inp["x"], inp["dt"], inp["A_head"], inp["B"], inp["C"], 64,
+                                out_dtype=torch.float32, y=y, final_state=fs, block_states=bs)
+        binding.ssd_chunked_bwd(inp["x"], inp["dt"], inp["A_head"], inp["B"], inp["C"], dy, 64,
+                                workspace=ws, out=out, block_states=bs)
+    ms_train = _time(train, reps)
     Q = 128
     flops = 2 * (3 * Q * Q * N + 2 * Q * Q * P + 4 * Q * P * N) * Bn * H * (L // Q)
     achieved = flops / (ms / 1e3) / 1e12
     return {"workload": "chunked-SSD gradient bf16 in / fp32 gradients, batch 32, L 256, 32 "
                         "heads, headdim 64, d_state 128, chunk 64",
             "ms": ms, "elements_per_s": Bn * L * H * P * N / (ms / 1e3),
+            "train_step_ms": ms_train,
+            "train_step": "forward keeping block states + gradient from them",
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": BF16_PEAK_TFLOPS,
                          "unit": "TFLOP/s", "frac": achieved / BF16_PEAK_TFLOPS,
                          "algorithmic_flops": flops}}

@@ -392,6 +392,28 @@ ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float* A, cons
                           size_t workspace_bytes, void* stream);
 
 /*
+ * Bytes of the block states ssd_chunked_fwd_ckpt keeps: the state entering
+ * every 128-step block and the final state, [batch * nheads][ceil(seqlen / 128)
+ * + 1][headdim][dstate] fp32.  0 if invalid or unsupported.
+ */
+size_t ssd_chunked_checkpoint_bytes(int batch, int seqlen, int nheads, int headdim, int dstate);
+
+/*
+ * ssd_chunked_fwd that also keeps the block states (device, at least
+ * ssd_chunked_checkpoint_bytes(...) bytes, not overlapping anything else) for
+ * ssd_chunked_bwd, so that a training step runs the forward once.  y and
+ * final_state are exactly ssd_chunked_fwd's (y may be NULL: states only); the
+ * same arguments and errors, plus SSM_ERR_NULL for a NULL `block_states` when
+ * there is work.  With seqlen == 0 nothing is written to block_states.
+ */
+ssm_status_t ssd_chunked_fwd_ckpt(const void* x, const float* dt, const float* A_head,
+                                  const void* B, const void* C, int chunk,
+                                  const float* initial_state, void* y, float* final_state,
+                                  float* block_states, int batch, int seqlen, int nheads,
+                                  int headdim, int dstate, int ngroups, ssm_dtype_t in_dtype,
+                                  ssm_dtype_t out_dtype, void* stream);
+
+/*
  * Bytes of device workspace ssd_chunked_bwd needs (a pure function of its
  * arguments; 0 if they are invalid or unsupported).  About batch * nheads *
  * (ceil(seqlen / 128) + 1) * 32 KiB of block states plus 2 * nheads * batch *
@@ -416,8 +438,10 @@ size_t ssd_chunked_bwd_workspace_bytes(int batch, int seqlen, int nheads, int he
  *   dB, dC          (batch, seqlen, ngroups, dstate)  fp32 (summed over the group's heads)
  *   dinitial_state  (batch, nheads, headdim, dstate)  fp32, may be NULL (not written)
  * Inputs as for ssd_chunked_fwd (x, B, C bf16; dt, A_head, initial_state fp32)
- * plus dy (batch, seqlen, nheads, headdim) in in_dtype and dfinal_state
- * (batch, nheads, headdim, dstate) fp32 or NULL (zero).
+ * plus dy (batch, seqlen, nheads, headdim) in in_dtype, dfinal_state
+ * (batch, nheads, headdim, dstate) fp32 or NULL (zero), and block_states: what
+ * ssd_chunked_fwd_ckpt kept for the same inputs, or NULL (the call then runs the
+ * forward once more to make them).
  * workspace: at least ssd_chunked_bwd_workspace_bytes(...) bytes, contents on
  * entry irrelevant; ssm_last_device_status reads it afterwards.  The call runs
  * the forward kernel once more to store the state entering every 128-step
@@ -432,7 +456,8 @@ size_t ssd_chunked_bwd_workspace_bytes(int batch, int seqlen, int nheads, int he
  */
 ssm_status_t ssd_chunked_bwd(const void* x, const float* dt, const float* A_head, const void* B,
                              const void* C, int chunk, const float* initial_state, const void* dy,
-                             const float* dfinal_state, float* dx, float* ddt, float* dA_head,
+                             const float* dfinal_state, const float* block_states, float* dx,
+                             float* ddt, float* dA_head,
                              float* dB, float* dC, float* dinitial_state, int batch, int seqlen,
                              int nheads, int headdim, int dstate, int ngroups,
                              ssm_dtype_t in_dtype, void* workspace, size_t workspace_bytes,

@@ -9,6 +9,7 @@ Entry points (same names as in ``include/ssm.h``): ``ssm_scan_fwd``,
 ``state_space_model_selective_gb300.build.build()``.
 """
 from .binding import (EXPORTS, SSMError, lib, ssd_chunked_bwd,  # noqa: F401
+                      ssd_chunked_checkpoint_bytes,
                       ssd_chunked_bwd_workspace_bytes, ssd_chunked_fwd, ssd_mamba3_fwd,
                       ssd_mamba3_mimo_fwd, ssm_abi_version, ssm_decode_step,
                       ssm_decode_step_mamba3, ssm_decode_step_mamba3_mimo,

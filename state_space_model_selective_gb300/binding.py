@@ -31,7 +31,8 @@ EXPORTS = ["ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_bytes", "
            "ssm_decode_step_mamba3", "ssm_decode_step_mamba3_mimo", "ssm_last_device_status",
            "ssm_scan_fwd_noalloc", "ssm_scan_bwd_workspace_bytes", "ssm_scan_bwd",
            "ssd_chunked_bwd_workspace_bytes", "ssd_chunked_bwd", "ssm_scan_fwd_host_workspace_bytes",
-           "ssm_scan_fwd_host", "ssm_scan_checkpoint_bytes", "ssm_scan_fwd_ckpt"]
+           "ssm_scan_fwd_host", "ssm_scan_checkpoint_bytes", "ssm_scan_fwd_ckpt",
+           "ssd_chunked_checkpoint_bytes", "ssd_chunked_fwd_ckpt"]
 
 
 class SSMError(RuntimeError):
@@ -85,7 +86,11 @@ def lib() -> ctypes.CDLL:
         L.ssd_chunked_bwd_workspace_bytes.restype = sz
         L.ssd_chunked_bwd_workspace_bytes.argtypes = [i] * 6
         L.ssd_chunked_bwd.restype = i
-        L.ssd_chunked_bwd.argtypes = [vp] * 5 + [i] + [vp] * 9 + [i] * 7 + [vp, sz, vp]
+        L.ssd_chunked_bwd.argtypes = [vp] * 5 + [i] + [vp] * 10 + [i] * 7 + [vp, sz, vp]
+        L.ssd_chunked_checkpoint_bytes.restype = sz
+        L.ssd_chunked_checkpoint_bytes.argtypes = [i] * 5
+        L.ssd_chunked_fwd_ckpt.restype = i
+        L.ssd_chunked_fwd_ckpt.argtypes = [vp] * 5 + [i] + [vp] * 4 + [i] * 8 + [vp]
         L.ssm_scan_fwd_host_workspace_bytes.restype = sz
         L.ssm_scan_fwd_host_workspace_bytes.argtypes = [i] * 7
         L.ssm_scan_fwd_host.restype = i
@@ -369,14 +374,20 @@ def ssd_chunked_bwd_workspace_bytes(batch, seqlen, nheads, headdim=64, dstate=12
                                                      ngroups))
 
 
+def ssd_chunked_checkpoint_bytes(batch, seqlen, nheads, headdim=64, dstate=128) -> int:
+    return int(lib().ssd_chunked_checkpoint_bytes(batch, seqlen, nheads, headdim, dstate))
+
+
 def ssd_chunked_bwd(x, dt, A_head, B, C, dy, chunk=64, initial_state=None, dfinal_state=None,
-                    workspace=None, want_dinitial_state=True, out=None, stream=None):
+                    workspace=None, want_dinitial_state=True, out=None, stream=None,
+                    block_states=None):
     """Gradient of ``ssd_chunked_fwd`` for the loss sum(dy * y) + sum(dfinal_state *
     final_state).  Inputs as for ``ssd_chunked_fwd``; dy like x (bf16); dfinal_state
     (batch, nheads, headdim, dstate) fp32 or None.  Returns a dict of fp32 tensors:
     dx (like x), ddt (like dt), dA_head (nheads,), dB, dC (like B) and dinitial_state
     (batch, nheads, headdim, dstate, or None).  ``out`` may map any of these names to
-    a preallocated fp32 tensor to write."""
+    a preallocated fp32 tensor to write.  ``block_states``: what
+    ``ssd_chunked_fwd(..., block_states=...)`` kept for the same inputs."""
     _req(x, "x", torch.bfloat16, 4)
     batch, seqlen, nheads, headdim = x.shape
     _req(dt, "dt", torch.float32, 3)
@@ -407,7 +418,9 @@ def ssd_chunked_bwd(x, dt, A_head, B, C, dy, chunk=64, initial_state=None, dfina
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     _req(workspace, "workspace", torch.uint8)
     st = lib().ssd_chunked_bwd(_ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C), int(chunk),
-                               _ptr(initial_state), _ptr(dy), _ptr(dfinal_state), _ptr(g["dx"]),
+                               _ptr(initial_state), _ptr(dy), _ptr(dfinal_state),
+                               _ptr(_opt(block_states, "block_states", torch.float32)),
+                               _ptr(g["dx"]),
                                _ptr(g["ddt"]), _ptr(g["dA_head"]), _ptr(g["dB"]), _ptr(g["dC"]),
                                _ptr(g["dinitial_state"]), batch, seqlen, nheads, headdim, dstate,
                                ngroups, _DT[torch.bfloat16], _ptr(workspace), workspace.numel(),
@@ -417,7 +430,7 @@ def ssd_chunked_bwd(x, dt, A_head, B, C, dy, chunk=64, initial_state=None, dfina
 
 
 def ssd_chunked_fwd(x, dt, A_head, B, C, chunk=64, out_dtype=None, y=None, final_state=None,
-                    return_final_state=True, stream=None, initial_state=None):
+                    return_final_state=True, stream=None, initial_state=None, block_states=None):
     """Chunked SSD.  x: (batch, seqlen, nheads, headdim); dt: (batch, seqlen, nheads) fp32;
     A_head: (nheads,) fp32; B, C: (batch, seqlen, ngroups, dstate); initial_state (optional,
     may be ``final_state`` itself): (batch, nheads, headdim, dstate) fp32.
@@ -443,6 +456,18 @@ def ssd_chunked_fwd(x, dt, A_head, B, C, chunk=64, out_dtype=None, y=None, final
     _opt(initial_state, "initial_state", torch.float32)
     if initial_state is not None and tuple(initial_state.shape) != (batch, nheads, headdim, dstate):
         raise ValueError("initial_state must be (batch, nheads, headdim, dstate)")
+    if block_states is not None:
+        _req(block_states, "block_states", torch.float32)
+        if block_states.numel() * 4 < ssd_chunked_checkpoint_bytes(batch, seqlen, nheads, headdim,
+                                                                   dstate):
+            raise ValueError("block_states is smaller than ssd_chunked_checkpoint_bytes(...)")
+        st = lib().ssd_chunked_fwd_ckpt(_ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C),
+                                        int(chunk), _ptr(initial_state), _ptr(y),
+                                        _ptr(final_state), _ptr(block_states), batch, seqlen,
+                                        nheads, headdim, dstate, ngroups, _DT[in_dt], _DT[out_dt],
+                                        _stream(stream))
+        _check(st, "ssd_chunked_fwd_ckpt")
+        return y, final_state
     st = lib().ssd_chunked_fwd(_ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C), int(chunk),
                                _ptr(initial_state), _ptr(y), _ptr(final_state), batch, seqlen,
                                nheads, headdim, dstate,

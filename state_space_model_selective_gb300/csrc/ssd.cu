@@ -108,8 +108,8 @@ __device__ __forceinline__ void mprime_chunk(const float* gv, const float* q2c, 
 // row u of a block is sub-token u % RK of step u / RK -- and sub-tokens share
 // their step's decay and weights; a sub-token sees every sub-token of its own
 // step (the block-diagonal part, weight gamma) and of earlier steps.
-// BS: write the state entering every block and the final state to a.bstates
-// instead of y (the backward pass's checkpoints).
+// BS: also write the state entering every block and the final state to
+// a.bstates (the backward pass's checkpoints); y is then optional.
 template <typename Tout, bool M3, int RK, bool BS = false>
 __global__ void __launch_bounds__(kThreads, 2)
     ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_B,
@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             if constexpr (BS) {
                 float* bs = a.bstates + (long long)item * (nblocks + 1) * kP * kNs;
                 for (int e = tid; e < (nblocks + 1) * kP * kNs; e += kThreads) bs[e] = nanv;
-                continue;
+                if (!a.y) continue;
             }
             for (int t = tid; t < nsub; t += kThreads) {
                 Tout* yr = reinterpret_cast<Tout*>(a.y) +
@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
         // ---- y rows out of the staged tile: each warp writes whole rows of
         // the head (coalesced); rows past the sequence end are skipped
-        if constexpr (!BS) {
+        if (!BS || a.y != nullptr) {
             const long long yrow0 = ((long long)b * nsub + t0) * a.nheads + h;
             if constexpr (sizeof(Tout) == 4) {
 #pragma unroll
@@ -596,8 +596,8 @@ ssm_status_t launch(const CUtensorMap& mc, const CUtensorMap& mb, const CUtensor
 ssm_status_t ssd_entry(const void* x, const float* dt, const float* lam, const float* A_head,
                        const void* B, const void* C, int chunk, int rank,
                        const float* initial_state, const void* prev_B, const void* prev_x,
-                       void* y, float* final_state, int batch, int seqlen, int nheads,
-                       int headdim, int dstate, int ngroups, ssm_dtype_t in_dtype,
+                       void* y, float* final_state, float* bstates, int batch, int seqlen,
+                       int nheads, int headdim, int dstate, int ngroups, ssm_dtype_t in_dtype,
                        ssm_dtype_t out_dtype, bool m3, void* stream) {
     using namespace ssm_host;
     if (batch < 0 || seqlen < 0 || nheads < 0 || headdim < 1 || dstate < 1 || ngroups < 1 ||
@@ -631,7 +631,7 @@ ssm_status_t ssd_entry(const void* x, const float* dt, const float* lam, const f
         }
         return SSM_OK;
     }
-    if (!x || !dt || !A_head || !B || !C || !y) return SSM_ERR_NULL;
+    if (!x || !dt || !A_head || !B || !C || (!y && !bstates)) return SSM_ERR_NULL;
     if (m3 && !lam) return SSM_ERR_NULL;
     const void* ptrs[] = {x, dt, A_head, B, C, y, final_state, initial_state, lam, prev_B, prev_x};
     for (const void* p : ptrs)
@@ -652,6 +652,16 @@ ssm_status_t ssd_entry(const void* x, const float* dt, const float* lam, const f
         if (overlaps(y, yb, r.p, r.n) || overlaps(final_state, fb, r.p, r.n)) return SSM_ERR_ALIAS;
     if (overlaps(y, yb, final_state, fb)) return SSM_ERR_ALIAS;
     if (initial_state && overlaps(y, yb, initial_state, sb)) return SSM_ERR_ALIAS;
+    if (bstates) {
+        if (m3 || rank != 1) return SSM_ERR_UNSUPPORTED;
+        if (!aligned16(bstates)) return SSM_ERR_ALIGN;
+        const size_t bsb = (size_t)batch * nheads * (((size_t)seqlen + kQ - 1) / kQ + 1) * kP * kNs * 4;
+        for (const R& r : ins)
+            if (overlaps(bstates, bsb, r.p, r.n)) return SSM_ERR_ALIAS;
+        if (overlaps(bstates, bsb, y, yb) || overlaps(bstates, bsb, final_state, fb) ||
+            (initial_state && overlaps(bstates, bsb, initial_state, sb)))
+            return SSM_ERR_ALIAS;
+    }
 
     CUtensorMap mc, mb, mx;
     const int nsub = seqlen * rank;
@@ -673,6 +683,11 @@ ssm_status_t ssd_entry(const void* x, const float* dt, const float* lam, const f
     a.nheads = nheads;
     a.ngroups = ngroups;
     const bool bf = out_dtype == SSM_BF16;
+    if (bstates) {  // Mamba-2 only (the backward pass is)
+        a.bstates = bstates;
+        return bf ? launch<__nv_bfloat16, false, 1, true>(mc, mb, mx, a, s)
+                  : launch<float, false, 1, true>(mc, mb, mx, a, s);
+    }
     if (!m3) return bf ? launch<__nv_bfloat16, false, 1>(mc, mb, mx, a, s)
                        : launch<float, false, 1>(mc, mb, mx, a, s);
     switch (rank) {
@@ -722,8 +737,28 @@ extern "C" ssm_status_t ssd_chunked_fwd(const void* x, const float* dt, const fl
                                         ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
                                         void* stream) {
     return ssd_entry(x, dt, nullptr, A_head, B, C, chunk, 1, initial_state, nullptr, nullptr, y,
-                     final_state, batch, seqlen, nheads, headdim, dstate, ngroups, in_dtype,
-                     out_dtype, false, stream);
+                     final_state, nullptr, batch, seqlen, nheads, headdim, dstate, ngroups,
+                     in_dtype, out_dtype, false, stream);
+}
+
+extern "C" size_t ssd_chunked_checkpoint_bytes(int batch, int seqlen, int nheads, int headdim,
+                                               int dstate) {
+    if (batch < 0 || seqlen < 0 || nheads < 0 || headdim != kP || dstate != kNs) return 0;
+    const size_t nblocks = ((size_t)seqlen + kQ - 1) / kQ;
+    return (size_t)batch * nheads * (nblocks + 1) * kP * kNs * sizeof(float);
+}
+
+extern "C" ssm_status_t ssd_chunked_fwd_ckpt(const void* x, const float* dt, const float* A_head,
+                                             const void* B, const void* C, int chunk,
+                                             const float* initial_state, void* y,
+                                             float* final_state, float* block_states, int batch,
+                                             int seqlen, int nheads, int headdim, int dstate,
+                                             int ngroups, ssm_dtype_t in_dtype,
+                                             ssm_dtype_t out_dtype, void* stream) {
+    if (!block_states && batch > 0 && nheads > 0 && seqlen > 0) return SSM_ERR_NULL;
+    return ssd_entry(x, dt, nullptr, A_head, B, C, chunk, 1, initial_state, nullptr, nullptr, y,
+                     final_state, block_states, batch, seqlen, nheads, headdim, dstate, ngroups,
+                     in_dtype, out_dtype, false, stream);
 }
 
 extern "C" ssm_status_t ssd_mamba3_fwd(const void* x, const float* dt, const float* lam,
@@ -734,8 +769,8 @@ extern "C" ssm_status_t ssd_mamba3_fwd(const void* x, const float* dt, const flo
                                        int dstate, int ngroups, ssm_dtype_t in_dtype,
                                        ssm_dtype_t out_dtype, void* stream) {
     return ssd_entry(x, dt, lam, A_head, B, C, chunk, 1, initial_state, prev_B, prev_x, y,
-                     final_state, batch, seqlen, nheads, headdim, dstate, ngroups, in_dtype,
-                     out_dtype, true, stream);
+                     final_state, nullptr, batch, seqlen, nheads, headdim, dstate, ngroups,
+                     in_dtype, out_dtype, true, stream);
 }
 
 extern "C" ssm_status_t ssd_mamba3_mimo_fwd(const void* x, const float* dt, const float* lam,
@@ -747,6 +782,6 @@ extern "C" ssm_status_t ssd_mamba3_mimo_fwd(const void* x, const float* dt, cons
                                             ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
                                             void* stream) {
     return ssd_entry(x, dt, lam, A_head, B, C, chunk, rank, initial_state, prev_B, prev_x, y,
-                     final_state, batch, seqlen, nheads, headdim, dstate, ngroups, in_dtype,
-                     out_dtype, true, stream);
+                     final_state, nullptr, batch, seqlen, nheads, headdim, dstate, ngroups,
+                     in_dtype, out_dtype, true, stream);
 }

@@ -750,7 +750,8 @@ extern "C" size_t ssd_chunked_bwd_workspace_bytes(int batch, int seqlen, int nhe
 extern "C" ssm_status_t ssd_chunked_bwd(const void* x, const float* dt, const float* A_head,
                                         const void* B, const void* C, int chunk,
                                         const float* initial_state, const void* dy,
-                                        const float* dfinal_state, float* dx, float* ddt,
+                                        const float* dfinal_state, const float* block_states,
+                                        float* dx, float* ddt,
                                         float* dA_head, float* dB, float* dC,
                                         float* dinitial_state, int batch, int seqlen, int nheads,
                                         int headdim, int dstate, int ngroups, ssm_dtype_t in_dtype,
@@ -772,15 +773,17 @@ extern "C" ssm_status_t ssd_chunked_bwd(const void* x, const float* dt, const fl
     if (work && (!x || !dt || !A_head || !B || !C || !dy || !dx || !ddt || !dB || !dC))
         return SSM_ERR_NULL;
     if (work && !workspace) return SSM_ERR_WORKSPACE;
-    const void* ptrs[] = {x, dt, A_head, B, C, initial_state, dy, dfinal_state, dx, ddt,
-                          dA_head, dB, dC, dinitial_state, workspace};
+    const void* ptrs[] = {x, dt, A_head, B, C, initial_state, dy, dfinal_state, block_states, dx,
+                          ddt, dA_head, dB, dC, dinitial_state, workspace};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return SSM_ERR_ALIGN;
     const size_t xb = steps * nheads * headdim * 2, bcb = steps * ngroups * dstate * 2;
     struct R { const void* p; size_t n; };
     const R ins[] = {{x, xb}, {dt, steps * nheads * 4}, {A_head, (size_t)nheads * 4}, {B, bcb},
                      {C, bcb}, {initial_state, initial_state ? sb : 0}, {dy, xb},
-                     {dfinal_state, dfinal_state ? sb : 0}};
+                     {dfinal_state, dfinal_state ? sb : 0},
+                     {block_states,
+                      block_states ? sb * (((size_t)seqlen + kQ - 1) / kQ + 1) : 0}};
     const R outs[] = {{dx, steps * nheads * headdim * 4}, {ddt, steps * nheads * 4},
                       {dA_head, (size_t)nheads * 4}, {dB, bcb * 2}, {dC, bcb * 2},
                       {dinitial_state, dinitial_state ? sb : 0}};
@@ -817,7 +820,7 @@ extern "C" ssm_status_t ssd_chunked_bwd(const void* x, const float* dt, const fl
     BwdArgs a{};
     a.dt = dt;
     a.A = A_head;
-    a.bstates = bstates;
+    a.bstates = block_states ? block_states : bstates;
     a.dfinal = dfinal_state;
     a.dx = dx;
     a.ddt = ddt;
@@ -831,10 +834,13 @@ extern "C" ssm_status_t ssd_chunked_bwd(const void* x, const float* dt, const fl
     a.nheads = nheads;
     a.ngroups = ngroups;
 
-    // 1. the state entering every block (and the final state)
-    ssm_status_t rc = ssd_internal::ssd_forward_block_states(
-        x, dt, A_head, B, C, initial_state, bstates, batch, seqlen, nheads, ngroups, s);
-    if (rc != SSM_OK) return rc;
+    // 1. the state entering every block (and the final state), unless the
+    // forward kept them
+    if (!block_states) {
+        const ssm_status_t rc = ssd_internal::ssd_forward_block_states(
+            x, dt, A_head, B, C, initial_state, bstates, batch, seqlen, nheads, ngroups, s);
+        if (rc != SSM_OK) return rc;
+    }
     // 2. the blocks in reverse, one CTA per (batch, head)
     CUtensorMap mc, mb, mx, mdy;
     if (!ssd_host::make_bc_map(&mc, C, batch, seqlen, ngroups) ||

@@ -301,7 +301,8 @@ def ssd_bwd_call(L, **kw):
     args.update(kw)
     a = args
     return L.ssd_chunked_bwd(a["x"], a["dt"], a["A"], a["B"], a["C"], a["chunk"], a["h0"], a["dy"],
-                             a["dfs"], a["dx"], a["ddt"], a["dA"], a["dB"], a["dC"], a["dh0"],
+                             a["dfs"], a.get("bs"), a["dx"], a["ddt"], a["dA"], a["dB"], a["dC"],
+                             a["dh0"],
                              a["batch"], a["seqlen"], a["nheads"], a["headdim"], a["dstate"],
                              a["ngroups"], a["in_dt"], a["ws"], a["wsb"], a["stream"])
 
@@ -325,6 +326,7 @@ def test_ssd_bwd_argument_errors(L):
     assert ssd_bwd_call(L, dx=P(0)) == ALIAS           # dx on top of x
     assert ssd_bwd_call(L, dC=P(9)) == ALIAS           # dB and dC on one buffer
     assert ssd_bwd_call(L, ws=P(8)) == ALIAS           # workspace on top of dA
+    assert ssd_bwd_call(L, bs=P(6)) == ALIAS           # block states under dx
     # no heads: nothing to write
     assert ssd_bwd_call(L, nheads=0, dA=None, x=None) == OK
 

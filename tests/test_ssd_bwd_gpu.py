@@ -172,3 +172,29 @@ def test_ssd_bwd_directional_derivatives(name, grad):
     # O(eps^2) truncation; the bound also scales with sum |g v| (a random
     # direction can make <g, v> cancel far below its terms)
     assert abs(fd - an) <= 5e-3 * abs(an) + 1e-3 * float(terms.abs().sum()), (name, fd, an)
+
+
+def test_ssd_block_states_from_the_forward():
+    """ssd_chunked_fwd with block states gives the plain forward's y and final
+    state bit for bit, and ssd_chunked_bwd from those states gives the same bits
+    as ssd_chunked_bwd recomputing them."""
+    batch, seqlen, nheads = 2, 320, 4
+    inp = inputs.ssd_inputs(batch, seqlen, nheads, 64, 128, 2, "bf16", seed=150)
+    d = {k: v.cuda() for k, v in inp.items()}
+    h0 = 0.1 * torch.randn(batch, nheads, 64, 128, generator=torch.Generator().manual_seed(151))
+    h0 = h0.cuda()
+    args = (d["x"], d["dt"], d["A_head"], d["B"], d["C"], 64)
+    y0, f0 = binding.ssd_chunked_fwd(*args, out_dtype=torch.float32, initial_state=h0)
+    bs = torch.full((binding.ssd_chunked_checkpoint_bytes(batch, seqlen, nheads) // 4,),
+                    float("nan"), device="cuda")
+    y1, f1 = binding.ssd_chunked_fwd(*args, out_dtype=torch.float32, initial_state=h0,
+                                     block_states=bs)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1) and torch.equal(f0, f1)
+    assert not torch.isnan(bs).any()
+    dy, dfinal = _cotangents(batch, seqlen, nheads, 152, True)
+    g0 = binding.ssd_chunked_bwd(*args[:5], dy.cuda(), 64, h0, dfinal.cuda())
+    g1 = binding.ssd_chunked_bwd(*args[:5], dy.cuda(), 64, h0, dfinal.cuda(), block_states=bs)
+    torch.cuda.synchronize()
+    for k, v in g0.items():
+        assert torch.equal(v, g1[k]), k
