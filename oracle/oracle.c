@@ -1031,6 +1031,130 @@ void oracle_ssd_bwd(const double* x, const double* dt, const double* A_head,
     free(adj);
 }
 
+/*
+ * Gradient of oracle_mamba3_recurrence for the loss  sum dy . y + sum dfinal .
+ * final_state, by differentiating Eq. 9 in reverse.  With Lambda_t = dL/dS_t:
+ *   Lambda_t = dy_t (outer) C_t + alpha_{t+1} Lambda_{t+1}
+ *   dC_t    += dy_t S_t
+ *   x_t and B_t enter twice: with gamma_t at step t and with beta_{t+1} at step t + 1:
+ *   dx_t     = gamma_t Lambda_t . B_t + beta_{t+1} Lambda_{t+1} . B_t
+ *   dB_t    += (gamma_t Lambda_t + beta_{t+1} Lambda_{t+1}) x_t
+ *   d gamma_t = x_t Lambda_t . B_t,  d beta_t = x_{t-1} Lambda_t . B_{t-1},
+ *   d alpha_t = Lambda_t . S_{t-1}
+ * then through alpha = exp(dt A), gamma = lambda dt, beta = dt (1 - lambda) alpha
+ * to ddt, dlambda and dA.  The token before the first (prev_B, prev_x) takes
+ * the t = 0 beta term's gradient; dh0 = alpha_0 Lambda_0.  Serial over rows.
+ * Arguments as oracle_mamba3_recurrence plus dy, dfinal in; out: dx, ddt,
+ * dlam, dA (nheads), dB, dC, dh0 (may be NULL), dprev_B, dprev_x (NULL when
+ * prev_B is).
+ */
+void oracle_mamba3_bwd(const double* x, const double* dt, const double* lam,
+                       const double* A_head, const double* Bm, const double* Cm,
+                       const double* h0, const double* prev_B, const double* prev_x,
+                       const double* dy, const double* dfinal,
+                       double* dx, double* ddt, double* dlam, double* dA, double* dB,
+                       double* dC, double* dh0, double* dprev_B, double* dprev_x,
+                       int batch, int seqlen, int nheads, int headdim, int dstate, int ngroups)
+{
+    const int heads_per_group = nheads / ngroups;
+    const size_t nbc = (size_t)batch * seqlen * ngroups * dstate;
+    memset(ddt, 0, sizeof(double) * (size_t)batch * seqlen * nheads);
+    memset(dlam, 0, sizeof(double) * (size_t)batch * seqlen * nheads);
+    memset(dA, 0, sizeof(double) * (size_t)nheads);
+    memset(dB, 0, sizeof(double) * nbc);
+    memset(dC, 0, sizeof(double) * nbc);
+    if (dprev_B) memset(dprev_B, 0, sizeof(double) * (size_t)batch * ngroups * dstate);
+    double* St = (double*)malloc(sizeof(double) * (size_t)(seqlen + 1) * dstate);  /* S_{t-1} at t */
+    double* adj = (double*)malloc(sizeof(double) * (size_t)dstate);      /* Lambda_t */
+    double* carry = (double*)malloc(sizeof(double) * (size_t)dstate);    /* alpha_{t+1} Lambda_{t+1} */
+    double* later = (double*)malloc(sizeof(double) * (size_t)dstate);    /* Lambda_{t+1} */
+    const long long rows = (long long)batch * nheads * headdim;
+    for (long long row = 0; row < rows; ++row) {
+        const int p = (int)(row % headdim);
+        const int h = (int)((row / headdim) % nheads);
+        const int b = (int)(row / ((long long)headdim * nheads));
+        const int g = h / heads_per_group;
+        const double* pB = prev_B ? prev_B + ((size_t)b * ngroups + g) * dstate : NULL;
+        const double px = prev_x ? prev_x[row] : 0.0;
+        /* forward, every state kept */
+        for (int n = 0; n < dstate; ++n) St[n] = h0 ? h0[row * dstate + n] : 0.0;
+        for (int t = 0; t < seqlen; ++t) {
+            const size_t bt = (size_t)b * seqlen + t;
+            const double step = dt[bt * nheads + h];
+            const double decay = exp(A_head[h] * step);
+            const double gam = lam[bt * nheads + h] * step;
+            const double bet = (step - gam) * decay;
+            const double xin = x[(bt * nheads + h) * headdim + p];
+            const double xlast = t > 0 ? x[((bt - 1) * nheads + h) * headdim + p] : px;
+            const double* Bcur = Bm + (bt * ngroups + g) * dstate;
+            const double* Blast = t > 0 ? Bm + ((bt - 1) * ngroups + g) * dstate : pB;
+            for (int n = 0; n < dstate; ++n)
+                St[(size_t)(t + 1) * dstate + n] = decay * St[(size_t)t * dstate + n] +
+                                                   bet * (Blast ? Blast[n] : 0.0) * xlast +
+                                                   gam * Bcur[n] * xin;
+        }
+        /* reverse */
+        for (int n = 0; n < dstate; ++n) {
+            carry[n] = dfinal ? dfinal[row * dstate + n] : 0.0;
+            later[n] = 0.0;
+        }
+        double bet_next = 0.0;  /* beta_{t+1} (none past the last step) */
+        for (int t = seqlen - 1; t >= 0; --t) {
+            const size_t bt = (size_t)b * seqlen + t;
+            const size_t ix = (bt * nheads + h) * headdim + p;
+            const double step = dt[bt * nheads + h];
+            const double lv = lam[bt * nheads + h];
+            const double decay = exp(A_head[h] * step);
+            const double gam = lv * step;
+            const double bet = (step - gam) * decay;
+            const double xin = x[ix], dyv = dy[ix];
+            const double xlast = t > 0 ? x[((bt - 1) * nheads + h) * headdim + p] : px;
+            const double* Bcur = Bm + (bt * ngroups + g) * dstate;
+            const double* Blast = t > 0 ? Bm + ((bt - 1) * ngroups + g) * dstate : pB;
+            const double* Ccur = Cm + (bt * ngroups + g) * dstate;
+            double* dBcur = dB + (bt * ngroups + g) * dstate;
+            double* dCcur = dC + (bt * ngroups + g) * dstate;
+            double on_B = 0.0, later_on_B = 0.0, on_Blast = 0.0, on_S = 0.0;
+            for (int n = 0; n < dstate; ++n) {
+                adj[n] = dyv * Ccur[n] + carry[n];
+                dCcur[n] += dyv * St[(size_t)(t + 1) * dstate + n];
+                on_B += adj[n] * Bcur[n];
+                later_on_B += later[n] * Bcur[n];
+                if (Blast) on_Blast += adj[n] * Blast[n];
+                on_S += adj[n] * St[(size_t)t * dstate + n];
+                dBcur[n] += (gam * adj[n] + bet_next * later[n]) * xin;
+            }
+            dx[ix] = gam * on_B + bet_next * later_on_B;
+            const double d_gam = xin * on_B;
+            const double d_bet = xlast * on_Blast;
+            const double d_alpha = on_S;
+            ddt[bt * nheads + h] += d_gam * lv +
+                                    d_bet * ((1.0 - lv) * decay + step * (1.0 - lv) * A_head[h] * decay) +
+                                    d_alpha * A_head[h] * decay;
+            dlam[bt * nheads + h] += d_gam * step - d_bet * step * decay;
+            dA[h] += d_bet * step * (1.0 - lv) * step * decay + d_alpha * step * decay;
+            if (t == 0 && pB) {
+                if (dprev_x) dprev_x[row] = bet * on_Blast;
+                if (dprev_B)
+                    for (int n = 0; n < dstate; ++n)
+                        dprev_B[((size_t)b * ngroups + g) * dstate + n] += bet * adj[n] * px;
+            }
+            for (int n = 0; n < dstate; ++n) {
+                later[n] = adj[n];
+                carry[n] = decay * adj[n];
+            }
+            bet_next = bet;
+        }
+        if (dh0)
+            for (int n = 0; n < dstate; ++n) dh0[row * dstate + n] = carry[n];
+        if (dprev_x && seqlen == 0) dprev_x[row] = 0.0;
+    }
+    free(St);
+    free(adj);
+    free(carry);
+    free(later);
+}
+
 int oracle_num_threads(void)
 {
     int n = 1;

@@ -789,3 +789,69 @@ def test_ssd_bwd_is_linear_in_the_cotangents():
     g3 = oracle.ssd_bwd(*args, dy + 2 * dy2, c["h0"], dfinal + 2 * df2)
     for k in g1:
         np.testing.assert_allclose(g3[k], g1[k] + 2 * g2[k], rtol=1e-11, atol=1e-12, err_msg=k)
+
+
+# --------------------------------------------------- Mamba-3 backward pins
+
+def _m3_bwd_case(seed, ngroups, use_h0, use_prev):
+    rng = _rng(seed)
+    batch, seqlen, nheads, headdim, dstate = 2, 5, 4, 3, 4
+    c = dict(x=rng.standard_normal((batch, seqlen, nheads, headdim)),
+             dt=rng.uniform(0.05, 0.6, (batch, seqlen, nheads)),
+             lam=rng.uniform(0.05, 0.95, (batch, seqlen, nheads)),
+             A_head=-rng.uniform(0.5, 2.0, nheads),
+             B=rng.standard_normal((batch, seqlen, ngroups, dstate)),
+             C=rng.standard_normal((batch, seqlen, ngroups, dstate)),
+             h0=rng.standard_normal((batch, nheads, headdim, dstate)) if use_h0 else None,
+             prev_B=rng.standard_normal((batch, ngroups, dstate)) if use_prev else None,
+             prev_x=rng.standard_normal((batch, nheads, headdim)) if use_prev else None)
+    dy = rng.standard_normal((batch, seqlen, nheads, headdim))
+    dfinal = rng.standard_normal((batch, nheads, headdim, dstate))
+    return c, dy, dfinal
+
+
+def _m3_loss(c, dy, dfinal):
+    y, hs = oracle.mamba3_recurrence(c["x"], c["dt"], c["lam"], c["A_head"], c["B"], c["C"],
+                                     c["h0"], c["prev_B"], c["prev_x"])
+    return float(np.sum(dy * y) + np.sum(dfinal * hs))
+
+
+@pytest.mark.parametrize("ngroups,use_h0,use_prev", [(1, True, True), (2, False, True),
+                                                     (4, True, False)])
+def test_mamba3_bwd_equals_finite_differences(ngroups, use_h0, use_prev):
+    """Every entry of the Mamba-3 gradient (x, dt, lambda, A, B, C, h0 and the
+    previous token) against a central difference of the Eq. 9 recurrence
+    oracle's loss sum(dy y) + sum(dfinal final_state)."""
+    c, dy, dfinal = _m3_bwd_case(401 + ngroups, ngroups, use_h0, use_prev)
+    g = oracle.mamba3_bwd(c["x"], c["dt"], c["lam"], c["A_head"], c["B"], c["C"], dy, c["h0"],
+                          c["prev_B"], c["prev_x"], dfinal)
+    names = {"x": "dx", "dt": "ddt", "lam": "dlam", "A_head": "dA", "B": "dB", "C": "dC",
+             "h0": "dh0", "prev_B": "dprev_B", "prev_x": "dprev_x"}
+    eps = 1e-6
+    for k, gk in names.items():
+        if c[k] is None:
+            continue
+        fd = np.zeros_like(c[k])
+        for idx in np.ndindex(c[k].shape):
+            cp = {kk: (None if vv is None else vv.copy()) for kk, vv in c.items()}
+            cp[k][idx] += eps
+            lp = _m3_loss(cp, dy, dfinal)
+            cp[k][idx] -= 2 * eps
+            lm = _m3_loss(cp, dy, dfinal)
+            fd[idx] = (lp - lm) / (2 * eps)
+        np.testing.assert_allclose(g[gk], fd, rtol=1e-6, atol=1e-7, err_msg=k)
+
+
+def test_mamba3_bwd_at_lambda_one_is_the_ssd_gradient():
+    """At lambda = 1 (beta = 0, gamma = dt) and no previous token, Eq. 9 is the
+    Mamba-2 recurrence: the gradients match the SSD gradient oracle's, and the
+    lambda gradient is the derivative through gamma and beta alone."""
+    c, dy, dfinal = _m3_bwd_case(431, 2, True, False)
+    lam1 = np.ones_like(c["lam"])
+    g = oracle.mamba3_bwd(c["x"], c["dt"], lam1, c["A_head"], c["B"], c["C"], dy, c["h0"],
+                          None, None, dfinal)
+    s = oracle.ssd_bwd(c["x"], c["dt"], c["A_head"], c["B"], c["C"], dy, c["h0"], dfinal)
+    tol = dict(rtol=1e-11, atol=1e-12)
+    for k, sk in (("dx", "dx"), ("ddt", "ddt"), ("dA", "dA"), ("dB", "dB"), ("dC", "dC"),
+                  ("dh0", "dh0")):
+        np.testing.assert_allclose(g[k], s[sk], err_msg=k, **tol)

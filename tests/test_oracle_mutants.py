@@ -79,6 +79,13 @@ MUTANTS = {
         "sum_dt += adj[n] * (A_head[h] * decay * s_prev);"),
     "ssd_bwd_dA_undecayed_state": ("dA[h] += adj[n] * step_dt * decay * s_prev;",
                                    "dA[h] += adj[n] * step_dt * s_prev;"),
+    "m3_bwd_dx_drops_beta_term": ("dx[ix] = gam * on_B + bet_next * later_on_B;",
+                                  "dx[ix] = gam * on_B;"),
+    "m3_bwd_dlam_sign": ("dlam[bt * nheads + h] += d_gam * step - d_bet * step * decay;",
+                         "dlam[bt * nheads + h] += d_gam * step + d_bet * step * decay;"),
+    "m3_bwd_adjoint_not_decayed": ("carry[n] = decay * adj[n];", "carry[n] = adj[n];"),
+    "m3_bwd_prev_x_weight": ("if (dprev_x) dprev_x[row] = bet * on_Blast;",
+                             "if (dprev_x) dprev_x[row] = gam * on_Blast;"),
     "mamba3_decode_terms_swapped": (
         "s[n] = alpha * s[n] + beta * Bp[n] * xp + gamma * Bt[n] * xv;",
         "s[n] = alpha * s[n] + beta * Bt[n] * xv + gamma * Bp[n] * xp;"),
