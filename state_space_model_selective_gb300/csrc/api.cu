@@ -23,7 +23,7 @@ EncodeTiledFn encode_tiled_fn() {
 }
 
 bool make_tmap_2d(CUtensorMap* map, const void* base, ssm_dtype_t dtype, uint64_t rows,
-                  uint64_t cols, uint32_t box_rows, uint32_t box_cols) {
+                  uint64_t cols, uint32_t box_rows, uint32_t box_cols, bool swizzle) {
     EncodeTiledFn fn = encode_tiled_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {cols, rows};
@@ -33,7 +33,8 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, ssm_dtype_t dtype, uint64_
     const CUtensorMapDataType dt =
         dtype == SSM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estride,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

@@ -221,8 +221,8 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 EncodeTiledFn encode_tiled_fn();
 
 // Row-major 2-D tensor (rows x cols, cols contiguous) with a box of
-// box_rows x box_cols, 128-byte swizzle, zero fill out of bounds.
+// box_rows x box_cols, 128-byte swizzle (or none), zero fill out of bounds.
 bool make_tmap_2d(CUtensorMap* map, const void* base, ssm_dtype_t dtype, uint64_t rows,
-                  uint64_t cols, uint32_t box_rows, uint32_t box_cols);
+                  uint64_t cols, uint32_t box_rows, uint32_t box_cols, bool swizzle = true);
 
 }  // namespace ssm_host

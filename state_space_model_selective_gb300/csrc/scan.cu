@@ -16,8 +16,9 @@
 //  * A producer warp streams 64-step tiles of u, delta, z, B and C into a
 //    ring of shared-memory stages with 2-D TMA (128-byte swizzle), tracked
 //    by mbarriers.  The compute warps first "prep" each tile once per
-//    (channel, step) -- dl = softplus(delta + bias) and dl*u -- and convert
-//    B/C to fp32 [t][n], then run the recurrence from shared memory.
+//    (channel, step) -- dl = softplus(delta + bias) and dl*u -- then run the
+//    recurrence, reading B and C straight from their [n][t] tiles (one
+//    16-byte load covers 8 bf16 or 4 fp32 steps of one state).
 //  * y partial sums over the 4 lanes' states are reduce-scattered with warp
 //    shuffles; each lane then finishes 2 of every 8 steps (D skip, silu gate)
 //    and stores them.
@@ -43,6 +44,7 @@ constexpr int kNG = kN / kSPT;  // threads per channel
 constexpr int kTL = 64;         // time steps per tile
 constexpr int kMaxChunks = 32;  // upper bound on L-chunks per channel block
 constexpr int kPrepStride = kTL * 8 + 16;  // bytes per channel row of the prep tile
+constexpr int kGroupUnroll = 4;  // 8-step groups unrolled together
 
 struct alignas(16) WsHeader {
     uint32_t ticket;
@@ -92,6 +94,16 @@ __device__ __forceinline__ int tile_off(int r, int t) {
     return box * (ROWS * 128) + r * 128 + ((((byte >> 4) ^ (r & 7)) << 4) | (byte & 15));
 }
 
+// Byte offset of (row r, step t) in the same boxes without the swizzle (the
+// B and C tiles: every lane of a quarter-warp reads one address, so there
+// are no bank conflicts to spread, and the offsets stay affine in t).
+template <typename T, int ROWS>
+__device__ __forceinline__ int tile_off_lin(int r, int t) {
+    constexpr int E = sizeof(T);
+    constexpr int TPB = 128 / E;
+    return (t / TPB) * (ROWS * 128) + r * 128 + (t % TPB) * E;
+}
+
 // 8 consecutive steps t0..t0+7 (t0 % 8 == 0) of row r, as fp32.
 template <typename T, int ROWS>
 __device__ __forceinline__ void load8(const uint8_t* tile, int r, int t0, float* v) {
@@ -107,21 +119,21 @@ __device__ __forceinline__ void load8(const uint8_t* tile, int r, int t0, float*
     }
 }
 
-// 2 consecutive steps t, t+1 (t even) of row r, as fp32.
-template <typename T, int ROWS>
-__device__ __forceinline__ void load2(const uint8_t* tile, int r, int t, float* v) {
-    if constexpr (sizeof(T) == 2) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(tile + tile_off<T, ROWS>(r, t));
-        v[0] = bf16lo(w); v[1] = bf16hi(w);
-    } else {
-        const float2 a = *reinterpret_cast<const float2*>(tile + tile_off<T, ROWS>(r, t));
-        v[0] = a.x; v[1] = a.y;
-    }
+// Element s of a 16-byte word holding consecutive steps of one row, as fp32
+// (bf16: 8 steps, s in 0..7; fp32: 4 steps, s in 0..3).
+template <typename T>
+__device__ __forceinline__ float word_elem(const uint4& w, int s) {
+    const uint32_t v = s / (sizeof(T) == 2 ? 2 : 1) == 0   ? w.x
+                       : s / (sizeof(T) == 2 ? 2 : 1) == 1 ? w.y
+                       : s / (sizeof(T) == 2 ? 2 : 1) == 2 ? w.z
+                                                           : w.w;
+    if constexpr (sizeof(T) == 2) return (s & 1) ? bf16hi(v) : bf16lo(v);
+    else return __uint_as_float(v);
 }
 
 // Fallback staging when the rows are not 16-byte aligned for TMA: plain
 // loads with bounds checks into the same swizzled layout.
-template <typename T, int ROWS>
+template <typename T, int ROWS, bool SWZ = true>
 __device__ __forceinline__ void stage_plain(uint8_t* tile, const T* src, long long row0,
                                             long long rows_total, int L, int t0, int tid,
                                             int nthreads) {
@@ -131,7 +143,7 @@ __device__ __forceinline__ void stage_plain(uint8_t* tile, const T* src, long lo
         const int tg = t0 + t;
         T v = from_f32<T>(0.0f);
         if (row < rows_total && tg < L) v = src[row * (long long)L + tg];
-        *reinterpret_cast<T*>(tile + tile_off<T, ROWS>(r, t)) = v;
+        *reinterpret_cast<T*>(tile + (SWZ ? tile_off<T, ROWS>(r, t) : tile_off_lin<T, ROWS>(r, t))) = v;
     }
 }
 
@@ -157,7 +169,7 @@ struct Geom {
     static constexpr int E = sizeof(Tin);
     static constexpr int TPB = 128 / E;       // steps per 128-byte box row
     static constexpr int NBOX = kTL / TPB;    // boxes per tile along time
-    static constexpr int kStages = E == 2 ? 3 : 2;
+    static constexpr int kStages = 2;
 };
 
 template <typename Tin, int CH, bool TMA>
@@ -167,10 +179,9 @@ struct Smem {
     static constexpr int BC_TILE = kN * kTL * E;
     static constexpr int STAGE = 3 * IN_TILE + 2 * BC_TILE;
     static constexpr int NSTAGE = TMA ? Geom<Tin>::kStages : 1;
-    static constexpr int PREP = CH * kPrepStride;
-    static constexpr int BCF = (E == 2 ? 1 : 2) * kTL * kN * 4;
+    static constexpr int PREP = 2 * CH * kPrepStride;  // (dl, dl*u) and (D*u, silu(z))
     static constexpr int BARS = 2 * NSTAGE * 8 + 16;
-    static constexpr int BYTES = NSTAGE * STAGE + PREP + BCF + BARS;
+    static constexpr int BYTES = NSTAGE * STAGE + PREP + BARS;
     static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024
 };
 
@@ -190,10 +201,7 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t* stages = smem;
     uint8_t* prep = stages + NSTAGE * S::STAGE;
-    float* bcf = reinterpret_cast<float*>(prep + S::PREP);  // [2][kTL][kN] fp32 B, C
-    uint8_t* bcf_raw = prep + S::PREP;  // bf16 inputs: [kTL][4] 16-byte B/C chunks
-    constexpr bool kPackedBC = sizeof(Tin) == 2;
-    uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(bcf) + S::BCF);
+    uint64_t* full = reinterpret_cast<uint64_t*>(prep + S::PREP);
     uint64_t* empty = full + NSTAGE;
     int* s_ticket = reinterpret_cast<int*>(empty + NSTAGE);
 
@@ -270,8 +278,11 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
 
     // ------------------------------------------------------------- compute
     const int warp = tid >> 5, lane = tid & 31;
-    const int cl = warp * 8 + (lane >> 2);  // channel within the block
-    const int ng = lane & 3;                // which 4 of the 16 states
+    // lanes l, l + 8, l + 16, l + 24 share a channel; a quarter-warp (the
+    // unit a 16-byte shared load serves at once) holds 8 channels with the
+    // same four states, so every B/C load it makes is one broadcast address
+    const int cl = warp * 8 + (lane & 7);  // channel within the block
+    const int ng = lane >> 3;              // which 4 of the 16 states
     const int n0 = ng * kSPT;
     const int d = d0 + cl;
     const bool valid = (cb * CH + cl) < a.dpg;
@@ -283,17 +294,17 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
         A2[k] = valid ? a.A[static_cast<long long>(d) * kN + n0 + k] * kLog2e : 0.0f;
         h[k] = 0.0f;
     }
-    const float Dd = (a.Dskip && valid) ? a.Dskip[d] : 0.0f;
 
-    // prep mapping: one channel, 16 consecutive steps per thread
-    const int pc = tid % CH;
-    const int pq = tid / CH;
-    const bool pvalid = (cb * CH + pc) < a.dpg;
-    const float pbias = (a.bias && pvalid) ? a.bias[d0 + pc] : 0.0f;
+    // prep mapping: each warp preps its own 8 channels (lane: channel cl,
+    // steps 16 pq .. 16 pq + 15), so a tile needs no barrier across warps
+    const int pq = ng;
+    const float pbias = (a.bias && valid) ? a.bias[d] : 0.0f;
+    const float pD = (a.Dskip && valid) ? a.Dskip[d] : 0.0f;
 
+    // prep tile rows: [CH][kTL] (dl, dl*u) pairs, then [CH][kTL] (D*u, g)
+    // pairs, g = silu(z) (1 without a gate)
     const float* prow = reinterpret_cast<const float*>(prep + cl * kPrepStride);
-    const float* Bt = bcf;
-    const float* Ct = bcf + kTL * kN;
+    const float* prow2 = reinterpret_cast<const float*>(prep + (CH + cl) * kPrepStride);
     Tout* yrow = reinterpret_cast<Tout*>(a.y) + drow * a.seqlen;
     // vector stores need the row start aligned to 2 elements; TMA implies it
     const bool vec_store = TMA;
@@ -306,7 +317,7 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
 
         if constexpr (TMA) {
             const bool got = mbar_wait(&full[s], (k / NSTAGE) & 1, a.status);
-            if (!named_bar_and(1, NCOMP, got)) { ok = false; break; }
+            if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
         } else {
             stage_plain<Tin, CH>(st, reinterpret_cast<const Tin*>(a.u), row0,
                                  (long long)a.batch * a.dim, a.seqlen, t0, tid, NCOMP);
@@ -315,25 +326,27 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
             if (has_z)
                 stage_plain<Tin, CH>(st + 2 * S::IN_TILE, reinterpret_cast<const Tin*>(a.z),
                                      row0, (long long)a.batch * a.dim, a.seqlen, t0, tid, NCOMP);
-            stage_plain<Tin, kN>(st + 3 * S::IN_TILE, reinterpret_cast<const Tin*>(a.Bm),
+            stage_plain<Tin, kN, false>(st + 3 * S::IN_TILE, reinterpret_cast<const Tin*>(a.Bm),
                                  bcrow0, (long long)a.batch * a.ngroups * kN, a.seqlen, t0, tid,
                                  NCOMP);
-            stage_plain<Tin, kN>(st + 3 * S::IN_TILE + S::BC_TILE,
+            stage_plain<Tin, kN, false>(st + 3 * S::IN_TILE + S::BC_TILE,
                                  reinterpret_cast<const Tin*>(a.Cm), bcrow0,
                                  (long long)a.batch * a.ngroups * kN, a.seqlen, t0, tid, NCOMP);
             named_bar_sync(1, NCOMP);
         }
 
-        // ---- prep: dl = softplus(delta + bias) (or delta + bias) and dl * u,
-        // once per (channel, step); steps past the chunk end get dl = 0, an
-        // exact identity step (exp(0) = 1, input term 0).
+        // ---- prep, once per (channel, step): dl = softplus(delta + bias)
+        // (or delta + bias), dl * u, and the read-out's D * u and silu(z);
+        // steps past the chunk end get dl = 0, an exact identity step
+        // (exp(0) = 1, input term 0).
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             const int tl = pq * 16 + hh * 8;
-            float uv[8], dv[8];
-            load8<Tin, CH>(st, pc, tl, uv);
-            load8<Tin, CH>(st + S::IN_TILE, pc, tl, dv);
-            float o[16];
+            float uv[8], dv[8], zv[8];
+            load8<Tin, CH>(st, cl, tl, uv);
+            load8<Tin, CH>(st + S::IN_TILE, cl, tl, dv);
+            if (has_z) load8<Tin, CH>(st + 2 * S::IN_TILE, cl, tl, zv);
+            float o[16], e[16];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const float x = dv[j] + pbias;
@@ -341,43 +354,18 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
                 if (t0 + tl + j >= t_end) dl = 0.0f;
                 o[2 * j] = dl;
                 o[2 * j + 1] = dl * uv[j];
+                e[2 * j] = pD * uv[j];
+                e[2 * j + 1] = has_z ? silu_f(zv[j]) : 1.0f;
             }
-            float4* dst = reinterpret_cast<float4*>(prep + pc * kPrepStride + tl * 8);
+            float4* dst = reinterpret_cast<float4*>(prep + cl * kPrepStride + tl * 8);
+            float4* dst2 = reinterpret_cast<float4*>(prep + (CH + cl) * kPrepStride + tl * 8);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < 4; ++j) {
                 dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-        }
-        if constexpr (kPackedBC) {
-            // ---- B, C (bf16, exact): swizzled [n][t] -> per step t, four
-            // 16-byte chunks, chunk g = B[4g..4g+3][t], C[4g..4g+3][t]
-            const uint8_t* tb = st + 3 * S::IN_TILE;
-            const uint8_t* tc = tb + S::BC_TILE;
-            for (int i = tid; i < 4 * kTL; i += NCOMP) {
-                const int t = i % kTL, g4 = i / kTL;
-                uint32_t hb[4], hc[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    hb[k] = *reinterpret_cast<const uint16_t*>(tb + tile_off<Tin, kN>(4 * g4 + k, t));
-                    hc[k] = *reinterpret_cast<const uint16_t*>(tc + tile_off<Tin, kN>(4 * g4 + k, t));
-                }
-                *reinterpret_cast<uint4*>(bcf_raw + (t * 4 + g4) * 16) =
-                    make_uint4(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16), hc[0] | (hc[1] << 16),
-                               hc[2] | (hc[3] << 16));
-            }
-        } else {
-            // ---- B, C: swizzled [n][t] in the input type -> fp32 [t][n]
-            for (int i = tid; i < 2 * kN * (kTL / 8); i += NCOMP) {
-                const int arr = i / (kN * kTL / 8);
-                const int rem = i % (kN * kTL / 8);
-                const int n = rem % kN, j = rem / kN;
-                float v[8];
-                load8<Tin, kN>(st + 3 * S::IN_TILE + arr * S::BC_TILE, n, j * 8, v);
-                float* dst = bcf + arr * kTL * kN;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) dst[(j * 8 + q) * kN + n] = v[q];
+                dst2[j] = make_float4(e[4 * j], e[4 * j + 1], e[4 * j + 2], e[4 * j + 3]);
             }
         }
-        named_bar_sync(1, NCOMP);
+        __syncwarp();
 
         // ---- carried-in state, once per CTA, after the first prep
         if (k == 0) {
@@ -389,7 +377,7 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
                 }
             } else {
                 const uint32_t* flag = a.flags + (size_t)(chunk - 1) * a.nblocks + blk;
-                if (tid == 0) {
+                if (lane == 0) {
                     bool seen = false;
                     uint32_t ns = 32;
                     for (uint32_t it = 0; it < kFlagSpinLimit; ++it) {
@@ -399,7 +387,7 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
                     }
                     if (!seen) record_status(a.status, SSM_ERR_TIMEOUT);
                 }
-                named_bar_sync(1, NCOMP);
+                __syncwarp();
                 (void)ld_acquire_gpu(flag);  // order this thread's reads after the flag
                 if (valid) {
                     const float4 v = __ldcg(reinterpret_cast<const float4*>(
@@ -409,9 +397,13 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
             }
         }
 
-        // ---- the recurrence over the tile, 8 steps per group
-        const uint8_t* tz = st + 2 * S::IN_TILE;
-#pragma unroll 2
+        // ---- the recurrence over the tile, 8 steps per group.  B and C are
+        // read straight from their TMA tiles ([n][t], not swizzled): one
+        // 16-byte load gives 16 / sizeof(Tin) consecutive steps of one state.
+        const uint8_t* tB = st + 3 * S::IN_TILE;
+        const uint8_t* tC = tB + S::BC_TILE;
+        constexpr int SPL = 16 / (int)sizeof(Tin);  // steps per 16-byte load
+#pragma unroll kGroupUnroll
         for (int j = 0; j < kTL / 8; ++j) {
             if (CK && (j & 1) == 0 && valid && t0 + j * 8 < a.seqlen) {
                 const long long seg = (t0 + j * 8) / 16;
@@ -420,72 +412,74 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
                        make_float4(h[0], h[1], h[2], h[3]));
             }
             float yp[8];
+            uint4 wb[kSPT], wc[kSPT];
 #pragma unroll
             for (int q = 0; q < 8; q += 2) {
+                if (q % SPL == 0) {
+#pragma unroll
+                    for (int k = 0; k < kSPT; ++k) {
+                        wb[k] = *reinterpret_cast<const uint4*>(
+                            tB + tile_off_lin<Tin, kN>(n0 + k, j * 8 + q));
+                        wc[k] = *reinterpret_cast<const uint4*>(
+                            tC + tile_off_lin<Tin, kN>(n0 + k, j * 8 + q));
+                    }
+                }
                 const float4 pp = *reinterpret_cast<const float4*>(prow + (j * 8 + q) * 2);
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const int t = j * 8 + q + r;
+                    const int s = (q + r) % SPL;  // step within the loaded words
                     const float dl = r ? pp.z : pp.x;
                     const float du = r ? pp.w : pp.y;
-                    float4 bv, cv;
-                    if constexpr (kPackedBC) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(bcf_raw + (t * 4 + ng) * 16);
-                        bv = make_float4(bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y));
-                        cv = make_float4(bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w));
-                    } else {
-                        bv = *reinterpret_cast<const float4*>(Bt + t * kN + n0);
-                        cv = *reinterpret_cast<const float4*>(Ct + t * kN + n0);
+                    float bv[kSPT], cv[kSPT];
+#pragma unroll
+                    for (int k = 0; k < kSPT; ++k) {
+                        bv[k] = word_elem<Tin>(wb[k], s);
+                        cv[k] = word_elem<Tin>(wc[k], s);
                     }
-                    h[0] = fmaf(ex2_approx(dl * A2[0]), h[0], du * bv.x);
-                    h[1] = fmaf(ex2_approx(dl * A2[1]), h[1], du * bv.y);
-                    h[2] = fmaf(ex2_approx(dl * A2[2]), h[2], du * bv.z);
-                    h[3] = fmaf(ex2_approx(dl * A2[3]), h[3], du * bv.w);
-                    float acc = cv.x * h[0];
-                    acc = fmaf(cv.y, h[1], acc);
-                    acc = fmaf(cv.z, h[2], acc);
-                    acc = fmaf(cv.w, h[3], acc);
+                    h[0] = fmaf(ex2_approx(dl * A2[0]), h[0], du * bv[0]);
+                    h[1] = fmaf(ex2_approx(dl * A2[1]), h[1], du * bv[1]);
+                    h[2] = fmaf(ex2_approx(dl * A2[2]), h[2], du * bv[2]);
+                    h[3] = fmaf(ex2_approx(dl * A2[3]), h[3], du * bv[3]);
+                    float acc = cv[0] * h[0];
+                    acc = fmaf(cv[1], h[1], acc);
+                    acc = fmaf(cv[2], h[2], acc);
+                    acc = fmaf(cv[3], h[3], acc);
                     yp[q + r] = acc;
                 }
             }
-            // reduce-scatter the 8 partial sums over the 4 lanes of the channel:
-            // afterwards lane ng holds the full sums of steps 2ng and 2ng+1.
+            // reduce-scatter the 8 partial sums over the 4 lanes of the channel
+            // (lane bits 3 and 4): afterwards lane ng holds the full sums of
+            // steps 2ng and 2ng+1, added as (p0 + p2) + (p1 + p3).
+            float f[2];
             const bool hi2 = ng & 2, hi1 = ng & 1;
             float k4[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float send = hi2 ? yp[i] : yp[i + 4];
                 const float keep = hi2 ? yp[i + 4] : yp[i];
-                k4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+                k4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
             }
-            float f[2];
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const float send = hi1 ? k4[i] : k4[i + 2];
                 const float keep = hi1 ? k4[i + 2] : k4[i];
-                f[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+                f[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
             }
             const int tl = j * 8 + 2 * ng;
             const int tg = t0 + tl;
-            float uu[2];
-            load2<Tin, CH>(st, cl, tl, uu);
-            float o0 = fmaf(Dd, uu[0], f[0]);
-            float o1 = fmaf(Dd, uu[1], f[1]);
-            if (has_z) {
-                float zz[2];
-                load2<Tin, CH>(tz, cl, tl, zz);
-                o0 *= silu_f(zz[0]);
-                o1 *= silu_f(zz[1]);
-            }
+            const float4 eg = *reinterpret_cast<const float4*>(prow2 + tl * 2);
+            const float o0 = (f[0] + eg.x) * eg.y;
+            const float o1 = (f[1] + eg.z) * eg.w;
             if ((!CK || a.y) && valid && tg < t_end)
                 store_y2<Tout>(yrow + tg, o0, o1, true, tg + 1 < t_end, vec_store);
         }
 
+        __syncwarp();  // this warp's prep rows are rewritten by the next tile
         if constexpr (TMA) {
-            __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
+        } else {
+            named_bar_sync(1, NCOMP);  // the single stage is restaged next
         }
-        named_bar_sync(1, NCOMP);  // prep / bcf are rewritten by the next tile
     }
 
     // ---- outgoing state: final_state for the last chunk, else the carry
@@ -628,8 +622,10 @@ ssm_status_t dispatch(ScanArgs& a, ssm_dtype_t in_dtype, bool tma, cudaStream_t 
         const uint32_t tpb = Geom<Tin>::TPB;
         bool okm = ssm_host::make_tmap_2d(&maps[0], a.u, in_dtype, rows, a.seqlen, 32, tpb) &&
                    ssm_host::make_tmap_2d(&maps[1], a.delta, in_dtype, rows, a.seqlen, 32, tpb) &&
-                   ssm_host::make_tmap_2d(&maps[3], a.Bm, in_dtype, bcrows, a.seqlen, kN, tpb) &&
-                   ssm_host::make_tmap_2d(&maps[4], a.Cm, in_dtype, bcrows, a.seqlen, kN, tpb);
+                   ssm_host::make_tmap_2d(&maps[3], a.Bm, in_dtype, bcrows, a.seqlen, kN, tpb,
+                                          false) &&
+                   ssm_host::make_tmap_2d(&maps[4], a.Cm, in_dtype, bcrows, a.seqlen, kN, tpb,
+                                          false);
         if (okm && a.z)
             okm = ssm_host::make_tmap_2d(&maps[2], a.z, in_dtype, rows, a.seqlen, 32, tpb);
         if (!okm) return SSM_ERR_CUDA;
