@@ -119,21 +119,68 @@ __device__ __forceinline__ void load8(const uint8_t* tile, int r, int t0, float*
     }
 }
 
-// Element s of a 16-byte word holding consecutive steps of one row, as fp32
-// (bf16: 8 steps, s in 0..7; fp32: 4 steps, s in 0..3).
+// 8 consecutive steps t0..t0+7 (t0 % 8 == 0) of row n of an unswizzled
+// B or C tile, as fp32.
 template <typename T>
-__device__ __forceinline__ float word_elem(const uint4& w, int s) {
-    const uint32_t v = s / (sizeof(T) == 2 ? 2 : 1) == 0   ? w.x
-                       : s / (sizeof(T) == 2 ? 2 : 1) == 1 ? w.y
-                       : s / (sizeof(T) == 2 ? 2 : 1) == 2 ? w.z
-                                                           : w.w;
-    if constexpr (sizeof(T) == 2) return (s & 1) ? bf16hi(v) : bf16lo(v);
-    else return __uint_as_float(v);
+__device__ __forceinline__ void row8_lin(const uint8_t* tile, int n, int t0, float* v) {
+    if constexpr (sizeof(T) == 2) {
+        const uint4 w = *reinterpret_cast<const uint4*>(tile + tile_off_lin<T, kN>(n, t0));
+        v[0] = bf16lo(w.x); v[1] = bf16hi(w.x); v[2] = bf16lo(w.y); v[3] = bf16hi(w.y);
+        v[4] = bf16lo(w.z); v[5] = bf16hi(w.z); v[6] = bf16lo(w.w); v[7] = bf16hi(w.w);
+    } else {
+        const float4 x = *reinterpret_cast<const float4*>(tile + tile_off_lin<T, kN>(n, t0));
+        const float4 y = *reinterpret_cast<const float4*>(tile + tile_off_lin<T, kN>(n, t0 + 4));
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+        v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+    }
+}
+
+// In-place conversion, by one warp (lane pl), of a stage's B and C tiles
+// ([n][t] in the input type, B then C from the region's start) into fp32 rows
+// [t][group g][B[4g..4g+3], C[4g..4g+3]] of 128 bytes per step.  Every lane
+// reads its values before any lane writes.
+template <typename T>
+__device__ __forceinline__ void convert_bc(uint8_t* region, int pl) {
+    constexpr int BC_TILE = kN * kTL * (int)sizeof(T);
+    const int g = pl & 3, blk = pl >> 2;  // states 4g..4g+3, steps 8 blk..8 blk+7
+    float vb[4][8], vc[4][8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        row8_lin<T>(region, 4 * g + k, 8 * blk, vb[k]);
+        row8_lin<T>(region + BC_TILE, 4 * g + k, 8 * blk, vc[k]);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+        float4* dst = reinterpret_cast<float4*>(region + (8 * blk + s) * 128 + g * 32);
+        dst[0] = make_float4(vb[0][s], vb[1][s], vb[2][s], vb[3][s]);
+        dst[1] = make_float4(vc[0][s], vc[1][s], vc[2][s], vc[3][s]);
+    }
+}
+
+// B and C of one tile straight into the fp32 [t][group] rows, with plain
+// loads and bounds checks (rows not 16-byte aligned for TMA).
+template <typename T>
+__device__ __forceinline__ void stage_bc_plain(uint8_t* region, const T* Bm, const T* Cm,
+                                               long long row0, int L, int t0, int tid,
+                                               int nthreads) {
+    for (int i = tid; i < kN * kTL; i += nthreads) {
+        const int n = i / kTL, t = i % kTL;
+        const int tg = t0 + t;
+        float vb = 0.0f, vc = 0.0f;
+        if (tg < L) {
+            vb = to_f32(Bm[(row0 + n) * (long long)L + tg]);
+            vc = to_f32(Cm[(row0 + n) * (long long)L + tg]);
+        }
+        float* dst = reinterpret_cast<float*>(region + t * 128 + (n / 4) * 32) + (n % 4);
+        dst[0] = vb;
+        dst[4] = vc;
+    }
 }
 
 // Fallback staging when the rows are not 16-byte aligned for TMA: plain
 // loads with bounds checks into the same swizzled layout.
-template <typename T, int ROWS, bool SWZ = true>
+template <typename T, int ROWS>
 __device__ __forceinline__ void stage_plain(uint8_t* tile, const T* src, long long row0,
                                             long long rows_total, int L, int t0, int tid,
                                             int nthreads) {
@@ -143,7 +190,7 @@ __device__ __forceinline__ void stage_plain(uint8_t* tile, const T* src, long lo
         const int tg = t0 + t;
         T v = from_f32<T>(0.0f);
         if (row < rows_total && tg < L) v = src[row * (long long)L + tg];
-        *reinterpret_cast<T*>(tile + (SWZ ? tile_off<T, ROWS>(r, t) : tile_off_lin<T, ROWS>(r, t))) = v;
+        *reinterpret_cast<T*>(tile + tile_off<T, ROWS>(r, t)) = v;
     }
 }
 
@@ -177,10 +224,14 @@ struct Smem {
     static constexpr int E = sizeof(Tin);
     static constexpr int IN_TILE = CH * kTL * E;
     static constexpr int BC_TILE = kN * kTL * E;
-    static constexpr int STAGE = 3 * IN_TILE + 2 * BC_TILE;
+    // B and C of a tile as fp32 [t][4 state groups][B 4 states, C 4 states];
+    // the TMA tiles of B and C land in its front half and are converted in place
+    static constexpr int BCF = kTL * kN * 2 * 4;
+    static_assert(2 * BC_TILE <= BCF, "the B/C tiles fit the converted region");
+    static constexpr int STAGE = 3 * IN_TILE + BCF;
     static constexpr int NSTAGE = TMA ? Geom<Tin>::kStages : 1;
     static constexpr int PREP = 2 * CH * kPrepStride;  // (dl, dl*u) and (D*u, silu(z))
-    static constexpr int BARS = 2 * NSTAGE * 8 + 16;
+    static constexpr int BARS = 3 * NSTAGE * 8 + 16;
     static constexpr int BYTES = NSTAGE * STAGE + PREP + BARS;
     static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024
 };
@@ -201,8 +252,9 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t* stages = smem;
     uint8_t* prep = stages + NSTAGE * S::STAGE;
-    uint64_t* full = reinterpret_cast<uint64_t*>(prep + S::PREP);
-    uint64_t* empty = full + NSTAGE;
+    uint64_t* full = reinterpret_cast<uint64_t*>(prep + S::PREP);  // TMA bytes landed
+    uint64_t* ready = full + NSTAGE;   // B/C converted: the tile can be used
+    uint64_t* empty = ready + NSTAGE;  // the compute warps are done with the stage
     int* s_ticket = reinterpret_cast<int*>(empty + NSTAGE);
 
     const int tid = threadIdx.x;
@@ -211,6 +263,7 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
         if constexpr (TMA) {
             for (int s = 0; s < NSTAGE; ++s) {
                 mbar_init(&full[s], 1);
+                mbar_init(&ready[s], 1);
                 mbar_init(&empty[s], NCOMP / 32);
             }
             fence_mbar_init();
@@ -234,44 +287,78 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
     const bool has_z = a.z != nullptr;
 
     // ------------------------------------------------------------ producer
+    // One warp: lane 0 issues the TMA loads of each tile; once a tile has
+    // landed the whole warp converts its B and C to the fp32 [t][n] layout
+    // the recurrence reads (while the compute warps work on the previous
+    // tile), then releases it on `ready`.
     if (tid >= NCOMP) {
         if constexpr (TMA) {
-            if (tid == NCOMP) {
+            const int pl = tid - NCOMP;
+            if (pl == 0) {
                 prefetch_tensormap(&tm_u);
                 prefetch_tensormap(&tm_d);
                 if (has_z) prefetch_tensormap(&tm_z);
                 prefetch_tensormap(&tm_B);
                 prefetch_tensormap(&tm_C);
-                const uint32_t bytes = (has_z ? 3 : 2) * S::IN_TILE + 2 * S::BC_TILE;
-                int issued = 0;
-                for (int k = 0; k < ntiles; ++k) {
-                    const int s = k % NSTAGE;
-                    if (k >= NSTAGE && !mbar_wait(&empty[s], ((k / NSTAGE) & 1) ^ 1, a.status))
-                        break;
-                    mbar_arrive_expect_tx(&full[s], bytes);
-                    uint8_t* st = stages + s * S::STAGE;
-                    const int t0 = t_begin + k * kTL;
-#pragma unroll
-                    for (int bx = 0; bx < G::NBOX; ++bx) {
-                        const int tc = t0 + bx * G::TPB;
-                        tma_load_2d(st + bx * CH * 128, &tm_u, &full[s], tc, (int)row0);
-                        tma_load_2d(st + S::IN_TILE + bx * CH * 128, &tm_d, &full[s], tc,
-                                    (int)row0);
-                        if (has_z)
-                            tma_load_2d(st + 2 * S::IN_TILE + bx * CH * 128, &tm_z, &full[s], tc,
-                                        (int)row0);
-                        tma_load_2d(st + 3 * S::IN_TILE + bx * kN * 128, &tm_B, &full[s], tc,
-                                    (int)bcrow0);
-                        tma_load_2d(st + 3 * S::IN_TILE + S::BC_TILE + bx * kN * 128, &tm_C,
-                                    &full[s], tc, (int)bcrow0);
-                    }
-                    issued = k + 1;
-                }
-                // Never leave the CTA with copies still landing in its shared
-                // memory: wait (bounded) for the last stages issued.
-                for (int k = max(0, issued - NSTAGE); k < issued; ++k)
-                    mbar_wait(&full[k % NSTAGE], (k / NSTAGE) & 1, a.status);
             }
+            const uint32_t bytes = (has_z ? 3 : 2) * S::IN_TILE + 2 * S::BC_TILE;
+            auto issue = [&](int k) {
+                const int s = k % NSTAGE;
+                mbar_arrive_expect_tx(&full[s], bytes);
+                uint8_t* st = stages + s * S::STAGE;
+                const int t0 = t_begin + k * kTL;
+#pragma unroll
+                for (int bx = 0; bx < G::NBOX; ++bx) {
+                    const int tc = t0 + bx * G::TPB;
+                    tma_load_2d(st + bx * CH * 128, &tm_u, &full[s], tc, (int)row0);
+                    tma_load_2d(st + S::IN_TILE + bx * CH * 128, &tm_d, &full[s], tc, (int)row0);
+                    if (has_z)
+                        tma_load_2d(st + 2 * S::IN_TILE + bx * CH * 128, &tm_z, &full[s], tc,
+                                    (int)row0);
+                    tma_load_2d(st + 3 * S::IN_TILE + bx * kN * 128, &tm_B, &full[s], tc,
+                                (int)bcrow0);
+                    tma_load_2d(st + 3 * S::IN_TILE + S::BC_TILE + bx * kN * 128, &tm_C,
+                                &full[s], tc, (int)bcrow0);
+                }
+            };
+            // tile k lands, is converted and published; its stage is reloaded
+            // with tile k + NSTAGE once the compute warps have released it.
+            auto land = [&](int k) -> bool {
+                const int s = k % NSTAGE;
+                if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (k / NSTAGE) & 1, a.status)))
+                    return false;
+                convert_bc<Tin>(stages + s * S::STAGE + 3 * S::IN_TILE, pl);
+                fence_proxy_async_smem();  // before the stage's next TMA writes
+                __syncwarp();
+                if (pl == 0) mbar_arrive(&ready[s]);
+                return true;
+            };
+            const int pro = min(NSTAGE, ntiles);
+            if (pl == 0)
+                for (int k = 0; k < pro; ++k) issue(k);
+            int issued = pro, landed = 0;
+            bool alive = ntiles > 0 && land(0);
+            if (alive) landed = 1;
+            for (int k = 0; alive && k < ntiles; ++k) {
+                if (k + 1 < ntiles) {
+                    if (!(alive = land(k + 1))) break;
+                    landed = k + 2;
+                }
+                const int kn = k + NSTAGE;
+                if (kn < ntiles) {
+                    const int s = k % NSTAGE;
+                    if (!(alive = __all_sync(0xffffffffu,
+                                             mbar_wait(&empty[s], ((kn / NSTAGE) & 1) ^ 1,
+                                                       a.status))))
+                        break;
+                    if (pl == 0) issue(kn);
+                    issued = kn + 1;
+                }
+            }
+            // Never leave the CTA with copies still landing in its shared
+            // memory: wait (bounded) for every stage issued but not waited on.
+            for (int k = landed; k < issued; ++k)
+                mbar_wait(&full[k % NSTAGE], (k / NSTAGE) & 1, a.status);
         }
         return;
     }
@@ -326,12 +413,9 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
             if (has_z)
                 stage_plain<Tin, CH>(st + 2 * S::IN_TILE, reinterpret_cast<const Tin*>(a.z),
                                      row0, (long long)a.batch * a.dim, a.seqlen, t0, tid, NCOMP);
-            stage_plain<Tin, kN, false>(st + 3 * S::IN_TILE, reinterpret_cast<const Tin*>(a.Bm),
-                                 bcrow0, (long long)a.batch * a.ngroups * kN, a.seqlen, t0, tid,
-                                 NCOMP);
-            stage_plain<Tin, kN, false>(st + 3 * S::IN_TILE + S::BC_TILE,
-                                 reinterpret_cast<const Tin*>(a.Cm), bcrow0,
-                                 (long long)a.batch * a.ngroups * kN, a.seqlen, t0, tid, NCOMP);
+            stage_bc_plain<Tin>(st + 3 * S::IN_TILE, reinterpret_cast<const Tin*>(a.Bm),
+                                reinterpret_cast<const Tin*>(a.Cm), bcrow0, a.seqlen, t0, tid,
+                                NCOMP);
             named_bar_sync(1, NCOMP);
         }
 
@@ -397,12 +481,14 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
             }
         }
 
-        // ---- the recurrence over the tile, 8 steps per group.  B and C are
-        // read straight from their TMA tiles ([n][t], not swizzled): one
-        // 16-byte load gives 16 / sizeof(Tin) consecutive steps of one state.
-        const uint8_t* tB = st + 3 * S::IN_TILE;
-        const uint8_t* tC = tB + S::BC_TILE;
-        constexpr int SPL = 16 / (int)sizeof(Tin);  // steps per 16-byte load
+        // ---- the recurrence over the tile, 8 steps per group, B and C from
+        // the stage's fp32 [t][state group] rows (one broadcast address per
+        // quarter-warp), once the producer has converted them
+        if constexpr (TMA) {
+            const bool got = mbar_wait(&ready[s], (k / NSTAGE) & 1, a.status);
+            if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        }
+        const uint8_t* tBC = st + 3 * S::IN_TILE + ng * 32;
 #pragma unroll kGroupUnroll
         for (int j = 0; j < kTL / 8; ++j) {
             if (CK && (j & 1) == 0 && valid && t0 + j * 8 < a.seqlen) {
@@ -412,38 +498,24 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
                        make_float4(h[0], h[1], h[2], h[3]));
             }
             float yp[8];
-            uint4 wb[kSPT], wc[kSPT];
 #pragma unroll
             for (int q = 0; q < 8; q += 2) {
-                if (q % SPL == 0) {
-#pragma unroll
-                    for (int k = 0; k < kSPT; ++k) {
-                        wb[k] = *reinterpret_cast<const uint4*>(
-                            tB + tile_off_lin<Tin, kN>(n0 + k, j * 8 + q));
-                        wc[k] = *reinterpret_cast<const uint4*>(
-                            tC + tile_off_lin<Tin, kN>(n0 + k, j * 8 + q));
-                    }
-                }
                 const float4 pp = *reinterpret_cast<const float4*>(prow + (j * 8 + q) * 2);
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const int s = (q + r) % SPL;  // step within the loaded words
+                    const int t = j * 8 + q + r;
                     const float dl = r ? pp.z : pp.x;
                     const float du = r ? pp.w : pp.y;
-                    float bv[kSPT], cv[kSPT];
-#pragma unroll
-                    for (int k = 0; k < kSPT; ++k) {
-                        bv[k] = word_elem<Tin>(wb[k], s);
-                        cv[k] = word_elem<Tin>(wc[k], s);
-                    }
-                    h[0] = fmaf(ex2_approx(dl * A2[0]), h[0], du * bv[0]);
-                    h[1] = fmaf(ex2_approx(dl * A2[1]), h[1], du * bv[1]);
-                    h[2] = fmaf(ex2_approx(dl * A2[2]), h[2], du * bv[2]);
-                    h[3] = fmaf(ex2_approx(dl * A2[3]), h[3], du * bv[3]);
-                    float acc = cv[0] * h[0];
-                    acc = fmaf(cv[1], h[1], acc);
-                    acc = fmaf(cv[2], h[2], acc);
-                    acc = fmaf(cv[3], h[3], acc);
+                    const float4 bv = *reinterpret_cast<const float4*>(tBC + t * 128);
+                    const float4 cv = *reinterpret_cast<const float4*>(tBC + t * 128 + 16);
+                    h[0] = fmaf(ex2_approx(dl * A2[0]), h[0], du * bv.x);
+                    h[1] = fmaf(ex2_approx(dl * A2[1]), h[1], du * bv.y);
+                    h[2] = fmaf(ex2_approx(dl * A2[2]), h[2], du * bv.z);
+                    h[3] = fmaf(ex2_approx(dl * A2[3]), h[3], du * bv.w);
+                    float acc = cv.x * h[0];
+                    acc = fmaf(cv.y, h[1], acc);
+                    acc = fmaf(cv.z, h[2], acc);
+                    acc = fmaf(cv.w, h[3], acc);
                     yp[q + r] = acc;
                 }
             }
