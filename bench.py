@@ -367,6 +367,7 @@ def measure_other_paths(dev, reps=20):
     del inp
     res["ssm_scan_bwd"] = _measure_scan_bwd(dev, reps)
     res["ssd_chunked_bwd"] = _measure_ssd_bwd(dev, reps)
+    res["ssd_mamba3_bwd"] = _measure_mamba3_bwd(dev, reps)
     m3 = inputs.mamba3_inputs(32, 256, 32, 64, 128, 1, "bf16", seed=1006, device="cuda")
 
     def ssd_m3():
@@ -564,6 +565,39 @@ def _measure_ssd_bwd(dev, reps):
             "ms": ms, "elements_per_s": Bn * L * H * P * N / (ms / 1e3),
             "train_step_ms": ms_train,
             "train_step": "forward keeping block states + gradient from them",
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": BF16_PEAK_TFLOPS,
+                         "unit": "TFLOP/s", "frac": achieved / BF16_PEAK_TFLOPS,
+                         "algorithmic_flops": flops}}
+
+
+def _measure_mamba3_bwd(dev, reps):
+    """The Mamba-3 SISO gradient (ssd_mamba3_bwd: the Mamba-3 forward for the block
+    states, the SSD gradient with the Mamba-3 input weights, elementwise kernels for
+    lambda, the diagonal correction and the previous token) on the SSD workload
+    with lambda, an initial state and a previous token, against the bf16 tensor
+    peak with the SSD gradient's algorithmic FLOPs (the Mamba-3 extras are
+    elementwise)."""
+    import torch
+    from state_space_model_selective_gb300 import binding, inputs
+    Bn, L, H, P, N = 32, 256, 32, 64, 128
+    m3 = inputs.mamba3_inputs(Bn, L, H, P, N, 1, "bf16", seed=1006, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1010)
+    dy = torch.randn(Bn, L, H, P, device=dev, generator=g).to(torch.bfloat16)
+    ws = torch.empty(binding.ssd_mamba3_bwd_workspace_bytes(Bn, L, H, P, N, 1),
+                     dtype=torch.uint8, device=dev)
+
+    def bwd():
+        binding.ssd_mamba3_bwd(m3["x"], m3["dt"], m3["lam"], m3["A_head"], m3["B"], m3["C"], dy,
+                               64, m3["h0"], m3["prev_B"], m3["prev_x"], workspace=ws)
+    ms = _time(bwd, reps)
+    Q = 128
+    flops = 2 * (3 * Q * Q * N + 2 * Q * Q * P + 4 * Q * P * N) * Bn * H * (L // Q)
+    achieved = flops / (ms / 1e3) / 1e12
+    return {"workload": "Mamba-3 SISO gradient bf16 in / fp32 gradients, batch 32, L 256, "
+                        "32 heads, headdim 64, d_state 128, chunk 64, initial state and "
+                        "previous token", "ms": ms,
+            "elements_per_s": Bn * L * H * P * N / (ms / 1e3),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": BF16_PEAK_TFLOPS,
                          "unit": "TFLOP/s", "frac": achieved / BF16_PEAK_TFLOPS,
                          "algorithmic_flops": flops}}

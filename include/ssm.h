@@ -12,6 +12,7 @@
  *   ssm_scan_bwd     gradient of ssm_scan_fwd (reverse mode, every input)
  *   ssm_scan_fwd_host  ssm_scan_fwd on host-resident activations, copies pipelined
  *   ssd_chunked_bwd  gradient of ssd_chunked_fwd, tensor cores
+ *   ssd_mamba3_bwd   gradient of ssd_mamba3_fwd (Mamba-3 SISO)
  *
  * Conventions shared by every entry point
  *  - Pointers are DEVICE pointers unless stated otherwise, to dense row-major
@@ -462,6 +463,59 @@ ssm_status_t ssd_chunked_bwd(const void* x, const float* dt, const float* A_head
                              int nheads, int headdim, int dstate, int ngroups,
                              ssm_dtype_t in_dtype, void* workspace, size_t workspace_bytes,
                              void* stream);
+
+/*
+ * Bytes of device workspace ssd_mamba3_bwd needs (a pure function of its
+ * arguments; 0 if they are invalid or unsupported): ssd_chunked_bwd's, plus
+ * per-step weights and dots and one state per (batch, head).
+ */
+size_t ssd_mamba3_bwd_workspace_bytes(int batch, int seqlen, int nheads, int headdim,
+                                      int dstate, int ngroups);
+
+/*
+ * Gradient of the Mamba-3 SISO chunked prefill.
+ *   The forward operation is ssd_mamba3_fwd's ("Mamba-3 NKI Kernels for AWS
+ *   Neuron", section "How it works", Eq. 9: S = alpha_t S + beta_t u_{t-1} +
+ *   gamma_t u_t with alpha = exp(dt A), gamma = lambda dt, beta = (dt - gamma)
+ *   alpha; section "Kernel details": the single-SSD form with scale =
+ *   gamma + dt_{t+1} (1 - lambda_{t+1}) and a diagonal correction).  The page
+ *   reports the mixer's gradients through autograd (section "Correctness")
+ *   and prints no backward formula; this is the exact reverse-mode derivative.
+ *
+ * For the loss sum(dy * y) + sum(dfinal_state * final_state), with y and
+ * final_state what ssd_mamba3_fwd returns for the same inputs, writes:
+ *   dx, ddt, dA_head, dB, dC, dinitial_state  as ssd_chunked_bwd
+ *   dlam     (batch, seqlen, nheads)  fp32 (lambda as given: no sigmoid)
+ *   dprev_B  (batch, ngroups, dstate) fp32 (summed over the group's heads) and
+ *   dprev_x  (batch, nheads, headdim) fp32, required when prev_B / prev_x are
+ *            given, not written otherwise.
+ * Inputs as for ssd_mamba3_fwd (x, B, C, prev_B, prev_x bf16; dt, lam, A_head,
+ * initial_state fp32), plus dy (batch, seqlen, nheads, headdim) bf16 and
+ * dfinal_state (batch, nheads, headdim, dstate) fp32 or NULL (zero).
+ * How: the three-term recurrence is the Mamba-2 SSD recurrence of S + c_t u_t
+ * (c_t = dt_{t+1} (1 - lambda_{t+1})) with input weights `scale` and y less
+ * c_t (C_t . B_t) x_t, so the call runs the Mamba-3 forward once more for the
+ * states entering each 128-step block, the SSD gradient with those weights,
+ * then small kernels that take the weights' and the correction's gradients
+ * back to dt, lambda, x, B, C and the previous token.  All on `stream`.
+ * workspace: at least ssd_mamba3_bwd_workspace_bytes(...) bytes, contents on
+ * entry irrelevant; ssm_last_device_status reads it afterwards.  Sums over
+ * heads and over the batch are added in a fixed order.
+ * Every output must be disjoint from every input, from the other outputs and
+ * from the workspace (SSM_ERR_ALIAS).  prev_B and prev_x must be both NULL or
+ * both given (else SSM_ERR_NULL).
+ * Supported: as ssd_chunked_bwd.  With no step (seqlen == 0 or batch == 0)
+ * dA_head is zeroed, dinitial_state = dfinal_state (or 0) and dprev_B, dprev_x
+ * are zeroed.
+ */
+ssm_status_t ssd_mamba3_bwd(const void* x, const float* dt, const float* lam, const float* A_head,
+                            const void* B, const void* C, int chunk, const float* initial_state,
+                            const void* prev_B, const void* prev_x, const void* dy,
+                            const float* dfinal_state, float* dx, float* ddt, float* dlam,
+                            float* dA_head, float* dB, float* dC, float* dinitial_state,
+                            float* dprev_B, float* dprev_x, int batch, int seqlen, int nheads,
+                            int headdim, int dstate, int ngroups, ssm_dtype_t in_dtype,
+                            void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Bytes of device workspace ssm_scan_fwd_host needs (a pure function of its

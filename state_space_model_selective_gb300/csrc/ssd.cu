@@ -727,6 +727,39 @@ ssm_status_t ssd_forward_block_states(const void* x, const float* dt, const floa
     return launch<float, false, 1, true>(mc, mb, mx, a, stream);
 }
 
+// The Mamba-3 SISO forward writing only the states its chunked form carries
+// between 128-step blocks (bstates [batch * nheads][nblocks + 1][64][128]):
+// the state entering each block including the pending previous-token term
+// (dt_{t+1} (1 - lambda_{t+1}) B_t (x) x_t of the block's last step), and the
+// final state.  Arguments are validated by the caller.
+ssm_status_t ssd_mamba3_forward_block_states(const void* x, const float* dt, const float* lam,
+                                             const float* A_head, const void* B, const void* C,
+                                             const float* initial_state, const void* prev_B,
+                                             const void* prev_x, float* bstates, int batch,
+                                             int seqlen, int nheads, int ngroups,
+                                             cudaStream_t stream) {
+    CUtensorMap mc, mb, mx;
+    if (!make_bc_map(&mc, C, batch, seqlen, ngroups) || !make_bc_map(&mb, B, batch, seqlen, ngroups) ||
+        !make_x_map(&mx, x, batch, seqlen, nheads))
+        return SSM_ERR_CUDA;
+    SsdArgs a{};
+    a.x = static_cast<const __nv_bfloat16*>(x);
+    a.dt = dt;
+    a.lam = lam;
+    a.A = A_head;
+    a.h0 = initial_state;
+    a.prev_B = static_cast<const __nv_bfloat16*>(prev_B);
+    a.prev_x = static_cast<const __nv_bfloat16*>(prev_x);
+    a.y = nullptr;
+    a.final_state = nullptr;
+    a.bstates = bstates;
+    a.batch = batch;
+    a.seqlen = seqlen;
+    a.nheads = nheads;
+    a.ngroups = ngroups;
+    return launch<float, true, 1, true>(mc, mb, mx, a, stream);
+}
+
 }  // namespace ssd_internal
 
 extern "C" ssm_status_t ssd_chunked_fwd(const void* x, const float* dt, const float* A_head,

@@ -7,7 +7,8 @@
 // y = C S).  Its reverse-mode derivative, for the loss sum(dy y) +
 // sum(dfinal final_state), is evaluated block by block in reverse, with the
 // adjoint state dS = dL/dS carried between blocks.  For a block of Q = 128
-// steps with cs_i = sum_{j<=i} dt_j A (inside the block), w = dt,
+// steps with cs_i = sum_{j<=i} dt_j A (inside the block), input weights w
+// (w = dt for ssd_chunked_bwd; the Mamba-3 gradient passes its scale weights),
 // L[i,j] = exp(cs_i - cs_j) for j <= i (else 0), S_in / S_out the states
 // entering / leaving the block and dS_out the adjoint leaving it:
 //   T       = dY X^T                      (Q x Q; (L o T) includes w_j)
@@ -16,7 +17,8 @@
 //   bracket = diag(e^(cs_last - cs)) B dS_out^T + (L o C B^T)^T dY,  dX = diag(w) bracket
 //   dS_in   = e^cs_last dS_out + (e^cs o dY)^T C
 //   d cs_i  = C_i . dC_i - B_i . dB_i  (+ <dS_out, S_out> at the block's last row)
-//   ddt_k   = x_k . bracket_k + A sum_{i >= k} d cs_i,   dA += sum_k dt_k sum_{i >= k} d cs_i
+//   dw_k    = x_k . bracket_k,  ddt_k = (dw_k if w = dt) + A sum_{i >= k} d cs_i,
+//   dA     += sum_k dt_k sum_{i >= k} d cs_i
 // (the C . dC - B . dB form of the log-decay gradient: every term of y_i and
 // of S_out depends on cs only through factors e^(cs_i - cs_j)).
 //
@@ -32,6 +34,7 @@
 // checkpoint mode.  dB and dC are per-head partials summed over a group's heads
 // by a second kernel, in a fixed order.
 #include <algorithm>
+#include <functional>
 
 #include "ssd_common.cuh"
 #include "ssd_internal.h"
@@ -68,6 +71,11 @@ constexpr uint32_t kTmemCols = 512;
 
 struct BwdArgs {
     const float* dt;       // (batch, seqlen, nheads)
+    // input weights w (batch, seqlen, nheads), or NULL for w = dt.  With w
+    // given, ddt receives only the log-decay part A sum_{i >= k} d cs_i and dw
+    // the input-weight part x_k . bracket_k.
+    const float* w;
+    float* dw;
     const float* A;        // (nheads,)
     const float* bstates;  // [batch * nheads][nblocks + 1][64][128]
     const float* dfinal;   // (batch, nheads, 64, 128) or NULL
@@ -127,9 +135,10 @@ __device__ __forceinline__ void mask_row_half(uint32_t taddr, const float* col2,
 // This warpgroup's half of row j of G^T and of T^T (two TMEM products with the
 // same mask and decay), each turned into its bf16 hi/lo operand in place:
 // columns i >= j kept, G^T with factor e^(cs_i - cs_j) = 2^(cs2[i] - cs2_j),
-// T^T with that factor times dt_j.  One exp2 per element serves both.
+// T^T with that factor times the input weight w_j.  One exp2 per element
+// serves both.
 __device__ __forceinline__ void mask_pair_half(uint32_t tg, uint32_t tt, const float* cs2,
-                                               float cs2_j, float dt_j, int j, int part) {
+                                               float cs2_j, float w_j, int j, int part) {
 #pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
         const int c0 = 64 * part + 32 * hh;
@@ -148,7 +157,7 @@ __device__ __forceinline__ void mask_pair_half(uint32_t tg, uint32_t tt, const f
                 if (c0 + q < j) f0 = 0.0f;
                 if (c0 + q + 1 < j) f1 = 0.0f;
                 split2_bf16(gv[q] * f0, gv[q + 1] * f1, gh[q >> 1], gl[q >> 1]);
-                split2_bf16(tv[q] * (f0 * dt_j), tv[q + 1] * (f1 * dt_j), th[q >> 1], tl[q >> 1]);
+                split2_bf16(tv[q] * (f0 * w_j), tv[q + 1] * (f1 * w_j), th[q >> 1], tl[q >> 1]);
             }
         }
         tmem_st16(tg + c0, gh);
@@ -252,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
     float* s_cs2 = reinterpret_cast<float*>(smem + kMisc);  // log2-scaled cs of each row
-    float* s_q2 = s_cs2 + kQ;                               // log2(dt_j) - cs2_j
+    float* s_q2 = s_cs2 + kQ;                               // log2(w_j) - cs2_j
     float* s_wsum = s_q2 + kQ;                              // [2][4] warp totals (cs scan)
     float* s_rsum = s_wsum + 8;                             // [4] warp totals (d cs suffix scan)
     float* s_dot = s_rsum + 8;                              // [8] <dS_out, S_out> per warp
@@ -430,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     load_xy(blk - 1);
                     p_xy = (int)(ph ^ 1u);
                 }
-                // dB = dt e^(cs_last - cs) o Q + (L o T w)^T C
+                // dB = w e^(cs_last - cs) o Q + (L o T w)^T C
                 if (!W(r_db)) break;
                 tc_fence_after();
 #pragma unroll
@@ -474,7 +483,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int t = blk * kQ + row;
             return t < L ? a.dt[((long long)b * L + t) * a.nheads + h] : 0.0f;
         };
+        const float* wsrc = a.w ? a.w : a.dt;
+        auto w_of = [&](int blk) {
+            const int t = blk * kQ + row;
+            return t < L ? wsrc[((long long)b * L + t) * a.nheads + h] : 0.0f;
+        };
         float dt_next = nblocks > 0 ? dt_of(nblocks - 1) : 0.0f;
+        float w_next = nblocks > 0 ? w_of(nblocks - 1) : 0.0f;
         // per-head dB, dC partials: [h][b][n][t], t contiguous (coalesced across a warp's rows)
         const long long pofs = ((long long)h * a.batch + b) * kNs * L;
 
@@ -486,8 +501,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return named_bar_and(1, kWorkers, got);
             };
             const int t = blk * kQ + row;
-            const float dtr = dt_next;
-            if (blk > 0) dt_next = dt_of(blk - 1);
+            const float dtr = dt_next;  // this row's step: log-decay dt A
+            const float wr = w_next;    // and input weight
+            if (blk > 0) {
+                dt_next = dt_of(blk - 1);
+                w_next = w_of(blk - 1);
+            }
 
             // ---- cumulative log-decay within the block
             float v = dtr * Ah;
@@ -507,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float cs2 = v * kLog2e, cs2_last = cs_last * kLog2e;
             float lg;
-            asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(dtr));
+            asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(wr));
             const float q2 = lg - cs2;
             if (part == 0) {
                 s_cs2[row] = cs2;
@@ -515,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float e_r = ex2_approx(cs2);
             const float eL_r = ex2_approx(cs2_last - cs2);
-            const float u_r = dtr * eL_r;
+            const float u_r = wr * eL_r;
             const float e_last = ex2_approx(cs2_last);
 
             // ---- S_in split [n = row][p]; <dS_out, S_out>; then dS_out and
@@ -553,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- (L o T w) and e^cs P, for dC
             if (!Wc(m_tp)) { ok = false; break; }
             tc_fence_after();
-            // (L o T w) row i = row: columns j <= i, factor e^(cs_i - cs_j) dt_j
+            // (L o T w) row i = row: columns j <= i, factor e^(cs_i - cs_j) w_j
             mask_row_half(t_lane + kTmT, s_q2, cs2, 0, row, part);
             scale_half(t_lane + kTmP, part, e_r);
             tmem_wait_st();
@@ -578,11 +597,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- (L o G)^T and (L o T w)^T, row j = row: columns i >= j
             if (!Wc(m_gt) || !Wc(m_tt)) { ok = false; break; }
             tc_fence_after();
-            mask_pair_half(t_lane + kTmGT, t_lane + kTmT, s_cs2, cs2, dtr, row, part);
+            mask_pair_half(t_lane + kTmGT, t_lane + kTmT, s_cs2, cs2, wr, row, part);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(r_br);
-            // ---- dX_j = dt_j bracket_j; the input-weight part of ddt_j is x_j . bracket_j
+            // ---- dX_j = w_j bracket_j; the input-weight gradient is x_j . bracket_j
             if (!Wc(m_br)) { ok = false; break; }
             tc_fence_after();
             float dw = 0.0f;
@@ -598,12 +617,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < 32; q += 4)
                         *reinterpret_cast<float4*>(dxr + q) = make_float4(
-                            dtr * br[q], dtr * br[q + 1], dtr * br[q + 2], dtr * br[q + 3]);
+                            wr * br[q], wr * br[q + 1], wr * br[q + 2], wr * br[q + 3]);
                 }
             }
             tc_fence_before();
             mbar_arrive(r_x);
-            // ---- Q row j scaled by dt_j e^(cs_last - cs_j)
+            // ---- Q row j scaled by w_j e^(cs_last - cs_j)
             if (!Wc(m_q)) { ok = false; break; }
             tc_fence_after();
             scale_half(t_lane + kTmQ, part, u_r);
@@ -643,7 +662,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int w = 0; w < 4; ++w)
                     if (w > quarter) dcs += s_rsum[w];
-                if (t < L) a.ddt[((long long)b * L + t) * a.nheads + h] = fmaf(Ah, dcs, dw_all);
+                if (t < L) {
+                    const long long o = ((long long)b * L + t) * a.nheads + h;
+                    if (a.dw) {
+                        a.ddt[o] = Ah * dcs;
+                        a.dw[o] = dw_all;
+                    } else {
+                        a.ddt[o] = fmaf(Ah, dcs, dw_all);
+                    }
+                }
                 dA_acc = fmaf(dtr, dcs, dA_acc);
             }
             named_bar_sync(1, kWorkers);  // s_* are rewritten by the next block
@@ -737,6 +764,79 @@ BwdWs bwd_workspace(int batch, int seqlen, int nheads) {
     return w;
 }
 
+using MakeStates = std::function<ssm_status_t(float*)>;
+
+// Steps 1-3 of the gradient, after validation: block states (from
+// `block_states`, else by `make_states` when given, else by the Mamba-2
+// forward), the reverse block walk with input weights `wts` (NULL: dt; with
+// weights, `dw` receives their gradient and ddt only the log-decay part), and
+// the fixed-order sums.  The workspace holds bwd_workspace(...).total bytes.
+
+ssm_status_t run_bwd(const void* x, const float* dt, const float* wts, const float* A_head,
+                     const void* B, const void* C, const float* initial_state, const void* dy,
+                     const float* dfinal_state, const float* block_states,
+                     const MakeStates& make_states, float* dx, float* ddt, float* dw,
+                     float* dA_head, float* dB, float* dC, float* dinitial_state, int batch,
+                     int seqlen, int nheads, int ngroups, void* workspace, cudaStream_t s) {
+    const size_t items = (size_t)batch * nheads;
+    const BwdWs w = bwd_workspace(batch, seqlen, nheads);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if (cudaMemsetAsync(ws, 0, w.header, s) != cudaSuccess) return SSM_ERR_CUDA;
+    float* bstates = reinterpret_cast<float*>(ws + w.header);
+    BwdArgs a{};
+    a.dt = dt;
+    a.w = wts;
+    a.dw = dw;
+    a.A = A_head;
+    a.bstates = block_states ? block_states : bstates;
+    a.dfinal = dfinal_state;
+    a.dx = dx;
+    a.ddt = ddt;
+    a.dh0 = dinitial_state;
+    a.pB = reinterpret_cast<float*>(ws + w.header + w.bstates);
+    a.pC = reinterpret_cast<float*>(ws + w.header + w.bstates + w.pb);
+    a.pA = reinterpret_cast<float*>(ws + w.header + w.bstates + w.pb + w.pc);
+    a.status = reinterpret_cast<uint32_t*>(ws + 4);  // the header's status word
+    a.batch = batch;
+    a.seqlen = seqlen;
+    a.nheads = nheads;
+    a.ngroups = ngroups;
+
+    // 1. the state entering every block (and the final state), unless the
+    // forward kept them
+    if (!block_states) {
+        const ssm_status_t rc =
+            make_states ? make_states(bstates)
+                        : ssd_internal::ssd_forward_block_states(x, dt, A_head, B, C, initial_state,
+                                                                 bstates, batch, seqlen, nheads,
+                                                                 ngroups, s);
+        if (rc != SSM_OK) return rc;
+    }
+    // 2. the blocks in reverse, one CTA per (batch, head)
+    CUtensorMap mc, mb, mx, mdy;
+    if (!ssd_host::make_bc_map(&mc, C, batch, seqlen, ngroups) ||
+        !ssd_host::make_bc_map(&mb, B, batch, seqlen, ngroups) ||
+        !ssd_host::make_x_map(&mx, x, batch, seqlen, nheads) ||
+        !ssd_host::make_x_map(&mdy, dy, batch, seqlen, nheads))
+        return SSM_ERR_CUDA;
+    if (cudaFuncSetAttribute(ssd_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemAlloc) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    ssd_bwd_kernel<<<(unsigned)items, kThreads, kSmemAlloc, s>>>(mc, mb, mx, mdy, a);
+    if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
+    // 3. sums over a group's heads and over the batch
+    {
+        const dim3 grid((unsigned)((seqlen + 31) / 32), kNs / 32,
+                        (unsigned)std::min<long long>(2LL * batch * ngroups, 65535));
+        ssd_bwd_reduce_bc_kernel<<<grid, dim3(32, 8), 0, s>>>(a.pB, a.pC, dB, dC, batch, seqlen,
+                                                             nheads, ngroups);
+        if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
+        ssd_bwd_reduce_a_kernel<<<(unsigned)((nheads + 127) / 128), 128, 0, s>>>(a.pA, dA_head,
+                                                                                batch, nheads);
+    }
+    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" size_t ssd_chunked_bwd_workspace_bytes(int batch, int seqlen, int nheads, int headdim,
@@ -814,54 +914,352 @@ extern "C" ssm_status_t ssd_chunked_bwd(const void* x, const float* dt, const fl
     for (const R& r : outs)
         if (overlaps(workspace, w.total, r.p, r.n)) return SSM_ERR_ALIAS;
 
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    if (cudaMemsetAsync(ws, 0, w.header, s) != cudaSuccess) return SSM_ERR_CUDA;
-    float* bstates = reinterpret_cast<float*>(ws + w.header);
-    BwdArgs a{};
-    a.dt = dt;
-    a.A = A_head;
-    a.bstates = block_states ? block_states : bstates;
-    a.dfinal = dfinal_state;
-    a.dx = dx;
-    a.ddt = ddt;
-    a.dh0 = dinitial_state;
-    a.pB = reinterpret_cast<float*>(ws + w.header + w.bstates);
-    a.pC = reinterpret_cast<float*>(ws + w.header + w.bstates + w.pb);
-    a.pA = reinterpret_cast<float*>(ws + w.header + w.bstates + w.pb + w.pc);
-    a.status = reinterpret_cast<uint32_t*>(ws + 4);  // the header's status word
-    a.batch = batch;
-    a.seqlen = seqlen;
-    a.nheads = nheads;
-    a.ngroups = ngroups;
+    return run_bwd(x, dt, nullptr, A_head, B, C, initial_state, dy, dfinal_state, block_states,
+                   MakeStates(), dx, ddt, nullptr, dA_head, dB, dC, dinitial_state, batch, seqlen,
+                   nheads, ngroups, workspace, s);
+}
 
-    // 1. the state entering every block (and the final state), unless the
-    // forward kept them
-    if (!block_states) {
-        const ssm_status_t rc = ssd_internal::ssd_forward_block_states(
-            x, dt, A_head, B, C, initial_state, bstates, batch, seqlen, nheads, ngroups, s);
-        if (rc != SSM_OK) return rc;
+// ------------------------------------------------ Mamba-3 SISO gradient
+//
+// The three-term recurrence of "Mamba-3 NKI Kernels for AWS Neuron" (section
+// "How it works", Eq. 9), h_t = alpha_t h_{t-1} + beta_t u_{t-1} + gamma_t u_t
+// with u_t = B_t (x) x_t, is the Mamba-2 SSD recurrence of
+//   s_t = h_t + c_t u_t,   c_t = dt_{t+1} (1 - lambda_{t+1})  (0 at the last step):
+//   s_t = alpha_t s_{t-1} + w_t u_t,   w_t = gamma_t + c_t  (the page's "scale"),
+//   y_t = C_t . s_t - c_t (C_t . B_t) x_t  (its diagonal correction),
+//   s_{-1} = h_init + c_{-1} prev_B (x) prev_x,  c_{-1} = dt_0 (1 - lambda_0),
+//   and s_{L-1} = h_{L-1}.
+// So the gradient is the SSD gradient with input weights w, from the block
+// states the Mamba-3 forward carries (which are s), plus the correction
+// term's, taken through w, c and s_{-1} back to dt, lambda, x, B, C and the
+// previous token:
+//   dc_t      = dw_t - (C_t . B_t)(x_t . dy_t),   dc_{-1} = <dS_init, prev_B (x) prev_x>
+//   ddt_t     = A sum_{i >= t} d cs_i + lambda_t dw_t + (1 - lambda_t) dc_{t-1}
+//   dlambda_t = dt_t dw_t - dt_t dc_{t-1}
+//   dx_t     -= c_t (C_t . B_t) dy_t
+//   dB_t     -= (sum_h c_t x_t . dy_t) C_t,   dC_t -= (sum_h c_t x_t . dy_t) B_t
+//   dh_init = dS_init, dprev_x = c_{-1} dS_init prev_B, dprev_B = sum_h c_{-1} dS_init^T prev_x.
+
+namespace {
+
+// w[b,t,h] = lambda_t dt_t + dt_{t+1} (1 - lambda_{t+1}), the second term 0 at
+// the last step.
+__global__ void m3_weights_kernel(const float* __restrict__ dt, const float* __restrict__ lam,
+                                  float* __restrict__ w, int batch, int seqlen, int nheads) {
+    const long long n = (long long)batch * seqlen * nheads;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)((i / nheads) % seqlen);
+        float v = lam[i] * dt[i];
+        if (t + 1 < seqlen) v = fmaf(dt[i + nheads], 1.0f - lam[i + nheads], v);
+        w[i] = v;
     }
-    // 2. the blocks in reverse, one CTA per (batch, head)
-    CUtensorMap mc, mb, mx, mdy;
-    if (!ssd_host::make_bc_map(&mc, C, batch, seqlen, ngroups) ||
-        !ssd_host::make_bc_map(&mb, B, batch, seqlen, ngroups) ||
-        !ssd_host::make_x_map(&mx, x, batch, seqlen, nheads) ||
-        !ssd_host::make_x_map(&mdy, dy, batch, seqlen, nheads))
-        return SSM_ERR_CUDA;
-    if (cudaFuncSetAttribute(ssd_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemAlloc) != cudaSuccess)
-        return SSM_ERR_CUDA;
-    ssd_bwd_kernel<<<(unsigned)items, kThreads, kSmemAlloc, s>>>(mc, mb, mx, mdy, a);
+}
+
+// xd[b,t,h] = x_t . dy_t over p (64) and cb[b,t,g] = C_t . B_t over n (128):
+// one warp per row, lanes summed by a fixed butterfly.
+__global__ void m3_dots_kernel(const __nv_bfloat16* __restrict__ x,
+                               const __nv_bfloat16* __restrict__ dy,
+                               const __nv_bfloat16* __restrict__ B,
+                               const __nv_bfloat16* __restrict__ C, float* __restrict__ xd,
+                               float* __restrict__ cb, int batch, int seqlen, int nheads,
+                               int ngroups) {
+    const long long steps = (long long)batch * seqlen;
+    const long long nx = steps * nheads, nb = steps * ngroups;
+    const int lane = threadIdx.x & 31;
+    const long long wstride = ((long long)gridDim.x * blockDim.x) >> 5;
+    for (long long r = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; r < nx + nb;
+         r += wstride) {
+        float acc;
+        if (r < nx) {
+            const uint32_t a = reinterpret_cast<const uint32_t*>(x + r * kP)[lane];
+            const uint32_t d = reinterpret_cast<const uint32_t*>(dy + r * kP)[lane];
+            acc = fmaf(bf16hi(a), bf16hi(d), bf16lo(a) * bf16lo(d));
+        } else {
+            const long long q = r - nx;
+            const uint2 bw = reinterpret_cast<const uint2*>(B + q * kNs)[lane];
+            const uint2 cw = reinterpret_cast<const uint2*>(C + q * kNs)[lane];
+            acc = bf16lo(bw.x) * bf16lo(cw.x);
+            acc = fmaf(bf16hi(bw.x), bf16hi(cw.x), acc);
+            acc = fmaf(bf16lo(bw.y), bf16lo(cw.y), acc);
+            acc = fmaf(bf16hi(bw.y), bf16hi(cw.y), acc);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) {
+            if (r < nx) xd[r] = acc;
+            else cb[r - nx] = acc;
+        }
+    }
+}
+
+// The previous token, per (b, h), from dS = dL/ds_{-1} [64 p][128 n] and
+// c0 = dt_0 (1 - lambda_0):
+//   dprev_x[b,h,p] = c0 sum_n dS[p,n] prev_B[g,n],
+//   pprevB[b,h,n]  = c0 sum_p dS[p,n] prev_x[h,p] (summed over the group next),
+//   dc0[b,h]       = sum_p prev_x[h,p] sum_n dS[p,n] prev_B[g,n].
+// 128 threads: thread n for the column sums, threads p < 64 for the rows.
+__global__ void m3_prev_kernel(const float* __restrict__ dS,
+                               const __nv_bfloat16* __restrict__ prev_B,
+                               const __nv_bfloat16* __restrict__ prev_x,
+                               const float* __restrict__ dt, const float* __restrict__ lam,
+                               float* __restrict__ dprev_x, float* __restrict__ pprevB,
+                               float* __restrict__ dc0, int batch, int seqlen, int nheads,
+                               int ngroups) {
+    __shared__ float pb[kNs], px[kP], red[2];
+    const int item = blockIdx.x, b = item / nheads, h = item % nheads;
+    const int g = h / (nheads / ngroups);
+    const int tid = threadIdx.x;
+    const long long i0 = (long long)b * seqlen * nheads + h;
+    const float c0 = dt[i0] * (1.0f - lam[i0]);
+    pb[tid] = __bfloat162float(prev_B[((long long)b * ngroups + g) * kNs + tid]);
+    if (tid < kP) px[tid] = __bfloat162float(prev_x[(long long)item * kP + tid]);
+    __syncthreads();
+    const float* S = dS + (long long)item * kP * kNs;
+    float col = 0.0f;
+    for (int p = 0; p < kP; ++p) col = fmaf(S[p * kNs + tid], px[p], col);
+    pprevB[(long long)item * kNs + tid] = c0 * col;
+    float part = 0.0f;
+    if (tid < kP) {
+        float row = 0.0f;
+        const float* Sp = S + tid * kNs;
+        for (int n = 0; n < kNs; ++n) row = fmaf(Sp[n], pb[n], row);
+        dprev_x[(long long)item * kP + tid] = c0 * row;
+        part = px[tid] * row;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if ((tid & 31) == 0) red[tid >> 5] = part;
+    }
+    __syncthreads();
+    if (tid == 0) dc0[item] = red[0] + red[1];
+}
+
+// dprev_B[b,g,n] = the group's heads' pprevB, added in head order.
+__global__ void m3_prev_b_kernel(const float* __restrict__ pprevB, float* __restrict__ dprev_B,
+                                 int batch, int nheads, int ngroups) {
+    const int hpg = nheads / ngroups;
+    const long long n = (long long)batch * ngroups * kNs;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int nn = (int)(i % kNs);
+        const long long bg = i / kNs;
+        const int b = (int)(bg / ngroups), g = (int)(bg % ngroups);
+        float acc = 0.0f;
+        for (int h = g * hpg; h < (g + 1) * hpg; ++h)
+            acc += pprevB[((long long)b * nheads + h) * kNs + nn];
+        dprev_B[i] = acc;
+    }
+}
+
+// One CTA per (b, t): ddt (holding the log-decay part on entry) and dlambda of
+// every head, then dx -= c_t (C_t . B_t) dy_t and dB, dC -= (sum over the
+// group's heads of c_t x_t . dy_t) C_t, B_t.  Shared memory: 2 * nheads floats.
+__global__ void m3_post_kernel(const float* __restrict__ dt, const float* __restrict__ lam,
+                               const float* __restrict__ dw, const float* __restrict__ xd,
+                               const float* __restrict__ cb, const float* __restrict__ dc0,
+                               const __nv_bfloat16* __restrict__ dy,
+                               const __nv_bfloat16* __restrict__ B,
+                               const __nv_bfloat16* __restrict__ C, float* __restrict__ ddt,
+                               float* __restrict__ dlam, float* __restrict__ dx,
+                               float* __restrict__ dB, float* __restrict__ dC, int batch,
+                               int seqlen, int nheads, int ngroups) {
+    extern __shared__ float sm[];
+    float* coef = sm;           // c_t (C_t . B_t) per head
+    float* cx = sm + nheads;    // c_t (x_t . dy_t) per head
+    const int hpg = nheads / ngroups;
+    for (long long row = blockIdx.x; row < (long long)batch * seqlen; row += gridDim.x) {
+        const int t = (int)(row % seqlen);
+        const int b = (int)(row / seqlen);
+        for (int h = threadIdx.x; h < nheads; h += blockDim.x) {
+            const long long i = row * nheads + h;
+            const int g = h / hpg;
+            const float c = t + 1 < seqlen ? dt[i + nheads] * (1.0f - lam[i + nheads]) : 0.0f;
+            float dcp = 0.0f;  // dL/dc_{t-1}
+            if (t > 0) dcp = dw[i - nheads] - cb[(row - 1) * ngroups + g] * xd[i - nheads];
+            else if (dc0) dcp = dc0[(long long)b * nheads + h];
+            const float dwt = dw[i], l = lam[i], d = dt[i];
+            ddt[i] = ddt[i] + l * dwt + (1.0f - l) * dcp;
+            dlam[i] = d * dwt - d * dcp;
+            coef[h] = c * cb[row * ngroups + g];
+            cx[h] = c * xd[i];
+        }
+        __syncthreads();
+        const long long xo = row * nheads * kP;
+        for (int idx = threadIdx.x; idx < nheads * kP; idx += blockDim.x)
+            dx[xo + idx] -= coef[idx / kP] * __bfloat162float(dy[xo + idx]);
+        const long long bo = row * ngroups * kNs;
+        for (int idx = threadIdx.x; idx < ngroups * kNs; idx += blockDim.x) {
+            const int g = idx / kNs;
+            float s = 0.0f;
+            for (int h = g * hpg; h < (g + 1) * hpg; ++h) s += cx[h];
+            dB[bo + idx] -= s * __bfloat162float(C[bo + idx]);
+            dC[bo + idx] -= s * __bfloat162float(B[bo + idx]);
+        }
+        __syncthreads();
+    }
+}
+
+struct M3Ws {
+    size_t ssd, w, dw, xd, cb, ds, dc0, ppb, total;
+};
+
+M3Ws m3_workspace(int batch, int seqlen, int nheads, int ngroups) {
+    M3Ws m{};
+    const size_t steps = (size_t)batch * seqlen, items = (size_t)batch * nheads;
+    m.ssd = bwd_workspace(batch, seqlen, nheads).total;
+    m.w = round256(steps * nheads * 4);
+    m.dw = m.w;
+    m.xd = m.w;
+    m.cb = round256(steps * ngroups * 4);
+    m.ds = round256(items * kP * kNs * 4);
+    m.dc0 = round256(items * 4);
+    m.ppb = round256(items * kNs * 4);
+    m.total = m.ssd + m.w + m.dw + m.xd + m.cb + m.ds + m.dc0 + m.ppb;
+    return m;
+}
+
+unsigned grid_for(long long n, int threads) {
+    return (unsigned)std::max<long long>(1, std::min<long long>((n + threads - 1) / threads, 65535));
+}
+
+}  // namespace
+
+extern "C" size_t ssd_mamba3_bwd_workspace_bytes(int batch, int seqlen, int nheads, int headdim,
+                                                 int dstate, int ngroups) {
+    if (batch < 0 || seqlen < 0 || nheads < 0 || ngroups < 1 || headdim != kP || dstate != kNs ||
+        nheads % ngroups != 0)
+        return 0;
+    return m3_workspace(batch, seqlen, nheads, ngroups).total;
+}
+
+extern "C" ssm_status_t ssd_mamba3_bwd(const void* x, const float* dt, const float* lam,
+                                       const float* A_head, const void* B, const void* C,
+                                       int chunk, const float* initial_state, const void* prev_B,
+                                       const void* prev_x, const void* dy,
+                                       const float* dfinal_state, float* dx, float* ddt,
+                                       float* dlam, float* dA_head, float* dB, float* dC,
+                                       float* dinitial_state, float* dprev_B, float* dprev_x,
+                                       int batch, int seqlen, int nheads, int headdim,
+                                       int dstate, int ngroups, ssm_dtype_t in_dtype,
+                                       void* workspace, size_t workspace_bytes, void* stream) {
+    using namespace ssm_host;
+    if (batch < 0 || seqlen < 0 || nheads < 0 || headdim < 1 || dstate < 1 || ngroups < 1 ||
+        chunk < 1)
+        return SSM_ERR_SHAPE;
+    if (nheads % ngroups != 0 || seqlen % chunk != 0) return SSM_ERR_SHAPE;
+    if (!dtype_ok(in_dtype)) return SSM_ERR_DTYPE;
+    if (chunk != 64 || headdim != kP || dstate != kNs || in_dtype != SSM_BF16)
+        return SSM_ERR_UNSUPPORTED;
+    if ((size_t)batch * nheads > (size_t)INT32_MAX) return SSM_ERR_UNSUPPORTED;
+    if ((prev_B == nullptr) != (prev_x == nullptr)) return SSM_ERR_NULL;
+    const bool has_prev = prev_B != nullptr;
+    const size_t items = (size_t)batch * nheads;
+    const size_t steps = (size_t)batch * seqlen;
+    const size_t sb = items * headdim * dstate * 4;
+    if (nheads > 0 && !dA_head) return SSM_ERR_NULL;
+    if (has_prev && items > 0 && (!dprev_B || !dprev_x)) return SSM_ERR_NULL;
+    const bool work = items > 0 && seqlen > 0;
+    if (work && (!x || !dt || !lam || !A_head || !B || !C || !dy || !dx || !ddt || !dlam ||
+                 !dB || !dC))
+        return SSM_ERR_NULL;
+    if (work && !workspace) return SSM_ERR_WORKSPACE;
+    const void* ptrs[] = {x, dt, lam, A_head, B, C, initial_state, prev_B, prev_x, dy,
+                          dfinal_state, dx, ddt, dlam, dA_head, dB, dC, dinitial_state, dprev_B,
+                          dprev_x, workspace};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return SSM_ERR_ALIGN;
+    const size_t xb = steps * nheads * headdim * 2, bcb = steps * ngroups * dstate * 2;
+    const size_t pbb = (size_t)batch * ngroups * dstate, pxb = items * headdim;
+    struct R { const void* p; size_t n; };
+    const R ins[] = {{x, xb}, {dt, steps * nheads * 4}, {lam, steps * nheads * 4},
+                     {A_head, (size_t)nheads * 4}, {B, bcb}, {C, bcb},
+                     {initial_state, initial_state ? sb : 0}, {prev_B, has_prev ? pbb * 2 : 0},
+                     {prev_x, has_prev ? pxb * 2 : 0}, {dy, xb},
+                     {dfinal_state, dfinal_state ? sb : 0}};
+    const R outs[] = {{dx, steps * nheads * headdim * 4}, {ddt, steps * nheads * 4},
+                      {dlam, steps * nheads * 4}, {dA_head, (size_t)nheads * 4},
+                      {dB, bcb * 2}, {dC, bcb * 2}, {dinitial_state, dinitial_state ? sb : 0},
+                      {dprev_B, has_prev ? pbb * 4 : 0}, {dprev_x, has_prev ? pxb * 4 : 0}};
+    constexpr int kOuts = sizeof(outs) / sizeof(outs[0]);
+    for (int i = 0; i < kOuts; ++i) {
+        for (const R& r : ins)
+            if (overlaps(outs[i].p, outs[i].n, r.p, r.n)) return SSM_ERR_ALIAS;
+        for (int j = i + 1; j < kOuts; ++j)
+            if (overlaps(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return SSM_ERR_ALIAS;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!work) {
+        // no step: dA = 0, the adjoint passes through to the initial state and
+        // the previous token never enters
+        if (nheads > 0 && cudaMemsetAsync(dA_head, 0, (size_t)nheads * 4, s) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        if (dinitial_state && sb) {
+            const cudaError_t e = dfinal_state ? cudaMemcpyAsync(dinitial_state, dfinal_state, sb,
+                                                                 cudaMemcpyDeviceToDevice, s)
+                                               : cudaMemsetAsync(dinitial_state, 0, sb, s);
+            if (e != cudaSuccess) return SSM_ERR_CUDA;
+        }
+        if (has_prev && items > 0) {
+            if (cudaMemsetAsync(dprev_B, 0, pbb * 4, s) != cudaSuccess ||
+                cudaMemsetAsync(dprev_x, 0, pxb * 4, s) != cudaSuccess)
+                return SSM_ERR_CUDA;
+        }
+        return SSM_OK;
+    }
+    const M3Ws m = m3_workspace(batch, seqlen, nheads, ngroups);
+    if (workspace_bytes < m.total) return SSM_ERR_WORKSPACE;
+    for (const R& r : ins)
+        if (overlaps(workspace, m.total, r.p, r.n)) return SSM_ERR_ALIAS;
+    for (const R& r : outs)
+        if (overlaps(workspace, m.total, r.p, r.n)) return SSM_ERR_ALIAS;
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* w = reinterpret_cast<float*>(ws + m.ssd);
+    float* dw = reinterpret_cast<float*>(ws + m.ssd + m.w);
+    float* xd = reinterpret_cast<float*>(ws + m.ssd + m.w + m.dw);
+    float* cb = reinterpret_cast<float*>(ws + m.ssd + m.w + m.dw + m.xd);
+    float* dS = reinterpret_cast<float*>(ws + m.ssd + m.w + m.dw + m.xd + m.cb);
+    float* dc0 = reinterpret_cast<float*>(ws + m.ssd + m.w + m.dw + m.xd + m.cb + m.ds);
+    float* ppb = reinterpret_cast<float*>(ws + m.ssd + m.w + m.dw + m.xd + m.cb + m.ds + m.dc0);
+    float* dS_out = dinitial_state ? dinitial_state : (has_prev ? dS : nullptr);
+
+    // 1. the input weights w = gamma + c
+    const long long nw = (long long)steps * nheads;
+    m3_weights_kernel<<<grid_for(nw, 256), 256, 0, s>>>(dt, lam, w, batch, seqlen, nheads);
     if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
-    // 3. sums over a group's heads and over the batch
-    {
-        const dim3 grid((unsigned)((seqlen + 31) / 32), kNs / 32,
-                        (unsigned)std::min<long long>(2LL * batch * ngroups, 65535));
-        ssd_bwd_reduce_bc_kernel<<<grid, dim3(32, 8), 0, s>>>(a.pB, a.pC, dB, dC, batch, seqlen,
-                                                             nheads, ngroups);
+    // 2. the SSD gradient with weights w from the Mamba-3 forward's block states
+    const MakeStates states = [&](float* bs) {
+        return ssd_internal::ssd_mamba3_forward_block_states(x, dt, lam, A_head, B, C,
+                                                             initial_state, prev_B, prev_x, bs,
+                                                             batch, seqlen, nheads, ngroups, s);
+    };
+    ssm_status_t rc = run_bwd(x, dt, w, A_head, B, C, initial_state, dy, dfinal_state, nullptr,
+                              states, dx, ddt, dw, dA_head, dB, dC, dS_out, batch, seqlen, nheads,
+                              ngroups, workspace, s);
+    if (rc != SSM_OK) return rc;
+    // 3. x . dy per head and C . B per group, every step
+    const long long nrows = (long long)steps * (nheads + ngroups);
+    m3_dots_kernel<<<grid_for(nrows * 32, 256), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(dy),
+        static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), xd, cb,
+        batch, seqlen, nheads, ngroups);
+    if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
+    // 4. the previous token's gradients and dL/dc_{-1}
+    if (has_prev) {
+        m3_prev_kernel<<<(unsigned)items, kNs, 0, s>>>(
+            dS_out, static_cast<const __nv_bfloat16*>(prev_B),
+            static_cast<const __nv_bfloat16*>(prev_x), dt, lam, dprev_x, ppb, dc0, batch, seqlen,
+            nheads, ngroups);
         if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
-        ssd_bwd_reduce_a_kernel<<<(unsigned)((nheads + 127) / 128), 128, 0, s>>>(a.pA, dA_head,
-                                                                                batch, nheads);
+        m3_prev_b_kernel<<<grid_for((long long)pbb, 256), 256, 0, s>>>(ppb, dprev_B, batch,
+                                                                       nheads, ngroups);
+        if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
     }
+    // 5. ddt, dlambda and the diagonal correction's terms
+    m3_post_kernel<<<(unsigned)std::min<long long>((long long)steps, 65535), 256,
+                     2 * nheads * sizeof(float), s>>>(
+        dt, lam, dw, xd, cb, has_prev ? dc0 : nullptr, static_cast<const __nv_bfloat16*>(dy),
+        static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), ddt, dlam, dx,
+        dB, dC, batch, seqlen, nheads, ngroups);
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }

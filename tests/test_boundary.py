@@ -340,6 +340,49 @@ def test_ssd_bwd_workspace_bytes():
     assert f(1, 64, 3, ngroups=2) == 0
 
 
+def m3_bwd_call(L, **kw):
+    args = dict(x=P(0), dt=P(1), lam=P(12), A=P(2), B=P(3), C=P(4), chunk=64, h0=None,
+                pB=None, px=None, dy=P(5), dfs=None, dx=P(6), ddt=P(7), dlam=P(13), dA=P(8),
+                dB=P(9), dC=P(10), dh0=None, dpB=None, dpx=None, batch=2, seqlen=128, nheads=4,
+                headdim=64, dstate=128, ngroups=1, in_dt=1, ws=P(11), wsb=1 << 30, stream=None)
+    args.update(kw)
+    a = args
+    return L.ssd_mamba3_bwd(a["x"], a["dt"], a["lam"], a["A"], a["B"], a["C"], a["chunk"],
+                            a["h0"], a["pB"], a["px"], a["dy"], a["dfs"], a["dx"], a["ddt"],
+                            a["dlam"], a["dA"], a["dB"], a["dC"], a["dh0"], a["dpB"], a["dpx"],
+                            a["batch"], a["seqlen"], a["nheads"], a["headdim"], a["dstate"],
+                            a["ngroups"], a["in_dt"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_mamba3_bwd_argument_errors(L):
+    assert m3_bwd_call(L, lam=None) == NULL
+    assert m3_bwd_call(L, dlam=None) == NULL
+    assert m3_bwd_call(L, dy=None) == NULL
+    assert m3_bwd_call(L, pB=P(14)) == NULL              # prev_B without prev_x
+    assert m3_bwd_call(L, pB=P(14), px=P(15)) == NULL    # previous token without its gradients
+    assert m3_bwd_call(L, seqlen=100) == SHAPE
+    assert m3_bwd_call(L, ngroups=3) == SHAPE
+    assert m3_bwd_call(L, chunk=32) == UNSUP
+    assert m3_bwd_call(L, dstate=64) == UNSUP
+    assert m3_bwd_call(L, in_dt=0) == UNSUP
+    assert m3_bwd_call(L, in_dt=9) == DTYPE
+    assert m3_bwd_call(L, dlam=ctypes.c_void_p(0x70000008)) == ALIGN
+    assert m3_bwd_call(L, ws=None) == WS
+    assert m3_bwd_call(L, wsb=1024) == WS
+    assert m3_bwd_call(L, dlam=P(12)) == ALIAS             # dlam on top of lam
+    assert m3_bwd_call(L, dlam=P(7)) == ALIAS              # dlam and ddt on one buffer
+    assert m3_bwd_call(L, pB=P(14), px=P(15), dpB=P(16), dpx=P(16)) == ALIAS
+    assert m3_bwd_call(L, nheads=0, dA=None, x=None) == OK
+
+
+def test_mamba3_bwd_workspace_bytes():
+    f = binding.ssd_mamba3_bwd_workspace_bytes
+    assert f(32, 256, 32) > binding.ssd_chunked_bwd_workspace_bytes(32, 256, 32)
+    assert f(32, 256, 32) == f(32, 256, 32)
+    assert f(1, 64, 2, headdim=32) == 0
+    assert f(1, 64, 3, ngroups=2) == 0
+
+
 def host_call(L, **kw):
     args = dict(u=P(0), delta=P(1), A=P(2), B=P(3), C=P(4), D=None, z=None, bias=None,
                 softplus=1, h0=None, y=P(5), fs=None, batch=2, dim=32, seqlen=64, dstate=16,
