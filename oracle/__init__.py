@@ -67,6 +67,7 @@ def _load():
             lib.oracle_scan_bwd.argtypes = [dp] * 8 + [i] + [dp] * 12 + [i] * 5
             lib.oracle_ssd_bwd.argtypes = [dp] * 14 + [i] * 6
             lib.oracle_mamba3_bwd.argtypes = [dp] * 20 + [i] * 6
+            lib.oracle_mamba3_mimo_bwd.argtypes = [dp] * 20 + [i] * 7
             lib.oracle_combine.argtypes = [ctypes.c_double] * 4 + [dp, dp]
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -334,6 +335,31 @@ def mamba3_mimo_recurrence(x, dt, lam, A_head, B, C, h0=None, prev_B=None, prev_
     hs = np.empty((batch, nheads, headdim, dstate), np.float64)
     _load().oracle_mamba3_mimo_recurrence(*[_ptr(a) for a in arrs], _ptr(y), _ptr(hs), *dims)
     return y, hs
+
+
+def mamba3_mimo_bwd(x, dt, lam, A_head, B, C, dy, h0=None, prev_B=None, prev_x=None,
+                    dfinal=None):
+    """Gradient of ``mamba3_mimo_recurrence`` for the loss sum(dy * y) +
+    sum(dfinal * final_state).  Returns a dict of float64 arrays: dx (like x), ddt,
+    dlam (B, L, H), dA (H,), dB, dC (like B), dh0 (B, H, P, N), and dprev_B,
+    dprev_x (like prev_B, prev_x; None without a previous token)."""
+    arrs, dims = _mimo_args(x, dt, lam, A_head, B, C, h0, prev_B, prev_x)
+    batch, seqlen, rank, nheads, headdim, dstate, ngroups = dims
+    dy, dfinal = _f64(dy), _f64(dfinal)
+    assert dy.shape == arrs[0].shape
+    assert dfinal is None or dfinal.shape == (batch, nheads, headdim, dstate)
+    has_prev = arrs[7] is not None
+    g = {"dx": np.empty(arrs[0].shape), "ddt": np.empty((batch, seqlen, nheads)),
+         "dlam": np.empty((batch, seqlen, nheads)), "dA": np.empty(nheads),
+         "dB": np.empty(arrs[4].shape), "dC": np.empty(arrs[4].shape),
+         "dh0": np.empty((batch, nheads, headdim, dstate)),
+         "dprev_B": np.empty(arrs[7].shape) if has_prev else None,
+         "dprev_x": np.empty(arrs[8].shape) if has_prev else None}
+    _load().oracle_mamba3_mimo_bwd(*[_ptr(a) for a in arrs], _ptr(dy), _ptr(dfinal),
+                                   _ptr(g["dx"]), _ptr(g["ddt"]), _ptr(g["dlam"]), _ptr(g["dA"]),
+                                   _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dh0"]),
+                                   _ptr(g["dprev_B"]), _ptr(g["dprev_x"]), *dims)
+    return g
 
 
 def mamba3_mimo_chunked(x, dt, lam, A_head, B, C, chunk, h0=None, prev_B=None, prev_x=None):

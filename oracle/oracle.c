@@ -1155,6 +1155,158 @@ void oracle_mamba3_bwd(const double* x, const double* dt, const double* lam,
     free(later);
 }
 
+/*
+ * Gradient of oracle_mamba3_mimo_recurrence for the loss  sum dy . y + sum
+ * dfinal . final_state, by differentiating the rank-R recurrence in reverse.
+ * Per row (b, h, p) with bx_t[n] = sum_r B_t[n,r] x_t[p,r] and Lambda_t = dL/dS_t:
+ *   Lambda_t  = sum_r dy_t[p,r] C_t[:,r] + alpha_{t+1} Lambda_{t+1}
+ *   dC_t[:,r] += dy_t[p,r] S_t
+ *   bx_t enters with gamma_t at step t and with beta_{t+1} at step t + 1, so
+ *   d bx_t = gamma_t Lambda_t + beta_{t+1} Lambda_{t+1}, and
+ *   dx_t[p,r] = d bx_t . B_t[:,r],  dB_t[:,r] += d bx_t x_t[p,r];
+ *   d gamma_t = Lambda_t . bx_t,  d beta_t = Lambda_t . bx_{t-1},  d alpha_t = Lambda_t . S_{t-1}
+ * then through alpha, gamma, beta to ddt, dlambda and dA as in
+ * oracle_mamba3_bwd.  The token before the first takes the t = 0 beta term's
+ * gradient; dh0 = alpha_0 Lambda_0.  Serial over rows.  Arguments as
+ * oracle_mamba3_mimo_recurrence plus dy (like x), dfinal in; out: dx (like
+ * x), ddt, dlam, dA (nheads), dB, dC (like B), dh0 (may be NULL), dprev_B,
+ * dprev_x (like prev_B, prev_x; NULL when prev_B is).
+ */
+void oracle_mamba3_mimo_bwd(const double* x, const double* dt, const double* lam,
+                            const double* A_head, const double* Bm, const double* Cm,
+                            const double* h0, const double* prev_B, const double* prev_x,
+                            const double* dy, const double* dfinal,
+                            double* dx, double* ddt, double* dlam, double* dA, double* dB,
+                            double* dC, double* dh0, double* dprev_B, double* dprev_x,
+                            int batch, int seqlen, int rank, int nheads, int headdim, int dstate,
+                            int ngroups)
+{
+    const int heads_per_group = nheads / ngroups;
+    const size_t nbc = (size_t)batch * seqlen * rank * ngroups * dstate;
+    memset(ddt, 0, sizeof(double) * (size_t)batch * seqlen * nheads);
+    memset(dlam, 0, sizeof(double) * (size_t)batch * seqlen * nheads);
+    memset(dA, 0, sizeof(double) * (size_t)nheads);
+    memset(dB, 0, sizeof(double) * nbc);
+    memset(dC, 0, sizeof(double) * nbc);
+    if (dprev_B) memset(dprev_B, 0, sizeof(double) * (size_t)batch * rank * ngroups * dstate);
+    if (dprev_x) memset(dprev_x, 0, sizeof(double) * (size_t)batch * rank * nheads * headdim);
+    const size_t ns = (size_t)dstate;
+    double* St = (double*)malloc(sizeof(double) * (size_t)(seqlen + 1) * ns);  /* S_{t-1} at t */
+    double* BX = (double*)malloc(sizeof(double) * (size_t)(seqlen + 1) * ns);  /* bx_{t-1} at t */
+    double* adj = (double*)malloc(sizeof(double) * ns);    /* Lambda_t */
+    double* carry = (double*)malloc(sizeof(double) * ns);  /* alpha_{t+1} Lambda_{t+1} */
+    double* later = (double*)malloc(sizeof(double) * ns);  /* Lambda_{t+1} */
+    double* dbx = (double*)malloc(sizeof(double) * ns);
+    const long long rows = (long long)batch * nheads * headdim;
+    for (long long row = 0; row < rows; ++row) {
+        const int p = (int)(row % headdim);
+        const int h = (int)((row / headdim) % nheads);
+        const int b = (int)(row / ((long long)headdim * nheads));
+        const int g = h / heads_per_group;
+        const int has_prev = prev_B && prev_x;
+#define XI(bt, r) ((((size_t)(bt) * rank + (r)) * nheads + h) * headdim + p)
+#define BI(bt, r) ((((size_t)(bt) * rank + (r)) * ngroups + g) * ns)
+        /* forward, every state and every bx kept */
+        for (size_t n = 0; n < ns; ++n) {
+            St[n] = h0 ? h0[row * dstate + n] : 0.0;
+            double bx = 0.0;
+            if (has_prev)
+                for (int r = 0; r < rank; ++r)
+                    bx += prev_B[(((size_t)b * rank + r) * ngroups + g) * ns + n] *
+                          prev_x[(((size_t)b * rank + r) * nheads + h) * headdim + p];
+            BX[n] = bx;
+        }
+        for (int t = 0; t < seqlen; ++t) {
+            const size_t bt = (size_t)b * seqlen + t;
+            const double step = dt[bt * nheads + h];
+            const double decay = exp(A_head[h] * step);
+            const double gam = lam[bt * nheads + h] * step;
+            const double bet = (step - gam) * decay;
+            for (size_t n = 0; n < ns; ++n) {
+                double bx = 0.0;
+                for (int r = 0; r < rank; ++r) bx += Bm[BI(bt, r) + n] * x[XI(bt, r)];
+                BX[(size_t)(t + 1) * ns + n] = bx;
+                St[(size_t)(t + 1) * ns + n] = decay * St[(size_t)t * ns + n] +
+                                               bet * BX[(size_t)t * ns + n] + gam * bx;
+            }
+        }
+        /* reverse */
+        for (size_t n = 0; n < ns; ++n) {
+            carry[n] = dfinal ? dfinal[row * dstate + n] : 0.0;
+            later[n] = 0.0;
+        }
+        double bet_next = 0.0;  /* beta_{t+1} (none past the last step) */
+        double bet0 = 0.0;
+        for (int t = seqlen - 1; t >= 0; --t) {
+            const size_t bt = (size_t)b * seqlen + t;
+            const double step = dt[bt * nheads + h];
+            const double lv = lam[bt * nheads + h];
+            const double decay = exp(A_head[h] * step);
+            const double gam = lv * step;
+            const double bet = (step - gam) * decay;
+            double on_bx = 0.0, on_bxlast = 0.0, on_S = 0.0;
+            for (size_t n = 0; n < ns; ++n) {
+                double a = carry[n];
+                for (int r = 0; r < rank; ++r) {
+                    const double dyv = dy[XI(bt, r)];
+                    a += dyv * Cm[BI(bt, r) + n];
+                    dC[BI(bt, r) + n] += dyv * St[(size_t)(t + 1) * ns + n];
+                }
+                adj[n] = a;
+                on_bx += a * BX[(size_t)(t + 1) * ns + n];
+                on_bxlast += a * BX[(size_t)t * ns + n];
+                on_S += a * St[(size_t)t * ns + n];
+                dbx[n] = gam * a + bet_next * later[n];
+            }
+            for (int r = 0; r < rank; ++r) {
+                double acc = 0.0;
+                const double xv = x[XI(bt, r)];
+                for (size_t n = 0; n < ns; ++n) {
+                    acc += dbx[n] * Bm[BI(bt, r) + n];
+                    dB[BI(bt, r) + n] += dbx[n] * xv;
+                }
+                dx[XI(bt, r)] = acc;
+            }
+            const double d_gam = on_bx, d_bet = on_bxlast, d_alpha = on_S;
+            ddt[bt * nheads + h] += d_gam * lv +
+                                    d_bet * ((1.0 - lv) * decay + step * (1.0 - lv) * A_head[h] * decay) +
+                                    d_alpha * A_head[h] * decay;
+            dlam[bt * nheads + h] += step * (d_gam - d_bet * decay);
+            dA[h] += d_bet * step * (1.0 - lv) * step * decay + d_alpha * step * decay;
+            for (size_t n = 0; n < ns; ++n) {
+                later[n] = adj[n];
+                carry[n] = adj[n] * decay;
+            }
+            bet_next = bet;
+            bet0 = bet;
+        }
+        if (has_prev && seqlen > 0 && dprev_B && dprev_x) {
+            /* bx_{-1} entered with beta_0 at step 0: d bx_{-1} = beta_0 Lambda_0 (= later) */
+            for (int r = 0; r < rank; ++r) {
+                const double* pBr = prev_B + (((size_t)b * rank + r) * ngroups + g) * ns;
+                const size_t ixr = (((size_t)b * rank + r) * nheads + h) * headdim + p;
+                double acc = 0.0;
+                for (size_t n = 0; n < ns; ++n) {
+                    acc += bet0 * later[n] * pBr[n];
+                    dprev_B[(((size_t)b * rank + r) * ngroups + g) * ns + n] +=
+                        bet0 * later[n] * prev_x[ixr];
+                }
+                dprev_x[ixr] = acc;
+            }
+        }
+        if (dh0)
+            for (size_t n = 0; n < ns; ++n) dh0[row * dstate + n] = carry[n];
+#undef XI
+#undef BI
+    }
+    free(St);
+    free(BX);
+    free(adj);
+    free(carry);
+    free(later);
+    free(dbx);
+}
+
 int oracle_num_threads(void)
 {
     int n = 1;

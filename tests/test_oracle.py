@@ -855,3 +855,86 @@ def test_mamba3_bwd_at_lambda_one_is_the_ssd_gradient():
     for k, sk in (("dx", "dx"), ("ddt", "ddt"), ("dA", "dA"), ("dB", "dB"), ("dC", "dC"),
                   ("dh0", "dh0")):
         np.testing.assert_allclose(g[k], s[sk], err_msg=k, **tol)
+
+
+# ---------------------------------------------- Mamba-3 MIMO backward pins
+
+def _mimo_bwd_case(seed, rank, ngroups, use_h0, use_prev):
+    rng = _rng(seed)
+    batch, seqlen, nheads, headdim, dstate = 2, 4, 4, 2, 3
+    c = dict(x=rng.standard_normal((batch, seqlen, rank, nheads, headdim)),
+             dt=rng.uniform(0.05, 0.6, (batch, seqlen, nheads)),
+             lam=rng.uniform(0.05, 0.95, (batch, seqlen, nheads)),
+             A_head=-rng.uniform(0.5, 2.0, nheads),
+             B=rng.standard_normal((batch, seqlen, rank, ngroups, dstate)),
+             C=rng.standard_normal((batch, seqlen, rank, ngroups, dstate)),
+             h0=rng.standard_normal((batch, nheads, headdim, dstate)) if use_h0 else None,
+             prev_B=rng.standard_normal((batch, rank, ngroups, dstate)) if use_prev else None,
+             prev_x=rng.standard_normal((batch, rank, nheads, headdim)) if use_prev else None)
+    dy = rng.standard_normal((batch, seqlen, rank, nheads, headdim))
+    dfinal = rng.standard_normal((batch, nheads, headdim, dstate))
+    return c, dy, dfinal
+
+
+def _mimo_loss(c, dy, dfinal):
+    y, hs = oracle.mamba3_mimo_recurrence(c["x"], c["dt"], c["lam"], c["A_head"], c["B"],
+                                          c["C"], c["h0"], c["prev_B"], c["prev_x"])
+    return float(np.sum(dy * y) + np.sum(dfinal * hs))
+
+
+@pytest.mark.parametrize("rank,ngroups,use_h0,use_prev", [(2, 1, True, True), (4, 2, False, True),
+                                                          (2, 4, True, False)])
+def test_mimo_bwd_equals_finite_differences(rank, ngroups, use_h0, use_prev):
+    """Every entry of the Mamba-3 MIMO gradient (x, dt, lambda, A, B, C, h0 and the
+    previous token, every rank) against a central difference of the rank-R
+    recurrence oracle's loss sum(dy y) + sum(dfinal final_state)."""
+    c, dy, dfinal = _mimo_bwd_case(501 + rank + ngroups, rank, ngroups, use_h0, use_prev)
+    g = oracle.mamba3_mimo_bwd(c["x"], c["dt"], c["lam"], c["A_head"], c["B"], c["C"], dy,
+                               c["h0"], c["prev_B"], c["prev_x"], dfinal)
+    names = {"x": "dx", "dt": "ddt", "lam": "dlam", "A_head": "dA", "B": "dB", "C": "dC",
+             "h0": "dh0", "prev_B": "dprev_B", "prev_x": "dprev_x"}
+    eps = 1e-6
+    for k, gk in names.items():
+        if c[k] is None:
+            assert g[gk] is None or k == "h0", k
+            continue
+        fd = np.zeros_like(c[k])
+        for idx in np.ndindex(c[k].shape):
+            cp = {kk: (None if vv is None else vv.copy()) for kk, vv in c.items()}
+            cp[k][idx] += eps
+            lp = _mimo_loss(cp, dy, dfinal)
+            cp[k][idx] -= 2 * eps
+            lm = _mimo_loss(cp, dy, dfinal)
+            fd[idx] = (lp - lm) / (2 * eps)
+        np.testing.assert_allclose(g[gk], fd, rtol=1e-6, atol=1e-7, err_msg=k)
+
+
+def test_mimo_bwd_rank_one_is_the_siso_gradient():
+    """At rank one the MIMO recurrence is the SISO one (Eq. 9): every gradient
+    equals the SISO gradient oracle's under the layout exchange."""
+    c, dy, dfinal = _mimo_bwd_case(521, 1, 2, True, True)
+    g = oracle.mamba3_mimo_bwd(c["x"], c["dt"], c["lam"], c["A_head"], c["B"], c["C"], dy,
+                               c["h0"], c["prev_B"], c["prev_x"], dfinal)
+    s = oracle.mamba3_bwd(c["x"][:, :, 0], c["dt"], c["lam"], c["A_head"], c["B"][:, :, 0],
+                          c["C"][:, :, 0], dy[:, :, 0], c["h0"], c["prev_B"][:, 0],
+                          c["prev_x"][:, 0], dfinal)
+    tol = dict(rtol=1e-12, atol=1e-13)
+    for k in ("dx", "dB", "dC"):
+        np.testing.assert_allclose(g[k][:, :, 0], s[k], err_msg=k, **tol)
+    for k in ("dprev_B", "dprev_x"):
+        np.testing.assert_allclose(g[k][:, 0], s[k], err_msg=k, **tol)
+    for k in ("ddt", "dlam", "dA", "dh0"):
+        np.testing.assert_allclose(g[k], s[k], err_msg=k, **tol)
+
+
+def test_mimo_bwd_is_linear_in_the_cotangents():
+    c, dy, dfinal = _mimo_bwd_case(531, 2, 1, True, True)
+    r = _rng(532)
+    dy2, df2 = r.standard_normal(dy.shape), r.standard_normal(dfinal.shape)
+    args = (c["x"], c["dt"], c["lam"], c["A_head"], c["B"], c["C"])
+    extra = (c["h0"], c["prev_B"], c["prev_x"])
+    g1 = oracle.mamba3_mimo_bwd(*args, dy, *extra, dfinal)
+    g2 = oracle.mamba3_mimo_bwd(*args, dy2, *extra, df2)
+    g3 = oracle.mamba3_mimo_bwd(*args, dy + 2 * dy2, *extra, dfinal + 2 * df2)
+    for k in g1:
+        np.testing.assert_allclose(g3[k], g1[k] + 2 * g2[k], rtol=1e-11, atol=1e-12, err_msg=k)

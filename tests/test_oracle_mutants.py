@@ -86,6 +86,14 @@ MUTANTS = {
     "m3_bwd_adjoint_not_decayed": ("carry[n] = decay * adj[n];", "carry[n] = adj[n];"),
     "m3_bwd_prev_x_weight": ("if (dprev_x) dprev_x[row] = bet * on_Blast;",
                              "if (dprev_x) dprev_x[row] = gam * on_Blast;"),
+    "mimo_bwd_dx_drops_beta_term": ("dbx[n] = gam * a + bet_next * later[n];",
+                                    "dbx[n] = gam * a;"),
+    "mimo_bwd_dC_from_previous_state": (
+        "dC[BI(bt, r) + n] += dyv * St[(size_t)(t + 1) * ns + n];",
+        "dC[BI(bt, r) + n] += dyv * St[(size_t)t * ns + n];"),
+    "mimo_bwd_prev_unweighted": ("acc += bet0 * later[n] * pBr[n];", "acc += later[n] * pBr[n];"),
+    "mimo_bwd_dB_to_rank0": ("dB[BI(bt, r) + n] += dbx[n] * xv;",
+                             "dB[BI(bt, 0) + n] += dbx[n] * xv;"),
     "mamba3_decode_terms_swapped": (
         "s[n] = alpha * s[n] + beta * Bp[n] * xp + gamma * Bt[n] * xv;",
         "s[n] = alpha * s[n] + beta * Bt[n] * xv + gamma * Bp[n] * xp;"),
