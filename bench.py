@@ -368,6 +368,7 @@ def measure_other_paths(dev, reps=20):
     res["ssm_scan_bwd"] = _measure_scan_bwd(dev, reps)
     res["ssd_chunked_bwd"] = _measure_ssd_bwd(dev, reps)
     res["ssd_mamba3_bwd"] = _measure_mamba3_bwd(dev, reps)
+    res["ssd_mamba3_mimo_bwd"] = _measure_mimo_bwd(dev, reps)
     m3 = inputs.mamba3_inputs(32, 256, 32, 64, 128, 1, "bf16", seed=1006, device="cuda")
 
     def ssd_m3():
@@ -598,6 +599,37 @@ def _measure_mamba3_bwd(dev, reps):
                         "32 heads, headdim 64, d_state 128, chunk 64, initial state and "
                         "previous token", "ms": ms,
             "elements_per_s": Bn * L * H * P * N / (ms / 1e3),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": BF16_PEAK_TFLOPS,
+                         "unit": "TFLOP/s", "frac": achieved / BF16_PEAK_TFLOPS,
+                         "algorithmic_flops": flops}}
+
+
+def _measure_mimo_bwd(dev, reps):
+    """The Mamba-3 MIMO gradient (ssd_mamba3_mimo_bwd) on the pages' MIMO shape (batch
+    32, L 256, rank 4, 32 heads, headdim 64, d_state 128, chunk 16) with an initial
+    state and a previous token, against the bf16 tensor peak with the SSD gradient's
+    algorithmic FLOPs over the L R sub-tokens."""
+    import torch
+    from state_space_model_selective_gb300 import binding, inputs
+    Bn, L, R, H, P, N = 32, 256, 4, 32, 64, 128
+    m = inputs.mamba3_mimo_inputs(Bn, L, R, H, P, N, 1, "bf16", seed=1007, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1011)
+    dy = torch.randn(Bn, L, R, H, P, device=dev, generator=g).to(torch.bfloat16)
+    ws = torch.empty(binding.ssd_mamba3_mimo_bwd_workspace_bytes(Bn, L, R, H, P, N, 1),
+                     dtype=torch.uint8, device=dev)
+
+    def bwd():
+        binding.ssd_mamba3_mimo_bwd(m["x"], m["dt"], m["lam"], m["A_head"], m["B"], m["C"], dy,
+                                    16, m["h0"], m["prev_B"], m["prev_x"], workspace=ws)
+    ms = _time(bwd, reps)
+    Q = 128
+    flops = 2 * (3 * Q * Q * N + 2 * Q * Q * P + 4 * Q * P * N) * Bn * H * (L * R // Q)
+    achieved = flops / (ms / 1e3) / 1e12
+    return {"workload": "Mamba-3 MIMO gradient bf16 in / fp32 gradients, batch 32, L 256, "
+                        "rank 4, 32 heads, headdim 64, d_state 128, chunk 16, initial state "
+                        "and previous token", "ms": ms,
+            "elements_per_s": Bn * L * R * H * P * N / (ms / 1e3),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": BF16_PEAK_TFLOPS,
                          "unit": "TFLOP/s", "frac": achieved / BF16_PEAK_TFLOPS,
                          "algorithmic_flops": flops}}

@@ -13,6 +13,7 @@
  *   ssm_scan_fwd_host  ssm_scan_fwd on host-resident activations, copies pipelined
  *   ssd_chunked_bwd  gradient of ssd_chunked_fwd, tensor cores
  *   ssd_mamba3_bwd   gradient of ssd_mamba3_fwd (Mamba-3 SISO)
+ *   ssd_mamba3_mimo_bwd  gradient of ssd_mamba3_mimo_fwd (Mamba-3 MIMO)
  *
  * Conventions shared by every entry point
  *  - Pointers are DEVICE pointers unless stated otherwise, to dense row-major
@@ -516,6 +517,49 @@ ssm_status_t ssd_mamba3_bwd(const void* x, const float* dt, const float* lam, co
                             float* dprev_B, float* dprev_x, int batch, int seqlen, int nheads,
                             int headdim, int dstate, int ngroups, ssm_dtype_t in_dtype,
                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Bytes of device workspace ssd_mamba3_mimo_bwd needs (a pure function of its
+ * arguments; 0 if they are invalid or unsupported).
+ */
+size_t ssd_mamba3_mimo_bwd_workspace_bytes(int batch, int seqlen, int rank, int nheads,
+                                           int headdim, int dstate, int ngroups);
+
+/*
+ * Gradient of the Mamba-3 MIMO chunked prefill.
+ *   The forward operation is ssd_mamba3_mimo_fwd's ("Mamba-3 NKI Kernels for
+ *   AWS Neuron", section "Kernel details", mamba3_mimo_ssd_kernel: rank R with
+ *   BX_t = sum_r B_{t,r} (x) x_{t,r} in Eq. 9 and y_{t,r} = C_{t,r} . S).  The
+ *   page reports the MIMO mixer's gradients through autograd (section
+ *   "Correctness"); this is the exact reverse-mode derivative.
+ *
+ * For the loss sum(dy * y) + sum(dfinal_state * final_state) writes:
+ *   dx       (batch, seqlen, rank, nheads, headdim)  fp32
+ *   ddt, dlam (batch, seqlen, nheads)                fp32
+ *   dA_head  (nheads,)                               fp32
+ *   dB, dC   (batch, seqlen, rank, ngroups, dstate)  fp32 (summed over the group's heads)
+ *   dinitial_state (batch, nheads, headdim, dstate)  fp32, may be NULL
+ *   dprev_B  (batch, rank, ngroups, dstate), dprev_x (batch, rank, nheads, headdim)
+ *            fp32, required when prev_B / prev_x are given.
+ * Inputs as for ssd_mamba3_mimo_fwd (bf16 x, B, C, prev_B, prev_x), plus dy
+ * like x (bf16) and dfinal_state fp32 or NULL.  The call runs the MIMO forward
+ * once more for the states entering each 128-row block of sub-tokens, the SSD
+ * gradient over the sub-tokens (block-lower-triangular mask, the step's decay
+ * on its first sub-token, its scale weight on every one), then elementwise
+ * kernels for lambda, the block-diagonal correction and the previous token.
+ * workspace, aliasing, determinism and the no-step case as ssd_mamba3_bwd.
+ * Supported: rank 1, 2 or 4 with chunk * rank == 64; headdim 64, dstate 128,
+ * bf16 in_dtype, seqlen % chunk == 0, nheads % ngroups == 0.
+ */
+ssm_status_t ssd_mamba3_mimo_bwd(const void* x, const float* dt, const float* lam,
+                                 const float* A_head, const void* B, const void* C, int chunk,
+                                 int rank, const float* initial_state, const void* prev_B,
+                                 const void* prev_x, const void* dy, const float* dfinal_state,
+                                 float* dx, float* ddt, float* dlam, float* dA_head, float* dB,
+                                 float* dC, float* dinitial_state, float* dprev_B,
+                                 float* dprev_x, int batch, int seqlen, int nheads, int headdim,
+                                 int dstate, int ngroups, ssm_dtype_t in_dtype, void* workspace,
+                                 size_t workspace_bytes, void* stream);
 
 /*
  * Bytes of device workspace ssm_scan_fwd_host needs (a pure function of its

@@ -33,7 +33,7 @@ EXPORTS = ["ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_bytes", "
            "ssd_chunked_bwd_workspace_bytes", "ssd_chunked_bwd", "ssm_scan_fwd_host_workspace_bytes",
            "ssm_scan_fwd_host", "ssm_scan_checkpoint_bytes", "ssm_scan_fwd_ckpt",
            "ssd_chunked_checkpoint_bytes", "ssd_chunked_fwd_ckpt", "ssd_mamba3_bwd_workspace_bytes",
-           "ssd_mamba3_bwd"]
+           "ssd_mamba3_bwd", "ssd_mamba3_mimo_bwd_workspace_bytes", "ssd_mamba3_mimo_bwd"]
 
 
 class SSMError(RuntimeError):
@@ -92,6 +92,10 @@ def lib() -> ctypes.CDLL:
         L.ssd_mamba3_bwd_workspace_bytes.argtypes = [i] * 6
         L.ssd_mamba3_bwd.restype = i
         L.ssd_mamba3_bwd.argtypes = [vp] * 6 + [i] + [vp] * 14 + [i] * 7 + [vp, sz, vp]
+        L.ssd_mamba3_mimo_bwd_workspace_bytes.restype = sz
+        L.ssd_mamba3_mimo_bwd_workspace_bytes.argtypes = [i] * 7
+        L.ssd_mamba3_mimo_bwd.restype = i
+        L.ssd_mamba3_mimo_bwd.argtypes = [vp] * 6 + [i, i] + [vp] * 14 + [i] * 7 + [vp, sz, vp]
         L.ssd_chunked_checkpoint_bytes.restype = sz
         L.ssd_chunked_checkpoint_bytes.argtypes = [i] * 5
         L.ssd_chunked_fwd_ckpt.restype = i
@@ -487,6 +491,65 @@ def ssd_mamba3_bwd(x, dt, lam, A_head, B, C, dy, chunk=64, initial_state=None, p
                               _DT[torch.bfloat16], _ptr(workspace), workspace.numel(),
                               _stream(stream))
     _check(st, "ssd_mamba3_bwd")
+    return g
+
+
+def ssd_mamba3_mimo_bwd_workspace_bytes(batch, seqlen, rank, nheads, headdim=64, dstate=128,
+                                        ngroups=1) -> int:
+    return int(lib().ssd_mamba3_mimo_bwd_workspace_bytes(batch, seqlen, rank, nheads, headdim,
+                                                         dstate, ngroups))
+
+
+def ssd_mamba3_mimo_bwd(x, dt, lam, A_head, B, C, dy, chunk=None, initial_state=None,
+                        prev_B=None, prev_x=None, dfinal_state=None, workspace=None,
+                        want_dinitial_state=True, stream=None):
+    """Gradient of ``ssd_mamba3_mimo_fwd``.  x, dy: (batch, seqlen, rank, nheads,
+    headdim) bf16; B, C: (batch, seqlen, rank, ngroups, dstate) bf16; prev_B (batch,
+    rank, ngroups, dstate), prev_x (batch, rank, nheads, headdim) bf16 or None.
+    ``chunk`` defaults to 64 // rank.  Returns a dict of fp32 tensors like
+    ``ssd_mamba3_bwd``'s, with dx, dB, dC, dprev_B, dprev_x shaped like their inputs."""
+    _req(x, "x", torch.bfloat16, 5)
+    batch, seqlen, rank, nheads, headdim = x.shape
+    _req(dt, "dt", torch.float32, 3)
+    _req(lam, "lam", torch.float32, 3)
+    _req(A_head, "A_head", torch.float32, 1)
+    _req(B, "B", torch.bfloat16, 5)
+    _req(C, "C", torch.bfloat16, 5)
+    _req(dy, "dy", torch.bfloat16, 5)
+    ngroups, dstate = B.shape[3], B.shape[4]
+    _opt(initial_state, "initial_state", torch.float32)
+    _opt(dfinal_state, "dfinal_state", torch.float32)
+    _opt(prev_B, "prev_B", torch.bfloat16)
+    _opt(prev_x, "prev_x", torch.bfloat16)
+    has_prev = prev_B is not None
+    chunk = 64 // rank if chunk is None else chunk
+    dev, f32 = x.device, torch.float32
+    g = {"dx": torch.empty(tuple(x.shape), dtype=f32, device=dev),
+         "ddt": torch.empty(tuple(dt.shape), dtype=f32, device=dev),
+         "dlam": torch.empty(tuple(dt.shape), dtype=f32, device=dev),
+         "dA_head": torch.empty(nheads, dtype=f32, device=dev),
+         "dB": torch.empty(tuple(B.shape), dtype=f32, device=dev),
+         "dC": torch.empty(tuple(C.shape), dtype=f32, device=dev),
+         "dinitial_state": (torch.empty((batch, nheads, headdim, dstate), dtype=f32, device=dev)
+                            if want_dinitial_state else None),
+         "dprev_B": (torch.empty(tuple(prev_B.shape), dtype=f32, device=dev)
+                     if has_prev else None),
+         "dprev_x": (torch.empty(tuple(prev_x.shape), dtype=f32, device=dev)
+                     if has_prev else None)}
+    need = ssd_mamba3_mimo_bwd_workspace_bytes(batch, seqlen, rank, nheads, headdim, dstate,
+                                               ngroups)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _req(workspace, "workspace", torch.uint8)
+    st = lib().ssd_mamba3_mimo_bwd(_ptr(x), _ptr(dt), _ptr(lam), _ptr(A_head), _ptr(B), _ptr(C),
+                                   int(chunk), int(rank), _ptr(initial_state), _ptr(prev_B),
+                                   _ptr(prev_x), _ptr(dy), _ptr(dfinal_state), _ptr(g["dx"]),
+                                   _ptr(g["ddt"]), _ptr(g["dlam"]), _ptr(g["dA_head"]),
+                                   _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dinitial_state"]),
+                                   _ptr(g["dprev_B"]), _ptr(g["dprev_x"]), batch, seqlen, nheads,
+                                   headdim, dstate, ngroups, _DT[torch.bfloat16], _ptr(workspace),
+                                   workspace.numel(), _stream(stream))
+    _check(st, "ssd_mamba3_mimo_bwd")
     return g
 
 

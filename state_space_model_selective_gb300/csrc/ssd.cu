@@ -727,20 +727,22 @@ ssm_status_t ssd_forward_block_states(const void* x, const float* dt, const floa
     return launch<float, false, 1, true>(mc, mb, mx, a, stream);
 }
 
-// The Mamba-3 SISO forward writing only the states its chunked form carries
-// between 128-step blocks (bstates [batch * nheads][nblocks + 1][64][128]):
-// the state entering each block including the pending previous-token term
-// (dt_{t+1} (1 - lambda_{t+1}) B_t (x) x_t of the block's last step), and the
-// final state.  Arguments are validated by the caller.
+// The Mamba-3 forward (SISO, or MIMO of rank 2 or 4 over 128-row blocks of
+// sub-tokens) writing only the states its chunked form carries between blocks
+// (bstates [batch * nheads][nblocks + 1][64][128]): the state entering each
+// block including the pending term dt_{t+1} (1 - lambda_{t+1}) BX_t of the
+// block's last step, and the final state.  Arguments are validated by the
+// caller.
 ssm_status_t ssd_mamba3_forward_block_states(const void* x, const float* dt, const float* lam,
                                              const float* A_head, const void* B, const void* C,
                                              const float* initial_state, const void* prev_B,
                                              const void* prev_x, float* bstates, int batch,
                                              int seqlen, int nheads, int ngroups,
-                                             cudaStream_t stream) {
+                                             cudaStream_t stream, int rank) {
+    const int nsub = seqlen * rank;
     CUtensorMap mc, mb, mx;
-    if (!make_bc_map(&mc, C, batch, seqlen, ngroups) || !make_bc_map(&mb, B, batch, seqlen, ngroups) ||
-        !make_x_map(&mx, x, batch, seqlen, nheads))
+    if (!make_bc_map(&mc, C, batch, nsub, ngroups) || !make_bc_map(&mb, B, batch, nsub, ngroups) ||
+        !make_x_map(&mx, x, batch, nsub, nheads))
         return SSM_ERR_CUDA;
     SsdArgs a{};
     a.x = static_cast<const __nv_bfloat16*>(x);
@@ -757,7 +759,12 @@ ssm_status_t ssd_mamba3_forward_block_states(const void* x, const float* dt, con
     a.seqlen = seqlen;
     a.nheads = nheads;
     a.ngroups = ngroups;
-    return launch<float, true, 1, true>(mc, mb, mx, a, stream);
+    switch (rank) {
+        case 1: return launch<float, true, 1, true>(mc, mb, mx, a, stream);
+        case 2: return launch<float, true, 2, true>(mc, mb, mx, a, stream);
+        case 4: return launch<float, true, 4, true>(mc, mb, mx, a, stream);
+    }
+    return SSM_ERR_UNSUPPORTED;
 }
 
 }  // namespace ssd_internal

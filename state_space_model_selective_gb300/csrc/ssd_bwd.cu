@@ -253,6 +253,10 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// RK > 1 (Mamba-3 MIMO): rows are sub-tokens, RK consecutive rows one step
+// that see one another fully (the mask is block-lower-triangular); the step's
+// dt sits on its first row (0 on the others) and its weight on every row.
+template <int RK>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_bwd_kernel(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_B,
                    const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
@@ -573,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!Wc(m_tp)) { ok = false; break; }
             tc_fence_after();
             // (L o T w) row i = row: columns j <= i, factor e^(cs_i - cs_j) w_j
-            mask_row_half(t_lane + kTmT, s_q2, cs2, 0, row, part);
+            mask_row_half(t_lane + kTmT, s_q2, cs2, 0, RK * (row / RK) + RK - 1, part);
             scale_half(t_lane + kTmP, part, e_r);
             tmem_wait_st();
             tc_fence_before();
@@ -597,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- (L o G)^T and (L o T w)^T, row j = row: columns i >= j
             if (!Wc(m_gt) || !Wc(m_tt)) { ok = false; break; }
             tc_fence_after();
-            mask_pair_half(t_lane + kTmGT, t_lane + kTmT, s_cs2, cs2, wr, row, part);
+            mask_pair_half(t_lane + kTmGT, t_lane + kTmT, s_cs2, cs2, wr, RK * (row / RK), part);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(r_br);
@@ -777,7 +781,8 @@ ssm_status_t run_bwd(const void* x, const float* dt, const float* wts, const flo
                      const float* dfinal_state, const float* block_states,
                      const MakeStates& make_states, float* dx, float* ddt, float* dw,
                      float* dA_head, float* dB, float* dC, float* dinitial_state, int batch,
-                     int seqlen, int nheads, int ngroups, void* workspace, cudaStream_t s) {
+                     int seqlen, int nheads, int ngroups, void* workspace, cudaStream_t s,
+                     int rank = 1) {
     const size_t items = (size_t)batch * nheads;
     const BwdWs w = bwd_workspace(batch, seqlen, nheads);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -819,10 +824,11 @@ ssm_status_t run_bwd(const void* x, const float* dt, const float* wts, const flo
         !ssd_host::make_x_map(&mx, x, batch, seqlen, nheads) ||
         !ssd_host::make_x_map(&mdy, dy, batch, seqlen, nheads))
         return SSM_ERR_CUDA;
-    if (cudaFuncSetAttribute(ssd_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemAlloc) != cudaSuccess)
+    auto kern = rank == 4 ? ssd_bwd_kernel<4> : rank == 2 ? ssd_bwd_kernel<2> : ssd_bwd_kernel<1>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
+        cudaSuccess)
         return SSM_ERR_CUDA;
-    ssd_bwd_kernel<<<(unsigned)items, kThreads, kSmemAlloc, s>>>(mc, mb, mx, mdy, a);
+    kern<<<(unsigned)items, kThreads, kSmemAlloc, s>>>(mc, mb, mx, mdy, a);
     if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
     // 3. sums over a group's heads and over the batch
     {
@@ -1261,5 +1267,403 @@ extern "C" ssm_status_t ssd_mamba3_bwd(const void* x, const float* dt, const flo
         dt, lam, dw, xd, cb, has_prev ? dc0 : nullptr, static_cast<const __nv_bfloat16*>(dy),
         static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), ddt, dlam, dx,
         dB, dC, batch, seqlen, nheads, ngroups);
+    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+// ------------------------------------------------ Mamba-3 MIMO gradient
+//
+// The rank-R recurrence (section "Kernel details", mamba3_mimo_ssd_kernel:
+// BX_t = sum_r B_{t,r} (x) x_{t,r}, S = alpha_t S + beta_t BX_{t-1} + gamma_t BX_t,
+// y_{t,r} = C_{t,r} . S) is taken the same way over sub-tokens (t, r): s_t =
+// h_t + c_t BX_t is the SSD state of the sub-token sequence with the step's dt
+// on its first sub-token (0 on the others), the weight w_t on every one and a
+// block-lower-triangular mask (a sub-token sees its whole step), and
+//   y_{t,r} = C_{t,r} . s_t - c_t sum_r' (C_{t,r} . B_{t,r'}) x_{t,r'},
+//   s_{-1} = h_init + c_{-1} sum_r prev_B_r (x) prev_x_r.
+// With G_{rr'} = C_{t,r} . B_{t,r'} (per group) and XD_{r'r} = x_{t,r'} . dy_{t,r}
+// (per head), the correction adds
+//   dx_{t,r'} -= c_t sum_r G_{rr'} dy_{t,r},  dB_{t,r'} -= c_t sum_h sum_r XD_{r'r} C_{t,r},
+//   dC_{t,r} -= c_t sum_h sum_r' XD_{r'r} B_{t,r'},  dc_t -= sum_{r,r'} G_{rr'} XD_{r'r};
+// dw_t is the sum of its sub-tokens' weight gradients, and ddt, dlambda follow
+// as for SISO.
+
+namespace {
+
+// Per sub-token row (b, t R + r, h): the step's dt on r = 0 (0 otherwise) and
+// its weight w_t = lambda_t dt_t + dt_{t+1} (1 - lambda_{t+1}) on every rank.
+__global__ void m3m_expand_kernel(const float* __restrict__ dt, const float* __restrict__ lam,
+                                  float* __restrict__ dts, float* __restrict__ wts, int batch,
+                                  int seqlen, int rank, int nheads) {
+    const long long n = (long long)batch * seqlen * rank * nheads;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int h = (int)(i % nheads);
+        const int r = (int)((i / nheads) % rank);
+        const long long bt = i / ((long long)nheads * rank);
+        const int t = (int)(bt % seqlen);
+        const long long src = bt * nheads + h;
+        float w = lam[src] * dt[src];
+        if (t + 1 < seqlen) w = fmaf(dt[src + nheads], 1.0f - lam[src + nheads], w);
+        dts[i] = r == 0 ? dt[src] : 0.0f;
+        wts[i] = w;
+    }
+}
+
+// XD[bt][h][r'][r] = x_{t,r'} . dy_{t,r} (over p) and G[bt][g][r][r'] =
+// C_{t,r} . B_{t,r'} (over n): one warp per dot.
+__global__ void m3m_dots_kernel(const __nv_bfloat16* __restrict__ x,
+                                const __nv_bfloat16* __restrict__ dy,
+                                const __nv_bfloat16* __restrict__ B,
+                                const __nv_bfloat16* __restrict__ C, float* __restrict__ XD,
+                                float* __restrict__ G, int batch, int seqlen, int rank,
+                                int nheads, int ngroups) {
+    const long long steps = (long long)batch * seqlen;
+    const int R2 = rank * rank;
+    const long long nx = steps * nheads * R2, nb = steps * ngroups * R2;
+    const int lane = threadIdx.x & 31;
+    const long long wstride = ((long long)gridDim.x * blockDim.x) >> 5;
+    for (long long q = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; q < nx + nb;
+         q += wstride) {
+        float acc;
+        if (q < nx) {
+            const int r = (int)(q % rank), rp = (int)((q / rank) % rank);
+            const long long bth = q / R2, bt = bth / nheads;
+            const int h = (int)(bth % nheads);
+            const uint32_t a = reinterpret_cast<const uint32_t*>(
+                x + ((bt * rank + rp) * nheads + h) * kP)[lane];
+            const uint32_t d = reinterpret_cast<const uint32_t*>(
+                dy + ((bt * rank + r) * nheads + h) * kP)[lane];
+            acc = fmaf(bf16hi(a), bf16hi(d), bf16lo(a) * bf16lo(d));
+        } else {
+            const long long q2 = q - nx;
+            const int rp = (int)(q2 % rank), r = (int)((q2 / rank) % rank);
+            const long long btg = q2 / R2, bt = btg / ngroups;
+            const int g = (int)(btg % ngroups);
+            const uint2 cw = reinterpret_cast<const uint2*>(C + ((bt * rank + r) * ngroups + g) * kNs)[lane];
+            const uint2 bw = reinterpret_cast<const uint2*>(B + ((bt * rank + rp) * ngroups + g) * kNs)[lane];
+            acc = bf16lo(bw.x) * bf16lo(cw.x);
+            acc = fmaf(bf16hi(bw.x), bf16hi(cw.x), acc);
+            acc = fmaf(bf16lo(bw.y), bf16lo(cw.y), acc);
+            acc = fmaf(bf16hi(bw.y), bf16hi(cw.y), acc);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) {
+            if (q < nx) XD[q] = acc;
+            else G[q - nx] = acc;
+        }
+    }
+}
+
+// The previous token per (b, h), rank by rank (as m3_prev_kernel):
+//   dprev_x[b,r,h,p] = c0 sum_n dS[p,n] prev_B[b,r,g,n],
+//   pprevB[b,h,r,n] = c0 sum_p dS[p,n] prev_x[b,r,h,p],
+//   dc0[b,h] = sum_r sum_p prev_x[b,r,h,p] sum_n dS[p,n] prev_B[b,r,g,n].
+__global__ void m3m_prev_kernel(const float* __restrict__ dS,
+                                const __nv_bfloat16* __restrict__ prev_B,
+                                const __nv_bfloat16* __restrict__ prev_x,
+                                const float* __restrict__ dt, const float* __restrict__ lam,
+                                float* __restrict__ dprev_x, float* __restrict__ pprevB,
+                                float* __restrict__ dc0, int batch, int seqlen, int rank,
+                                int nheads, int ngroups) {
+    __shared__ float pb[kNs], px[kP], red[2];
+    const int item = blockIdx.x, b = item / nheads, h = item % nheads;
+    const int g = h / (nheads / ngroups);
+    const int tid = threadIdx.x;
+    const long long i0 = (long long)b * seqlen * nheads + h;
+    const float c0 = dt[i0] * (1.0f - lam[i0]);
+    const float* S = dS + (long long)item * kP * kNs;
+    float total = 0.0f;
+    for (int r = 0; r < rank; ++r) {
+        __syncthreads();  // pb, px, red of the previous rank are read
+        pb[tid] = __bfloat162float(prev_B[(((long long)b * rank + r) * ngroups + g) * kNs + tid]);
+        const long long xo = (((long long)b * rank + r) * nheads + h) * kP;
+        if (tid < kP) px[tid] = __bfloat162float(prev_x[xo + tid]);
+        __syncthreads();
+        float col = 0.0f;
+        for (int p = 0; p < kP; ++p) col = fmaf(S[p * kNs + tid], px[p], col);
+        pprevB[((long long)item * rank + r) * kNs + tid] = c0 * col;
+        if (tid < kP) {
+            float row = 0.0f;
+            const float* Sp = S + tid * kNs;
+            for (int n = 0; n < kNs; ++n) row = fmaf(Sp[n], pb[n], row);
+            dprev_x[xo + tid] = c0 * row;
+            float part = px[tid] * row;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            if ((tid & 31) == 0) red[tid >> 5] = part;
+        }
+        __syncthreads();
+        total += red[0] + red[1];
+    }
+    if (tid == 0) dc0[item] = total;
+}
+
+// dprev_B[b,r,g,n] = the group's heads' pprevB, added in head order.
+__global__ void m3m_prev_b_kernel(const float* __restrict__ pprevB, float* __restrict__ dprev_B,
+                                  int batch, int rank, int nheads, int ngroups) {
+    const int hpg = nheads / ngroups;
+    const long long n = (long long)batch * rank * ngroups * kNs;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int nn = (int)(i % kNs);
+        const int g = (int)((i / kNs) % ngroups);
+        const int r = (int)((i / ((long long)kNs * ngroups)) % rank);
+        const int b = (int)(i / ((long long)kNs * ngroups * rank));
+        float acc = 0.0f;
+        for (int h = g * hpg; h < (g + 1) * hpg; ++h)
+            acc += pprevB[(((long long)b * nheads + h) * rank + r) * kNs + nn];
+        dprev_B[i] = acc;
+    }
+}
+
+// sum_{r,r'} G_{rr'} XD_{r'r} for step row bt, head h.
+__device__ __forceinline__ float m3m_corr(const float* G, const float* XD, long long bt, int h,
+                                          int g, int rank, int nheads, int ngroups) {
+    const float* Gp = G + (bt * ngroups + g) * rank * rank;
+    const float* Xp = XD + (bt * nheads + h) * rank * rank;
+    float acc = 0.0f;
+    for (int r = 0; r < rank; ++r)
+        for (int rp = 0; rp < rank; ++rp) acc = fmaf(Gp[r * rank + rp], Xp[rp * rank + r], acc);
+    return acc;
+}
+
+// One CTA per (b, t): ddt and dlambda of every head (the step's log-decay part
+// from its first sub-token row, dw summed over its ranks), then the
+// correction's terms in dx, dB and dC.  Shared memory: 2 * nheads * R^2 floats.
+__global__ void m3m_post_kernel(const float* __restrict__ dt, const float* __restrict__ lam,
+                                const float* __restrict__ dw_rows,
+                                const float* __restrict__ ddec_rows, const float* __restrict__ XD,
+                                const float* __restrict__ G, const float* __restrict__ dc0,
+                                const __nv_bfloat16* __restrict__ dy,
+                                const __nv_bfloat16* __restrict__ B,
+                                const __nv_bfloat16* __restrict__ C, float* __restrict__ ddt,
+                                float* __restrict__ dlam, float* __restrict__ dx,
+                                float* __restrict__ dB, float* __restrict__ dC, int batch,
+                                int seqlen, int rank, int nheads, int ngroups) {
+    extern __shared__ float sm[];
+    const int R2 = rank * rank;
+    float* cG = sm;                  // [h][r][r'] c_t G_{rr'}
+    float* cX = sm + nheads * R2;    // [h][r'][r] c_t XD_{r'r}
+    const int hpg = nheads / ngroups;
+    for (long long bt = blockIdx.x; bt < (long long)batch * seqlen; bt += gridDim.x) {
+        const int t = (int)(bt % seqlen);
+        const int b = (int)(bt / seqlen);
+        for (int h = threadIdx.x; h < nheads; h += blockDim.x) {
+            const long long i = bt * nheads + h;
+            const int g = h / hpg;
+            const float c = t + 1 < seqlen ? dt[i + nheads] * (1.0f - lam[i + nheads]) : 0.0f;
+            float dwt = 0.0f, dwp = 0.0f;
+            for (int r = 0; r < rank; ++r) {
+                dwt += dw_rows[(bt * rank + r) * nheads + h];
+                if (t > 0) dwp += dw_rows[((bt - 1) * rank + r) * nheads + h];
+            }
+            float dcp = 0.0f;  // dL/dc_{t-1}
+            if (t > 0) dcp = dwp - m3m_corr(G, XD, bt - 1, h, g, rank, nheads, ngroups);
+            else if (dc0) dcp = dc0[(long long)b * nheads + h];
+            const float l = lam[i], d = dt[i];
+            ddt[i] = ddec_rows[(bt * rank) * nheads + h] + l * dwt + (1.0f - l) * dcp;
+            dlam[i] = d * dwt - d * dcp;
+            const float* Gp = G + (bt * ngroups + g) * R2;
+            const float* Xp = XD + (bt * nheads + h) * R2;
+            for (int k = 0; k < R2; ++k) {
+                cG[h * R2 + k] = c * Gp[k];
+                cX[h * R2 + k] = c * Xp[k];
+            }
+        }
+        __syncthreads();
+        // dx_{t,r'} -= sum_r c G_{rr'} dy_{t,r}
+        for (int idx = threadIdx.x; idx < rank * nheads * kP; idx += blockDim.x) {
+            const int p = idx % kP, h = (idx / kP) % nheads, rp = idx / (kP * nheads);
+            float acc = 0.0f;
+            for (int r = 0; r < rank; ++r)
+                acc = fmaf(cG[h * R2 + r * rank + rp],
+                           __bfloat162float(dy[((bt * rank + r) * nheads + h) * kP + p]), acc);
+            dx[((bt * rank + rp) * nheads + h) * kP + p] -= acc;
+        }
+        // dB_{t,r'} -= sum_h sum_r c XD_{r'r} C_{t,r};  dC_{t,r} -= sum_h sum_r' c XD_{r'r} B_{t,r'}
+        for (int idx = threadIdx.x; idx < rank * ngroups * kNs; idx += blockDim.x) {
+            const int n = idx % kNs, g = (idx / kNs) % ngroups, ra = idx / (kNs * ngroups);
+            float accB = 0.0f, accC = 0.0f;
+            for (int h = g * hpg; h < (g + 1) * hpg; ++h) {
+                for (int r = 0; r < rank; ++r) {
+                    accB = fmaf(cX[h * R2 + ra * rank + r],
+                                __bfloat162float(C[((bt * rank + r) * ngroups + g) * kNs + n]), accB);
+                    accC = fmaf(cX[h * R2 + r * rank + ra],
+                                __bfloat162float(B[((bt * rank + r) * ngroups + g) * kNs + n]), accC);
+                }
+            }
+            dB[((bt * rank + ra) * ngroups + g) * kNs + n] -= accB;
+            dC[((bt * rank + ra) * ngroups + g) * kNs + n] -= accC;
+        }
+        __syncthreads();
+    }
+}
+
+struct M3mWs {
+    size_t ssd, dts, wts, dw, ddec, xd, g, ds, dc0, ppb, total;
+};
+
+M3mWs m3m_workspace(int batch, int seqlen, int rank, int nheads, int ngroups) {
+    M3mWs m{};
+    const size_t steps = (size_t)batch * seqlen, items = (size_t)batch * nheads;
+    m.ssd = bwd_workspace(batch, seqlen * rank, nheads).total;
+    m.dts = round256(steps * rank * nheads * 4);
+    m.wts = m.dts;
+    m.dw = m.dts;
+    m.ddec = m.dts;
+    m.xd = round256(steps * nheads * rank * rank * 4);
+    m.g = round256(steps * ngroups * rank * rank * 4);
+    m.ds = round256(items * kP * kNs * 4);
+    m.dc0 = round256(items * 4);
+    m.ppb = round256(items * rank * kNs * 4);
+    m.total = m.ssd + m.dts + m.wts + m.dw + m.ddec + m.xd + m.g + m.ds + m.dc0 + m.ppb;
+    return m;
+}
+
+}  // namespace
+
+extern "C" size_t ssd_mamba3_mimo_bwd_workspace_bytes(int batch, int seqlen, int rank, int nheads,
+                                                      int headdim, int dstate, int ngroups) {
+    if (batch < 0 || seqlen < 0 || nheads < 0 || ngroups < 1 || headdim != kP || dstate != kNs ||
+        nheads % ngroups != 0 || (rank != 1 && rank != 2 && rank != 4))
+        return 0;
+    return m3m_workspace(batch, seqlen, rank, nheads, ngroups).total;
+}
+
+extern "C" ssm_status_t ssd_mamba3_mimo_bwd(
+    const void* x, const float* dt, const float* lam, const float* A_head, const void* B,
+    const void* C, int chunk, int rank, const float* initial_state, const void* prev_B,
+    const void* prev_x, const void* dy, const float* dfinal_state, float* dx, float* ddt,
+    float* dlam, float* dA_head, float* dB, float* dC, float* dinitial_state, float* dprev_B,
+    float* dprev_x, int batch, int seqlen, int nheads, int headdim, int dstate, int ngroups,
+    ssm_dtype_t in_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    using namespace ssm_host;
+    if (batch < 0 || seqlen < 0 || nheads < 0 || headdim < 1 || dstate < 1 || ngroups < 1 ||
+        chunk < 1 || rank < 1)
+        return SSM_ERR_SHAPE;
+    if (nheads % ngroups != 0 || seqlen % chunk != 0) return SSM_ERR_SHAPE;
+    if (!dtype_ok(in_dtype)) return SSM_ERR_DTYPE;
+    if ((rank != 1 && rank != 2 && rank != 4) || chunk * rank != 64 || headdim != kP ||
+        dstate != kNs || in_dtype != SSM_BF16)
+        return SSM_ERR_UNSUPPORTED;
+    if ((size_t)batch * nheads > (size_t)INT32_MAX ||
+        (size_t)seqlen * rank > (size_t)INT32_MAX)
+        return SSM_ERR_UNSUPPORTED;
+    if ((prev_B == nullptr) != (prev_x == nullptr)) return SSM_ERR_NULL;
+    const bool has_prev = prev_B != nullptr;
+    const size_t items = (size_t)batch * nheads;
+    const size_t steps = (size_t)batch * seqlen, subs = steps * rank;
+    const size_t sb = items * headdim * dstate * 4;
+    if (nheads > 0 && !dA_head) return SSM_ERR_NULL;
+    if (has_prev && items > 0 && (!dprev_B || !dprev_x)) return SSM_ERR_NULL;
+    const bool work = items > 0 && seqlen > 0;
+    if (work && (!x || !dt || !lam || !A_head || !B || !C || !dy || !dx || !ddt || !dlam ||
+                 !dB || !dC))
+        return SSM_ERR_NULL;
+    if (work && !workspace) return SSM_ERR_WORKSPACE;
+    const void* ptrs[] = {x, dt, lam, A_head, B, C, initial_state, prev_B, prev_x, dy,
+                          dfinal_state, dx, ddt, dlam, dA_head, dB, dC, dinitial_state, dprev_B,
+                          dprev_x, workspace};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return SSM_ERR_ALIGN;
+    const size_t xb = subs * nheads * headdim * 2, bcb = subs * ngroups * dstate * 2;
+    const size_t pbb = (size_t)batch * rank * ngroups * dstate,
+                 pxb = (size_t)batch * rank * nheads * headdim;
+    struct R { const void* p; size_t n; };
+    const R ins[] = {{x, xb}, {dt, steps * nheads * 4}, {lam, steps * nheads * 4},
+                     {A_head, (size_t)nheads * 4}, {B, bcb}, {C, bcb},
+                     {initial_state, initial_state ? sb : 0}, {prev_B, has_prev ? pbb * 2 : 0},
+                     {prev_x, has_prev ? pxb * 2 : 0}, {dy, xb},
+                     {dfinal_state, dfinal_state ? sb : 0}};
+    const R outs[] = {{dx, subs * nheads * headdim * 4}, {ddt, steps * nheads * 4},
+                      {dlam, steps * nheads * 4}, {dA_head, (size_t)nheads * 4},
+                      {dB, bcb * 2}, {dC, bcb * 2}, {dinitial_state, dinitial_state ? sb : 0},
+                      {dprev_B, has_prev ? pbb * 4 : 0}, {dprev_x, has_prev ? pxb * 4 : 0}};
+    constexpr int kOuts = sizeof(outs) / sizeof(outs[0]);
+    for (int i = 0; i < kOuts; ++i) {
+        for (const R& r : ins)
+            if (overlaps(outs[i].p, outs[i].n, r.p, r.n)) return SSM_ERR_ALIAS;
+        for (int j = i + 1; j < kOuts; ++j)
+            if (overlaps(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return SSM_ERR_ALIAS;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!work) {
+        if (nheads > 0 && cudaMemsetAsync(dA_head, 0, (size_t)nheads * 4, s) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        if (dinitial_state && sb) {
+            const cudaError_t e = dfinal_state ? cudaMemcpyAsync(dinitial_state, dfinal_state, sb,
+                                                                 cudaMemcpyDeviceToDevice, s)
+                                               : cudaMemsetAsync(dinitial_state, 0, sb, s);
+            if (e != cudaSuccess) return SSM_ERR_CUDA;
+        }
+        if (has_prev && items > 0) {
+            if (cudaMemsetAsync(dprev_B, 0, pbb * 4, s) != cudaSuccess ||
+                cudaMemsetAsync(dprev_x, 0, pxb * 4, s) != cudaSuccess)
+                return SSM_ERR_CUDA;
+        }
+        return SSM_OK;
+    }
+    const M3mWs m = m3m_workspace(batch, seqlen, rank, nheads, ngroups);
+    if (workspace_bytes < m.total) return SSM_ERR_WORKSPACE;
+    for (const R& r : ins)
+        if (overlaps(workspace, m.total, r.p, r.n)) return SSM_ERR_ALIAS;
+    for (const R& r : outs)
+        if (overlaps(workspace, m.total, r.p, r.n)) return SSM_ERR_ALIAS;
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    size_t o = m.ssd;
+    auto take = [&](size_t bytes) { float* p = reinterpret_cast<float*>(ws + o); o += bytes; return p; };
+    float* dts = take(m.dts);
+    float* wts = take(m.wts);
+    float* dw = take(m.dw);
+    float* ddec = take(m.ddec);
+    float* XD = take(m.xd);
+    float* Gd = take(m.g);
+    float* dS = take(m.ds);
+    float* dc0 = take(m.dc0);
+    float* ppb = take(m.ppb);
+    float* dS_out = dinitial_state ? dinitial_state : (has_prev ? dS : nullptr);
+
+    // 1. per sub-token: the step's dt on its first row and its weight on every row
+    m3m_expand_kernel<<<grid_for((long long)subs * nheads, 256), 256, 0, s>>>(
+        dt, lam, dts, wts, batch, seqlen, rank, nheads);
+    if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
+    // 2. the SSD gradient over the sub-tokens (block-lower-triangular mask)
+    const MakeStates states = [&](float* bs) {
+        return ssd_internal::ssd_mamba3_forward_block_states(x, dt, lam, A_head, B, C,
+                                                             initial_state, prev_B, prev_x, bs,
+                                                             batch, seqlen, nheads, ngroups, s,
+                                                             rank);
+    };
+    ssm_status_t rc = run_bwd(x, dts, wts, A_head, B, C, initial_state, dy, dfinal_state, nullptr,
+                              states, dx, ddec, dw, dA_head, dB, dC, dS_out, batch,
+                              seqlen * rank, nheads, ngroups, workspace, s, rank);
+    if (rc != SSM_OK) return rc;
+    // 3. the rank-by-rank dots of every step
+    const long long ndots = (long long)steps * (nheads + ngroups) * rank * rank;
+    m3m_dots_kernel<<<grid_for(ndots * 32, 256), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(dy),
+        static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), XD, Gd,
+        batch, seqlen, rank, nheads, ngroups);
+    if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
+    // 4. the previous token
+    if (has_prev) {
+        m3m_prev_kernel<<<(unsigned)items, kNs, 0, s>>>(
+            dS_out, static_cast<const __nv_bfloat16*>(prev_B),
+            static_cast<const __nv_bfloat16*>(prev_x), dt, lam, dprev_x, ppb, dc0, batch, seqlen,
+            rank, nheads, ngroups);
+        if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
+        m3m_prev_b_kernel<<<grid_for((long long)pbb, 256), 256, 0, s>>>(ppb, dprev_B, batch,
+                                                                        rank, nheads, ngroups);
+        if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
+    }
+    // 5. ddt, dlambda and the block-diagonal correction's terms
+    m3m_post_kernel<<<(unsigned)std::min<long long>((long long)steps, 65535), 256,
+                      2 * nheads * rank * rank * sizeof(float), s>>>(
+        dt, lam, dw, ddec, XD, Gd, has_prev ? dc0 : nullptr,
+        static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(B),
+        static_cast<const __nv_bfloat16*>(C), ddt, dlam, dx, dB, dC, batch, seqlen, rank, nheads,
+        ngroups);
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }

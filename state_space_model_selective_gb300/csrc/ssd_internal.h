@@ -17,16 +17,17 @@ ssm_status_t ssd_forward_block_states(const void* x, const float* dt, const floa
                                       float* bstates, int batch, int seqlen, int nheads,
                                       int ngroups, cudaStream_t stream);
 
-// The Mamba-3 SISO forward writing only the states its chunked form carries
-// between blocks: the state entering each 128-step block (with the pending
-// dt_{t+1} (1 - lambda_{t+1}) B_t (x) x_t of the step before, and the previous
-// token's term in block 0) and the final state, laid out as above.  prev_B,
-// prev_x (bf16) may both be NULL.  Arguments are validated by the caller.
+// The Mamba-3 forward (rank 1, 2 or 4; MIMO blocks are 128 rows of
+// sub-tokens) writing only the states its chunked form carries between
+// blocks: the state entering each block (with the pending dt_{t+1} (1 -
+// lambda_{t+1}) BX_t of the step before, and the previous token's term in block
+// 0) and the final state, laid out as above.  prev_B, prev_x (bf16) may both be
+// NULL.  Arguments are validated by the caller.
 ssm_status_t ssd_mamba3_forward_block_states(const void* x, const float* dt, const float* lam,
                                              const float* A_head, const void* B, const void* C,
                                              const float* initial_state, const void* prev_B,
                                              const void* prev_x, float* bstates, int batch,
                                              int seqlen, int nheads, int ngroups,
-                                             cudaStream_t stream);
+                                             cudaStream_t stream, int rank = 1);
 
 }  // namespace ssd_internal

@@ -383,6 +383,43 @@ def test_mamba3_bwd_workspace_bytes():
     assert f(1, 64, 3, ngroups=2) == 0
 
 
+def mimo_bwd_call(L, **kw):
+    args = dict(x=P(0), dt=P(1), lam=P(12), A=P(2), B=P(3), C=P(4), chunk=16, rank=4, h0=None,
+                pB=None, px=None, dy=P(5), dfs=None, dx=P(6), ddt=P(7), dlam=P(13), dA=P(8),
+                dB=P(9), dC=P(10), dh0=None, dpB=None, dpx=None, batch=2, seqlen=64, nheads=4,
+                headdim=64, dstate=128, ngroups=1, in_dt=1, ws=P(11), wsb=1 << 30, stream=None)
+    args.update(kw)
+    a = args
+    return L.ssd_mamba3_mimo_bwd(a["x"], a["dt"], a["lam"], a["A"], a["B"], a["C"], a["chunk"],
+                                 a["rank"], a["h0"], a["pB"], a["px"], a["dy"], a["dfs"], a["dx"],
+                                 a["ddt"], a["dlam"], a["dA"], a["dB"], a["dC"], a["dh0"],
+                                 a["dpB"], a["dpx"], a["batch"], a["seqlen"], a["nheads"],
+                                 a["headdim"], a["dstate"], a["ngroups"], a["in_dt"], a["ws"],
+                                 a["wsb"], a["stream"])
+
+
+def test_mimo_bwd_argument_errors(L):
+    assert mimo_bwd_call(L, lam=None) == NULL
+    assert mimo_bwd_call(L, px=P(15)) == NULL            # prev_x without prev_B
+    assert mimo_bwd_call(L, pB=P(14), px=P(15)) == NULL  # previous token without its gradients
+    assert mimo_bwd_call(L, seqlen=60) == SHAPE          # not a multiple of the chunk
+    assert mimo_bwd_call(L, rank=0) == SHAPE
+    assert mimo_bwd_call(L, rank=3, chunk=16) == UNSUP
+    assert mimo_bwd_call(L, rank=4, chunk=32) == UNSUP   # chunk * rank != 64
+    assert mimo_bwd_call(L, in_dt=0) == UNSUP
+    assert mimo_bwd_call(L, dx=ctypes.c_void_p(0x70000008)) == ALIGN
+    assert mimo_bwd_call(L, wsb=1024) == WS
+    assert mimo_bwd_call(L, dB=P(3)) == ALIAS             # dB on top of B
+    assert mimo_bwd_call(L, nheads=0, dA=None, x=None) == OK
+
+
+def test_mimo_bwd_workspace_bytes():
+    f = binding.ssd_mamba3_mimo_bwd_workspace_bytes
+    assert f(32, 256, 4, 32) > binding.ssd_chunked_bwd_workspace_bytes(32, 1024, 32)
+    assert f(2, 64, 3, 4) == 0
+    assert f(1, 64, 4, 3, ngroups=2) == 0
+
+
 def host_call(L, **kw):
     args = dict(u=P(0), delta=P(1), A=P(2), B=P(3), C=P(4), D=None, z=None, bias=None,
                 softplus=1, h0=None, y=P(5), fs=None, batch=2, dim=32, seqlen=64, dstate=16,
