@@ -1310,93 +1310,132 @@ __global__ void m3m_expand_kernel(const float* __restrict__ dt, const float* __r
 }
 
 // XD[bt][h][r'][r] = x_{t,r'} . dy_{t,r} (over p) and G[bt][g][r][r'] =
-// C_{t,r} . B_{t,r'} (over n): one warp per dot.
+// C_{t,r} . B_{t,r'} (over n): one warp per (step, head) or (step, group) row
+// reads its RK x (or C) and RK dy (or B) rows once and forms all RK^2 dots,
+// each summed over the lanes by a fixed butterfly.
+template <int RK>
 __global__ void m3m_dots_kernel(const __nv_bfloat16* __restrict__ x,
                                 const __nv_bfloat16* __restrict__ dy,
                                 const __nv_bfloat16* __restrict__ B,
                                 const __nv_bfloat16* __restrict__ C, float* __restrict__ XD,
-                                float* __restrict__ G, int batch, int seqlen, int rank,
-                                int nheads, int ngroups) {
+                                float* __restrict__ G, int batch, int seqlen, int nheads,
+                                int ngroups) {
     const long long steps = (long long)batch * seqlen;
-    const int R2 = rank * rank;
-    const long long nx = steps * nheads * R2, nb = steps * ngroups * R2;
+    const long long nx = steps * nheads, nb = steps * ngroups;
     const int lane = threadIdx.x & 31;
     const long long wstride = ((long long)gridDim.x * blockDim.x) >> 5;
     for (long long q = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; q < nx + nb;
          q += wstride) {
-        float acc;
+        float acc[RK][RK];
         if (q < nx) {
-            const int r = (int)(q % rank), rp = (int)((q / rank) % rank);
-            const long long bth = q / R2, bt = bth / nheads;
-            const int h = (int)(bth % nheads);
-            const uint32_t a = reinterpret_cast<const uint32_t*>(
-                x + ((bt * rank + rp) * nheads + h) * kP)[lane];
-            const uint32_t d = reinterpret_cast<const uint32_t*>(
-                dy + ((bt * rank + r) * nheads + h) * kP)[lane];
-            acc = fmaf(bf16hi(a), bf16hi(d), bf16lo(a) * bf16lo(d));
+            const long long bt = q / nheads;
+            const int h = (int)(q % nheads);
+            uint32_t a[RK], d[RK];
+#pragma unroll
+            for (int r = 0; r < RK; ++r) {
+                a[r] = reinterpret_cast<const uint32_t*>(x + ((bt * RK + r) * nheads + h) * kP)[lane];
+                d[r] = reinterpret_cast<const uint32_t*>(dy + ((bt * RK + r) * nheads + h) * kP)[lane];
+            }
+#pragma unroll
+            for (int rp = 0; rp < RK; ++rp)
+#pragma unroll
+                for (int r = 0; r < RK; ++r)
+                    acc[rp][r] = fmaf(bf16hi(a[rp]), bf16hi(d[r]), bf16lo(a[rp]) * bf16lo(d[r]));
         } else {
             const long long q2 = q - nx;
-            const int rp = (int)(q2 % rank), r = (int)((q2 / rank) % rank);
-            const long long btg = q2 / R2, bt = btg / ngroups;
-            const int g = (int)(btg % ngroups);
-            const uint2 cw = reinterpret_cast<const uint2*>(C + ((bt * rank + r) * ngroups + g) * kNs)[lane];
-            const uint2 bw = reinterpret_cast<const uint2*>(B + ((bt * rank + rp) * ngroups + g) * kNs)[lane];
-            acc = bf16lo(bw.x) * bf16lo(cw.x);
-            acc = fmaf(bf16hi(bw.x), bf16hi(cw.x), acc);
-            acc = fmaf(bf16lo(bw.y), bf16lo(cw.y), acc);
-            acc = fmaf(bf16hi(bw.y), bf16hi(cw.y), acc);
+            const long long bt = q2 / ngroups;
+            const int g = (int)(q2 % ngroups);
+            uint2 cw[RK], bw[RK];
+#pragma unroll
+            for (int r = 0; r < RK; ++r) {
+                cw[r] = reinterpret_cast<const uint2*>(C + ((bt * RK + r) * ngroups + g) * kNs)[lane];
+                bw[r] = reinterpret_cast<const uint2*>(B + ((bt * RK + r) * ngroups + g) * kNs)[lane];
+            }
+#pragma unroll
+            for (int r = 0; r < RK; ++r)
+#pragma unroll
+                for (int rp = 0; rp < RK; ++rp) {
+                    float v = bf16lo(bw[rp].x) * bf16lo(cw[r].x);
+                    v = fmaf(bf16hi(bw[rp].x), bf16hi(cw[r].x), v);
+                    v = fmaf(bf16lo(bw[rp].y), bf16lo(cw[r].y), v);
+                    acc[r][rp] = fmaf(bf16hi(bw[rp].y), bf16hi(cw[r].y), v);
+                }
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        for (int u = 0; u < RK; ++u)
+#pragma unroll
+            for (int v = 0; v < RK; ++v)
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    acc[u][v] += __shfl_xor_sync(0xffffffffu, acc[u][v], o);
         if (lane == 0) {
-            if (q < nx) XD[q] = acc;
-            else G[q - nx] = acc;
+            float* out = q < nx ? XD + q * RK * RK : G + (q - nx) * RK * RK;
+#pragma unroll
+            for (int u = 0; u < RK; ++u)
+#pragma unroll
+                for (int v = 0; v < RK; ++v) out[u * RK + v] = acc[u][v];
         }
     }
 }
 
-// The previous token per (b, h), rank by rank (as m3_prev_kernel):
+// The previous token per (b, h), all ranks in one pass over dS (as
+// m3_prev_kernel):
 //   dprev_x[b,r,h,p] = c0 sum_n dS[p,n] prev_B[b,r,g,n],
 //   pprevB[b,h,r,n] = c0 sum_p dS[p,n] prev_x[b,r,h,p],
 //   dc0[b,h] = sum_r sum_p prev_x[b,r,h,p] sum_n dS[p,n] prev_B[b,r,g,n].
+template <int RK>
 __global__ void m3m_prev_kernel(const float* __restrict__ dS,
                                 const __nv_bfloat16* __restrict__ prev_B,
                                 const __nv_bfloat16* __restrict__ prev_x,
                                 const float* __restrict__ dt, const float* __restrict__ lam,
                                 float* __restrict__ dprev_x, float* __restrict__ pprevB,
-                                float* __restrict__ dc0, int batch, int seqlen, int rank,
-                                int nheads, int ngroups) {
-    __shared__ float pb[kNs], px[kP], red[2];
+                                float* __restrict__ dc0, int batch, int seqlen, int nheads,
+                                int ngroups) {
+    __shared__ float pb[RK][kNs], px[RK][kP], red[2];
     const int item = blockIdx.x, b = item / nheads, h = item % nheads;
     const int g = h / (nheads / ngroups);
     const int tid = threadIdx.x;
     const long long i0 = (long long)b * seqlen * nheads + h;
     const float c0 = dt[i0] * (1.0f - lam[i0]);
-    const float* S = dS + (long long)item * kP * kNs;
-    float total = 0.0f;
-    for (int r = 0; r < rank; ++r) {
-        __syncthreads();  // pb, px, red of the previous rank are read
-        pb[tid] = __bfloat162float(prev_B[(((long long)b * rank + r) * ngroups + g) * kNs + tid]);
-        const long long xo = (((long long)b * rank + r) * nheads + h) * kP;
-        if (tid < kP) px[tid] = __bfloat162float(prev_x[xo + tid]);
-        __syncthreads();
-        float col = 0.0f;
-        for (int p = 0; p < kP; ++p) col = fmaf(S[p * kNs + tid], px[p], col);
-        pprevB[((long long)item * rank + r) * kNs + tid] = c0 * col;
-        if (tid < kP) {
-            float row = 0.0f;
-            const float* Sp = S + tid * kNs;
-            for (int n = 0; n < kNs; ++n) row = fmaf(Sp[n], pb[n], row);
-            dprev_x[xo + tid] = c0 * row;
-            float part = px[tid] * row;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-            if ((tid & 31) == 0) red[tid >> 5] = part;
-        }
-        __syncthreads();
-        total += red[0] + red[1];
+    for (int r = 0; r < RK; ++r) {
+        pb[r][tid] = __bfloat162float(prev_B[(((long long)b * RK + r) * ngroups + g) * kNs + tid]);
+        if (tid < kP) px[r][tid] = __bfloat162float(prev_x[(((long long)b * RK + r) * nheads + h) * kP + tid]);
     }
-    if (tid == 0) dc0[item] = total;
+    __syncthreads();
+    const float* S = dS + (long long)item * kP * kNs;
+    float col[RK];
+#pragma unroll
+    for (int r = 0; r < RK; ++r) col[r] = 0.0f;
+    for (int p = 0; p < kP; ++p) {
+        const float sv = S[p * kNs + tid];
+#pragma unroll
+        for (int r = 0; r < RK; ++r) col[r] = fmaf(sv, px[r][p], col[r]);
+    }
+#pragma unroll
+    for (int r = 0; r < RK; ++r) pprevB[((long long)item * RK + r) * kNs + tid] = c0 * col[r];
+    if (tid < kP) {
+        float row[RK];
+#pragma unroll
+        for (int r = 0; r < RK; ++r) row[r] = 0.0f;
+        const float* Sp = S + tid * kNs;
+        for (int n = 0; n < kNs; ++n) {
+            const float sv = Sp[n];
+#pragma unroll
+            for (int r = 0; r < RK; ++r) row[r] = fmaf(sv, pb[r][n], row[r]);
+        }
+        float part = 0.0f;
+#pragma unroll
+        for (int r = 0; r < RK; ++r) {
+            dprev_x[(((long long)b * RK + r) * nheads + h) * kP + tid] = c0 * row[r];
+            part = fmaf(px[r][tid], row[r], part);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if ((tid & 31) == 0) red[tid >> 5] = part;
+    }
+    __syncthreads();
+    if (tid == 0) dc0[item] = red[0] + red[1];
 }
 
 // dprev_B[b,r,g,n] = the group's heads' pprevB, added in head order.
@@ -1417,20 +1456,11 @@ __global__ void m3m_prev_b_kernel(const float* __restrict__ pprevB, float* __res
     }
 }
 
-// sum_{r,r'} G_{rr'} XD_{r'r} for step row bt, head h.
-__device__ __forceinline__ float m3m_corr(const float* G, const float* XD, long long bt, int h,
-                                          int g, int rank, int nheads, int ngroups) {
-    const float* Gp = G + (bt * ngroups + g) * rank * rank;
-    const float* Xp = XD + (bt * nheads + h) * rank * rank;
-    float acc = 0.0f;
-    for (int r = 0; r < rank; ++r)
-        for (int rp = 0; rp < rank; ++rp) acc = fmaf(Gp[r * rank + rp], Xp[rp * rank + r], acc);
-    return acc;
-}
-
 // One CTA per (b, t): ddt and dlambda of every head (the step's log-decay part
 // from its first sub-token row, dw summed over its ranks), then the
-// correction's terms in dx, dB and dC.  Shared memory: 2 * nheads * R^2 floats.
+// correction's terms in dx, dB and dC (c XD summed over the group's heads
+// first, in head order).  Shared memory: (2 nheads + ngroups) R^2 floats.
+template <int RK>
 __global__ void m3m_post_kernel(const float* __restrict__ dt, const float* __restrict__ lam,
                                 const float* __restrict__ dw_rows,
                                 const float* __restrict__ ddec_rows, const float* __restrict__ XD,
@@ -1440,11 +1470,12 @@ __global__ void m3m_post_kernel(const float* __restrict__ dt, const float* __res
                                 const __nv_bfloat16* __restrict__ C, float* __restrict__ ddt,
                                 float* __restrict__ dlam, float* __restrict__ dx,
                                 float* __restrict__ dB, float* __restrict__ dC, int batch,
-                                int seqlen, int rank, int nheads, int ngroups) {
+                                int seqlen, int nheads, int ngroups) {
     extern __shared__ float sm[];
-    const int R2 = rank * rank;
-    float* cG = sm;                  // [h][r][r'] c_t G_{rr'}
-    float* cX = sm + nheads * R2;    // [h][r'][r] c_t XD_{r'r}
+    constexpr int R2 = RK * RK;
+    float* cG = sm;                    // [h][r][r'] c_t G_{rr'}
+    float* cX = sm + nheads * R2;      // [h][r'][r] c_t XD_{r'r}
+    float* sX = sm + 2 * nheads * R2;  // [g][r'][r] sum over the group's heads of cX
     const int hpg = nheads / ngroups;
     for (long long bt = blockIdx.x; bt < (long long)batch * seqlen; bt += gridDim.x) {
         const int t = (int)(bt % seqlen);
@@ -1454,47 +1485,67 @@ __global__ void m3m_post_kernel(const float* __restrict__ dt, const float* __res
             const int g = h / hpg;
             const float c = t + 1 < seqlen ? dt[i + nheads] * (1.0f - lam[i + nheads]) : 0.0f;
             float dwt = 0.0f, dwp = 0.0f;
-            for (int r = 0; r < rank; ++r) {
-                dwt += dw_rows[(bt * rank + r) * nheads + h];
-                if (t > 0) dwp += dw_rows[((bt - 1) * rank + r) * nheads + h];
+#pragma unroll
+            for (int r = 0; r < RK; ++r) {
+                dwt += dw_rows[(bt * RK + r) * nheads + h];
+                if (t > 0) dwp += dw_rows[((bt - 1) * RK + r) * nheads + h];
             }
             float dcp = 0.0f;  // dL/dc_{t-1}
-            if (t > 0) dcp = dwp - m3m_corr(G, XD, bt - 1, h, g, rank, nheads, ngroups);
-            else if (dc0) dcp = dc0[(long long)b * nheads + h];
+            if (t > 0) {
+                const float* Gp = G + ((bt - 1) * ngroups + g) * R2;
+                const float* Xp = XD + ((bt - 1) * nheads + h) * R2;
+                float corr = 0.0f;
+#pragma unroll
+                for (int r = 0; r < RK; ++r)
+#pragma unroll
+                    for (int rp = 0; rp < RK; ++rp)
+                        corr = fmaf(Gp[r * RK + rp], Xp[rp * RK + r], corr);
+                dcp = dwp - corr;
+            } else if (dc0) {
+                dcp = dc0[(long long)b * nheads + h];
+            }
             const float l = lam[i], d = dt[i];
-            ddt[i] = ddec_rows[(bt * rank) * nheads + h] + l * dwt + (1.0f - l) * dcp;
+            ddt[i] = ddec_rows[(bt * RK) * nheads + h] + l * dwt + (1.0f - l) * dcp;
             dlam[i] = d * dwt - d * dcp;
             const float* Gp = G + (bt * ngroups + g) * R2;
             const float* Xp = XD + (bt * nheads + h) * R2;
+#pragma unroll
             for (int k = 0; k < R2; ++k) {
                 cG[h * R2 + k] = c * Gp[k];
                 cX[h * R2 + k] = c * Xp[k];
             }
         }
         __syncthreads();
+        for (int idx = threadIdx.x; idx < ngroups * R2; idx += blockDim.x) {
+            const int g = idx / R2, k = idx % R2;
+            float acc = 0.0f;
+            for (int h = g * hpg; h < (g + 1) * hpg; ++h) acc += cX[h * R2 + k];
+            sX[idx] = acc;
+        }
+        __syncthreads();
         // dx_{t,r'} -= sum_r c G_{rr'} dy_{t,r}
-        for (int idx = threadIdx.x; idx < rank * nheads * kP; idx += blockDim.x) {
+        for (int idx = threadIdx.x; idx < RK * nheads * kP; idx += blockDim.x) {
             const int p = idx % kP, h = (idx / kP) % nheads, rp = idx / (kP * nheads);
             float acc = 0.0f;
-            for (int r = 0; r < rank; ++r)
-                acc = fmaf(cG[h * R2 + r * rank + rp],
-                           __bfloat162float(dy[((bt * rank + r) * nheads + h) * kP + p]), acc);
-            dx[((bt * rank + rp) * nheads + h) * kP + p] -= acc;
+#pragma unroll
+            for (int r = 0; r < RK; ++r)
+                acc = fmaf(cG[h * R2 + r * RK + rp],
+                           __bfloat162float(dy[((bt * RK + r) * nheads + h) * kP + p]), acc);
+            dx[((bt * RK + rp) * nheads + h) * kP + p] -= acc;
         }
-        // dB_{t,r'} -= sum_h sum_r c XD_{r'r} C_{t,r};  dC_{t,r} -= sum_h sum_r' c XD_{r'r} B_{t,r'}
-        for (int idx = threadIdx.x; idx < rank * ngroups * kNs; idx += blockDim.x) {
+        // dB_{t,r'} -= sum_r sX_{r'r} C_{t,r};  dC_{t,r} -= sum_r' sX_{r'r} B_{t,r'}
+        for (int idx = threadIdx.x; idx < RK * ngroups * kNs; idx += blockDim.x) {
             const int n = idx % kNs, g = (idx / kNs) % ngroups, ra = idx / (kNs * ngroups);
             float accB = 0.0f, accC = 0.0f;
-            for (int h = g * hpg; h < (g + 1) * hpg; ++h) {
-                for (int r = 0; r < rank; ++r) {
-                    accB = fmaf(cX[h * R2 + ra * rank + r],
-                                __bfloat162float(C[((bt * rank + r) * ngroups + g) * kNs + n]), accB);
-                    accC = fmaf(cX[h * R2 + r * rank + ra],
-                                __bfloat162float(B[((bt * rank + r) * ngroups + g) * kNs + n]), accC);
-                }
+#pragma unroll
+            for (int r = 0; r < RK; ++r) {
+                accB = fmaf(sX[g * R2 + ra * RK + r],
+                            __bfloat162float(C[((bt * RK + r) * ngroups + g) * kNs + n]), accB);
+                accC = fmaf(sX[g * R2 + r * RK + ra],
+                            __bfloat162float(B[((bt * RK + r) * ngroups + g) * kNs + n]), accC);
             }
-            dB[((bt * rank + ra) * ngroups + g) * kNs + n] -= accB;
-            dC[((bt * rank + ra) * ngroups + g) * kNs + n] -= accC;
+            dB[((bt * RK + ra) * ngroups + g) * kNs + n] -= accB;
+            dC[((bt * RK + ra) * ngroups + g) * kNs + n] -= accC;
         }
         __syncthreads();
     }
@@ -1519,6 +1570,40 @@ M3mWs m3m_workspace(int batch, int seqlen, int rank, int nheads, int ngroups) {
     m.ppb = round256(items * rank * kNs * 4);
     m.total = m.ssd + m.dts + m.wts + m.dw + m.ddec + m.xd + m.g + m.ds + m.dc0 + m.ppb;
     return m;
+}
+
+// Steps 3-5 of the MIMO gradient for rank RK.
+template <int RK>
+ssm_status_t m3m_tail(const void* x, const float* dt, const float* lam, const void* B,
+                      const void* C, const void* dy, bool has_prev, const void* prev_B,
+                      const void* prev_x, const float* dS, const float* dw, const float* ddec,
+                      float* XD, float* Gd, float* dc0, float* ppb, float* ddt, float* dlam,
+                      float* dx, float* dB, float* dC, float* dprev_B, float* dprev_x, int batch,
+                      int seqlen, int nheads, int ngroups, cudaStream_t s) {
+    const long long steps = (long long)batch * seqlen;
+    const long long nrows = steps * (nheads + ngroups);
+    m3m_dots_kernel<RK><<<grid_for(nrows * 32, 256), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(dy),
+        static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), XD, Gd,
+        batch, seqlen, nheads, ngroups);
+    if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
+    if (has_prev) {
+        m3m_prev_kernel<RK><<<(unsigned)((long long)batch * nheads), kNs, 0, s>>>(
+            dS, static_cast<const __nv_bfloat16*>(prev_B),
+            static_cast<const __nv_bfloat16*>(prev_x), dt, lam, dprev_x, ppb, dc0, batch, seqlen,
+            nheads, ngroups);
+        if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
+        m3m_prev_b_kernel<<<grid_for((long long)batch * RK * ngroups * kNs, 256), 256, 0, s>>>(
+            ppb, dprev_B, batch, RK, nheads, ngroups);
+        if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
+    }
+    m3m_post_kernel<RK><<<(unsigned)std::min<long long>(steps, 65535), 256,
+                          (2 * nheads + ngroups) * RK * RK * sizeof(float), s>>>(
+        dt, lam, dw, ddec, XD, Gd, has_prev ? dc0 : nullptr,
+        static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(B),
+        static_cast<const __nv_bfloat16*>(C), ddt, dlam, dx, dB, dC, batch, seqlen, nheads,
+        ngroups);
+    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 }  // namespace
@@ -1640,30 +1725,9 @@ extern "C" ssm_status_t ssd_mamba3_mimo_bwd(
                               states, dx, ddec, dw, dA_head, dB, dC, dS_out, batch,
                               seqlen * rank, nheads, ngroups, workspace, s, rank);
     if (rc != SSM_OK) return rc;
-    // 3. the rank-by-rank dots of every step
-    const long long ndots = (long long)steps * (nheads + ngroups) * rank * rank;
-    m3m_dots_kernel<<<grid_for(ndots * 32, 256), 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(dy),
-        static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), XD, Gd,
-        batch, seqlen, rank, nheads, ngroups);
-    if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
-    // 4. the previous token
-    if (has_prev) {
-        m3m_prev_kernel<<<(unsigned)items, kNs, 0, s>>>(
-            dS_out, static_cast<const __nv_bfloat16*>(prev_B),
-            static_cast<const __nv_bfloat16*>(prev_x), dt, lam, dprev_x, ppb, dc0, batch, seqlen,
-            rank, nheads, ngroups);
-        if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
-        m3m_prev_b_kernel<<<grid_for((long long)pbb, 256), 256, 0, s>>>(ppb, dprev_B, batch,
-                                                                        rank, nheads, ngroups);
-        if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
-    }
-    // 5. ddt, dlambda and the block-diagonal correction's terms
-    m3m_post_kernel<<<(unsigned)std::min<long long>((long long)steps, 65535), 256,
-                      2 * nheads * rank * rank * sizeof(float), s>>>(
-        dt, lam, dw, ddec, XD, Gd, has_prev ? dc0 : nullptr,
-        static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(B),
-        static_cast<const __nv_bfloat16*>(C), ddt, dlam, dx, dB, dC, batch, seqlen, rank, nheads,
-        ngroups);
-    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+    // 3.-5. the dots, the previous token and the per-step terms
+    auto tail = rank == 1 ? m3m_tail<1> : rank == 2 ? m3m_tail<2> : m3m_tail<4>;
+    rc = tail(x, dt, lam, B, C, dy, has_prev, prev_B, prev_x, dS_out, dw, ddec, XD, Gd, dc0, ppb,
+              ddt, dlam, dx, dB, dC, dprev_B, dprev_x, batch, seqlen, nheads, ngroups, s);
+    return rc;
 }
