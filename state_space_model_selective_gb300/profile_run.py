@@ -6,6 +6,8 @@
     python -m state_space_model_selective_gb300.profile_run scan_bwd [--reps 5]
     python -m state_space_model_selective_gb300.profile_run ssd_bwd [--reps 5]
     python -m state_space_model_selective_gb300.profile_run decode_mimo [--reps 5]
+    python -m state_space_model_selective_gb300.profile_run m3_bwd [--reps 5]
+    python -m state_space_model_selective_gb300.profile_run mimo_bwd [--reps 5]
 
 scan:     selective scan, bf16 in / fp32 y, batch 8, L 2048, D 1536, N 16
 ssd:      chunked SSD, bf16 in / fp32 y, batch 32, L 256, 32 heads, headdim 64, N 128
@@ -13,6 +15,8 @@ decode:   decode step, fp32, batch 256, 32 heads, headdim 64, N 128
 scan_bwd: the scan's gradient on the scan workload (D, gate, bias, softplus)
 ssd_bwd:  the chunked SSD's gradient on the SSD workload
 decode_mimo: Mamba-3 MIMO rank-4 decode step, fp32, batch 256, 32 heads, headdim 64, N 128
+m3_bwd:   Mamba-3 SISO gradient on the SSD workload (initial state, previous token)
+mimo_bwd: Mamba-3 MIMO rank-4 gradient, batch 32, L 256, 32 heads, headdim 64, N 128, chunk 16
 Inputs are drawn on the GPU (seeded); the process exits non-zero on any error.
 """
 from __future__ import annotations
@@ -27,7 +31,8 @@ from . import binding, inputs
 def main(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("workload",
-                   choices=["scan", "ssd", "decode", "scan_bwd", "ssd_bwd", "decode_mimo"])
+                   choices=["scan", "ssd", "decode", "scan_bwd", "ssd_bwd", "decode_mimo",
+                            "m3_bwd", "mimo_bwd"])
     p.add_argument("--reps", type=int, default=5)
     a = p.parse_args(argv)
     dev = torch.device("cuda")
@@ -74,6 +79,31 @@ def main(argv=None):
         for _ in range(a.reps):
             binding.ssd_chunked_bwd(inp["x"], inp["dt"], inp["A_head"], inp["B"], inp["C"], dy,
                                     64, workspace=ws)
+        torch.cuda.synchronize()
+        assert binding.ssm_last_device_status(ws) == 0
+    elif a.workload == "m3_bwd":
+        m3 = inputs.mamba3_inputs(32, 256, 32, 64, 128, 1, "bf16", seed=1006, device="cuda")
+        g = torch.Generator(device=dev)
+        g.manual_seed(1010)
+        dy = torch.randn(32, 256, 32, 64, device=dev, generator=g).to(torch.bfloat16)
+        ws = torch.empty(binding.ssd_mamba3_bwd_workspace_bytes(32, 256, 32), dtype=torch.uint8,
+                         device=dev)
+        for _ in range(a.reps):
+            binding.ssd_mamba3_bwd(m3["x"], m3["dt"], m3["lam"], m3["A_head"], m3["B"], m3["C"],
+                                   dy, 64, m3["h0"], m3["prev_B"], m3["prev_x"], workspace=ws)
+        torch.cuda.synchronize()
+        assert binding.ssm_last_device_status(ws) == 0
+    elif a.workload == "mimo_bwd":
+        m = inputs.mamba3_mimo_inputs(32, 256, 4, 32, 64, 128, 1, "bf16", seed=1007,
+                                      device="cuda")
+        g = torch.Generator(device=dev)
+        g.manual_seed(1011)
+        dy = torch.randn(32, 256, 4, 32, 64, device=dev, generator=g).to(torch.bfloat16)
+        ws = torch.empty(binding.ssd_mamba3_mimo_bwd_workspace_bytes(32, 256, 4, 32),
+                         dtype=torch.uint8, device=dev)
+        for _ in range(a.reps):
+            binding.ssd_mamba3_mimo_bwd(m["x"], m["dt"], m["lam"], m["A_head"], m["B"], m["C"],
+                                        dy, 16, m["h0"], m["prev_B"], m["prev_x"], workspace=ws)
         torch.cuda.synchronize()
         assert binding.ssm_last_device_status(ws) == 0
     elif a.workload == "decode_mimo":
