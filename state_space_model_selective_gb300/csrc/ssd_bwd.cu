@@ -1523,15 +1523,25 @@ __global__ void m3m_post_kernel(const float* __restrict__ dt, const float* __res
             sX[idx] = acc;
         }
         __syncthreads();
-        // dx_{t,r'} -= sum_r c G_{rr'} dy_{t,r}
-        for (int idx = threadIdx.x; idx < RK * nheads * kP; idx += blockDim.x) {
-            const int p = idx % kP, h = (idx / kP) % nheads, rp = idx / (kP * nheads);
-            float acc = 0.0f;
+        // dx_{t,r'} -= sum_r c G_{rr'} dy_{t,r}, four consecutive p per thread
+        for (int idx = threadIdx.x; idx < RK * nheads * (kP / 4); idx += blockDim.x) {
+            const int p4 = idx % (kP / 4), h = (idx / (kP / 4)) % nheads;
+            const int rp = idx / ((kP / 4) * nheads);
+            float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
-            for (int r = 0; r < RK; ++r)
-                acc = fmaf(cG[h * R2 + r * RK + rp],
-                           __bfloat162float(dy[((bt * RK + r) * nheads + h) * kP + p]), acc);
-            dx[((bt * RK + rp) * nheads + h) * kP + p] -= acc;
+            for (int r = 0; r < RK; ++r) {
+                const float cg = cG[h * R2 + r * RK + rp];
+                const uint2 d = *reinterpret_cast<const uint2*>(
+                    dy + ((bt * RK + r) * nheads + h) * kP + 4 * p4);
+                acc.x = fmaf(cg, bf16lo(d.x), acc.x);
+                acc.y = fmaf(cg, bf16hi(d.x), acc.y);
+                acc.z = fmaf(cg, bf16lo(d.y), acc.z);
+                acc.w = fmaf(cg, bf16hi(d.y), acc.w);
+            }
+            float4* o = reinterpret_cast<float4*>(dx + ((bt * RK + rp) * nheads + h) * kP + 4 * p4);
+            float4 v = *o;
+            v.x -= acc.x; v.y -= acc.y; v.z -= acc.z; v.w -= acc.w;
+            *o = v;
         }
         // dB_{t,r'} -= sum_r sX_{r'r} C_{t,r};  dC_{t,r} -= sum_r' sX_{r'r} B_{t,r'}
         for (int idx = threadIdx.x; idx < RK * ngroups * kNs; idx += blockDim.x) {
