@@ -138,3 +138,29 @@ def test_mamba3_bwd_directional_derivatives(name, grad):
     terms = g[grad].double().cpu() * v.double()
     an = float(terms.sum())
     assert abs(fd - an) <= 5e-3 * abs(an) + 1e-3 * float(terms.abs().sum()), (name, fd, an)
+
+
+def test_mamba3_bwd_full_size_properties():
+    """32 x 256 x 32 heads (headdim 64, d_state 128), the bench's Mamba-3 gradient
+    workload, in its launch configuration.  With dy zero after step 64, no final
+    cotangent and no previous token, the loss depends on the first 64 steps only:
+    dx, dB, dC are exactly zero from step 64 on and ddt, dlambda from step 65 on
+    (dt_64 and lambda_64 enter the first 64 steps' algebra only through terms that
+    cancel), and the first 64 steps, dA and the initial state's gradient match the
+    oracle run on those steps alone."""
+    batch, seqlen, nheads, T = 32, 256, 32, 64
+    inp, dy, _ = _case_inputs(batch, seqlen, nheads, 1, 1006, True, False, False)
+    dy[:, T:] = 0
+    g = _gpu(inp, dy, None)
+    for key in ("dx", "dB", "dC"):
+        assert torch.count_nonzero(g[key][:, T:]).item() == 0, key
+    for key in ("ddt", "dlam"):
+        assert torch.count_nonzero(g[key][:, T + 1:]).item() == 0, key
+    head = {k: (v[:, :T].contiguous() if k in ("x", "dt", "lam", "B", "C") else v)
+            for k, v in inp.items()}
+    ref = _ref(head, dy[:, :T].contiguous(), None)
+    for key, rkey, tol in KEYS:
+        if ref[rkey] is None:
+            continue
+        got = g[key][:, :T] if key in ("dx", "ddt", "dlam", "dB", "dC") else g[key]
+        assert_close(got, ref[rkey], tol, key)
