@@ -592,6 +592,21 @@ def _measure_mamba3_bwd(dev, reps):
         binding.ssd_mamba3_bwd(m3["x"], m3["dt"], m3["lam"], m3["A_head"], m3["B"], m3["C"], dy,
                                64, m3["h0"], m3["prev_B"], m3["prev_x"], workspace=ws)
     ms = _time(bwd, reps)
+    # a training step: the forward keeping block states, then the gradient from them
+    f = dict(dtype=torch.float32, device=dev)
+    y = torch.empty(Bn, L, H, P, **f)
+    fs = torch.empty(Bn, H, P, N, **f)
+    bs = torch.empty(binding.ssd_chunked_checkpoint_bytes(Bn, L, H, P, N) // 4, **f)
+
+    def train():
+        binding.ssd_mamba3_fwd(m3["x"], m3["dt"], m3["lam"], m3["A_head"], m3["B"], m3["C"], 64,
+                               out_dtype=torch.float32, y=y, final_state=fs,
+                               initial_state=m3["h0"], prev_B=m3["prev_B"],
+                               prev_x=m3["prev_x"], block_states=bs)
+        binding.ssd_mamba3_bwd(m3["x"], m3["dt"], m3["lam"], m3["A_head"], m3["B"], m3["C"], dy,
+                               64, m3["h0"], m3["prev_B"], m3["prev_x"], workspace=ws,
+                               block_states=bs)
+    ms_train = _time(train, reps)
     Q = 128
     flops = 2 * (3 * Q * Q * N + 2 * Q * Q * P + 4 * Q * P * N) * Bn * H * (L // Q)
     achieved = flops / (ms / 1e3) / 1e12
@@ -599,6 +614,8 @@ def _measure_mamba3_bwd(dev, reps):
                         "32 heads, headdim 64, d_state 128, chunk 64, initial state and "
                         "previous token", "ms": ms,
             "elements_per_s": Bn * L * H * P * N / (ms / 1e3),
+            "train_step_ms": ms_train,
+            "train_step": "forward keeping block states + gradient from them",
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": BF16_PEAK_TFLOPS,
                          "unit": "TFLOP/s", "frac": achieved / BF16_PEAK_TFLOPS,
                          "algorithmic_flops": flops}}
@@ -623,6 +640,20 @@ def _measure_mimo_bwd(dev, reps):
         binding.ssd_mamba3_mimo_bwd(m["x"], m["dt"], m["lam"], m["A_head"], m["B"], m["C"], dy,
                                     16, m["h0"], m["prev_B"], m["prev_x"], workspace=ws)
     ms = _time(bwd, reps)
+    f = dict(dtype=torch.float32, device=dev)
+    y = torch.empty(Bn, L, R, H, P, **f)
+    fs = torch.empty(Bn, H, P, N, **f)
+    bs = torch.empty(binding.ssd_chunked_checkpoint_bytes(Bn, L * R, H, P, N) // 4, **f)
+
+    def train():
+        binding.ssd_mamba3_mimo_fwd(m["x"], m["dt"], m["lam"], m["A_head"], m["B"], m["C"], 16,
+                                    out_dtype=torch.float32, y=y, final_state=fs,
+                                    initial_state=m["h0"], prev_B=m["prev_B"],
+                                    prev_x=m["prev_x"], block_states=bs)
+        binding.ssd_mamba3_mimo_bwd(m["x"], m["dt"], m["lam"], m["A_head"], m["B"], m["C"], dy,
+                                    16, m["h0"], m["prev_B"], m["prev_x"], workspace=ws,
+                                    block_states=bs)
+    ms_train = _time(train, reps)
     Q = 128
     flops = 2 * (3 * Q * Q * N + 2 * Q * Q * P + 4 * Q * P * N) * Bn * H * (L * R // Q)
     achieved = flops / (ms / 1e3) / 1e12
@@ -630,6 +661,8 @@ def _measure_mimo_bwd(dev, reps):
                         "rank 4, 32 heads, headdim 64, d_state 128, chunk 16, initial state "
                         "and previous token", "ms": ms,
             "elements_per_s": Bn * L * R * H * P * N / (ms / 1e3),
+            "train_step_ms": ms_train,
+            "train_step": "forward keeping block states + gradient from them",
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": BF16_PEAK_TFLOPS,
                          "unit": "TFLOP/s", "frac": achieved / BF16_PEAK_TFLOPS,
                          "algorithmic_flops": flops}}

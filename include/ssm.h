@@ -416,6 +416,35 @@ ssm_status_t ssd_chunked_fwd_ckpt(const void* x, const float* dt, const float* A
                                   ssm_dtype_t out_dtype, void* stream);
 
 /*
+ * ssd_mamba3_fwd and ssd_mamba3_mimo_fwd that also keep the states their
+ * chunked form carries between 128-row blocks (device, at least
+ * ssd_chunked_checkpoint_bytes(batch, seqlen * rank, nheads, headdim, dstate)
+ * bytes, not overlapping anything else) for ssd_mamba3_bwd /
+ * ssd_mamba3_mimo_bwd, so that a training step runs the forward once.  These
+ * are the states of S + c_t BX_t (c_t = dt_{t+1} (1 - lambda_{t+1})), the form
+ * the gradients walk.  y and final_state are exactly the plain forwards' (y may
+ * be NULL: states only); the same arguments and errors, plus SSM_ERR_NULL for a
+ * NULL `block_states` when there is work.  The pages have no counterpart: these
+ * keep what an autograd training step would save between the forward and the
+ * backward pass.
+ */
+ssm_status_t ssd_mamba3_fwd_ckpt(const void* x, const float* dt, const float* lam,
+                                 const float* A_head, const void* B, const void* C, int chunk,
+                                 const float* initial_state, const void* prev_B,
+                                 const void* prev_x, void* y, float* final_state,
+                                 float* block_states, int batch, int seqlen, int nheads,
+                                 int headdim, int dstate, int ngroups, ssm_dtype_t in_dtype,
+                                 ssm_dtype_t out_dtype, void* stream);
+ssm_status_t ssd_mamba3_mimo_fwd_ckpt(const void* x, const float* dt, const float* lam,
+                                      const float* A_head, const void* B, const void* C,
+                                      int chunk, int rank, const float* initial_state,
+                                      const void* prev_B, const void* prev_x, void* y,
+                                      float* final_state, float* block_states, int batch,
+                                      int seqlen, int nheads, int headdim, int dstate,
+                                      int ngroups, ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
+                                      void* stream);
+
+/*
  * Bytes of device workspace ssd_chunked_bwd needs (a pure function of its
  * arguments; 0 if they are invalid or unsupported).  About batch * nheads *
  * (ceil(seqlen / 128) + 1) * 32 KiB of block states plus 2 * nheads * batch *
@@ -492,7 +521,9 @@ size_t ssd_mamba3_bwd_workspace_bytes(int batch, int seqlen, int nheads, int hea
  *            given, not written otherwise.
  * Inputs as for ssd_mamba3_fwd (x, B, C, prev_B, prev_x bf16; dt, lam, A_head,
  * initial_state fp32), plus dy (batch, seqlen, nheads, headdim) bf16 and
- * dfinal_state (batch, nheads, headdim, dstate) fp32 or NULL (zero).
+ * dfinal_state (batch, nheads, headdim, dstate) fp32 or NULL (zero), and
+ * block_states: what ssd_mamba3_fwd_ckpt kept for the same inputs, or NULL (the
+ * call then runs the Mamba-3 forward once more to make them).
  * How: the three-term recurrence is the Mamba-2 SSD recurrence of S + c_t u_t
  * (c_t = dt_{t+1} (1 - lambda_{t+1})) with input weights `scale` and y less
  * c_t (C_t . B_t) x_t, so the call runs the Mamba-3 forward once more for the
@@ -512,7 +543,8 @@ size_t ssd_mamba3_bwd_workspace_bytes(int batch, int seqlen, int nheads, int hea
 ssm_status_t ssd_mamba3_bwd(const void* x, const float* dt, const float* lam, const float* A_head,
                             const void* B, const void* C, int chunk, const float* initial_state,
                             const void* prev_B, const void* prev_x, const void* dy,
-                            const float* dfinal_state, float* dx, float* ddt, float* dlam,
+                            const float* dfinal_state, const float* block_states, float* dx,
+                            float* ddt, float* dlam,
                             float* dA_head, float* dB, float* dC, float* dinitial_state,
                             float* dprev_B, float* dprev_x, int batch, int seqlen, int nheads,
                             int headdim, int dstate, int ngroups, ssm_dtype_t in_dtype,
@@ -542,8 +574,10 @@ size_t ssd_mamba3_mimo_bwd_workspace_bytes(int batch, int seqlen, int rank, int 
  *   dprev_B  (batch, rank, ngroups, dstate), dprev_x (batch, rank, nheads, headdim)
  *            fp32, required when prev_B / prev_x are given.
  * Inputs as for ssd_mamba3_mimo_fwd (bf16 x, B, C, prev_B, prev_x), plus dy
- * like x (bf16) and dfinal_state fp32 or NULL.  The call runs the MIMO forward
- * once more for the states entering each 128-row block of sub-tokens, the SSD
+ * like x (bf16), dfinal_state fp32 or NULL, and block_states: what
+ * ssd_mamba3_mimo_fwd_ckpt kept for the same inputs, or NULL.  The call runs the
+ * MIMO forward once more (unless given block_states) for the states entering
+ * each 128-row block of sub-tokens, the SSD
  * gradient over the sub-tokens (block-lower-triangular mask, the step's decay
  * on its first sub-token, its scale weight on every one), then elementwise
  * kernels for lambda, the block-diagonal correction and the previous token.
@@ -555,7 +589,8 @@ ssm_status_t ssd_mamba3_mimo_bwd(const void* x, const float* dt, const float* la
                                  const float* A_head, const void* B, const void* C, int chunk,
                                  int rank, const float* initial_state, const void* prev_B,
                                  const void* prev_x, const void* dy, const float* dfinal_state,
-                                 float* dx, float* ddt, float* dlam, float* dA_head, float* dB,
+                                 const float* block_states, float* dx, float* ddt, float* dlam,
+                                 float* dA_head, float* dB,
                                  float* dC, float* dinitial_state, float* dprev_B,
                                  float* dprev_x, int batch, int seqlen, int nheads, int headdim,
                                  int dstate, int ngroups, ssm_dtype_t in_dtype, void* workspace,

@@ -33,7 +33,8 @@ EXPORTS = ["ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_bytes", "
            "ssd_chunked_bwd_workspace_bytes", "ssd_chunked_bwd", "ssm_scan_fwd_host_workspace_bytes",
            "ssm_scan_fwd_host", "ssm_scan_checkpoint_bytes", "ssm_scan_fwd_ckpt",
            "ssd_chunked_checkpoint_bytes", "ssd_chunked_fwd_ckpt", "ssd_mamba3_bwd_workspace_bytes",
-           "ssd_mamba3_bwd", "ssd_mamba3_mimo_bwd_workspace_bytes", "ssd_mamba3_mimo_bwd"]
+           "ssd_mamba3_bwd", "ssd_mamba3_mimo_bwd_workspace_bytes", "ssd_mamba3_mimo_bwd",
+           "ssd_mamba3_fwd_ckpt", "ssd_mamba3_mimo_fwd_ckpt"]
 
 
 class SSMError(RuntimeError):
@@ -91,11 +92,15 @@ def lib() -> ctypes.CDLL:
         L.ssd_mamba3_bwd_workspace_bytes.restype = sz
         L.ssd_mamba3_bwd_workspace_bytes.argtypes = [i] * 6
         L.ssd_mamba3_bwd.restype = i
-        L.ssd_mamba3_bwd.argtypes = [vp] * 6 + [i] + [vp] * 14 + [i] * 7 + [vp, sz, vp]
+        L.ssd_mamba3_bwd.argtypes = [vp] * 6 + [i] + [vp] * 15 + [i] * 7 + [vp, sz, vp]
+        L.ssd_mamba3_fwd_ckpt.restype = i
+        L.ssd_mamba3_fwd_ckpt.argtypes = [vp] * 6 + [i] + [vp] * 6 + [i] * 7 + [vp]
+        L.ssd_mamba3_mimo_fwd_ckpt.restype = i
+        L.ssd_mamba3_mimo_fwd_ckpt.argtypes = [vp] * 6 + [i, i] + [vp] * 6 + [i] * 7 + [vp]
         L.ssd_mamba3_mimo_bwd_workspace_bytes.restype = sz
         L.ssd_mamba3_mimo_bwd_workspace_bytes.argtypes = [i] * 7
         L.ssd_mamba3_mimo_bwd.restype = i
-        L.ssd_mamba3_mimo_bwd.argtypes = [vp] * 6 + [i, i] + [vp] * 14 + [i] * 7 + [vp, sz, vp]
+        L.ssd_mamba3_mimo_bwd.argtypes = [vp] * 6 + [i, i] + [vp] * 15 + [i] * 7 + [vp, sz, vp]
         L.ssd_chunked_checkpoint_bytes.restype = sz
         L.ssd_chunked_checkpoint_bytes.argtypes = [i] * 5
         L.ssd_chunked_fwd_ckpt.restype = i
@@ -446,7 +451,7 @@ def ssd_mamba3_bwd_workspace_bytes(batch, seqlen, nheads, headdim=64, dstate=128
 
 def ssd_mamba3_bwd(x, dt, lam, A_head, B, C, dy, chunk=64, initial_state=None, prev_B=None,
                    prev_x=None, dfinal_state=None, workspace=None, want_dinitial_state=True,
-                   stream=None):
+                   stream=None, block_states=None):
     """Gradient of ``ssd_mamba3_fwd`` for the loss sum(dy * y) + sum(dfinal_state *
     final_state).  Inputs as for ``ssd_mamba3_fwd`` (bf16 x, B, C, prev_B, prev_x);
     dy like x (bf16).  Returns a dict of fp32 tensors: dx, ddt, dlam, dA_head, dB, dC,
@@ -484,7 +489,9 @@ def ssd_mamba3_bwd(x, dt, lam, A_head, B, C, dy, chunk=64, initial_state=None, p
     _req(workspace, "workspace", torch.uint8)
     st = lib().ssd_mamba3_bwd(_ptr(x), _ptr(dt), _ptr(lam), _ptr(A_head), _ptr(B), _ptr(C),
                               int(chunk), _ptr(initial_state), _ptr(prev_B), _ptr(prev_x),
-                              _ptr(dy), _ptr(dfinal_state), _ptr(g["dx"]), _ptr(g["ddt"]),
+                              _ptr(dy), _ptr(dfinal_state),
+                              _ptr(_opt(block_states, "block_states", torch.float32)),
+                              _ptr(g["dx"]), _ptr(g["ddt"]),
                               _ptr(g["dlam"]), _ptr(g["dA_head"]), _ptr(g["dB"]), _ptr(g["dC"]),
                               _ptr(g["dinitial_state"]), _ptr(g["dprev_B"]), _ptr(g["dprev_x"]),
                               batch, seqlen, nheads, headdim, dstate, ngroups,
@@ -502,7 +509,7 @@ def ssd_mamba3_mimo_bwd_workspace_bytes(batch, seqlen, rank, nheads, headdim=64,
 
 def ssd_mamba3_mimo_bwd(x, dt, lam, A_head, B, C, dy, chunk=None, initial_state=None,
                         prev_B=None, prev_x=None, dfinal_state=None, workspace=None,
-                        want_dinitial_state=True, stream=None):
+                        want_dinitial_state=True, stream=None, block_states=None):
     """Gradient of ``ssd_mamba3_mimo_fwd``.  x, dy: (batch, seqlen, rank, nheads,
     headdim) bf16; B, C: (batch, seqlen, rank, ngroups, dstate) bf16; prev_B (batch,
     rank, ngroups, dstate), prev_x (batch, rank, nheads, headdim) bf16 or None.
@@ -543,7 +550,9 @@ def ssd_mamba3_mimo_bwd(x, dt, lam, A_head, B, C, dy, chunk=None, initial_state=
     _req(workspace, "workspace", torch.uint8)
     st = lib().ssd_mamba3_mimo_bwd(_ptr(x), _ptr(dt), _ptr(lam), _ptr(A_head), _ptr(B), _ptr(C),
                                    int(chunk), int(rank), _ptr(initial_state), _ptr(prev_B),
-                                   _ptr(prev_x), _ptr(dy), _ptr(dfinal_state), _ptr(g["dx"]),
+                                   _ptr(prev_x), _ptr(dy), _ptr(dfinal_state),
+                                   _ptr(_opt(block_states, "block_states", torch.float32)),
+                                   _ptr(g["dx"]),
                                    _ptr(g["ddt"]), _ptr(g["dlam"]), _ptr(g["dA_head"]),
                                    _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dinitial_state"]),
                                    _ptr(g["dprev_B"]), _ptr(g["dprev_x"]), batch, seqlen, nheads,
@@ -634,11 +643,13 @@ def ssm_last_device_status(workspace, stream=None) -> int:
 
 def ssd_mamba3_fwd(x, dt, lam, A_head, B, C, chunk=64, out_dtype=None, y=None, final_state=None,
                    return_final_state=True, initial_state=None, prev_B=None, prev_x=None,
-                   stream=None):
+                   stream=None, block_states=None):
     """Mamba-3 SISO chunked prefill.  As ``ssd_chunked_fwd`` plus lam: (batch, seqlen,
     nheads) fp32 (lambda after sigmoid) and the token before the first, prev_B:
     (batch, ngroups, dstate) and prev_x: (batch, nheads, headdim) in x's dtype (both or
-    neither).  B and C are taken already rotated.  Returns (y, final_state)."""
+    neither).  B and C are taken already rotated.  ``block_states`` (fp32, at least
+    ``ssd_chunked_checkpoint_bytes(batch, seqlen, nheads)`` bytes) also keeps the
+    states ``ssd_mamba3_bwd`` starts from.  Returns (y, final_state)."""
     _req(x, "x", ndim=4)
     in_dt = x.dtype
     if in_dt not in _DT:
@@ -661,6 +672,18 @@ def ssd_mamba3_fwd(x, dt, lam, A_head, B, C, chunk=64, out_dtype=None, y=None, f
     _opt(initial_state, "initial_state", torch.float32)
     _opt(prev_B, "prev_B", in_dt)
     _opt(prev_x, "prev_x", in_dt)
+    if block_states is not None:
+        _req(block_states, "block_states", torch.float32)
+        if block_states.numel() * 4 < ssd_chunked_checkpoint_bytes(batch, seqlen, nheads, headdim,
+                                                                   dstate):
+            raise ValueError("block_states is smaller than ssd_chunked_checkpoint_bytes(...)")
+        st = lib().ssd_mamba3_fwd_ckpt(_ptr(x), _ptr(dt), _ptr(lam), _ptr(A_head), _ptr(B),
+                                       _ptr(C), int(chunk), _ptr(initial_state), _ptr(prev_B),
+                                       _ptr(prev_x), _ptr(y), _ptr(final_state),
+                                       _ptr(block_states), batch, seqlen, nheads, headdim,
+                                       dstate, ngroups, _DT[in_dt], _DT[out_dt], _stream(stream))
+        _check(st, "ssd_mamba3_fwd_ckpt")
+        return y, final_state
     st = lib().ssd_mamba3_fwd(_ptr(x), _ptr(dt), _ptr(lam), _ptr(A_head), _ptr(B), _ptr(C),
                               int(chunk), _ptr(initial_state), _ptr(prev_B), _ptr(prev_x),
                               _ptr(y), _ptr(final_state), batch, seqlen, nheads, headdim, dstate,
@@ -704,11 +727,13 @@ def ssm_decode_step_mamba3(state, prev_B, prev_x, x, dt, lam, A, B, C, D=None, z
 
 def ssd_mamba3_mimo_fwd(x, dt, lam, A_head, B, C, chunk=16, out_dtype=None, y=None,
                         final_state=None, return_final_state=True, initial_state=None,
-                        prev_B=None, prev_x=None, stream=None):
+                        prev_B=None, prev_x=None, stream=None, block_states=None):
     """Mamba-3 MIMO (rank R) chunked prefill.  x: (batch, seqlen, R, nheads, headdim);
     B, C: (batch, seqlen, R, ngroups, dstate); dt, lam: (batch, seqlen, nheads) fp32;
     prev_B: (batch, R, ngroups, dstate), prev_x: (batch, R, nheads, headdim) (both or
-    neither).  Returns (y (batch, seqlen, R, nheads, headdim), final_state)."""
+    neither).  ``block_states`` (fp32, at least ``ssd_chunked_checkpoint_bytes(batch,
+    seqlen * R, nheads)`` bytes) also keeps the states ``ssd_mamba3_mimo_bwd`` starts
+    from.  Returns (y (batch, seqlen, R, nheads, headdim), final_state)."""
     _req(x, "x", ndim=5)
     in_dt = x.dtype
     if in_dt not in _DT:
@@ -731,6 +756,19 @@ def ssd_mamba3_mimo_fwd(x, dt, lam, A_head, B, C, chunk=16, out_dtype=None, y=No
     _opt(initial_state, "initial_state", torch.float32)
     _opt(prev_B, "prev_B", in_dt)
     _opt(prev_x, "prev_x", in_dt)
+    if block_states is not None:
+        _req(block_states, "block_states", torch.float32)
+        if block_states.numel() * 4 < ssd_chunked_checkpoint_bytes(batch, seqlen * rank, nheads,
+                                                                   headdim, dstate):
+            raise ValueError("block_states is smaller than ssd_chunked_checkpoint_bytes(...)")
+        st = lib().ssd_mamba3_mimo_fwd_ckpt(_ptr(x), _ptr(dt), _ptr(lam), _ptr(A_head), _ptr(B),
+                                            _ptr(C), int(chunk), int(rank), _ptr(initial_state),
+                                            _ptr(prev_B), _ptr(prev_x), _ptr(y), _ptr(final_state),
+                                            _ptr(block_states), batch, seqlen, nheads, headdim,
+                                            dstate, ngroups, _DT[in_dt], _DT[out_dt],
+                                            _stream(stream))
+        _check(st, "ssd_mamba3_mimo_fwd_ckpt")
+        return y, final_state
     st = lib().ssd_mamba3_mimo_fwd(_ptr(x), _ptr(dt), _ptr(lam), _ptr(A_head), _ptr(B), _ptr(C),
                                    int(chunk), int(rank), _ptr(initial_state), _ptr(prev_B),
                                    _ptr(prev_x), _ptr(y), _ptr(final_state), batch, seqlen,

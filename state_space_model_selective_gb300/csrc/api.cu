@@ -41,7 +41,7 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, ssm_dtype_t dtype, uint64_
 
 }  // namespace ssm_host
 
-extern "C" int ssm_abi_version(void) { return 3; }
+extern "C" int ssm_abi_version(void) { return 4; }
 
 extern "C" const char* ssm_status_string(ssm_status_t s) {
     switch (s) {

@@ -653,9 +653,9 @@ ssm_status_t ssd_entry(const void* x, const float* dt, const float* lam, const f
     if (overlaps(y, yb, final_state, fb)) return SSM_ERR_ALIAS;
     if (initial_state && overlaps(y, yb, initial_state, sb)) return SSM_ERR_ALIAS;
     if (bstates) {
-        if (m3 || rank != 1) return SSM_ERR_UNSUPPORTED;
         if (!aligned16(bstates)) return SSM_ERR_ALIGN;
-        const size_t bsb = (size_t)batch * nheads * (((size_t)seqlen + kQ - 1) / kQ + 1) * kP * kNs * 4;
+        const size_t bsb =
+            (size_t)batch * nheads * (((size_t)seqlen * rank + kQ - 1) / kQ + 1) * kP * kNs * 4;
         for (const R& r : ins)
             if (overlaps(bstates, bsb, r.p, r.n)) return SSM_ERR_ALIAS;
         if (overlaps(bstates, bsb, y, yb) || overlaps(bstates, bsb, final_state, fb) ||
@@ -683,10 +683,19 @@ ssm_status_t ssd_entry(const void* x, const float* dt, const float* lam, const f
     a.nheads = nheads;
     a.ngroups = ngroups;
     const bool bf = out_dtype == SSM_BF16;
-    if (bstates) {  // Mamba-2 only (the backward pass is)
+    if (bstates) {  // the states the gradients start from, kept by the forward
         a.bstates = bstates;
-        return bf ? launch<__nv_bfloat16, false, 1, true>(mc, mb, mx, a, s)
-                  : launch<float, false, 1, true>(mc, mb, mx, a, s);
+        if (!m3)
+            return bf ? launch<__nv_bfloat16, false, 1, true>(mc, mb, mx, a, s)
+                      : launch<float, false, 1, true>(mc, mb, mx, a, s);
+        switch (rank) {
+            case 1: return bf ? launch<__nv_bfloat16, true, 1, true>(mc, mb, mx, a, s)
+                              : launch<float, true, 1, true>(mc, mb, mx, a, s);
+            case 2: return bf ? launch<__nv_bfloat16, true, 2, true>(mc, mb, mx, a, s)
+                              : launch<float, true, 2, true>(mc, mb, mx, a, s);
+            default: return bf ? launch<__nv_bfloat16, true, 4, true>(mc, mb, mx, a, s)
+                               : launch<float, true, 4, true>(mc, mb, mx, a, s);
+        }
     }
     if (!m3) return bf ? launch<__nv_bfloat16, false, 1>(mc, mb, mx, a, s)
                        : launch<float, false, 1>(mc, mb, mx, a, s);
@@ -799,6 +808,32 @@ extern "C" ssm_status_t ssd_chunked_fwd_ckpt(const void* x, const float* dt, con
     return ssd_entry(x, dt, nullptr, A_head, B, C, chunk, 1, initial_state, nullptr, nullptr, y,
                      final_state, block_states, batch, seqlen, nheads, headdim, dstate, ngroups,
                      in_dtype, out_dtype, false, stream);
+}
+
+extern "C" ssm_status_t ssd_mamba3_fwd_ckpt(const void* x, const float* dt, const float* lam,
+                                            const float* A_head, const void* B, const void* C,
+                                            int chunk, const float* initial_state,
+                                            const void* prev_B, const void* prev_x, void* y,
+                                            float* final_state, float* block_states, int batch,
+                                            int seqlen, int nheads, int headdim, int dstate,
+                                            int ngroups, ssm_dtype_t in_dtype,
+                                            ssm_dtype_t out_dtype, void* stream) {
+    if (!block_states && batch > 0 && nheads > 0 && seqlen > 0) return SSM_ERR_NULL;
+    return ssd_entry(x, dt, lam, A_head, B, C, chunk, 1, initial_state, prev_B, prev_x, y,
+                     final_state, block_states, batch, seqlen, nheads, headdim, dstate, ngroups,
+                     in_dtype, out_dtype, true, stream);
+}
+
+extern "C" ssm_status_t ssd_mamba3_mimo_fwd_ckpt(
+    const void* x, const float* dt, const float* lam, const float* A_head, const void* B,
+    const void* C, int chunk, int rank, const float* initial_state, const void* prev_B,
+    const void* prev_x, void* y, float* final_state, float* block_states, int batch, int seqlen,
+    int nheads, int headdim, int dstate, int ngroups, ssm_dtype_t in_dtype,
+    ssm_dtype_t out_dtype, void* stream) {
+    if (!block_states && batch > 0 && nheads > 0 && seqlen > 0) return SSM_ERR_NULL;
+    return ssd_entry(x, dt, lam, A_head, B, C, chunk, rank, initial_state, prev_B, prev_x, y,
+                     final_state, block_states, batch, seqlen, nheads, headdim, dstate, ngroups,
+                     in_dtype, out_dtype, true, stream);
 }
 
 extern "C" ssm_status_t ssd_mamba3_fwd(const void* x, const float* dt, const float* lam,

@@ -1142,7 +1142,8 @@ extern "C" ssm_status_t ssd_mamba3_bwd(const void* x, const float* dt, const flo
                                        const float* A_head, const void* B, const void* C,
                                        int chunk, const float* initial_state, const void* prev_B,
                                        const void* prev_x, const void* dy,
-                                       const float* dfinal_state, float* dx, float* ddt,
+                                       const float* dfinal_state, const float* block_states,
+                                       float* dx, float* ddt,
                                        float* dlam, float* dA_head, float* dB, float* dC,
                                        float* dinitial_state, float* dprev_B, float* dprev_x,
                                        int batch, int seqlen, int nheads, int headdim,
@@ -1170,18 +1171,19 @@ extern "C" ssm_status_t ssd_mamba3_bwd(const void* x, const float* dt, const flo
         return SSM_ERR_NULL;
     if (work && !workspace) return SSM_ERR_WORKSPACE;
     const void* ptrs[] = {x, dt, lam, A_head, B, C, initial_state, prev_B, prev_x, dy,
-                          dfinal_state, dx, ddt, dlam, dA_head, dB, dC, dinitial_state, dprev_B,
-                          dprev_x, workspace};
+                          dfinal_state, block_states, dx, ddt, dlam, dA_head, dB, dC,
+                          dinitial_state, dprev_B, dprev_x, workspace};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return SSM_ERR_ALIGN;
     const size_t xb = steps * nheads * headdim * 2, bcb = steps * ngroups * dstate * 2;
     const size_t pbb = (size_t)batch * ngroups * dstate, pxb = items * headdim;
+    const size_t bsb = block_states ? sb * (((size_t)seqlen + kQ - 1) / kQ + 1) : 0;
     struct R { const void* p; size_t n; };
     const R ins[] = {{x, xb}, {dt, steps * nheads * 4}, {lam, steps * nheads * 4},
                      {A_head, (size_t)nheads * 4}, {B, bcb}, {C, bcb},
                      {initial_state, initial_state ? sb : 0}, {prev_B, has_prev ? pbb * 2 : 0},
                      {prev_x, has_prev ? pxb * 2 : 0}, {dy, xb},
-                     {dfinal_state, dfinal_state ? sb : 0}};
+                     {dfinal_state, dfinal_state ? sb : 0}, {block_states, bsb}};
     const R outs[] = {{dx, steps * nheads * headdim * 4}, {ddt, steps * nheads * 4},
                       {dlam, steps * nheads * 4}, {dA_head, (size_t)nheads * 4},
                       {dB, bcb * 2}, {dC, bcb * 2}, {dinitial_state, dinitial_state ? sb : 0},
@@ -1239,9 +1241,9 @@ extern "C" ssm_status_t ssd_mamba3_bwd(const void* x, const float* dt, const flo
                                                              initial_state, prev_B, prev_x, bs,
                                                              batch, seqlen, nheads, ngroups, s);
     };
-    ssm_status_t rc = run_bwd(x, dt, w, A_head, B, C, initial_state, dy, dfinal_state, nullptr,
-                              states, dx, ddt, dw, dA_head, dB, dC, dS_out, batch, seqlen, nheads,
-                              ngroups, workspace, s);
+    ssm_status_t rc = run_bwd(x, dt, w, A_head, B, C, initial_state, dy, dfinal_state,
+                              block_states, states, dx, ddt, dw, dA_head, dB, dC, dS_out, batch,
+                              seqlen, nheads, ngroups, workspace, s);
     if (rc != SSM_OK) return rc;
     // 3. x . dy per head and C . B per group, every step
     const long long nrows = (long long)steps * (nheads + ngroups);
@@ -1629,8 +1631,9 @@ extern "C" size_t ssd_mamba3_mimo_bwd_workspace_bytes(int batch, int seqlen, int
 extern "C" ssm_status_t ssd_mamba3_mimo_bwd(
     const void* x, const float* dt, const float* lam, const float* A_head, const void* B,
     const void* C, int chunk, int rank, const float* initial_state, const void* prev_B,
-    const void* prev_x, const void* dy, const float* dfinal_state, float* dx, float* ddt,
-    float* dlam, float* dA_head, float* dB, float* dC, float* dinitial_state, float* dprev_B,
+    const void* prev_x, const void* dy, const float* dfinal_state, const float* block_states,
+    float* dx, float* ddt, float* dlam, float* dA_head, float* dB, float* dC,
+    float* dinitial_state, float* dprev_B,
     float* dprev_x, int batch, int seqlen, int nheads, int headdim, int dstate, int ngroups,
     ssm_dtype_t in_dtype, void* workspace, size_t workspace_bytes, void* stream) {
     using namespace ssm_host;
@@ -1658,11 +1661,12 @@ extern "C" ssm_status_t ssd_mamba3_mimo_bwd(
         return SSM_ERR_NULL;
     if (work && !workspace) return SSM_ERR_WORKSPACE;
     const void* ptrs[] = {x, dt, lam, A_head, B, C, initial_state, prev_B, prev_x, dy,
-                          dfinal_state, dx, ddt, dlam, dA_head, dB, dC, dinitial_state, dprev_B,
-                          dprev_x, workspace};
+                          dfinal_state, block_states, dx, ddt, dlam, dA_head, dB, dC,
+                          dinitial_state, dprev_B, dprev_x, workspace};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return SSM_ERR_ALIGN;
     const size_t xb = subs * nheads * headdim * 2, bcb = subs * ngroups * dstate * 2;
+    const size_t bsb = block_states ? sb * (((size_t)seqlen * rank + kQ - 1) / kQ + 1) : 0;
     const size_t pbb = (size_t)batch * rank * ngroups * dstate,
                  pxb = (size_t)batch * rank * nheads * headdim;
     struct R { const void* p; size_t n; };
@@ -1670,7 +1674,7 @@ extern "C" ssm_status_t ssd_mamba3_mimo_bwd(
                      {A_head, (size_t)nheads * 4}, {B, bcb}, {C, bcb},
                      {initial_state, initial_state ? sb : 0}, {prev_B, has_prev ? pbb * 2 : 0},
                      {prev_x, has_prev ? pxb * 2 : 0}, {dy, xb},
-                     {dfinal_state, dfinal_state ? sb : 0}};
+                     {dfinal_state, dfinal_state ? sb : 0}, {block_states, bsb}};
     const R outs[] = {{dx, subs * nheads * headdim * 4}, {ddt, steps * nheads * 4},
                       {dlam, steps * nheads * 4}, {dA_head, (size_t)nheads * 4},
                       {dB, bcb * 2}, {dC, bcb * 2}, {dinitial_state, dinitial_state ? sb : 0},
@@ -1731,8 +1735,8 @@ extern "C" ssm_status_t ssd_mamba3_mimo_bwd(
                                                              batch, seqlen, nheads, ngroups, s,
                                                              rank);
     };
-    ssm_status_t rc = run_bwd(x, dts, wts, A_head, B, C, initial_state, dy, dfinal_state, nullptr,
-                              states, dx, ddec, dw, dA_head, dB, dC, dS_out, batch,
+    ssm_status_t rc = run_bwd(x, dts, wts, A_head, B, C, initial_state, dy, dfinal_state,
+                              block_states, states, dx, ddec, dw, dA_head, dB, dC, dS_out, batch,
                               seqlen * rank, nheads, ngroups, workspace, s, rank);
     if (rc != SSM_OK) return rc;
     // 3.-5. the dots, the previous token and the per-step terms

@@ -39,7 +39,7 @@ def test_header_symbols_exported(L):
 
 
 def test_version_and_status_strings(L):
-    assert binding.ssm_abi_version() == 3
+    assert binding.ssm_abi_version() == 4
     for code in range(10):
         s = binding.status_string(code)
         assert isinstance(s, str) and s
@@ -348,7 +348,8 @@ def m3_bwd_call(L, **kw):
     args.update(kw)
     a = args
     return L.ssd_mamba3_bwd(a["x"], a["dt"], a["lam"], a["A"], a["B"], a["C"], a["chunk"],
-                            a["h0"], a["pB"], a["px"], a["dy"], a["dfs"], a["dx"], a["ddt"],
+                            a["h0"], a["pB"], a["px"], a["dy"], a["dfs"], a.get("bs"), a["dx"],
+                            a["ddt"],
                             a["dlam"], a["dA"], a["dB"], a["dC"], a["dh0"], a["dpB"], a["dpx"],
                             a["batch"], a["seqlen"], a["nheads"], a["headdim"], a["dstate"],
                             a["ngroups"], a["in_dt"], a["ws"], a["wsb"], a["stream"])
@@ -372,6 +373,8 @@ def test_mamba3_bwd_argument_errors(L):
     assert m3_bwd_call(L, dlam=P(12)) == ALIAS             # dlam on top of lam
     assert m3_bwd_call(L, dlam=P(7)) == ALIAS              # dlam and ddt on one buffer
     assert m3_bwd_call(L, pB=P(14), px=P(15), dpB=P(16), dpx=P(16)) == ALIAS
+    assert m3_bwd_call(L, bs=P(6)) == ALIAS                # block states under dx
+    assert m3_bwd_call(L, bs=ctypes.c_void_p(0x70000008)) == ALIGN
     assert m3_bwd_call(L, nheads=0, dA=None, x=None) == OK
 
 
@@ -391,7 +394,8 @@ def mimo_bwd_call(L, **kw):
     args.update(kw)
     a = args
     return L.ssd_mamba3_mimo_bwd(a["x"], a["dt"], a["lam"], a["A"], a["B"], a["C"], a["chunk"],
-                                 a["rank"], a["h0"], a["pB"], a["px"], a["dy"], a["dfs"], a["dx"],
+                                 a["rank"], a["h0"], a["pB"], a["px"], a["dy"], a["dfs"],
+                                 a.get("bs"), a["dx"],
                                  a["ddt"], a["dlam"], a["dA"], a["dB"], a["dC"], a["dh0"],
                                  a["dpB"], a["dpx"], a["batch"], a["seqlen"], a["nheads"],
                                  a["headdim"], a["dstate"], a["ngroups"], a["in_dt"], a["ws"],

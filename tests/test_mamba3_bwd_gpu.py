@@ -164,3 +164,28 @@ def test_mamba3_bwd_full_size_properties():
             continue
         got = g[key][:, :T] if key in ("dx", "ddt", "dlam", "dB", "dC") else g[key]
         assert_close(got, ref[rkey], tol, key)
+
+
+def test_mamba3_block_states_from_the_forward():
+    """ssd_mamba3_fwd keeping block states gives the plain forward's y and final state
+    bit for bit, and ssd_mamba3_bwd from those states gives the same bits as
+    ssd_mamba3_bwd recomputing them."""
+    batch, seqlen, nheads = 2, 320, 4
+    inp, dy, dfinal = _case_inputs(batch, seqlen, nheads, 2, 450, True, True, True)
+    d = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+    args = (d["x"], d["dt"], d["lam"], d["A_head"], d["B"], d["C"], 64)
+    kw = dict(initial_state=d["h0"], prev_B=d["prev_B"], prev_x=d["prev_x"])
+    y0, f0 = binding.ssd_mamba3_fwd(*args, out_dtype=torch.float32, **kw)
+    bs = torch.full((binding.ssd_chunked_checkpoint_bytes(batch, seqlen, nheads) // 4,),
+                    float("nan"), device="cuda")
+    y1, f1 = binding.ssd_mamba3_fwd(*args, out_dtype=torch.float32, block_states=bs, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1) and torch.equal(f0, f1)
+    assert not torch.isnan(bs).any()
+    g0 = binding.ssd_mamba3_bwd(*args[:6], dy.cuda(), 64, d["h0"], d["prev_B"], d["prev_x"],
+                                dfinal.cuda())
+    g1 = binding.ssd_mamba3_bwd(*args[:6], dy.cuda(), 64, d["h0"], d["prev_B"], d["prev_x"],
+                                dfinal.cuda(), block_states=bs)
+    torch.cuda.synchronize()
+    for k, v in g0.items():
+        assert torch.equal(v, g1[k]), k

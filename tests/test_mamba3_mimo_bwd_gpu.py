@@ -143,3 +143,30 @@ def test_mimo_bwd_directional_derivatives(name, grad):
     terms = g[grad].double().cpu() * v.double()
     an = float(terms.sum())
     assert abs(fd - an) <= 5e-3 * abs(an) + 1e-3 * float(terms.abs().sum()), (name, fd, an)
+
+
+def test_mimo_block_states_from_the_forward():
+    """ssd_mamba3_mimo_fwd keeping block states gives the plain forward's y and final
+    state bit for bit, and ssd_mamba3_mimo_bwd from those states gives the same bits as
+    ssd_mamba3_mimo_bwd recomputing them."""
+    batch, seqlen, rank, nheads = 2, 80, 4, 4
+    inp, dy, dfinal = _case(batch, seqlen, rank, nheads, 2, 690, True, True, True)
+    d = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+    args = (d["x"], d["dt"], d["lam"], d["A_head"], d["B"], d["C"])
+    kw = dict(initial_state=d["h0"], prev_B=d["prev_B"], prev_x=d["prev_x"])
+    y0, f0 = binding.ssd_mamba3_mimo_fwd(*args, 16, out_dtype=torch.float32, **kw)
+    bs = torch.full((binding.ssd_chunked_checkpoint_bytes(batch, seqlen * rank, nheads) // 4,),
+                    float("nan"), device="cuda")
+    y1, f1 = binding.ssd_mamba3_mimo_fwd(*args, 16, out_dtype=torch.float32, block_states=bs,
+                                         **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1) and torch.equal(f0, f1)
+    assert not torch.isnan(bs).any()
+    g0 = binding.ssd_mamba3_mimo_bwd(*args, dy.cuda(), 16, d["h0"], d["prev_B"], d["prev_x"],
+                                     dfinal.cuda())
+    g1 = binding.ssd_mamba3_mimo_bwd(*args, dy.cuda(), 16, d["h0"], d["prev_B"], d["prev_x"],
+                                     dfinal.cuda(), block_states=bs)
+    torch.cuda.synchronize()
+    for k, v in g0.items():
+        if v is not None:
+            assert torch.equal(v, g1[k]), k
