@@ -536,9 +536,9 @@ size_t ssd_mamba3_bwd_workspace_bytes(int batch, int seqlen, int nheads, int hea
  * Every output must be disjoint from every input, from the other outputs and
  * from the workspace (SSM_ERR_ALIAS).  prev_B and prev_x must be both NULL or
  * both given (else SSM_ERR_NULL).
- * Supported: as ssd_chunked_bwd.  With no step (seqlen == 0 or batch == 0)
- * dA_head is zeroed, dinitial_state = dfinal_state (or 0) and dprev_B, dprev_x
- * are zeroed.
+ * Supported: as ssd_chunked_bwd, with nheads <= 6144.  With no step (seqlen == 0
+ * or batch == 0) dA_head is zeroed, dinitial_state = dfinal_state (or 0) and
+ * dprev_B, dprev_x are zeroed.
  */
 ssm_status_t ssd_mamba3_bwd(const void* x, const float* dt, const float* lam, const float* A_head,
                             const void* B, const void* C, int chunk, const float* initial_state,
@@ -583,7 +583,8 @@ size_t ssd_mamba3_mimo_bwd_workspace_bytes(int batch, int seqlen, int rank, int 
  * kernels for lambda, the block-diagonal correction and the previous token.
  * workspace, aliasing, determinism and the no-step case as ssd_mamba3_bwd.
  * Supported: rank 1, 2 or 4 with chunk * rank == 64; headdim 64, dstate 128,
- * bf16 in_dtype, seqlen % chunk == 0, nheads % ngroups == 0.
+ * bf16 in_dtype, seqlen % chunk == 0, nheads % ngroups == 0, and
+ * (2 nheads + ngroups) rank^2 <= 12288.
  */
 ssm_status_t ssd_mamba3_mimo_bwd(const void* x, const float* dt, const float* lam,
                                  const float* A_head, const void* B, const void* C, int chunk,

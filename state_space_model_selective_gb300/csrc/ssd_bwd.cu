@@ -1158,6 +1158,8 @@ extern "C" ssm_status_t ssd_mamba3_bwd(const void* x, const float* dt, const flo
     if (chunk != 64 || headdim != kP || dstate != kNs || in_dtype != SSM_BF16)
         return SSM_ERR_UNSUPPORTED;
     if ((size_t)batch * nheads > (size_t)INT32_MAX) return SSM_ERR_UNSUPPORTED;
+    // the per-step kernel keeps two floats per head in shared memory (48 KB)
+    if ((size_t)nheads * 2 * sizeof(float) > 48 * 1024) return SSM_ERR_UNSUPPORTED;
     if ((prev_B == nullptr) != (prev_x == nullptr)) return SSM_ERR_NULL;
     const bool has_prev = prev_B != nullptr;
     const size_t items = (size_t)batch * nheads;
@@ -1647,6 +1649,9 @@ extern "C" ssm_status_t ssd_mamba3_mimo_bwd(
         return SSM_ERR_UNSUPPORTED;
     if ((size_t)batch * nheads > (size_t)INT32_MAX ||
         (size_t)seqlen * rank > (size_t)INT32_MAX)
+        return SSM_ERR_UNSUPPORTED;
+    // the per-step kernel keeps (2 nheads + ngroups) rank^2 floats in shared memory (48 KB)
+    if ((size_t)(2 * nheads + ngroups) * rank * rank * sizeof(float) > 48 * 1024)
         return SSM_ERR_UNSUPPORTED;
     if ((prev_B == nullptr) != (prev_x == nullptr)) return SSM_ERR_NULL;
     const bool has_prev = prev_B != nullptr;

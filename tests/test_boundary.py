@@ -375,6 +375,7 @@ def test_mamba3_bwd_argument_errors(L):
     assert m3_bwd_call(L, pB=P(14), px=P(15), dpB=P(16), dpx=P(16)) == ALIAS
     assert m3_bwd_call(L, bs=P(6)) == ALIAS                # block states under dx
     assert m3_bwd_call(L, bs=ctypes.c_void_p(0x70000008)) == ALIGN
+    assert m3_bwd_call(L, nheads=8192, ngroups=1) == UNSUP  # per-step shared memory
     assert m3_bwd_call(L, nheads=0, dA=None, x=None) == OK
 
 
@@ -414,6 +415,7 @@ def test_mimo_bwd_argument_errors(L):
     assert mimo_bwd_call(L, dx=ctypes.c_void_p(0x70000008)) == ALIGN
     assert mimo_bwd_call(L, wsb=1024) == WS
     assert mimo_bwd_call(L, dB=P(3)) == ALIAS             # dB on top of B
+    assert mimo_bwd_call(L, nheads=512, ngroups=1) == UNSUP  # per-step shared memory
     assert mimo_bwd_call(L, nheads=0, dA=None, x=None) == OK
 
 
