@@ -700,38 +700,49 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // dB, dC = the per-head partials ([h][b][n][t]) summed over each group's heads,
-// in head order, and written as (batch, seqlen, ngroups, dstate): a 32 x 32
-// (n, t) tile per block, transposed through shared memory so that both the
-// reads (t contiguous) and the writes (n contiguous) are coalesced.
+// in head order, and written as (batch, seqlen, ngroups, dstate): a 128 x 32
+// (t, n) tile per block, each thread adding four consecutive steps of four
+// rows with 16-byte loads, transposed through shared memory so that both the
+// reads (t contiguous) and the writes (n contiguous) are coalesced.  seqlen is
+// a multiple of 4 (of the chunk).
 __global__ void ssd_bwd_reduce_bc_kernel(const float* __restrict__ pB, const float* __restrict__ pC,
                                          float* __restrict__ dB, float* __restrict__ dC, int batch,
                                          int seqlen, int nheads, int ngroups) {
-    __shared__ float tile[32][33];
+    __shared__ float tile[32][129];
     const int hpg = nheads / ngroups;
-    const int t0 = blockIdx.x * 32, n0 = blockIdx.y * 32;
+    const int t0 = blockIdx.x * 128, n0 = blockIdx.y * 32;
     const long long L = seqlen;
     for (int z = blockIdx.z; z < 2 * batch * ngroups; z += gridDim.z) {
         const bool isC = z & 1;
         const int bg = z >> 1, bb = bg / ngroups, gg = bg % ngroups;
         const float* src = isC ? pC : pB;
         {
-            // rows n0 + threadIdx.y + 8 k, k < 4: four independent loads per head
-            const int t = t0 + threadIdx.x;
-            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            if (t < seqlen) {
-#pragma unroll 4
-                for (int hh = gg * hpg; hh < (gg + 1) * hpg; ++hh) {
-                    const float* p0 = src + (((long long)hh * batch + bb) * kNs + n0 + threadIdx.y) * L + t;
+            // rows n0 + threadIdx.y + 8 k, k < 4; steps t .. t + 3
+            const int t = t0 + 4 * threadIdx.x;
+            float4 acc[4];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) acc[k] += p0[8 * k * L];
+            for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (t < seqlen) {
+#pragma unroll 2
+                for (int hh = gg * hpg; hh < (gg + 1) * hpg; ++hh) {
+                    const float* p0 =
+                        src + (((long long)hh * batch + bb) * kNs + n0 + threadIdx.y) * L + t;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float4 v = *reinterpret_cast<const float4*>(p0 + 8 * k * L);
+                        acc[k].x += v.x; acc[k].y += v.y; acc[k].z += v.z; acc[k].w += v.w;
+                    }
                 }
             }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) tile[threadIdx.y + 8 * k][threadIdx.x] = acc[k];
+            for (int k = 0; k < 4; ++k) {
+                float* row = &tile[threadIdx.y + 8 * k][4 * threadIdx.x];
+                row[0] = acc[k].x; row[1] = acc[k].y; row[2] = acc[k].z; row[3] = acc[k].w;
+            }
         }
         __syncthreads();
         float* dst = isC ? dC : dB;
-        for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+        for (int r = threadIdx.y; r < 128; r += blockDim.y) {
             const int t = t0 + r, n = n0 + threadIdx.x;
             if (t < seqlen) dst[(((long long)bb * L + t) * ngroups + gg) * kNs + n] = tile[threadIdx.x][r];
         }
@@ -832,7 +843,7 @@ ssm_status_t run_bwd(const void* x, const float* dt, const float* wts, const flo
     if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
     // 3. sums over a group's heads and over the batch
     {
-        const dim3 grid((unsigned)((seqlen + 31) / 32), kNs / 32,
+        const dim3 grid((unsigned)((seqlen + 127) / 128), kNs / 32,
                         (unsigned)std::min<long long>(2LL * batch * ngroups, 65535));
         ssd_bwd_reduce_bc_kernel<<<grid, dim3(32, 8), 0, s>>>(a.pB, a.pC, dB, dC, batch, seqlen,
                                                              nheads, ngroups);
