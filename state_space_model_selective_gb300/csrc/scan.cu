@@ -69,9 +69,9 @@ struct ScanArgs {
     float* carry;     // [nchunks - 1][batch * dim][kN]
     const void* Bm;
     const void* Cm;
-    // checkpoint mode (kernel flag CK): the state entering every 16-step
-    // segment, [seg][batch * dim][kN] (the backward pass recomputes from
-    // these); y is then optional
+    // checkpoint mode (kernel flag CK = 1, or 2 without the read-out): the
+    // state entering every 16-step segment, [seg][batch * dim][kN] (the
+    // backward pass recomputes from these); y is then optional
     float* ckpt;
     int batch, dim, seqlen, ngroups;
     int dpg;          // channels per group
@@ -236,7 +236,7 @@ struct Smem {
     static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024
 };
 
-template <typename Tin, typename Tout, int CH, bool TMA, bool CK = false>
+template <typename Tin, typename Tout, int CH, bool TMA, int CK = 0>
 __global__ void __launch_bounds__(CH * kNG + 32, 3)
     scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u,
                     const __grid_constant__ CUtensorMap tm_d,
@@ -438,15 +438,18 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
                 if (t0 + tl + j >= t_end) dl = 0.0f;
                 o[2 * j] = dl;
                 o[2 * j + 1] = dl * uv[j];
-                e[2 * j] = pD * uv[j];
-                e[2 * j + 1] = has_z ? silu_f(zv[j]) : 1.0f;
+                if constexpr (CK != 2) {
+                    e[2 * j] = pD * uv[j];
+                    e[2 * j + 1] = has_z ? silu_f(zv[j]) : 1.0f;
+                }
             }
             float4* dst = reinterpret_cast<float4*>(prep + cl * kPrepStride + tl * 8);
             float4* dst2 = reinterpret_cast<float4*>(prep + (CH + cl) * kPrepStride + tl * 8);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-                dst2[j] = make_float4(e[4 * j], e[4 * j + 1], e[4 * j + 2], e[4 * j + 3]);
+                if constexpr (CK != 2)
+                    dst2[j] = make_float4(e[4 * j], e[4 * j + 1], e[4 * j + 2], e[4 * j + 3]);
             }
         }
         __syncwarp();
@@ -491,7 +494,7 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
         const uint8_t* tBC = st + 3 * S::IN_TILE + ng * 32;
 #pragma unroll kGroupUnroll
         for (int j = 0; j < kTL / 8; ++j) {
-            if (CK && (j & 1) == 0 && valid && t0 + j * 8 < a.seqlen) {
+            if (CK != 0 && (j & 1) == 0 && valid && t0 + j * 8 < a.seqlen) {
                 const long long seg = (t0 + j * 8) / 16;
                 __stcg(reinterpret_cast<float4*>(
                            a.ckpt + (seg * a.batch * a.dim + drow) * kN + n0),
@@ -507,18 +510,21 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
                     const float dl = r ? pp.z : pp.x;
                     const float du = r ? pp.w : pp.y;
                     const float4 bv = *reinterpret_cast<const float4*>(tBC + t * 128);
-                    const float4 cv = *reinterpret_cast<const float4*>(tBC + t * 128 + 16);
                     h[0] = fmaf(ex2_approx(dl * A2[0]), h[0], du * bv.x);
                     h[1] = fmaf(ex2_approx(dl * A2[1]), h[1], du * bv.y);
                     h[2] = fmaf(ex2_approx(dl * A2[2]), h[2], du * bv.z);
                     h[3] = fmaf(ex2_approx(dl * A2[3]), h[3], du * bv.w);
-                    float acc = cv.x * h[0];
-                    acc = fmaf(cv.y, h[1], acc);
-                    acc = fmaf(cv.z, h[2], acc);
-                    acc = fmaf(cv.w, h[3], acc);
-                    yp[q + r] = acc;
+                    if constexpr (CK != 2) {
+                        const float4 cv = *reinterpret_cast<const float4*>(tBC + t * 128 + 16);
+                        float acc = cv.x * h[0];
+                        acc = fmaf(cv.y, h[1], acc);
+                        acc = fmaf(cv.z, h[2], acc);
+                        acc = fmaf(cv.w, h[3], acc);
+                        yp[q + r] = acc;
+                    }
                 }
             }
+            if constexpr (CK == 2) continue;  // states only: no read-out
             // reduce-scatter the 8 partial sums over the 4 lanes of the channel
             // (lane bits 3 and 4): afterwards lane ng holds the full sums of
             // steps 2ng and 2ng+1, added as (p0 + p2) + (p1 + p3).
@@ -542,7 +548,7 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
             const float4 eg = *reinterpret_cast<const float4*>(prow2 + tl * 2);
             const float o0 = (f[0] + eg.x) * eg.y;
             const float o1 = (f[1] + eg.z) * eg.w;
-            if ((!CK || a.y) && valid && tg < t_end)
+            if ((CK == 0 || a.y) && valid && tg < t_end)
                 store_y2<Tout>(yrow + tg, o0, o1, true, tg + 1 < t_end, vec_store);
         }
 
@@ -615,7 +621,7 @@ size_t workspace_bound(long long batch, long long dim, int seqlen, int ngroups) 
     return round256(bytes);
 }
 
-template <typename Tin, typename Tout, int CH, bool TMA, bool CK = false>
+template <typename Tin, typename Tout, int CH, bool TMA, int CK = 0>
 int occupancy_blocks() {
     using S = Smem<Tin, CH, TMA>;
     static int cached = -1;
@@ -629,7 +635,7 @@ int occupancy_blocks() {
     return cached;
 }
 
-template <typename Tin, typename Tout, int CH, bool TMA, bool CK = false>
+template <typename Tin, typename Tout, int CH, bool TMA, int CK = 0>
 ssm_status_t launch(const ScanArgs& base, const Plan& p, const CUtensorMap* maps,
                     cudaStream_t stream) {
     using S = Smem<Tin, CH, TMA>;
@@ -648,7 +654,7 @@ ssm_status_t launch(const ScanArgs& base, const Plan& p, const CUtensorMap* maps
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
-template <typename Tin, typename Tout, int CH, bool TMA, bool CK = false>
+template <typename Tin, typename Tout, int CH, bool TMA, int CK = 0>
 void plan_for(const ScanArgs& a, Plan& p) {
     p.CH = CH;
     p.tma = TMA;
@@ -668,7 +674,7 @@ void plan_for(const ScanArgs& a, Plan& p) {
     p.nchunks = (tiles + p.chunk_tiles - 1) / p.chunk_tiles;
 }
 
-template <typename Tin, typename Tout, bool CK = false>
+template <typename Tin, typename Tout, int CK = 0>
 ssm_status_t dispatch(ScanArgs& a, ssm_dtype_t in_dtype, bool tma, cudaStream_t stream,
                       void* workspace) {
     Plan p{};
@@ -732,8 +738,8 @@ ssm_status_t scan_forward_checkpoints(const void* u, const void* delta, const fl
     const size_t es = in_dtype == SSM_BF16 ? 2 : 4;
     const bool tma = ((size_t)seqlen * es) % 16 == 0;
     if (in_dtype == SSM_BF16)
-        return dispatch<__nv_bfloat16, float, true>(a, in_dtype, tma, stream, workspace);
-    return dispatch<float, float, true>(a, in_dtype, tma, stream, workspace);
+        return dispatch<__nv_bfloat16, float, 2>(a, in_dtype, tma, stream, workspace);
+    return dispatch<float, float, 2>(a, in_dtype, tma, stream, workspace);
 }
 
 }  // namespace ssm_internal
