@@ -169,8 +169,12 @@ def test_workload_scan_bf16_sampled(shape, seed):
 @pytest.mark.parametrize("case", [(2, 64, 700, 1, "bf16", torch.float32, True),
                                   (1, 96, 1000, 2, "f32", torch.float32, False),
                                   (3, 40, 64, 4, "bf16", torch.bfloat16, True),
-                                  (2, 32, 30, 1, "f32", torch.float32, True)],
-                         ids=["bf16-L700", "f32-L1000-G2", "bf16out-L64", "L30"])
+                                  (2, 32, 30, 1, "f32", torch.float32, True),
+                                  (5, 64, 300, 1, "bf16", torch.float32, True),
+                                  (9, 48, 130, 2, "f32", torch.float32, False),
+                                  (4, 32, 64, 4, "bf16", torch.bfloat16, True)],
+                         ids=["bf16-L700", "f32-L1000-G2", "bf16out-L64", "L30",
+                              "B5-L300", "B9-G2-L130", "B4-bf16out-G4"])
 def test_scan_host_buffers_equal_device_scan(case):
     """ssm_scan_fwd_host (host-resident activations, copies pipelined over
     segments chained through the state) gives the same bits as ssm_scan_fwd on
