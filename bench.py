@@ -365,6 +365,7 @@ def measure_other_paths(dev, reps=20):
                      "frac": nbytes / (ms / 1e3) / 1e9 / HBM_PEAK_GBS,
                      "algorithmic_bytes": nbytes}}
     del inp
+    res["ssm_scan_fwd_long"] = _measure_scan_long(dev, reps)
     res["ssm_scan_bwd"] = _measure_scan_bwd(dev, reps)
     res["ssd_chunked_bwd"] = _measure_ssd_bwd(dev, reps)
     res["ssd_mamba3_bwd"] = _measure_mamba3_bwd(dev, reps)
@@ -464,6 +465,39 @@ def measure_other_paths(dev, reps=20):
                      "frac": nbytes3 / (ms / 1e3) / 1e9 / HBM_PEAK_GBS,
                      "algorithmic_bytes": nbytes3}}
     return res
+
+
+def _measure_scan_long(dev, reps):
+    """The long-sequence scan (bf16 in, fp32 y, batch 4, L 16384, 5120
+    channels, N 16, one B/C group, gate and softplus on): the channel blocks
+    outnumber the resident CTA slots, so the sequence runs as chained L-chunks
+    that hand the state on through the workspace.  Against the MUFU roofline,
+    like the benchmark step."""
+    import torch
+    from state_space_model_selective_gb300 import binding, inputs
+    batch, dim, seqlen = 4, 5120, 16384
+    x = inputs.scan_inputs(batch, dim, seqlen, DSTATE, 1, "bf16", seed=1003, device="cuda")
+    y = torch.empty((batch, dim, seqlen), dtype=torch.float32, device=dev)
+    fs = torch.empty((batch, dim, DSTATE), dtype=torch.float32, device=dev)
+    ws = torch.empty(binding.ssm_scan_workspace_bytes(batch, dim, seqlen, DSTATE, 1),
+                     dtype=torch.uint8, device=dev)
+
+    def fwd():
+        binding.ssm_scan_fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"],
+                             x["delta_bias"], True, out_dtype=torch.float32, y=y,
+                             final_state=fs, workspace=ws)
+    ms = _time(fwd, reps)
+    assert binding.ssm_last_device_status(ws) == 0
+    bld = batch * seqlen * dim
+    el = bld * DSTATE
+    mufu = el + 4 * bld
+    achieved = mufu / (ms / 1e3) / 1e9
+    return {"workload": "selective scan bf16 in / fp32 y, batch 4, L 16384, 5120 channels, "
+                        "d_state 16, 1 group, gate, softplus (chained L-chunks)",
+            "ms": ms, "elements_per_s": el / (ms / 1e3),
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": MUFU_PEAK_GOPS,
+                         "unit": "Gop/s (MUFU)", "frac": achieved / MUFU_PEAK_GOPS,
+                         "algorithmic_mufu_ops": mufu}}
 
 
 def _measure_scan_bwd(dev, reps):
