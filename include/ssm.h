@@ -646,6 +646,24 @@ ssm_status_t ssm_scan_fwd_host(const void* u, const void* delta, const float* A,
  */
 ssm_status_t ssm_last_device_status(const void* workspace, void* stream);
 
+/*
+ * Test hook for the scan's bounded look-back wait (every entry point that
+ * runs the scan kernel: ssm_scan_fwd, _ckpt, _noalloc, _host and the forward
+ * inside ssm_scan_bwd).  When the channel blocks outnumber the resident CTA
+ * slots the scan cuts the sequence into chunks chained through the state:
+ * chunk c of a block polls the flag chunk c-1 publishes (the decoupled
+ * look-back of Merrill and Garland's single-pass prefix scan), and a poll
+ * loop that runs out records SSM_ERR_TIMEOUT in the workspace and goes on.
+ *  - spin_limit: polls before that happens (0 restores the default, about a
+ *    second).
+ *  - drop_first_publish: nonzero makes chunk 0 of every block skip its
+ *    publish, so chunk 1 waits until its limit: a wait on a flag that nothing
+ *    sets, with no fault.  The scan's outputs are then undefined.
+ *  - Process-wide setting, read when each scan is enqueued; not for use while
+ *    other threads enqueue scans.  Always returns SSM_OK.
+ */
+ssm_status_t ssm_debug_set_lookback(int drop_first_publish, unsigned int spin_limit);
+
 #ifdef __cplusplus
 }
 #endif

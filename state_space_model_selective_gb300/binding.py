@@ -34,7 +34,7 @@ EXPORTS = ["ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_bytes", "
            "ssm_scan_fwd_host", "ssm_scan_checkpoint_bytes", "ssm_scan_fwd_ckpt",
            "ssd_chunked_checkpoint_bytes", "ssd_chunked_fwd_ckpt", "ssd_mamba3_bwd_workspace_bytes",
            "ssd_mamba3_bwd", "ssd_mamba3_mimo_bwd_workspace_bytes", "ssd_mamba3_mimo_bwd",
-           "ssd_mamba3_fwd_ckpt", "ssd_mamba3_mimo_fwd_ckpt"]
+           "ssd_mamba3_fwd_ckpt", "ssd_mamba3_mimo_fwd_ckpt", "ssm_debug_set_lookback"]
 
 
 class SSMError(RuntimeError):
@@ -111,6 +111,8 @@ def lib() -> ctypes.CDLL:
         L.ssm_scan_fwd_host.argtypes = [vp] * 8 + [i] + [vp] * 3 + [i] * 7 + [vp, sz, vp]
         L.ssm_last_device_status.restype = i
         L.ssm_last_device_status.argtypes = [vp, vp]
+        L.ssm_debug_set_lookback.restype = i
+        L.ssm_debug_set_lookback.argtypes = [i, ctypes.c_uint]
         _lib = L
     return _lib
 
@@ -639,6 +641,15 @@ def ssm_decode_step(state, x, dt, A, B, C, D=None, z=None, y=None, stream=None):
 def ssm_last_device_status(workspace, stream=None) -> int:
     """Device-side status recorded in a scan workspace (waits for the stream)."""
     return int(lib().ssm_last_device_status(_ptr(workspace), _stream(stream)))
+
+
+def ssm_debug_set_lookback(drop_first_publish: bool = False, spin_limit: int = 0) -> None:
+    """Test hook of the scan's chained L-chunks: chunk 0 withholds its publish
+    (so chunk 1's bounded wait runs out and records SSM_ERR_TIMEOUT) and the
+    wait gives up after ``spin_limit`` polls (0: the default).  Process-wide;
+    call with no arguments to restore the defaults."""
+    _check(lib().ssm_debug_set_lookback(1 if drop_first_publish else 0, int(spin_limit)),
+           "ssm_debug_set_lookback")
 
 
 def ssd_mamba3_fwd(x, dt, lam, A_head, B, C, chunk=64, out_dtype=None, y=None, final_state=None,

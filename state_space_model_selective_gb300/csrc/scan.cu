@@ -30,6 +30,7 @@
 //    The associativity of the recurrence ("We built the parallel scan"
 //    section of the first page) is what makes the chunk split exact.
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -80,6 +81,8 @@ struct ScanArgs {
     int nchunks;
     int chunk_tiles;  // tiles per chunk
     int softplus;
+    uint32_t flag_spin_limit;  // look-back polls before SSM_ERR_TIMEOUT
+    int drop_first_publish;    // test hook: chunk 0 never publishes its carry
 };
 
 // Byte offset of (row r, step t) in a tile of ROWS rows x kTL steps laid out
@@ -467,7 +470,7 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
                 if (lane == 0) {
                     bool seen = false;
                     uint32_t ns = 32;
-                    for (uint32_t it = 0; it < kFlagSpinLimit; ++it) {
+                    for (uint32_t it = 0; it < a.flag_spin_limit; ++it) {
                         if (ld_acquire_gpu(flag)) { seen = true; break; }
                         __nanosleep(ns);
                         ns = ns < 256 ? ns * 2 : 256;
@@ -575,11 +578,18 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
     if (chunk < a.nchunks - 1) {
         __threadfence();
         named_bar_sync(1, NCOMP);
-        if (tid == 0) st_release_gpu(a.flags + (size_t)chunk * a.nblocks + blk, 1u);
+        if (tid == 0 && !(a.drop_first_publish && chunk == 0))
+            st_release_gpu(a.flags + (size_t)chunk * a.nblocks + blk, 1u);
     }
 }
 
 // ------------------------------------------------------------------ host
+
+// Look-back settings of every scan launch, set by ssm_debug_set_lookback:
+// the poll limit (0: kFlagSpinLimit) and whether chunk 0 withholds its
+// publish, so that a test can watch the bounded wait run out.
+std::atomic<uint32_t> g_flag_spin_limit{0};
+std::atomic<int> g_drop_first_publish{0};
 
 struct Plan {
     int CH;
@@ -644,6 +654,9 @@ ssm_status_t launch(const ScanArgs& base, const Plan& p, const CUtensorMap* maps
         cudaSuccess)
         return SSM_ERR_CUDA;
     ScanArgs a = base;
+    const uint32_t lim = g_flag_spin_limit.load(std::memory_order_relaxed);
+    a.flag_spin_limit = lim ? lim : kFlagSpinLimit;
+    a.drop_first_publish = g_drop_first_publish.load(std::memory_order_relaxed);
     a.bpg = p.bpg;
     a.nblocks = p.nblocks;
     a.nchunks = p.nchunks;
@@ -990,4 +1003,10 @@ extern "C" ssm_status_t ssm_scan_fwd_noalloc(const void* u, const void* delta, c
     }
     return out_dtype == SSM_BF16 ? dispatch<float, __nv_bfloat16>(a, in_dtype, tma, s, scratch)
                                  : dispatch<float, float>(a, in_dtype, tma, s, scratch);
+}
+
+extern "C" ssm_status_t ssm_debug_set_lookback(int drop_first_publish, unsigned int spin_limit) {
+    g_flag_spin_limit.store(spin_limit, std::memory_order_relaxed);
+    g_drop_first_publish.store(drop_first_publish ? 1 : 0, std::memory_order_relaxed);
+    return SSM_OK;
 }
