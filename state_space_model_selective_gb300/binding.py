@@ -156,6 +156,18 @@ def _opt(t, name, dtype=None, ndim=None):
     return None if t is None else _req(t, name, dtype, ndim)
 
 
+def _use_out(g, out):
+    """Puts the caller's preallocated fp32 tensors (``out``: name -> tensor) in
+    place of the gradient buffers ``g`` would allocate."""
+    for k, t in (out or {}).items():
+        if k not in g or g[k] is None:
+            raise ValueError(f"out[{k!r}] is not an output of this call")
+        _req(t, f"out[{k!r}]", torch.float32)
+        if t.shape != g[k].shape:
+            raise ValueError(f"out[{k!r}] must have shape {tuple(g[k].shape)}")
+        g[k] = t
+
+
 def ssm_scan_workspace_bytes(batch, dim, seqlen, dstate=16, ngroups=1) -> int:
     return int(lib().ssm_scan_workspace_bytes(batch, dim, seqlen, dstate, ngroups))
 
@@ -269,13 +281,7 @@ def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_s
         g["dz"] = torch.empty((batch, dim, seqlen), dtype=f32, device=dev)
     if want_dinitial_state:
         g["dinitial_state"] = torch.empty((batch, dim, dstate), dtype=f32, device=dev)
-    for k, t in (out or {}).items():
-        if k not in g or g[k] is None:
-            raise ValueError(f"out[{k!r}] is not an output of this call")
-        _req(t, f"out[{k!r}]", f32)
-        if t.shape != g[k].shape:
-            raise ValueError(f"out[{k!r}] must have shape {tuple(g[k].shape)}")
-        g[k] = t
+    _use_out(g, out)
     need = ssm_scan_bwd_workspace_bytes(batch, dim, seqlen, dstate, ngroups)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
@@ -422,13 +428,7 @@ def ssd_chunked_bwd(x, dt, A_head, B, C, dy, chunk=64, initial_state=None, dfina
          "dC": torch.empty(tuple(C.shape), dtype=f32, device=dev),
          "dinitial_state": (torch.empty((batch, nheads, headdim, dstate), dtype=f32, device=dev)
                             if want_dinitial_state else None)}
-    for k, t in (out or {}).items():
-        if k not in g or g[k] is None:
-            raise ValueError(f"out[{k!r}] is not an output of this call")
-        _req(t, f"out[{k!r}]", f32)
-        if t.shape != g[k].shape:
-            raise ValueError(f"out[{k!r}] must have shape {tuple(g[k].shape)}")
-        g[k] = t
+    _use_out(g, out)
     need = ssd_chunked_bwd_workspace_bytes(batch, seqlen, nheads, headdim, dstate, ngroups)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
@@ -453,11 +453,12 @@ def ssd_mamba3_bwd_workspace_bytes(batch, seqlen, nheads, headdim=64, dstate=128
 
 def ssd_mamba3_bwd(x, dt, lam, A_head, B, C, dy, chunk=64, initial_state=None, prev_B=None,
                    prev_x=None, dfinal_state=None, workspace=None, want_dinitial_state=True,
-                   stream=None, block_states=None):
+                   stream=None, block_states=None, out=None):
     """Gradient of ``ssd_mamba3_fwd`` for the loss sum(dy * y) + sum(dfinal_state *
     final_state).  Inputs as for ``ssd_mamba3_fwd`` (bf16 x, B, C, prev_B, prev_x);
     dy like x (bf16).  Returns a dict of fp32 tensors: dx, ddt, dlam, dA_head, dB, dC,
-    dinitial_state (or None) and dprev_B, dprev_x (None without a previous token)."""
+    dinitial_state (or None) and dprev_B, dprev_x (None without a previous token).
+    ``out`` may map any of these names to a preallocated fp32 tensor to write."""
     _req(x, "x", torch.bfloat16, 4)
     batch, seqlen, nheads, headdim = x.shape
     _req(dt, "dt", torch.float32, 3)
@@ -485,6 +486,7 @@ def ssd_mamba3_bwd(x, dt, lam, A_head, B, C, dy, chunk=64, initial_state=None, p
                      if has_prev else None),
          "dprev_x": (torch.empty((batch, nheads, headdim), dtype=f32, device=dev)
                      if has_prev else None)}
+    _use_out(g, out)
     need = ssd_mamba3_bwd_workspace_bytes(batch, seqlen, nheads, headdim, dstate, ngroups)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
@@ -511,12 +513,13 @@ def ssd_mamba3_mimo_bwd_workspace_bytes(batch, seqlen, rank, nheads, headdim=64,
 
 def ssd_mamba3_mimo_bwd(x, dt, lam, A_head, B, C, dy, chunk=None, initial_state=None,
                         prev_B=None, prev_x=None, dfinal_state=None, workspace=None,
-                        want_dinitial_state=True, stream=None, block_states=None):
+                        want_dinitial_state=True, stream=None, block_states=None, out=None):
     """Gradient of ``ssd_mamba3_mimo_fwd``.  x, dy: (batch, seqlen, rank, nheads,
     headdim) bf16; B, C: (batch, seqlen, rank, ngroups, dstate) bf16; prev_B (batch,
     rank, ngroups, dstate), prev_x (batch, rank, nheads, headdim) bf16 or None.
     ``chunk`` defaults to 64 // rank.  Returns a dict of fp32 tensors like
-    ``ssd_mamba3_bwd``'s, with dx, dB, dC, dprev_B, dprev_x shaped like their inputs."""
+    ``ssd_mamba3_bwd``'s, with dx, dB, dC, dprev_B, dprev_x shaped like their inputs;
+    ``out`` as for ``ssd_mamba3_bwd``."""
     _req(x, "x", torch.bfloat16, 5)
     batch, seqlen, rank, nheads, headdim = x.shape
     _req(dt, "dt", torch.float32, 3)
@@ -545,6 +548,7 @@ def ssd_mamba3_mimo_bwd(x, dt, lam, A_head, B, C, dy, chunk=None, initial_state=
                      if has_prev else None),
          "dprev_x": (torch.empty(tuple(prev_x.shape), dtype=f32, device=dev)
                      if has_prev else None)}
+    _use_out(g, out)
     need = ssd_mamba3_mimo_bwd_workspace_bytes(batch, seqlen, rank, nheads, headdim, dstate,
                                                ngroups)
     if workspace is None:

@@ -47,6 +47,9 @@ CASES = [
     (2, 40, 130, 4, "bf16", True, "randn", True),    # 10 channels per group: partial blocks
     (1, 32, 1000, 1, "bf16", False, "ones", True),   # bf16 rows 16B-aligned, ragged tail
     (2, 32, 77, 1, "bf16", True, "ones", False),     # odd L with bf16: plain-load path
+    (1, 32, 1, 1, "f32", True, "randn", True),       # a single step
+    (2, 32, 65, 1, "f32", True, "ones", True),       # one step past a tile, plain loads
+    (2, 64, 72, 2, "bf16", True, "ones", True),      # one 8-step group past a tile, TMA rows
 ]
 
 
