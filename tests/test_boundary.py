@@ -38,6 +38,13 @@ def test_header_symbols_exported(L):
         assert hasattr(L, name), f"libssm.so does not export {name}"
 
 
+def test_lookback_debug_hook_is_host_only(L):
+    # a process-wide setting read at enqueue time: setting and restoring it
+    # touches no device
+    assert L.ssm_debug_set_lookback(1, 2000) == OK
+    assert L.ssm_debug_set_lookback(0, 0) == OK
+
+
 def test_version_and_status_strings(L):
     assert binding.ssm_abi_version() == 4
     for code in range(10):
