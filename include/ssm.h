@@ -18,8 +18,10 @@
  * Conventions shared by every entry point
  *  - Pointers are DEVICE pointers unless stated otherwise, to dense row-major
  *    (C-contiguous) arrays in the layouts given per function.  The caller owns
- *    every buffer, including the scan's workspace; the library allocates
- *    nothing and keeps no state between calls.
+ *    every buffer, including the scan's workspace; the library allocates no
+ *    device memory.  State it keeps between calls: ssm_scan_fwd_host's copy
+ *    streams and events, ssm_scan_fwd_noalloc's fixed scratch array, and the
+ *    ssm_debug_set_lookback setting.
  *  - Every base pointer must be 16-byte aligned (any cudaMalloc or PyTorch
  *    allocation is), else SSM_ERR_ALIGN.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
