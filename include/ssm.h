@@ -109,6 +109,22 @@ size_t ssm_scan_workspace_bytes(int batch, int dim, int seqlen, int dstate, int 
  *                     call that may run concurrently.
  * Supported: dstate == 16; dim % ngroups == 0; any batch, dim, seqlen >= 0.
  * seqlen == 0 writes final_state = initial_state (or 0).
+ *
+ * Two kernels compute it (the same result up to fp32 rounding order):
+ *  - batch * dim > 3072: the work-efficient chained scan.  Each channel's 16
+ *    states sit in registers and walk the sequence in order (one exp per
+ *    element); when the channel blocks outnumber the GPU's resident CTA slots
+ *    the sequence is cut into chunks chained through the state.
+ *  - batch * dim <= 3072 (too few channels to fill the GPU): the
+ *    sequence-parallel scan.  The sequence is cut into 128-step chunks (one
+ *    CTA each) and each chunk into 8, 16 or 32 segments (one lane each); a
+ *    span of steps acts on the state as h -> P h + q and spans compose by
+ *    (P1, q1) o (P2, q2) = (P1 P2, P2 q1 + q2) (the associativity of the first
+ *    page's section "We built the parallel scan -- and it taught us something
+ *    sharper").  Lanes combine their segments with warp shuffles; chunks
+ *    combine through a decoupled look-back in the workspace, each chunk
+ *    publishing its aggregate (P, q) before it knows its entry state.  Every
+ *    element then costs two exps (one pass from zero, one replay).
  */
 ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const float* A,
                           const void* B, const void* C, const float* D, const void* z,
@@ -287,12 +303,16 @@ ssm_status_t ssm_decode_step_mamba3_mimo(float* state, const void* prev_B, const
  * a fixed 4 MiB array inside the library's device image, which every GPU that
  * loads the library holds until the process exits.  It allocates nothing.
  *
- *  - Limit: problems whose scratch (a 256-byte header, plus, when the scan
- *    is split into chained L-chunks on this GPU, one flag per chunk and
- *    channel block and 64 bytes of carried state per channel and chunk)
- *    exceeds 4 MiB are rejected with SSM_ERR_WORKSPACE before anything is
- *    enqueued; ssm_scan_fwd with a caller-supplied workspace handles them.
- *  - The first call on each device looks up the array's device address
+ *  - Limit: problems whose scratch exceeds 4 MiB are rejected with
+ *    SSM_ERR_WORKSPACE before anything is enqueued; ssm_scan_fwd with a
+ *    caller-supplied workspace handles them.  The scratch is a 256-byte
+ *    header, plus, for the chained scan split into L-chunks on this GPU, one
+ *    flag per chunk and channel block and 64 bytes of carried state per
+ *    channel and chunk; for the sequence-parallel scan (batch * dim <= 3072,
+ *    more than 128 steps), one flag per 128-step chunk and channel block and
+ *    192 bytes of aggregate and state per channel and chunk.
+ *  - The first call on each device (and the first after a cudaDeviceReset
+ *    gave the device a new context) looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current); make that first call
  *    before any stream capture.
  *  - All calls on a device share the one array, which keeps the contents the
@@ -300,7 +320,10 @@ ssm_status_t ssm_decode_step_mamba3_mimo(float* state, const void* prev_B, const
  *    Calls whose executions overlap on the GPU (different streams, or
  *    different host threads without ordering) race on the array and give
  *    undefined results: serialise them.
- *  - ssm_last_device_status does not apply (there is no workspace to read).
+ *  - A device-side wait that runs out records SSM_ERR_TIMEOUT in the array's
+ *    header, as ssm_scan_fwd does in its workspace: read it with
+ *    ssm_noalloc_last_status (ssm_last_device_status has no workspace to
+ *    read here).
  */
 ssm_status_t ssm_scan_fwd_noalloc(const void* u, const void* delta, const float* A,
                                   const void* B, const void* C, const float* D, const void* z,
@@ -308,6 +331,15 @@ ssm_status_t ssm_scan_fwd_noalloc(const void* u, const void* delta, const float*
                                   const float* initial_state, void* y, float* final_state,
                                   int batch, int dim, int seqlen, int dstate, int ngroups,
                                   ssm_dtype_t in_dtype, ssm_dtype_t out_dtype, void* stream);
+
+/*
+ * Waits for `stream` to drain, then returns the device-side status that the
+ * last ssm_scan_fwd_noalloc on the current device recorded in its scratch
+ * array (SSM_OK or SSM_ERR_TIMEOUT), or SSM_ERR_CUDA if the stream reports an
+ * error.  Allocates nothing (the status is copied into a host stack variable).
+ * No counterpart on the pages.
+ */
+ssm_status_t ssm_noalloc_last_status(void* stream);
 
 /*
  * Bytes of the checkpoints ssm_scan_fwd_ckpt keeps: the state entering every
@@ -321,7 +353,10 @@ size_t ssm_scan_checkpoint_bytes(int batch, int dim, int seqlen, int dstate);
  * state entering every 16-step segment -- what ssm_scan_bwd needs, so that a
  * training step does not run the forward recurrence twice.  y and final_state
  * are exactly ssm_scan_fwd's; the same arguments and errors, plus SSM_ERR_NULL
- * for a NULL `checkpoints` when there is work.
+ * for a NULL `checkpoints` when there is work.  (For batch * dim <= 3072,
+ * where ssm_scan_fwd runs the sequence-parallel scan, y and final_state come
+ * from that scan and the checkpoints from a second, states-only pass of the
+ * chained scan.)
  */
 ssm_status_t ssm_scan_fwd_ckpt(const void* u, const void* delta, const float* A, const void* B,
                                const void* C, const float* D, const void* z,
@@ -620,8 +655,10 @@ size_t ssm_scan_fwd_host_workspace_bytes(int batch, int dim, int seqlen, int dst
  *   built the parallel scan -- and it taught us something sharper"); each
  *   segment's rows are copied in with 2-D DMA copies, scanned on `stream` from
  *   the previous segment's final state, and its y copied back, with the copies
- *   of neighbouring segments in flight during the scan.  The result is bit-equal
- *   to ssm_scan_fwd on device copies of the same inputs.
+ *   of neighbouring segments in flight during the scan.  Segments are whole
+ *   multiples of 128 steps and every segment is scanned with the whole
+ *   sequence's plan, so the result is bit-equal to ssm_scan_fwd on device
+ *   copies of the same inputs.
  *
  *  - Asynchronous like every entry point: work is enqueued on `stream` and on
  *    two copy streams of the library's own (created on the first call on a
@@ -629,8 +666,8 @@ size_t ssm_scan_fwd_host_workspace_bytes(int batch, int dim, int seqlen, int dst
  *    every copy of the call.  The host buffers must not be modified (inputs) or
  *    read (outputs) until then.
  *  - workspace: at least ssm_scan_fwd_host_workspace_bytes(...) bytes, not
- *    shared with a concurrent call; ssm_last_device_status reports the last
- *    segment's device status.
+ *    shared with a concurrent call; ssm_last_device_status reports the first
+ *    device-side timeout of any segment (SSM_OK if none).
  *  - Calls on one device are enqueued one at a time (an internal lock).
  */
 ssm_status_t ssm_scan_fwd_host(const void* u, const void* delta, const float* A, const void* B,
@@ -649,22 +686,37 @@ ssm_status_t ssm_scan_fwd_host(const void* u, const void* delta, const float* A,
 ssm_status_t ssm_last_device_status(const void* workspace, void* stream);
 
 /*
- * Test hook for the scan's bounded look-back wait (every entry point that
- * runs the scan kernel: ssm_scan_fwd, _ckpt, _noalloc, _host and the forward
- * inside ssm_scan_bwd).  When the channel blocks outnumber the resident CTA
- * slots the scan cuts the sequence into chunks chained through the state:
- * chunk c of a block polls the flag chunk c-1 publishes (the decoupled
- * look-back of Merrill and Garland's single-pass prefix scan), and a poll
- * loop that runs out records SSM_ERR_TIMEOUT in the workspace and goes on.
+ * Test hook for the scan's bounded look-back waits (every entry point that
+ * runs a scan kernel: ssm_scan_fwd, _ckpt, _noalloc, _host and the forward
+ * inside ssm_scan_bwd).  The chained scan cuts the sequence into chunks when
+ * the channel blocks outnumber the resident CTA slots, and chunk c of a block
+ * polls the flag chunk c-1 publishes with its final state.  The
+ * sequence-parallel scan always cuts it into 128-step chunks, and chunk c
+ * polls the flags of chunks c-1, c-2, ... (aggregate or inclusive state: the
+ * decoupled look-back of Merrill and Garland's single-pass prefix scan).  A
+ * poll loop that runs out records SSM_ERR_TIMEOUT in the workspace and goes
+ * on.
  *  - spin_limit: polls before that happens (0 restores the default, about a
  *    second).
  *  - drop_first_publish: nonzero makes chunk 0 of every block skip its
- *    publish, so chunk 1 waits until its limit: a wait on a flag that nothing
- *    sets, with no fault.  The scan's outputs are then undefined.
+ *    publish of its final (inclusive) state, so chunk 1 waits until its
+ *    limit: a wait on a flag that nothing sets, with no fault.  The scan's
+ *    outputs are then undefined.
  *  - Process-wide setting, read when each scan is enqueued; not for use while
  *    other threads enqueue scans.  Always returns SSM_OK.
  */
 ssm_status_t ssm_debug_set_lookback(int drop_first_publish, unsigned int spin_limit);
+
+/*
+ * Test hook choosing the forward scan's kernel, so that tests can run both on
+ * the same problem.  path: 0 as planned (see ssm_scan_fwd), 1 always the
+ * chained scan, 2 the sequence-parallel scan wherever batch * dim <= 3072
+ * (larger problems keep the chained scan: the workspace size does not cover
+ * the other).  segments: the sequence-parallel scan's segments per 128-step
+ * chunk, 8, 16 or 32 (0 = planned).  Process-wide, read when each scan is
+ * enqueued.  Returns SSM_ERR_SHAPE for other values, else SSM_OK.
+ */
+ssm_status_t ssm_debug_set_scan_path(int path, int segments);
 
 #ifdef __cplusplus
 }

@@ -34,7 +34,8 @@ EXPORTS = ["ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_bytes", "
            "ssm_scan_fwd_host", "ssm_scan_checkpoint_bytes", "ssm_scan_fwd_ckpt",
            "ssd_chunked_checkpoint_bytes", "ssd_chunked_fwd_ckpt", "ssd_mamba3_bwd_workspace_bytes",
            "ssd_mamba3_bwd", "ssd_mamba3_mimo_bwd_workspace_bytes", "ssd_mamba3_mimo_bwd",
-           "ssd_mamba3_fwd_ckpt", "ssd_mamba3_mimo_fwd_ckpt", "ssm_debug_set_lookback"]
+           "ssd_mamba3_fwd_ckpt", "ssd_mamba3_mimo_fwd_ckpt", "ssm_debug_set_lookback",
+           "ssm_debug_set_scan_path", "ssm_noalloc_last_status"]
 
 
 class SSMError(RuntimeError):
@@ -113,6 +114,10 @@ def lib() -> ctypes.CDLL:
         L.ssm_last_device_status.argtypes = [vp, vp]
         L.ssm_debug_set_lookback.restype = i
         L.ssm_debug_set_lookback.argtypes = [i, ctypes.c_uint]
+        L.ssm_debug_set_scan_path.restype = i
+        L.ssm_debug_set_scan_path.argtypes = [i, i]
+        L.ssm_noalloc_last_status.restype = i
+        L.ssm_noalloc_last_status.argtypes = [vp]
         _lib = L
     return _lib
 
@@ -154,6 +159,38 @@ def _req(t, name, dtype=None, ndim=None):
 
 def _opt(t, name, dtype=None, ndim=None):
     return None if t is None else _req(t, name, dtype, ndim)
+
+
+def _shape(t, name, shape):
+    """Raises ValueError unless tensor ``t`` (when given) has exactly ``shape``."""
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _scan_shapes(u, delta, A, B, C, D, z, delta_bias, initial_state, y, final_state,
+                 dy=None, dfinal_state=None):
+    """Checks every scan tensor against u's (batch, dim, seqlen), A's dstate and
+    B's ngroups, so that no kernel reads or writes past a buffer the caller passed."""
+    batch, dim, seqlen = u.shape
+    if A.dim() != 2 or A.shape[0] != dim:
+        raise ValueError(f"A must have shape ({dim}, dstate), got {tuple(A.shape)}")
+    dstate = A.shape[1]
+    if B.dim() != 4 or B.shape[0] != batch or B.shape[2] != dstate or B.shape[3] != seqlen:
+        raise ValueError(f"B must have shape ({batch}, ngroups, {dstate}, {seqlen}), "
+                         f"got {tuple(B.shape)}")
+    ngroups = B.shape[1]
+    act = (batch, dim, seqlen)
+    _shape(delta, "delta", act)
+    _shape(z, "z", act)
+    _shape(y, "y", act)
+    _shape(dy, "dy", act)
+    _shape(C, "C", (batch, ngroups, dstate, seqlen))
+    _shape(D, "D", (dim,))
+    _shape(delta_bias, "delta_bias", (dim,))
+    for t, name in ((initial_state, "initial_state"), (final_state, "final_state"),
+                    (dfinal_state, "dfinal_state")):
+        _shape(t, name, (batch, dim, dstate))
+    return batch, dim, seqlen, dstate, ngroups
 
 
 def _use_out(g, out):
@@ -206,6 +243,7 @@ def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softp
     if final_state is None and return_final_state:
         final_state = torch.empty((batch, dim, dstate), dtype=torch.float32, device=u.device)
     _opt(final_state, "final_state", torch.float32)
+    _scan_shapes(u, delta, A, B, C, D, z, delta_bias, initial_state, y, final_state)
     need = ssm_scan_workspace_bytes(batch, dim, seqlen, dstate, ngroups)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=u.device)
@@ -266,6 +304,8 @@ def ssm_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_s
     _opt(delta_bias, "delta_bias", torch.float32)
     _opt(initial_state, "initial_state", torch.float32)
     _opt(dfinal_state, "dfinal_state", torch.float32)
+    _scan_shapes(u, delta, A, B, C, D, z, delta_bias, initial_state, None, None, dy=dy,
+                 dfinal_state=dfinal_state)
     dev, f32 = u.device, torch.float32
     g = {"du": torch.empty((batch, dim, seqlen), dtype=f32, device=dev),
          "ddelta": torch.empty((batch, dim, seqlen), dtype=f32, device=dev),
@@ -345,6 +385,7 @@ def ssm_scan_fwd_host(u, delta, A, B, C, y, final_state=None, D=None, z=None, de
         raise TypeError("y must be float32 or bfloat16")
     if final_state is not None:
         _pinned(final_state, "final_state", torch.float32)
+    _scan_shapes(u, delta, A, B, C, D, z, delta_bias, initial_state, y, final_state)
     need = ssm_scan_fwd_host_workspace_bytes(batch, dim, seqlen, dstate, ngroups, in_dt, y.dtype)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=A.device)
@@ -381,6 +422,7 @@ def ssm_scan_fwd_noalloc(u, delta, A, B, C, y, final_state=None, D=None, z=None,
     if y.dtype not in _DT:
         raise TypeError("y must be float32 or bfloat16")
     _opt(final_state, "final_state", torch.float32)
+    _scan_shapes(u, delta, A, B, C, D, z, delta_bias, initial_state, y, final_state)
     st = lib().ssm_scan_fwd_noalloc(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
                                     _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)),
                                     _ptr(initial_state), _ptr(y), _ptr(final_state), batch, dim,
@@ -593,8 +635,15 @@ def ssd_chunked_fwd(x, dt, A_head, B, C, chunk=64, out_dtype=None, y=None, final
                                   device=x.device)
     _opt(final_state, "final_state", torch.float32)
     _opt(initial_state, "initial_state", torch.float32)
-    if initial_state is not None and tuple(initial_state.shape) != (batch, nheads, headdim, dstate):
-        raise ValueError("initial_state must be (batch, nheads, headdim, dstate)")
+    _shape(dt, "dt", (batch, seqlen, nheads))
+    _shape(A_head, "A_head", (nheads,))
+    if B.shape[0] != batch or B.shape[1] != seqlen:
+        raise ValueError(f"B must have shape ({batch}, {seqlen}, ngroups, dstate), "
+                         f"got {tuple(B.shape)}")
+    _shape(C, "C", tuple(B.shape))
+    _shape(y, "y", tuple(x.shape))
+    _shape(initial_state, "initial_state", (batch, nheads, headdim, dstate))
+    _shape(final_state, "final_state", (batch, nheads, headdim, dstate))
     if block_states is not None:
         _req(block_states, "block_states", torch.float32)
         if block_states.numel() * 4 < ssd_chunked_checkpoint_bytes(batch, seqlen, nheads, headdim,
@@ -635,6 +684,15 @@ def ssm_decode_step(state, x, dt, A, B, C, D=None, z=None, y=None, stream=None):
     if y is None:
         y = torch.empty_like(x)
     _req(y, "y", dt_)
+    _shape(x, "x", (batch, nheads, headdim))
+    _shape(z, "z", (batch, nheads, headdim))
+    _shape(y, "y", (batch, nheads, headdim))
+    _shape(dt, "dt", (batch, nheads))
+    _shape(A, "A", (nheads,))
+    _shape(D, "D", (nheads,))
+    if B.shape[0] != batch or B.shape[2] != dstate:
+        raise ValueError(f"B must have shape ({batch}, ngroups, {dstate}), got {tuple(B.shape)}")
+    _shape(C, "C", tuple(B.shape))
     st = lib().ssm_decode_step(_ptr(state), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
                                _ptr(D), _ptr(z), _ptr(y), batch, nheads, headdim, dstate,
                                ngroups, _DT[dt_], _stream(stream))
@@ -654,6 +712,20 @@ def ssm_debug_set_lookback(drop_first_publish: bool = False, spin_limit: int = 0
     call with no arguments to restore the defaults."""
     _check(lib().ssm_debug_set_lookback(1 if drop_first_publish else 0, int(spin_limit)),
            "ssm_debug_set_lookback")
+
+
+def ssm_debug_set_scan_path(path: int = 0, segments: int = 0) -> None:
+    """Test hook choosing the forward scan's kernel: path 0 as planned, 1 the
+    chained scan, 2 the sequence-parallel scan (where batch * dim <= 3072);
+    segments: the sequence-parallel scan's segments per 128-step chunk (8, 16,
+    32; 0 = planned).  Process-wide; call with no arguments to restore."""
+    _check(lib().ssm_debug_set_scan_path(int(path), int(segments)), "ssm_debug_set_scan_path")
+
+
+def ssm_noalloc_last_status(stream=None) -> int:
+    """Device-side status the last ``ssm_scan_fwd_noalloc`` on the current device
+    recorded in its scratch array (waits for the stream)."""
+    return int(lib().ssm_noalloc_last_status(_stream(stream)))
 
 
 def ssd_mamba3_fwd(x, dt, lam, A_head, B, C, chunk=64, out_dtype=None, y=None, final_state=None,

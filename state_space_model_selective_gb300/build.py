@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libssm.so")
-SOURCES = ["scan.cu", "scan_bwd.cu", "scan_host.cu", "decode.cu", "ssd.cu", "ssd_bwd.cu",
+SOURCES = ["scan.cu", "scan_seg.cu", "scan_bwd.cu", "scan_host.cu", "decode.cu", "ssd.cu", "ssd_bwd.cu",
            "api.cu"]
 PEAKS_SRC = "peaks.cu"
 PEAKS_LIB = os.path.join(PKG, "libssm_peaks.so")

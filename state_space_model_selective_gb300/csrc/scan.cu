@@ -34,6 +34,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "scan_internal.h"
 
 namespace {
 
@@ -620,7 +621,7 @@ size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Workspace is sized for the largest plan any device could pick, so that
 // ssm_scan_workspace_bytes is a pure function of the problem.
-size_t workspace_bound(long long batch, long long dim, int seqlen, int ngroups) {
+size_t chained_workspace_bound(long long batch, long long dim, int seqlen, int ngroups) {
     const long long dpg = dim / ngroups;
     const long long max_blocks = batch * ngroups * ((dpg + 15) / 16);
     const long long tiles = (seqlen + kTL - 1) / kTL;
@@ -629,6 +630,23 @@ size_t workspace_bound(long long batch, long long dim, int seqlen, int ngroups) 
     bytes += round256(sizeof(uint32_t) * (size_t)(max_chunks - 1) * (size_t)max_blocks);
     bytes += (size_t)(max_chunks - 1) * (size_t)batch * (size_t)dim * kN * sizeof(float);
     return round256(bytes);
+}
+
+// Which forward path runs (ssm_debug_set_scan_path): 0 planned, 1 the chained
+// scan, 2 the sequence-parallel scan (only for problems eligible for it).
+std::atomic<int> g_scan_path{0};
+
+bool use_seg_path(long long batch, long long dim) {
+    if (!ssm_internal::scan_seg_eligible(batch, dim)) return false;
+    return g_scan_path.load(std::memory_order_relaxed) != 1;
+}
+
+size_t workspace_bound(long long batch, long long dim, int seqlen, int ngroups) {
+    size_t bytes = chained_workspace_bound(batch, dim, seqlen, ngroups);
+    if (ssm_internal::scan_seg_eligible(batch, dim))
+        bytes = std::max(bytes, ssm_internal::scan_seg_workspace_bytes(
+                                    (int)batch, (int)dim, seqlen, ngroups));
+    return bytes;
 }
 
 template <typename Tin, typename Tout, int CH, bool TMA, int CK = 0>
@@ -689,7 +707,7 @@ void plan_for(const ScanArgs& a, Plan& p) {
 
 template <typename Tin, typename Tout, int CK = 0>
 ssm_status_t dispatch(ScanArgs& a, ssm_dtype_t in_dtype, bool tma, cudaStream_t stream,
-                      void* workspace) {
+                      void* workspace, bool keep_status = false) {
     Plan p{};
     if (tma) plan_for<Tin, Tout, 32, true, CK>(a, p);
     else plan_for<Tin, Tout, 32, false, CK>(a, p);
@@ -702,8 +720,17 @@ ssm_status_t dispatch(ScanArgs& a, ssm_dtype_t in_dtype, bool tma, cudaStream_t 
     a.flags = reinterpret_cast<uint32_t*>(ws + sizeof(WsHeader));
     const size_t flag_bytes = round256(sizeof(uint32_t) * (size_t)(p.nchunks - 1) * p.nblocks);
     a.carry = reinterpret_cast<float*>(ws + sizeof(WsHeader) + flag_bytes);
-    if (cudaMemsetAsync(ws, 0, sizeof(WsHeader) + flag_bytes, stream) != cudaSuccess)
+    // the ticket, the status word (unless an earlier call's status is being
+    // accumulated) and the flags start at zero
+    if (keep_status) {
+        if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), stream) != cudaSuccess ||
+            cudaMemsetAsync(ws + 2 * sizeof(uint32_t), 0,
+                            sizeof(WsHeader) - 2 * sizeof(uint32_t) + flag_bytes,
+                            stream) != cudaSuccess)
+            return SSM_ERR_CUDA;
+    } else if (cudaMemsetAsync(ws, 0, sizeof(WsHeader) + flag_bytes, stream) != cudaSuccess) {
         return SSM_ERR_CUDA;
+    }
 
     CUtensorMap maps[5];
     memset(maps, 0, sizeof(maps));
@@ -772,7 +799,8 @@ ssm_status_t scan_fwd_entry(const void* u, const void* delta, const float* A, co
                             int delta_softplus, const float* initial_state, void* y,
                             float* final_state, float* ckpt, int batch, int dim, int seqlen,
                             int dstate, int ngroups, ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
-                            void* workspace, size_t workspace_bytes, void* stream) {
+                            void* workspace, size_t workspace_bytes, void* stream,
+                            int seg_ts = 0, bool keep_status = false) {
     using namespace ssm_host;
     if (batch < 0 || dim < 0 || seqlen < 0 || ngroups < 1 || dstate < 1) return SSM_ERR_SHAPE;
     if (dim % ngroups != 0) return SSM_ERR_SHAPE;
@@ -829,6 +857,27 @@ ssm_status_t scan_fwd_entry(const void* u, const void* delta, const float* A, co
     for (const R& r : ins)
         if (overlaps(workspace, need, r.p, r.n)) return SSM_ERR_ALIAS;
 
+    if (use_seg_path(batch, dim)) {
+        const uint32_t lim = g_flag_spin_limit.load(std::memory_order_relaxed);
+        const ssm_status_t st = ssm_internal::scan_seg_forward(
+            u, delta, A, B, C, D, z, delta_bias, delta_softplus, initial_state, y, final_state,
+            batch, dim, seqlen, ngroups, in_dtype, out_dtype, workspace,
+            lim ? lim : kFlagSpinLimit, g_drop_first_publish.load(std::memory_order_relaxed),
+            seg_ts, keep_status, s);
+        if (st != SSM_OK || !ckpt) return st;
+        // the checkpoints from the chained scan's states-only pass; y and
+        // final_state stay the sequence-parallel scan's, as ssm_scan_fwd gives
+        ScanArgs c{};
+        c.u = u; c.delta = delta; c.z = nullptr; c.A = A; c.Dskip = nullptr; c.bias = delta_bias;
+        c.h0 = initial_state; c.y = nullptr; c.final_state = nullptr; c.Bm = B; c.Cm = C;
+        c.ckpt = ckpt; c.batch = batch; c.dim = dim; c.seqlen = seqlen; c.ngroups = ngroups;
+        c.dpg = dim / ngroups; c.softplus = delta_softplus ? 1 : 0;
+        const bool tma_c = ((size_t)seqlen * es) % 16 == 0;
+        return in_dtype == SSM_BF16
+                   ? dispatch<__nv_bfloat16, float, 2>(c, in_dtype, tma_c, s, workspace, true)
+                   : dispatch<float, float, 2>(c, in_dtype, tma_c, s, workspace, true);
+    }
+
     ScanArgs a{};
     a.u = u; a.delta = delta; a.z = z; a.A = A; a.Dskip = D; a.bias = delta_bias;
     a.h0 = initial_state; a.y = y; a.final_state = final_state; a.Bm = B; a.Cm = C; a.ckpt = ckpt;
@@ -839,19 +888,36 @@ ssm_status_t scan_fwd_entry(const void* u, const void* delta, const float* A, co
     const bool tma = ((size_t)seqlen * es) % 16 == 0;
     if (in_dtype == SSM_BF16) {
         return out_dtype == SSM_BF16
-                   ? (ckpt ? dispatch<__nv_bfloat16, __nv_bfloat16, true>(a, in_dtype, tma, s, workspace)
-                           : dispatch<__nv_bfloat16, __nv_bfloat16>(a, in_dtype, tma, s, workspace))
-                   : (ckpt ? dispatch<__nv_bfloat16, float, true>(a, in_dtype, tma, s, workspace)
-                           : dispatch<__nv_bfloat16, float>(a, in_dtype, tma, s, workspace));
+                   ? (ckpt ? dispatch<__nv_bfloat16, __nv_bfloat16, true>(a, in_dtype, tma, s, workspace, keep_status)
+                           : dispatch<__nv_bfloat16, __nv_bfloat16>(a, in_dtype, tma, s, workspace, keep_status))
+                   : (ckpt ? dispatch<__nv_bfloat16, float, true>(a, in_dtype, tma, s, workspace, keep_status)
+                           : dispatch<__nv_bfloat16, float>(a, in_dtype, tma, s, workspace, keep_status));
     }
     if (out_dtype == SSM_BF16)
-        return ckpt ? dispatch<float, __nv_bfloat16, true>(a, in_dtype, tma, s, workspace)
-                    : dispatch<float, __nv_bfloat16>(a, in_dtype, tma, s, workspace);
-    return ckpt ? dispatch<float, float, true>(a, in_dtype, tma, s, workspace)
-                : dispatch<float, float>(a, in_dtype, tma, s, workspace);
+        return ckpt ? dispatch<float, __nv_bfloat16, true>(a, in_dtype, tma, s, workspace, keep_status)
+                    : dispatch<float, __nv_bfloat16>(a, in_dtype, tma, s, workspace, keep_status);
+    return ckpt ? dispatch<float, float, true>(a, in_dtype, tma, s, workspace, keep_status)
+                : dispatch<float, float>(a, in_dtype, tma, s, workspace, keep_status);
 }
 
 }  // namespace
+
+namespace ssm_internal {
+
+ssm_status_t scan_forward_segment(const void* u, const void* delta, const float* A, const void* B,
+                                  const void* C, const float* D, const void* z,
+                                  const float* delta_bias, int delta_softplus,
+                                  const float* initial_state, void* y, float* final_state,
+                                  int batch, int dim, int seqlen, int ngroups,
+                                  ssm_dtype_t in_dtype, ssm_dtype_t out_dtype, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream, int seg_ts,
+                                  bool keep_status) {
+    return scan_fwd_entry(u, delta, A, B, C, D, z, delta_bias, delta_softplus, initial_state, y,
+                          final_state, nullptr, batch, dim, seqlen, kN, ngroups, in_dtype,
+                          out_dtype, workspace, workspace_bytes, stream, seg_ts, keep_status);
+}
+
+}  // namespace ssm_internal
 
 extern "C" ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const float* A,
                                      const void* B, const void* C, const float* D, const void* z,
@@ -898,19 +964,49 @@ constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
+// cuCtxGetCurrent, fetched from the driver through the runtime (the library
+// has no link-time dependency on libcuda).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    return fn;
+}
+
 // Device address of g_noalloc_scratch on the current device.  In host code
 // the symbol names a host-side shadow, not device memory, so the address is
-// looked up once per device with that device current, then cached.
+// looked up with the device current (cudaGetSymbolAddress) and cached per
+// device.  The cache is keyed by the device's current context too: after a
+// cudaDeviceReset the device gets a new context, the library's module is
+// loaded again at a new address, and the first call in the new context looks
+// the address up again.
 void* noalloc_scratch_address() {
     static std::mutex m;
     static void* addr[128] = {};
+    static CUcontext ctx_of[128] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+    CtxGetCurrentFn get = ctx_get_current_fn();
+    CUcontext ctx = nullptr;
+    if (!get || get(&ctx) != CUDA_SUCCESS) return nullptr;
     std::lock_guard<std::mutex> lk(m);
-    if (!addr[dev]) {
+    if (!ctx || !addr[dev] || ctx_of[dev] != ctx) {
+        // the look-up also makes the device's primary context current when no
+        // context was yet; the context is read again after it
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        if (get(&ctx) != CUDA_SUCCESS || !ctx) return nullptr;
         addr[dev] = p;
+        ctx_of[dev] = ctx;
     }
     return addr[dev];
 }
@@ -978,6 +1074,19 @@ extern "C" ssm_status_t ssm_scan_fwd_noalloc(const void* u, const void* delta, c
     void* scratch = noalloc_scratch_address();
     if (!scratch) return SSM_ERR_CUDA;
 
+    if (use_seg_path(batch, dim)) {
+        if (ssm_internal::scan_seg_workspace_bytes(batch, dim, seqlen, ngroups) >
+            kNoAllocScratchBytes)
+            return SSM_ERR_WORKSPACE;
+        const uint32_t lim = g_flag_spin_limit.load(std::memory_order_relaxed);
+        return ssm_internal::scan_seg_forward(u, delta, A, B, C, D, z, delta_bias,
+                                              delta_softplus, initial_state, y, final_state,
+                                              batch, dim, seqlen, ngroups, in_dtype, out_dtype,
+                                              scratch, lim ? lim : kFlagSpinLimit,
+                                              g_drop_first_publish.load(std::memory_order_relaxed),
+                                              0, false, s);
+    }
+
     ScanArgs a{};
     a.u = u; a.delta = delta; a.z = z; a.A = A; a.Dskip = D; a.bias = delta_bias;
     a.h0 = initial_state; a.y = y; a.final_state = final_state; a.Bm = B; a.Cm = C;
@@ -1003,6 +1112,27 @@ extern "C" ssm_status_t ssm_scan_fwd_noalloc(const void* u, const void* delta, c
     }
     return out_dtype == SSM_BF16 ? dispatch<float, __nv_bfloat16>(a, in_dtype, tma, s, scratch)
                                  : dispatch<float, float>(a, in_dtype, tma, s, scratch);
+}
+
+extern "C" ssm_status_t ssm_noalloc_last_status(void* stream) {
+    void* scratch = noalloc_scratch_address();
+    if (!scratch) return SSM_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the status word is the second 32-bit word of the scratch header, in
+    // both scan paths' layouts; read into the host's stack (pageable)
+    uint32_t hdr[2] = {0, 0};
+    if (cudaMemcpyAsync(hdr, scratch, sizeof(hdr), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SSM_ERR_CUDA;
+    return hdr[1] == 0 ? SSM_OK : static_cast<ssm_status_t>(hdr[1]);
+}
+
+extern "C" ssm_status_t ssm_debug_set_scan_path(int path, int segments) {
+    if (path < 0 || path > 2) return SSM_ERR_SHAPE;
+    if (segments != 0 && segments != 8 && segments != 16 && segments != 32) return SSM_ERR_SHAPE;
+    g_scan_path.store(path, std::memory_order_relaxed);
+    ssm_internal::scan_seg_debug_force_ts(segments);
+    return SSM_OK;
 }
 
 extern "C" ssm_status_t ssm_debug_set_lookback(int drop_first_publish, unsigned int spin_limit) {

@@ -21,6 +21,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "scan_internal.h"
 
 namespace {
 
@@ -42,9 +43,11 @@ size_t r256(size_t x) { return (x + 255) & ~size_t(255); }
 
 Plan plan_for(int batch, int dim, int seqlen, int ngroups, size_t es, size_t eo) {
     Plan p{};
-    // about eight segments, each a multiple of 64 steps (16-byte rows for TMA)
+    // about eight segments, each a multiple of 128 steps (16-byte rows for
+    // TMA, and the sequence-parallel scan's chunk boundaries where the whole
+    // sequence's scan has them)
     const int want = (seqlen + 7) / 8;
-    p.seg = std::max(64, (want + 63) / 64 * 64);
+    p.seg = std::max(128, (want + 127) / 128 * 128);
     p.seg = std::min(p.seg, std::max(seqlen, 1));
     p.nseg = seqlen > 0 ? (seqlen + p.seg - 1) / p.seg : 0;
     const size_t rows = (size_t)batch * dim, bcrows = (size_t)batch * ngroups * kN;
@@ -183,6 +186,7 @@ extern "C" ssm_status_t ssm_scan_fwd_host(const void* u, const void* delta, cons
         return ok ? SSM_OK : SSM_ERR_CUDA;
     }
     const size_t L = (size_t)seqlen, bcrows = (size_t)batch * ngroups * kN;
+    const int seg_ts = ssm_internal::scan_seg_plan_ts(batch, dim, seqlen);
     ssm_status_t rc = SSM_OK;
     for (int k = 0; k < pl.nseg && ok && rc == SSM_OK; ++k) {
         const int sl = k % kSlots;
@@ -212,9 +216,12 @@ extern "C" ssm_status_t ssm_scan_fwd_host(const void* u, const void* delta, cons
         if (k >= kSlots) chk(cudaStreamWaitEvent(s, q->ev_out[sl], 0));
         if (!ok) break;
         const float* st_in = k == 0 ? (initial_state ? fsb[1] : nullptr) : fsb[(k - 1) % 2];
-        rc = ssm_scan_fwd(du, dd, A, dB, dC, D, z ? dz : nullptr, delta_bias, delta_softplus, st_in,
-                          dy, fsb[k % 2], batch, dim, (int)Lk, kN, ngroups, in_dtype, out_dtype,
-                          scan_ws, pl.scan_ws, s);
+        // every segment with the whole sequence's plan; the status word keeps
+        // the first timeout of any segment
+        rc = ssm_internal::scan_forward_segment(
+            du, dd, A, dB, dC, D, z ? dz : nullptr, delta_bias, delta_softplus, st_in, dy,
+            fsb[k % 2], batch, dim, (int)Lk, ngroups, in_dtype, out_dtype, scan_ws, pl.scan_ws, s,
+            seg_ts, k > 0);
         chk(cudaEventRecord(q->ev_comp[sl], s));
         // segment k's y back to the host
         chk(cudaStreamWaitEvent(q->copy_out, q->ev_comp[sl], 0));

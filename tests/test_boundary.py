@@ -45,6 +45,44 @@ def test_lookback_debug_hook_is_host_only(L):
     assert L.ssm_debug_set_lookback(0, 0) == OK
 
 
+def test_scan_path_debug_hook_is_host_only(L):
+    # the forward scan's kernel choice, a process-wide setting read at enqueue
+    # time; out-of-range values are rejected
+    for path, segs in ((1, 0), (2, 8), (2, 16), (2, 32), (0, 0)):
+        assert L.ssm_debug_set_scan_path(path, segs) == OK
+    assert L.ssm_debug_set_scan_path(3, 0) == SHAPE
+    assert L.ssm_debug_set_scan_path(-1, 0) == SHAPE
+    assert L.ssm_debug_set_scan_path(2, 12) == SHAPE
+    assert L.ssm_debug_set_scan_path(0, 0) == OK
+
+
+def _t(*shape, dtype=None):
+    import torch
+    return torch.empty(shape, dtype=dtype or torch.float32)
+
+
+def test_binding_rejects_mismatched_scan_shapes():
+    """Every tensor handed to a scan entry point is checked against u's
+    (batch, dim, seqlen), A's dstate and B's ngroups before the C call, so a
+    short buffer can never be read or written past its end (pure shape
+    logic: CPU tensors, no call reaches the library)."""
+    b, d, l, n, g = 2, 8, 20, 16, 2
+    good = dict(u=_t(b, d, l), delta=_t(b, d, l), A=_t(d, n), B=_t(b, g, n, l), C=_t(b, g, n, l),
+                D=_t(d), z=_t(b, d, l), delta_bias=_t(d), initial_state=_t(b, d, n),
+                y=_t(b, d, l), final_state=_t(b, d, n))
+    assert binding._scan_shapes(**good) == (b, d, l, n, g)
+    bad = {"delta": _t(b, d, l - 1), "A": _t(d + 1, n), "B": _t(b, g, n, l + 1),
+           "C": _t(b, 1, n, l), "D": _t(d - 1), "z": _t(b, d + 1, l), "delta_bias": _t(2 * d),
+           "initial_state": _t(b, d, n - 1), "y": _t(b, d, l - 5), "final_state": _t(1, d, n)}
+    for name, t in bad.items():
+        with pytest.raises(ValueError, match=name):
+            binding._scan_shapes(**{**good, name: t})
+    with pytest.raises(ValueError, match="dy"):
+        binding._scan_shapes(**good, dy=_t(b, d, 1))
+    with pytest.raises(ValueError, match="dfinal_state"):
+        binding._scan_shapes(**good, dfinal_state=_t(b, 1, n))
+
+
 def test_version_and_status_strings(L):
     assert binding.ssm_abi_version() == 4
     for code in range(10):
@@ -62,6 +100,9 @@ def test_workspace_bytes_pure_function():
     assert f(-1, 10, 5) == 0
     # grows with the problem
     assert f(4, 5120, 16384) > f(8, 1536, 2048)
+    # few channels and many 128-step chunks: room for the sequence-parallel
+    # scan's flags, aggregates and inclusive states of every chunk
+    assert f(1, 64, 1024) >= 256 + 8 * 64 * (2 * 16 + 16) * 4
 
 
 # fake, 16-byte aligned device addresses, far apart (never dereferenced)

@@ -64,3 +64,29 @@ def test_lookback_custom_limit_without_withheld_publish_is_clean():
         binding.ssm_debug_set_lookback()
     assert status == OK
     assert torch.equal(y, y_ref) and torch.equal(fs, fs_ref)
+
+
+def test_seqpar_lookback_wait_runs_out_and_reports_timeout():
+    """The sequence-parallel scan's look-back: chunk 0 withholds its inclusive
+    state, so chunk 1 polls a flag that never reaches it; the bounded wait
+    records SSM_ERR_TIMEOUT and the kernel finishes; the next scan on the same
+    context gives the clean run's bits."""
+    batch, dim, seqlen = 1, 64, 1024  # 64 channels: the sequence-parallel scan, 8 chunks
+    x = inputs.scan_inputs(batch, dim, seqlen, 16, 1, "f32", seed=152, device="cuda")
+    ws = torch.empty(binding.ssm_scan_workspace_bytes(batch, dim, seqlen, 16, 1),
+                     dtype=torch.uint8, device="cuda")
+    y_ref, fs_ref = _scan(x, ws)
+    assert binding.ssm_last_device_status(ws) == OK
+    try:
+        binding.ssm_debug_set_lookback(True, 2000)
+        t0 = time.perf_counter()
+        _scan(x, ws)
+        status = binding.ssm_last_device_status(ws)
+        elapsed = time.perf_counter() - t0
+    finally:
+        binding.ssm_debug_set_lookback()
+    assert status == TIMEOUT
+    assert elapsed < 0.5, elapsed
+    y, fs = _scan(x, ws)
+    assert binding.ssm_last_device_status(ws) == OK
+    assert torch.equal(y, y_ref) and torch.equal(fs, fs_ref)

@@ -5,7 +5,7 @@ import torch
 
 import oracle
 from state_space_model_selective_gb300 import binding, inputs
-from tests.helpers import TOL_BF16, TOL_F32, assert_close, to64
+from tests.helpers import TOL_BF16, TOL_F32, assert_close, assert_elementwise, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -33,6 +33,26 @@ def _run(inp, out_dtype=torch.float32, initial_state=None, poison=True):
     return y, fs
 
 
+# the forward scan's two kernels (ssm_debug_set_scan_path): the chained scan,
+# and the sequence-parallel scan with its planned or a forced segment count
+PATHS = {"chained": (1, 0), "seqpar": (2, 0), "seqpar8": (2, 8), "seqpar16": (2, 16),
+         "seqpar32": (2, 32)}
+
+
+@pytest.fixture(params=["chained", "seqpar"])
+def path(request):
+    binding.ssm_debug_set_scan_path(*PATHS[request.param])
+    yield request.param
+    binding.ssm_debug_set_scan_path()
+
+
+@pytest.fixture(params=["seqpar8", "seqpar16", "seqpar32"])
+def seg_path(request):
+    binding.ssm_debug_set_scan_path(*PATHS[request.param])
+    yield request.param
+    binding.ssm_debug_set_scan_path()
+
+
 def _oracle(inp, initial_state=None):
     return oracle.scan(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
                        inp["delta_bias"], inp["delta_softplus"], initial_state)
@@ -54,7 +74,7 @@ CASES = [
 
 
 @pytest.mark.parametrize("case", CASES, ids=[f"B{c[0]}D{c[1]}L{c[2]}G{c[3]}{c[4]}" for c in CASES])
-def test_scan_matches_oracle(case):
+def test_scan_matches_oracle(case, path):
     batch, dim, seqlen, ngroups, dt, gate, dskip, softplus = case
     inp = inputs.scan_inputs(batch, dim, seqlen, 16, ngroups, dt, seed=100 + seqlen, gate=gate,
                              dskip=dskip)
@@ -69,7 +89,7 @@ def test_scan_matches_oracle(case):
     assert_close(fs, fs_ref, tol, "final_state")
 
 
-def test_scan_initial_state_and_resume():
+def test_scan_initial_state_and_resume(path):
     """Scanning [0, k) then [k, L) from the first part's final state equals one scan."""
     inp = inputs.scan_inputs(2, 64, 384, 16, 1, "f32", seed=5)
     h0 = torch.randn(2, 64, 16, generator=torch.Generator().manual_seed(1)) * 0.5
@@ -88,7 +108,7 @@ def test_scan_initial_state_and_resume():
     assert_close(f2, fs_ref, TOL_F32, "resumed final_state")
 
 
-def test_scan_bf16_output_is_rounded_fp32_output():
+def test_scan_bf16_output_is_rounded_fp32_output(path):
     inp = inputs.scan_inputs(2, 64, 256, 16, 1, "bf16", seed=9)
     y32, f32 = _run(inp, torch.float32)
     y16, f16 = _run(inp, torch.bfloat16)
@@ -96,14 +116,14 @@ def test_scan_bf16_output_is_rounded_fp32_output():
     assert torch.equal(f16, f32)
 
 
-def test_scan_deterministic():
+def test_scan_deterministic(path):
     inp = inputs.scan_inputs(2, 64, 300, 16, 1, "bf16", seed=11)
     a = _run(inp)
     b = _run(inp)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-def test_scan_empty_and_zero_length():
+def test_scan_empty_and_zero_length(path):
     u = torch.zeros(2, 32, 0, device="cuda")
     A = -torch.ones(32, 16, device="cuda")
     B = torch.zeros(2, 1, 16, 0, device="cuda")
@@ -132,41 +152,119 @@ def test_scan_chained_chunks_many_blocks():
     assert_close(fss, fs_ref, TOL_BF16, "final_state rows")
 
 
+# ------------------------------------------------- sequence-parallel scan
+
+SEG_CASES = [
+    # batch, dim, seqlen, ngroups, dtype: chunk counts 1 .. 41 (more than the
+    # 32 chunks one look-back round examines), ragged last chunks and segments
+    (1, 16, 5200, 1, "f32"),
+    (2, 48, 1500, 3, "bf16"),
+    (3, 20, 777, 1, "f32"),     # odd length: element loads; partial CTAs
+    (1, 8, 4097, 1, "bf16"),    # one step into the 33rd chunk
+    (2, 24, 129, 2, "f32"),     # one step into the second chunk
+    (1, 4, 100, 1, "bf16"),     # a single partial chunk
+]
+
+
+@pytest.mark.parametrize("case", SEG_CASES,
+                         ids=[f"B{c[0]}D{c[1]}L{c[2]}G{c[3]}{c[4]}" for c in SEG_CASES])
+def test_seqpar_lookback_matches_oracle(case, seg_path):
+    """Chunks joined by the decoupled look-back (aggregates composed with the
+    associative operator) and segments joined by the in-warp shuffle scan give
+    the recurrence, for every segment count."""
+    batch, dim, seqlen, ngroups, dt = case
+    inp = inputs.scan_inputs(batch, dim, seqlen, 16, ngroups, dt, seed=300 + seqlen)
+    h0 = torch.randn(batch, dim, 16, generator=torch.Generator().manual_seed(seqlen)) * 0.5
+    y, fs = _run(inp, initial_state=h0)
+    y_ref, fs_ref = _oracle(inp, h0)
+    tol = TOL_F32 if dt == "f32" else TOL_BF16
+    assert_close(y, y_ref, tol, "y")
+    assert_close(fs, fs_ref, tol, "final_state")
+    assert_elementwise(y, y_ref, "y")
+
+
+def test_seqpar_deterministic_and_resumable():
+    """The look-back's result does not depend on which predecessor it stopped
+    at, so repeated runs give the same bits; and a sequence scanned in pieces
+    cut at multiples of 128 steps, each resumed from the previous final state,
+    gives the bits of the whole scan (with the same segment count)."""
+    inp = inputs.scan_inputs(2, 40, 1280, 16, 1, "bf16", seed=321)
+    binding.ssm_debug_set_scan_path(2, 16)
+    try:
+        y, fs = _run(inp)
+        for _ in range(3):
+            y2, fs2 = _run(inp)
+            assert torch.equal(y, y2) and torch.equal(fs, fs2)
+        parts, state, ys = [(0, 384), (384, 1152), (1152, 1280)], None, []
+        for a, b in parts:
+            piece = {k: (v[..., a:b].contiguous() if k in ("u", "delta", "z", "B", "C") else v)
+                     for k, v in inp.items()}
+            yp, state = _run(piece, initial_state=None if state is None else state.cpu())
+            ys.append(yp)
+        assert torch.equal(torch.cat(ys, -1), y)
+        assert torch.equal(state, fs)
+    finally:
+        binding.ssm_debug_set_scan_path()
+
+
+def test_seqpar_and_chained_agree():
+    """Both kernels on one problem: each within the tolerance of the oracle and
+    of each other."""
+    inp = inputs.scan_inputs(2, 64, 1000, 16, 2, "f32", seed=322)
+    out = {}
+    for name in ("chained", "seqpar"):
+        binding.ssm_debug_set_scan_path(*PATHS[name])
+        try:
+            out[name] = _run(inp)
+        finally:
+            binding.ssm_debug_set_scan_path()
+    y_ref, fs_ref = _oracle(inp)
+    for name, (y, fs) in out.items():
+        assert_close(y, y_ref, TOL_F32, f"y ({name})")
+        assert_close(fs, fs_ref, TOL_F32, f"final_state ({name})")
+    assert_close(out["seqpar"][0], out["chained"][0], 2 * TOL_F32, "y, one kernel vs the other")
+
+
 # ------------------------------------------------------------------ workloads
 
-def test_workload_scan_fp32_L128_D1536():
+def test_workload_scan_fp32_L128_D1536(path):
     """Selective scan fp32, batch 1, L 128, 1536 channels, N 16: every output."""
     inp = inputs.scan_inputs(1, 1536, 128, 16, 1, "f32", seed=1001)
     y, fs = _run(inp)
     y_ref, fs_ref = _oracle(inp)
     assert_close(y, y_ref, TOL_F32, "y")
     assert_close(fs, fs_ref, TOL_F32, "final_state")
-
-
-def _sampled_rows(batch, dim, n, seed):
-    rng = np.random.default_rng(seed)
-    rows = {(0, 0), (batch - 1, dim - 1)}
-    while len(rows) < n:
-        rows.add((int(rng.integers(batch)), int(rng.integers(dim))))
-    return sorted(rows)
+    assert_elementwise(y, y_ref, "y")
 
 
 @pytest.mark.parametrize("shape,seed", [((8, 1536, 2048), 1002), ((4, 5120, 16384), 1003)],
                          ids=["B8_D1536_L2048", "B4_D5120_L16384"])
-def test_workload_scan_bf16_sampled(shape, seed):
-    """Full-size bf16 workloads, launched as the benchmark launches them;
-    sampled (batch, channel) rows checked against the oracle."""
+def test_workload_scan_bf16_whole(shape, seed):
+    """Full-size bf16 workloads, launched as the benchmark launches them; every
+    output element checked against the oracle, one batch row at a time (the
+    oracle's fp64 copies of a whole 5.4e9-element workload would not fit in
+    host memory comfortably)."""
     batch, dim, seqlen = shape
     inp = inputs.scan_inputs(batch, dim, seqlen, 16, 1, "bf16", seed=seed)
     y, fs = _run(inp, poison=False)
-    rows = _sampled_rows(batch, dim, 24, seed)
-    y_ref, fs_ref = oracle.scan_rows(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], rows,
-                                     inp["D"], inp["z"], inp["delta_bias"], True)
-    ys = torch.stack([y[b, d] for b, d in rows])
-    fss = torch.stack([fs[b, d] for b, d in rows])
-    assert_close(ys, y_ref, TOL_BF16, "y rows")
-    assert_close(fss, fs_ref, TOL_BF16, "final_state rows")
-    assert torch.isfinite(y).all() and torch.isfinite(fs).all()
+    num_y = den_y = num_f = den_f = 0.0
+    ew = 0.0
+    for b in range(batch):
+        sl = slice(b, b + 1)
+        y_ref, fs_ref = oracle.scan(inp["u"][sl], inp["delta"][sl], inp["A"], inp["B"][sl],
+                                    inp["C"][sl], inp["D"], inp["z"][sl], inp["delta_bias"], True)
+        yb, fb = to64(y[sl]), to64(fs[sl])
+        assert np.isfinite(yb).all() and np.isfinite(fb).all()
+        num_y = max(num_y, float(np.max(np.abs(yb - y_ref))))
+        den_y = max(den_y, float(np.max(np.abs(y_ref))))
+        num_f = max(num_f, float(np.max(np.abs(fb - fs_ref))))
+        den_f = max(den_f, float(np.max(np.abs(fs_ref))))
+        ew = max(ew, assert_elementwise(yb, y_ref, f"y batch row {b}"))
+        del y_ref, yb
+    print(f"normwise y {num_y / den_y:.3e}, final_state {num_f / den_f:.3e}, "
+          f"element-wise y {ew:.3e}")
+    assert num_y / den_y <= TOL_BF16, num_y / den_y
+    assert num_f / den_f <= TOL_BF16, num_f / den_f
 
 
 @pytest.mark.parametrize("case", [(2, 64, 700, 1, "bf16", torch.float32, True),
