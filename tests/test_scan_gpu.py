@@ -139,6 +139,34 @@ def test_scan_empty_and_zero_length(path):
     assert y.shape == (0, 32, 10)
 
 
+WIDE_CASES = [
+    # batch, dim, seqlen, ngroups, dtype, with initial state: a few hundred
+    # 32-channel blocks of the chained scan, every output checked
+    (2, 3840, 333, 2, "bf16", True),   # odd bf16 length: the plain-load path
+    (1, 7680, 1000, 1, "f32", False),  # TMA rows, ragged last tile
+    (3, 2560, 520, 4, "bf16", True),   # groups, 8 full tiles + 8 steps
+]
+
+
+@pytest.mark.parametrize("case", WIDE_CASES,
+                         ids=[f"B{c[0]}D{c[1]}L{c[2]}G{c[3]}{c[4]}" for c in WIDE_CASES])
+def test_scan_many_channels_match_oracle(case):
+    """The chained scan on thousands of channels: every output against the
+    oracle, and bf16 y exactly the fp32 y rounded."""
+    batch, dim, seqlen, ngroups, dt, with_h0 = case
+    inp = inputs.scan_inputs(batch, dim, seqlen, 16, ngroups, dt, seed=400 + seqlen)
+    h0 = (torch.randn(batch, dim, 16, generator=torch.Generator().manual_seed(4)) * 0.5
+          if with_h0 else None)
+    y, fs = _run(inp, initial_state=h0)
+    y_ref, fs_ref = _oracle(inp, h0)
+    tol = TOL_F32 if dt == "f32" else TOL_BF16
+    assert_close(y, y_ref, tol, "y")
+    assert_close(fs, fs_ref, tol, "final_state")
+    assert_elementwise(y, y_ref, "y")
+    y16, fs16 = _run(inp, torch.bfloat16, initial_state=h0)
+    assert torch.equal(y16, y.to(torch.bfloat16)) and torch.equal(fs16, fs)
+
+
 def test_scan_chained_chunks_many_blocks():
     """Enough channel blocks that L is cut into chained chunks across CTAs."""
     inp = inputs.scan_inputs(4, 4096, 512, 16, 1, "bf16", seed=21)
