@@ -1,11 +1,17 @@
 """Benchmark of the selective-scan hot path on GB300.
 
-Workload (one "step"): one ssm_scan_fwd over the bf16 selective-scan
-workload batch 8, L 2048, 1536 channels, N 16 (z gate and softplus on,
-final_state returned, y in fp32), inputs resident in HBM.  Metric: scan
-elements per second, B*L*D*N / time, whole job.
+Workload (one "step"): one ssm_scan_fwd over the long-sequence bf16
+selective-scan workload batch 4, L 16384, 5120 channels, N 16, one B/C group
+(z gate and softplus on, final_state returned, y in fp32), inputs resident in
+HBM.  Metric: scan elements per second, B*L*D*N / time, whole job.
+`other_paths` adds the other workloads' device times against their rooflines:
+the scan at batch 8, L 2048, 1536 channels and at batch 1, L 128, 1536
+channels (fp32; launch-latency bound, timed as CUDA-graph replays), the
+chunked SSD, the decode steps, the Mamba-3 forms and the gradients.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+        python bench.py --profile NAME [--reps R]   (one workload, for ncu)
+        python bench.py --peaks                     (arithmetic-unit probes)
 Under torchrun each rank runs its own copy of the workload on its GPU
 (independent problems, no collective on the data path: weak scaling); the
 timed region is bracketed by barriers and the slowest rank's time is used.
@@ -28,24 +34,23 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-BATCH, DIM, SEQLEN, DSTATE, NGROUPS = 8, 1536, 2048, 16, 1
+BATCH, DIM, SEQLEN, DSTATE, NGROUPS = 4, 5120, 16384, 16, 1
 METRIC = "scan elements/s (B*L*D*N per s)"
 UNIT = "elements/s"
-WORKLOAD = ("selective scan, bf16 inputs / fp32 state / fp32 y, batch 8, L 2048, "
-            "D 1536, N 16, z gate + softplus(delta + bias), final_state")
+WORKLOAD = ("selective scan, bf16 inputs / fp32 state / fp32 y, batch 4, L 16384, "
+            "D 5120, N 16, 1 B/C group, z gate + softplus(delta + bias), final_state")
 
 # Roofline of the scan kernel: multi-function-unit (MUFU) bound.  Per
 # element (b, l, d, n) one exp2; per (b, l, d) two MUFU ops for softplus
 # (ex2, rcp) and two for the silu gate (ex2, rcp).  Peak = 152 SMs x 32 MUFU
-# results per clock (the ex2 rate measured on GB300 by
-# state_space_model_selective_gb300.peaks: 31.4 per SM per clock) x 2070 MHz
-# (maximum SM clock).
+# results per clock (the ex2 rate measured on GB300 by `bench.py --peaks`:
+# 31.7 per SM per clock) x 2070 MHz (maximum SM clock).
 SMS, MUFU_PER_CLK, SM_MAX_MHZ = 152, 32, 2070.0
 HBM_PEAK_GBS = 6778.0  # measured copy bandwidth of the GB300s
 BF16_PEAK_TFLOPS = 1908.5  # measured cuBLAS bf16 GEMM burst rate of the GB300s
 MUFU_PEAK_GOPS = SMS * MUFU_PER_CLK * SM_MAX_MHZ * 1e6 / 1e9
 # FP32 pipe: 128 lane-operations per SM per clock (FFMA rate measured by
-# state_space_model_selective_gb300.peaks: 123 per SM per clock).
+# `bench.py --peaks`: 121 per SM per clock).
 FP32_PER_CLK = 128
 FP32_PEAK_GOPS = SMS * FP32_PER_CLK * SM_MAX_MHZ * 1e6 / 1e9
 # The scan gradient's arithmetic per element (b, l, d, n), counted on the FP32
@@ -53,10 +58,11 @@ FP32_PEAK_GOPS = SMS * FP32_PER_CLK * SM_MAX_MHZ * 1e6 / 1e9
 # (lambda += dy0 C, lambda *= a, and dl*A for a), dC (dy0 h), dB (lambda dl u),
 # dA (lambda h_{t-1} a, times dl), d dl (two FMAs), du (one FMA): 12 ops.
 SCAN_BWD_FP32_PER_ELEMENT = 12
-# DRAM bytes per launch of the scan kernel from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum = 152.3 MB + 67.1 MB) of this
-# kernel build on this workload; None whenever the kernel has changed since.
-SCAN_TRAFFIC_BYTES = 219351296
+# DRAM bytes per launch of the scan kernel on this workload, from one ncu
+# capture (dram__bytes_read.sum + dram__bytes_write.sum) of the same kernel
+# build on batch 4, L 4096, 5120 channels (a quarter of the sequence, the same
+# channel blocks), scaled by 4; None whenever the kernel has changed since.
+SCAN_TRAFFIC_BYTES = 3284400000  # (513.23 MB + 307.87 MB) x 4
 
 
 def algorithmic_counts():
@@ -317,7 +323,7 @@ def run_ours(args):
             "config": {"workload": WORKLOAD, "batch": BATCH, "seqlen": SEQLEN, "dim": DIM,
                        "dstate": DSTATE, "ngroups": NGROUPS, "in_dtype": "bf16",
                        "state_dtype": "f32", "out_dtype": "f32",
-                       "l2": "inputs 152 MB > 129 MB L2 (no flush)",
+                       "l2": "inputs 2.0 GB > 129 MB L2 (no flush)",
                        "parallelism": f"independent workload per GPU x{world}"},
             "e2e": {"value": e2e_total / (e2e_ms / 1e3), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -365,7 +371,8 @@ def measure_other_paths(dev, reps=20):
                      "frac": nbytes / (ms / 1e3) / 1e9 / HBM_PEAK_GBS,
                      "algorithmic_bytes": nbytes}}
     del inp
-    res["ssm_scan_fwd_long"] = _measure_scan_long(dev, reps)
+    res["ssm_scan_fwd_b8_l2048"] = _measure_scan(dev, 8, 1536, 2048, "bf16", reps)
+    res["ssm_scan_fwd_b1_l128_f32"] = _measure_scan(dev, 1, 1536, 128, "f32", reps, graph=True)
     res["ssm_scan_bwd"] = _measure_scan_bwd(dev, reps)
     res["ssd_chunked_bwd"] = _measure_ssd_bwd(dev, reps)
     res["ssd_mamba3_bwd"] = _measure_mamba3_bwd(dev, reps)
@@ -467,16 +474,16 @@ def measure_other_paths(dev, reps=20):
     return res
 
 
-def _measure_scan_long(dev, reps):
-    """The long-sequence scan (bf16 in, fp32 y, batch 4, L 16384, 5120
-    channels, N 16, one B/C group, gate and softplus on): the channel blocks
-    outnumber the resident CTA slots, so the sequence runs as chained L-chunks
-    that hand the state on through the workspace.  Against the MUFU roofline,
-    like the benchmark step."""
+def _measure_scan(dev, batch, dim, seqlen, dt, reps, graph=False):
+    """The forward scan (gate, softplus, final_state, y in fp32) on one of the
+    other scan workloads, against the MUFU roofline like the benchmark step.
+    With graph=True (the 3.1e6-element fp32 workload, whose launch overhead is
+    larger than its work) the calls are captured in a CUDA graph and timed as
+    replays, and the plain back-to-back launch time is reported beside it."""
     import torch
     from state_space_model_selective_gb300 import binding, inputs
-    batch, dim, seqlen = 4, 5120, 16384
-    x = inputs.scan_inputs(batch, dim, seqlen, DSTATE, 1, "bf16", seed=1003, device="cuda")
+    seed = {2048: 1002, 128: 1001}.get(seqlen, 1000)
+    x = inputs.scan_inputs(batch, dim, seqlen, DSTATE, 1, dt, seed=seed, device="cuda")
     y = torch.empty((batch, dim, seqlen), dtype=torch.float32, device=dev)
     fs = torch.empty((batch, dim, DSTATE), dtype=torch.float32, device=dev)
     ws = torch.empty(binding.ssm_scan_workspace_bytes(batch, dim, seqlen, DSTATE, 1),
@@ -487,25 +494,34 @@ def _measure_scan_long(dev, reps):
                              x["delta_bias"], True, out_dtype=torch.float32, y=y,
                              final_state=fs, workspace=ws)
     ms = _time(fwd, reps)
+    out = {}
+    if graph:
+        out["ms_plain_launches"] = ms
+        ms = _time_graph(fwd, 200)
     assert binding.ssm_last_device_status(ws) == 0
     bld = batch * seqlen * dim
     el = bld * DSTATE
     mufu = el + 4 * bld
     achieved = mufu / (ms / 1e3) / 1e9
-    return {"workload": "selective scan bf16 in / fp32 y, batch 4, L 16384, 5120 channels, "
-                        "d_state 16, 1 group, gate, softplus (chained L-chunks)",
-            "ms": ms, "elements_per_s": el / (ms / 1e3),
-            "roofline": {"bound": "alu", "achieved": achieved, "peak": MUFU_PEAK_GOPS,
-                         "unit": "Gop/s (MUFU)", "frac": achieved / MUFU_PEAK_GOPS,
-                         "algorithmic_mufu_ops": mufu}}
+    path = "sequence-parallel scan" if batch * dim <= 3072 else "chained scan"
+    out.update({
+        "workload": f"selective scan {dt} in / fp32 y, batch {batch}, L {seqlen}, {dim} "
+                    f"channels, d_state 16, 1 group, gate, softplus ({path})",
+        "ms": ms, "elements_per_s": el / (ms / 1e3),
+        "timing": "CUDA-graph replay of 200 calls" if graph else f"mean of {reps} launches",
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": MUFU_PEAK_GOPS,
+                     "unit": "Gop/s (MUFU)", "frac": achieved / MUFU_PEAK_GOPS,
+                     "algorithmic_mufu_ops": mufu}})
+    return out
 
 
 def _measure_scan_bwd(dev, reps):
     """The scan gradient (ssm_scan_bwd: checkpointing forward, reverse sweep,
-    reductions) on the benchmark workload (bf16, batch 8, L 2048, 1536
-    channels, d_state 16, D, gate, bias, softplus), against the FP32 pipe."""
+    reductions) on the batch 8, L 2048, 1536-channel scan workload (bf16,
+    d_state 16, D, gate, bias, softplus), against the FP32 pipe."""
     import torch
     from state_space_model_selective_gb300 import binding, inputs
+    BATCH, DIM, SEQLEN = 8, 1536, 2048
     inp = inputs.scan_inputs(BATCH, DIM, SEQLEN, DSTATE, 1, "bf16", seed=1002, device=dev)
     g = torch.Generator(device=dev)
     g.manual_seed(1008)
@@ -702,6 +718,33 @@ def _measure_mimo_bwd(dev, reps):
                          "algorithmic_flops": flops}}
 
 
+def _time_graph(fn, n):
+    """Mean device time per call of fn, captured n times in a CUDA graph and
+    replayed (the launch overhead of single calls removed)."""
+    import torch
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(n):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    times = []
+    with torch.cuda.stream(s):  # the replay runs on the current stream
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1) / n)
+    return statistics.median(times)
+
+
 def _time(fn, reps):
     import torch
     for _ in range(3):
@@ -755,13 +798,247 @@ def run_reference(args):
     return out
 
 
+# ------------------------------------------------------------------ profiling
+
+def _profile_setup(name):
+    """One workload as a callable (inputs drawn on the GPU, seeded), the target
+    of ncu captures: `python bench.py --profile NAME --reps R`."""
+    import torch
+    from state_space_model_selective_gb300 import binding, inputs
+    dev = torch.device("cuda")
+    scans = {"scan": (4, 5120, 16384, "bf16", 1003), "scan_l4096": (4, 5120, 4096, "bf16", 1003),
+             "scan_b8": (8, 1536, 2048, "bf16", 1002), "scan_b1_f32": (1, 1536, 128, "f32", 1001)}
+    if name in scans:
+        B, D, L, dt, seed = scans[name]
+        inp = inputs.scan_inputs(B, D, L, 16, 1, dt, seed=seed, device="cuda")
+        y = torch.empty(B, D, L, device=dev)
+        fs = torch.empty(B, D, 16, device=dev)
+        ws = torch.empty(binding.ssm_scan_workspace_bytes(B, D, L), dtype=torch.uint8, device=dev)
+
+        def fn():
+            binding.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                 inp["z"], inp["delta_bias"], True, out_dtype=torch.float32,
+                                 y=y, final_state=fs, workspace=ws)
+        return fn, lambda: binding.ssm_last_device_status(ws) == 0
+    if name == "ssd":
+        inp = inputs.ssd_inputs(32, 256, 32, 64, 128, 1, "bf16", seed=1004, device="cuda")
+        y = torch.empty(inp["x"].shape, device=dev)
+        fs = torch.empty(32, 32, 64, 128, device=dev)
+
+        def fn():
+            binding.ssd_chunked_fwd(inp["x"], inp["dt"], inp["A_head"], inp["B"], inp["C"], 64,
+                                    out_dtype=torch.float32, y=y, final_state=fs)
+        return fn, None
+    if name == "scan_bwd":
+        B, D, L = 8, 1536, 2048
+        inp = inputs.scan_inputs(B, D, L, 16, 1, "bf16", seed=1002, device="cuda")
+        g = torch.Generator(device=dev)
+        g.manual_seed(1008)
+        dy = torch.randn(B, D, L, device=dev, generator=g).to(torch.bfloat16)
+        ws = torch.empty(binding.ssm_scan_bwd_workspace_bytes(B, D, L), dtype=torch.uint8,
+                         device=dev)
+
+        def fn():
+            binding.ssm_scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], dy,
+                                 inp["D"], inp["z"], inp["delta_bias"], True, workspace=ws)
+        return fn, lambda: binding.ssm_last_device_status(ws) == 0
+    if name in ("ssd_bwd", "m3_bwd", "mimo_bwd"):
+        g = torch.Generator(device=dev)
+        if name == "ssd_bwd":
+            inp = inputs.ssd_inputs(32, 256, 32, 64, 128, 1, "bf16", seed=1004, device="cuda")
+            g.manual_seed(1009)
+            dy = torch.randn(32, 256, 32, 64, device=dev, generator=g).to(torch.bfloat16)
+            ws = torch.empty(binding.ssd_chunked_bwd_workspace_bytes(32, 256, 32),
+                             dtype=torch.uint8, device=dev)
+
+            def fn():
+                binding.ssd_chunked_bwd(inp["x"], inp["dt"], inp["A_head"], inp["B"], inp["C"],
+                                        dy, 64, workspace=ws)
+        elif name == "m3_bwd":
+            m3 = inputs.mamba3_inputs(32, 256, 32, 64, 128, 1, "bf16", seed=1006, device="cuda")
+            g.manual_seed(1010)
+            dy = torch.randn(32, 256, 32, 64, device=dev, generator=g).to(torch.bfloat16)
+            ws = torch.empty(binding.ssd_mamba3_bwd_workspace_bytes(32, 256, 32),
+                             dtype=torch.uint8, device=dev)
+
+            def fn():
+                binding.ssd_mamba3_bwd(m3["x"], m3["dt"], m3["lam"], m3["A_head"], m3["B"],
+                                       m3["C"], dy, 64, m3["h0"], m3["prev_B"], m3["prev_x"],
+                                       workspace=ws)
+        else:
+            m = inputs.mamba3_mimo_inputs(32, 256, 4, 32, 64, 128, 1, "bf16", seed=1007,
+                                          device="cuda")
+            g.manual_seed(1011)
+            dy = torch.randn(32, 256, 4, 32, 64, device=dev, generator=g).to(torch.bfloat16)
+            ws = torch.empty(binding.ssd_mamba3_mimo_bwd_workspace_bytes(32, 256, 4, 32),
+                             dtype=torch.uint8, device=dev)
+
+            def fn():
+                binding.ssd_mamba3_mimo_bwd(m["x"], m["dt"], m["lam"], m["A_head"], m["B"],
+                                            m["C"], dy, 16, m["h0"], m["prev_B"], m["prev_x"],
+                                            workspace=ws)
+        return fn, lambda: binding.ssm_last_device_status(ws) == 0
+    if name == "decode_mimo":
+        g = torch.Generator(device=dev)
+        g.manual_seed(1005)
+        B_, H, P, N, R = 256, 32, 64, 128, 4
+        state = 0.1 * torch.randn(B_, H, P, N, device=dev, generator=g)
+        dt = torch.nn.functional.softplus(torch.randn(B_, H, device=dev, generator=g) - 4)
+        lam = torch.sigmoid(torch.randn(B_, H, device=dev, generator=g))
+        A = -(1 + 15 * torch.rand(H, device=dev, generator=g))
+        D = torch.ones(H, device=dev)
+        xr, xpr = (torch.randn(B_, R, H, P, device=dev, generator=g) for _ in range(2))
+        Br, Cr, Bpr = (torch.randn(B_, R, 1, N, device=dev, generator=g) for _ in range(3))
+        yr = torch.empty_like(xr)
+
+        def fn():
+            binding.ssm_decode_step_mamba3_mimo(state, Bpr, xpr, xr, dt, lam, A, Br, Cr, D, y=yr)
+        return fn, None
+    if name == "decode":
+        inp = inputs.decode_inputs(256, 32, 64, 128, 1, 1, "f32", seed=1005, device="cuda")
+        state = inp["state"]
+
+        def fn():
+            binding.ssm_decode_step(state, inp["x"][0], inp["dt"][0], inp["A"], inp["B"][0],
+                                    inp["C"][0], inp["D"])
+        return fn, None
+    raise SystemExit(f"unknown workload {name!r}")
+
+
+PROFILE_WORKLOADS = ["scan", "scan_l4096", "scan_b8", "scan_b1_f32", "ssd", "decode",
+                     "decode_mimo", "scan_bwd", "ssd_bwd", "m3_bwd", "mimo_bwd"]
+
+
+def run_profile(name, reps):
+    """Runs one workload `reps` times (the process exits non-zero on any error):
+    scan: the benchmark step's scan; scan_l4096: the same channels over L 4096;
+    scan_b8: batch 8, L 2048, 1536 channels; scan_b1_f32: batch 1, L 128, 1536
+    channels, fp32; ssd: chunked SSD batch 32, L 256, 32 heads; decode,
+    decode_mimo: decode steps batch 256, 32 heads; scan_bwd, ssd_bwd, m3_bwd,
+    mimo_bwd: the gradients on those workloads."""
+    import torch
+    fn, check = _profile_setup(name)
+    for _ in range(reps):
+        fn()
+    torch.cuda.synchronize()
+    if check is not None:
+        assert check(), "device-side status not OK"
+    print(f"{name}: {reps} runs ok", flush=True)
+
+
+# ------------------------------------------------------------------ peaks
+
+PEAKS_SRC = os.path.join(ROOT, "bench_peaks.cu")
+PEAKS_LIB = os.path.join(ROOT, "_build", "libbench_peaks.so")
+
+
+def build_peaks(force=False):
+    """Compiles bench_peaks.cu (sm_103a) into _build/libbench_peaks.so."""
+    if not force and os.path.exists(PEAKS_LIB) and \
+            os.path.getmtime(PEAKS_LIB) >= os.path.getmtime(PEAKS_SRC):
+        return PEAKS_LIB
+    import shutil
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    os.makedirs(os.path.dirname(PEAKS_LIB), exist_ok=True)
+    r = subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17",
+                        "-lineinfo", "-Xcompiler", "-fPIC", "-shared", "-o", PEAKS_LIB, PEAKS_SRC,
+                        "-cudart", "static"], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed on bench_peaks.cu:\n{r.stderr}")
+    return PEAKS_LIB
+
+
+def _sm_clock_mhz():
+    import torch
+    try:
+        r = subprocess.run(["nvidia-smi", "--query-gpu=clocks.sm", "--format=csv,noheader,nounits",
+                            f"--id={torch.cuda.current_device()}"],
+                           capture_output=True, text=True, timeout=10)
+        return float(r.stdout.strip().splitlines()[0])
+    except Exception:
+        return None
+
+
+def run_peaks(iters=20000, reps=3):
+    """Per-clock throughput of the units the scan uses, on this GPU: MUFU ex2,
+    fp32 FMA, packed fp32x2 FMA (per SM per clock, the SM clock sampled with
+    nvidia-smi after each probe), the scan's per-step arithmetic mixes
+    (sub-partition cycles per element), shared-load costs, latencies, and the
+    issue-slot sharing of MUFU, FP32 and broadcast loads (cycles per warp-step
+    from clock64)."""
+    import ctypes
+    import torch
+    lib = ctypes.CDLL(build_peaks())
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    sms = props.multi_processor_count
+    out = torch.empty(sms * 8 * 256, device="cuda")
+    cyc = torch.empty(sms * 8, dtype=torch.int64, device="cuda")
+    st = torch.cuda.current_stream()
+    sp, op = vp(st.cuda_stream), vp(out.data_ptr())
+    res = {"sms": sms, "gpu": props.name}
+
+    def timed(launch):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        n = launch()
+        e1.record(st)
+        torch.cuda.synchronize()
+        return n, e0.elapsed_time(e1) / 1e3, _sm_clock_mhz()
+
+    lib.ssm_peak_probe.restype = ctypes.c_double
+    lib.ssm_peak_probe.argtypes = [i] * 4 + [vp, vp]
+    for kind, name, blocks, threads in ((0, "mufu_ex2", sms * 8, 256), (1, "ffma", sms * 8, 256),
+                                        (2, "ffma2_lanes", sms * 8, 256),
+                                        (0, "mufu_ex2_1warp_per_smsp", sms * 4, 32),
+                                        (2, "ffma2_lanes_1warp_per_smsp", sms * 4, 32)):
+        best = None
+        for _ in range(reps):
+            n, sec, mhz = timed(lambda: lib.ssm_peak_probe(kind, blocks, threads, iters, op, sp))
+            if n <= 0:
+                raise RuntimeError("probe launch failed")
+            if best is None or n / sec > best[0]:
+                best = (n / sec, mhz)
+        rate, mhz = best
+        res[name] = {"per_s": rate, "sm_mhz": mhz,
+                     "per_sm_per_clk": rate / sms / (mhz * 1e6) if mhz else None}
+    # the issue-slot sharing of MUFU, FP32 and broadcast shared loads
+    lib.ssm_overlap_probe.restype = i
+    lib.ssm_overlap_probe.argtypes = [i, i, i, vp, vp, vp]
+    names = ["8x(FMUL+MUFU ex2)", "32 FFMA", "16 FFMA2", "8 broadcast LDS.128",
+             "8x(FMUL+MUFU) + 24 FFMA", "8x(FMUL+MUFU) + 12 FFMA2",
+             "8x(FMUL+MUFU) + 24 FFMA + 4 LDS.128", "8x(FMUL+MUFU) + 12 FFMA2 + 8 LDS.128"]
+    ov = {}
+    for wps in (2, 4):
+        for which, nm in enumerate(names):
+            it = 2000
+            lib.ssm_overlap_probe(which, sms * wps, 10, op, vp(cyc.data_ptr()), sp)
+            if not lib.ssm_overlap_probe(which, sms * wps, it, op, vp(cyc.data_ptr()), sp):
+                raise RuntimeError("overlap probe launch failed")
+            torch.cuda.synchronize()
+            mx = int(cyc[:sms * wps].max().item())
+            ov[f"{nm} @ {wps} warps/SMSP"] = mx / (it * 8 * wps)  # cycles per warp-step
+    res["issue_sharing_cycles_per_warp_step"] = ov
+    return res
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__)
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
-    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--profile", choices=PROFILE_WORKLOADS, default=None)
+    p.add_argument("--reps", type=int, default=3)
+    p.add_argument("--peaks", action="store_true")
     args = p.parse_args(argv)
+    if args.profile:
+        return run_profile(args.profile, args.reps)
+    if args.peaks:
+        import torch
+        torch.cuda.init()
+        print(json.dumps(run_peaks()), flush=True)
+        return None
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -1,7 +1,9 @@
-// peaks.cu -- throughput probes for the arithmetic units the selective scan
-// uses (multi-function-unit ex2, fp32 FMA, packed fp32x2 FMA), so that the
+// bench_peaks.cu -- throughput probes for the arithmetic units the selective
+// scan uses (multi-function-unit ex2, fp32 FMA, packed fp32x2 FMA, broadcast
+// shared loads, and how they share the issue slots when mixed), so that the
 // scan's roofline is set against measured per-clock rates on this GPU.
-// Built into its own library (libssm_peaks.so); not part of the ssm.h ABI.
+// A measurement tool of bench.py (`python bench.py --peaks`), built into its
+// own library under _build/; not part of the library or its ABI.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -312,4 +314,95 @@ extern "C" double ssm_peak_probe(int kind, int blocks, int threads, int iters, f
     }
     if (cudaGetLastError() != cudaSuccess) return -1.0;
     return lanes * iters * kChains * (kind == 2 ? 2.0 : 1.0);
+}
+
+// ---------------------------------------------------------------- overlap
+//
+// How the MUFU, the FP32 pipe and broadcast shared loads share a warp
+// scheduler's issue slots.  Per "step" each thread runs, by mode bit:
+//   1: 8 x (FMUL + MUFU ex2) on 8 independent chains
+//   2: NF scalar FFMAs on 16 independent accumulators
+//   4: NF packed fp32x2 FMAs on 8 independent accumulator pairs
+// plus NL warp-uniform (broadcast) 16-byte shared loads.  Returns the SM
+// clocks of the slowest CTA; the caller divides by warp-steps per
+// sub-partition.
+namespace {
+
+__device__ __forceinline__ unsigned long long pk2(float a, float b) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+template <int MODE, int NF, int NL>
+__global__ void __launch_bounds__(128) overlap_probe(float* out, int iters, long long* cyc,
+                                                     float k) {
+    __shared__ float4 sm[64];
+    const int tid = threadIdx.x;
+    if (tid < 64) sm[tid] = make_float4(tid * 0.01f, 0.5f, 0.25f, 0.125f);
+    __syncthreads();
+    const long long c0 = clock64();
+    float m[8], f[16];
+    unsigned long long pv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { m[i] = 0.1f * i + tid * 1e-4f; pv[i] = pk2(0.01f * i, 0.02f * i); }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) f[i] = 0.01f * i;
+    float acc = 0.0f;
+    const unsigned long long k2 = pk2(0.999f, 0.998f), c2 = pk2(1e-3f, 2e-3f);
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            if (MODE & 1) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(m[i]) : "f"(m[i] * k));
+            }
+            if (MODE & 2) {
+#pragma unroll
+                for (int j = 0; j < NF; ++j) f[j & 15] = fmaf(f[j & 15], 0.999f, 1e-3f);
+            }
+            if (MODE & 4) {
+#pragma unroll
+                for (int j = 0; j < NF; ++j)
+                    asm volatile("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(pv[j & 7]) : "l"(k2), "l"(c2));
+            }
+#pragma unroll
+            for (int l = 0; l < NL; ++l) acc += sm[(s * NL + l) & 63].x;
+        }
+    }
+    const long long c1 = clock64();
+    float r = acc;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float a, b;
+        asm("mov.b64 {%0,%1}, %2;" : "=f"(a), "=f"(b) : "l"(pv[i]));
+        r += m[i] + a + b;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) r += f[i];
+    out[blockIdx.x * blockDim.x + tid] = r;
+    if (tid == 0) cyc[blockIdx.x] = c1 - c0;
+}
+
+}  // namespace
+
+// case: 0 MUFU only, 1 FFMA only, 2 FFMA2 only, 3 broadcast loads only,
+// 4 MUFU + 24 FFMA, 5 MUFU + 12 FFMA2, 6 MUFU + 24 FFMA + 4 loads,
+// 7 MUFU + 12 FFMA2 + 8 loads.  blocks: 4 warps each; out: blocks * 128
+// floats; cyc: blocks int64.  Returns 0 on a launch error, else 1.
+extern "C" int ssm_overlap_probe(int which, int blocks, int iters, float* out, long long* cyc,
+                                 void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (which) {
+        case 0: overlap_probe<1, 0, 0><<<blocks, 128, 0, s>>>(out, iters, cyc, 0.5f); break;
+        case 1: overlap_probe<2, 32, 0><<<blocks, 128, 0, s>>>(out, iters, cyc, 0.5f); break;
+        case 2: overlap_probe<4, 16, 0><<<blocks, 128, 0, s>>>(out, iters, cyc, 0.5f); break;
+        case 3: overlap_probe<0, 0, 8><<<blocks, 128, 0, s>>>(out, iters, cyc, 0.5f); break;
+        case 4: overlap_probe<3, 24, 0><<<blocks, 128, 0, s>>>(out, iters, cyc, 0.5f); break;
+        case 5: overlap_probe<5, 12, 0><<<blocks, 128, 0, s>>>(out, iters, cyc, 0.5f); break;
+        case 6: overlap_probe<3, 24, 4><<<blocks, 128, 0, s>>>(out, iters, cyc, 0.5f); break;
+        default: overlap_probe<5, 12, 8><<<blocks, 128, 0, s>>>(out, iters, cyc, 0.5f); break;
+    }
+    return cudaGetLastError() == cudaSuccess ? 1 : 0;
 }

@@ -20,8 +20,6 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libssm.so")
 SOURCES = ["scan.cu", "scan_seg.cu", "scan_bwd.cu", "scan_host.cu", "decode.cu", "ssd.cu", "ssd_bwd.cu",
            "api.cu"]
-PEAKS_SRC = "peaks.cu"
-PEAKS_LIB = os.path.join(PKG, "libssm_peaks.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,
                      "-Xptxas", "-v"]
@@ -58,13 +56,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
             f.write(r.stderr)
         return obj
 
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES) + 1) as ex:
-        objs = list(ex.map(compile_one, SOURCES + [PEAKS_SRC]))
-    peaks_obj = objs.pop()
-    r = subprocess.run([nvcc] + ARCH + ["-shared", "-o", PEAKS_LIB, peaks_obj, "-cudart", "static"],
-                       capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link of libssm_peaks.so failed:\n{r.stderr}")
+    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
