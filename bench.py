@@ -1019,6 +1019,49 @@ def run_peaks(iters=20000, reps=3):
             mx = int(cyc[:sms * wps].max().item())
             ov[f"{nm} @ {wps} warps/SMSP"] = mx / (it * 8 * wps)  # cycles per warp-step
     res["issue_sharing_cycles_per_warp_step"] = ov
+    # the scan's per-step arithmetic from registers (ns states per thread;
+    # scalar, and scalar vs packed fp32x2): sub-partition cycles per element
+    lib.ssm_scan_mix_probe.restype = ctypes.c_double
+    lib.ssm_scan_mix_probe.argtypes = [i] * 4 + [vp, vp]
+    lib.ssm_scan_mix2_probe.restype = ctypes.c_double
+    lib.ssm_scan_mix2_probe.argtypes = [i] * 5 + [vp, vp]
+    mix, mix2 = {}, {}
+    for ns in (4, 8, 16):
+        for wps in (1, 2, 3, 4):
+            steps = 4000
+            lib.ssm_scan_mix_probe(ns, sms * 4 * wps, 32, 100, op, sp)
+            _, sec, mhz = timed(lambda: lib.ssm_scan_mix_probe(ns, sms * 4 * wps, 32, steps, op, sp))
+            mix[f"ns{ns}_{wps}warp_per_smsp"] = sec * (mhz or SM_MAX_MHZ) * 1e6 / steps / (wps * 32 * ns)
+        for packed in (0, 1):
+            for wps in (1, 2, 4):
+                steps = 4000
+                lib.ssm_scan_mix2_probe(ns, packed, sms * 4 * wps, 32, 100, op, sp)
+                _, sec, mhz = timed(lambda: lib.ssm_scan_mix2_probe(ns, packed, sms * 4 * wps, 32,
+                                                                    steps, op, sp))
+                mix2[f"{'x2' if packed else 'f32'}_ns{ns}_{wps}warp_per_smsp"] = \
+                    sec * (mhz or SM_MAX_MHZ) * 1e6 / steps / (wps * 32 * ns)
+    res["scan_step_mix_cycles_per_element"] = mix
+    res["scan_full_mix_cycles_per_element"] = mix2
+    # shared-memory load cost by width and address pattern: SM clocks per
+    # warp-wide load instruction (1 = one 128-byte wavefront per clock)
+    lib.ssm_lds_probe.restype = ctypes.c_double
+    lib.ssm_lds_probe.argtypes = [i] * 5 + [vp, vp]
+    lds = {}
+    pat = {0: "same_addr", 1: "4addr_lane_mod4", 2: "4addr_per_quarter", 3: "32addr"}
+    for width in (4, 8, 16):
+        for pattern in (0, 1, 2, 3):
+            its = 4000
+            lib.ssm_lds_probe(width, pattern, sms * 4, 512, 50, op, sp)
+            n, sec, mhz = timed(lambda: lib.ssm_lds_probe(width, pattern, sms * 4, 512, its, op, sp))
+            lds[f"lds{width * 8}_{pat[pattern]}"] = sec * (mhz or SM_MAX_MHZ) * 1e6 * sms / n
+    res["lds_clocks_per_warp_load"] = lds
+    lib.ssm_latency_probe.restype = ctypes.c_float
+    lib.ssm_latency_probe.argtypes = [i, i, vp, vp]
+    lat = {}
+    for kind, name in ((0, "ex2"), (1, "rcp"), (2, "ffma"), (3, "ffma2"), (4, "lds")):
+        lib.ssm_latency_probe(kind, 64, op, sp)
+        lat[name] = lib.ssm_latency_probe(kind, 2000, op, sp)
+    res["latency_cycles"] = lat
     return res
 
 
