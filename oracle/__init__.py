@@ -68,6 +68,7 @@ def _load():
             lib.oracle_ssd_bwd.argtypes = [dp] * 14 + [i] * 6
             lib.oracle_mamba3_bwd.argtypes = [dp] * 20 + [i] * 6
             lib.oracle_mamba3_mimo_bwd.argtypes = [dp] * 20 + [i] * 7
+            lib.oracle_mamba3_rope.argtypes = [dp] * 8 + [i] * 6
             lib.oracle_combine.argtypes = [ctypes.c_double] * 4 + [dp, dp]
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -434,3 +435,34 @@ def scan_rows(u, delta, A, B, C, rows, D=None, z=None, delta_bias=None,
         out_y.append(y[0, 0])
         out_h.append(h[0, 0])
     return np.stack(out_y), np.stack(out_h)
+
+
+def mamba3_rope(B, C, dt, theta, angle0=None):
+    """Mamba-3's data-dependent RoPE (oracle.c, oracle_mamba3_rope): the angles
+    -cumsum(dt * theta) along the sequence (from angle0), and B, C rotated by
+    them pair by pair, one copy per head.
+
+    B, C: (batch, L, G, N) or, with a rank axis, (batch, L, R, G, N); dt
+    (batch, L, H); theta (batch, L, H, N/2); angle0 (batch, H, N/2) or None.
+    Returns (B_rot, C_rot, angle_out): B_rot, C_rot (batch, L, H, N) or
+    (batch, L, R, H, N), angle_out (batch, H, N/2), all float64.
+    """
+    B, C, dt, theta, angle0 = (_f64(t) for t in (B, C, dt, theta, angle0))
+    siso = B.ndim == 4
+    if siso:
+        B, C = B[:, :, None], C[:, :, None]
+    batch, seqlen, rank, ngroups, dstate = B.shape
+    nheads = dt.shape[2]
+    assert C.shape == B.shape and dstate % 2 == 0 and nheads % ngroups == 0
+    assert dt.shape == (batch, seqlen, nheads)
+    assert theta.shape == (batch, seqlen, nheads, dstate // 2)
+    assert angle0 is None or angle0.shape == (batch, nheads, dstate // 2)
+    B, C = np.ascontiguousarray(B), np.ascontiguousarray(C)
+    Br = np.empty((batch, seqlen, rank, nheads, dstate))
+    Cr = np.empty_like(Br)
+    ang = np.empty((batch, nheads, dstate // 2))
+    _load().oracle_mamba3_rope(_ptr(B), _ptr(C), _ptr(dt), _ptr(theta), _ptr(angle0), _ptr(Br),
+                               _ptr(Cr), _ptr(ang), batch, seqlen, rank, nheads, ngroups, dstate)
+    if siso:
+        Br, Cr = Br[:, :, 0], Cr[:, :, 0]
+    return Br, Cr, ang

@@ -41,6 +41,10 @@
  *       B x = sum_r B[n,r] x[p,r] and y[p,r] = sum_n state[n,p] C[n,r], and the
  *       rank-flattened chunked form with a block-diagonal correction
  *       (oracle_mamba3_mimo_*).
+ *  [P2] same page, "How it works", Phase 1: the angle cumsum
+ *       cum_angles = -cumsum(dt * theta), then RoPE applied to B and C
+ *       (oracle_mamba3_rope; the complex-valued state of the page's feature
+ *       list, "Complex-valued state via data-dependent RoPE").
  *  oracle_scan_bwd: the gradient of the scan above by reverse-mode
  *       differentiation of the same recurrence (the pages mention backward
  *       parity but print no formula; the derivative is pinned by finite
@@ -1305,6 +1309,56 @@ void oracle_mamba3_mimo_bwd(const double* x, const double* dt, const double* lam
     free(carry);
     free(later);
     free(dbx);
+}
+
+/*
+ * oracle_mamba3_rope -- [P2] "How it works", Phase 1: the angle cumsum
+ * cum_angles = -cumsum(dt * theta) along the sequence, then RoPE applied to
+ * B and C.  Readings taken where the page is silent:
+ *  - theta holds one angular rate per (batch, step, head, state pair), so it
+ *    multiplies dt elementwise; the heads of a group rotate the group's B
+ *    and C by their own angles, so the results have one row per head.
+ *  - State pair k is (2k, 2k + 1), rotated as the complex number
+ *    B[2k] + i B[2k+1] times exp(i angle) (the original RoPE pairing).
+ *  - The cumsum is inclusive: step t's angle includes dt_t theta_t.  The
+ *    angle entering the sequence is angle0 (0 when NULL); the angle after the
+ *    last step is written to angle_out (when not NULL), so a resumed prefill
+ *    or a decode step continues the sequence.
+ *  - MIMO: every rank of a step is rotated by the step's angle.
+ * Layouts: B, C [batch][L][R][G][N]; dt [batch][L][H]; theta, the angles
+ * [batch][L][H][N/2] and [batch][H][N/2]; Brot, Crot [batch][L][R][H][N].
+ */
+void oracle_mamba3_rope(const double* Bm, const double* Cm, const double* dt,
+                        const double* theta, const double* angle0, double* Brot, double* Crot,
+                        double* angle_out, int batch, int seqlen, int rank, int nheads,
+                        int ngroups, int dstate)
+{
+    const int half = dstate / 2;
+    const int heads_per_group = nheads / ngroups;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < batch; ++b) {
+        for (int h = 0; h < nheads; ++h) {
+            const int g = h / heads_per_group;
+            for (int k = 0; k < half; ++k) {
+                const size_t ai = ((size_t)b * nheads + h) * half + k;
+                double angle = angle0 ? angle0[ai] : 0.0;
+                for (int t = 0; t < seqlen; ++t) {
+                    const size_t bt = (size_t)b * seqlen + t;
+                    angle -= dt[bt * nheads + h] * theta[(bt * nheads + h) * half + k];
+                    const double c = cos(angle), sn = sin(angle);
+                    for (int r = 0; r < rank; ++r) {
+                        const size_t src = ((bt * rank + r) * ngroups + g) * dstate + 2 * k;
+                        const size_t dst = ((bt * rank + r) * nheads + h) * dstate + 2 * k;
+                        Brot[dst] = Bm[src] * c - Bm[src + 1] * sn;
+                        Brot[dst + 1] = Bm[src] * sn + Bm[src + 1] * c;
+                        Crot[dst] = Cm[src] * c - Cm[src + 1] * sn;
+                        Crot[dst + 1] = Cm[src] * sn + Cm[src + 1] * c;
+                    }
+                }
+                if (angle_out) angle_out[ai] = angle;
+            }
+        }
+    }
 }
 
 int oracle_num_threads(void)

@@ -938,3 +938,128 @@ def test_mimo_bwd_is_linear_in_the_cotangents():
     g3 = oracle.mamba3_mimo_bwd(*args, dy + 2 * dy2, *extra, dfinal + 2 * df2)
     for k in g1:
         np.testing.assert_allclose(g3[k], g1[k] + 2 * g2[k], rtol=1e-11, atol=1e-12, err_msg=k)
+
+
+# ---------------------------------------------------------------- Mamba-3 RoPE
+# "Mamba-3 NKI Kernels for AWS Neuron", section "How it works", Phase 1:
+# cum_angles = -cumsum(dt * theta), then RoPE on B and C; the page's feature
+# list calls the result a complex-valued state.
+
+def _rope_inputs(seed, batch=2, seqlen=11, rank=None, nheads=4, ngroups=2, dstate=6):
+    rng = _rng(seed)
+    shape = ((batch, seqlen, ngroups, dstate) if rank is None
+             else (batch, seqlen, rank, ngroups, dstate))
+    B = rng.normal(size=shape)
+    C = rng.normal(size=shape)
+    dt = rng.uniform(0.02, 0.3, size=(batch, seqlen, nheads))
+    theta = rng.normal(size=(batch, seqlen, nheads, dstate // 2)) * 2.0
+    angle0 = rng.uniform(-3, 3, size=(batch, nheads, dstate // 2))
+    return B, C, dt, theta, angle0
+
+
+def _per_head(X, nheads):
+    """(..., G, N) -> (..., H, N): each head takes its group's row."""
+    ngroups = X.shape[-2]
+    return np.repeat(X, nheads // ngroups, axis=-2)
+
+
+@pytest.mark.parametrize("rank", [None, 3])
+def test_rope_equals_complex_rotation_by_numpy_cumsum(rank):
+    """Each pair (B[2k], B[2k+1]) as the complex number B[2k] + i B[2k+1],
+    multiplied by exp(i phi), phi = angle0 - numpy.cumsum(dt theta) over the
+    steps: written with numpy's complex arithmetic and cumsum, not the
+    oracle's sin/cos loop."""
+    B, C, dt, theta, angle0 = _rope_inputs(21, rank=rank)
+    nheads = dt.shape[2]
+    phi = angle0[:, None] - np.cumsum(dt[..., None] * theta, axis=1)  # (b, L, H, N/2)
+    if rank is not None:
+        phi_r = phi[:, :, None]
+    else:
+        phi_r = phi
+    got_B, got_C, ang = oracle.mamba3_rope(B, C, dt, theta, angle0)
+    for X, got in ((B, got_B), (C, got_C)):
+        Xh = _per_head(X, nheads)
+        z = (Xh[..., 0::2] + 1j * Xh[..., 1::2]) * np.exp(1j * phi_r)
+        np.testing.assert_allclose(got[..., 0::2], z.real, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(got[..., 1::2], z.imag, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(ang, phi[:, -1], rtol=1e-13, atol=1e-13)
+
+
+def test_rope_zero_rate_is_identity_and_keeps_the_angle():
+    B, C, dt, theta, angle0 = _rope_inputs(22)
+    got_B, got_C, ang = oracle.mamba3_rope(B, C, dt, np.zeros_like(theta))
+    np.testing.assert_array_equal(got_B, _per_head(B, dt.shape[2]))
+    np.testing.assert_array_equal(got_C, _per_head(C, dt.shape[2]))
+    np.testing.assert_array_equal(ang, 0.0)
+    _, _, ang = oracle.mamba3_rope(B, C, dt, np.zeros_like(theta), angle0)
+    np.testing.assert_array_equal(ang, angle0)
+
+
+def test_rope_preserves_each_pair_norm():
+    B, C, dt, theta, angle0 = _rope_inputs(23)
+    got_B, _, _ = oracle.mamba3_rope(B, C, dt, theta, angle0)
+    Bh = _per_head(B, dt.shape[2])
+    n_in = Bh[..., 0::2] ** 2 + Bh[..., 1::2] ** 2
+    n_out = got_B[..., 0::2] ** 2 + got_B[..., 1::2] ** 2
+    np.testing.assert_allclose(n_out, n_in, rtol=1e-12)
+
+
+def test_rope_constant_rate_closed_form():
+    """dt theta = w for every step and pair, B = (1, 0) pairs: step t's pair is
+    (cos(-w (t + 1)), sin(-w (t + 1)))."""
+    batch, seqlen, nheads, dstate, w = 1, 9, 2, 4, 0.37
+    B = np.zeros((batch, seqlen, 1, dstate))
+    B[..., 0::2] = 1.0
+    dt = np.full((batch, seqlen, nheads), 0.5)
+    theta = np.full((batch, seqlen, nheads, dstate // 2), w / 0.5)
+    got_B, _, ang = oracle.mamba3_rope(B, B, dt, theta)
+    t = np.arange(1, seqlen + 1)[None, :, None, None]
+    np.testing.assert_allclose(got_B[..., 0::2], np.broadcast_to(np.cos(-w * t), got_B[..., 0::2].shape), atol=1e-13)
+    np.testing.assert_allclose(got_B[..., 1::2], np.broadcast_to(np.sin(-w * t), got_B[..., 1::2].shape), atol=1e-13)
+    np.testing.assert_allclose(ang, -w * seqlen, atol=1e-13)
+
+
+def test_rope_resumes_from_its_final_angle():
+    B, C, dt, theta, angle0 = _rope_inputs(24, seqlen=12)
+    whole_B, whole_C, whole_ang = oracle.mamba3_rope(B, C, dt, theta, angle0)
+    k = 5
+    B1, C1, a1 = oracle.mamba3_rope(B[:, :k], C[:, :k], dt[:, :k], theta[:, :k], angle0)
+    B2, C2, a2 = oracle.mamba3_rope(B[:, k:], C[:, k:], dt[:, k:], theta[:, k:], a1)
+    np.testing.assert_allclose(np.concatenate([B1, B2], 1), whole_B, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(np.concatenate([C1, C2], 1), whole_C, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(a2, whole_ang, rtol=1e-12, atol=1e-12)
+
+
+def _complex_ssm(x, dt, A_head, B, C, theta):
+    """The complex-valued SSM the rotation encodes, written directly: per
+    (batch, head, p) and state pair k, with z_t = B_t[2k] + i B_t[2k+1],
+    H_t = exp(dt_t A + i dt_t theta_t) H_{t-1} + dt_t x_t z_t, and
+    y_t = sum_k Re(conj(c_t) H_t), c_t = C_t[2k] + i C_t[2k+1]."""
+    batch, seqlen, nheads, headdim = x.shape
+    Bh, Ch = _per_head(B, nheads), _per_head(C, nheads)
+    zb = Bh[..., 0::2] + 1j * Bh[..., 1::2]
+    zc = Ch[..., 0::2] + 1j * Ch[..., 1::2]
+    y = np.zeros(x.shape)
+    H = np.zeros((batch, nheads, headdim, zb.shape[-1]), dtype=complex)
+    for t in range(seqlen):
+        eig = np.exp(dt[:, t, :, None] * (A_head[None, :, None] + 1j * theta[:, t]))  # (b, H, N/2)
+        H = eig[:, :, None, :] * H + (dt[:, t, :, None, None] * x[:, t, :, :, None]) * zb[:, t, :, None, :]
+        y[:, t] = np.real(np.sum(np.conj(zc[:, t, :, None, :]) * H, axis=-1))
+    return y
+
+
+def test_rope_then_real_recurrence_is_the_complex_ssm():
+    """The Mamba-2 recurrence (oracle.ssd_recurrence, lambda = 1 of Mamba-3)
+    on the rotated B and C equals the complex-valued SSM with eigenvalues
+    exp(dt (A + i theta)), written out with numpy complex numbers; with a zero
+    initial state the angle the sequence starts from does not matter."""
+    rng = _rng(25)
+    batch, seqlen, nheads, headdim, ngroups, dstate = 2, 13, 4, 3, 2, 6
+    B, C, dt, theta, angle0 = _rope_inputs(25, batch, seqlen, None, nheads, ngroups, dstate)
+    x = rng.normal(size=(batch, seqlen, nheads, headdim))
+    A_head = -rng.uniform(0.5, 2.0, size=nheads)
+    want = _complex_ssm(x, dt, A_head, B, C, theta)
+    for a0 in (None, angle0):
+        Br, Cr, _ = oracle.mamba3_rope(B, C, dt, theta, a0)
+        y, _ = oracle.ssd_recurrence(x, dt, A_head, Br, Cr)
+        np.testing.assert_allclose(y, want, rtol=1e-10, atol=1e-11)

@@ -94,6 +94,24 @@ MUTANTS = {
     "mimo_bwd_prev_unweighted": ("acc += bet0 * later[n] * pBr[n];", "acc += later[n] * pBr[n];"),
     "mimo_bwd_dB_to_rank0": ("dB[BI(bt, r) + n] += dbx[n] * xv;",
                              "dB[BI(bt, 0) + n] += dbx[n] * xv;"),
+    "rope_angle_sign": (
+        'angle -= dt[bt * nheads + h] * theta[(bt * nheads + h) * half + k];',
+        'angle += dt[bt * nheads + h] * theta[(bt * nheads + h) * half + k];'),
+    "rope_drops_dt": (
+        'angle -= dt[bt * nheads + h] * theta[(bt * nheads + h) * half + k];',
+        'angle -= theta[(bt * nheads + h) * half + k];'),
+    "rope_rotation_transposed": (
+        'Brot[dst] = Bm[src] * c - Bm[src + 1] * sn;',
+        'Brot[dst] = Bm[src] * c + Bm[src + 1] * sn;'),
+    "rope_exclusive_cumsum": (
+        '                    angle -= dt[bt * nheads + h] * theta[(bt * nheads + h) * half + k];\n                    const double c = cos(angle), sn = sin(angle);',
+        '                    const double c = cos(angle), sn = sin(angle);\n                    angle -= dt[bt * nheads + h] * theta[(bt * nheads + h) * half + k];'),
+    "rope_wrong_group": (
+        '            const int g = h / heads_per_group;\n            for (int k = 0; k < half; ++k) {',
+        '            const int g = h % ngroups;\n            for (int k = 0; k < half; ++k) {'),
+    "rope_C_not_rotated": (
+        'Crot[dst + 1] = Cm[src] * sn + Cm[src + 1] * c;',
+        'Crot[dst + 1] = Cm[src + 1];'),
     "mamba3_decode_terms_swapped": (
         "s[n] = alpha * s[n] + beta * Bp[n] * xp + gamma * Bt[n] * xv;",
         "s[n] = alpha * s[n] + beta * Bt[n] * xv + gamma * Bp[n] * xp;"),
