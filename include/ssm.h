@@ -9,6 +9,7 @@
  *   ssd_mamba3_fwd, ssm_decode_step_mamba3  the same two for Mamba-3 SISO
  *                    (trapezoidal three-term recurrence)
  *   ssd_mamba3_mimo_fwd, ssm_decode_step_mamba3_mimo  Mamba-3 MIMO (rank R)
+ *   ssm_mamba3_rope  Mamba-3's data-dependent rotation of B and C
  *   ssm_scan_bwd     gradient of ssm_scan_fwd (reverse mode, every input)
  *   ssm_scan_fwd_host  ssm_scan_fwd on host-resident activations, copies pipelined
  *   ssd_chunked_bwd  gradient of ssd_chunked_fwd, tensor cores
@@ -288,6 +289,39 @@ ssm_status_t ssm_decode_step_mamba3_mimo(float* state, const void* prev_B, const
                                          const float* D, const void* z, void* y, int batch,
                                          int rank, int nheads, int headdim, int dstate,
                                          int ngroups, ssm_dtype_t dtype, void* stream);
+
+/*
+ * Mamba-3's data-dependent rotation of B and C.
+ *   "Mamba-3 NKI Kernels for AWS Neuron", section "How it works", Phase 1:
+ *   the angle cumsum cum_angles = -cumsum(dt * theta), then RoPE applied to B
+ *   and C -- the page's "complex-valued state via data-dependent RoPE".
+ *
+ * For every batch b, head h (group g = h / (nheads / ngroups)), state pair
+ * k < dstate / 2, step t and rank r, in fp32:
+ *   angle   = angle0[b,h,k] (0 when angle0 is NULL), then per step
+ *   angle  -= dt[b,t,h] * theta[b,t,h,k]          (inclusive cumsum)
+ *   (B_rot[b,t,r,h,2k], B_rot[b,t,r,h,2k+1]) = the pair (B[b,t,r,g,2k],
+ *       B[b,t,r,g,2k+1]) rotated by angle: (x cos - y sin, x sin + y cos);
+ *   the same for C;  angle_out[b,h,k] = angle after the last step.
+ * The rotated rows are per head, so the SSD and decode entry points take
+ * them with ngroups = nheads.  With seqlen = 1 this is the rotation of one
+ * decode step (angle0 = the previous step's angle_out; angle_out may be
+ * angle0 itself, updated in place).  The angle is a Kahan-compensated fp32
+ * sum: its error stays near one rounding of its value (about 1e-7 |angle|).
+ *
+ * Layouts (dtype for B, C, B_rot, C_rot; everything else fp32):
+ *   B, C            (batch, seqlen, rank, ngroups, dstate)   rank 1 = SISO
+ *   dt              (batch, seqlen, nheads)   already discretised (softplus)
+ *   theta           (batch, seqlen, nheads, dstate / 2)
+ *   angle0, angle_out (batch, nheads, dstate / 2), each may be NULL
+ *   B_rot, C_rot    (batch, seqlen, rank, nheads, dstate)
+ * Supported: any sizes with dstate even, nheads % ngroups == 0, rank >= 1.
+ * Outputs may not overlap inputs (except angle_out == angle0).
+ */
+ssm_status_t ssm_mamba3_rope(const void* B, const void* C, const float* dt, const float* theta,
+                             const float* angle0, void* B_rot, void* C_rot, float* angle_out,
+                             int batch, int seqlen, int rank, int nheads, int ngroups, int dstate,
+                             ssm_dtype_t dtype, void* stream);
 
 /*
  * Selective scan for callers that cannot allocate device memory.

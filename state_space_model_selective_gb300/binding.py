@@ -35,7 +35,7 @@ EXPORTS = ["ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_bytes", "
            "ssd_chunked_checkpoint_bytes", "ssd_chunked_fwd_ckpt", "ssd_mamba3_bwd_workspace_bytes",
            "ssd_mamba3_bwd", "ssd_mamba3_mimo_bwd_workspace_bytes", "ssd_mamba3_mimo_bwd",
            "ssd_mamba3_fwd_ckpt", "ssd_mamba3_mimo_fwd_ckpt", "ssm_debug_set_lookback",
-           "ssm_debug_set_scan_path", "ssm_noalloc_last_status"]
+           "ssm_debug_set_scan_path", "ssm_noalloc_last_status", "ssm_mamba3_rope"]
 
 
 class SSMError(RuntimeError):
@@ -118,6 +118,8 @@ def lib() -> ctypes.CDLL:
         L.ssm_debug_set_scan_path.argtypes = [i, i]
         L.ssm_noalloc_last_status.restype = i
         L.ssm_noalloc_last_status.argtypes = [vp]
+        L.ssm_mamba3_rope.restype = i
+        L.ssm_mamba3_rope.argtypes = [vp] * 8 + [i] * 7 + [vp]
         _lib = L
     return _lib
 
@@ -726,6 +728,56 @@ def ssm_noalloc_last_status(stream=None) -> int:
     """Device-side status the last ``ssm_scan_fwd_noalloc`` on the current device
     recorded in its scratch array (waits for the stream)."""
     return int(lib().ssm_noalloc_last_status(_stream(stream)))
+
+
+def ssm_mamba3_rope(B, C, dt, theta, angle0=None, B_rot=None, C_rot=None, angle_out=None,
+                    return_angle=True, stream=None):
+    """Mamba-3's data-dependent RoPE: angles -cumsum(dt * theta) (from angle0),
+    B and C rotated by them pair by pair, one row per head.  B, C: (batch, L, G, N)
+    or with a rank axis (batch, L, R, G, N); dt (batch, L, H) fp32; theta
+    (batch, L, H, N/2) fp32; angle0 (batch, H, N/2) fp32 or None.  Returns
+    (B_rot, C_rot, angle_out) with B_rot, C_rot (batch, L, [R,] H, N) in B's dtype;
+    angle_out may be angle0 itself (updated in place)."""
+    _req(B, "B")
+    dt_ = B.dtype
+    if dt_ not in _DT:
+        raise TypeError("B must be float32 or bfloat16")
+    siso = B.dim() == 4
+    if B.dim() not in (4, 5):
+        raise ValueError("B must have 4 dims (batch, L, G, N) or 5 (batch, L, R, G, N)")
+    if siso:
+        batch, seqlen, ngroups, dstate = B.shape
+        rank = 1
+    else:
+        batch, seqlen, rank, ngroups, dstate = B.shape
+    _req(C, "C", dt_)
+    _shape(C, "C", tuple(B.shape))
+    _req(dt, "dt", torch.float32, 3)
+    nheads = dt.shape[2]
+    _shape(dt, "dt", (batch, seqlen, nheads))
+    _req(theta, "theta", torch.float32, 4)
+    _shape(theta, "theta", (batch, seqlen, nheads, dstate // 2))
+    _opt(angle0, "angle0", torch.float32)
+    _shape(angle0, "angle0", (batch, nheads, dstate // 2))
+    rot = (batch, seqlen, nheads, dstate) if siso else (batch, seqlen, rank, nheads, dstate)
+    if B_rot is None:
+        B_rot = torch.empty(rot, dtype=dt_, device=B.device)
+    if C_rot is None:
+        C_rot = torch.empty(rot, dtype=dt_, device=B.device)
+    _req(B_rot, "B_rot", dt_)
+    _req(C_rot, "C_rot", dt_)
+    _shape(B_rot, "B_rot", rot)
+    _shape(C_rot, "C_rot", rot)
+    if angle_out is None and return_angle:
+        angle_out = torch.empty((batch, nheads, dstate // 2), dtype=torch.float32,
+                                device=B.device)
+    _opt(angle_out, "angle_out", torch.float32)
+    _shape(angle_out, "angle_out", (batch, nheads, dstate // 2))
+    st = lib().ssm_mamba3_rope(_ptr(B), _ptr(C), _ptr(dt), _ptr(theta), _ptr(angle0),
+                               _ptr(B_rot), _ptr(C_rot), _ptr(angle_out), batch, seqlen, rank,
+                               nheads, ngroups, dstate, _DT[dt_], _stream(stream))
+    _check(st, "ssm_mamba3_rope")
+    return B_rot, C_rot, angle_out
 
 
 def ssd_mamba3_fwd(x, dt, lam, A_head, B, C, chunk=64, out_dtype=None, y=None, final_state=None,

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libssm.so")
-SOURCES = ["scan.cu", "scan_seg.cu", "scan_bwd.cu", "scan_host.cu", "decode.cu", "ssd.cu", "ssd_bwd.cu",
+SOURCES = ["scan.cu", "scan_seg.cu", "rope.cu", "scan_bwd.cu", "scan_host.cu", "decode.cu", "ssd.cu", "ssd_bwd.cu",
            "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,

@@ -179,3 +179,15 @@ def decode_inputs(batch: int, nheads: int, headdim: int, dstate: int, ngroups: i
         zs.append(_randn((batch, nheads, headdim), g, device).to(td) if gate else None)
     return {"state": state.contiguous(), "A": A_head.contiguous(), "D": D,
             "x": xs, "dt": dts, "B": Bs, "C": Cs, "z": zs}
+
+
+def rope_inputs(batch: int, seqlen: int, nheads: int, dstate: int, seed: int = 1008,
+                device: str = "cpu") -> dict:
+    """Inputs of Mamba-3's data-dependent rotation (no page gives their
+    distribution): theta (B, L, H, N/2) fp32 ~ N(0, 1), one angular rate per
+    head and state pair, and a starting angle angle0 (B, H, N/2) fp32 ~
+    U[-pi, pi)."""
+    g = _gen(seed, device)
+    theta = _randn((batch, seqlen, nheads, dstate // 2), g, device).contiguous()
+    angle0 = ((_rand((batch, nheads, dstate // 2), g, device) * 2.0 - 1.0) * 3.141592653589793)
+    return {"theta": theta, "angle0": angle0.contiguous()}

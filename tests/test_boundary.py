@@ -503,3 +503,27 @@ def test_scan_host_argument_errors(L):
     # two slots of about an eighth of the sequence (u, delta, z, B, C in, y out)
     assert f(8, 1536, 2048) >= 2 * (8 * 1536 * 256 * (3 * 2 + 4))
     assert f(8, 1536, 2048, dstate=8) == 0
+
+
+def rope_call(L, **kw):
+    args = dict(B=P(0), C=P(1), dt=P(2), theta=P(3), a0=None, Br=P(4), Cr=P(5), aout=P(6),
+                batch=2, seqlen=8, rank=1, nheads=4, ngroups=2, dstate=16, dtype=1, stream=None)
+    args.update(kw)
+    return L.ssm_mamba3_rope(args["B"], args["C"], args["dt"], args["theta"], args["a0"],
+                             args["Br"], args["Cr"], args["aout"], args["batch"],
+                             args["seqlen"], args["rank"], args["nheads"], args["ngroups"],
+                             args["dstate"], args["dtype"], args["stream"])
+
+
+def test_rope_rejects_bad_arguments_on_the_host(L):
+    assert rope_call(L, dstate=15) == SHAPE          # state pairs need an even dstate
+    assert rope_call(L, ngroups=3) == SHAPE          # heads not a multiple of groups
+    assert rope_call(L, rank=0) == SHAPE
+    assert rope_call(L, batch=-1) == SHAPE
+    assert rope_call(L, dtype=7) == DTYPE
+    assert rope_call(L, B=None) == NULL
+    assert rope_call(L, Cr=None) == NULL
+    assert rope_call(L, theta=ctypes.c_void_p(0x10000008)) == ALIGN
+    assert rope_call(L, Br=P(0)) == ALIAS            # output over an input
+    assert rope_call(L, Cr=P(4)) == ALIAS            # the two outputs overlap
+    assert rope_call(L, batch=0) == OK               # nothing to do, nothing launched
