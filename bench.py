@@ -414,6 +414,7 @@ def measure_other_paths(dev, reps=20):
                      "peak": HBM_PEAK_GBS, "unit": "GB/s",
                      "frac": nbm / (ms / 1e3) / 1e9 / HBM_PEAK_GBS, "algorithmic_bytes": nbm}}
     del mi, ym, fsm
+    res["ssm_mamba3_rope"] = _measure_rope(dev, reps)
     g = torch.Generator(device="cuda")
     g.manual_seed(1005)
     B_, H, P, N = 256, 32, 64, 128
@@ -513,6 +514,34 @@ def _measure_scan(dev, batch, dim, seqlen, dt, reps, graph=False):
                      "unit": "Gop/s (MUFU)", "frac": achieved / MUFU_PEAK_GOPS,
                      "algorithmic_mufu_ops": mufu}})
     return out
+
+
+def _measure_rope(dev, reps):
+    """Mamba-3's data-dependent rotation of B and C (ssm_mamba3_rope) on the SSD
+    workload (batch 32, L 256, 32 heads, one group, d_state 128, bf16 B, C), against
+    the HBM roofline of its algorithmic bytes: dt, theta, B, C in; the per-head
+    rotated B, C out."""
+    import torch
+    from state_space_model_selective_gb300 import binding, inputs
+    Bn, L, H, P, N = 32, 256, 32, 64, 128
+    inp = inputs.ssd_inputs(Bn, L, H, P, N, 1, "bf16", seed=1004, device=dev)
+    r = inputs.rope_inputs(Bn, L, H, N, seed=1008, device=dev)
+    Br = torch.empty(Bn, L, H, N, dtype=torch.bfloat16, device=dev)
+    Cr = torch.empty_like(Br)
+    ang = torch.empty(Bn, H, N // 2, device=dev)
+
+    def rope():
+        binding.ssm_mamba3_rope(inp["B"], inp["C"], inp["dt"], r["theta"], r["angle0"],
+                                B_rot=Br, C_rot=Cr, angle_out=ang)
+    ms = _time(rope, reps)
+    nbytes = (inp["dt"].numel() * 4 + r["theta"].numel() * 4 + 2 * inp["B"].numel() * 2 +
+              2 * Br.numel() * 2 + 2 * ang.numel() * 4)
+    return {"workload": "Mamba-3 RoPE on B, C: bf16, batch 32, L 256, 32 heads, 1 group, "
+                        "d_state 128 (per-head rotated B, C out)", "ms": ms,
+            "roofline": {"bound": "hbm", "achieved": nbytes / (ms / 1e3) / 1e9,
+                         "peak": HBM_PEAK_GBS, "unit": "GB/s",
+                         "frac": nbytes / (ms / 1e3) / 1e9 / HBM_PEAK_GBS,
+                         "algorithmic_bytes": nbytes}}
 
 
 def _measure_scan_bwd(dev, reps):
