@@ -27,6 +27,7 @@
 // TMEM lane: row i of G / Y, and row n of S_chunk^T with the running state
 // S_prev[n, :] kept in its registers.
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "ssd_common.cuh"
@@ -38,6 +39,7 @@ using namespace ssm;
 using namespace ssd_detail;
 using ssd_host::make_bc_map;
 using ssd_host::make_x_map;
+using ssd_host::make_y_map;
 constexpr int kThreads = 256;  // two warpgroups; each per-row phase splits a row's columns
 constexpr int kHalf = 32;      // columns of a 64-wide row per warpgroup
 
@@ -113,7 +115,8 @@ __device__ __forceinline__ void mprime_chunk(const float* gv, const float* q2c, 
 template <typename Tout, bool M3, int RK, bool BS = false>
 __global__ void __launch_bounds__(kThreads, 2)
     ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_B,
-                   const __grid_constant__ CUtensorMap tm_x, const SsdArgs a) {
+                   const __grid_constant__ CUtensorMap tm_x,
+                   const __grid_constant__ CUtensorMap tm_y, const SsdArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
     float* s_q2 = reinterpret_cast<float*>(smem + kMisc);
@@ -172,6 +175,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         prefetch_tensormap(&tm_C);
         prefetch_tensormap(&tm_B);
         prefetch_tensormap(&tm_x);
+        if (a.y) prefetch_tensormap(&tm_y);
     }
     tc_fence_before();
     __syncthreads();
@@ -316,7 +320,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (lane >= o) v += u;
         }
         if (lane == 31) s_wsum[part * 4 + quarter] = v;
-        __syncthreads();  // also: the previous step's y tile has been read out
+        // the previous step's y tile (in the S region) has been read by its
+        // TMA store before anyone rewrites the region
+        if (tid == kLoader) bulk_wait_read_all();
+        __syncthreads();
         float cs_last = 0.0f;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
@@ -495,37 +502,21 @@ __global__ void __launch_bounds__(kThreads, 2)
                                    pack_bf16(yv[8 * c + 6], yv[8 * c + 7]));
             }
         }
+        fence_proxy_async_smem();  // the staged tile is read by the TMA store
         tc_fence_before();  // every TMEM read of the step precedes the next step's MMAs
         __syncthreads();
         if (tid == 0) tc_fence_after();
 
-        // ---- y rows out of the staged tile: each warp writes whole rows of
-        // the head (coalesced); rows past the sequence end are skipped
-        if (!BS || a.y != nullptr) {
-            const long long yrow0 = ((long long)b * nsub + t0) * a.nheads + h;
+        // ---- y out of the staged tile by TMA stores (one thread; rows past
+        // the sequence end are clipped by the map)
+        if ((!BS || a.y != nullptr) && tid == kLoader) {
             if constexpr (sizeof(Tout) == 4) {
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int idx = tid + kThreads * r;
-                    const int t = idx >> 4, c16 = idx & 15;
-                    const float4 v = *reinterpret_cast<const float4*>(
-                        smem + kRS + (c16 >> 3) * 16384 + t * 128 + (((c16 & 7) ^ (t & 7)) << 4));
-                    if (t0 + t < nsub)
-                        *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.y) +
-                                                   (yrow0 + (long long)t * a.nheads) * kP + 4 * c16) = v;
-                }
+                tma_store_3d(&tm_y, smem + kRS, h * kP, t0, b);
+                tma_store_3d(&tm_y, smem + kRS + 16384, h * kP + kHalf, t0, b);
             } else {
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int idx = tid + kThreads * r;
-                    const int t = idx >> 3, c = idx & 7;
-                    const uint4 v = *reinterpret_cast<const uint4*>(smem + kRS + t * 128 +
-                                                                    ((c ^ (t & 7)) << 4));
-                    if (t0 + t < nsub)
-                        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.y) +
-                                                  (yrow0 + (long long)t * a.nheads) * kP + 8 * c) = v;
-                }
+                tma_store_3d(&tm_y, smem + kRS, h * kP, t0, b);
             }
+            bulk_commit();
         }
 
         // ---- state: S_prev[n = row][32 part + :] = exp(cs_last) S_prev + S_chunk^T;
@@ -552,6 +543,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     (void)ok;
 
     if (tid == kLoader) {
+        bulk_wait_all();  // every y store has completed
         // never leave with a load still landing in shared memory: wait (bounded)
         // for the phase of the last load issued on each barrier
         if (cb_issued > 0) (void)mbar_wait(bar_cb, (uint32_t)((cb_issued - 1) & 1), nullptr);
@@ -564,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 template <typename Tout, bool M3, int RK, bool BS = false>
 ssm_status_t launch(const CUtensorMap& mc, const CUtensorMap& mb, const CUtensorMap& mx,
-                    const SsdArgs& a, cudaStream_t s) {
+                    const CUtensorMap& my, const SsdArgs& a, cudaStream_t s) {
     auto kern = ssd_fwd_kernel<Tout, M3, RK, BS>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
         cudaSuccess)
@@ -586,7 +578,7 @@ ssm_status_t launch(const CUtensorMap& mc, const CUtensorMap& mb, const CUtensor
     }
     const long long items = (long long)a.batch * a.nheads;
     const unsigned grid = (unsigned)std::min<long long>(items, 2LL * sms);
-    kern<<<grid, kThreads, kSmemBytes, s>>>(mc, mb, mx, a);
+    kern<<<grid, kThreads, kSmemBytes, s>>>(mc, mb, mx, my, a);
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
@@ -663,11 +655,13 @@ ssm_status_t ssd_entry(const void* x, const float* dt, const float* lam, const f
             return SSM_ERR_ALIAS;
     }
 
-    CUtensorMap mc, mb, mx;
+    CUtensorMap mc, mb, mx, my;
     const int nsub = seqlen * rank;
     if (!make_bc_map(&mc, C, batch, nsub, ngroups) || !make_bc_map(&mb, B, batch, nsub, ngroups) ||
         !make_x_map(&mx, x, batch, nsub, nheads))
         return SSM_ERR_CUDA;
+    memset(&my, 0, sizeof(my));
+    if (y && !make_y_map(&my, y, batch, nsub, nheads, out_dtype)) return SSM_ERR_CUDA;
     SsdArgs a{};
     a.x = static_cast<const __nv_bfloat16*>(x);
     a.dt = dt;
@@ -686,26 +680,26 @@ ssm_status_t ssd_entry(const void* x, const float* dt, const float* lam, const f
     if (bstates) {  // the states the gradients start from, kept by the forward
         a.bstates = bstates;
         if (!m3)
-            return bf ? launch<__nv_bfloat16, false, 1, true>(mc, mb, mx, a, s)
-                      : launch<float, false, 1, true>(mc, mb, mx, a, s);
+            return bf ? launch<__nv_bfloat16, false, 1, true>(mc, mb, mx, my, a, s)
+                      : launch<float, false, 1, true>(mc, mb, mx, my, a, s);
         switch (rank) {
-            case 1: return bf ? launch<__nv_bfloat16, true, 1, true>(mc, mb, mx, a, s)
-                              : launch<float, true, 1, true>(mc, mb, mx, a, s);
-            case 2: return bf ? launch<__nv_bfloat16, true, 2, true>(mc, mb, mx, a, s)
-                              : launch<float, true, 2, true>(mc, mb, mx, a, s);
-            default: return bf ? launch<__nv_bfloat16, true, 4, true>(mc, mb, mx, a, s)
-                               : launch<float, true, 4, true>(mc, mb, mx, a, s);
+            case 1: return bf ? launch<__nv_bfloat16, true, 1, true>(mc, mb, mx, my, a, s)
+                              : launch<float, true, 1, true>(mc, mb, mx, my, a, s);
+            case 2: return bf ? launch<__nv_bfloat16, true, 2, true>(mc, mb, mx, my, a, s)
+                              : launch<float, true, 2, true>(mc, mb, mx, my, a, s);
+            default: return bf ? launch<__nv_bfloat16, true, 4, true>(mc, mb, mx, my, a, s)
+                               : launch<float, true, 4, true>(mc, mb, mx, my, a, s);
         }
     }
-    if (!m3) return bf ? launch<__nv_bfloat16, false, 1>(mc, mb, mx, a, s)
-                       : launch<float, false, 1>(mc, mb, mx, a, s);
+    if (!m3) return bf ? launch<__nv_bfloat16, false, 1>(mc, mb, mx, my, a, s)
+                       : launch<float, false, 1>(mc, mb, mx, my, a, s);
     switch (rank) {
-        case 1: return bf ? launch<__nv_bfloat16, true, 1>(mc, mb, mx, a, s)
-                          : launch<float, true, 1>(mc, mb, mx, a, s);
-        case 2: return bf ? launch<__nv_bfloat16, true, 2>(mc, mb, mx, a, s)
-                          : launch<float, true, 2>(mc, mb, mx, a, s);
-        default: return bf ? launch<__nv_bfloat16, true, 4>(mc, mb, mx, a, s)
-                           : launch<float, true, 4>(mc, mb, mx, a, s);
+        case 1: return bf ? launch<__nv_bfloat16, true, 1>(mc, mb, mx, my, a, s)
+                          : launch<float, true, 1>(mc, mb, mx, my, a, s);
+        case 2: return bf ? launch<__nv_bfloat16, true, 2>(mc, mb, mx, my, a, s)
+                          : launch<float, true, 2>(mc, mb, mx, my, a, s);
+        default: return bf ? launch<__nv_bfloat16, true, 4>(mc, mb, mx, my, a, s)
+                           : launch<float, true, 4>(mc, mb, mx, my, a, s);
     }
 }
 
@@ -717,10 +711,11 @@ ssm_status_t ssd_forward_block_states(const void* x, const float* dt, const floa
                                       const void* B, const void* C, const float* initial_state,
                                       float* bstates, int batch, int seqlen, int nheads,
                                       int ngroups, cudaStream_t stream) {
-    CUtensorMap mc, mb, mx;
+    CUtensorMap mc, mb, mx, my;
     if (!make_bc_map(&mc, C, batch, seqlen, ngroups) || !make_bc_map(&mb, B, batch, seqlen, ngroups) ||
         !make_x_map(&mx, x, batch, seqlen, nheads))
         return SSM_ERR_CUDA;
+    memset(&my, 0, sizeof(my));  // no y is written
     SsdArgs a{};
     a.x = static_cast<const __nv_bfloat16*>(x);
     a.dt = dt;
@@ -733,7 +728,7 @@ ssm_status_t ssd_forward_block_states(const void* x, const float* dt, const floa
     a.seqlen = seqlen;
     a.nheads = nheads;
     a.ngroups = ngroups;
-    return launch<float, false, 1, true>(mc, mb, mx, a, stream);
+    return launch<float, false, 1, true>(mc, mb, mx, my, a, stream);
 }
 
 // The Mamba-3 forward (SISO, or MIMO of rank 2 or 4 over 128-row blocks of
@@ -749,10 +744,11 @@ ssm_status_t ssd_mamba3_forward_block_states(const void* x, const float* dt, con
                                              int seqlen, int nheads, int ngroups,
                                              cudaStream_t stream, int rank) {
     const int nsub = seqlen * rank;
-    CUtensorMap mc, mb, mx;
+    CUtensorMap mc, mb, mx, my;
     if (!make_bc_map(&mc, C, batch, nsub, ngroups) || !make_bc_map(&mb, B, batch, nsub, ngroups) ||
         !make_x_map(&mx, x, batch, nsub, nheads))
         return SSM_ERR_CUDA;
+    memset(&my, 0, sizeof(my));  // no y is written
     SsdArgs a{};
     a.x = static_cast<const __nv_bfloat16*>(x);
     a.dt = dt;
@@ -769,9 +765,9 @@ ssm_status_t ssd_mamba3_forward_block_states(const void* x, const float* dt, con
     a.nheads = nheads;
     a.ngroups = ngroups;
     switch (rank) {
-        case 1: return launch<float, true, 1, true>(mc, mb, mx, a, stream);
-        case 2: return launch<float, true, 2, true>(mc, mb, mx, a, stream);
-        case 4: return launch<float, true, 4, true>(mc, mb, mx, a, stream);
+        case 1: return launch<float, true, 1, true>(mc, mb, mx, my, a, stream);
+        case 2: return launch<float, true, 2, true>(mc, mb, mx, my, a, stream);
+        case 4: return launch<float, true, 4, true>(mc, mb, mx, my, a, stream);
     }
     return SSM_ERR_UNSUPPORTED;
 }

@@ -89,4 +89,27 @@ inline bool make_x_map(CUtensorMap* map, const void* base, int batch, int seqlen
            CUDA_SUCCESS;
 }
 
+// y (batch, seqlen, nheads, headdim) in fp32 or bf16 as a 3-D map {nheads *
+// headdim, seqlen, batch} whose boxes are one 128-byte row span (32 fp32 or 64
+// bf16 columns) x 128 steps x 1 (128-byte swizzle), the layout the forward
+// kernel stages y in; stores clip at the sequence end.
+inline bool make_y_map(CUtensorMap* map, void* base, int batch, int seqlen, int nheads,
+                       ssm_dtype_t dtype) {
+    using ssd_detail::kP;
+    using ssd_detail::kQ;
+    ssm_host::EncodeTiledFn fn = ssm_host::encode_tiled_fn();
+    if (!fn) return false;
+    const cuuint64_t es = dtype == SSM_BF16 ? 2 : 4;
+    const cuuint64_t dims[3] = {(cuuint64_t)nheads * kP, (cuuint64_t)seqlen, (cuuint64_t)batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)nheads * kP * es,
+                                   (cuuint64_t)seqlen * nheads * kP * es};
+    const cuuint32_t box[3] = {(cuuint32_t)(128 / es), (cuuint32_t)kQ, 1};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    return fn(map, dtype == SSM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+              3, base, dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace ssd_host
