@@ -210,19 +210,31 @@ __global__ void __launch_bounds__(kThreads, 4)
     }
 
     // ---- B and C of the chunk into shared memory as fp32 [t][n]: thread
-    // (state n, 4-step group) reads 4 steps of B and of C
-    for (int i = tid; i < kN * (kChunk / 4); i += kThreads) {
-        const int n = i % kN, t = (i / kN) * 4;
-        float vb[4], vc[4];
-        load_steps<Tin, 4>(reinterpret_cast<const Tin*>(a.Bm), (long long)bg * kN + n, c0 + t,
-                           a.seqlen, vec, vb);
-        load_steps<Tin, 4>(reinterpret_cast<const Tin*>(a.Cm), (long long)bg * kN + n, c0 + t,
-                           a.seqlen, vec, vc);
+    // (state n, 4-step group) reads 4 steps of B and of C, every load of the
+    // thread issued before its first store (one round trip, not four)
+    {
+        constexpr int kIters = kN * (kChunk / 4) / kThreads;
+        static_assert(kN * (kChunk / 4) % kThreads == 0, "whole staging rounds");
+        float vb[kIters][4], vc[kIters][4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            float* r = reinterpret_cast<float*>(smem + SM::off(t + k));
-            r[n] = vb[k];
-            r[kN + n] = vc[k];
+        for (int r = 0; r < kIters; ++r) {
+            const int i = tid + r * kThreads;
+            const int n = i % kN, t = (i / kN) * 4;
+            load_steps<Tin, 4>(reinterpret_cast<const Tin*>(a.Bm), (long long)bg * kN + n, c0 + t,
+                               a.seqlen, vec, vb[r]);
+            load_steps<Tin, 4>(reinterpret_cast<const Tin*>(a.Cm), (long long)bg * kN + n, c0 + t,
+                               a.seqlen, vec, vc[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < kIters; ++r) {
+            const int i = tid + r * kThreads;
+            const int n = i % kN, t = (i / kN) * 4;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float* row = reinterpret_cast<float*>(smem + SM::off(t + k));
+                row[n] = vb[r][k];
+                row[kN + n] = vc[r][k];
+            }
         }
     }
     __syncthreads();
