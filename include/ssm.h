@@ -158,6 +158,11 @@ ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const float* A,
  * place), any other overlap returns SSM_ERR_ALIAS.
  * Supported: chunk == 64, headdim == 64, dstate == 128, in_dtype == SSM_BF16,
  * seqlen % chunk == 0 (else SSM_ERR_SHAPE), nheads % ngroups == 0.
+ * `chunk` is the granularity the call validates (the pages' chunk size and
+ * their seqlen % chunk rule); the kernel itself evaluates the chunked form in
+ * 128-step blocks, so that every product is an M = 128 tensor-core MMA.  The
+ * chunked form equals the recurrence for any block length, so the result does
+ * not depend on this choice beyond fp32 rounding.
  * seqlen == 0 writes final_state = initial_state (or 0).
  */
 ssm_status_t ssd_chunked_fwd(const void* x, const float* dt, const float* A_head,
