@@ -931,11 +931,23 @@ def _profile_setup(name):
             binding.ssm_decode_step(state, inp["x"][0], inp["dt"][0], inp["A"], inp["B"][0],
                                     inp["C"][0], inp["D"])
         return fn, None
+    if name == "rope":
+        Bn, L, H, P, N = 32, 256, 32, 64, 128
+        inp = inputs.ssd_inputs(Bn, L, H, P, N, 1, "bf16", seed=1004, device=dev)
+        r = inputs.rope_inputs(Bn, L, H, N, seed=1008, device=dev)
+        Br = torch.empty(Bn, L, H, N, dtype=torch.bfloat16, device=dev)
+        Cr = torch.empty_like(Br)
+        ang = torch.empty(Bn, H, N // 2, device=dev)
+
+        def fn():
+            binding.ssm_mamba3_rope(inp["B"], inp["C"], inp["dt"], r["theta"], r["angle0"],
+                                    B_rot=Br, C_rot=Cr, angle_out=ang)
+        return fn, None
     raise SystemExit(f"unknown workload {name!r}")
 
 
 PROFILE_WORKLOADS = ["scan", "scan_l4096", "scan_b8", "scan_b1_f32", "ssd", "decode",
-                     "decode_mimo", "scan_bwd", "ssd_bwd", "m3_bwd", "mimo_bwd"]
+                     "decode_mimo", "scan_bwd", "ssd_bwd", "m3_bwd", "mimo_bwd", "rope"]
 
 
 def run_profile(name, reps):
@@ -944,7 +956,8 @@ def run_profile(name, reps):
     scan_b8: batch 8, L 2048, 1536 channels; scan_b1_f32: batch 1, L 128, 1536
     channels, fp32; ssd: chunked SSD batch 32, L 256, 32 heads; decode,
     decode_mimo: decode steps batch 256, 32 heads; scan_bwd, ssd_bwd, m3_bwd,
-    mimo_bwd: the gradients on those workloads."""
+    mimo_bwd: the gradients on those workloads; rope: Mamba-3's rotation of B
+    and C on the SSD workload."""
     import torch
     fn, check = _profile_setup(name)
     for _ in range(reps):

@@ -311,8 +311,10 @@ ssm_status_t ssm_decode_step_mamba3_mimo(float* state, const void* prev_B, const
  * The rotated rows are per head, so the SSD and decode entry points take
  * them with ngroups = nheads.  With seqlen = 1 this is the rotation of one
  * decode step (angle0 = the previous step's angle_out; angle_out may be
- * angle0 itself, updated in place).  The angle is a Kahan-compensated fp32
- * sum: its error stays near one rounding of its value (about 1e-7 |angle|).
+ * angle0 itself, updated in place).  The angle is carried as a compensated
+ * float-float sum (the steps of a tile scanned in segments, the segment sums
+ * composed by TwoSum): its error stays near one rounding of its value (about
+ * 1e-7 |angle|); angle_out is that sum rounded once to fp32.
  *
  * Layouts (dtype for B, C, B_rot, C_rot; everything else fp32):
  *   B, C            (batch, seqlen, rank, ngroups, dstate)   rank 1 = SISO

@@ -26,6 +26,9 @@ CASES = [  # batch, seqlen, rank, nheads, ngroups, dstate, dtype, with angle0
     (1, 256, 1, 8, 1, 128, "bf16", False),
     (2, 33, 4, 4, 4, 128, "bf16", True),
     (3, 17, 2, 6, 3, 16, "f32", False),
+    (2, 700, 1, 2, 1, 6, "bf16", True),   # 3 pairs: scalar loads, a 512-step tile + tail
+    (1, 75, 1, 2, 1, 160, "f32", True),   # 80 pairs: two CTAs per head, the second partial
+    (1, 1, 3, 2, 2, 128, "bf16", True),   # one step (a decode step's rotation), rank 3
 ]
 
 
