@@ -677,9 +677,9 @@ ssm_status_t ssd_mamba3_mimo_bwd(const void* x, const float* dt, const float* la
 
 /*
  * Bytes of device workspace ssm_scan_fwd_host needs (a pure function of its
- * arguments; 0 if they are invalid).  About two segments' worth of u, delta, z,
- * B, C and y (a segment is ~1/8 of the sequence, a multiple of 64 steps), two
- * states and one segment's ssm_scan_workspace_bytes.
+ * arguments; 0 if they are invalid).  Two segments' worth of u, delta, z, B, C,
+ * y and states (a segment is about 1/8 of the (batch, channel) rows, all
+ * steps), plus the largest segment's ssm_scan_workspace_bytes.
  */
 size_t ssm_scan_fwd_host_workspace_bytes(int batch, int dim, int seqlen, int dstate, int ngroups,
                                          ssm_dtype_t in_dtype, ssm_dtype_t out_dtype);
@@ -690,16 +690,16 @@ size_t ssm_scan_fwd_host_workspace_bytes(int batch, int dim, int seqlen, int dst
  *   but u, delta, z, B, C, initial_state, y and final_state are HOST pointers to
  *   page-locked memory (cudaHostAlloc / cudaMallocHost / cudaHostRegister;
  *   anything else returns SSM_ERR_UNSUPPORTED); A, D, delta_bias and the
- *   workspace are DEVICE pointers.  The sequence is cut into segments that
- *   chain through the state (the scan is associative: "We brought Mamba to
- *   Trainium -- and mapped where custom kernels actually help", section "We
- *   built the parallel scan -- and it taught us something sharper"); each
- *   segment's rows are copied in with 2-D DMA copies, scanned on `stream` from
- *   the previous segment's final state, and its y copied back, with the copies
- *   of neighbouring segments in flight during the scan.  Segments are whole
- *   multiples of 128 steps and every segment is scanned with the whole
- *   sequence's plan, so the result is bit-equal to ssm_scan_fwd on device
- *   copies of the same inputs.
+ *   workspace are DEVICE pointers.  Every channel's recurrence is independent
+ *   of the others, so the (batch, channel) rows are cut into about eight
+ *   segments -- whole batches, whole B/C groups of one batch, or part of one
+ *   group -- each of whose arrays is one contiguous block of host memory.  A
+ *   segment's u, delta, z, its groups' B and C and its initial state are
+ *   copied in with one 1-D copy each, scanned on `stream`, and its y and final
+ *   state copied back, with the copies of neighbouring segments in flight
+ *   during the scan.  Every segment is scanned by the kernel, and with the
+ *   plan, that ssm_scan_fwd would use for the whole problem, so the result is
+ *   bit-equal to ssm_scan_fwd on device copies of the same inputs.
  *
  *  - Asynchronous like every entry point: work is enqueued on `stream` and on
  *    two copy streams of the library's own (created on the first call on a

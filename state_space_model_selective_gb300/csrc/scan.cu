@@ -800,7 +800,7 @@ ssm_status_t scan_fwd_entry(const void* u, const void* delta, const float* A, co
                             float* final_state, float* ckpt, int batch, int dim, int seqlen,
                             int dstate, int ngroups, ssm_dtype_t in_dtype, ssm_dtype_t out_dtype,
                             void* workspace, size_t workspace_bytes, void* stream,
-                            int seg_ts = 0, bool keep_status = false) {
+                            int seg_ts = 0, bool keep_status = false, int force_path = 0) {
     using namespace ssm_host;
     if (batch < 0 || dim < 0 || seqlen < 0 || ngroups < 1 || dstate < 1) return SSM_ERR_SHAPE;
     if (dim % ngroups != 0) return SSM_ERR_SHAPE;
@@ -857,7 +857,9 @@ ssm_status_t scan_fwd_entry(const void* u, const void* delta, const float* A, co
     for (const R& r : ins)
         if (overlaps(workspace, need, r.p, r.n)) return SSM_ERR_ALIAS;
 
-    if (use_seg_path(batch, dim)) {
+    if (force_path == 2 && !ssm_internal::scan_seg_eligible(batch, dim)) return SSM_ERR_UNSUPPORTED;
+    const bool seg = force_path == 2 || (force_path == 0 && use_seg_path(batch, dim));
+    if (seg) {
         const uint32_t lim = g_flag_spin_limit.load(std::memory_order_relaxed);
         const ssm_status_t st = ssm_internal::scan_seg_forward(
             u, delta, A, B, C, D, z, delta_bias, delta_softplus, initial_state, y, final_state,
@@ -911,11 +913,14 @@ ssm_status_t scan_forward_segment(const void* u, const void* delta, const float*
                                   int batch, int dim, int seqlen, int ngroups,
                                   ssm_dtype_t in_dtype, ssm_dtype_t out_dtype, void* workspace,
                                   size_t workspace_bytes, cudaStream_t stream, int seg_ts,
-                                  bool keep_status) {
+                                  bool keep_status, int path) {
     return scan_fwd_entry(u, delta, A, B, C, D, z, delta_bias, delta_softplus, initial_state, y,
                           final_state, nullptr, batch, dim, seqlen, kN, ngroups, in_dtype,
-                          out_dtype, workspace, workspace_bytes, stream, seg_ts, keep_status);
+                          out_dtype, workspace, workspace_bytes, stream, seg_ts, keep_status,
+                          path);
 }
+
+bool scan_uses_seg_path(long long batch, long long dim) { return use_seg_path(batch, dim); }
 
 }  // namespace ssm_internal
 

@@ -1,24 +1,30 @@
 // scan_host.cu -- the selective scan on host-resident activations
 // (ssm_scan_fwd_host): host -> device copies, the scan and device -> host copies
-// pipelined over segments of the sequence.
+// pipelined over segments of the problem's channels.
 //
 // What it computes is exactly ssm_scan_fwd's ("We brought Mamba to Trainium --
 // and mapped where custom kernels actually help", section "Mamba: bringing an
-// unsupported model to the chip, and writing its missing kernel"), with the
-// sequence cut into segments that chain through the state: scanning [t0, t1)
-// from the state after t0 equals the whole scan restricted to [t0, t1) (the
-// associativity of the recurrence, section "We built the parallel scan -- and
-// it taught us something sharper").
+// unsupported model to the chip, and writing its missing kernel"): every
+// channel's recurrence is independent of the others, so a range of channels is
+// a problem of its own.
 //
-// How: segment k's rows of u, delta, z, B, C (strided in the host layout) are
-// copied with 2-D DMA copies on a copy stream into one of two device slots; the
-// caller's stream runs ssm_scan_fwd on the slot with the previous segment's
-// final state; a second copy stream brings y's rows back.  Copies in both
-// directions run on the copy engines while the SMs scan the neighbouring
+// How: the (batch, channel) rows are cut into about eight segments, each a
+// contiguous range of rows -- whole batches, whole B/C groups of one batch, or
+// part of one group; the first and the last are halved again, since nothing
+// overlaps the first one's input copy or the last one's scan and output copy --
+// so that every array of a segment (u, delta, z, y, the
+// states, and its groups' B and C) is one contiguous block of host memory,
+// moved by a single 1-D copy at the link's full rate (2-D copies of short rows
+// run well below it).  Segment k's inputs are copied on a copy stream into one
+// of two device slots, the caller's stream scans the slot with the kernel and
+// plan the whole problem would use (so the result is the whole call's, bit for
+// bit), and a second copy stream brings y and the final state back.  Copies in
+// both directions run on the copy engines while the SMs scan the neighbouring
 // segments.  The two copy streams and the events are created once per device
 // and kept for the life of the process.
 #include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 #include "scan_internal.h"
@@ -29,37 +35,98 @@ using namespace ssm_host;
 
 constexpr int kN = 16;
 constexpr int kSlots = 2;
+constexpr long long kTargetSegments = 8;
+
+// One segment: batches [b0, b0 + nb), channels [c0, c0 + nc) of each, which lie
+// in groups [g0, g0 + ng).  Either whole batches (c0 = 0, nc = dim), or one
+// batch with whole groups, or one batch with part of one group; in each case
+// its rows of u, delta, z, y and of the states, and its rows of B and C, are
+// contiguous.
+struct Seg {
+    int b0, nb, c0, nc, g0, ng;
+};
 
 struct Plan {
-    int seg;       // steps per segment (all but the last)
-    int nseg;      // segments
-    size_t act_in, bc_in, act_out;  // bytes of one slot's u (and delta, z), B (and C), y
-    size_t state;                   // bytes of one state (batch * dim * 16 fp32)
-    size_t scan_ws;                 // bytes of ssm_scan_fwd's workspace (one segment)
-    size_t slot, total;
+    std::vector<Seg> segs;
+    long long max_rows = 0, max_bcrows = 0, max_nc = 0;
+    size_t act_in = 0, bc_in = 0, act_out = 0, state = 0, par = 0;  // one slot's regions
+    size_t scan_ws = 0;  // bytes of ssm_scan_fwd's workspace for the largest segment
+    size_t slot = 0, total = 0;
 };
 
 size_t r256(size_t x) { return (x + 255) & ~size_t(255); }
 
 Plan plan_for(int batch, int dim, int seqlen, int ngroups, size_t es, size_t eo) {
     Plan p{};
-    // about eight segments, each a multiple of 128 steps (16-byte rows for
-    // TMA, and the sequence-parallel scan's chunk boundaries where the whole
-    // sequence's scan has them)
-    const int want = (seqlen + 7) / 8;
-    p.seg = std::max(128, (want + 127) / 128 * 128);
-    p.seg = std::min(p.seg, std::max(seqlen, 1));
-    p.nseg = seqlen > 0 ? (seqlen + p.seg - 1) / p.seg : 0;
-    const size_t rows = (size_t)batch * dim, bcrows = (size_t)batch * ngroups * kN;
-    p.act_in = r256(rows * p.seg * es);
-    p.bc_in = r256(bcrows * p.seg * es);
-    p.act_out = r256(rows * p.seg * eo);
-    p.state = r256(rows * kN * 4);
-    p.scan_ws = r256(ssm_scan_workspace_bytes(batch, dim, p.seg, kN, ngroups));
-    p.slot = 3 * p.act_in + 2 * p.bc_in + p.act_out;
-    // scan workspace first (ssm_last_device_status reads its header), then the
-    // two slots and the two states (a segment's initial and final state)
-    p.total = p.scan_ws + kSlots * p.slot + 2 * p.state;
+    const long long rows = (long long)batch * dim;
+    const int cg = dim / ngroups;  // channels per group
+    const long long target = std::max(1LL, (rows + kTargetSegments - 1) / kTargetSegments);
+    if (target >= dim) {
+        const int per = (int)std::min<long long>(target / dim, batch);
+        for (int b = 0; b < batch; b += per)
+            p.segs.push_back({b, std::min(per, batch - b), 0, dim, 0, ngroups});
+    } else if (target >= cg) {
+        const int per = (int)(target / cg);
+        for (int b = 0; b < batch; ++b)
+            for (int g = 0; g < ngroups; g += per) {
+                const int ng = std::min(per, ngroups - g);
+                p.segs.push_back({b, 1, g * cg, ng * cg, g, ng});
+            }
+    } else {
+        const int pieces = (int)((cg + target - 1) / target);
+        const int pc = (cg + pieces - 1) / pieces;
+        for (int b = 0; b < batch; ++b)
+            for (int g = 0; g < ngroups; ++g)
+                for (int c = 0; c < cg; c += pc)
+                    p.segs.push_back({b, 1, g * cg + c, std::min(pc, cg - c), g, 1});
+    }
+    // The first segment's input copy runs before anything can overlap it, and the
+    // last segment's scan and output copy after: both are halved.
+    if (p.segs.size() >= 2) {
+        std::vector<Seg> cut;
+        const size_t n = p.segs.size();
+        for (size_t i = 0; i < n; ++i) {
+            const Seg& sg = p.segs[i];
+            if (i != 0 && i != n - 1) {
+                cut.push_back(sg);
+                continue;
+            }
+            if (sg.nb > 1) {  // whole batches
+                const int h = sg.nb / 2;
+                cut.push_back({sg.b0, h, 0, dim, 0, ngroups});
+                cut.push_back({sg.b0 + h, sg.nb - h, 0, dim, 0, ngroups});
+            } else if (sg.ng > 1) {  // whole groups
+                const int h = sg.ng / 2;
+                cut.push_back({sg.b0, 1, sg.c0, h * cg, sg.g0, h});
+                cut.push_back({sg.b0, 1, sg.c0 + h * cg, (sg.ng - h) * cg, sg.g0 + h, sg.ng - h});
+            } else if (sg.nc > 1) {  // part of one group
+                const int h = sg.nc / 2;
+                cut.push_back({sg.b0, 1, sg.c0, h, sg.g0, 1});
+                cut.push_back({sg.b0, 1, sg.c0 + h, sg.nc - h, sg.g0, 1});
+            } else {
+                cut.push_back(sg);
+            }
+        }
+        p.segs.swap(cut);
+    }
+    for (const Seg& sg : p.segs) {
+        p.max_rows = std::max(p.max_rows, (long long)sg.nb * sg.nc);
+        p.max_bcrows = std::max(p.max_bcrows, (long long)sg.nb * sg.ng * kN);
+        p.max_nc = std::max(p.max_nc, (long long)sg.nc);
+        p.scan_ws = std::max(p.scan_ws, ssm_scan_workspace_bytes(sg.nb, sg.nc, seqlen, kN, sg.ng));
+    }
+    const size_t L = (size_t)seqlen;
+    p.act_in = r256((size_t)p.max_rows * L * es);
+    p.bc_in = r256((size_t)p.max_bcrows * L * es);
+    p.act_out = r256((size_t)p.max_rows * L * eo);
+    p.state = r256((size_t)p.max_rows * kN * 4);
+    p.par = r256((size_t)p.max_nc * 4);
+    p.scan_ws = r256(p.scan_ws);
+    // per slot: u, delta, z, B, C in; y out; the initial and final state; D
+    // and delta_bias slices that need realigning
+    p.slot = 3 * p.act_in + 2 * p.bc_in + p.act_out + 2 * p.state + 2 * p.par;
+    // scan workspace first (ssm_last_device_status reads its header)
+    p.total = p.scan_ws + kSlots * p.slot;
     return p;
 }
 
@@ -165,10 +232,6 @@ extern "C" ssm_status_t ssm_scan_fwd_host(const void* u, const void* delta, cons
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     void* scan_ws = ws;
-    auto slot_base = [&](int k) { return ws + pl.scan_ws + (size_t)(k % kSlots) * pl.slot; };
-    float* fsb[2] = {reinterpret_cast<float*>(ws + pl.scan_ws + kSlots * pl.slot),
-                     reinterpret_cast<float*>(ws + pl.scan_ws + kSlots * pl.slot + pl.state)};
-    const size_t sbytes = rows * kN * 4;
     bool ok = true;
     auto chk = [&](cudaError_t e) { ok = ok && e == cudaSuccess; };
 
@@ -177,61 +240,74 @@ extern "C" ssm_status_t ssm_scan_fwd_host(const void* u, const void* delta, cons
     chk(cudaEventRecord(q->ev_done, s));
     chk(cudaStreamWaitEvent(q->copy_in, q->ev_done, 0));
     chk(cudaStreamWaitEvent(q->copy_out, q->ev_done, 0));
-    if (initial_state) chk(cudaMemcpyAsync(fsb[1], initial_state, sbytes, cudaMemcpyHostToDevice, s));
-    if (seqlen == 0) {
-        if (final_state) {
-            if (!initial_state) chk(cudaMemsetAsync(fsb[1], 0, sbytes, s));
-            chk(cudaMemcpyAsync(final_state, fsb[1], sbytes, cudaMemcpyDeviceToHost, s));
-        }
-        return ok ? SSM_OK : SSM_ERR_CUDA;
-    }
-    const size_t L = (size_t)seqlen, bcrows = (size_t)batch * ngroups * kN;
+    const size_t L = (size_t)seqlen;
+    // the kernel and plan of the whole problem, used for every segment
+    const int path = ssm_internal::scan_uses_seg_path(batch, dim) ? 2 : 1;
     const int seg_ts = ssm_internal::scan_seg_plan_ts(batch, dim, seqlen);
     ssm_status_t rc = SSM_OK;
-    for (int k = 0; k < pl.nseg && ok && rc == SSM_OK; ++k) {
-        const int sl = k % kSlots;
-        const size_t t0 = (size_t)k * pl.seg;
-        const size_t Lk = std::min((size_t)pl.seg, L - t0);
-        uint8_t* base = slot_base(k);
-        uint8_t* du = base;
+    for (size_t k = 0; k < pl.segs.size() && ok && rc == SSM_OK; ++k) {
+        const Seg& sg = pl.segs[k];
+        const int sl = (int)(k % kSlots);
+        const size_t r0 = (size_t)sg.b0 * dim + sg.c0;            // first row
+        const size_t nrows = (size_t)sg.nb * sg.nc;
+        const size_t bc0 = ((size_t)sg.b0 * ngroups + sg.g0) * kN;  // first B/C row
+        const size_t nbc = (size_t)sg.nb * sg.ng * kN;
+        uint8_t* du = ws + pl.scan_ws + (size_t)sl * pl.slot;
         uint8_t* dd = du + pl.act_in;
         uint8_t* dz = dd + pl.act_in;
         uint8_t* dB = dz + pl.act_in;
         uint8_t* dC = dB + pl.bc_in;
         uint8_t* dy = dC + pl.bc_in;
+        float* dh0 = reinterpret_cast<float*>(dy + pl.act_out);
+        float* dfs = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dh0) + pl.state);
+        float* dD = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dfs) + pl.state);
+        float* dbias = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dD) + pl.par);
         // segment k's inputs into the slot, once the scan two segments back is done with it
-        if (k >= kSlots) chk(cudaStreamWaitEvent(q->copy_in, q->ev_comp[sl], 0));
-        auto in2d = [&](void* dst, const void* src, size_t nrows) {
-            chk(cudaMemcpy2DAsync(dst, Lk * es, static_cast<const uint8_t*>(src) + t0 * es, L * es,
-                                  Lk * es, nrows, cudaMemcpyHostToDevice, q->copy_in));
+        if (k >= (size_t)kSlots) chk(cudaStreamWaitEvent(q->copy_in, q->ev_comp[sl], 0));
+        auto in1d = [&](void* dst, const void* src, size_t off, size_t bytes) {
+            chk(cudaMemcpyAsync(dst, static_cast<const uint8_t*>(src) + off, bytes,
+                                cudaMemcpyHostToDevice, q->copy_in));
         };
-        in2d(du, u, rows);
-        in2d(dd, delta, rows);
-        if (z) in2d(dz, z, rows);
-        in2d(dB, B, bcrows);
-        in2d(dC, C, bcrows);
+        if (L > 0) {
+            in1d(du, u, r0 * L * es, nrows * L * es);
+            in1d(dd, delta, r0 * L * es, nrows * L * es);
+            if (z) in1d(dz, z, r0 * L * es, nrows * L * es);
+            in1d(dB, B, bc0 * L * es, nbc * L * es);
+            in1d(dC, C, bc0 * L * es, nbc * L * es);
+        }
+        if (initial_state) in1d(dh0, initial_state, r0 * kN * 4, nrows * kN * 4);
         chk(cudaEventRecord(q->ev_in[sl], q->copy_in));
-        // the scan of segment k on the caller's stream, from the previous state
+        // the scan of segment k on the caller's stream
         chk(cudaStreamWaitEvent(s, q->ev_in[sl], 0));
-        if (k >= kSlots) chk(cudaStreamWaitEvent(s, q->ev_out[sl], 0));
+        if (k >= (size_t)kSlots) chk(cudaStreamWaitEvent(s, q->ev_out[sl], 0));
         if (!ok) break;
-        const float* st_in = k == 0 ? (initial_state ? fsb[1] : nullptr) : fsb[(k - 1) % 2];
-        // every segment with the whole sequence's plan; the status word keeps
-        // the first timeout of any segment
+        // per-channel parameters of the segment: A's rows are 64 bytes (always
+        // 16-byte aligned); D and delta_bias slices are copied when their
+        // offset is not
+        const float* pD = D ? D + sg.c0 : nullptr;
+        const float* pbias = delta_bias ? delta_bias + sg.c0 : nullptr;
+        if (sg.c0 % 4 != 0) {
+            if (D) chk(cudaMemcpyAsync(dD, pD, (size_t)sg.nc * 4, cudaMemcpyDeviceToDevice, s));
+            if (delta_bias)
+                chk(cudaMemcpyAsync(dbias, pbias, (size_t)sg.nc * 4, cudaMemcpyDeviceToDevice, s));
+            pD = D ? dD : nullptr;
+            pbias = delta_bias ? dbias : nullptr;
+        }
         rc = ssm_internal::scan_forward_segment(
-            du, dd, A, dB, dC, D, z ? dz : nullptr, delta_bias, delta_softplus, st_in, dy,
-            fsb[k % 2], batch, dim, (int)Lk, ngroups, in_dtype, out_dtype, scan_ws, pl.scan_ws, s,
-            seg_ts, k > 0);
+            du, dd, A + (size_t)sg.c0 * kN, dB, dC, pD, z ? dz : nullptr, pbias, delta_softplus,
+            initial_state ? dh0 : nullptr, dy, final_state ? dfs : nullptr, sg.nb, sg.nc,
+            seqlen, sg.ng, in_dtype, out_dtype, scan_ws, pl.scan_ws, s, seg_ts, k > 0, path);
         chk(cudaEventRecord(q->ev_comp[sl], s));
-        // segment k's y back to the host
+        // segment k's y and final state back to the host
         chk(cudaStreamWaitEvent(q->copy_out, q->ev_comp[sl], 0));
-        chk(cudaMemcpy2DAsync(static_cast<uint8_t*>(y) + t0 * eo, L * eo, dy, Lk * eo, Lk * eo, rows,
-                              cudaMemcpyDeviceToHost, q->copy_out));
+        if (L > 0)
+            chk(cudaMemcpyAsync(static_cast<uint8_t*>(y) + r0 * L * eo, dy, nrows * L * eo,
+                                cudaMemcpyDeviceToHost, q->copy_out));
+        if (final_state)
+            chk(cudaMemcpyAsync(final_state + r0 * kN, dfs, nrows * kN * 4, cudaMemcpyDeviceToHost,
+                                q->copy_out));
         chk(cudaEventRecord(q->ev_out[sl], q->copy_out));
     }
-    if (ok && rc == SSM_OK && final_state)
-        chk(cudaMemcpyAsync(final_state, fsb[(pl.nseg - 1) % 2], sbytes, cudaMemcpyDeviceToHost,
-                            q->copy_out));
     // the caller's stream completes after every copy of this call
     chk(cudaEventRecord(q->ev_done, q->copy_out));
     chk(cudaStreamWaitEvent(s, q->ev_done, 0));

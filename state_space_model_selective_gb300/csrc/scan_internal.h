@@ -23,11 +23,13 @@ ssm_status_t scan_forward_checkpoints(const void* u, const void* delta, const fl
                                       ssm_dtype_t in_dtype, void* workspace,
                                       cudaStream_t stream);
 
-// ssm_scan_fwd (validation included) for one piece of a sequence scanned in
-// pieces: seg_ts forces the sequence-parallel path's segments per chunk (0:
-// planned for this piece), so that every piece uses the whole sequence's
-// plan; keep_status leaves the workspace's status word as the previous piece
-// left it, so that a timeout in any piece stays visible.
+// ssm_scan_fwd (validation included) for one piece of a problem scanned in
+// pieces (a range of its channels): path forces the kernel (0: planned for
+// this piece, 1: the chained scan, 2: the sequence-parallel scan) and seg_ts
+// the sequence-parallel path's segments per chunk (0: planned), so that every
+// piece runs exactly as it would inside the whole problem's call; keep_status
+// leaves the workspace's status word as the previous piece left it, so that a
+// timeout in any piece stays visible.
 ssm_status_t scan_forward_segment(const void* u, const void* delta, const float* A, const void* B,
                                   const void* C, const float* D, const void* z,
                                   const float* delta_bias, int delta_softplus,
@@ -35,7 +37,10 @@ ssm_status_t scan_forward_segment(const void* u, const void* delta, const float*
                                   int batch, int dim, int seqlen, int ngroups,
                                   ssm_dtype_t in_dtype, ssm_dtype_t out_dtype, void* workspace,
                                   size_t workspace_bytes, cudaStream_t stream, int seg_ts,
-                                  bool keep_status);
+                                  bool keep_status, int path);
+
+// Whether ssm_scan_fwd takes the sequence-parallel path for this many channels.
+bool scan_uses_seg_path(long long batch, long long dim);
 
 // ---- the sequence-parallel path (scan_seg.cu)
 

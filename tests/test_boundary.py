@@ -527,3 +527,7 @@ def test_rope_rejects_bad_arguments_on_the_host(L):
     assert rope_call(L, Br=P(0)) == ALIAS            # output over an input
     assert rope_call(L, Cr=P(4)) == ALIAS            # the two outputs overlap
     assert rope_call(L, batch=0) == OK               # nothing to do, nothing launched
+    # a tile's (step, rank, head) offsets must fit in int: 32 steps x 2^20 heads x 128
+    far = [ctypes.c_void_p(0x10000000000 * (i + 1)) for i in range(7)]
+    assert rope_call(L, B=far[0], C=far[1], dt=far[2], theta=far[3], Br=far[4], Cr=far[5],
+                     aout=far[6], nheads=1 << 20, ngroups=1 << 20, dstate=128) == UNSUP

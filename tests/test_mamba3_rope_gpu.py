@@ -66,6 +66,18 @@ def test_rope_matches_oracle(case):
     np.testing.assert_allclose(to64(ang), ang_ref, rtol=2e-6, atol=2e-6)
 
 
+def test_rope_empty_sequence_hands_the_angle_on():
+    """seqlen 0: no rows to rotate; the final angle is the initial one."""
+    r = inputs.rope_inputs(2, 1, 3, 16, seed=5, device="cuda")
+    B = torch.zeros(2, 0, 1, 16, device="cuda")
+    dt = torch.zeros(2, 0, 3, device="cuda")
+    th = torch.zeros(2, 0, 3, 8, device="cuda")
+    Br, Cr, ang = binding.ssm_mamba3_rope(B, B.clone(), dt, th, r["angle0"])
+    torch.cuda.synchronize()
+    assert Br.shape == (2, 0, 3, 16) and Cr.shape == (2, 0, 3, 16)
+    assert torch.equal(ang, r["angle0"])
+
+
 def test_rope_resumes_in_place():
     """Three calls over consecutive pieces, the angle updated in place,
     give the bits of one call over the whole sequence."""

@@ -301,13 +301,20 @@ def test_workload_scan_bf16_whole(shape, seed):
                                   (2, 32, 30, 1, "f32", torch.float32, True),
                                   (5, 64, 300, 1, "bf16", torch.float32, True),
                                   (9, 48, 130, 2, "f32", torch.float32, False),
-                                  (4, 32, 64, 4, "bf16", torch.bfloat16, True)],
+                                  (4, 32, 64, 4, "bf16", torch.bfloat16, True),
+                                  (2, 36, 200, 6, "f32", torch.float32, True),
+                                  (1, 100, 300, 1, "bf16", torch.float32, True),
+                                  (2, 2048, 256, 1, "bf16", torch.float32, True)],
                          ids=["bf16-L700", "f32-L1000-G2", "bf16out-L64", "L30",
-                              "B5-L300", "B9-G2-L130", "B4-bf16out-G4"])
+                              "B5-L300", "B9-G2-L130", "B4-bf16out-G4", "G6-whole-groups",
+                              "part-groups-D100", "chained-whole"])
 def test_scan_host_buffers_equal_device_scan(case):
     """ssm_scan_fwd_host (host-resident activations, copies pipelined over
-    segments chained through the state) gives the same bits as ssm_scan_fwd on
-    device copies, and matches the oracle."""
+    segments of the channels) gives the same bits as ssm_scan_fwd on device
+    copies, and matches the oracle.  The cases cut segments at whole batches,
+    whole groups (channel offsets that leave D and the bias unaligned) and
+    inside a group; the last is a problem the chained scan takes whose
+    segments alone would take the sequence-parallel one."""
     batch, dim, seqlen, ngroups, dt, out_dt, with_h0 = case
     inp = inputs.scan_inputs(batch, dim, seqlen, 16, ngroups, dt, seed=120 + seqlen)
     h0 = (torch.randn(batch, dim, 16, generator=torch.Generator().manual_seed(3)) * 0.5
