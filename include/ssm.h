@@ -677,9 +677,9 @@ ssm_status_t ssd_mamba3_mimo_bwd(const void* x, const float* dt, const float* la
 
 /*
  * Bytes of device workspace ssm_scan_fwd_host needs (a pure function of its
- * arguments; 0 if they are invalid).  Two segments' worth of u, delta, z, B, C,
- * y and states (a segment is about 1/8 of the (batch, channel) rows, all
- * steps), plus the largest segment's ssm_scan_workspace_bytes.
+ * arguments; 0 if they are invalid).  Four slots, each the largest segment's u,
+ * delta, z, B, C, y and states (a segment is at most about 1/8 of the (batch,
+ * channel) rows, all steps), plus the largest segment's ssm_scan_workspace_bytes.
  */
 size_t ssm_scan_fwd_host_workspace_bytes(int batch, int dim, int seqlen, int dstate, int ngroups,
                                          ssm_dtype_t in_dtype, ssm_dtype_t out_dtype);

@@ -10,18 +10,19 @@
 //
 // How: the (batch, channel) rows are cut into about eight segments, each a
 // contiguous range of rows -- whole batches, whole B/C groups of one batch, or
-// part of one group; the first and the last are halved again, since nothing
+// part of one group; the first and the last are cut smaller, since nothing
 // overlaps the first one's input copy or the last one's scan and output copy --
 // so that every array of a segment (u, delta, z, y, the
 // states, and its groups' B and C) is one contiguous block of host memory,
 // moved by a single 1-D copy at the link's full rate (2-D copies of short rows
 // run well below it).  Segment k's inputs are copied on a copy stream into one
-// of two device slots, the caller's stream scans the slot with the kernel and
+// of four device slots, the caller's stream scans the slot with the kernel and
 // plan the whole problem would use (so the result is the whole call's, bit for
-// bit), and a second copy stream brings y and the final state back.  Copies in
-// both directions run on the copy engines while the SMs scan the neighbouring
-// segments.  The two copy streams and the events are created once per device
-// and kept for the life of the process.
+// bit), and a second copy stream brings y and the final state back.  Four
+// slots let the input copies run up to three segments ahead of the scans.
+// Copies in both directions run on the copy engines while the SMs scan the
+// neighbouring segments.  The two copy streams and the events are created once
+// per device and kept for the life of the process.
 #include <algorithm>
 #include <mutex>
 #include <vector>
@@ -34,7 +35,7 @@ namespace {
 using namespace ssm_host;
 
 constexpr int kN = 16;
-constexpr int kSlots = 2;
+constexpr int kSlots = 4;
 constexpr long long kTargetSegments = 8;
 
 // One segment: batches [b0, b0 + nb), channels [c0, c0 + nc) of each, which lie
@@ -81,31 +82,33 @@ Plan plan_for(int batch, int dim, int seqlen, int ngroups, size_t es, size_t eo)
                     p.segs.push_back({b, 1, g * cg + c, std::min(pc, cg - c), g, 1});
     }
     // The first segment's input copy runs before anything can overlap it, and the
-    // last segment's scan and output copy after: both are halved.
+    // last segment's scan and output copy after: the end segments are halved.
+    // (Halving them again measured slower: a scan of a segment takes about as
+    // long whatever its size, about 0.8 ms on the largest problems, and more
+    // of them no longer hide behind the copies.)
+    auto halve = [&](const Seg& sg, std::vector<Seg>& out) {
+        if (sg.nb > 1) {  // whole batches
+            const int h = sg.nb / 2;
+            out.push_back({sg.b0, h, 0, dim, 0, ngroups});
+            out.push_back({sg.b0 + h, sg.nb - h, 0, dim, 0, ngroups});
+        } else if (sg.ng > 1) {  // whole groups
+            const int h = sg.ng / 2;
+            out.push_back({sg.b0, 1, sg.c0, h * cg, sg.g0, h});
+            out.push_back({sg.b0, 1, sg.c0 + h * cg, (sg.ng - h) * cg, sg.g0 + h, sg.ng - h});
+        } else if (sg.nc > 1) {  // part of one group
+            const int h = sg.nc / 2;
+            out.push_back({sg.b0, 1, sg.c0, h, sg.g0, 1});
+            out.push_back({sg.b0, 1, sg.c0 + h, sg.nc - h, sg.g0, 1});
+        } else {
+            out.push_back(sg);
+        }
+    };
     if (p.segs.size() >= 2) {
         std::vector<Seg> cut;
         const size_t n = p.segs.size();
         for (size_t i = 0; i < n; ++i) {
-            const Seg& sg = p.segs[i];
-            if (i != 0 && i != n - 1) {
-                cut.push_back(sg);
-                continue;
-            }
-            if (sg.nb > 1) {  // whole batches
-                const int h = sg.nb / 2;
-                cut.push_back({sg.b0, h, 0, dim, 0, ngroups});
-                cut.push_back({sg.b0 + h, sg.nb - h, 0, dim, 0, ngroups});
-            } else if (sg.ng > 1) {  // whole groups
-                const int h = sg.ng / 2;
-                cut.push_back({sg.b0, 1, sg.c0, h * cg, sg.g0, h});
-                cut.push_back({sg.b0, 1, sg.c0 + h * cg, (sg.ng - h) * cg, sg.g0 + h, sg.ng - h});
-            } else if (sg.nc > 1) {  // part of one group
-                const int h = sg.nc / 2;
-                cut.push_back({sg.b0, 1, sg.c0, h, sg.g0, 1});
-                cut.push_back({sg.b0, 1, sg.c0 + h, sg.nc - h, sg.g0, 1});
-            } else {
-                cut.push_back(sg);
-            }
+            if (i == 0 || i == n - 1) halve(p.segs[i], cut);
+            else cut.push_back(p.segs[i]);
         }
         p.segs.swap(cut);
     }
