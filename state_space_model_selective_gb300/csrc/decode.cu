@@ -409,7 +409,13 @@ __global__ void __launch_bounds__(kBulkThreads)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nchunks = (headdim + kBulkRows - 1) / kBulkRows;
     const long long ntiles = (long long)batch * nheads * nchunks;
-    const long long my = ntiles > blockIdx.x ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    // CTA k takes an equal contiguous range of tiles: consecutive heads of one
+    // batch share their group's B, prev_B and C, which then stay in registers.
+    // (Measured against the strided order, CTA k taking tiles k, k + grid, ...:
+    // 106 against 114 us on batch 256, 32 heads, rank 4; runs of 2-16
+    // consecutive tiles, strided, balance worse.)
+    const long long t_begin = ntiles * blockIdx.x / gridDim.x;
+    const long long my = ntiles * (blockIdx.x + 1) / gridDim.x - t_begin;
 
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
@@ -421,7 +427,7 @@ __global__ void __launch_bounds__(kBulkThreads)
     __syncthreads();
 
     auto tile = [&](long long i, long long& bh, int& p0, int& nr) {
-        const long long t = blockIdx.x + i * gridDim.x;
+        const long long t = t_begin + i;
         bh = t / nchunks;
         p0 = (int)(t % nchunks) * kBulkRows;
         nr = min(kBulkRows, headdim - p0);
@@ -434,34 +440,69 @@ __global__ void __launch_bounds__(kBulkThreads)
 
     const long long rstride_x = (long long)nheads * headdim;  // between ranks of x
     const long long rstride_b = (long long)ngroups * kBulkN;  // between ranks of B
+    // the tile's per-head inputs (dt, lambda, A, this thread's share of the x and
+    // prev_x values the tile stages) are loaded one tile ahead, so that their
+    // latency hides behind the previous tile's work
+    constexpr int kStageVals = RK * kBulkRows / kBulkCompute;
+    static_assert(kStageVals * kBulkCompute == RK * kBulkRows, "staging split");
+    struct HeadIn {
+        float dtv, lam, A;
+        float xs[kStageVals], xps[kStageVals];
+    };
+    auto load_head = [&](long long i, HeadIn& t) {
+        long long bh; int p0, nr;
+        tile(i, bh, p0, nr);
+        const int h = (int)(bh % nheads);
+        const long long b = bh / nheads;
+        t.dtv = dt[bh];
+        t.lam = m3.lam[bh];
+        t.A = A[h];
+        const long long xrow0 = (b * RK * nheads + h) * (long long)headdim + p0;  // rank 0
+#pragma unroll
+        for (int j = 0; j < kStageVals; ++j) {
+            const int k = tid + j * kBulkCompute;
+            const int r = k / kBulkRows, p = k % kBulkRows;
+            const bool v = p < nr;
+            t.xs[j] = v ? to_f32(x[xrow0 + r * rstride_x + p]) : 0.0f;
+            t.xps[j] = v ? to_f32(m3.prev_x[xrow0 + r * rstride_x + p]) : 0.0f;
+        }
+    };
+    HeadIn nxt;
+    if (my > 0) load_head(0, nxt);
+    float bv[RK][4], bp[RK][4], cv[RK][4];  // the group's rows, while (b, g) stays
+    long long cur_bg = -1;
     for (long long i = 0; i < my; ++i) {
         const int s = (int)(i & 1);
+        const HeadIn cur = nxt;
         long long bh; int p0, nr;
         tile(i, bh, p0, nr);
         const int h = (int)(bh % nheads);
         const long long b = bh / nheads;
         const int g = h / (nheads / ngroups);
-        const long long bc = ((b * RK) * ngroups + g) * kBulkN + 4 * lane;
-        float bv[RK][4], bp[RK][4], cv[RK][4];
+        if (b * ngroups + g != cur_bg) {
+            cur_bg = b * ngroups + g;
+            const long long bc = ((b * RK) * ngroups + g) * kBulkN + 4 * lane;
 #pragma unroll
-        for (int r = 0; r < RK; ++r) {
-            load4<T>(Bm + bc + r * rstride_b, bv[r]);
-            load4<T>(m3.prev_B + bc + r * rstride_b, bp[r]);
-            load4<T>(Cm + bc + r * rstride_b, cv[r]);
+            for (int r = 0; r < RK; ++r) {
+                load4<T>(Bm + bc + r * rstride_b, bv[r]);
+                load4<T>(m3.prev_B + bc + r * rstride_b, bp[r]);
+                load4<T>(Cm + bc + r * rstride_b, cv[r]);
+            }
         }
-        const float dtv = dt[bh];
-        const float alpha = expf(dtv * A[h]);
-        const float gam = m3.lam[bh] * dtv;
+        const float dtv = cur.dtv;
+        const float alpha = expf(dtv * cur.A);
+        const float gam = cur.lam * dtv;
         const float bet = (dtv - gam) * alpha;
         const long long xrow0 = (b * RK * nheads + h) * (long long)headdim + p0;  // rank 0
         // stage gamma x and beta prev_x of the tile's rows (the previous tile's
         // reads are finished: named barrier at the end of each tile)
-        for (int k = tid; k < RK * kBulkRows; k += kBulkCompute) {
-            const int r = k / kBulkRows, p = k % kBulkRows;
-            const bool v = p < nr;
-            sx[k] = v ? gam * to_f32(x[xrow0 + r * rstride_x + p]) : 0.0f;
-            sxp[k] = v ? bet * to_f32(m3.prev_x[xrow0 + r * rstride_x + p]) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < kStageVals; ++j) {
+            const int k = tid + j * kBulkCompute;
+            sx[k] = gam * cur.xs[j];
+            sxp[k] = bet * cur.xps[j];
         }
+        if (i + 1 < my) load_head(i + 1, nxt);
         // every compute warp takes the same branch: a timed-out wait ends all of
         // them here, before the barrier at the end of the tile
         const bool got = mbar_wait(&full[s], (uint32_t)((i >> 1) & 1), nullptr);
