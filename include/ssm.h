@@ -689,7 +689,8 @@ size_t ssm_scan_fwd_host_workspace_bytes(int batch, int dim, int seqlen, int dst
  *   Computes exactly what ssm_scan_fwd computes, same arguments and layouts,
  *   but u, delta, z, B, C, initial_state, y and final_state are HOST pointers to
  *   page-locked memory (cudaHostAlloc / cudaMallocHost / cudaHostRegister;
- *   anything else returns SSM_ERR_UNSUPPORTED); A, D, delta_bias and the
+ *   anything else returns SSM_ERR_UNSUPPORTED, except arrays of zero bytes,
+ *   which are never touched); A, D, delta_bias and the
  *   workspace are DEVICE pointers.  Every channel's recurrence is independent
  *   of the others, so the (batch, channel) rows are cut into about eight
  *   segments -- whole batches, whole B/C groups of one batch, or part of one

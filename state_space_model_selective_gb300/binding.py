@@ -348,7 +348,9 @@ def ssm_scan_fwd_host_workspace_bytes(batch, dim, seqlen, dstate=16, ngroups=1,
 
 
 def _pinned(t, name, dtype=None, ndim=None):
-    if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_pinned():
+    # an empty tensor is never read or written, and may not be page-locked
+    if (not isinstance(t, torch.Tensor) or t.is_cuda
+            or (t.numel() > 0 and not t.is_pinned())):
         raise TypeError(f"{name} must be a pinned (page-locked) CPU tensor")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")

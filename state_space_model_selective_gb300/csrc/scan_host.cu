@@ -222,7 +222,11 @@ extern "C" ssm_status_t ssm_scan_fwd_host(const void* u, const void* delta, cons
     if (workspace_bytes < pl.total) return SSM_ERR_WORKSPACE;
     // where each pointer lives: activations and results on the host (page-locked),
     // parameters and workspace on the device
-    const void* host_ptrs[] = {u, delta, z, B, C, initial_state, y, final_state};
+    // (arrays of no bytes -- the activations when seqlen is 0 -- are never touched)
+    const void* host_ptrs[] = {seqlen ? u : nullptr, seqlen ? delta : nullptr,
+                               seqlen ? z : nullptr,  seqlen ? B : nullptr,
+                               seqlen ? C : nullptr,  initial_state,
+                               seqlen ? y : nullptr,  final_state};
     for (const void* p : host_ptrs)
         if (!is_pinned(p)) return SSM_ERR_UNSUPPORTED;
     for (const void* p : dev_ptrs)

@@ -335,3 +335,21 @@ def test_scan_host_buffers_equal_device_scan(case):
         tol = TOL_F32 if dt == "f32" else TOL_BF16
         assert_close(y_h, y_ref, tol, "y")
         assert_close(fs_h, fs_ref, tol, "final_state")
+
+
+@pytest.mark.parametrize("with_h0", [True, False])
+def test_scan_host_empty_sequence(with_h0):
+    """ssm_scan_fwd_host with seqlen 0: no rows to scan; the final state is the
+    initial state (zeros without one), as ssm_scan_fwd gives."""
+    batch, dim = 3, 40
+    inp = inputs.scan_inputs(batch, dim, 0, 16, 2, "bf16", seed=7)
+    h0 = torch.randn(batch, dim, 16, generator=torch.Generator().manual_seed(5)) if with_h0 else None
+    pin = {k: (v.pin_memory() if isinstance(v, torch.Tensor) and k in ("u", "delta", "z", "B", "C")
+               else v) for k, v in inp.items()}
+    y_h = torch.empty((batch, dim, 0), dtype=torch.float32).pin_memory()
+    fs_h = torch.full((batch, dim, 16), float("nan")).pin_memory()
+    binding.ssm_scan_fwd_host(pin["u"], pin["delta"], inp["A"].cuda(), pin["B"], pin["C"], y_h,
+                              fs_h, inp["D"].cuda(), pin["z"], inp["delta_bias"].cuda(), True,
+                              None if h0 is None else h0.pin_memory())
+    torch.cuda.synchronize()
+    assert torch.equal(fs_h, h0 if with_h0 else torch.zeros_like(fs_h))
