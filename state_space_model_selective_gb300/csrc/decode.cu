@@ -406,6 +406,8 @@ __global__ void __launch_bounds__(kBulkThreads)
     // the tile's weighted inputs, gamma x[r][p] and beta prev_x[r][p], fp32
     float* sx = reinterpret_cast<float*>(dsm + 2 * kTileBytes + 64);
     float* sxp = sx + RK * kBulkRows;
+    float* sxr = sxp + RK * kBulkRows;  // x itself (the skip term), and z (the gate)
+    float* szr = sxr + RK * kBulkRows;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nchunks = (headdim + kBulkRows - 1) / kBulkRows;
     const long long ntiles = (long long)batch * nheads * nchunks;
@@ -446,8 +448,8 @@ __global__ void __launch_bounds__(kBulkThreads)
     constexpr int kStageVals = RK * kBulkRows / kBulkCompute;
     static_assert(kStageVals * kBulkCompute == RK * kBulkRows, "staging split");
     struct HeadIn {
-        float dtv, lam, A;
-        float xs[kStageVals], xps[kStageVals];
+        float dtv, lam, A, D;
+        float xs[kStageVals], xps[kStageVals], zs[kStageVals];
     };
     auto load_head = [&](long long i, HeadIn& t) {
         long long bh; int p0, nr;
@@ -457,6 +459,7 @@ __global__ void __launch_bounds__(kBulkThreads)
         t.dtv = dt[bh];
         t.lam = m3.lam[bh];
         t.A = A[h];
+        t.D = Dskip ? Dskip[h] : 0.0f;
         const long long xrow0 = (b * RK * nheads + h) * (long long)headdim + p0;  // rank 0
 #pragma unroll
         for (int j = 0; j < kStageVals; ++j) {
@@ -465,6 +468,7 @@ __global__ void __launch_bounds__(kBulkThreads)
             const bool v = p < nr;
             t.xs[j] = v ? to_f32(x[xrow0 + r * rstride_x + p]) : 0.0f;
             t.xps[j] = v ? to_f32(m3.prev_x[xrow0 + r * rstride_x + p]) : 0.0f;
+            t.zs[j] = (v && z) ? to_f32(z[xrow0 + r * rstride_x + p]) : 0.0f;
         }
     };
     HeadIn nxt;
@@ -501,6 +505,8 @@ __global__ void __launch_bounds__(kBulkThreads)
             const int k = tid + j * kBulkCompute;
             sx[k] = gam * cur.xs[j];
             sxp[k] = bet * cur.xps[j];
+            sxr[k] = cur.xs[j];
+            szr[k] = cur.zs[j];
         }
         if (i + 1 < my) load_head(i + 1, nxt);
         // every compute warp takes the same branch: a timed-out wait ends all of
@@ -562,15 +568,15 @@ __global__ void __launch_bounds__(kBulkThreads)
             const int p = warp + 4 * (4 * g4 + k4);
             if ((lane & (kLow - 1)) == 0 && p < nr) {
                 const long long row = xrow0 + r * rstride_x + p;
-                float out = acc[0] + (Dskip ? Dskip[h] : 0.0f) * to_f32(x[row]);
-                if (z) out *= silu_f(to_f32(z[row]));
+                float out = acc[0] + cur.D * sxr[r * kBulkRows + p];
+                if (z) out *= silu_f(szr[r * kBulkRows + p]);
                 y[row] = from_f32<T>(out);
             }
         }
         fence_proxy_async_smem();  // the updated tile is read by the bulk store
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-        named_bar_sync(1, kBulkCompute);  // sx, sxp are rewritten for the next tile
+        named_bar_sync(1, kBulkCompute);  // sx, sxp, sxr, szr are rewritten for the next tile
     }
 }
 
@@ -623,7 +629,7 @@ ssm_status_t launch_bulk_mimo(float* state, const void* x, const float* dt, cons
                 return SSM_ERR_CUDA;
             if (cudaFuncSetAttribute(decode_bulk_mimo_kernel<T, RK>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kBulkSmem + 2 * RK * kBulkRows * 4) != cudaSuccess)
+                                     kBulkSmem + 4 * RK * kBulkRows * 4) != cudaSuccess)
                 return SSM_ERR_CUDA;
             cached_dev = dev;
         }
@@ -631,7 +637,7 @@ ssm_status_t launch_bulk_mimo(float* state, const void* x, const float* dt, cons
     const long long tiles =
         (long long)batch * nheads * ((headdim + kBulkRows - 1) / kBulkRows);
     const unsigned grid = (unsigned)std::min<long long>(tiles, 3LL * sms);
-    decode_bulk_mimo_kernel<T, RK><<<grid, kBulkThreads, kBulkSmem + 2 * RK * kBulkRows * 4, s>>>(
+    decode_bulk_mimo_kernel<T, RK><<<grid, kBulkThreads, kBulkSmem + 4 * RK * kBulkRows * 4, s>>>(
         state, static_cast<const T*>(x), dt, A, static_cast<const T*>(B),
         static_cast<const T*>(C), D, static_cast<const T*>(z), static_cast<T*>(y), batch, nheads,
         headdim, ngroups, m3);
