@@ -15,10 +15,10 @@
 //    and walks the chunk's time steps in order.
 //  * A producer warp streams 64-step tiles of u, delta, z, B and C into a
 //    ring of shared-memory stages with 2-D TMA (128-byte swizzle), tracked
-//    by mbarriers.  The compute warps first "prep" each tile once per
-//    (channel, step) -- dl = softplus(delta + bias) and dl*u -- then run the
-//    recurrence, reading B and C straight from their [n][t] tiles (one
-//    16-byte load covers 8 bf16 or 4 fp32 steps of one state).
+//    by mbarriers.  The compute warps first "prep" each group of 16 or 64
+//    steps of a tile once per (channel, step) -- dl = softplus(delta + bias)
+//    and dl*u -- then run the group's recurrence, reading B and C from the
+//    tile's fp32 [t][state group] rows.
 //  * y partial sums over the 4 lanes' states are reduce-scattered with warp
 //    shuffles; each lane then finishes 2 of every 8 steps (D skip, silu gate)
 //    and stores them.
@@ -45,8 +45,9 @@ constexpr int kSPT = 4;         // states per thread
 constexpr int kNG = kN / kSPT;  // threads per channel
 constexpr int kTL = 64;         // time steps per tile
 constexpr int kMaxChunks = 32;  // upper bound on L-chunks per channel block
-constexpr int kPrepStride = kTL * 8 + 16;  // bytes per channel row of the prep tile
-constexpr int kGroupUnroll = 4;  // 8-step groups unrolled together
+// Steps prepped at a time (PS): 16 (a quarter of a tile, so that four CTAs'
+// shared memory fits on an SM) or 64 (the whole tile, three CTAs).
+__host__ __device__ constexpr int prep_stride(int ps) { return ps * 8 + 16; }  // bytes per channel row
 
 struct alignas(16) WsHeader {
     uint32_t ticket;
@@ -120,6 +121,18 @@ __device__ __forceinline__ void load8(const uint8_t* tile, int r, int t0, float*
         const float4 b = *reinterpret_cast<const float4*>(tile + tile_off<T, ROWS>(r, t0 + 4));
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
         v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+}
+
+// 4 consecutive steps t0..t0+3 (t0 % 4 == 0) of row r, as fp32.
+template <typename T, int ROWS>
+__device__ __forceinline__ void load4s(const uint8_t* tile, int r, int t0, float* v) {
+    if constexpr (sizeof(T) == 2) {
+        const uint2 w = *reinterpret_cast<const uint2*>(tile + tile_off<T, ROWS>(r, t0));
+        v[0] = bf16lo(w.x); v[1] = bf16hi(w.x); v[2] = bf16lo(w.y); v[3] = bf16hi(w.y);
+    } else {
+        const float4 a = *reinterpret_cast<const float4*>(tile + tile_off<T, ROWS>(r, t0));
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
     }
 }
 
@@ -223,7 +236,7 @@ struct Geom {
     static constexpr int kStages = 2;
 };
 
-template <typename Tin, int CH, bool TMA>
+template <typename Tin, int CH, bool TMA, int PS>
 struct Smem {
     static constexpr int E = sizeof(Tin);
     static constexpr int IN_TILE = CH * kTL * E;
@@ -234,22 +247,25 @@ struct Smem {
     static_assert(2 * BC_TILE <= BCF, "the B/C tiles fit the converted region");
     static constexpr int STAGE = 3 * IN_TILE + BCF;
     static constexpr int NSTAGE = TMA ? Geom<Tin>::kStages : 1;
-    static constexpr int PREP = 2 * CH * kPrepStride;  // (dl, dl*u) and (D*u, silu(z))
+    static constexpr int PREP = 2 * CH * prep_stride(PS);  // (dl, dl*u) and (D*u, silu(z))
     static constexpr int BARS = 3 * NSTAGE * 8 + 16;
     static constexpr int BYTES = NSTAGE * STAGE + PREP + BARS;
     static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024
 };
 
-template <typename Tin, typename Tout, int CH, bool TMA, int CK = 0>
-__global__ void __launch_bounds__(CH * kNG + 32, 3)
+template <typename Tin, typename Tout, int CH, bool TMA, int CK, int PS>
+__global__ void __launch_bounds__(CH * kNG + 32, PS == 16 ? 4 : 3)
     scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u,
                     const __grid_constant__ CUtensorMap tm_d,
                     const __grid_constant__ CUtensorMap tm_z,
                     const __grid_constant__ CUtensorMap tm_B,
                     const __grid_constant__ CUtensorMap tm_C, const ScanArgs a) {
-    using S = Smem<Tin, CH, TMA>;
+    using S = Smem<Tin, CH, TMA, PS>;
     using G = Geom<Tin>;
     constexpr int NCOMP = CH * kNG;
+    constexpr int kPrepStride = prep_stride(PS);
+    constexpr int LPS = PS / 4;  // steps a lane preps per group
+    static_assert(PS == 16 || PS == 64, "prep groups of 16 or 64 steps");
     constexpr int NSTAGE = S::NSTAGE;
 
     extern __shared__ uint8_t smem_raw[];
@@ -423,140 +439,161 @@ __global__ void __launch_bounds__(CH * kNG + 32, 3)
             named_bar_sync(1, NCOMP);
         }
 
-        // ---- prep, once per (channel, step): dl = softplus(delta + bias)
-        // (or delta + bias), dl * u, and the read-out's D * u and silu(z);
-        // steps past the chunk end get dl = 0, an exact identity step
-        // (exp(0) = 1, input term 0).
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int tl = pq * 16 + hh * 8;
-            float uv[8], dv[8], zv[8];
-            load8<Tin, CH>(st, cl, tl, uv);
-            load8<Tin, CH>(st + S::IN_TILE, cl, tl, dv);
-            if (has_z) load8<Tin, CH>(st + 2 * S::IN_TILE, cl, tl, zv);
-            float o[16], e[16];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float x = dv[j] + pbias;
-                float dl = a.softplus ? softplus_f(x) : x;
-                if (t0 + tl + j >= t_end) dl = 0.0f;
-                o[2 * j] = dl;
-                o[2 * j + 1] = dl * uv[j];
-                if constexpr (CK != 2) {
-                    e[2 * j] = pD * uv[j];
-                    e[2 * j + 1] = has_z ? silu_f(zv[j]) : 1.0f;
-                }
-            }
-            float4* dst = reinterpret_cast<float4*>(prep + cl * kPrepStride + tl * 8);
-            float4* dst2 = reinterpret_cast<float4*>(prep + (CH + cl) * kPrepStride + tl * 8);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-                if constexpr (CK != 2)
-                    dst2[j] = make_float4(e[4 * j], e[4 * j + 1], e[4 * j + 2], e[4 * j + 3]);
-            }
-        }
-        __syncwarp();
-
-        // ---- carried-in state, once per CTA, after the first prep
-        if (k == 0) {
-            if (chunk == 0) {
-                if (a.h0 && valid) {
-                    const float4 v =
-                        *reinterpret_cast<const float4*>(a.h0 + drow * kN + n0);
-                    h[0] = v.x; h[1] = v.y; h[2] = v.z; h[3] = v.w;
-                }
-            } else {
-                const uint32_t* flag = a.flags + (size_t)(chunk - 1) * a.nblocks + blk;
-                if (lane == 0) {
-                    bool seen = false;
-                    uint32_t ns = 32;
-                    for (uint32_t it = 0; it < a.flag_spin_limit; ++it) {
-                        if (ld_acquire_gpu(flag)) { seen = true; break; }
-                        __nanosleep(ns);
-                        ns = ns < 256 ? ns * 2 : 256;
-                    }
-                    if (!seen) record_status(a.status, SSM_ERR_TIMEOUT);
-                }
-                __syncwarp();
-                (void)ld_acquire_gpu(flag);  // order this thread's reads after the flag
-                if (valid) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4*>(
-                        a.carry + ((size_t)(chunk - 1) * a.batch * a.dim + drow) * kN + n0));
-                    h[0] = v.x; h[1] = v.y; h[2] = v.z; h[3] = v.w;
-                }
-            }
-        }
-
-        // ---- the recurrence over the tile, 8 steps per group, B and C from
-        // the stage's fp32 [t][state group] rows (one broadcast address per
-        // quarter-warp), once the producer has converted them
-        if constexpr (TMA) {
-            const bool got = mbar_wait(&ready[s], (k / NSTAGE) & 1, a.status);
-            if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-        }
+        // The tile runs in groups of PS steps: each warp preps its own 8
+        // channels for the group (lane: channel cl, steps LPS pq .. LPS pq +
+        // LPS - 1), then runs the group's 8-step recurrence blocks.  Only one
+        // group's prep rows are held at a time.
         const uint8_t* tBC = st + 3 * S::IN_TILE + ng * 32;
-#pragma unroll kGroupUnroll
-        for (int j = 0; j < kTL / 8; ++j) {
-            if (CK != 0 && (j & 1) == 0 && valid && t0 + j * 8 < a.seqlen) {
-                const long long seg = (t0 + j * 8) / 16;
-                __stcg(reinterpret_cast<float4*>(
-                           a.ckpt + (seg * a.batch * a.dim + drow) * kN + n0),
-                       make_float4(h[0], h[1], h[2], h[3]));
-            }
-            float yp[8];
+        for (int qt = 0; qt < kTL / PS && ok; ++qt) {
+            // ---- prep, once per (channel, step): dl = softplus(delta + bias)
+            // (or delta + bias), dl * u, and the read-out's D * u and silu(z);
+            // steps past the chunk end get dl = 0, an exact identity step
+            // (exp(0) = 1, input term 0).
+            constexpr int CS = LPS >= 8 ? 8 : 4;  // steps per chunk (one 16- or 8-byte load)
 #pragma unroll
-            for (int q = 0; q < 8; q += 2) {
-                const float4 pp = *reinterpret_cast<const float4*>(prow + (j * 8 + q) * 2);
+            for (int c = 0; c < LPS / CS; ++c) {
+                const int tq = pq * LPS + c * CS;  // step within the group
+                const int tl = qt * PS + tq;       // step within the tile
+                float uv[CS], dv[CS], zv[CS];
+                if constexpr (CS == 8) {
+                    load8<Tin, CH>(st, cl, tl, uv);
+                    load8<Tin, CH>(st + S::IN_TILE, cl, tl, dv);
+                    if (has_z) load8<Tin, CH>(st + 2 * S::IN_TILE, cl, tl, zv);
+                } else {
+                    load4s<Tin, CH>(st, cl, tl, uv);
+                    load4s<Tin, CH>(st + S::IN_TILE, cl, tl, dv);
+                    if (has_z) load4s<Tin, CH>(st + 2 * S::IN_TILE, cl, tl, zv);
+                }
+                float o[2 * CS], e[2 * CS];
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    const int t = j * 8 + q + r;
-                    const float dl = r ? pp.z : pp.x;
-                    const float du = r ? pp.w : pp.y;
-                    const float4 bv = *reinterpret_cast<const float4*>(tBC + t * 128);
-                    h[0] = fmaf(ex2_approx(dl * A2[0]), h[0], du * bv.x);
-                    h[1] = fmaf(ex2_approx(dl * A2[1]), h[1], du * bv.y);
-                    h[2] = fmaf(ex2_approx(dl * A2[2]), h[2], du * bv.z);
-                    h[3] = fmaf(ex2_approx(dl * A2[3]), h[3], du * bv.w);
+                for (int j = 0; j < CS; ++j) {
+                    const float x = dv[j] + pbias;
+                    float dl = a.softplus ? softplus_f(x) : x;
+                    if (t0 + tl + j >= t_end) dl = 0.0f;
+                    o[2 * j] = dl;
+                    o[2 * j + 1] = dl * uv[j];
                     if constexpr (CK != 2) {
-                        const float4 cv = *reinterpret_cast<const float4*>(tBC + t * 128 + 16);
-                        float acc = cv.x * h[0];
-                        acc = fmaf(cv.y, h[1], acc);
-                        acc = fmaf(cv.z, h[2], acc);
-                        acc = fmaf(cv.w, h[3], acc);
-                        yp[q + r] = acc;
+                        e[2 * j] = pD * uv[j];
+                        e[2 * j + 1] = has_z ? silu_f(zv[j]) : 1.0f;
                     }
                 }
-            }
-            if constexpr (CK == 2) continue;  // states only: no read-out
-            // reduce-scatter the 8 partial sums over the 4 lanes of the channel
-            // (lane bits 3 and 4): afterwards lane ng holds the full sums of
-            // steps 2ng and 2ng+1, added as (p0 + p2) + (p1 + p3).
-            float f[2];
-            const bool hi2 = ng & 2, hi1 = ng & 1;
-            float k4[4];
+                float4* dst = reinterpret_cast<float4*>(prep + cl * kPrepStride + tq * 8);
+                float4* dst2 = reinterpret_cast<float4*>(prep + (CH + cl) * kPrepStride + tq * 8);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float send = hi2 ? yp[i] : yp[i + 4];
-                const float keep = hi2 ? yp[i + 4] : yp[i];
-                k4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+                for (int j = 0; j < CS / 2; ++j) {
+                    dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+                    if constexpr (CK != 2)
+                        dst2[j] = make_float4(e[4 * j], e[4 * j + 1], e[4 * j + 2], e[4 * j + 3]);
+                }
             }
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const float send = hi1 ? k4[i] : k4[i + 2];
-                const float keep = hi1 ? k4[i + 2] : k4[i];
-                f[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-            }
-            const int tl = j * 8 + 2 * ng;
-            const int tg = t0 + tl;
-            const float4 eg = *reinterpret_cast<const float4*>(prow2 + tl * 2);
-            const float o0 = (f[0] + eg.x) * eg.y;
-            const float o1 = (f[1] + eg.z) * eg.w;
-            if ((CK == 0 || a.y) && valid && tg < t_end)
-                store_y2<Tout>(yrow + tg, o0, o1, true, tg + 1 < t_end, vec_store);
-        }
+            __syncwarp();
 
-        __syncwarp();  // this warp's prep rows are rewritten by the next tile
+            if (qt == 0) {
+                // ---- carried-in state, once per CTA, after the first prep
+                if (k == 0) {
+                    if (chunk == 0) {
+                        if (a.h0 && valid) {
+                            const float4 v =
+                                *reinterpret_cast<const float4*>(a.h0 + drow * kN + n0);
+                            h[0] = v.x; h[1] = v.y; h[2] = v.z; h[3] = v.w;
+                        }
+                    } else {
+                        const uint32_t* flag = a.flags + (size_t)(chunk - 1) * a.nblocks + blk;
+                        if (lane == 0) {
+                            bool seen = false;
+                            uint32_t ns = 32;
+                            for (uint32_t it = 0; it < a.flag_spin_limit; ++it) {
+                                if (ld_acquire_gpu(flag)) { seen = true; break; }
+                                __nanosleep(ns);
+                                ns = ns < 256 ? ns * 2 : 256;
+                            }
+                            if (!seen) record_status(a.status, SSM_ERR_TIMEOUT);
+                        }
+                        __syncwarp();
+                        (void)ld_acquire_gpu(flag);  // order this thread's reads after the flag
+                        if (valid) {
+                            const float4 v = __ldcg(reinterpret_cast<const float4*>(
+                                a.carry + ((size_t)(chunk - 1) * a.batch * a.dim + drow) * kN + n0));
+                            h[0] = v.x; h[1] = v.y; h[2] = v.z; h[3] = v.w;
+                        }
+                    }
+                }
+                // ---- B and C from the stage's fp32 [t][state group] rows (one
+                // broadcast address per quarter-warp), once the producer has
+                // converted them
+                if constexpr (TMA) {
+                    const bool got = mbar_wait(&ready[s], (k / NSTAGE) & 1, a.status);
+                    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                }
+            }
+
+            // ---- the recurrence over the group, 8 steps per block (unrolled by
+            // 4 blocks at most: further unrolling measured slower)
+            constexpr int kUnroll = PS / 8 < 4 ? PS / 8 : 4;
+#pragma unroll kUnroll
+            for (int jj = 0; jj < PS / 8; ++jj) {
+                const int j = qt * (PS / 8) + jj;  // 8-step block within the tile
+                if (CK != 0 && (j & 1) == 0 && valid && t0 + j * 8 < a.seqlen) {
+                    const long long seg = (t0 + j * 8) / 16;
+                    __stcg(reinterpret_cast<float4*>(
+                               a.ckpt + (seg * a.batch * a.dim + drow) * kN + n0),
+                           make_float4(h[0], h[1], h[2], h[3]));
+                }
+                float yp[8];
+#pragma unroll
+                for (int q = 0; q < 8; q += 2) {
+                    const float4 pp = *reinterpret_cast<const float4*>(prow + (jj * 8 + q) * 2);
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int t = j * 8 + q + r;
+                        const float dl = r ? pp.z : pp.x;
+                        const float du = r ? pp.w : pp.y;
+                        const float4 bv = *reinterpret_cast<const float4*>(tBC + t * 128);
+                        h[0] = fmaf(ex2_approx(dl * A2[0]), h[0], du * bv.x);
+                        h[1] = fmaf(ex2_approx(dl * A2[1]), h[1], du * bv.y);
+                        h[2] = fmaf(ex2_approx(dl * A2[2]), h[2], du * bv.z);
+                        h[3] = fmaf(ex2_approx(dl * A2[3]), h[3], du * bv.w);
+                        if constexpr (CK != 2) {
+                            const float4 cv = *reinterpret_cast<const float4*>(tBC + t * 128 + 16);
+                            float acc = cv.x * h[0];
+                            acc = fmaf(cv.y, h[1], acc);
+                            acc = fmaf(cv.z, h[2], acc);
+                            acc = fmaf(cv.w, h[3], acc);
+                            yp[q + r] = acc;
+                        }
+                    }
+                }
+                if constexpr (CK == 2) continue;  // states only: no read-out
+                // reduce-scatter the 8 partial sums over the 4 lanes of the channel
+                // (lane bits 3 and 4): afterwards lane ng holds the full sums of
+                // steps 2ng and 2ng+1, added as (p0 + p2) + (p1 + p3).
+                float f[2];
+                const bool hi2 = ng & 2, hi1 = ng & 1;
+                float k4[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float send = hi2 ? yp[i] : yp[i + 4];
+                    const float keep = hi2 ? yp[i + 4] : yp[i];
+                    k4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+                }
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const float send = hi1 ? k4[i] : k4[i + 2];
+                    const float keep = hi1 ? k4[i + 2] : k4[i];
+                    f[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+                }
+                const int tq = jj * 8 + 2 * ng;  // step within the group
+                const int tg = t0 + j * 8 + 2 * ng;
+                const float4 eg = *reinterpret_cast<const float4*>(prow2 + tq * 2);
+                const float o0 = (f[0] + eg.x) * eg.y;
+                const float o1 = (f[1] + eg.z) * eg.w;
+                if ((CK == 0 || a.y) && valid && tg < t_end)
+                    store_y2<Tout>(yrow + tg, o0, o1, true, tg + 1 < t_end, vec_store);
+            }
+            __syncwarp();  // this warp's prep rows are rewritten by the next group
+        }
+        if (!ok) break;
+
         if constexpr (TMA) {
             if (lane == 0) mbar_arrive(&empty[s]);
         } else {
@@ -594,6 +631,7 @@ std::atomic<int> g_drop_first_publish{0};
 
 struct Plan {
     int CH;
+    int ps;  // steps prepped at a time: 16 (four CTAs per SM) or 64 (three)
     int bpg, nblocks, nchunks, chunk_tiles;
     bool tma;
 };
@@ -649,12 +687,12 @@ size_t workspace_bound(long long batch, long long dim, int seqlen, int ngroups) 
     return bytes;
 }
 
-template <typename Tin, typename Tout, int CH, bool TMA, int CK = 0>
+template <typename Tin, typename Tout, int CH, bool TMA, int CK, int PS>
 int occupancy_blocks() {
-    using S = Smem<Tin, CH, TMA>;
+    using S = Smem<Tin, CH, TMA, PS>;
     static int cached = -1;
     if (cached < 0) {
-        auto kern = scan_fwd_kernel<Tin, Tout, CH, TMA, CK>;
+        auto kern = scan_fwd_kernel<Tin, Tout, CH, TMA, CK, PS>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
         int nb = 0;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, CH * kNG + 32, S::ALLOC);
@@ -663,11 +701,11 @@ int occupancy_blocks() {
     return cached;
 }
 
-template <typename Tin, typename Tout, int CH, bool TMA, int CK = 0>
+template <typename Tin, typename Tout, int CH, bool TMA, int CK, int PS>
 ssm_status_t launch(const ScanArgs& base, const Plan& p, const CUtensorMap* maps,
                     cudaStream_t stream) {
-    using S = Smem<Tin, CH, TMA>;
-    auto kern = scan_fwd_kernel<Tin, Tout, CH, TMA, CK>;
+    using S = Smem<Tin, CH, TMA, PS>;
+    auto kern = scan_fwd_kernel<Tin, Tout, CH, TMA, CK, PS>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC) !=
         cudaSuccess)
         return SSM_ERR_CUDA;
@@ -685,14 +723,16 @@ ssm_status_t launch(const ScanArgs& base, const Plan& p, const CUtensorMap* maps
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
-template <typename Tin, typename Tout, int CH, bool TMA, int CK = 0>
+template <typename Tin, typename Tout, int CH, bool TMA, int CK, int PS>
 void plan_for(const ScanArgs& a, Plan& p) {
     p.CH = CH;
+    p.ps = PS;
     p.tma = TMA;
     p.bpg = (a.dpg + CH - 1) / CH;
     p.nblocks = a.batch * a.ngroups * p.bpg;
     const int tiles = (a.seqlen + kTL - 1) / kTL;
-    const long long slots = (long long)occupancy_blocks<Tin, Tout, CH, TMA, CK>() * dev_info().sms;
+    const long long slots =
+        (long long)occupancy_blocks<Tin, Tout, CH, TMA, CK, PS>() * dev_info().sms;
     int nchunks = 1;
     if (p.nblocks >= slots) {
         // Enough independent channel blocks to fill the GPU: cut L into
@@ -705,12 +745,31 @@ void plan_for(const ScanArgs& a, Plan& p) {
     p.nchunks = (tiles + p.chunk_tiles - 1) / p.chunk_tiles;
 }
 
+// The variant with 16-step prep groups holds four CTAs per SM; it runs when the
+// channel blocks fill four on every SM (the larger problems, where the extra
+// warps hide latency: batch 4, L 16384, 5120 channels in 1.84 ms against 1.92
+// with the whole-tile prep).  Otherwise the whole-tile prep at three CTAs per
+// SM, which does less work per step (batch 8, L 2048, 1536 channels: 176 us
+// against 180 with 16-step groups).
+template <typename Tin, typename Tout, bool TMA, int CK>
+void choose_plan_tma(const ScanArgs& a, Plan& p) {
+    plan_for<Tin, Tout, 32, TMA, CK, 16>(a, p);
+    const long long slots16 =
+        (long long)occupancy_blocks<Tin, Tout, 32, TMA, CK, 16>() * dev_info().sms;
+    if (p.nblocks < slots16) plan_for<Tin, Tout, 32, TMA, CK, 64>(a, p);
+}
+
+template <typename Tin, typename Tout, int CK>
+void choose_plan(const ScanArgs& a, bool tma, Plan& p) {
+    if (tma) choose_plan_tma<Tin, Tout, true, CK>(a, p);
+    else choose_plan_tma<Tin, Tout, false, CK>(a, p);
+}
+
 template <typename Tin, typename Tout, int CK = 0>
 ssm_status_t dispatch(ScanArgs& a, ssm_dtype_t in_dtype, bool tma, cudaStream_t stream,
                       void* workspace, bool keep_status = false) {
     Plan p{};
-    if (tma) plan_for<Tin, Tout, 32, true, CK>(a, p);
-    else plan_for<Tin, Tout, 32, false, CK>(a, p);
+    choose_plan<Tin, Tout, CK>(a, tma, p);
 
     // workspace: header | flags | carry
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -747,9 +806,11 @@ ssm_status_t dispatch(ScanArgs& a, ssm_dtype_t in_dtype, bool tma, cudaStream_t 
         if (okm && a.z)
             okm = ssm_host::make_tmap_2d(&maps[2], a.z, in_dtype, rows, a.seqlen, 32, tpb);
         if (!okm) return SSM_ERR_CUDA;
-        return launch<Tin, Tout, 32, true, CK>(a, p, maps, stream);
+        return p.ps == 16 ? launch<Tin, Tout, 32, true, CK, 16>(a, p, maps, stream)
+                          : launch<Tin, Tout, 32, true, CK, 64>(a, p, maps, stream);
     }
-    return launch<Tin, Tout, 32, false, CK>(a, p, maps, stream);
+    return p.ps == 16 ? launch<Tin, Tout, 32, false, CK, 16>(a, p, maps, stream)
+                      : launch<Tin, Tout, 32, false, CK, 64>(a, p, maps, stream);
 }
 
 }  // namespace
@@ -1021,8 +1082,7 @@ void* noalloc_scratch_address() {
 template <typename Tin, typename Tout>
 size_t planned_scratch_bytes(const ScanArgs& a, bool tma) {
     Plan p{};
-    if (tma) plan_for<Tin, Tout, 32, true>(a, p);
-    else plan_for<Tin, Tout, 32, false>(a, p);
+    choose_plan<Tin, Tout, 0>(a, tma, p);
     return sizeof(WsHeader) + round256(sizeof(uint32_t) * (size_t)(p.nchunks - 1) * p.nblocks) +
            (size_t)(p.nchunks - 1) * (size_t)a.batch * a.dim * kN * sizeof(float);
 }
