@@ -240,13 +240,17 @@ def test_scan_bwd_directional_derivatives(name, grad):
     assert abs(fd - an) <= 2e-3 * abs(an) + 1e-3 * float(terms.abs().sum()), (name, fd, an)
 
 
+@pytest.mark.parametrize("shape", [(2, 96, 530, 2), (4, 5120, 256, 1)],
+                         ids=["small", "640-blocks"])
 @pytest.mark.parametrize("dt,out_dt", [("bf16", torch.float32), ("f32", torch.bfloat16)])
-def test_scan_checkpoints_from_the_forward(dt, out_dt):
+def test_scan_checkpoints_from_the_forward(dt, out_dt, shape):
     """ssm_scan_fwd with checkpoints gives the plain forward's y and final state
     bit for bit, and ssm_scan_bwd from those checkpoints gives the same bits as
-    ssm_scan_bwd recomputing them."""
-    batch, dim, seqlen = 2, 96, 530
-    inp = inputs.scan_inputs(batch, dim, seqlen, 16, 2, dt, seed=140)
+    ssm_scan_bwd recomputing them.  The second shape has enough channel blocks
+    for the forward kernels' 16-step prep groups (four CTAs per SM) in all three
+    modes: plain, checkpointing and states only."""
+    batch, dim, seqlen, ngroups = shape
+    inp = inputs.scan_inputs(batch, dim, seqlen, 16, ngroups, dt, seed=140)
     x = {k: (_dev(v) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     h0 = torch.randn(batch, dim, 16, generator=torch.Generator().manual_seed(141)).cuda()
     args = (x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], True, h0)
