@@ -332,6 +332,13 @@ __global__ void __launch_bounds__(kBulkThreads)
             dbx[r] = p < nr ? wx * to_f32(x[row0 + p]) : 0.0f;
             pbx[r] = (M3 && p < nr) ? wp * to_f32(m3.prev_x[row0 + p]) : 0.0f;
         }
+        // the output row this lane finishes (lanes 2k, 2k + 1: warp-local row
+        // k), its x, gate and D loaded now, before the wait for the state
+        const int pe = warp + 4 * (lane >> 1);
+        const bool oute = (lane & 1) == 0 && pe < nr;
+        const float xe = oute ? to_f32(x[row0 + pe]) : 0.0f;
+        const float ze = (oute && z) ? to_f32(z[row0 + pe]) : 0.0f;
+        const float De = Dskip ? Dskip[h] : 0.0f;
         if (!mbar_wait(&full[s], (uint32_t)((i >> 1) & 1), nullptr)) break;
 
         // rows warp, warp + 4, ...: state (in place) and the C^T h partial sums
@@ -373,13 +380,10 @@ __global__ void __launch_bounds__(kBulkThreads)
             }
         }
         acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 1);
-        const int p = warp + 4 * (lane >> 1);
-        if ((lane & 1) == 0 && p < nr) {
-            const long long row = row0 + p;
-            const float xv = to_f32(x[row]);
-            float out = acc[0] + (Dskip ? Dskip[h] : 0.0f) * xv;
-            if (z) out *= silu_f(to_f32(z[row]));
-            y[row] = from_f32<T>(out);
+        if (oute) {
+            float out = acc[0] + De * xe;
+            if (z) out *= silu_f(ze);
+            y[row0 + pe] = from_f32<T>(out);
         }
     }
 }
