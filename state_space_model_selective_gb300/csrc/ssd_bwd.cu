@@ -87,6 +87,14 @@ struct BwdArgs {
     float* pA;             // [batch * nheads]
     uint32_t* status;
     int batch, seqlen, nheads, ngroups;
+    // Mamba-3's diagonal correction of dx, applied as dx is written (NULL:
+    // none): dx_{t,r'} -= c_t sum_r G_t[r][r'] dy_{t,r}, c_t = dt_{t+1} (1 -
+    // lambda_{t+1}) (0 at the last step), G_t[r][r'] = C_{t,r} . B_{t,r'}
+    // ([step][group][RK][RK]); dt, lambda per step (batch, steps, nheads)
+    const float* corr_g;
+    const float* corr_dt;
+    const float* corr_lam;
+    int corr_steps;
 };
 
 // One 32-column chunk of a masked, decayed Q x Q row, split into bf16 hi/lo:
@@ -256,7 +264,9 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 // RK > 1 (Mamba-3 MIMO): rows are sub-tokens, RK consecutive rows one step
 // that see one another fully (the mask is block-lower-triangular); the step's
 // dt sits on its first row (0 on the others) and its weight on every row.
-template <int RK>
+// CORR: Mamba-3's diagonal correction is applied to dx as it is written
+// (BwdArgs::corr_*); without it the plain SSD gradient's dx write is unchanged.
+template <int RK, bool CORR>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_bwd_kernel(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_B,
                    const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
@@ -616,12 +626,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_ld();
 #pragma unroll
                 for (int q = 0; q < 32; ++q) dw = fmaf(xv[q], br[q], dw);
-                if (t < L) {
+                if (!CORR && t < L) {
                     float* dxr = a.dx + (((long long)b * L + t) * a.nheads + h) * kP + 32 * part;
 #pragma unroll
                     for (int q = 0; q < 32; q += 4)
                         *reinterpret_cast<float4*>(dxr + q) = make_float4(
                             wr * br[q], wr * br[q + 1], wr * br[q + 2], wr * br[q + 3]);
+                }
+                if (CORR && t < L) {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) br[q] *= wr;
+                    {
+                        // the step's RK rows of dy: tile rows row - rp .. row - rp + RK - 1
+                        const int ts = t / RK, rp = t - ts * RK;
+                        const long long bt = (long long)b * a.corr_steps + ts;
+                        const float c = ts + 1 < a.corr_steps
+                                            ? a.corr_dt[(bt + 1) * a.nheads + h] *
+                                                  (1.0f - a.corr_lam[(bt + 1) * a.nheads + h])
+                                            : 0.0f;
+                        const float* Gp = a.corr_g + (bt * a.ngroups + g) * (RK * RK);
+#pragma unroll
+                        for (int r = 0; r < RK; ++r) {
+                            const float coef = c * Gp[r * RK + rp];
+                            float dyv[32];
+                            load_tile_half(smem + kSDY, row - rp + r, part, dyv);
+#pragma unroll
+                            for (int q = 0; q < 32; ++q) br[q] = fmaf(-coef, dyv[q], br[q]);
+                        }
+                    }
+                    float* dxr = a.dx + (((long long)b * L + t) * a.nheads + h) * kP + 32 * part;
+#pragma unroll
+                    for (int q = 0; q < 32; q += 4)
+                        *reinterpret_cast<float4*>(dxr + q) =
+                            make_float4(br[q], br[q + 1], br[q + 2], br[q + 3]);
                 }
             }
             tc_fence_before();
@@ -787,13 +824,21 @@ using MakeStates = std::function<ssm_status_t(float*)>;
 // weights, `dw` receives their gradient and ddt only the log-decay part), and
 // the fixed-order sums.  The workspace holds bwd_workspace(...).total bytes.
 
+// Mamba-3's diagonal correction of dx (BwdArgs::corr_*); g = NULL: none.
+struct DxCorr {
+    const float* g = nullptr;
+    const float* dt = nullptr;
+    const float* lam = nullptr;
+    int steps = 0;
+};
+
 ssm_status_t run_bwd(const void* x, const float* dt, const float* wts, const float* A_head,
                      const void* B, const void* C, const float* initial_state, const void* dy,
                      const float* dfinal_state, const float* block_states,
                      const MakeStates& make_states, float* dx, float* ddt, float* dw,
                      float* dA_head, float* dB, float* dC, float* dinitial_state, int batch,
                      int seqlen, int nheads, int ngroups, void* workspace, cudaStream_t s,
-                     int rank = 1) {
+                     int rank = 1, const DxCorr& corr = DxCorr{}) {
     const size_t items = (size_t)batch * nheads;
     const BwdWs w = bwd_workspace(batch, seqlen, nheads);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -817,6 +862,10 @@ ssm_status_t run_bwd(const void* x, const float* dt, const float* wts, const flo
     a.seqlen = seqlen;
     a.nheads = nheads;
     a.ngroups = ngroups;
+    a.corr_g = corr.g;
+    a.corr_dt = corr.dt;
+    a.corr_lam = corr.lam;
+    a.corr_steps = corr.steps;
 
     // 1. the state entering every block (and the final state), unless the
     // forward kept them
@@ -835,7 +884,10 @@ ssm_status_t run_bwd(const void* x, const float* dt, const float* wts, const flo
         !ssd_host::make_x_map(&mx, x, batch, seqlen, nheads) ||
         !ssd_host::make_x_map(&mdy, dy, batch, seqlen, nheads))
         return SSM_ERR_CUDA;
-    auto kern = rank == 4 ? ssd_bwd_kernel<4> : rank == 2 ? ssd_bwd_kernel<2> : ssd_bwd_kernel<1>;
+    auto kern = rank == 4   ? ssd_bwd_kernel<4, true>
+                : rank == 2 ? ssd_bwd_kernel<2, true>
+                : corr.g    ? ssd_bwd_kernel<1, true>
+                            : ssd_bwd_kernel<1, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
         cudaSuccess)
         return SSM_ERR_CUDA;
@@ -1069,20 +1121,19 @@ __global__ void m3_prev_b_kernel(const float* __restrict__ pprevB, float* __rest
 }
 
 // One CTA per (b, t): ddt (holding the log-decay part on entry) and dlambda of
-// every head, then dx -= c_t (C_t . B_t) dy_t and dB, dC -= (sum over the
-// group's heads of c_t x_t . dy_t) C_t, B_t.  Shared memory: 2 * nheads floats.
+// every head, then dB, dC -= (sum over the group's heads of c_t x_t . dy_t)
+// C_t, B_t.  (dx's term -c_t (C_t . B_t) dy_t is applied by the gradient
+// kernel as it writes dx.)  Shared memory: nheads floats.
 __global__ void m3_post_kernel(const float* __restrict__ dt, const float* __restrict__ lam,
                                const float* __restrict__ dw, const float* __restrict__ xd,
                                const float* __restrict__ cb, const float* __restrict__ dc0,
-                               const __nv_bfloat16* __restrict__ dy,
                                const __nv_bfloat16* __restrict__ B,
                                const __nv_bfloat16* __restrict__ C, float* __restrict__ ddt,
-                               float* __restrict__ dlam, float* __restrict__ dx,
-                               float* __restrict__ dB, float* __restrict__ dC, int batch,
-                               int seqlen, int nheads, int ngroups) {
+                               float* __restrict__ dlam, float* __restrict__ dB,
+                               float* __restrict__ dC, int batch, int seqlen, int nheads,
+                               int ngroups) {
     extern __shared__ float sm[];
-    float* coef = sm;           // c_t (C_t . B_t) per head
-    float* cx = sm + nheads;    // c_t (x_t . dy_t) per head
+    float* cx = sm;  // c_t (x_t . dy_t) per head
     const int hpg = nheads / ngroups;
     for (long long row = blockIdx.x; row < (long long)batch * seqlen; row += gridDim.x) {
         const int t = (int)(row % seqlen);
@@ -1097,13 +1148,9 @@ __global__ void m3_post_kernel(const float* __restrict__ dt, const float* __rest
             const float dwt = dw[i], l = lam[i], d = dt[i];
             ddt[i] = ddt[i] + l * dwt + (1.0f - l) * dcp;
             dlam[i] = d * dwt - d * dcp;
-            coef[h] = c * cb[row * ngroups + g];
             cx[h] = c * xd[i];
         }
         __syncthreads();
-        const long long xo = row * nheads * kP;
-        for (int idx = threadIdx.x; idx < nheads * kP; idx += blockDim.x)
-            dx[xo + idx] -= coef[idx / kP] * __bfloat162float(dy[xo + idx]);
         const long long bo = row * ngroups * kNs;
         for (int idx = threadIdx.x; idx < ngroups * kNs; idx += blockDim.x) {
             const int g = idx / kNs;
@@ -1248,23 +1295,29 @@ extern "C" ssm_status_t ssd_mamba3_bwd(const void* x, const float* dt, const flo
     const long long nw = (long long)steps * nheads;
     m3_weights_kernel<<<grid_for(nw, 256), 256, 0, s>>>(dt, lam, w, batch, seqlen, nheads);
     if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
-    // 2. the SSD gradient with weights w from the Mamba-3 forward's block states
     const MakeStates states = [&](float* bs) {
         return ssd_internal::ssd_mamba3_forward_block_states(x, dt, lam, A_head, B, C,
                                                              initial_state, prev_B, prev_x, bs,
                                                              batch, seqlen, nheads, ngroups, s);
     };
-    ssm_status_t rc = run_bwd(x, dt, w, A_head, B, C, initial_state, dy, dfinal_state,
-                              block_states, states, dx, ddt, dw, dA_head, dB, dC, dS_out, batch,
-                              seqlen, nheads, ngroups, workspace, s);
-    if (rc != SSM_OK) return rc;
-    // 3. x . dy per head and C . B per group, every step
+    // 2. x . dy per head and C . B per group, every step (inputs only; C . B
+    // feeds the diagonal correction the gradient kernel applies to dx)
     const long long nrows = (long long)steps * (nheads + ngroups);
     m3_dots_kernel<<<grid_for(nrows * 32, 256), 256, 0, s>>>(
         static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(dy),
         static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), xd, cb,
         batch, seqlen, nheads, ngroups);
     if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
+    // 3. the SSD gradient with weights w from the Mamba-3 forward's block states
+    DxCorr corr;
+    corr.g = cb;
+    corr.dt = dt;
+    corr.lam = lam;
+    corr.steps = seqlen;
+    ssm_status_t rc = run_bwd(x, dt, w, A_head, B, C, initial_state, dy, dfinal_state,
+                              block_states, states, dx, ddt, dw, dA_head, dB, dC, dS_out, batch,
+                              seqlen, nheads, ngroups, workspace, s, 1, corr);
+    if (rc != SSM_OK) return rc;
     // 4. the previous token's gradients and dL/dc_{-1}
     if (has_prev) {
         m3_prev_kernel<<<(unsigned)items, kNs, 0, s>>>(
@@ -1278,10 +1331,9 @@ extern "C" ssm_status_t ssd_mamba3_bwd(const void* x, const float* dt, const flo
     }
     // 5. ddt, dlambda and the diagonal correction's terms
     m3_post_kernel<<<(unsigned)std::min<long long>((long long)steps, 65535), 256,
-                     2 * nheads * sizeof(float), s>>>(
-        dt, lam, dw, xd, cb, has_prev ? dc0 : nullptr, static_cast<const __nv_bfloat16*>(dy),
-        static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), ddt, dlam, dx,
-        dB, dC, batch, seqlen, nheads, ngroups);
+                     nheads * sizeof(float), s>>>(
+        dt, lam, dw, xd, cb, has_prev ? dc0 : nullptr, static_cast<const __nv_bfloat16*>(B),
+        static_cast<const __nv_bfloat16*>(C), ddt, dlam, dB, dC, batch, seqlen, nheads, ngroups);
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
@@ -1517,24 +1569,23 @@ __global__ void m3m_prev_b_kernel(const float* __restrict__ pprevB, float* __res
 
 // One CTA per (b, t): ddt and dlambda of every head (the step's log-decay part
 // from its first sub-token row, dw summed over its ranks), then the
-// correction's terms in dx, dB and dC (c XD summed over the group's heads
-// first, in head order).  Shared memory: (2 nheads + ngroups) R^2 floats.
+// correction's terms in dB and dC (c XD summed over the group's heads first,
+// in head order).  The correction's term in dx is applied by the gradient
+// kernel as it writes dx.  Shared memory: (nheads + ngroups) R^2 floats.
 template <int RK>
 __global__ void m3m_post_kernel(const float* __restrict__ dt, const float* __restrict__ lam,
                                 const float* __restrict__ dw_rows,
                                 const float* __restrict__ ddec_rows, const float* __restrict__ XD,
                                 const float* __restrict__ G, const float* __restrict__ dc0,
-                                const __nv_bfloat16* __restrict__ dy,
                                 const __nv_bfloat16* __restrict__ B,
                                 const __nv_bfloat16* __restrict__ C, float* __restrict__ ddt,
-                                float* __restrict__ dlam, float* __restrict__ dx,
-                                float* __restrict__ dB, float* __restrict__ dC, int batch,
-                                int seqlen, int nheads, int ngroups) {
+                                float* __restrict__ dlam, float* __restrict__ dB,
+                                float* __restrict__ dC, int batch, int seqlen, int nheads,
+                                int ngroups) {
     extern __shared__ float sm[];
     constexpr int R2 = RK * RK;
-    float* cG = sm;                    // [h][r][r'] c_t G_{rr'}
-    float* cX = sm + nheads * R2;      // [h][r'][r] c_t XD_{r'r}
-    float* sX = sm + 2 * nheads * R2;  // [g][r'][r] sum over the group's heads of cX
+    float* cX = sm;                // [h][r'][r] c_t XD_{r'r}
+    float* sX = sm + nheads * R2;  // [g][r'][r] sum over the group's heads of cX
     const int hpg = nheads / ngroups;
     for (long long bt = blockIdx.x; bt < (long long)batch * seqlen; bt += gridDim.x) {
         const int t = (int)(bt % seqlen);
@@ -1566,13 +1617,9 @@ __global__ void m3m_post_kernel(const float* __restrict__ dt, const float* __res
             const float l = lam[i], d = dt[i];
             ddt[i] = ddec_rows[(bt * RK) * nheads + h] + l * dwt + (1.0f - l) * dcp;
             dlam[i] = d * dwt - d * dcp;
-            const float* Gp = G + (bt * ngroups + g) * R2;
             const float* Xp = XD + (bt * nheads + h) * R2;
 #pragma unroll
-            for (int k = 0; k < R2; ++k) {
-                cG[h * R2 + k] = c * Gp[k];
-                cX[h * R2 + k] = c * Xp[k];
-            }
+            for (int k = 0; k < R2; ++k) cX[h * R2 + k] = c * Xp[k];
         }
         __syncthreads();
         for (int idx = threadIdx.x; idx < ngroups * R2; idx += blockDim.x) {
@@ -1582,26 +1629,6 @@ __global__ void m3m_post_kernel(const float* __restrict__ dt, const float* __res
             sX[idx] = acc;
         }
         __syncthreads();
-        // dx_{t,r'} -= sum_r c G_{rr'} dy_{t,r}, four consecutive p per thread
-        for (int idx = threadIdx.x; idx < RK * nheads * (kP / 4); idx += blockDim.x) {
-            const int p4 = idx % (kP / 4), h = (idx / (kP / 4)) % nheads;
-            const int rp = idx / ((kP / 4) * nheads);
-            float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll
-            for (int r = 0; r < RK; ++r) {
-                const float cg = cG[h * R2 + r * RK + rp];
-                const uint2 d = *reinterpret_cast<const uint2*>(
-                    dy + ((bt * RK + r) * nheads + h) * kP + 4 * p4);
-                acc.x = fmaf(cg, bf16lo(d.x), acc.x);
-                acc.y = fmaf(cg, bf16hi(d.x), acc.y);
-                acc.z = fmaf(cg, bf16lo(d.y), acc.z);
-                acc.w = fmaf(cg, bf16hi(d.y), acc.w);
-            }
-            float4* o = reinterpret_cast<float4*>(dx + ((bt * RK + rp) * nheads + h) * kP + 4 * p4);
-            float4 v = *o;
-            v.x -= acc.x; v.y -= acc.y; v.z -= acc.z; v.w -= acc.w;
-            *o = v;
-        }
         // dB_{t,r'} -= sum_r sX_{r'r} C_{t,r};  dC_{t,r} -= sum_r' sX_{r'r} B_{t,r'}
         for (int idx = threadIdx.x; idx < RK * ngroups * kNs; idx += blockDim.x) {
             const int n = idx % kNs, g = (idx / kNs) % ngroups, ra = idx / (kNs * ngroups);
@@ -1641,21 +1668,29 @@ M3mWs m3m_workspace(int batch, int seqlen, int rank, int nheads, int ngroups) {
     return m;
 }
 
-// Steps 3-5 of the MIMO gradient for rank RK.
+// Step 3 of the MIMO gradient for rank RK: the per-step rank dots x . dy and
+// C . B (inputs only, so they run before the gradient kernel, which applies
+// the diagonal correction to dx from them).
 template <int RK>
-ssm_status_t m3m_tail(const void* x, const float* dt, const float* lam, const void* B,
-                      const void* C, const void* dy, bool has_prev, const void* prev_B,
-                      const void* prev_x, const float* dS, const float* dw, const float* ddec,
-                      float* XD, float* Gd, float* dc0, float* ppb, float* ddt, float* dlam,
-                      float* dx, float* dB, float* dC, float* dprev_B, float* dprev_x, int batch,
-                      int seqlen, int nheads, int ngroups, cudaStream_t s) {
-    const long long steps = (long long)batch * seqlen;
-    const long long nrows = steps * (nheads + ngroups);
+ssm_status_t m3m_dots(const void* x, const void* B, const void* C, const void* dy, float* XD,
+                      float* Gd, int batch, int seqlen, int nheads, int ngroups, cudaStream_t s) {
+    const long long nrows = (long long)batch * seqlen * (nheads + ngroups);
     m3m_dots_kernel<RK><<<grid_for(nrows * 8, 256), 256, 0, s>>>(
         static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(dy),
         static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), XD, Gd,
         batch, seqlen, nheads, ngroups);
-    if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+// Steps 4-5 of the MIMO gradient for rank RK.
+template <int RK>
+ssm_status_t m3m_tail(const float* dt, const float* lam, const void* B, const void* C,
+                      bool has_prev, const void* prev_B, const void* prev_x, const float* dS,
+                      const float* dw, const float* ddec, const float* XD, const float* Gd,
+                      float* dc0, float* ppb, float* ddt, float* dlam, float* dB, float* dC,
+                      float* dprev_B, float* dprev_x, int batch, int seqlen, int nheads,
+                      int ngroups, cudaStream_t s) {
+    const long long steps = (long long)batch * seqlen;
     if (has_prev) {
         m3m_prev_kernel<RK><<<(unsigned)((long long)batch * nheads), kNs, 0, s>>>(
             dS, static_cast<const __nv_bfloat16*>(prev_B),
@@ -1667,11 +1702,9 @@ ssm_status_t m3m_tail(const void* x, const float* dt, const float* lam, const vo
         if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
     }
     m3m_post_kernel<RK><<<(unsigned)std::min<long long>(steps, 65535), 256,
-                          (2 * nheads + ngroups) * RK * RK * sizeof(float), s>>>(
-        dt, lam, dw, ddec, XD, Gd, has_prev ? dc0 : nullptr,
-        static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(B),
-        static_cast<const __nv_bfloat16*>(C), ddt, dlam, dx, dB, dC, batch, seqlen, nheads,
-        ngroups);
+                          (nheads + ngroups) * RK * RK * sizeof(float), s>>>(
+        dt, lam, dw, ddec, XD, Gd, has_prev ? dc0 : nullptr, static_cast<const __nv_bfloat16*>(B),
+        static_cast<const __nv_bfloat16*>(C), ddt, dlam, dB, dC, batch, seqlen, nheads, ngroups);
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
@@ -1788,20 +1821,29 @@ extern "C" ssm_status_t ssd_mamba3_mimo_bwd(
     m3m_expand_kernel<<<grid_for((long long)subs * nheads, 256), 256, 0, s>>>(
         dt, lam, dts, wts, batch, seqlen, rank, nheads);
     if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
-    // 2. the SSD gradient over the sub-tokens (block-lower-triangular mask)
     const MakeStates states = [&](float* bs) {
         return ssd_internal::ssd_mamba3_forward_block_states(x, dt, lam, A_head, B, C,
                                                              initial_state, prev_B, prev_x, bs,
                                                              batch, seqlen, nheads, ngroups, s,
                                                              rank);
     };
-    ssm_status_t rc = run_bwd(x, dts, wts, A_head, B, C, initial_state, dy, dfinal_state,
-                              block_states, states, dx, ddec, dw, dA_head, dB, dC, dS_out, batch,
-                              seqlen * rank, nheads, ngroups, workspace, s, rank);
+    // 2. the per-step rank dots (they feed the gradient kernel's dx correction)
+    auto dots = rank == 1 ? m3m_dots<1> : rank == 2 ? m3m_dots<2> : m3m_dots<4>;
+    ssm_status_t rc = dots(x, B, C, dy, XD, Gd, batch, seqlen, nheads, ngroups, s);
     if (rc != SSM_OK) return rc;
-    // 3.-5. the dots, the previous token and the per-step terms
+    // 3. the SSD gradient over the sub-tokens (block-lower-triangular mask)
+    DxCorr corr;
+    corr.g = Gd;
+    corr.dt = dt;
+    corr.lam = lam;
+    corr.steps = seqlen;
+    rc = run_bwd(x, dts, wts, A_head, B, C, initial_state, dy, dfinal_state, block_states,
+                 states, dx, ddec, dw, dA_head, dB, dC, dS_out, batch, seqlen * rank, nheads,
+                 ngroups, workspace, s, rank, corr);
+    if (rc != SSM_OK) return rc;
+    // 4.-5. the previous token and the per-step terms
     auto tail = rank == 1 ? m3m_tail<1> : rank == 2 ? m3m_tail<2> : m3m_tail<4>;
-    rc = tail(x, dt, lam, B, C, dy, has_prev, prev_B, prev_x, dS_out, dw, ddec, XD, Gd, dc0, ppb,
-              ddt, dlam, dx, dB, dC, dprev_B, dprev_x, batch, seqlen, nheads, ngroups, s);
+    rc = tail(dt, lam, B, C, has_prev, prev_B, prev_x, dS_out, dw, ddec, XD, Gd, dc0, ppb, ddt,
+              dlam, dB, dC, dprev_B, dprev_x, batch, seqlen, nheads, ngroups, s);
     return rc;
 }
