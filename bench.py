@@ -300,12 +300,14 @@ def run_ours(args):
 
     e2e_step()
     torch.cuda.synchronize(dev)
-    # three windows of steps, each timed whole (copies in and out of every step
-    # inside it); the median window is reported and all three are listed, so a
-    # stall of the shared host link in one window does not decide the number
-    win_steps = max(1, e2e_steps // 3)
+    # five windows of steps, each timed whole (copies in and out of every step
+    # inside it); the median window is reported and all five are listed, so a
+    # stall of the shared host link in one or two windows does not decide the
+    # number
+    n_windows = 5
+    win_steps = max(1, e2e_steps // n_windows)
     e2e_windows = []
-    for _ in range(3):
+    for _ in range(n_windows):
         barrier(dist)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -335,7 +337,7 @@ def run_ours(args):
                        "parallelism": f"independent workload per GPU x{world}"},
             "e2e": {"value": e2e_value, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "timing": f"median of 3 windows of {win_steps} steps",
+                    "timing": f"median of {n_windows} windows of {win_steps} steps",
                     "windows": e2e_windows},
             "gpu_launches": args.steps,
             "roofline": {"bound": "alu", "achieved": achieved, "peak": MUFU_PEAK_GOPS,
