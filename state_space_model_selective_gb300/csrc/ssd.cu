@@ -111,13 +111,16 @@ __device__ __forceinline__ void mprime_chunk(const float* gv, const float* q2c, 
 // their step's decay and weights; a sub-token sees every sub-token of its own
 // step (the block-diagonal part, weight gamma) and of earlier steps.
 // BS: also write the state entering every block and the final state to
-// a.bstates (the backward pass's checkpoints); y is then optional.
-template <typename Tout, bool M3, int RK, bool BS = false>
+// a.bstates (the backward pass's checkpoints): 1 with y as well (y optional),
+// 2 states only -- no C tile, no G, M', Y_off or Y_diag products and no y; a
+// block is then cs, X' and S_chunk^T = B^T X' only.
+template <typename Tout, bool M3, int RK, int BS = 0>
 __global__ void __launch_bounds__(kThreads, 2)
     ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_B,
                    const __grid_constant__ CUtensorMap tm_x,
                    const __grid_constant__ CUtensorMap tm_y, const SsdArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
+    constexpr bool SO = BS == 2;  // states only
     const uint32_t sbase = smem_u32(smem);
     float* s_q2 = reinterpret_cast<float*>(smem + kMisc);
     float* s_wsum = s_q2 + kQ;  // [2][4] per-warpgroup warp totals
@@ -149,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int it = 0; it < my_items; ++it) {
             const int item = (int)blockIdx.x + it * (int)gridDim.x;
             const int hh = item % a.nheads, bb = item / a.nheads;
-            if constexpr (BS) {
+            if constexpr (BS != 0) {
                 float* bs = a.bstates + (long long)item * (nblocks + 1) * kP * kNs;
                 for (int e = tid; e < (nblocks + 1) * kP * kNs; e += kThreads) bs[e] = nanv;
                 if (!a.y) continue;
@@ -203,9 +206,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     auto load_cb = [&](int st) {
         int hn, bn, gn, tn;
         step_coords(st, hn, bn, gn, tn);
-        mbar_arrive_expect_tx(bar_cb, 2 * 32768);
-        tma_load_4d(smem + kRC, &tm_C, bar_cb, 0, gn, tn, bn);
-        tma_load_4d(smem + kRC + 16384, &tm_C, bar_cb, 64, gn, tn, bn);
+        mbar_arrive_expect_tx(bar_cb, SO ? 32768 : 2 * 32768);
+        if constexpr (!SO) {  // states only: no C (the region holds X')
+            tma_load_4d(smem + kRC, &tm_C, bar_cb, 0, gn, tn, bn);
+            tma_load_4d(smem + kRC + 16384, &tm_C, bar_cb, 64, gn, tn, bn);
+        }
         tma_load_4d(smem + kRB, &tm_B, bar_cb, 0, gn, tn, bn);
         tma_load_4d(smem + kRB + 16384, &tm_B, bar_cb, 64, gn, tn, bn);
         ++cb_issued;
@@ -279,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
         }
 
-        if constexpr (BS) {
+        if constexpr (BS != 0) {
             float* bs = a.bstates +
                         (((long long)item * (nblocks + 1) + blk) * kP + kHalf * part) * kNs + row;
 #pragma unroll
@@ -287,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
 
         // ---- G = C B^T as soon as the C and B tiles are in (thread 0)
-        if (tid == 0) {
+        if (!SO && tid == 0) {
             const bool got = mbar_wait(bar_cb, ph, nullptr);
             tc_fence_after();
             if (got) {
@@ -307,13 +312,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float dti = in.dt;
         // input weight of this row's step (Mamba-2: dt; Mamba-3: scale) and, for
         // Mamba-3, the diagonal weight gamma
+        // (every product below is rounded on its own, __fmul_rn, so that no
+        // instance of this kernel -- with y, or states only -- contracts it
+        // into a neighbouring add: all of them carry the same states, bit for bit)
         float w_i = dti, gamma_i = 0.0f;
         if constexpr (M3) {
-            gamma_i = in.lam * dti;
-            w_i = gamma_i + in.dt1 * (1.0f - in.lam1);
+            gamma_i = __fmul_rn(in.lam, dti);
+            w_i = __fadd_rn(gamma_i, __fmul_rn(in.dt1, 1.0f - in.lam1));
         }
         // the step's log-decay enters the running sum once, at its first sub-token
-        float v = (RK == 1 || row % RK == 0) ? dti * in.A : 0.0f;
+        float v = (RK == 1 || row % RK == 0) ? __fmul_rn(dti, in.A) : 0.0f;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const float u = __shfl_up_sync(0xffffffffu, v, o);
@@ -331,8 +339,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (w < quarter) v += ws;
             cs_last += ws;
         }
-        const float cs2_i = v * kLog2e;           // log2-scaled cs_i
-        const float cs2_last = cs_last * kLog2e;
+        const float cs2_i = __fmul_rn(v, kLog2e);  // log2-scaled cs_i
+        const float cs2_last = __fmul_rn(cs_last, kLog2e);
         // q2_j = log2(w_j) - cs_j log2(e): exp(cs_i - cs_j) w_j = 2^(cs2_i + q2_j)
         if (part == 0) {
             float lg;
@@ -343,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float a_blk = ex2_approx(cs2_last);
 
         // ---- S_prev as the hi/lo operand of Y_off (row n, p contiguous)
-        if (carry) {
+        if (!SO && carry) {
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
                 uint32_t hp[4], lp[4];
@@ -361,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
         // ---- Y_off = C S_prev^T: N = 128, S_hi in columns 0..63, S_lo in 64..127
         // (none when no state enters the block)
-        if (tid == 0) {
+        if (!SO && tid == 0) {
             tc_fence_after();
             if (carry) {
                 constexpr uint32_t id128n = idesc_bf16_f32(128, 128) | kIdescBMN;
@@ -377,38 +385,41 @@ __global__ void __launch_bounds__(kThreads, 2)
         // split hi/lo and written back over G in TMEM (row i = this lane).
         // 32-column chunk k of this warpgroup is wholly above the diagonal for
         // k > quarter, on it for k == quarter, below it otherwise.
-        {
-            const bool got = mbar_wait(bar_g, ph, nullptr);
-            if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int ck = 2 * part + half;
-            const int c0 = 32 * ck;
-            uint32_t hp[16], lp[16];
-            if (ck > quarter) {
-#pragma unroll
-                for (int q = 0; q < 16; ++q) hp[q] = lp[q] = 0u;
-            } else {
-                float gv[32];
-                tmem_ld32(t_lane + kTmG + c0, gv);
-                tmem_wait_ld();
-                if (ck == quarter)
-                    mprime_chunk<true, M3>(gv, s_q2 + c0, cs2_i, RK * (lane / RK) + RK - 1,
-                                           RK * (lane / RK), gamma_i, hp, lp);
-                else
-                    mprime_chunk<false, M3>(gv, s_q2 + c0, cs2_i, 31, 0, gamma_i, hp, lp);
+        if constexpr (!SO) {
+            {
+                const bool got = mbar_wait(bar_g, ph, nullptr);
+                if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
             }
-            tmem_st16(t_lane + kTmG + c0, hp);
-            tmem_st16(t_lane + kTmG + c0 + 16, lp);
+            tc_fence_after();
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int ck = 2 * part + half;
+                const int c0 = 32 * ck;
+                uint32_t hp[16], lp[16];
+                if (ck > quarter) {
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) hp[q] = lp[q] = 0u;
+                } else {
+                    float gv[32];
+                    tmem_ld32(t_lane + kTmG + c0, gv);
+                    tmem_wait_ld();
+                    if (ck == quarter)
+                        mprime_chunk<true, M3>(gv, s_q2 + c0, cs2_i, RK * (lane / RK) + RK - 1,
+                                               RK * (lane / RK), gamma_i, hp, lp);
+                    else
+                        mprime_chunk<false, M3>(gv, s_q2 + c0, cs2_i, 31, 0, gamma_i, hp, lp);
+                }
+                tmem_st16(t_lane + kTmG + c0, hp);
+                tmem_st16(t_lane + kTmG + c0 + 16, lp);
+            }
         }
 
         // ---- Y_off done (the C region is free):  X' = w o X (w_j = exp(cs_last -
         // cs_j) dt_j), hi and lo, into the C region in the x tile's own MN-major
         // layout; Y_off summed over its hi/lo halves and scaled by exp(cs_i)
         {
-            const bool got = mbar_wait(bar_yoff, ph, nullptr) && mbar_wait(bar_x, ph, nullptr);
+            const bool got =
+                (SO || mbar_wait(bar_yoff, ph, nullptr)) && mbar_wait(bar_x, ph, nullptr);
             if (!named_bar_and(1, kThreads, got)) { ok = false; break; }
         }
         tc_fence_after();
@@ -422,12 +433,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
             uint32_t hp[4], lp[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) split2_bf16(bf16lo(xw[e]) * w, bf16hi(xw[e]) * w, hp[e], lp[e]);
+            for (int e = 0; e < 4; ++e)
+                split2_bf16(__fmul_rn(bf16lo(xw[e]), w), __fmul_rn(bf16hi(xw[e]), w), hp[e], lp[e]);
             *reinterpret_cast<uint4*>(smem + kRC + off) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
             *reinterpret_cast<uint4*>(smem + kRC + 16384 + off) =
                 make_uint4(lp[0], lp[1], lp[2], lp[3]);
         }
-        if (carry) {
+        if (!SO && carry) {
             float yo[kHalf], yl[kHalf];
             tmem_ld32(t_lane + kTmY + kHalf * part, yo);
             tmem_ld32(t_lane + kTmY + kP + kHalf * part, yl);
@@ -445,24 +457,32 @@ __global__ void __launch_bounds__(kThreads, 2)
         // then Y += M' X (hi + lo)
         if (tid == 0) {
             tc_fence_after();
+            // states only: the B tile (no G product waited for it)
+            const bool go = !SO || mbar_wait(bar_cb, ph, nullptr);
+            if (SO) tc_fence_after();
             constexpr uint32_t idS = idesc_bf16_f32(128, 64) | kIdescAMN | kIdescBMN;
             constexpr uint32_t idY = idesc_bf16_f32(128, 64) | kIdescBMN;
+            if (go) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                mma_bf16(tmem + kTmS, mdesc(sbase + kRB, kk, 16384), mdesc(sbase + kRC, kk, 16384),
-                         idS, kk > 0);
-                mma_bf16(tmem + kTmS, mdesc(sbase + kRB, kk, 16384),
-                         mdesc(sbase + kRC + 16384, kk, 16384), idS, 1);
-            }
-            mma_commit(bar_s);
+                for (int kk = 0; kk < 8; ++kk) {
+                    mma_bf16(tmem + kTmS, mdesc(sbase + kRB, kk, 16384),
+                             mdesc(sbase + kRC, kk, 16384), idS, kk > 0);
+                    mma_bf16(tmem + kTmS, mdesc(sbase + kRB, kk, 16384),
+                             mdesc(sbase + kRC + 16384, kk, 16384), idS, 1);
+                }
+                mma_commit(bar_s);
+                if constexpr (!SO) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                mma_bf16_ta(tmem + kTmY, tmem + kTmG + mcol_hi(kk), mdesc(sbase + kRX, kk, 16384),
-                            idY, (carry || kk > 0) ? 1u : 0u);
-                mma_bf16_ta(tmem + kTmY, tmem + kTmG + mcol_hi(kk) + 16,
-                            mdesc(sbase + kRX, kk, 16384), idY, 1);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        mma_bf16_ta(tmem + kTmY, tmem + kTmG + mcol_hi(kk),
+                                    mdesc(sbase + kRX, kk, 16384), idY,
+                                    (carry || kk > 0) ? 1u : 0u);
+                        mma_bf16_ta(tmem + kTmY, tmem + kTmG + mcol_hi(kk) + 16,
+                                    mdesc(sbase + kRX, kk, 16384), idY, 1);
+                    }
+                }
+                mma_commit(bar_mma2);
             }
-            mma_commit(bar_mma2);
         }
         // ---- next step's loads (the next block, or the next item's first):
         // C and B once S_chunk has read the B and X' regions, x after Y_diag
@@ -480,7 +500,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         // staged in the S region (128-byte rows, 16-byte chunks XOR-swizzled by
         // row mod 8): fp32 as two [128 t][32 p] halves, bf16 as one [128 t][64 p]
         float sc[kHalf];
-        {
+        if constexpr (SO) {
+            tmem_ld32(t_lane + kTmS + kHalf * part, sc);
+            tmem_wait_ld();
+        } else {
             float yv[kHalf];
             tmem_ld32(t_lane + kTmY + kHalf * part, yv);
             tmem_ld32(t_lane + kTmS + kHalf * part, sc);
@@ -509,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
         // ---- y out of the staged tile by TMA stores (one thread; rows past
         // the sequence end are clipped by the map)
-        if ((!BS || a.y != nullptr) && tid == kLoader) {
+        if ((BS == 0 || a.y != nullptr) && tid == kLoader) {
             if constexpr (sizeof(Tout) == 4) {
                 tma_store_3d(&tm_y, smem + kRS, h * kP, t0, b);
                 tma_store_3d(&tm_y, smem + kRS + 16384, h * kP + kHalf, t0, b);
@@ -524,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int q = 0; q < kHalf; ++q) S[q] = fmaf(a_blk, S[q], sc[q]);
         if (blk == nblocks - 1) {
-            if constexpr (BS) {
+            if constexpr (BS != 0) {
                 float* bs = a.bstates + (((long long)item * (nblocks + 1) + nblocks) * kP +
                                          kHalf * part) * kNs + row;
 #pragma unroll
@@ -554,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <typename Tout, bool M3, int RK, bool BS = false>
+template <typename Tout, bool M3, int RK, int BS = 0>
 ssm_status_t launch(const CUtensorMap& mc, const CUtensorMap& mb, const CUtensorMap& mx,
                     const CUtensorMap& my, const SsdArgs& a, cudaStream_t s) {
     auto kern = ssd_fwd_kernel<Tout, M3, RK, BS>;
@@ -680,15 +703,15 @@ ssm_status_t ssd_entry(const void* x, const float* dt, const float* lam, const f
     if (bstates) {  // the states the gradients start from, kept by the forward
         a.bstates = bstates;
         if (!m3)
-            return bf ? launch<__nv_bfloat16, false, 1, true>(mc, mb, mx, my, a, s)
-                      : launch<float, false, 1, true>(mc, mb, mx, my, a, s);
+            return bf ? launch<__nv_bfloat16, false, 1, 1>(mc, mb, mx, my, a, s)
+                      : launch<float, false, 1, 1>(mc, mb, mx, my, a, s);
         switch (rank) {
-            case 1: return bf ? launch<__nv_bfloat16, true, 1, true>(mc, mb, mx, my, a, s)
-                              : launch<float, true, 1, true>(mc, mb, mx, my, a, s);
-            case 2: return bf ? launch<__nv_bfloat16, true, 2, true>(mc, mb, mx, my, a, s)
-                              : launch<float, true, 2, true>(mc, mb, mx, my, a, s);
-            default: return bf ? launch<__nv_bfloat16, true, 4, true>(mc, mb, mx, my, a, s)
-                               : launch<float, true, 4, true>(mc, mb, mx, my, a, s);
+            case 1: return bf ? launch<__nv_bfloat16, true, 1, 1>(mc, mb, mx, my, a, s)
+                              : launch<float, true, 1, 1>(mc, mb, mx, my, a, s);
+            case 2: return bf ? launch<__nv_bfloat16, true, 2, 1>(mc, mb, mx, my, a, s)
+                              : launch<float, true, 2, 1>(mc, mb, mx, my, a, s);
+            default: return bf ? launch<__nv_bfloat16, true, 4, 1>(mc, mb, mx, my, a, s)
+                               : launch<float, true, 4, 1>(mc, mb, mx, my, a, s);
         }
     }
     if (!m3) return bf ? launch<__nv_bfloat16, false, 1>(mc, mb, mx, my, a, s)
@@ -728,7 +751,7 @@ ssm_status_t ssd_forward_block_states(const void* x, const float* dt, const floa
     a.seqlen = seqlen;
     a.nheads = nheads;
     a.ngroups = ngroups;
-    return launch<float, false, 1, true>(mc, mb, mx, my, a, stream);
+    return launch<float, false, 1, 2>(mc, mb, mx, my, a, stream);
 }
 
 // The Mamba-3 forward (SISO, or MIMO of rank 2 or 4 over 128-row blocks of
@@ -765,9 +788,9 @@ ssm_status_t ssd_mamba3_forward_block_states(const void* x, const float* dt, con
     a.nheads = nheads;
     a.ngroups = ngroups;
     switch (rank) {
-        case 1: return launch<float, true, 1, true>(mc, mb, mx, my, a, stream);
-        case 2: return launch<float, true, 2, true>(mc, mb, mx, my, a, stream);
-        case 4: return launch<float, true, 4, true>(mc, mb, mx, my, a, stream);
+        case 1: return launch<float, true, 1, 2>(mc, mb, mx, my, a, stream);
+        case 2: return launch<float, true, 2, 2>(mc, mb, mx, my, a, stream);
+        case 4: return launch<float, true, 4, 2>(mc, mb, mx, my, a, stream);
     }
     return SSM_ERR_UNSUPPORTED;
 }
