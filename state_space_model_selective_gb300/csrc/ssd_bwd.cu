@@ -1063,44 +1063,100 @@ __global__ void m3_dots_kernel(const __nv_bfloat16* __restrict__ x,
 }
 
 // The previous token, per (b, h), from dS = dL/ds_{-1} [64 p][128 n] and
-// c0 = dt_0 (1 - lambda_0):
-//   dprev_x[b,h,p] = c0 sum_n dS[p,n] prev_B[g,n],
-//   pprevB[b,h,n]  = c0 sum_p dS[p,n] prev_x[h,p] (summed over the group next),
-//   dc0[b,h]       = sum_p prev_x[h,p] sum_n dS[p,n] prev_B[g,n].
-// 128 threads: thread n for the column sums, threads p < 64 for the rows.
-__global__ void m3_prev_kernel(const float* __restrict__ dS,
-                               const __nv_bfloat16* __restrict__ prev_B,
-                               const __nv_bfloat16* __restrict__ prev_x,
-                               const float* __restrict__ dt, const float* __restrict__ lam,
-                               float* __restrict__ dprev_x, float* __restrict__ pprevB,
-                               float* __restrict__ dc0, int batch, int seqlen, int nheads,
-                               int ngroups) {
-    __shared__ float pb[kNs], px[kP], red[2];
+// c0 = dt_0 (1 - lambda_0), all RK ranks in one pass over dS (RK = 1: the
+// single-input gradient):
+//   dprev_x[b,r,h,p] = c0 sum_n dS[p,n] prev_B[b,r,g,n],
+//   pprevB[b,h,r,n]  = c0 sum_p dS[p,n] prev_x[b,r,h,p] (summed over the group next),
+//   dc0[b,h]         = sum_r sum_p prev_x[b,r,h,p] sum_n dS[p,n] prev_B[b,r,g,n].
+// 128 threads: dS staged in shared memory, thread n for the column sums, a
+// thread pair per row for the row sums.
+template <int RK>
+__global__ void __launch_bounds__(kNs) m3m_prev_kernel(const float* __restrict__ dS,
+                                                     const __nv_bfloat16* __restrict__ prev_B,
+                                                     const __nv_bfloat16* __restrict__ prev_x,
+                                                     const float* __restrict__ dt,
+                                                     const float* __restrict__ lam,
+                                                     float* __restrict__ dprev_x,
+                                                     float* __restrict__ pprevB,
+                                                     float* __restrict__ dc0, int batch,
+                                                     int seqlen, int nheads, int ngroups) {
+    // dS[p][n] staged with rows of kNs + 2 floats: the column pass (thread n)
+    // and the row pass (a thread pair per row p, split by the parity of n)
+    // both read distinct banks
+    constexpr int kRow = kNs + 2;
+    __shared__ float Ss[kP * kRow];
+    __shared__ float pb[RK][kNs], px[RK][kP], red[kNs / 32];
     const int item = blockIdx.x, b = item / nheads, h = item % nheads;
     const int g = h / (nheads / ngroups);
     const int tid = threadIdx.x;
     const long long i0 = (long long)b * seqlen * nheads + h;
     const float c0 = dt[i0] * (1.0f - lam[i0]);
-    pb[tid] = __bfloat162float(prev_B[((long long)b * ngroups + g) * kNs + tid]);
-    if (tid < kP) px[tid] = __bfloat162float(prev_x[(long long)item * kP + tid]);
+    {
+        const float4* S4 = reinterpret_cast<const float4*>(dS + (long long)item * kP * kNs);
+        constexpr int kVec = kP * kNs / 4 / kNs;  // float4 loads per thread
+        float4 v[kVec];
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) v[j] = __ldg(S4 + tid + j * kNs);
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            const int e = (tid + j * kNs) * 4, pp = e / kNs, n = e % kNs;
+            float* d = Ss + pp * kRow + n;
+            d[0] = v[j].x; d[1] = v[j].y; d[2] = v[j].z; d[3] = v[j].w;
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < RK; ++r) {
+        pb[r][tid] = __bfloat162float(prev_B[(((long long)b * RK + r) * ngroups + g) * kNs + tid]);
+        if (tid < kP) px[r][tid] = __bfloat162float(prev_x[(((long long)b * RK + r) * nheads + h) * kP + tid]);
+    }
     __syncthreads();
-    const float* S = dS + (long long)item * kP * kNs;
-    float col = 0.0f;
-    for (int p = 0; p < kP; ++p) col = fmaf(S[p * kNs + tid], px[p], col);
-    pprevB[(long long)item * kNs + tid] = c0 * col;
-    float part = 0.0f;
-    if (tid < kP) {
-        float row = 0.0f;
-        const float* Sp = S + tid * kNs;
-        for (int n = 0; n < kNs; ++n) row = fmaf(Sp[n], pb[n], row);
-        dprev_x[(long long)item * kP + tid] = c0 * row;
-        part = px[tid] * row;
+    // pprevB[r][n] = c0 sum_p dS[p][n] prev_x[r][p]
+    {
+        float col[RK];
+#pragma unroll
+        for (int r = 0; r < RK; ++r) col[r] = 0.0f;
+#pragma unroll 8
+        for (int pp = 0; pp < kP; ++pp) {
+            const float sv = Ss[pp * kRow + tid];
+#pragma unroll
+            for (int r = 0; r < RK; ++r) col[r] = fmaf(sv, px[r][pp], col[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < RK; ++r) pprevB[((long long)item * RK + r) * kNs + tid] = c0 * col[r];
+    }
+    // dprev_x[r][p] = c0 sum_n dS[p][n] prev_B[r][n]: row p = tid / 2, n of
+    // parity tid % 2, the pair combined by one shuffle
+    {
+        const int pp = tid >> 1, par = tid & 1;
+        float row[RK];
+#pragma unroll
+        for (int r = 0; r < RK; ++r) row[r] = 0.0f;
+        const float* Sp = Ss + pp * kRow + par;
+#pragma unroll 8
+        for (int m = 0; m < kNs / 2; ++m) {
+            const float sv = Sp[2 * m];
+#pragma unroll
+            for (int r = 0; r < RK; ++r) row[r] = fmaf(sv, pb[r][2 * m + par], row[r]);
+        }
+        float part = 0.0f;
+#pragma unroll
+        for (int r = 0; r < RK; ++r) {
+            row[r] += __shfl_xor_sync(0xffffffffu, row[r], 1);
+            if (par == 0) dprev_x[(((long long)b * RK + r) * nheads + h) * kP + pp] = c0 * row[r];
+            part = fmaf(px[r][pp], row[r], part);
+        }
+        if (par) part = 0.0f;  // each row once
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
         if ((tid & 31) == 0) red[tid >> 5] = part;
     }
     __syncthreads();
-    if (tid == 0) dc0[item] = red[0] + red[1];
+    if (tid == 0) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kNs / 32; ++w) sum += red[w];
+        dc0[item] = sum;
+    }
 }
 
 // dprev_B[b,g,n] = the group's heads' pprevB, added in head order.
@@ -1320,7 +1376,7 @@ extern "C" ssm_status_t ssd_mamba3_bwd(const void* x, const float* dt, const flo
     if (rc != SSM_OK) return rc;
     // 4. the previous token's gradients and dL/dc_{-1}
     if (has_prev) {
-        m3_prev_kernel<<<(unsigned)items, kNs, 0, s>>>(
+        m3m_prev_kernel<1><<<(unsigned)items, kNs, 0, s>>>(
             dS_out, static_cast<const __nv_bfloat16*>(prev_B),
             static_cast<const __nv_bfloat16*>(prev_x), dt, lam, dprev_x, ppb, dc0, batch, seqlen,
             nheads, ngroups);
@@ -1487,66 +1543,6 @@ __global__ void m3m_dots_kernel(const __nv_bfloat16* __restrict__ x,
             if ((sub & (8 / R2 - 1)) == 0) out[base] = acc[0];
         }
     }
-}
-
-// The previous token per (b, h), all ranks in one pass over dS (as
-// m3_prev_kernel):
-//   dprev_x[b,r,h,p] = c0 sum_n dS[p,n] prev_B[b,r,g,n],
-//   pprevB[b,h,r,n] = c0 sum_p dS[p,n] prev_x[b,r,h,p],
-//   dc0[b,h] = sum_r sum_p prev_x[b,r,h,p] sum_n dS[p,n] prev_B[b,r,g,n].
-template <int RK>
-__global__ void m3m_prev_kernel(const float* __restrict__ dS,
-                                const __nv_bfloat16* __restrict__ prev_B,
-                                const __nv_bfloat16* __restrict__ prev_x,
-                                const float* __restrict__ dt, const float* __restrict__ lam,
-                                float* __restrict__ dprev_x, float* __restrict__ pprevB,
-                                float* __restrict__ dc0, int batch, int seqlen, int nheads,
-                                int ngroups) {
-    __shared__ float pb[RK][kNs], px[RK][kP], red[2];
-    const int item = blockIdx.x, b = item / nheads, h = item % nheads;
-    const int g = h / (nheads / ngroups);
-    const int tid = threadIdx.x;
-    const long long i0 = (long long)b * seqlen * nheads + h;
-    const float c0 = dt[i0] * (1.0f - lam[i0]);
-#pragma unroll
-    for (int r = 0; r < RK; ++r) {
-        pb[r][tid] = __bfloat162float(prev_B[(((long long)b * RK + r) * ngroups + g) * kNs + tid]);
-        if (tid < kP) px[r][tid] = __bfloat162float(prev_x[(((long long)b * RK + r) * nheads + h) * kP + tid]);
-    }
-    __syncthreads();
-    const float* S = dS + (long long)item * kP * kNs;
-    float col[RK];
-#pragma unroll
-    for (int r = 0; r < RK; ++r) col[r] = 0.0f;
-    for (int p = 0; p < kP; ++p) {
-        const float sv = S[p * kNs + tid];
-#pragma unroll
-        for (int r = 0; r < RK; ++r) col[r] = fmaf(sv, px[r][p], col[r]);
-    }
-#pragma unroll
-    for (int r = 0; r < RK; ++r) pprevB[((long long)item * RK + r) * kNs + tid] = c0 * col[r];
-    if (tid < kP) {
-        float row[RK];
-#pragma unroll
-        for (int r = 0; r < RK; ++r) row[r] = 0.0f;
-        const float* Sp = S + tid * kNs;
-        for (int n = 0; n < kNs; ++n) {
-            const float sv = Sp[n];
-#pragma unroll
-            for (int r = 0; r < RK; ++r) row[r] = fmaf(sv, pb[r][n], row[r]);
-        }
-        float part = 0.0f;
-#pragma unroll
-        for (int r = 0; r < RK; ++r) {
-            dprev_x[(((long long)b * RK + r) * nheads + h) * kP + tid] = c0 * row[r];
-            part = fmaf(px[r][tid], row[r], part);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-        if ((tid & 31) == 0) red[tid >> 5] = part;
-    }
-    __syncthreads();
-    if (tid == 0) dc0[item] = red[0] + red[1];
 }
 
 // dprev_B[b,r,g,n] = the group's heads' pprevB, added in head order.
