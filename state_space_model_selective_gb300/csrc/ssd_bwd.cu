@@ -1025,39 +1025,112 @@ __global__ void m3_weights_kernel(const float* __restrict__ dt, const float* __r
     }
 }
 
-// xd[b,t,h] = x_t . dy_t over p (64) and cb[b,t,g] = C_t . B_t over n (128):
-// one warp per row, lanes summed by a fixed butterfly.
-__global__ void m3_dots_kernel(const __nv_bfloat16* __restrict__ x,
-                               const __nv_bfloat16* __restrict__ dy,
-                               const __nv_bfloat16* __restrict__ B,
-                               const __nv_bfloat16* __restrict__ C, float* __restrict__ xd,
-                               float* __restrict__ cb, int batch, int seqlen, int nheads,
-                               int ngroups) {
+__device__ __forceinline__ void unpack8(uint4 w, float (&v)[8]) {
+    v[0] = bf16lo(w.x); v[1] = bf16hi(w.x); v[2] = bf16lo(w.y); v[3] = bf16hi(w.y);
+    v[4] = bf16lo(w.z); v[5] = bf16hi(w.z); v[6] = bf16lo(w.w); v[7] = bf16hi(w.w);
+}
+
+// The per-step rank dots: for every (step, head) the R x R products
+// XD[r'][r] = x_{t,r'} . dy_{t,r} over headdim, and for every (step, group)
+// G[r][r'] = C_{t,r} . B_{t,r'} over dstate.  Eight lanes take one item, each
+// a 16-byte vector of every row (x, dy: 8 of 64 elements; B, C: 16 of 128 in
+// two passes); the R^2 partial dots are reduce-scattered over the 8 lanes
+// (rank 4: 14 shuffles, each lane stores 2 of them; rank 2: 4 shuffles, one
+// lane of each pair stores; rank 1, the single-input gradient's x.dy and
+// C.B: 3 shuffles, one lane of the 8 stores).
+template <int RK>
+__global__ void m3m_dots_kernel(const __nv_bfloat16* __restrict__ x,
+                                const __nv_bfloat16* __restrict__ dy,
+                                const __nv_bfloat16* __restrict__ B,
+                                const __nv_bfloat16* __restrict__ C, float* __restrict__ XD,
+                                float* __restrict__ G, int batch, int seqlen, int nheads,
+                                int ngroups) {
+    constexpr int R2 = RK * RK;
+    static_assert(R2 == 1 || R2 == 4 || R2 == 16, "ranks 1, 2, 4");
+    constexpr int kLanes = 8;
     const long long steps = (long long)batch * seqlen;
     const long long nx = steps * nheads, nb = steps * ngroups;
-    const int lane = threadIdx.x & 31;
-    const long long wstride = ((long long)gridDim.x * blockDim.x) >> 5;
-    for (long long r = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; r < nx + nb;
-         r += wstride) {
-        float acc;
-        if (r < nx) {
-            const uint32_t a = reinterpret_cast<const uint32_t*>(x + r * kP)[lane];
-            const uint32_t d = reinterpret_cast<const uint32_t*>(dy + r * kP)[lane];
-            acc = fmaf(bf16hi(a), bf16hi(d), bf16lo(a) * bf16lo(d));
-        } else {
-            const long long q = r - nx;
-            const uint2 bw = reinterpret_cast<const uint2*>(B + q * kNs)[lane];
-            const uint2 cw = reinterpret_cast<const uint2*>(C + q * kNs)[lane];
-            acc = bf16lo(bw.x) * bf16lo(cw.x);
-            acc = fmaf(bf16hi(bw.x), bf16hi(cw.x), acc);
-            acc = fmaf(bf16lo(bw.y), bf16lo(cw.y), acc);
-            acc = fmaf(bf16hi(bw.y), bf16hi(cw.y), acc);
-        }
+    const int sub = threadIdx.x & (kLanes - 1);  // lane within the item
+    // whole warps step together (4 items each), so every shuffle has all lanes
+    const long long wstride = ((long long)gridDim.x * blockDim.x) / 32 * 4;
+    const long long w0 = (blockIdx.x * (long long)blockDim.x + threadIdx.x) / 32 * 4;
+    for (long long qw = w0; qw < nx + nb; qw += wstride) {
+        const long long q = qw + (threadIdx.x & 31) / kLanes;
+        float acc[R2];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) {
-            if (r < nx) xd[r] = acc;
-            else cb[r - nx] = acc;
+        for (int k = 0; k < R2; ++k) acc[k] = 0.0f;
+        if (q >= nx + nb) {
+            // past the last item: zeros through the shuffles, nothing stored
+        } else if (q < nx) {
+            const long long bt = q / nheads;
+            const int h = (int)(q % nheads);
+            float a[RK][8], d[RK][8];
+#pragma unroll
+            for (int r = 0; r < RK; ++r) {
+                const long long row = ((bt * RK + r) * nheads + h) * kP + 8 * sub;
+                unpack8(__ldg(reinterpret_cast<const uint4*>(x + row)), a[r]);
+                unpack8(__ldg(reinterpret_cast<const uint4*>(dy + row)), d[r]);
+            }
+#pragma unroll
+            for (int rp = 0; rp < RK; ++rp)
+#pragma unroll
+                for (int r = 0; r < RK; ++r)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        acc[rp * RK + r] = fmaf(a[rp][e], d[r][e], acc[rp * RK + r]);
+        } else {
+            const long long q2 = q - nx;
+            const long long bt = q2 / ngroups;
+            const int g = (int)(q2 % ngroups);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float bw[RK][8], cw[RK][8];
+#pragma unroll
+                for (int r = 0; r < RK; ++r) {
+                    const long long row = ((bt * RK + r) * ngroups + g) * kNs + 64 * half + 8 * sub;
+                    unpack8(__ldg(reinterpret_cast<const uint4*>(B + row)), bw[r]);
+                    unpack8(__ldg(reinterpret_cast<const uint4*>(C + row)), cw[r]);
+                }
+#pragma unroll
+                for (int r = 0; r < RK; ++r)
+#pragma unroll
+                    for (int rp = 0; rp < RK; ++rp)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            acc[r * RK + rp] = fmaf(cw[r][e], bw[rp][e], acc[r * RK + rp]);
+            }
+        }
+        // reduce-scatter over the item's 8 lanes (lane bits 2, 1, 0): afterwards
+        // a lane holds the totals of R2 / 8 values from index base (R2 >= 8), or
+        // of value base, shared by 8 / R2 lanes of which the lowest stores it
+        int base = 0;
+        int n = R2;
+#pragma unroll
+        for (int m = 4; m >= 1; m >>= 1) {
+            if (n == 1) {
+                acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], m);
+                continue;
+            }
+            n >>= 1;
+            const bool hi = sub & m;
+#pragma unroll
+            for (int k = 0; k < R2 / 2; ++k) {
+                if (k < n) {
+                    const float send = hi ? acc[k] : acc[k + n];
+                    const float keep = hi ? acc[k + n] : acc[k];
+                    acc[k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                }
+            }
+            if (hi) base += n;
+        }
+        if (q >= nx + nb) continue;
+        float* out = q < nx ? XD + q * R2 : G + (q - nx) * R2;
+        if constexpr (R2 >= 8) {
+            constexpr int per = R2 / 8;
+#pragma unroll
+            for (int k = 0; k < per; ++k) out[base + k] = acc[k];
+        } else {
+            if ((sub & (8 / R2 - 1)) == 0) out[base] = acc[0];
         }
     }
 }
@@ -1359,7 +1432,7 @@ extern "C" ssm_status_t ssd_mamba3_bwd(const void* x, const float* dt, const flo
     // 2. x . dy per head and C . B per group, every step (inputs only; C . B
     // feeds the diagonal correction the gradient kernel applies to dx)
     const long long nrows = (long long)steps * (nheads + ngroups);
-    m3_dots_kernel<<<grid_for(nrows * 32, 256), 256, 0, s>>>(
+    m3m_dots_kernel<1><<<grid_for(nrows * 8, 256), 256, 0, s>>>(
         static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(dy),
         static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), xd, cb,
         batch, seqlen, nheads, ngroups);
@@ -1436,114 +1509,6 @@ __global__ void m3m_expand_kernel(const float* __restrict__ dt, const float* __r
 // C_{t,r} . B_{t,r'} (over n): one warp per (step, head) or (step, group) row
 // reads its RK x (or C) and RK dy (or B) rows once and forms all RK^2 dots,
 // each summed over the lanes by a fixed butterfly.
-template <int RK>
-__device__ __forceinline__ void unpack8(uint4 w, float (&v)[8]) {
-    v[0] = bf16lo(w.x); v[1] = bf16hi(w.x); v[2] = bf16lo(w.y); v[3] = bf16hi(w.y);
-    v[4] = bf16lo(w.z); v[5] = bf16hi(w.z); v[6] = bf16lo(w.w); v[7] = bf16hi(w.w);
-}
-
-// The per-step rank dots: for every (step, head) the R x R products
-// XD[r'][r] = x_{t,r'} . dy_{t,r} over headdim, and for every (step, group)
-// G[r][r'] = C_{t,r} . B_{t,r'} over dstate.  Eight lanes take one item, each
-// a 16-byte vector of every row (x, dy: 8 of 64 elements; B, C: 16 of 128 in
-// two passes); the R^2 partial dots are reduce-scattered over the 8 lanes
-// (14 shuffles), and each lane stores 2 of them.
-template <int RK>
-__global__ void m3m_dots_kernel(const __nv_bfloat16* __restrict__ x,
-                                const __nv_bfloat16* __restrict__ dy,
-                                const __nv_bfloat16* __restrict__ B,
-                                const __nv_bfloat16* __restrict__ C, float* __restrict__ XD,
-                                float* __restrict__ G, int batch, int seqlen, int nheads,
-                                int ngroups) {
-    constexpr int R2 = RK * RK;
-    static_assert(R2 == 1 || R2 == 4 || R2 == 16, "ranks 1, 2, 4");
-    constexpr int kLanes = 8;
-    const long long steps = (long long)batch * seqlen;
-    const long long nx = steps * nheads, nb = steps * ngroups;
-    const int sub = threadIdx.x & (kLanes - 1);  // lane within the item
-    // whole warps step together (4 items each), so every shuffle has all lanes
-    const long long wstride = ((long long)gridDim.x * blockDim.x) / 32 * 4;
-    const long long w0 = (blockIdx.x * (long long)blockDim.x + threadIdx.x) / 32 * 4;
-    for (long long qw = w0; qw < nx + nb; qw += wstride) {
-        const long long q = qw + (threadIdx.x & 31) / kLanes;
-        float acc[R2];
-#pragma unroll
-        for (int k = 0; k < R2; ++k) acc[k] = 0.0f;
-        if (q >= nx + nb) {
-            // past the last item: zeros through the shuffles, nothing stored
-        } else if (q < nx) {
-            const long long bt = q / nheads;
-            const int h = (int)(q % nheads);
-            float a[RK][8], d[RK][8];
-#pragma unroll
-            for (int r = 0; r < RK; ++r) {
-                const long long row = ((bt * RK + r) * nheads + h) * kP + 8 * sub;
-                unpack8<RK>(__ldg(reinterpret_cast<const uint4*>(x + row)), a[r]);
-                unpack8<RK>(__ldg(reinterpret_cast<const uint4*>(dy + row)), d[r]);
-            }
-#pragma unroll
-            for (int rp = 0; rp < RK; ++rp)
-#pragma unroll
-                for (int r = 0; r < RK; ++r)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        acc[rp * RK + r] = fmaf(a[rp][e], d[r][e], acc[rp * RK + r]);
-        } else {
-            const long long q2 = q - nx;
-            const long long bt = q2 / ngroups;
-            const int g = (int)(q2 % ngroups);
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float bw[RK][8], cw[RK][8];
-#pragma unroll
-                for (int r = 0; r < RK; ++r) {
-                    const long long row = ((bt * RK + r) * ngroups + g) * kNs + 64 * half + 8 * sub;
-                    unpack8<RK>(__ldg(reinterpret_cast<const uint4*>(B + row)), bw[r]);
-                    unpack8<RK>(__ldg(reinterpret_cast<const uint4*>(C + row)), cw[r]);
-                }
-#pragma unroll
-                for (int r = 0; r < RK; ++r)
-#pragma unroll
-                    for (int rp = 0; rp < RK; ++rp)
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            acc[r * RK + rp] = fmaf(cw[r][e], bw[rp][e], acc[r * RK + rp]);
-            }
-        }
-        // reduce-scatter over the item's 8 lanes (lane bits 2, 1, 0): afterwards
-        // a lane holds the totals of R2 / 8 values from index base (R2 >= 8), or
-        // of value base, shared by 8 / R2 lanes of which the lowest stores it
-        int base = 0;
-        int n = R2;
-#pragma unroll
-        for (int m = 4; m >= 1; m >>= 1) {
-            if (n == 1) {
-                acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], m);
-                continue;
-            }
-            n >>= 1;
-            const bool hi = sub & m;
-#pragma unroll
-            for (int k = 0; k < R2 / 2; ++k) {
-                if (k < n) {
-                    const float send = hi ? acc[k] : acc[k + n];
-                    const float keep = hi ? acc[k + n] : acc[k];
-                    acc[k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-                }
-            }
-            if (hi) base += n;
-        }
-        if (q >= nx + nb) continue;
-        float* out = q < nx ? XD + q * R2 : G + (q - nx) * R2;
-        if constexpr (R2 >= 8) {
-            constexpr int per = R2 / 8;
-#pragma unroll
-            for (int k = 0; k < per; ++k) out[base + k] = acc[k];
-        } else {
-            if ((sub & (8 / R2 - 1)) == 0) out[base] = acc[0];
-        }
-    }
-}
 
 // dprev_B[b,r,g,n] = the group's heads' pprevB, added in head order.
 __global__ void m3m_prev_b_kernel(const float* __restrict__ pprevB, float* __restrict__ dprev_B,
