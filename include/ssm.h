@@ -679,7 +679,8 @@ ssm_status_t ssd_mamba3_mimo_bwd(const void* x, const float* dt, const float* la
  * Bytes of device workspace ssm_scan_fwd_host needs (a pure function of its
  * arguments; 0 if they are invalid).  Four slots, each the largest segment's u,
  * delta, z, B, C, y and states (a segment is at most about 1/8 of the (batch,
- * channel) rows, all steps), plus the largest segment's ssm_scan_workspace_bytes.
+ * channel) rows, and at most 3072 rows on long sequences, all steps), plus the
+ * largest segment's ssm_scan_workspace_bytes.
  */
 size_t ssm_scan_fwd_host_workspace_bytes(int batch, int dim, int seqlen, int dstate, int ngroups,
                                          ssm_dtype_t in_dtype, ssm_dtype_t out_dtype);
@@ -698,9 +699,17 @@ size_t ssm_scan_fwd_host_workspace_bytes(int batch, int dim, int seqlen, int dst
  *   segment's u, delta, z, its groups' B and C and its initial state are
  *   copied in with one 1-D copy each, scanned on `stream`, and its y and final
  *   state copied back, with the copies of neighbouring segments in flight
- *   during the scan.  Every segment is scanned by the kernel, and with the
- *   plan, that ssm_scan_fwd would use for the whole problem, so the result is
- *   bit-equal to ssm_scan_fwd on device copies of the same inputs.
+ *   during the scan.
+ *  - Kernel per segment: where every segment fits the sequence-parallel scan
+ *    (at most 3072 channels; on long sequences segments are capped to fit)
+ *    while the whole problem does not, every segment takes that scan with one
+ *    segments-per-chunk count, so a segment's scan time shrinks with its size
+ *    (the chained scan's CTAs each walk the whole sequence).  Each channel's
+ *    result is then bit-equal to ssm_scan_fwd run on any channel subset the
+ *    sequence-parallel scan takes with the same count, and within the stated
+ *    tolerance of the oracle, like either kernel.  Otherwise every segment is
+ *    scanned with the kernel and plan ssm_scan_fwd would use for the whole
+ *    problem, and the result is bit-equal to ssm_scan_fwd on device copies.
  *
  *  - Asynchronous like every entry point: work is enqueued on `stream` and on
  *    two copy streams of the library's own (created on the first call on a

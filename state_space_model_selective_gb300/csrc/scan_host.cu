@@ -16,13 +16,25 @@
 // states, and its groups' B and C) is one contiguous block of host memory,
 // moved by a single 1-D copy at the link's full rate (2-D copies of short rows
 // run well below it).  Segment k's inputs are copied on a copy stream into one
-// of four device slots, the caller's stream scans the slot with the kernel and
-// plan the whole problem would use (so the result is the whole call's, bit for
-// bit), and a second copy stream brings y and the final state back.  Four
-// slots let the input copies run up to three segments ahead of the scans.
-// Copies in both directions run on the copy engines while the SMs scan the
-// neighbouring segments.  The two copy streams and the events are created once
-// per device and kept for the life of the process.
+// of four device slots, the caller's stream scans the slot, and a second copy
+// stream brings y and the final state back.  Four slots let the input copies
+// run up to three segments ahead of the scans.  Copies in both directions run
+// on the copy engines while the SMs scan the neighbouring segments.  The two
+// copy streams and the events are created once per device and kept for the
+// life of the process.
+//
+// Which kernel scans a segment: a segment of a few thousand channels leaves
+// most SMs idle in the chained scan, whose CTAs each walk the whole sequence
+// (about 0.8 ms for any segment of a 16 k-step problem), and the last
+// segment's scan is on the critical path.  So when every segment fits the
+// sequence-parallel scan, all segments take it, with one segments-per-chunk
+// count, and its time shrinks with the segment (on long sequences the
+// segments are capped to fit it).  A channel's arithmetic depends only on the
+// kernel and that count, so the result is bit-equal to ssm_scan_fwd of any
+// channel subset the sequence-parallel scan takes with the same count.  Other
+// problems (those ssm_scan_fwd itself gives to the sequence-parallel scan,
+// and short sequences with segments too large for it) run every segment with
+// the whole problem's kernel and plan: bit-equal to ssm_scan_fwd.
 #include <algorithm>
 #include <mutex>
 #include <vector>
@@ -37,6 +49,9 @@ using namespace ssm_host;
 constexpr int kN = 16;
 constexpr int kSlots = 4;
 constexpr long long kTargetSegments = 8;
+// Input and output bytes a segment capped to the sequence-parallel scan's size
+// must still move for the cap to apply.
+constexpr size_t kMinCappedSegmentBytes = size_t(32) << 20;
 
 // One segment: batches [b0, b0 + nb), channels [c0, c0 + nc) of each, which lie
 // in groups [g0, g0 + ng).  Either whole batches (c0 = 0, nc = dim), or one
@@ -61,7 +76,12 @@ Plan plan_for(int batch, int dim, int seqlen, int ngroups, size_t es, size_t eo)
     Plan p{};
     const long long rows = (long long)batch * dim;
     const int cg = dim / ngroups;  // channels per group
-    const long long target = std::max(1LL, (rows + kTargetSegments - 1) / kTargetSegments);
+    long long target = std::max(1LL, (rows + kTargetSegments - 1) / kTargetSegments);
+    // on long sequences, segments small enough for the sequence-parallel scan
+    // (their copies still far outweigh a segment's fixed launch and copy costs)
+    const long long cap = ssm_internal::kScanSegMaxChannels;
+    if (target > cap && (size_t)cap * seqlen * (3 * es + eo) >= kMinCappedSegmentBytes)
+        target = cap;
     if (target >= dim) {
         const int per = (int)std::min<long long>(target / dim, batch);
         for (int b = 0; b < batch; b += per)
@@ -232,6 +252,17 @@ extern "C" ssm_status_t ssm_scan_fwd_host(const void* u, const void* delta, cons
     for (const void* p : dev_ptrs)
         if (!is_device(p)) return SSM_ERR_UNSUPPORTED;
 
+    // every segment's arrays fit its slot's regions (the plan's own invariant,
+    // checked before anything is enqueued)
+    for (const Seg& sg : pl.segs) {
+        const size_t nrows = (size_t)sg.nb * sg.nc, nbc = (size_t)sg.nb * sg.ng * kN;
+        if (nrows * seqlen * es > pl.act_in || nbc * seqlen * es > pl.bc_in ||
+            nrows * seqlen * eo > pl.act_out || nrows * kN * 4 > pl.state ||
+            (size_t)sg.nc * 4 > pl.par ||
+            ssm_scan_workspace_bytes(sg.nb, sg.nc, seqlen, kN, sg.ng) > pl.scan_ws)
+            return SSM_ERR_WORKSPACE;
+    }
+
     std::mutex* lock = nullptr;
     DeviceQueues* q = queues(lock);
     if (!q) return SSM_ERR_CUDA;
@@ -248,9 +279,18 @@ extern "C" ssm_status_t ssm_scan_fwd_host(const void* u, const void* delta, cons
     chk(cudaStreamWaitEvent(q->copy_in, q->ev_done, 0));
     chk(cudaStreamWaitEvent(q->copy_out, q->ev_done, 0));
     const size_t L = (size_t)seqlen;
-    // the kernel and plan of the whole problem, used for every segment
-    const int path = ssm_internal::scan_uses_seg_path(batch, dim) ? 2 : 1;
-    const int seg_ts = ssm_internal::scan_seg_plan_ts(batch, dim, seqlen);
+    // the kernel (path) and sequence-parallel segments per chunk of every segment
+    int path, seg_ts;
+    if (ssm_internal::scan_seg_eligible(batch, dim) ||
+        !ssm_internal::scan_seg_eligible(1, pl.max_rows)) {
+        // the whole problem's kernel and plan
+        path = ssm_internal::scan_uses_seg_path(batch, dim) ? 2 : 1;
+        seg_ts = ssm_internal::scan_seg_plan_ts(batch, dim, seqlen);
+    } else {
+        // every segment fits the sequence-parallel scan: one count for all
+        path = ssm_internal::scan_uses_seg_path(1, pl.max_rows) ? 2 : 1;
+        seg_ts = ssm_internal::scan_seg_plan_ts(1, pl.max_rows, seqlen);
+    }
     ssm_status_t rc = SSM_OK;
     for (size_t k = 0; k < pl.segs.size() && ok && rc == SSM_OK; ++k) {
         const Seg& sg = pl.segs[k];

@@ -304,17 +304,19 @@ def test_workload_scan_bf16_whole(shape, seed):
                                   (4, 32, 64, 4, "bf16", torch.bfloat16, True),
                                   (2, 36, 200, 6, "f32", torch.float32, True),
                                   (1, 100, 300, 1, "bf16", torch.float32, True),
-                                  (2, 2048, 256, 1, "bf16", torch.float32, True)],
+                                  (8, 4096, 64, 1, "f32", torch.float32, True)],
                          ids=["bf16-L700", "f32-L1000-G2", "bf16out-L64", "L30",
                               "B5-L300", "B9-G2-L130", "B4-bf16out-G4", "G6-whole-groups",
-                              "part-groups-D100", "chained-whole"])
+                              "part-groups-D100", "chained-segments"])
 def test_scan_host_buffers_equal_device_scan(case):
     """ssm_scan_fwd_host (host-resident activations, copies pipelined over
     segments of the channels) gives the same bits as ssm_scan_fwd on device
     copies, and matches the oracle.  The cases cut segments at whole batches,
     whole groups (channel offsets that leave D and the bias unaligned) and
-    inside a group; the last is a problem the chained scan takes whose
-    segments alone would take the sequence-parallel one."""
+    inside a group.  All but the last are problems ssm_scan_fwd gives to the
+    sequence-parallel scan; the last is a short sequence whose 4096-channel
+    segments are too large for it, so every segment takes the chained scan,
+    as the whole call does."""
     batch, dim, seqlen, ngroups, dt, out_dt, with_h0 = case
     inp = inputs.scan_inputs(batch, dim, seqlen, 16, ngroups, dt, seed=120 + seqlen)
     h0 = (torch.randn(batch, dim, 16, generator=torch.Generator().manual_seed(3)) * 0.5
@@ -335,6 +337,69 @@ def test_scan_host_buffers_equal_device_scan(case):
         tol = TOL_F32 if dt == "f32" else TOL_BF16
         assert_close(y_h, y_ref, tol, "y")
         assert_close(fs_h, fs_ref, tol, "final_state")
+
+
+def _piece(inp, h0, b, c0, c1):
+    """The problem of batch row b's channels [c0, c1), all in one B/C group."""
+    dim, ngroups = inp["u"].shape[1], inp["B"].shape[1]
+    g = c0 // (dim // ngroups)
+    assert (c1 - 1) // (dim // ngroups) == g
+    x = dict(inp)
+    for k in ("u", "delta", "z"):
+        if inp[k] is not None:
+            x[k] = inp[k][b:b + 1, c0:c1].contiguous()
+    for k in ("B", "C"):
+        x[k] = inp[k][b:b + 1, g:g + 1].contiguous()
+    for k in ("A", "D", "delta_bias"):
+        if inp[k] is not None:
+            x[k] = inp[k][c0:c1].contiguous()
+    return x, (None if h0 is None else h0[b:b + 1, c0:c1].contiguous())
+
+
+@pytest.mark.parametrize("case", [
+    # batch, dim, seqlen, dtype, out dtype, channels per device piece, forced segments per chunk
+    (2, 2048, 256, "bf16", torch.float32, 2048, 16),
+    (8, 4096, 1100, "bf16", torch.float32, 2048, 8),
+], ids=["seqpar-segments", "capped-segments"])
+def test_scan_host_sequence_parallel_segments(case):
+    """Problems the chained scan takes whole, whose host-path segments each fit
+    the sequence-parallel scan, have every segment scanned by that kernel with
+    one segment count.  A channel's arithmetic then depends only on the kernel
+    and that count: with the count forced, the host path gives the bits of
+    ssm_scan_fwd run on device pieces of the channels; as planned it matches
+    the oracle.  The second case is a long sequence whose segments, an eighth
+    of the 32768 channels (4096) by default, are capped to fit the
+    sequence-parallel scan (at most 3072 channels; here half a batch row)."""
+    batch, dim, seqlen, dt, out_dt, piece, ts = case
+    inp = inputs.scan_inputs(batch, dim, seqlen, 16, 1, dt, seed=160 + seqlen)
+    h0 = torch.randn(batch, dim, 16, generator=torch.Generator().manual_seed(5)) * 0.5
+    pin = {k: (v.pin_memory() if isinstance(v, torch.Tensor) and k in ("u", "delta", "z", "B", "C")
+               else v) for k, v in inp.items()}
+
+    def host():
+        y_h = torch.full((batch, dim, seqlen), float("nan"), dtype=out_dt).pin_memory()
+        fs_h = torch.full((batch, dim, 16), float("nan")).pin_memory()
+        binding.ssm_scan_fwd_host(pin["u"], pin["delta"], inp["A"].cuda(), pin["B"], pin["C"],
+                                  y_h, fs_h, inp["D"].cuda(), pin["z"], inp["delta_bias"].cuda(),
+                                  True, h0.pin_memory())
+        torch.cuda.synchronize()
+        return y_h, fs_h
+
+    binding.ssm_debug_set_scan_path(0, ts)
+    try:
+        y_h, fs_h = host()
+        for b in range(batch):
+            for c0 in range(0, dim, piece):
+                x, h = _piece(inp, h0, b, c0, c0 + piece)
+                y_p, fs_p = _run(x, out_dtype=out_dt, initial_state=h)
+                assert torch.equal(y_h[b:b + 1, c0:c0 + piece], y_p.cpu()), (b, c0)
+                assert torch.equal(fs_h[b:b + 1, c0:c0 + piece], fs_p.cpu()), (b, c0)
+    finally:
+        binding.ssm_debug_set_scan_path()
+    y_h, fs_h = host()
+    y_ref, fs_ref = _oracle(inp, h0)
+    assert_close(y_h, y_ref, TOL_BF16, "y")
+    assert_close(fs_h, fs_ref, TOL_BF16, "final_state")
 
 
 @pytest.mark.parametrize("with_h0", [True, False])
