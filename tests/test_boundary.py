@@ -505,6 +505,23 @@ def test_scan_host_argument_errors(L):
     assert f(8, 1536, 2048, dstate=8) == 0
 
 
+def test_scan_host_segments_capped_on_long_sequences():
+    """On a long sequence the host path's segments are capped at the
+    sequence-parallel scan's 3072 channels, whatever the problem's channel count;
+    on a short one (a capped segment would move under 32 MB) a segment stays about
+    an eighth of the (batch, channel) rows."""
+    f = binding.ssm_scan_fwd_host_workspace_bytes
+    # 16 x 4096 rows, 4 groups of 1024 channels, bf16 in / fp32 out: 10 bytes per
+    # row-step.  Capped: segments of 3 groups (3072 rows) and 1 group.
+    L = 4096
+    capped = 4 * 3072 * L * 10 + binding.ssm_scan_workspace_bytes(1, 3072, L, 16, 3)
+    assert 0 < f(16, 4096, L, ngroups=4) <= 1.05 * capped
+    # an eighth of the rows (8192) per slot, as without the cap
+    assert f(16, 4096, L, ngroups=4) < 4 * 8192 * L * 10
+    # L 64: a 3072-row segment would move 2 MB, so segments stay 8192 rows
+    assert f(16, 4096, 64, ngroups=4) >= 4 * 8192 * 64 * 10
+
+
 def rope_call(L, **kw):
     args = dict(B=P(0), C=P(1), dt=P(2), theta=P(3), a0=None, Br=P(4), Cr=P(5), aout=P(6),
                 batch=2, seqlen=8, rank=1, nheads=4, ngroups=2, dstate=16, dtype=1, stream=None)
