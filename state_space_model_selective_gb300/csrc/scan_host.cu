@@ -103,9 +103,10 @@ Plan plan_for(int batch, int dim, int seqlen, int ngroups, size_t es, size_t eo)
     }
     // The first segment's input copy runs before anything can overlap it, and the
     // last segment's scan and output copy after: the end segments are halved.
-    // (Halving them again measured slower: a scan of a segment takes about as
-    // long whatever its size, about 0.8 ms on the largest problems, and more
-    // of them no longer hide behind the copies.)
+    // (Halving them again gained nothing on a 16 k-step problem: with the
+    // chained scan each extra segment's scan, about 0.8 ms whatever its size,
+    // no longer hid behind the copies; with the sequence-parallel scan the
+    // copies alone set the time.)
     auto halve = [&](const Seg& sg, std::vector<Seg>& out) {
         if (sg.nb > 1) {  // whole batches
             const int h = sg.nb / 2;
