@@ -247,7 +247,7 @@ struct Smem {
     static_assert(2 * BC_TILE <= BCF, "the B/C tiles fit the converted region");
     static constexpr int STAGE = 3 * IN_TILE + BCF;
     static constexpr int NSTAGE = TMA ? Geom<Tin>::kStages : 1;
-    static constexpr int PREP = 2 * CH * prep_stride(PS);  // (dl, dl*u) and (D*u, silu(z))
+    static constexpr int PREP = 2 * CH * prep_stride(PS);  // (dl, dl*u) and (u, silu(z))
     static constexpr int BARS = 3 * NSTAGE * 8 + 16;
     static constexpr int BYTES = NSTAGE * STAGE + PREP + BARS;
     static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(CH * kNG + 32, PS == 16 ? 4 : 3)
     const float pbias = (a.bias && valid) ? a.bias[d] : 0.0f;
     const float pD = (a.Dskip && valid) ? a.Dskip[d] : 0.0f;
 
-    // prep tile rows: [CH][kTL] (dl, dl*u) pairs, then [CH][kTL] (D*u, g)
+    // prep tile rows: [CH][kTL] (dl, dl*u) pairs, then [CH][kTL] (u, g)
     // pairs, g = silu(z) (1 without a gate)
     const float* prow = reinterpret_cast<const float*>(prep + cl * kPrepStride);
     const float* prow2 = reinterpret_cast<const float*>(prep + (CH + cl) * kPrepStride);
@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(CH * kNG + 32, PS == 16 ? 4 : 3)
         const uint8_t* tBC = st + 3 * S::IN_TILE + ng * 32;
         for (int qt = 0; qt < kTL / PS && ok; ++qt) {
             // ---- prep, once per (channel, step): dl = softplus(delta + bias)
-            // (or delta + bias), dl * u, and the read-out's D * u and silu(z);
+            // (or delta + bias), dl * u, and the read-out's u and silu(z);
             // steps past the chunk end get dl = 0, an exact identity step
             // (exp(0) = 1, input term 0).
             constexpr int CS = LPS >= 8 ? 8 : 4;  // steps per chunk (one 16- or 8-byte load)
@@ -468,14 +468,20 @@ __global__ void __launch_bounds__(CH * kNG + 32, PS == 16 ? 4 : 3)
 #pragma unroll
                 for (int j = 0; j < CS; ++j) {
                     const float x = dv[j] + pbias;
-                    float dl = a.softplus ? softplus_f(x) : x;
-                    if (t0 + tl + j >= t_end) dl = 0.0f;
+                    const float dl = a.softplus ? softplus_f(x) : x;
                     o[2 * j] = dl;
                     o[2 * j + 1] = dl * uv[j];
                     if constexpr (CK != 2) {
-                        e[2 * j] = pD * uv[j];
+                        e[2 * j] = uv[j];  // the read-out adds D u with one FMA
                         e[2 * j + 1] = has_z ? silu_f(zv[j]) : 1.0f;
                     }
+                }
+                // only the tile that runs past the sequence end (uniform over
+                // the CTA) has steps to neutralise
+                if (t0 + kTL > t_end) {
+#pragma unroll
+                    for (int j = 0; j < CS; ++j)
+                        if (t0 + tl + j >= t_end) o[2 * j] = o[2 * j + 1] = 0.0f;
                 }
                 float4* dst = reinterpret_cast<float4*>(prep + cl * kPrepStride + tq * 8);
                 float4* dst2 = reinterpret_cast<float4*>(prep + (CH + cl) * kPrepStride + tq * 8);
@@ -585,8 +591,8 @@ __global__ void __launch_bounds__(CH * kNG + 32, PS == 16 ? 4 : 3)
                 const int tq = jj * 8 + 2 * ng;  // step within the group
                 const int tg = t0 + j * 8 + 2 * ng;
                 const float4 eg = *reinterpret_cast<const float4*>(prow2 + tq * 2);
-                const float o0 = (f[0] + eg.x) * eg.y;
-                const float o1 = (f[1] + eg.z) * eg.w;
+                const float o0 = fmaf(pD, eg.x, f[0]) * eg.y;
+                const float o1 = fmaf(pD, eg.z, f[1]) * eg.w;
                 if ((CK == 0 || a.y) && valid && tg < t_end)
                     store_y2<Tout>(yrow + tg, o0, o1, true, tg + 1 < t_end, vec_store);
             }
