@@ -1,0 +1,168 @@
+"""Parity with the fp64 oracle on seeded random shapes: channel counts that are no
+multiple of any tile, lengths around tile and chunk boundaries, mixed groups and
+the optional inputs switched on and off.  The shape lists are drawn once from a
+fixed seed, so every run checks the same problems."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from state_space_model_selective_gb300 import binding, inputs
+from tests.helpers import TOL_BF16, TOL_F32, assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _draw_scan(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        ngroups = int(rng.integers(1, 5))
+        cases.append(dict(batch=int(rng.integers(1, 5)), ngroups=ngroups,
+                          dim=ngroups * int(rng.integers(1, 121)),
+                          seqlen=int(rng.choice([1, 2, 7, 31, 63, 64, 65, 127, 128, 129,
+                                                 191, 256, 300, 513, 600])),
+                          dtype=str(rng.choice(["f32", "bf16"])), gate=bool(rng.integers(2)),
+                          dskip=str(rng.choice(["none", "ones", "randn"])),
+                          softplus=bool(rng.integers(2)), h0=bool(rng.integers(2))))
+    return cases
+
+
+SCAN_CASES = _draw_scan(16, 2024)
+
+
+@pytest.mark.parametrize("path", [(0, 0), (1, 0)], ids=["planned", "chained"])
+@pytest.mark.parametrize("case", SCAN_CASES,
+                         ids=[f"B{c['batch']}D{c['dim']}L{c['seqlen']}G{c['ngroups']}{c['dtype']}"
+                              for c in SCAN_CASES])
+def test_scan_random_shapes(case, path):
+    c = case
+    inp = inputs.scan_inputs(c["batch"], c["dim"], c["seqlen"], 16, c["ngroups"], c["dtype"],
+                             seed=c["dim"] * 7 + c["seqlen"], gate=c["gate"], dskip=c["dskip"])
+    inp["delta_softplus"] = c["softplus"]
+    if not c["softplus"]:  # without softplus, delta + bias must stay positive
+        inp["delta"] = (inp["delta"].float().abs() * 0.1).to(inp["delta"].dtype)
+        inp["delta_bias"] = torch.full_like(inp["delta_bias"], 0.01)
+    h0 = (torch.randn(c["batch"], c["dim"], 16, generator=torch.Generator().manual_seed(c["dim"]))
+          * 0.5 if c["h0"] else None)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    binding.ssm_debug_set_scan_path(*path)
+    try:
+        y, fs = binding.ssm_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                                     d["delta_bias"], c["softplus"],
+                                     None if h0 is None else h0.cuda(), out_dtype=torch.float32)
+        torch.cuda.synchronize()
+    finally:
+        binding.ssm_debug_set_scan_path()
+    y_ref, fs_ref = oracle.scan(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                inp["z"], inp["delta_bias"], c["softplus"], h0)
+    tol = TOL_F32 if c["dtype"] == "f32" else TOL_BF16
+    assert_close(y, y_ref, tol, "y")
+    assert_close(fs, fs_ref, tol, "final_state")
+
+
+def _draw_ssd(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        ngroups = int(rng.integers(1, 4))
+        cases.append(dict(batch=int(rng.integers(1, 4)), seqlen=64 * int(rng.integers(1, 11)),
+                          ngroups=ngroups, nheads=ngroups * int(rng.integers(1, 4)),
+                          h0=bool(rng.integers(2)), prev=bool(rng.integers(2))))
+    return cases
+
+
+SSD_CASES = _draw_ssd(8, 2025)
+
+
+@pytest.mark.parametrize("case", SSD_CASES,
+                         ids=[f"B{c['batch']}L{c['seqlen']}H{c['nheads']}G{c['ngroups']}"
+                              for c in SSD_CASES])
+def test_ssd_random_shapes(case):
+    c = case
+    inp = inputs.ssd_inputs(c["batch"], c["seqlen"], c["nheads"], 64, 128, c["ngroups"], "bf16",
+                            seed=300 + c["seqlen"] + c["nheads"])
+    h0 = (torch.randn(c["batch"], c["nheads"], 64, 128,
+                      generator=torch.Generator().manual_seed(c["seqlen"])) * 0.3
+          if c["h0"] else None)
+    d = {k: v.cuda() for k, v in inp.items()}
+    y = torch.full(d["x"].shape, float("nan"), device="cuda")
+    fs = torch.full((c["batch"], c["nheads"], 64, 128), float("nan"), device="cuda")
+    binding.ssd_chunked_fwd(d["x"], d["dt"], d["A_head"], d["B"], d["C"], 64,
+                            out_dtype=torch.float32, y=y, final_state=fs,
+                            initial_state=None if h0 is None else h0.cuda())
+    torch.cuda.synchronize()
+    y_ref, fs_ref = oracle.ssd_recurrence(inp["x"], inp["dt"], inp["A_head"], inp["B"], inp["C"],
+                                          None if h0 is None else h0.double().numpy())
+    assert_close(y, y_ref, TOL_BF16, "y")
+    assert_close(fs, fs_ref, TOL_BF16, "final_state")
+
+
+@pytest.mark.parametrize("case", SSD_CASES,
+                         ids=[f"B{c['batch']}L{c['seqlen']}H{c['nheads']}G{c['ngroups']}"
+                              for c in SSD_CASES])
+def test_mamba3_prefill_random_shapes(case):
+    c = case
+    inp = inputs.mamba3_inputs(c["batch"], c["seqlen"], c["nheads"], 64, 128, c["ngroups"],
+                               "bf16", seed=400 + c["seqlen"] + c["nheads"])
+    h0 = inp["h0"] if c["h0"] else None
+    d = {k: v.cuda() for k, v in inp.items()}
+    y = torch.full(d["x"].shape, float("nan"), device="cuda")
+    fs = torch.full((c["batch"], c["nheads"], 64, 128), float("nan"), device="cuda")
+    binding.ssd_mamba3_fwd(d["x"], d["dt"], d["lam"], d["A_head"], d["B"], d["C"], 64,
+                           out_dtype=torch.float32, y=y, final_state=fs,
+                           initial_state=None if h0 is None else h0.cuda(),
+                           prev_B=d["prev_B"] if c["prev"] else None,
+                           prev_x=d["prev_x"] if c["prev"] else None)
+    torch.cuda.synchronize()
+    y_ref, fs_ref = oracle.mamba3_recurrence(
+        inp["x"], inp["dt"], inp["lam"], inp["A_head"], inp["B"], inp["C"],
+        None if h0 is None else h0.double().numpy(),
+        inp["prev_B"] if c["prev"] else None, inp["prev_x"] if c["prev"] else None)
+    assert_close(y, y_ref, TOL_BF16, "y")
+    assert_close(fs, fs_ref, TOL_BF16, "final_state")
+
+
+def _draw_decode(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        ngroups = int(rng.integers(1, 4))
+        cases.append(dict(batch=int(rng.integers(1, 7)), ngroups=ngroups,
+                          nheads=ngroups * int(rng.integers(1, 4)),
+                          headdim=int(rng.integers(1, 131)),
+                          dstate=int(rng.choice([16, 32, 64, 128, 256])),
+                          dtype=str(rng.choice(["f32", "bf16"])), gate=bool(rng.integers(2)),
+                          dskip=str(rng.choice(["none", "ones", "randn"]))))
+    return cases
+
+
+DECODE_CASES = _draw_decode(10, 2026)
+
+
+@pytest.mark.parametrize("case", DECODE_CASES,
+                         ids=[f"B{c['batch']}H{c['nheads']}P{c['headdim']}N{c['dstate']}"
+                              f"G{c['ngroups']}{c['dtype']}" for c in DECODE_CASES])
+def test_decode_random_shapes(case):
+    c = case
+    steps = 3
+    inp = inputs.decode_inputs(c["batch"], c["nheads"], c["headdim"], c["dstate"], c["ngroups"],
+                               steps, c["dtype"], seed=500 + c["headdim"], gate=c["gate"],
+                               dskip=c["dskip"])
+    state = inp["state"].cuda()
+    ref_state = inp["state"]
+    tol = TOL_F32 if c["dtype"] == "f32" else TOL_BF16
+    D = inp["D"]
+    for t in range(steps):
+        z = inp["z"][t]
+        y = binding.ssm_decode_step(state, inp["x"][t].cuda(), inp["dt"][t].cuda(),
+                                    inp["A"].cuda(), inp["B"][t].cuda(), inp["C"][t].cuda(),
+                                    None if D is None else D.cuda(),
+                                    None if z is None else z.cuda())
+        y_ref, ref_state = oracle.decode_step(ref_state, inp["x"][t], inp["dt"][t], inp["A"],
+                                              inp["B"][t], inp["C"][t], D, z)
+        if c["dtype"] == "f32":
+            assert_close(y, y_ref, tol, f"y step {t}")
+        else:  # bf16 y: the rounding of the exact result, within one bf16 ulp
+            assert_close(y, y_ref, 2 ** -7, f"y step {t}")
+        assert_close(state, ref_state, tol, f"state step {t}")
