@@ -166,3 +166,121 @@ def test_decode_random_shapes(case):
         else:  # bf16 y: the rounding of the exact result, within one bf16 ulp
             assert_close(y, y_ref, 2 ** -7, f"y step {t}")
         assert_close(state, ref_state, tol, f"state step {t}")
+
+
+def _draw_mimo(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        rank = int(rng.choice([1, 2, 4]))
+        chunk = 64 // rank
+        ngroups = int(rng.integers(1, 3))
+        cases.append(dict(batch=int(rng.integers(1, 3)), rank=rank,
+                          seqlen=chunk * int(rng.integers(1, 9)), ngroups=ngroups,
+                          nheads=ngroups * int(rng.integers(1, 4)), h0=bool(rng.integers(2)),
+                          prev=bool(rng.integers(2))))
+    return cases
+
+
+MIMO_CASES = _draw_mimo(8, 2027)
+
+
+@pytest.mark.parametrize("case", MIMO_CASES,
+                         ids=[f"B{c['batch']}L{c['seqlen']}R{c['rank']}H{c['nheads']}"
+                              f"G{c['ngroups']}" for c in MIMO_CASES])
+def test_mimo_prefill_random_shapes(case):
+    c = case
+    inp = inputs.mamba3_mimo_inputs(c["batch"], c["seqlen"], c["rank"], c["nheads"], 64, 128,
+                                    c["ngroups"], "bf16", seed=600 + c["seqlen"] + c["rank"])
+    h0 = inp["h0"] if c["h0"] else None
+    d = {k: v.cuda() for k, v in inp.items()}
+    y = torch.full(d["x"].shape, float("nan"), device="cuda")
+    fs = torch.full((c["batch"], c["nheads"], 64, 128), float("nan"), device="cuda")
+    binding.ssd_mamba3_mimo_fwd(d["x"], d["dt"], d["lam"], d["A_head"], d["B"], d["C"],
+                                64 // c["rank"], out_dtype=torch.float32, y=y, final_state=fs,
+                                initial_state=None if h0 is None else h0.cuda(),
+                                prev_B=d["prev_B"] if c["prev"] else None,
+                                prev_x=d["prev_x"] if c["prev"] else None)
+    torch.cuda.synchronize()
+    y_ref, fs_ref = oracle.mamba3_mimo_recurrence(
+        inp["x"], inp["dt"], inp["lam"], inp["A_head"], inp["B"], inp["C"],
+        None if h0 is None else h0.double().numpy(),
+        inp["prev_B"] if c["prev"] else None, inp["prev_x"] if c["prev"] else None)
+    assert_close(y, y_ref, TOL_BF16, "y")
+    assert_close(fs, fs_ref, TOL_BF16, "final_state")
+
+
+def _draw_rope(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        ngroups = int(rng.integers(1, 4))
+        cases.append(dict(batch=int(rng.integers(1, 4)), seqlen=int(rng.integers(1, 400)),
+                          rank=int(rng.choice([1, 2, 3, 4])), ngroups=ngroups,
+                          nheads=ngroups * int(rng.integers(1, 4)),
+                          dstate=2 * int(rng.integers(1, 90)), a0=bool(rng.integers(2))))
+    return cases
+
+
+ROPE_CASES = _draw_rope(10, 2028)
+
+
+@pytest.mark.parametrize("case", ROPE_CASES,
+                         ids=[f"B{c['batch']}L{c['seqlen']}R{c['rank']}H{c['nheads']}"
+                              f"G{c['ngroups']}N{c['dstate']}" for c in ROPE_CASES])
+def test_rope_random_shapes(case):
+    c = case
+    g = torch.Generator().manual_seed(c["seqlen"] * 5 + c["dstate"])
+    shape = ((c["batch"], c["seqlen"], c["ngroups"], c["dstate"]) if c["rank"] == 1 else
+             (c["batch"], c["seqlen"], c["rank"], c["ngroups"], c["dstate"]))
+    B = torch.randn(*shape, generator=g)
+    C = torch.randn(*shape, generator=g)
+    dt = torch.nn.functional.softplus(torch.randn(c["batch"], c["seqlen"], c["nheads"],
+                                                  generator=g) - 4)
+    r = inputs.rope_inputs(c["batch"], c["seqlen"], c["nheads"], c["dstate"],
+                           seed=700 + c["seqlen"])
+    a0 = r["angle0"] if c["a0"] else None
+    Br, Cr, ang = binding.ssm_mamba3_rope(B.cuda(), C.cuda(), dt.cuda(), r["theta"].cuda(),
+                                          None if a0 is None else a0.cuda())
+    torch.cuda.synchronize()
+    Br_ref, Cr_ref, ang_ref = oracle.mamba3_rope(B, C, dt, r["theta"], a0)
+    assert_close(Br, Br_ref, TOL_F32, "B_rot")
+    assert_close(Cr, Cr_ref, TOL_F32, "C_rot")
+    np.testing.assert_allclose(ang.cpu().double().numpy(), ang_ref, rtol=2e-6, atol=2e-6)
+
+
+@pytest.mark.parametrize("case", SCAN_CASES[:10],
+                         ids=[f"B{c['batch']}D{c['dim']}L{c['seqlen']}G{c['ngroups']}{c['dtype']}"
+                              for c in SCAN_CASES[:10]])
+def test_scan_bwd_random_shapes(case):
+    from tests.test_scan_bwd_gpu import _compare, _dy, _gpu_grad, _oracle_grad
+    c = case
+    inp = inputs.scan_inputs(c["batch"], c["dim"], c["seqlen"], 16, c["ngroups"], c["dtype"],
+                             seed=c["dim"] * 3 + c["seqlen"], gate=c["gate"], dskip=c["dskip"])
+    inp["delta_softplus"] = c["softplus"]
+    if not c["softplus"]:
+        inp["delta"] = (inp["delta"].float().abs() * 0.1).to(inp["delta"].dtype)
+        inp["delta_bias"] = torch.full_like(inp["delta_bias"], 0.01)
+    dy = _dy((c["batch"], c["dim"], c["seqlen"]), c["dtype"], 9 + c["seqlen"])
+    gen = torch.Generator().manual_seed(c["dim"])
+    h0 = torch.randn(c["batch"], c["dim"], 16, generator=gen) * 0.5 if c["h0"] else None
+    dfinal = torch.randn(c["batch"], c["dim"], 16, generator=gen) if c["h0"] else None
+    _compare(_gpu_grad(inp, dy, h0, dfinal), _oracle_grad(inp, dy, h0, dfinal))
+
+
+@pytest.mark.parametrize("case", SSD_CASES[:6],
+                         ids=[f"B{c['batch']}L{c['seqlen']}H{c['nheads']}G{c['ngroups']}"
+                              for c in SSD_CASES[:6]])
+def test_ssd_bwd_random_shapes(case):
+    from tests.test_ssd_bwd_gpu import KEYS, _cotangents, _gpu, _ref
+    c = case
+    inp = inputs.ssd_inputs(c["batch"], c["seqlen"], c["nheads"], 64, 128, c["ngroups"], "bf16",
+                            seed=800 + c["seqlen"] + c["nheads"])
+    dy, dfinal = _cotangents(c["batch"], c["seqlen"], c["nheads"], 801 + c["seqlen"], c["h0"])
+    h0 = (0.1 * torch.randn(c["batch"], c["nheads"], 64, 128,
+                            generator=torch.Generator().manual_seed(c["nheads"]))
+          if c["h0"] else None)
+    g = _gpu(inp, dy, h0, dfinal)
+    ref = _ref(inp, dy, h0, dfinal)
+    for key, rkey, tol in KEYS:
+        assert_close(g[key], ref[rkey], tol, key)
