@@ -245,7 +245,8 @@ ssm_status_t ssd_mamba3_mimo_fwd(const void* x, const float* dt, const float* la
  * Layouts: state (batch, nheads, headdim, dstate) fp32, read and written;
  * x, z, y (batch, nheads, headdim) in dtype; dt (batch, nheads) fp32;
  * A, D (nheads,) fp32 (D may be NULL); B, C (batch, ngroups, dstate) in
- * dtype; z may be NULL.  Supported: dstate % 32 == 0 and dstate <= 256.
+ * dtype; z may be NULL.  Supported: dstate 16, 32, 64, 128 or 256 (else
+ * SSM_ERR_UNSUPPORTED).
  */
 ssm_status_t ssm_decode_step(float* state, const void* x, const float* dt,
                              const float* A, const void* B, const void* C,

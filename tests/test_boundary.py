@@ -193,6 +193,8 @@ def test_decode_argument_errors(L):
     assert decode_call(L, y=None) == NULL
     assert decode_call(L, nheads=6, ngroups=4) == SHAPE
     assert decode_call(L, dstate=48) == UNSUP
+    assert decode_call(L, dstate=96) == UNSUP   # a multiple of 32 with no kernel build
+    assert decode_call(L, dstate=512) == UNSUP
     assert decode_call(L, dtype=3) == DTYPE
     assert decode_call(L, x=ctypes.c_void_p(0x20000004)) == ALIGN
     assert decode_call(L, y=P(1)) == ALIAS
