@@ -284,3 +284,148 @@ def test_ssd_bwd_random_shapes(case):
     ref = _ref(inp, dy, h0, dfinal)
     for key, rkey, tol in KEYS:
         assert_close(g[key], ref[rkey], tol, key)
+
+
+@pytest.mark.parametrize("case", SSD_CASES[:6],
+                         ids=[f"B{c['batch']}L{c['seqlen']}H{c['nheads']}G{c['ngroups']}"
+                              for c in SSD_CASES[:6]])
+def test_mamba3_bwd_random_shapes(case):
+    from tests.test_mamba3_bwd_gpu import KEYS, _case_inputs, _gpu, _ref
+    c = case
+    inp, dy, dfinal = _case_inputs(c["batch"], c["seqlen"], c["nheads"], c["ngroups"],
+                                   900 + c["seqlen"] + c["nheads"], c["h0"], c["prev"], c["h0"])
+    g = _gpu(inp, dy, dfinal)
+    ref = _ref(inp, dy, dfinal)
+    for key, rkey, tol in KEYS:
+        if ref[rkey] is None:
+            assert g[key] is None, key
+            continue
+        assert_close(g[key], ref[rkey], tol, key)
+
+
+@pytest.mark.parametrize("case", MIMO_CASES[:6],
+                         ids=[f"B{c['batch']}L{c['seqlen']}R{c['rank']}H{c['nheads']}"
+                              f"G{c['ngroups']}" for c in MIMO_CASES[:6]])
+def test_mimo_bwd_random_shapes(case):
+    from tests.test_mamba3_mimo_bwd_gpu import KEYS, _case, _gpu, _ref
+    c = case
+    inp, dy, dfinal = _case(c["batch"], c["seqlen"], c["rank"], c["nheads"], c["ngroups"],
+                            950 + c["seqlen"] + c["rank"], c["h0"], c["prev"], not c["h0"])
+    g = _gpu(inp, dy, dfinal)
+    ref = _ref(inp, dy, dfinal)
+    for key, rkey, tol in KEYS:
+        if ref[rkey] is None:
+            assert g[key] is None, key
+            continue
+        assert_close(g[key], ref[rkey], tol, key)
+
+
+@pytest.mark.parametrize("case", DECODE_CASES,
+                         ids=[f"B{c['batch']}H{c['nheads']}P{c['headdim']}N{c['dstate']}"
+                              f"G{c['ngroups']}{c['dtype']}" for c in DECODE_CASES])
+def test_mamba3_decode_random_shapes(case):
+    c = case
+    steps = 3
+    inp = inputs.decode_inputs(c["batch"], c["nheads"], c["headdim"], c["dstate"], c["ngroups"],
+                               steps + 1, c["dtype"], seed=1500 + c["headdim"], gate=c["gate"],
+                               dskip=c["dskip"])
+    g = torch.Generator().manual_seed(c["headdim"])
+    lams = [torch.sigmoid(torch.randn(c["batch"], c["nheads"], generator=g))
+            for _ in range(steps)]
+    tol = TOL_F32 if c["dtype"] == "f32" else TOL_BF16
+    state = inp["state"].clone().cuda()
+    st_ref = inp["state"].double().numpy()
+    D = inp["D"]
+    cu = lambda v: None if v is None else v.cuda()  # noqa: E731
+    for t in range(1, steps + 1):  # step 0's x and B serve as the previous token
+        y = binding.ssm_decode_step_mamba3(state, cu(inp["B"][t - 1]), cu(inp["x"][t - 1]),
+                                           cu(inp["x"][t]), cu(inp["dt"][t]), cu(lams[t - 1]),
+                                           inp["A"].cuda(), cu(inp["B"][t]), cu(inp["C"][t]),
+                                           cu(D), cu(inp["z"][t]))
+        torch.cuda.synchronize()
+        y_ref, st_ref = oracle.mamba3_decode_step(st_ref, inp["B"][t - 1], inp["x"][t - 1],
+                                                  inp["x"][t], inp["dt"][t], lams[t - 1],
+                                                  inp["A"], inp["B"][t], inp["C"][t], D,
+                                                  inp["z"][t])
+        if c["dtype"] == "f32":
+            assert_close(y, y_ref, tol, f"y step {t}")
+        else:  # bf16 y: the rounding of the exact result, within one bf16 ulp
+            assert_close(y, y_ref, 2 ** -7, f"y step {t}")
+        assert_close(state, st_ref, tol, f"state step {t}")
+
+
+def _draw_mimo_decode(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        ngroups = int(rng.integers(1, 4))
+        cases.append(dict(batch=int(rng.integers(1, 5)), rank=int(rng.choice([2, 4])),
+                          ngroups=ngroups, nheads=ngroups * int(rng.integers(1, 4)),
+                          headdim=int(rng.integers(1, 150)),
+                          dtype=str(rng.choice(["f32", "bf16"])), gate=bool(rng.integers(2)),
+                          dskip=bool(rng.integers(2))))
+    return cases
+
+
+MIMO_DECODE_CASES = _draw_mimo_decode(8, 2029)
+
+
+@pytest.mark.parametrize("case", MIMO_DECODE_CASES,
+                         ids=[f"B{c['batch']}R{c['rank']}H{c['nheads']}P{c['headdim']}"
+                              f"G{c['ngroups']}{c['dtype']}" for c in MIMO_DECODE_CASES])
+def test_mimo_decode_random_shapes(case):
+    c = case
+    steps = 3
+    inp = inputs.mamba3_mimo_inputs(c["batch"], steps + 1, c["rank"], c["nheads"], c["headdim"],
+                                    128, c["ngroups"], c["dtype"], seed=1600 + c["headdim"])
+    g = torch.Generator().manual_seed(c["headdim"] + 1)
+    D = torch.randn(c["nheads"], generator=g) if c["dskip"] else None
+    zs = [torch.randn(c["batch"], c["rank"], c["nheads"], c["headdim"],
+                      generator=g).to(inp["x"].dtype) if c["gate"] else None
+          for _ in range(steps + 1)]
+    tol = TOL_F32 if c["dtype"] == "f32" else TOL_BF16
+    state = inp["h0"].clone().cuda()
+    st_ref = inp["h0"].double().numpy()
+    cu = lambda v: None if v is None else v.contiguous().cuda()  # noqa: E731
+    for t in range(1, steps + 1):
+        y = binding.ssm_decode_step_mamba3_mimo(
+            state, cu(inp["B"][:, t - 1]), cu(inp["x"][:, t - 1]), cu(inp["x"][:, t]),
+            cu(inp["dt"][:, t]), cu(inp["lam"][:, t]), inp["A_head"].cuda(), cu(inp["B"][:, t]),
+            cu(inp["C"][:, t]), cu(D), cu(zs[t]))
+        torch.cuda.synchronize()
+        y_ref, st_ref = oracle.mamba3_mimo_decode_step(
+            st_ref, inp["B"][:, t - 1], inp["x"][:, t - 1], inp["x"][:, t], inp["dt"][:, t],
+            inp["lam"][:, t], inp["A_head"], inp["B"][:, t], inp["C"][:, t], D, zs[t])
+        if c["dtype"] == "f32":
+            assert_close(y, y_ref, tol, f"y step {t}")
+        else:
+            assert_close(y, y_ref, 2 ** -7, f"y step {t}")
+        assert_close(state, st_ref, tol, f"state step {t}")
+
+
+@pytest.mark.parametrize("case", SCAN_CASES[:8],
+                         ids=[f"B{c['batch']}D{c['dim']}L{c['seqlen']}G{c['ngroups']}{c['dtype']}"
+                              for c in SCAN_CASES[:8]])
+def test_scan_host_buffers_random_shapes(case):
+    """ssm_scan_fwd_host on pinned host buffers gives ssm_scan_fwd's bits (these
+    problems are small enough that both take the whole problem's kernel)."""
+    c = case
+    inp = inputs.scan_inputs(c["batch"], c["dim"], c["seqlen"], 16, c["ngroups"], c["dtype"],
+                             seed=c["dim"] * 11 + c["seqlen"], gate=c["gate"], dskip=c["dskip"])
+    h0 = (torch.randn(c["batch"], c["dim"], 16, generator=torch.Generator().manual_seed(3)) * 0.5
+          if c["h0"] else None)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    y_dev, fs_dev = binding.ssm_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"],
+                                         d["z"], d["delta_bias"], True,
+                                         None if h0 is None else h0.cuda(),
+                                         out_dtype=torch.float32)
+    pin = {k: (v.pin_memory() if isinstance(v, torch.Tensor) and k in ("u", "delta", "z", "B", "C")
+               else v) for k, v in inp.items()}
+    y_h = torch.full((c["batch"], c["dim"], c["seqlen"]), float("nan")).pin_memory()
+    fs_h = torch.full((c["batch"], c["dim"], 16), float("nan")).pin_memory()
+    binding.ssm_scan_fwd_host(pin["u"], pin["delta"], d["A"], pin["B"], pin["C"], y_h, fs_h,
+                              d["D"], pin["z"], d["delta_bias"], True,
+                              None if h0 is None else h0.pin_memory())
+    torch.cuda.synchronize()
+    assert torch.equal(y_h, y_dev.cpu())
+    assert torch.equal(fs_h, fs_dev.cpu())
