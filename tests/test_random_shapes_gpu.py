@@ -429,3 +429,31 @@ def test_scan_host_buffers_random_shapes(case):
     torch.cuda.synchronize()
     assert torch.equal(y_h, y_dev.cpu())
     assert torch.equal(fs_h, fs_dev.cpu())
+
+
+def _draw_scan_chained(n, seed):
+    """Problems whose 32-channel blocks fill every resident CTA slot, so the
+    chained scan cuts the sequence into L-chunks carried through the workspace."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        ngroups = int(rng.choice([1, 2, 4]))
+        dpg = int(rng.integers(5000, 6200)) // ngroups
+        seqlen = int(rng.integers(65, 1300))
+        if i % 2 == 0:  # rows 16-byte aligned for bf16: the TMA path (else plain loads)
+            seqlen -= seqlen % 8
+        cases.append(dict(batch=4, ngroups=ngroups, dim=ngroups * dpg, seqlen=seqlen,
+                          dtype=str(rng.choice(["f32", "bf16"])), gate=bool(rng.integers(2)),
+                          dskip=str(rng.choice(["none", "ones", "randn"])),
+                          softplus=True, h0=bool(rng.integers(2))))
+    return cases
+
+
+SCAN_CHAINED_CASES = _draw_scan_chained(4, 2030)
+
+
+@pytest.mark.parametrize("case", SCAN_CHAINED_CASES,
+                         ids=[f"B{c['batch']}D{c['dim']}L{c['seqlen']}G{c['ngroups']}{c['dtype']}"
+                              for c in SCAN_CHAINED_CASES])
+def test_scan_chained_chunks_random_shapes(case):
+    test_scan_random_shapes(case, (0, 0))
