@@ -848,7 +848,10 @@ def _profile_setup(name):
     from state_space_model_selective_gb300 import binding, inputs
     dev = torch.device("cuda")
     scans = {"scan": (4, 5120, 16384, "bf16", 1003), "scan_l4096": (4, 5120, 4096, "bf16", 1003),
-             "scan_b8": (8, 1536, 2048, "bf16", 1002), "scan_b1_f32": (1, 1536, 128, "f32", 1001)}
+             "scan_b8": (8, 1536, 2048, "bf16", 1002), "scan_b1_f32": (1, 1536, 128, "f32", 1001),
+             # one middle segment of the end-to-end leg: 2560 channels of one batch row,
+             # which the sequence-parallel kernel scans
+             "scan_segment": (1, 2560, 16384, "bf16", 1003)}
     if name in scans:
         B, D, L, dt, seed = scans[name]
         inp = inputs.scan_inputs(B, D, L, 16, 1, dt, seed=seed, device="cuda")
@@ -958,15 +961,16 @@ def _profile_setup(name):
     raise SystemExit(f"unknown workload {name!r}")
 
 
-PROFILE_WORKLOADS = ["scan", "scan_l4096", "scan_b8", "scan_b1_f32", "ssd", "decode",
-                     "decode_mimo", "scan_bwd", "ssd_bwd", "m3_bwd", "mimo_bwd", "rope"]
+PROFILE_WORKLOADS = ["scan", "scan_l4096", "scan_b8", "scan_b1_f32", "scan_segment", "ssd",
+                     "decode", "decode_mimo", "scan_bwd", "ssd_bwd", "m3_bwd", "mimo_bwd", "rope"]
 
 
 def run_profile(name, reps):
     """Runs one workload `reps` times (the process exits non-zero on any error):
     scan: the benchmark step's scan; scan_l4096: the same channels over L 4096;
     scan_b8: batch 8, L 2048, 1536 channels; scan_b1_f32: batch 1, L 128, 1536
-    channels, fp32; ssd: chunked SSD batch 32, L 256, 32 heads; decode,
+    channels, fp32; scan_segment: 2560 channels of one batch row over L 16384 (a
+    segment of the end-to-end leg); ssd: chunked SSD batch 32, L 256, 32 heads; decode,
     decode_mimo: decode steps batch 256, 32 heads; scan_bwd, ssd_bwd, m3_bwd,
     mimo_bwd: the gradients on those workloads; rope: Mamba-3's rotation of B
     and C on the SSD workload."""
